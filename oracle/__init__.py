@@ -1,0 +1,192 @@
+"""ctypes binding of the CPU oracle (ft_oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the CPU-baseline
+leg of the benchmark may import this package; the CUDA library and its Python
+binding never do.  The shared object is built with gcc into ``_build/`` under
+a name that carries the source hash, so a stale build is never picked up.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import hashlib
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ft_oracle.c")
+_HDR = os.path.join(_HERE, "ft_oracle.h")
+_LOCK = threading.Lock()
+_LIB = None
+
+QK = 32
+Q4_0_BYTES = 18
+Q8_1_BYTES = 36
+
+
+def _source_hash(src=_SRC) -> str:
+    h = hashlib.sha256()
+    for p in (src, _HDR):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def build(src: str = _SRC, out_dir: str | None = None, extra_flags=()) -> str:
+    """Compile the oracle (or a copy of it) with gcc; returns the .so path."""
+    out_dir = out_dir or os.path.join(_HERE, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    so = os.path.join(out_dir, f"liboracle_{_source_hash(src)}.so")
+    if not os.path.exists(so):
+        tmp = so + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off",
+               "-I", _HERE, *extra_flags, src, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, so)
+    return so
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """Numpy-facing wrapper around one loaded oracle shared object."""
+
+    def __init__(self, so_path: str):
+        L = ctypes.CDLL(so_path)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+        L.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+        L.oracle_half_to_double.restype = ctypes.c_double
+        L.oracle_float_to_half.argtypes = [ctypes.c_float]
+        L.oracle_float_to_half.restype = ctypes.c_uint16
+        L.oracle_quantize_q4_0.argtypes = [vp, i64, vp]
+        L.oracle_dequantize_q4_0.argtypes = [vp, i64, vp]
+        L.oracle_quantize_q8_1.argtypes = [vp, i64, i64, vp]
+        L.oracle_dequantize_q8_1.argtypes = [vp, i64, vp]
+        L.oracle_route.argtypes = [vp, i64, i32, vp, vp, vp]
+        L.oracle_route.restype = i64
+        L.oracle_block_dot.argtypes = [vp, vp]
+        L.oracle_block_dot.restype = i32
+        L.oracle_moe_q4_0_q8_1.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64]
+        L.oracle_moe_sample.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp, vp, i64, vp]
+        L.oracle_moe_block_dots.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp]
+        L.oracle_moe_dequant_bruteforce.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp]
+        self.lib = L
+        self.path = so_path
+
+    # fp16 ------------------------------------------------------------
+    def half_to_double(self, h: int) -> float:
+        return self.lib.oracle_half_to_double(int(h))
+
+    def float_to_half(self, f: float) -> int:
+        return int(self.lib.oracle_float_to_half(float(np.float32(f))))
+
+    # formats ---------------------------------------------------------
+    def quantize_q4_0(self, w: np.ndarray) -> np.ndarray:
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        assert w.shape[-1] % QK == 0
+        nb = w.size // QK
+        out = np.empty((nb, Q4_0_BYTES), dtype=np.uint8)
+        self.lib.oracle_quantize_q4_0(_p(w), nb, _p(out))
+        return out.reshape(*w.shape[:-1], w.shape[-1] // QK, Q4_0_BYTES)
+
+    def dequantize_q4_0(self, blocks: np.ndarray) -> np.ndarray:
+        blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+        nb = blocks.size // Q4_0_BYTES
+        out = np.empty(nb * QK, dtype=np.float64)
+        self.lib.oracle_dequantize_q4_0(_p(blocks), nb, _p(out))
+        return out.reshape(*blocks.shape[:-2], blocks.shape[-2] * QK)
+
+    def quantize_q8_1(self, x_fp16: np.ndarray) -> np.ndarray:
+        x = np.ascontiguousarray(x_fp16, dtype=np.float16)
+        T, K = x.shape
+        assert K % QK == 0
+        out = np.empty((T, K // QK, Q8_1_BYTES), dtype=np.uint8)
+        self.lib.oracle_quantize_q8_1(_p(x.view(np.uint16)), T, K, _p(out))
+        return out
+
+    def dequantize_q8_1(self, blocks: np.ndarray) -> np.ndarray:
+        blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+        nb = blocks.size // Q8_1_BYTES
+        out = np.empty(nb * QK, dtype=np.float64)
+        self.lib.oracle_dequantize_q8_1(_p(blocks), nb, _p(out))
+        return out.reshape(*blocks.shape[:-2], blocks.shape[-2] * QK)
+
+    # route -----------------------------------------------------------
+    def route(self, topk_ids: np.ndarray, n_experts: int):
+        ids = np.ascontiguousarray(topk_ids, dtype=np.int32).reshape(-1)
+        S = ids.size
+        counts = np.empty(n_experts, dtype=np.int32)
+        offsets = np.empty(n_experts + 1, dtype=np.int32)
+        perm = np.empty(S, dtype=np.int32)
+        bad = self.lib.oracle_route(_p(ids), S, n_experts, _p(counts), _p(offsets), _p(perm))
+        return counts, offsets, perm, int(bad)
+
+    # dot -------------------------------------------------------------
+    def block_dot(self, w_block: np.ndarray, a_block: np.ndarray) -> int:
+        w = np.ascontiguousarray(w_block, dtype=np.uint8)
+        a = np.ascontiguousarray(a_block, dtype=np.uint8)
+        assert w.size == Q4_0_BYTES and a.size == Q8_1_BYTES
+        return int(self.lib.oracle_block_dot(_p(w), _p(a)))
+
+    @staticmethod
+    def _shape(weights, act, topk_ids):
+        E, N, nb, _ = weights.shape
+        T = act.shape[0]
+        k = topk_ids.shape[1]
+        return E, N, nb * QK, T, k
+
+    def moe(self, weights, act, topk_ids) -> np.ndarray:
+        weights = np.ascontiguousarray(weights, dtype=np.uint8)
+        act = np.ascontiguousarray(act, dtype=np.uint8)
+        ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+        E, N, K, T, k = self._shape(weights, act, ids)
+        out = np.empty((T, k, N), dtype=np.float32)
+        self.lib.oracle_moe_q4_0_q8_1(_p(weights), _p(act), _p(ids), _p(out), T, k, E, N, K)
+        return out
+
+    def moe_sample(self, weights, act, topk_ids, slots, rows) -> np.ndarray:
+        weights = np.ascontiguousarray(weights, dtype=np.uint8)
+        act = np.ascontiguousarray(act, dtype=np.uint8)
+        ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+        E, N, K, T, k = self._shape(weights, act, ids)
+        slots = np.ascontiguousarray(slots, dtype=np.int64)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        assert slots.shape == rows.shape
+        assert slots.size == 0 or (slots.min() >= 0 and slots.max() < T * k)
+        assert rows.size == 0 or (rows.min() >= 0 and rows.max() < N)
+        out = np.empty(slots.size, dtype=np.float64)
+        self.lib.oracle_moe_sample(_p(weights), _p(act), _p(ids), T, k, E, N, K,
+                                   _p(slots), _p(rows), slots.size, _p(out))
+        return out
+
+    def moe_block_dots(self, weights, act, topk_ids) -> np.ndarray:
+        weights = np.ascontiguousarray(weights, dtype=np.uint8)
+        act = np.ascontiguousarray(act, dtype=np.uint8)
+        ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+        E, N, K, T, k = self._shape(weights, act, ids)
+        out = np.empty((T * k, N, K // QK), dtype=np.int32)
+        self.lib.oracle_moe_block_dots(_p(weights), _p(act), _p(ids), T, k, E, N, K, _p(out))
+        return out
+
+    def moe_dequant_bruteforce(self, weights, act, topk_ids) -> np.ndarray:
+        weights = np.ascontiguousarray(weights, dtype=np.uint8)
+        act = np.ascontiguousarray(act, dtype=np.uint8)
+        ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+        E, N, K, T, k = self._shape(weights, act, ids)
+        out = np.empty((T, k, N), dtype=np.float64)
+        self.lib.oracle_moe_dequant_bruteforce(_p(weights), _p(act), _p(ids), T, k, E, N, K, _p(out))
+        return out
+
+
+def get() -> Oracle:
+    """The oracle built from the committed source (built once per process)."""
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            _LIB = Oracle(build())
+        return _LIB

@@ -1,0 +1,319 @@
+/*
+ * CPU oracle for the routed Q4_0 x Q8_1 MoE expert matmul.
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by the tests, the smoke check and the CPU
+ * baseline leg of the benchmark; never by the CUDA library.  See ft_oracle.h
+ * for the byte layouts and the list of pins.
+ *
+ * Sources.  The pages describe one computation, the per-(token, top-k slot)
+ * dot product of the routed expert's Q4_0 weight rows with the token's Q8_1
+ * activation (FreeToken PR #185, "Problem": moe_vec_q4_0_q8_1 over the flat
+ * (token, top-k) index), its quantizer quantize_row_q8_1 ("Fix"), and the
+ * expert-grouped form built on expert_offsets with a leading 0 and a
+ * searchsorted(right=True) slot-to-expert map (nvfp4-megamoe-kernel
+ * CURRENT_BUG.md, Bugs 2 and 4).  The pages do not print the block formats;
+ * they are the GGUF Q4_0 / Q8_1 formats restated in ft_oracle.h.
+ *
+ * Readings where the pages are silent (all listed in the design notes):
+ *   - "round" is round-half-away-from-zero (C roundf);
+ *   - Q8_1 divides by the fp32 scale amax/127, not by its fp16 value;
+ *   - s = fp16(d32 * (float)sum(q)) with d32 the fp32 scale;
+ *   - the dot uses the exact integer sum of (q_w - 8) * q_a per block and
+ *     never the rounded s;
+ *   - slots whose expert id is out of range are left out of the routing and
+ *     produce zero output rows.
+ *
+ * Build: plain C99, -ffp-contract=off so that no multiply-add is fused.
+ */
+#include "ft_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define QK 32
+#define Q4_0_BYTES 18
+#define Q8_1_BYTES 36
+
+/* ------------------------------------------------------------------ fp16 */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int exp = (h >> 10) & 0x1f;
+    int frac = h & 0x3ff;
+    double v;
+    if (exp == 0)
+        v = ldexp((double)frac, -24);                    /* zero / subnormal */
+    else if (exp == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + frac), exp - 25);      /* 1.frac * 2^(exp-15) */
+    return sign ? -v : v;
+}
+
+/* Round a float to the nearest binary16, ties to even. */
+uint16_t oracle_float_to_half(float f)
+{
+    double a = fabs((double)f);
+    uint16_t sign = signbit(f) ? 0x8000 : 0;
+    if (isnan(f))
+        return sign | 0x7e00;
+    if (a >= 65520.0)                                    /* past the max finite + half an ulp */
+        return sign | 0x7c00;
+    if (a < ldexp(1.0, -14)) {                           /* subnormal range: units of 2^-24 */
+        double q = nearbyint(a * ldexp(1.0, 24));        /* default mode: to nearest, ties even */
+        return sign | (uint16_t)q;                       /* q == 1024 encodes the smallest normal */
+    }
+    int e;
+    double m = frexp(a, &e);                             /* a = m * 2^e, m in [0.5, 1) */
+    double q = nearbyint(m * 2048.0);                    /* 11 significant bits */
+    if (q == 2048.0) {
+        q = 1024.0;
+        e += 1;
+    }
+    int biased = e - 1 + 15;
+    if (biased >= 31)
+        return sign | 0x7c00;
+    return sign | (uint16_t)(biased << 10) | (uint16_t)((int)q - 1024);
+}
+
+static uint16_t rd16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+static void wr16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)(v & 0xff); p[1] = (uint8_t)(v >> 8); }
+
+/* ------------------------------------------------------------------ Q4_0 */
+
+/* Q4_0 quantizer used for synthetic weights: d = m / -8 where m is the
+ * block's element of largest magnitude (first on ties, sign kept),
+ * q = clamp(round(w / d) + 8, 0, 15), value (q - 8) * d. */
+void oracle_quantize_q4_0(const float* w, int64_t n_blocks, uint8_t* out)
+{
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        const float* x = w + b * QK;
+        float m = 0.0f, amax = 0.0f;
+        for (int i = 0; i < QK; ++i) {
+            if (fabsf(x[i]) > amax) {
+                amax = fabsf(x[i]);
+                m = x[i];
+            }
+        }
+        float d = m / -8.0f;
+        uint8_t q[QK];
+        for (int i = 0; i < QK; ++i) {
+            int v = 8;
+            if (d != 0.0f) {
+                v = (int)roundf(x[i] / d) + 8;
+                if (v < 0) v = 0;
+                if (v > 15) v = 15;
+            }
+            q[i] = (uint8_t)v;
+        }
+        uint8_t* o = out + b * Q4_0_BYTES;
+        wr16(o, oracle_float_to_half(d));
+        for (int j = 0; j < 16; ++j)
+            o[2 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
+    }
+}
+
+static int q4_0_nibble(const uint8_t* block, int i)
+{
+    const uint8_t* qs = block + 2;
+    return i < 16 ? (qs[i] & 0x0f) : (qs[i - 16] >> 4);
+}
+
+void oracle_dequantize_q4_0(const uint8_t* blocks, int64_t n_blocks, double* out)
+{
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        const uint8_t* blk = blocks + b * Q4_0_BYTES;
+        double d = oracle_half_to_double(rd16(blk));
+        for (int i = 0; i < QK; ++i)
+            out[b * QK + i] = (double)(q4_0_nibble(blk, i) - 8) * d;
+    }
+}
+
+/* ------------------------------------------------------------------ Q8_1 */
+
+/* Activation quantizer (quantize_row_q8_1 on FreeToken PR #185, "Fix"),
+ * per 32-block of an fp16 row, in fp32: amax = max |x|, d = amax / 127,
+ * q = round(x / d) clamped to [-127, 127] (0 when amax == 0), s = d * sum q.
+ * d and s are stored as fp16. */
+void oracle_quantize_q8_1(const uint16_t* x_fp16, int64_t tokens, int64_t ncols, uint8_t* out)
+{
+    int64_t nb = ncols / QK;
+    for (int64_t t = 0; t < tokens; ++t) {
+        for (int64_t b = 0; b < nb; ++b) {
+            float x[QK];
+            for (int i = 0; i < QK; ++i)
+                x[i] = (float)oracle_half_to_double(x_fp16[t * ncols + b * QK + i]);
+            float amax = 0.0f;
+            for (int i = 0; i < QK; ++i)
+                if (fabsf(x[i]) > amax) amax = fabsf(x[i]);
+            float d = amax / 127.0f;
+            int sum = 0;
+            uint8_t* o = out + (t * nb + b) * Q8_1_BYTES;
+            for (int i = 0; i < QK; ++i) {
+                int q = 0;
+                if (amax != 0.0f) {
+                    q = (int)roundf(x[i] / d);
+                    if (q < -127) q = -127;
+                    if (q > 127) q = 127;
+                }
+                sum += q;
+                o[4 + i] = (uint8_t)(int8_t)q;
+            }
+            float s = d * (float)sum;
+            wr16(o, oracle_float_to_half(d));
+            wr16(o + 2, oracle_float_to_half(s));
+        }
+    }
+}
+
+void oracle_dequantize_q8_1(const uint8_t* blocks, int64_t n_blocks, double* out)
+{
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        const uint8_t* blk = blocks + b * Q8_1_BYTES;
+        double d = oracle_half_to_double(rd16(blk));
+        for (int i = 0; i < QK; ++i)
+            out[b * QK + i] = (double)(int8_t)blk[4 + i] * d;
+    }
+}
+
+/* ----------------------------------------------------------------- route */
+
+/* Stable counting sort of the flat slots by expert id.
+ * counts[e] = number of slots routed to e; offsets has E+1 entries with a
+ * leading 0 (nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 4), offsets[e+1] =
+ * offsets[e] + counts[e]; perm[offsets[e] + r] = the r-th slot, in ascending
+ * slot order, whose id is e.  Positions p with offsets[e] <= p < offsets[e+1]
+ * belong to expert e, which is the searchsorted(right=True) map of Bug 2.
+ * Slots with ids outside [0, E) are left out; perm past offsets[E] is -1.
+ * Returns the number of such slots. */
+int64_t oracle_route(const int32_t* topk_ids, int64_t n_slots, int32_t n_experts,
+                     int32_t* counts, int32_t* offsets, int32_t* perm)
+{
+    int64_t bad = 0;
+    for (int32_t e = 0; e < n_experts; ++e) counts[e] = 0;
+    for (int64_t s = 0; s < n_slots; ++s) {
+        int32_t e = topk_ids[s];
+        if (e < 0 || e >= n_experts) { ++bad; continue; }
+        counts[e] += 1;
+    }
+    offsets[0] = 0;
+    for (int32_t e = 0; e < n_experts; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    int32_t* cursor = (int32_t*)calloc((size_t)n_experts + 1, sizeof(int32_t));
+    for (int64_t s = 0; s < n_slots; ++s) {
+        int32_t e = topk_ids[s];
+        if (e < 0 || e >= n_experts) continue;
+        perm[offsets[e] + cursor[e]] = (int32_t)s;
+        cursor[e] += 1;
+    }
+    free(cursor);
+    for (int64_t p = offsets[n_experts]; p < n_slots; ++p) perm[p] = -1;
+    return bad;
+}
+
+/* ------------------------------------------------------------------- dot */
+
+/* Exact integer dot of one Q4_0 block with one Q8_1 block:
+ * sum_i (q_w[i] - 8) * q_a[i]; |result| <= 32 * 8 * 127 = 32512. */
+int32_t oracle_block_dot(const uint8_t* w_block, const uint8_t* a_block)
+{
+    int32_t acc = 0;
+    for (int i = 0; i < QK; ++i)
+        acc += (q4_0_nibble(w_block, i) - 8) * (int32_t)(int8_t)a_block[4 + i];
+    return acc;
+}
+
+/* y[s, r] = sum_b d_w[e(s), r, b] * d_a[t(s), b] * dot_b, t(s) = s / k,
+ * e(s) = topk_ids[s]; fp64 sum in block order; 0 for a bad id. */
+static double moe_one(const uint8_t* weights, const uint8_t* act, const int32_t* topk_ids,
+                      int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols,
+                      int64_t s, int64_t r)
+{
+    int64_t nb = ncols / QK;
+    int32_t e = topk_ids[s];
+    if (e < 0 || e >= n_experts)
+        return 0.0;
+    int64_t t = s / top_k;
+    const uint8_t* wrow = weights + ((int64_t)e * nrows + r) * nb * Q4_0_BYTES;
+    const uint8_t* arow = act + t * nb * Q8_1_BYTES;
+    double y = 0.0;
+    for (int64_t b = 0; b < nb; ++b) {
+        const uint8_t* wb = wrow + b * Q4_0_BYTES;
+        const uint8_t* ab = arow + b * Q8_1_BYTES;
+        double dw = oracle_half_to_double(rd16(wb));
+        double da = oracle_half_to_double(rd16(ab));
+        y += dw * da * (double)oracle_block_dot(wb, ab);
+    }
+    return y;
+}
+
+void oracle_moe_q4_0_q8_1(const uint8_t* weights, const uint8_t* act, const int32_t* topk_ids,
+                          float* out, int64_t tokens, int32_t top_k, int32_t n_experts,
+                          int64_t nrows, int64_t ncols)
+{
+    int64_t n_slots = tokens * top_k;
+    for (int64_t s = 0; s < n_slots; ++s)
+        for (int64_t r = 0; r < nrows; ++r)
+            out[s * nrows + r] = (float)moe_one(weights, act, topk_ids, top_k, n_experts,
+                                                nrows, ncols, s, r);
+}
+
+void oracle_moe_sample(const uint8_t* weights, const uint8_t* act, const int32_t* topk_ids,
+                       int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows,
+                       int64_t ncols, const int64_t* slots, const int64_t* rows, int64_t n,
+                       double* out)
+{
+    (void)tokens;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = moe_one(weights, act, topk_ids, top_k, n_experts, nrows, ncols, slots[i], rows[i]);
+}
+
+/* dots[s][r][b] = the exact block dot; 0 for a bad id. */
+void oracle_moe_block_dots(const uint8_t* weights, const uint8_t* act, const int32_t* topk_ids,
+                           int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows,
+                           int64_t ncols, int32_t* dots)
+{
+    int64_t nb = ncols / QK;
+    int64_t n_slots = tokens * top_k;
+    for (int64_t s = 0; s < n_slots; ++s) {
+        int32_t e = topk_ids[s];
+        int64_t t = s / top_k;
+        for (int64_t r = 0; r < nrows; ++r)
+            for (int64_t b = 0; b < nb; ++b) {
+                int32_t v = 0;
+                if (e >= 0 && e < n_experts)
+                    v = oracle_block_dot(weights + (((int64_t)e * nrows + r) * nb + b) * Q4_0_BYTES,
+                                         act + (t * nb + b) * Q8_1_BYTES);
+                dots[(s * nrows + r) * nb + b] = v;
+            }
+    }
+}
+
+/* Dequantize both operands to fp64 values and take the plain dot over K. */
+void oracle_moe_dequant_bruteforce(const uint8_t* weights, const uint8_t* act,
+                                   const int32_t* topk_ids, int64_t tokens, int32_t top_k,
+                                   int32_t n_experts, int64_t nrows, int64_t ncols, double* out)
+{
+    int64_t nb = ncols / QK;
+    int64_t n_slots = tokens * top_k;
+    double* wv = (double*)malloc((size_t)ncols * sizeof(double));
+    double* av = (double*)malloc((size_t)ncols * sizeof(double));
+    for (int64_t s = 0; s < n_slots; ++s) {
+        int32_t e = topk_ids[s];
+        int64_t t = s / top_k;
+        oracle_dequantize_q8_1(act + t * nb * Q8_1_BYTES, nb, av);
+        for (int64_t r = 0; r < nrows; ++r) {
+            double y = 0.0;
+            if (e >= 0 && e < n_experts) {
+                oracle_dequantize_q4_0(weights + ((int64_t)e * nrows + r) * nb * Q4_0_BYTES, nb, wv);
+                for (int64_t i = 0; i < ncols; ++i)
+                    y += wv[i] * av[i];
+            }
+            out[s * nrows + r] = y;
+        }
+    }
+    free(wv);
+    free(av);
+}

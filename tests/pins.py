@@ -1,0 +1,351 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with what the workload definitions and arithmetic
+fix.  ``test_oracle_pins.py`` runs them on the committed oracle (all must
+pass) and on mutated copies of it (each mutant must fail at least one), which
+shows the pins are sensitive to the plausible mistakes they are meant to catch.
+
+Block formats (GGUF, restated): Q4_0 = fp16 d + 16 bytes, weight j < 16 in the
+low nibble of byte j, weight j + 16 in its high nibble, value (q - 8) d;
+Q8_1 = fp16 d + fp16 s + 32 int8 q, value q d, s = d * sum(q).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+QK = 32
+
+
+# ------------------------------------------------------------------ helpers
+def q4_block(d_bits: int, q: list[int]) -> np.ndarray:
+    """Assemble one Q4_0 block from fp16 bits and 32 nibble values (test-side, by hand)."""
+    assert len(q) == 32
+    b = np.zeros(18, dtype=np.uint8)
+    b[0], b[1] = d_bits & 0xFF, d_bits >> 8
+    for j in range(16):
+        b[2 + j] = (q[j] & 15) | ((q[j + 16] & 15) << 4)
+    return b
+
+
+def q8_block(d_bits: int, s_bits: int, q: list[int]) -> np.ndarray:
+    b = np.zeros(36, dtype=np.uint8)
+    b[0], b[1] = d_bits & 0xFF, d_bits >> 8
+    b[2], b[3] = s_bits & 0xFF, s_bits >> 8
+    b[4:] = np.asarray(q, dtype=np.int8).view(np.uint8)
+    return b
+
+
+def numpy_decode_q4_0(w: np.ndarray) -> np.ndarray:
+    """Independent vectorised decode of Q4_0 bytes [..., nb, 18] -> fp64 [..., nb*32]."""
+    d = np.ascontiguousarray(w[..., 0:2]).view(np.float16)[..., 0].astype(np.float64)
+    qs = w[..., 2:].astype(np.int64)
+    q = np.concatenate([qs & 15, qs >> 4], axis=-1) - 8
+    v = q * d[..., None]
+    return v.reshape(*w.shape[:-2], w.shape[-2] * QK)
+
+
+def numpy_decode_q8_1(a: np.ndarray) -> np.ndarray:
+    d = np.ascontiguousarray(a[..., 0:2]).view(np.float16)[..., 0].astype(np.float64)
+    q = np.ascontiguousarray(a[..., 4:]).view(np.int8).astype(np.float64)
+    v = q * d[..., None]
+    return v.reshape(*a.shape[:-2], a.shape[-2] * QK)
+
+
+def tiny_case(seed=0, E=6, k=2, K=128, N=24, T=7, x_scale=1.0):
+    from bit_quantized_moe_quantize_gb300 import synth
+    rng = np.random.default_rng(seed)
+    w = (rng.standard_normal((E, N, K)) * 0.02).astype(np.float32)
+    x = (rng.standard_normal((T, K)) * x_scale).astype(np.float16)
+    ids = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    return synth.encode_q4_0(w), x, ids
+
+
+# ------------------------------------------------------------------- fp16
+def pin_fp16(o):
+    special = np.array([0.0, -0.0, 1.0, -1.0, 65504.0, 65519.99, 65520.0, 1e6, -1e6,
+                        2.0 ** -14, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, 2.0 ** -26,
+                        1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 0.1, 1 / 3, 2048.5, 4097.0],
+                       dtype=np.float32)
+    rng = np.random.default_rng(1)
+    rand = (rng.standard_normal(20000) * np.exp2(rng.integers(-30, 18, 20000))).astype(np.float32)
+    for f in np.concatenate([special, -special, rand]):
+        with np.errstate(over="ignore"):
+            want = int(np.float32(f).astype(np.float16).view(np.uint16))
+        got = o.float_to_half(f)
+        assert got == want, (float(f), hex(got), hex(want))
+    bits = np.arange(0, 1 << 16, 7, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    for b, r in zip(bits, ref):
+        if np.isnan(r):
+            continue
+        assert o.half_to_double(int(b)) == r, hex(int(b))
+
+
+# ------------------------------------------------------------------- Q4_0
+def pin_q4_0_hand(o):
+    # largest magnitude -1.0 first at index 0 -> d = 0.125 (fp16 0x3000); w = (q - 8) d
+    q = [i // 2 for i in range(32)]
+    w = np.array([(qi - 8) * 0.125 for qi in q], dtype=np.float32)
+    got = o.quantize_q4_0(w[None, :])[0, 0]
+    want = np.array([0x00, 0x30] + [(j // 2) | ((j // 2 + 8) << 4) for j in range(16)],
+                    dtype=np.uint8)
+    assert np.array_equal(got, want), (got, want)
+    # positive extreme: m = +2 -> d = -0.25 (0xB400); 2 -> q 0, 1 -> 4, -1 -> 12, 0 -> 8
+    w = np.zeros(32, dtype=np.float32)
+    w[0], w[1], w[17] = 2.0, 1.0, -1.0
+    got = o.quantize_q4_0(w[None, :])[0, 0]
+    want = np.full(18, 0x88, dtype=np.uint8)
+    want[0], want[1] = 0x00, 0xB4
+    want[2] = 0x80 | 0x0            # qs[0]: low q[0] = 0, high q[16] = 8
+    want[3] = (12 << 4) | 4         # qs[1]: low q[1] = 4, high q[17] = 12
+    assert np.array_equal(got, want), (got, want)
+    # opposite extreme saturates: m = +1 first, -1 -> round(8) + 8 = 16 -> 15
+    w = np.zeros(32, dtype=np.float32)
+    w[0], w[5] = 1.0, -1.0
+    got = o.quantize_q4_0(w[None, :])[0, 0]
+    assert got[2] & 15 == 0 and got[2 + 5] & 15 == 15
+    # all zero -> d = +0 / -8 = -0.0 in IEEE arithmetic (fp16 0x8000), every nibble 8
+    got = o.quantize_q4_0(np.zeros((1, 32), np.float32))[0, 0]
+    assert np.array_equal(got, np.array([0x00, 0x80] + [0x88] * 16, dtype=np.uint8))
+
+
+def pin_q4_0_nearest_level(o):
+    """q is the nearest level to w/d (ties away from zero), clamped: brute-force search."""
+    rng = np.random.default_rng(2)
+    w = (rng.standard_normal((64, 32)) * 0.02).astype(np.float32)
+    w[3, 7] = -np.abs(w[3]).max() * 1.5  # a negative extreme
+    blocks = o.quantize_q4_0(w)[:, 0]
+    for bi in range(w.shape[0]):
+        m = w[bi][np.argmax(np.abs(w[bi]))]
+        d = np.float32(m) / np.float32(-8.0)
+        d16 = int(np.float32(d).astype(np.float16).view(np.uint16))
+        assert int(blocks[bi, 0]) | (int(blocks[bi, 1]) << 8) == d16
+        for i in range(32):
+            r = float(np.float32(w[bi, i]) / d)
+            best, bestd = None, None
+            for c in range(-8, 8 + 1):
+                dist = abs(r - c)
+                if bestd is None or dist < bestd - 1e-12 or (abs(dist - bestd) <= 1e-12 and abs(c) > abs(best)):
+                    best, bestd = c, dist
+            qwant = min(15, max(0, best + 8))
+            byte = blocks[bi, 2 + (i % 16)]
+            qgot = (byte & 15) if i < 16 else (byte >> 4)
+            assert qgot == qwant, (bi, i, qgot, qwant)
+        # the extreme element always maps to level 0
+        i = int(np.argmax(np.abs(w[bi])))
+        byte = blocks[bi, 2 + (i % 16)]
+        assert ((byte & 15) if i < 16 else (byte >> 4)) == 0
+
+
+def pin_q4_0_matches_generator(o):
+    from bit_quantized_moe_quantize_gb300 import synth
+    rng = np.random.default_rng(3)
+    w = (rng.standard_normal((3, 5, 256)) * 0.02).astype(np.float32)
+    w[0, 0, :32] = 0.0
+    w[1, 2, 40] = -w[1, 2, 32:64].max() * 3
+    assert np.array_equal(o.quantize_q4_0(w), synth.encode_q4_0(w))
+
+
+def pin_q4_0_dequant(o):
+    rng = np.random.default_rng(4)
+    w = (rng.standard_normal((10, 64)) * 0.02).astype(np.float32)
+    blocks = o.quantize_q4_0(w)
+    deq = o.dequantize_q4_0(blocks)
+    assert np.array_equal(deq, numpy_decode_q4_0(blocks))
+    # round trip: within half a level of w/d (plus the fp16 rounding of d), except where
+    # w/d lies past 7.5, the top level 7 being the last one (then within one level)
+    wb = w.reshape(10, 2, 32)
+    d32 = np.array([[np.float32(b[np.argmax(np.abs(b))]) / np.float32(-8) for b in row] for row in wb])
+    r = wb.astype(np.float64) / d32[..., None]
+    err = np.abs(deq.reshape(10, 2, 32) - wb.astype(np.float64))
+    ad = np.abs(d32)[..., None]
+    sat = r > 7.5
+    bound = np.where(sat, 1.0, 0.5) * ad * (1 + 1e-6) + 8 * ad * 2.0 ** -11
+    assert np.all(err <= bound)
+    assert np.all(np.abs(r) <= 8 * (1 + 1e-6))
+
+
+# ------------------------------------------------------------------- Q8_1
+def _q8_numpy_fp32(x16: np.ndarray):
+    """fp32 replay of the activation quantizer as the workload defines it."""
+    x = x16.astype(np.float32).reshape(-1, 32)
+    amax = np.abs(x).max(axis=1)
+    d = (amax / np.float32(127.0)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (x / d[:, None]).astype(np.float64)
+    q = np.where(amax[:, None] == 0, 0, np.trunc(r + np.copysign(0.5, r)))
+    q = np.clip(q, -127, 127).astype(np.int64)
+    s = (d * q.sum(axis=1).astype(np.float32)).astype(np.float32)
+    return d.astype(np.float16), s.astype(np.float16), q
+
+
+def pin_q8_1_hand(o):
+    # all 2.0: d = fp16(2/127), every q = 127, s = fp16(d32 * 4064) = 64.0
+    x = np.full((1, 32), 2.0, dtype=np.float16)
+    blk = o.quantize_q8_1(x)[0, 0]
+    assert np.all(blk[4:].view(np.int8) == 127)
+    d = np.frombuffer(blk[0:2].tobytes(), np.float16)[0]
+    s = np.frombuffer(blk[2:4].tobytes(), np.float16)[0]
+    assert d == np.float16(2.0 / 127.0)
+    assert s == np.float16(64.0)
+    # zero block: every byte 0
+    blk = o.quantize_q8_1(np.zeros((1, 32), np.float16))[0, 0]
+    assert not blk.any()
+    # one nonzero element -0.5 at index 9: q[9] = -127, the rest 0, s = -d*127 = -0.5
+    x = np.zeros((1, 32), np.float16)
+    x[0, 9] = -0.5
+    blk = o.quantize_q8_1(x)[0, 0]
+    q = blk[4:].view(np.int8)
+    assert q[9] == -127 and np.count_nonzero(q) == 1
+    assert np.frombuffer(blk[2:4].tobytes(), np.float16)[0] == np.float16(-0.5)
+    # amax = 127 -> d32 = 1 exactly, so q = x for integer x
+    x = np.zeros((1, 32), np.float16)
+    x[0, :8] = [127, -127, 1, -1, 2, 50, -99, 3]
+    blk = o.quantize_q8_1(x)[0, 0]
+    assert blk[0] == 0x00 and blk[1] == 0x3C                       # d = 1.0
+    assert blk[4:].view(np.int8)[:8].tolist() == [127, -127, 1, -1, 2, 50, -99, 3]
+    assert np.frombuffer(blk[2:4].tobytes(), np.float16)[0] == np.float16(-44.0)
+    # amax = 63.5 -> d32 = 0.5 exactly, so q = 2x
+    x = np.zeros((1, 32), np.float16)
+    x[0, 30:32] = [63.5, 0.5]
+    x[0, 0:3] = [-63.5, -0.5, 10.0]
+    blk = o.quantize_q8_1(x)[0, 0]
+    assert blk[0] == 0x00 and blk[1] == 0x38                       # d = 0.5
+    q = blk[4:].view(np.int8)
+    assert q[[0, 1, 2, 30, 31]].tolist() == [-127, -1, 20, 127, 1]
+    assert np.count_nonzero(q) == 5
+
+
+def pin_q8_1_numpy(o):
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((9, 256)).astype(np.float16)
+    x[2, 32:64] = 0
+    x[3, :] *= np.float16(20)
+    x[4, 64:96] = np.float16(6e-5)   # tiny block: d lands in fp16 subnormals
+    blk = o.quantize_q8_1(x).reshape(-1, 36)
+    d, s, q = _q8_numpy_fp32(x)
+    assert np.array_equal(blk[:, 0:2].copy().view(np.float16)[:, 0].view(np.uint16), d.view(np.uint16))
+    assert np.array_equal(blk[:, 2:4].copy().view(np.float16)[:, 0].view(np.uint16), s.view(np.uint16))
+    assert np.array_equal(blk[:, 4:].view(np.int8).astype(np.int64), q)
+
+
+def pin_q8_1_error_bound(o):
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((16, 512)).astype(np.float16)
+    blk = o.quantize_q8_1(x)
+    deq = o.dequantize_q8_1(blk)
+    assert np.array_equal(deq, numpy_decode_q8_1(blk))
+    xb = x.astype(np.float64).reshape(-1, 32)
+    amax = np.abs(xb).max(axis=1)
+    d32 = amax / 127.0
+    err = np.abs(deq.reshape(-1, 32) - xb)
+    # half a level plus the fp16 rounding of d applied to |q| <= 127
+    bound = 0.5 * d32 * (1 + 1e-6) + 127 * d32 * 2.0 ** -11
+    assert np.all(err <= bound[:, None])
+    q = blk.reshape(-1, 36)[:, 4:].view(np.int8)
+    assert np.all(np.abs(q).max(axis=1) == 127)
+
+
+# ------------------------------------------------------------------ route
+def pin_route(o):
+    rng = np.random.default_rng(7)
+    for S, E in [(0, 4), (1, 1), (37, 5), (500, 16), (64, 128)]:
+        ids = rng.integers(0, E, S).astype(np.int32)
+        counts, offsets, perm, bad = o.route(ids, E)
+        assert bad == 0
+        assert np.array_equal(counts, np.bincount(ids, minlength=E))
+        assert offsets[0] == 0 and offsets[-1] == S
+        assert np.array_equal(np.diff(offsets), counts)
+        assert np.array_equal(perm, np.argsort(ids, kind="stable"))
+    ids = np.array([3, -1, 0, 7, 3, 9, 0], dtype=np.int32)
+    counts, offsets, perm, bad = o.route(ids, 4)
+    assert bad == 3
+    assert counts.tolist() == [2, 0, 0, 2]
+    assert offsets.tolist() == [0, 2, 2, 2, 4]
+    assert perm.tolist() == [2, 6, 0, 4, -1, -1, -1]
+
+
+# -------------------------------------------------------------------- dot
+def pin_block_dot_hand(o):
+    zero_d = 0x3C00   # fp16 1.0 (the scales do not enter the integer dot)
+    assert o.block_dot(q4_block(zero_d, [9] * 32), q8_block(zero_d, 0, [1] * 32)) == 32
+    assert o.block_dot(q4_block(zero_d, [0] * 32), q8_block(zero_d, 0, [127] * 32)) == -32512
+    assert o.block_dot(q4_block(zero_d, [15] * 32), q8_block(zero_d, 0, [-127] * 32)) == -28448
+    # single nonzero weight in the high-nibble half: only a[20] matters
+    qw = [8] * 32
+    qw[20] = 15
+    qa = list(range(-16, 16))
+    assert o.block_dot(q4_block(zero_d, qw), q8_block(zero_d, 0, qa)) == 7 * qa[20]
+    # single nonzero weight in the low-nibble half
+    qw = [8] * 32
+    qw[3] = 1
+    assert o.block_dot(q4_block(zero_d, qw), q8_block(zero_d, 0, qa)) == -7 * qa[3]
+
+
+def pin_moe_closed_form_vs_bruteforce(o):
+    for seed, T in [(10, 7), (11, 1), (12, 13)]:
+        w, x, ids = tiny_case(seed=seed, T=T)
+        act = o.quantize_q8_1(x)
+        y = o.moe(w, act, ids).astype(np.float64)
+        bf = o.moe_dequant_bruteforce(w, act, ids)
+        scale = np.abs(bf).max()
+        assert np.all(np.abs(y - bf) <= 1e-6 * np.abs(bf) + 1e-12 * scale)
+        ys = o.moe_sample(w, act, ids, np.arange(T * ids.shape[1]), np.zeros(T * ids.shape[1], np.int64))
+        assert np.all(np.abs(ys - bf[:, :, 0].reshape(-1)) <= 1e-12 * scale)
+
+
+def pin_moe_numpy_einsum(o):
+    """Decode both operands independently in numpy and contract with einsum."""
+    for seed, T, k in [(20, 9, 2), (21, 4, 3)]:
+        w, x, ids = tiny_case(seed=seed, T=T, k=k)
+        act = o.quantize_q8_1(x)
+        W = numpy_decode_q4_0(w)                   # [E, N, K]
+        A = numpy_decode_q8_1(act)                 # [T, K]
+        want = np.einsum("tjnk,tk->tjn", W[ids], A)
+        got = o.moe(w, act, ids).astype(np.float64)
+        tol = 1e-6 * np.abs(want) + 1e-9 * np.abs(want).max()
+        assert np.all(np.abs(got - want) <= tol)
+
+
+def pin_moe_block_dots(o):
+    w, x, ids = tiny_case(seed=30, T=3, K=64, N=5)
+    act = o.quantize_q8_1(x)
+    dots = o.moe_block_dots(w, act, ids)
+    qs = w[..., 2:].astype(np.int64)
+    Wq = np.concatenate([qs & 15, qs >> 4], axis=-1) - 8          # [E, N, nb, 32] levels
+    Aq = np.ascontiguousarray(act[..., 4:]).view(np.int8).astype(np.int64)   # [T, nb, 32]
+    flat = ids.reshape(-1)
+    for s in range(flat.size):
+        e, t = flat[s], s // ids.shape[1]
+        want = (Wq[e] * Aq[t][None]).sum(axis=-1)                # [N, nb]
+        assert np.array_equal(dots[s], want)
+
+
+def pin_moe_split_invariance(o):
+    w, x, ids = tiny_case(seed=40, T=11)
+    act = o.quantize_q8_1(x)
+    y = o.moe(w, act, ids)
+    y1 = o.moe(w, act[:5], ids[:5])
+    y2 = o.moe(w, act[5:], ids[5:])
+    assert np.array_equal(y, np.concatenate([y1, y2]))
+
+
+def pin_moe_bad_ids(o):
+    w, x, ids = tiny_case(seed=50, T=4)
+    ids = ids.copy()
+    ids[1, 0] = -3
+    ids[2, 1] = w.shape[0]
+    act = o.quantize_q8_1(x)
+    y = o.moe(w, act, ids)
+    assert not y[1, 0].any() and not y[2, 1].any()
+    assert y[0].any() and y[3].any()
+
+
+ALL_PINS = [
+    pin_fp16, pin_q4_0_hand, pin_q4_0_nearest_level, pin_q4_0_matches_generator, pin_q4_0_dequant,
+    pin_q8_1_hand, pin_q8_1_numpy, pin_q8_1_error_bound, pin_route, pin_block_dot_hand,
+    pin_moe_closed_form_vs_bruteforce, pin_moe_numpy_einsum, pin_moe_block_dots,
+    pin_moe_split_invariance, pin_moe_bad_ids,
+]

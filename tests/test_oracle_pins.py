@@ -1,0 +1,96 @@
+"""The CPU oracle against its pins, and mutated oracles against the same pins.
+
+CPU only.  The mutation half copies ``oracle/ft_oracle.c``, plants one
+plausible mistake in the copy, builds it in a temporary directory and runs
+every pin on it in a fresh process: at least one pin must fail.  The committed
+oracle is never modified.
+"""
+
+import multiprocessing as mp
+import os
+import shutil
+
+import numpy as np
+import pytest
+
+import pins
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(oracle, pin):
+    pin(oracle)
+
+
+def test_workload_quantized_through_oracle(oracle):
+    """The tiny-layer workload goes through the oracle end to end; the result is
+    finite, has the documented shape and its zero pattern matches the routing."""
+    from bit_quantized_moe_quantize_gb300 import synth
+    case = synth.make_case("tiny", 16)
+    act = oracle.quantize_q8_1(case["x"])
+    y = oracle.moe(case["weights"], act, case["topk_ids"])
+    assert y.shape == (16, 2, 128) and np.isfinite(y).all()
+    assert np.abs(y).max() > 0
+
+
+MUTANTS = {
+    "q4_nibble_order_quantizer": ("(q[j] | (q[j + 16] << 4))", "(q[j + 16] | (q[j] << 4))"),
+    "q4_nibble_order_decode": ("return i < 16 ? (qs[i] & 0x0f) : (qs[i - 16] >> 4);",
+                               "return i < 16 ? (qs[i] >> 4) : (qs[i - 16] & 0x0f);"),
+    "q4_offset_7": ("(q4_0_nibble(w_block, i) - 8)", "(q4_0_nibble(w_block, i) - 7)"),
+    "q4_scale_sign": ("float d = m / -8.0f;", "float d = m / 8.0f;"),
+    "token_index_mod": ("int64_t t = s / top_k;", "int64_t t = s % top_k;"),
+    "q8_truncate": ("q = (int)roundf(x[i] / d);", "q = (int)(x[i] / d);"),
+    "q8_scale_128": ("float d = amax / 127.0f;", "float d = amax / 128.0f;"),
+    "q8_s_from_fp16_d": ("float s = d * (float)sum;",
+                         "float s = (float)oracle_half_to_double(oracle_float_to_half(d)) * (float)sum;"),
+    "dot_drops_act_scale": ("y += dw * da * (double)oracle_block_dot(wb, ab);",
+                            "y += dw * (double)oracle_block_dot(wb, ab);"),
+    "route_unstable": ("perm[offsets[e] + cursor[e]] = (int32_t)s;",
+                       "perm[offsets[e] + counts[e] - 1 - cursor[e]] = (int32_t)s;"),
+    "fp16_truncates": ("double q = nearbyint(m * 2048.0);", "double q = floor(m * 2048.0);"),
+    "bad_id_not_zeroed": ("    if (e < 0 || e >= n_experts)\n        return 0.0;\n",
+                          "    if (e < 0 || e >= n_experts)\n        e = 0;\n"),
+}
+
+
+def _run_pins_on(so_path, q):
+    import sys
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle as oracle_pkg
+    import pins as pins_mod
+    o = oracle_pkg.Oracle(so_path)
+    failed = []
+    for pin in pins_mod.ALL_PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            failed.append(pin.__name__)
+        except Exception as exc:  # a mutant that misbehaves otherwise also counts as caught
+            failed.append(f"{pin.__name__}:{type(exc).__name__}")
+    q.put(failed)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    import oracle as oracle_pkg
+    src = os.path.join(ROOT, "oracle", "ft_oracle.c")
+    text = open(src).read()
+    old, new = MUTANTS[name]
+    assert text.count(old) >= 1, f"mutation site for {name} not found"
+    mut = tmp_path / "ft_oracle.c"
+    mut.write_text(text.replace(old, new))
+    shutil.copy(os.path.join(ROOT, "oracle", "ft_oracle.h"), tmp_path / "ft_oracle.h")
+    so = oracle_pkg.build(src=str(mut), out_dir=str(tmp_path))
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_run_pins_on, args=(so, q))
+    p.start()
+    p.join(300)
+    if p.is_alive():
+        p.kill()
+        pytest.fail(f"mutant {name} hung")
+    failed = q.get() if p.exitcode == 0 else [f"crashed({p.exitcode})"]
+    assert failed, f"mutant {name} passed every pin"

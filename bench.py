@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Benchmark of the routed Q4_0 x Q8_1 MoE expert matmul (quantize + route +
+matmul per step) on GB300; prints one JSON line.
+
+Default workload: the prefill batch shaped like the kernel benchmark of
+FreeToken PR #185 ("Performance": nrows 1408, hidden 2816, top_k 8, 8191
+tokens), with 128 experts, uniform routing, seed 1; synthetic inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME:TOKENS]
+
+ours       value = routed tokens/s over all ranks with inputs resident in HBM
+           (L2 flushed between steps); e2e = the same through the Python API
+           with pinned host buffers and the host<->device copies in the timed
+           region; roofline of the dominant kernel from CUDA events the library
+           records on its launch stream; cpu_baseline = the CPU oracle on a
+           bounded sample (rank 0 only).
+reference  the CPU oracle (the only reference this project has) on a bounded
+           sample of the same workload per step, rank 0 only.
+Multi-GPU: one process per GPU, each an independent replica on its own batch
+(weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "routed tokens/s"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Tesla T4, moe_vec q4_0 x q8_1 after the grid.x fix, 8191 tokens: 705.8 ms
+# (FreeToken PR #185, "Performance"); context only, other hardware.
+PAGES_T4_TOKENS_PER_S = {("prefill", 8191): 8191 / 0.7058, ("prefill", 4096): 4096 / 0.3461,
+                         ("prefill", 2048): 2048 / 0.1740}
+# DRAM bytes per launch of the dominant kernel from one ncu capture, keyed by
+# the library source hash it was taken on (stale entries are not reported).
+NCU_TRAFFIC = {}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill:8191")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload(spec):
+    from bit_quantized_moe_quantize_gb300 import synth
+    name, _, t = spec.partition(":")
+    wl = synth.WORKLOADS[name]
+    T = int(t) if t else max(wl.tokens)
+    return name, wl, T
+
+
+def make_inputs(wl, T, rank):
+    from bit_quantized_moe_quantize_gb300 import synth
+    w = synth.make_weights(wl)
+    # each replica gets its own batch (same weights, different tokens)
+    wl_r = synth.Workload(**{**wl.__dict__, "seed": wl.seed + 7919 * rank}) if rank else wl
+    x = synth.make_activations(wl_r, T)
+    ids = synth.make_topk_ids(wl_r, T)
+    return w, x, ids
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "begin":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.samples:
+            if self.t0 is not None and not (self.t0 - 0.1 <= ts <= (self.t1 or ts) + 0.1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({self.NAMES[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_tokens_per_s(wl, w, x, ids, budget_s, max_tokens=None):
+    """Time the CPU oracle (quantize + route + matmul) on the first n tokens, n
+    sized so the run takes about budget_s; returns (tokens/s, n, seconds)."""
+    import oracle as oracle_pkg
+    o = oracle_pkg.get()
+
+    def run(n):
+        t0 = time.perf_counter()
+        act = o.quantize_q8_1(x[:n])
+        o.route(ids[:n], wl.n_experts)
+        o.moe(w, act, ids[:n])
+        return time.perf_counter() - t0
+
+    t1 = run(1)
+    n = int(max(1, min(max_tokens or x.shape[0], budget_s / max(t1, 1e-6))))
+    dt = run(n)
+    return n / dt, n, dt
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    name, wl, T = workload(args.workload)
+    w, x, ids = make_inputs(wl, T, 0)
+    import oracle as oracle_pkg
+    o = oracle_pkg.get()
+    total_budget = 150.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    t0 = time.perf_counter()
+    act = o.quantize_q8_1(x[:1])
+    o.moe(w, act, ids[:1])
+    t_tok = time.perf_counter() - t0
+    n = int(max(1, min(T, per_step / max(t_tok, 1e-6))))
+    times = []
+    for i in range(args.warmup + args.steps):
+        s0 = (i * n) % max(1, T - n + 1)
+        t0 = time.perf_counter()
+        act = o.quantize_q8_1(x[s0:s0 + n])
+        o.route(ids[s0:s0 + n], wl.n_experts)
+        o.moe(w, act, ids[s0:s0 + n])
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1000 * statistics.mean(times)
+    value = n / (ms / 1000)
+    sample = f"{n} of {T} tokens per step (quantize + route + matmul in the oracle, single thread)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(name, wl, T, world),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(name, wl, T, world):
+    return {"workload": f"{name} E={wl.n_experts} k={wl.top_k} K={wl.ncols} N={wl.nrows} T={T}",
+            "n_experts": wl.n_experts, "top_k": wl.top_k, "ncols": wl.ncols, "nrows": wl.nrows, "tokens": T,
+            "routing": wl.routing, "seed": wl.seed, "replicas": world,
+            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)"}
+
+
+# ------------------------------------------------------------------ ours
+def ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import bit_quantized_moe_quantize_gb300 as ft
+    from bit_quantized_moe_quantize_gb300 import build
+    build.build()
+    ft.load()
+    ft.set_path("auto")
+
+    name, wl, T = workload(args.workload)
+    w, x, ids = make_inputs(wl, T, rank)
+    E, k, K, N = wl.n_experts, wl.top_k, wl.ncols, wl.nrows
+    S = T * k
+    path = {1: "gemv", 2: "gemm"}[ft.selected_path(T, k, E, N, K)]
+
+    dw = torch.from_numpy(w).to(dev)
+    dx = torch.from_numpy(x).to(dev)
+    di = torch.from_numpy(ids).to(dev)
+    act = torch.empty((T, K // 32, 36), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, k, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ft.reserve(T, k, E, N, K)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ft.quantize_q8_1(dx, out=act)
+        ft.moe_q4_0_q8_1(dw, act, di, out=out)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if ft.read_device_error():
+        raise RuntimeError("device error flag raised during warm-up")
+
+    gpu_index = torch.cuda.current_device()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[gpu_index])
+        except ValueError:
+            pass
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ft.profile_enable(args.steps)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.mark("begin")
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks.mark("end")
+    prof = ft.profile_read()
+    ft.profile_enable(0)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = T * world / (ms / 1000.0)
+
+    # e2e through the public API: pinned host input -> device -> result -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.from_numpy(x).pin_memory()
+        hi = torch.from_numpy(ids).pin_memory()
+        ho = torch.empty((T, k, N), dtype=torch.float32).pin_memory()
+        n_e2e = max(3, min(args.steps, 50))
+        e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
+        for i in range(args.warmup + n_e2e):
+            flush.zero_()
+            j = i - args.warmup
+            if j >= 0:
+                e_ev[j][0].record(stream)
+            dx.copy_(hx, non_blocking=True)
+            di.copy_(hi, non_blocking=True)
+            step()
+            ho.copy_(out, non_blocking=True)
+            if j >= 0:
+                e_ev[j][1].record(stream)
+        torch.cuda.synchronize()
+        e_ms = statistics.mean(a.elapsed_time(b) for a, b in e_ev)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": T * world / (e_ms / 1000.0), "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": int(x.nbytes + ids.nbytes), "d2h_bytes_per_step": int(S * N * 4)}
+        assert np.array_equal(ho.numpy(), out.cpu().numpy())
+    if ft.read_device_error():
+        raise RuntimeError("device error flag raised during the timed region")
+    clk = clocks.stop()
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    calls = max(1, prof["calls"])
+    mm_ms = prof["matmul_ms"] / calls
+    flops = 2.0 * S * N * K
+    counts = np.bincount(ids.reshape(-1), minlength=E)
+    nb = K // 32
+    alg_bytes = int((counts > 0).sum()) * N * nb * 18 + T * nb * 36 + S * N * 4
+    if path == "gemm":
+        kern = "moe_gemm_tc_kernel"
+        achieved = flops / (mm_ms / 1000.0) / 1e12
+        roof = {"kernel": kern, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "peak_note": f"fp16 kind::f16 MMA at the bf16 rate (nominal ratio 1.0), burst, of {peak_src}",
+                "algorithmic": f"2*S*N*K = {flops:.4g} FLOP per launch", "kernel_ms": mm_ms}
+    else:
+        kern = "moe_gemv_kernel"
+        achieved = alg_bytes / (mm_ms / 1000.0) / 1e9
+        roof = {"kernel": kern, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_note": f"copy bandwidth, of {peak_src}",
+                "algorithmic": f"unique expert weights + Q8_1 act + fp32 out = {alg_bytes} B per launch",
+                "kernel_ms": mm_ms}
+    from bit_quantized_moe_quantize_gb300 import build as _b
+    tr = NCU_TRAFFIC.get((kern, _b.source_hash(), args.workload))
+    roof["traffic"] = tr
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        tps, n, dt = oracle_tokens_per_s(wl, w, x, ids, budget_s=12.0)
+        cpu = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"first {n} of {T} tokens: quantize + route + matmul, {dt:.1f} s single thread"}
+
+    base = PAGES_T4_TOKENS_PER_S.get((name, T))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / base) if base else None,
+        "vs_baseline_note": "pages' Tesla T4 moe_vec time for this token count (context, other hardware)"
+        if base else None,
+        "dtype": "q4_0 x q8_1: exact int block dots (f16 MMA / dp4a), f32 scaling",
+        "data": "synthetic", "config": {**config_of(name, wl, T, world), "path": path},
+        "effective_tops": 2.0 * S * N * K * world / (ms / 1000.0) / 1e12,
+        "kernels_ms_per_step": {"quantize": prof["quantize_ms"] / calls, "route": prof["route_ms"] / calls,
+                                "matmul": mm_ms},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(prof["launches"]), "clocks": clk, "wall_s_timed": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return reference_arm(args)
+    return ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

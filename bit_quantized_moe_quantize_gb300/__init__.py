@@ -1,0 +1,19 @@
+"""GB300 (sm_103a) routed Q4_0 x Q8_1 MoE expert matmul.
+
+The computation lives in ``libft_moe.so`` (hand-written CUDA, C ABI in
+``include/ft_moe.h``); this package is its thin Python binding plus the seeded
+synthetic-input generator used by the tests and the benchmark.
+
+    act = quantize_q8_1(x_fp16)                       # fp16 [T, K] -> Q8_1
+    out = moe_q4_0_q8_1(weights_q4_0, act, topk_ids)  # fp32 [T, k, N]
+"""
+
+from ._lib import (FT_DEVERR_BAD_EXPERT_ID, FT_DEVERR_WAIT_TIMEOUT, FT_PATH_AUTO, FT_PATH_GEMM, FT_PATH_GEMV,
+                   FtError, block_dots, last_error, load, moe_q4_0_q8_1, profile_enable, profile_read, quantize_q8_1,
+                   read_device_error, release, reserve, route_offsets, selected_path, set_path, workspace_bytes)
+
+__all__ = [
+    "FT_DEVERR_BAD_EXPERT_ID", "FT_DEVERR_WAIT_TIMEOUT", "FT_PATH_AUTO", "FT_PATH_GEMM", "FT_PATH_GEMV", "FtError",
+    "block_dots", "last_error", "load", "moe_q4_0_q8_1", "profile_enable", "profile_read", "quantize_q8_1", "read_device_error", "release", "reserve",
+    "route_offsets", "selected_path", "set_path", "workspace_bytes",
+]

@@ -1,0 +1,227 @@
+"""ctypes binding of libft_moe.so: argument marshalling only.
+
+Every function here checks tensor dtypes, devices and shapes, then passes raw
+device pointers and the current CUDA stream to the C ABI declared in
+``include/ft_moe.h``.  No arithmetic of the routed matmul happens in Python,
+and there is no fallback: if the library is missing or was built from other
+sources, loading raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libft_moe.so")
+
+FT_OK, FT_ERR_ARG, FT_ERR_SIZE, FT_ERR_ALIGN, FT_ERR_LAUNCH, FT_ERR_WORKSPACE, FT_ERR_CUDA, FT_ERR_DEVICE_FLAG = range(8)
+STATUS_NAMES = {0: "FT_OK", 1: "FT_ERR_ARG", 2: "FT_ERR_SIZE", 3: "FT_ERR_ALIGN", 4: "FT_ERR_LAUNCH",
+                5: "FT_ERR_WORKSPACE", 6: "FT_ERR_CUDA", 7: "FT_ERR_DEVICE_FLAG"}
+FT_DEVERR_BAD_EXPERT_ID = 0x1
+FT_DEVERR_WAIT_TIMEOUT = 0x2
+FT_PATH_AUTO, FT_PATH_GEMV, FT_PATH_GEMM = 0, 1, 2
+PATHS = {"auto": FT_PATH_AUTO, "gemv": FT_PATH_GEMV, "gemm": FT_PATH_GEMM}
+
+EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_moe_workspace_bytes",
+           "ft_moe_reserve", "ft_moe_release", "ft_moe_read_device_error", "ft_moe_set_path",
+           "ft_moe_selected_path", "ft_moe_block_dots", "ft_last_error", "ft_abi_version", "ft_profile_enable",
+           "ft_profile_read")
+
+
+class FtError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library, refusing a build whose source hash is stale."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        from . import build as _build
+        if not os.path.exists(path):
+            raise FtError(FT_ERR_CUDA, f"{path} is missing: run bit_quantized_moe_quantize_gb300.build.build()")
+        if path == LIB_PATH and not _build.is_current():
+            raise FtError(FT_ERR_CUDA, f"{path} was built from other sources: rebuild it")
+        L = ctypes.CDLL(path)
+        i64, i32, vp, u32p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)
+        L.ft_quantize_q8_1.argtypes = [vp, vp, i64, i64, vp]
+        L.ft_moe_route_offsets.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp]
+        L.ft_moe_q4_0_q8_1.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
+        L.ft_moe_block_dots.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
+        L.ft_moe_workspace_bytes.argtypes = [i64, i32, i32, i64, i64]
+        L.ft_moe_workspace_bytes.restype = ctypes.c_size_t
+        L.ft_moe_reserve.argtypes = [i64, i32, i32, i64, i64]
+        L.ft_moe_release.argtypes = []
+        L.ft_moe_read_device_error.argtypes = [vp, u32p]
+        L.ft_moe_set_path.argtypes = [i32]
+        L.ft_moe_selected_path.argtypes = [i64, i32, i32, i64, i64]
+        L.ft_last_error.argtypes = []
+        L.ft_last_error.restype = ctypes.c_char_p
+        L.ft_abi_version.argtypes = []
+        L.ft_profile_enable.argtypes = [i32]
+        dp, lp = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)
+        L.ft_profile_read.argtypes = [dp, dp, dp, lp, lp]
+        for name in EXPORTS:
+            getattr(L, name).restype = getattr(L, name).restype or ctypes.c_int
+        L.ft_moe_workspace_bytes.restype = ctypes.c_size_t
+        L.ft_last_error.restype = ctypes.c_char_p
+        _lib = L
+        return L
+
+
+def last_error() -> str:
+    return load().ft_last_error().decode()
+
+
+def _check(status: int):
+    if status != FT_OK:
+        raise FtError(status, last_error())
+
+
+# ------------------------------------------------------------------ tensors
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(t):
+    torch = _torch()
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _dev(t, dtype, name, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def quantize_q8_1(x, out=None):
+    """fp16 [T, K] -> Q8_1 uint8 [T, K/32, 36] (ft_quantize_q8_1)."""
+    torch = _torch()
+    px = _dev(x, torch.float16, "x", 2)
+    T, K = x.shape
+    if out is None:
+        out = torch.empty((T, K // 32, 36), dtype=torch.uint8, device=x.device)
+    po = _dev(out, torch.uint8, "out")
+    _check(load().ft_quantize_q8_1(px, po, T, K, _stream(x)))
+    return out
+
+
+def route_offsets(topk_ids, n_experts, counts=None, offsets=None, perm=None, dev_err=None):
+    """int32 [T, k] -> (counts [E], offsets [E+1], perm [T*k]) (ft_moe_route_offsets)."""
+    torch = _torch()
+    pid = _dev(topk_ids, torch.int32, "topk_ids", 2)
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    counts = torch.empty(n_experts, dtype=torch.int32, device=dev) if counts is None else counts
+    offsets = torch.empty(n_experts + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev) if perm is None else perm
+    pe = ctypes.c_void_p(0) if dev_err is None else _dev(dev_err, torch.int32, "dev_err")
+    _check(load().ft_moe_route_offsets(pid, T, k, n_experts, _dev(counts, torch.int32, "counts"),
+                                       _dev(offsets, torch.int32, "offsets"), _dev(perm, torch.int32, "perm"),
+                                       pe, _stream(topk_ids)))
+    return counts, offsets, perm
+
+
+def _matmul_shape(weights, act, topk_ids):
+    torch = _torch()
+    _dev(weights, torch.uint8, "weights", 4)
+    _dev(act, torch.uint8, "act", 3)
+    _dev(topk_ids, torch.int32, "topk_ids", 2)
+    E, N, nb, wb = weights.shape
+    T, nb2, ab = act.shape
+    if wb != 18 or ab != 36 or nb != nb2 or topk_ids.shape[0] != T:
+        raise ValueError(f"shape mismatch: weights {tuple(weights.shape)} act {tuple(act.shape)} "
+                         f"topk_ids {tuple(topk_ids.shape)}")
+    return E, N, nb * 32, T, topk_ids.shape[1]
+
+
+def moe_q4_0_q8_1(weights, act, topk_ids, out=None):
+    """Routed matmul: Q4_0 [E,N,K/32,18] x Q8_1 [T,K/32,36] -> fp32 [T, k, N] (ft_moe_q4_0_q8_1)."""
+    torch = _torch()
+    E, N, K, T, k = _matmul_shape(weights, act, topk_ids)
+    if out is None:
+        out = torch.empty((T, k, N), dtype=torch.float32, device=weights.device)
+    po = _dev(out, torch.float32, "out")
+    _check(load().ft_moe_q4_0_q8_1(ctypes.c_void_p(weights.data_ptr()), ctypes.c_void_p(act.data_ptr()),
+                                   ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, E, N, K, _stream(weights)))
+    return out
+
+
+def block_dots(weights, act, topk_ids, out=None):
+    """Diagnostic: int32 [T*k, N, K/32] per-block integer dots (ft_moe_block_dots)."""
+    torch = _torch()
+    E, N, K, T, k = _matmul_shape(weights, act, topk_ids)
+    if out is None:
+        out = torch.empty((T * k, N, K // 32), dtype=torch.int32, device=weights.device)
+    po = _dev(out, torch.int32, "out")
+    _check(load().ft_moe_block_dots(ctypes.c_void_p(weights.data_ptr()), ctypes.c_void_p(act.data_ptr()),
+                                    ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, E, N, K, _stream(weights)))
+    return out
+
+
+def workspace_bytes(tokens, top_k, n_experts, nrows, ncols) -> int:
+    return int(load().ft_moe_workspace_bytes(tokens, top_k, n_experts, nrows, ncols))
+
+
+def reserve(max_tokens, max_top_k, n_experts, nrows, ncols):
+    _check(load().ft_moe_reserve(max_tokens, max_top_k, n_experts, nrows, ncols))
+
+
+def release():
+    _check(load().ft_moe_release())
+
+
+def read_device_error(stream=None) -> int:
+    """Synchronize, return and clear the library's device error word (no raise)."""
+    torch = _torch()
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream if stream is None else stream)
+    flags = ctypes.c_uint32(0)
+    st = load().ft_moe_read_device_error(s, ctypes.byref(flags))
+    if st not in (FT_OK, FT_ERR_DEVICE_FLAG):
+        raise FtError(st, last_error())
+    return int(flags.value)
+
+
+def set_path(path) -> int:
+    p = PATHS[path] if isinstance(path, str) else int(path)
+    prev = load().ft_moe_set_path(p)
+    if prev < 0:
+        raise ValueError(f"unknown path {path!r}")
+    return prev
+
+
+def selected_path(tokens, top_k, n_experts, nrows, ncols) -> int:
+    return int(load().ft_moe_selected_path(tokens, top_k, n_experts, nrows, ncols))
+
+
+def profile_enable(max_calls: int):
+    """Record CUDA events around this library's kernels for the next max_calls calls (0 stops)."""
+    _check(load().ft_profile_enable(int(max_calls)))
+
+
+def profile_read() -> dict:
+    """Synchronize on the recorded events; summed kernel times (ms), calls and launches; resets."""
+    q, r, m = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    n, nl = ctypes.c_int64(), ctypes.c_int64()
+    _check(load().ft_profile_read(ctypes.byref(q), ctypes.byref(r), ctypes.byref(m), ctypes.byref(n),
+                                  ctypes.byref(nl)))
+    return {"quantize_ms": q.value, "route_ms": r.value, "matmul_ms": m.value, "calls": n.value,
+            "launches": nl.value}

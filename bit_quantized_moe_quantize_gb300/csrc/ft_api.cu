@@ -1,0 +1,580 @@
+// C ABI of libft_moe.so: argument validation, workspace, path dispatch and
+// launch checks around the kernels.  See include/ft_moe.h for the contract.
+//
+// Every size product is formed in 64-bit (mlxcel PR #652, "Fix": the int32
+// product m * n that overflowed and yielded a zero grid), and every kernel
+// launch is followed by a check of its status that names the kernel and its
+// grid (FreeToken PR #185, "Fix": FT_MOE_VEC_LAUNCH_CHECK after each launch,
+// so a rejected geometry is reported where it happens instead of by the next
+// unrelated CUDA call).
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "../../include/ft_moe.h"
+#include "ft_internal.h"
+
+namespace ft {
+
+static thread_local std::string g_last_error;
+
+int fail(int status, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
+// ---------------------------------------------------------------- profiling
+struct Prof {
+    std::mutex mu;
+    bool on = false;
+    int max_calls = 0;
+    cudaEvent_t* ev = nullptr;       // [max_calls][5]: quant b/e, route b, matmul b/e
+    int n_quant = 0, n_mm = 0;
+    bool quant_open = false, mm_open = false;
+    int64_t launches = 0;
+};
+static Prof g_prof;
+
+void prof_count_launch() {
+    if (g_prof.on) {
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        ++g_prof.launches;
+    }
+}
+
+void prof_mark(ProfPoint p, cudaStream_t s) {
+    if (!g_prof.on) return;
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    Prof& P = g_prof;
+    switch (p) {
+        case kProfQuantBegin:
+            if (P.n_quant < P.max_calls) {
+                cudaEventRecord(P.ev[P.n_quant * 5 + 0], s);
+                P.quant_open = true;
+            }
+            break;
+        case kProfQuantEnd:
+            if (P.quant_open) {
+                cudaEventRecord(P.ev[P.n_quant * 5 + 1], s);
+                P.quant_open = false;
+                ++P.n_quant;
+            }
+            break;
+        case kProfRouteBegin:
+            if (P.n_mm < P.max_calls) {
+                cudaEventRecord(P.ev[P.n_mm * 5 + 2], s);
+                P.mm_open = true;
+            }
+            break;
+        case kProfMatmulBegin:
+            if (P.mm_open) cudaEventRecord(P.ev[P.n_mm * 5 + 3], s);
+            break;
+        case kProfMatmulEnd:
+            if (P.mm_open) {
+                cudaEventRecord(P.ev[P.n_mm * 5 + 4], s);
+                P.mm_open = false;
+                ++P.n_mm;
+            }
+            break;
+    }
+}
+
+int check_launch(const char* kernel, dim3 grid, dim3 block, size_t smem) {
+    prof_count_launch();
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) return FT_OK;
+    return fail(FT_ERR_LAUNCH, "launch of %s failed: %s (grid %u x %u x %u, block %u x %u x %u, smem %zu)", kernel,
+                cudaGetErrorString(e), grid.x, grid.y, grid.z, block.x, block.y, block.z, smem);
+}
+
+static int cuda_fail(cudaError_t e, const char* what) {
+    return fail(FT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static std::mutex g_attr_mu;
+
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 148;
+    }
+    return cache[dev];
+}
+
+int set_smem_limit(const void* kernel, int bytes) {
+    struct Entry {
+        const void* k;
+        int dev;
+        int bytes;
+    };
+    static Entry done[256];
+    static int n_done = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].k == kernel && done[i].dev == dev && done[i].bytes >= bytes) return FT_OK;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].k == kernel && done[i].dev == dev) {
+            done[i].bytes = bytes;
+            return FT_OK;
+        }
+    if (n_done < 256) done[n_done++] = Entry{kernel, dev, bytes};
+    return FT_OK;
+}
+
+// ------------------------------------------------------------- validation
+static bool mul_ok(int64_t a, int64_t b, int64_t* r) {
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > INT64_MAX / a) return false;
+    *r = a * b;
+    return true;
+}
+
+struct Shape {
+    int64_t tokens, n_slots, nrows, ncols, nb;
+    int32_t top_k, n_experts;
+};
+
+// Checks the routing arguments; fills n_slots.
+static int check_route_args(int64_t tokens, int32_t top_k, int32_t n_experts, Shape* sh) {
+    if (tokens < 0) return fail(FT_ERR_ARG, "tokens must be >= 0 (got %lld)", (long long)tokens);
+    if (n_experts < 1 || n_experts > FT_MAX_EXPERTS)
+        return fail(FT_ERR_ARG, "n_experts must be in [1, %d] (got %d)", FT_MAX_EXPERTS, n_experts);
+    if (top_k < 1 || top_k > n_experts)
+        return fail(FT_ERR_ARG, "top_k must be in [1, n_experts=%d] (got %d)", n_experts, top_k);
+    int64_t s;
+    if (!mul_ok(tokens, top_k, &s) || s > INT32_MAX)
+        return fail(FT_ERR_SIZE, "tokens * top_k = %lld * %d must be < 2^31", (long long)tokens, top_k);
+    sh->tokens = tokens;
+    sh->top_k = top_k;
+    sh->n_experts = n_experts;
+    sh->n_slots = s;
+    return FT_OK;
+}
+
+static int check_matmul_args(int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols,
+                             Shape* sh) {
+    if (int st = check_route_args(tokens, top_k, n_experts, sh)) return st;
+    if (ncols <= 0 || ncols % 32 != 0)
+        return fail(FT_ERR_ARG, "ncols must be a positive multiple of 32 (got %lld)", (long long)ncols);
+    if (ncols > FT_MAX_NCOLS) return fail(FT_ERR_SIZE, "ncols must be <= %d (got %lld)", FT_MAX_NCOLS, (long long)ncols);
+    if (nrows <= 0) return fail(FT_ERR_ARG, "nrows must be > 0 (got %lld)", (long long)nrows);
+    int64_t en, wbytes, obytes;
+    if (!mul_ok(n_experts, nrows, &en) || en > INT32_MAX)
+        return fail(FT_ERR_SIZE, "n_experts * nrows must be < 2^31");
+    if (!mul_ok(en, (ncols / 32) * 18, &wbytes)) return fail(FT_ERR_SIZE, "weight size overflows int64");
+    if (!mul_ok(sh->n_slots, nrows, &obytes) || obytes > INT64_MAX / 4)
+        return fail(FT_ERR_SIZE, "output size overflows int64");
+    sh->nrows = nrows;
+    sh->ncols = ncols;
+    sh->nb = ncols / 32;
+    return FT_OK;
+}
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+static int get_stream_capturing(cudaStream_t s, bool* capturing) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    *capturing = cs != cudaStreamCaptureStatusNone;
+    return FT_OK;
+}
+
+// -------------------------------------------------------------- workspace
+// Per device: one cudaMalloc'ed block.  Layout (each part 256-byte aligned):
+//   err word | counts[E] | offsets[E+1] | perm[S] | tiles_gemv[E+1] |
+//   tiles_gemm[E+1] | hist[nchunks][E]
+struct WsLayout {
+    size_t err, counts, offsets, perm, tiles_gemv, tiles_gemm, hist, total;
+};
+
+static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static WsLayout ws_layout(int64_t n_slots, int32_t n_experts) {
+    WsLayout L{};
+    size_t o = 0;
+    L.err = o;
+    o = al256(o + 4);
+    L.counts = o;
+    o = al256(o + 4 * static_cast<size_t>(n_experts));
+    L.offsets = o;
+    o = al256(o + 4 * (static_cast<size_t>(n_experts) + 1));
+    L.perm = o;
+    o = al256(o + 4 * static_cast<size_t>(n_slots));
+    L.tiles_gemv = o;
+    o = al256(o + 4 * (static_cast<size_t>(n_experts) + 1));
+    L.tiles_gemm = o;
+    o = al256(o + 4 * (static_cast<size_t>(n_experts) + 1));
+    L.hist = o;
+    o = al256(o + 4 * static_cast<size_t>(route_chunks(n_slots)) * n_experts);
+    L.total = o;
+    return L;
+}
+
+struct DeviceWs {
+    void* base = nullptr;
+    size_t bytes = 0;
+};
+
+constexpr int kMaxDevices = 64;
+static DeviceWs g_ws[kMaxDevices];
+static std::mutex g_ws_mu;
+
+static int current_device(int* dev) {
+    const cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (*dev < 0 || *dev >= kMaxDevices) return fail(FT_ERR_CUDA, "device ordinal %d out of range", *dev);
+    return FT_OK;
+}
+
+// Ensures the current device's workspace holds `need` bytes; returns its base.
+static int ws_acquire(size_t need, cudaStream_t s, uint8_t** base) {
+    int dev;
+    if (int st = current_device(&dev)) return st;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    DeviceWs& w = g_ws[dev];
+    if (w.bytes < need) {
+        bool capturing = false;
+        if (int st = get_stream_capturing(s, &capturing)) return st;
+        if (capturing)
+            return fail(FT_ERR_WORKSPACE,
+                        "workspace of %zu bytes needed but %zu reserved, and the stream is being captured; call "
+                        "ft_moe_reserve before capture",
+                        need, w.bytes);
+        if (w.base) {
+            cudaError_t e = cudaDeviceSynchronize();
+            if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize before workspace growth");
+            cudaFree(w.base);
+            w.base = nullptr;
+            w.bytes = 0;
+        }
+        void* p = nullptr;
+        cudaError_t e = cudaMalloc(&p, need);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+        e = cudaMemset(p, 0, need);
+        if (e != cudaSuccess) {
+            cudaFree(p);
+            return cuda_fail(e, "cudaMemset(workspace)");
+        }
+        w.base = p;
+        w.bytes = need;
+    }
+    *base = static_cast<uint8_t*>(w.base);
+    return FT_OK;
+}
+
+// ------------------------------------------------------------------ paths
+static int g_path = -1;   // -1: not yet read from the environment
+static std::mutex g_path_mu;
+
+static int path_setting() {
+    std::lock_guard<std::mutex> lk(g_path_mu);
+    if (g_path < 0) {
+        g_path = FT_PATH_AUTO;
+        const char* v = std::getenv("FT_MOE_PATH");
+        if (v && std::strcmp(v, "gemv") == 0) g_path = FT_PATH_GEMV;
+        if (v && std::strcmp(v, "gemm") == 0) g_path = FT_PATH_GEMM;
+    }
+    return g_path;
+}
+
+static bool gemm_shape_ok(const Shape& sh) { return sh.ncols % 256 == 0; }
+
+// Host-side choice from the shape only (no device read): the tensor-core path
+// pays off once experts see enough slots to fill a 128-column MMA tile.
+static int choose_path(const Shape& sh, int setting) {
+    if (setting == FT_PATH_GEMV) return FT_PATH_GEMV;
+    if (setting == FT_PATH_GEMM) return FT_PATH_GEMM;
+    if (!gemm_shape_ok(sh)) return FT_PATH_GEMV;
+    const double mean = static_cast<double>(sh.n_slots) / sh.n_experts;
+    return mean >= 16.0 ? FT_PATH_GEMM : FT_PATH_GEMV;
+}
+
+static int run_matmul(const void* weights, const void* act, const int32_t* topk_ids, float* out, int32_t* dots,
+                      const Shape& sh, cudaStream_t s) {
+    const int path = choose_path(sh, path_setting());
+    if (path == FT_PATH_GEMM && !gemm_shape_ok(sh))
+        return fail(FT_ERR_ARG, "the tensor-core path needs ncols %% 256 == 0 (got %lld)", (long long)sh.ncols);
+    const WsLayout L = ws_layout(sh.n_slots, sh.n_experts);
+    uint8_t* ws = nullptr;
+    if (int st = ws_acquire(L.total, s, &ws)) return st;
+    RouteBuffers rb{};
+    rb.counts = reinterpret_cast<int32_t*>(ws + L.counts);
+    rb.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+    rb.perm = reinterpret_cast<int32_t*>(ws + L.perm);
+    rb.hist = reinterpret_cast<int32_t*>(ws + L.hist);
+    rb.tiles_gemv = reinterpret_cast<int32_t*>(ws + L.tiles_gemv);
+    rb.tiles_gemm = reinterpret_cast<int32_t*>(ws + L.tiles_gemm);
+    rb.err = reinterpret_cast<uint32_t*>(ws + L.err);
+
+    const GemvPlan gp = plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols);
+    if (path == FT_PATH_GEMV && gp.smem > 227 * 1024)
+        return fail(FT_ERR_SIZE, "GEMV tile needs %zu bytes of shared memory", gp.smem);
+    uint32_t* zero_rows = dots ? reinterpret_cast<uint32_t*>(dots) : reinterpret_cast<uint32_t*>(out);
+    const int64_t row_words = dots ? sh.nrows * sh.nb : sh.nrows;
+    prof_mark(kProfRouteBegin, s);
+    if (int st = launch_route(topk_ids, sh.n_slots, sh.n_experts, rb, gp.group, kGemmBN, zero_rows, row_words, s))
+        return st;
+    prof_mark(kProfMatmulBegin, s);
+    int st;
+    if (path == FT_PATH_GEMV)
+        st = launch_gemv(gp, static_cast<const uint8_t*>(weights), static_cast<const uint8_t*>(act), rb.perm,
+                         rb.offsets, rb.tiles_gemv, out, dots, rb.err, sh.n_slots, sh.top_k, sh.n_experts, sh.nrows,
+                         sh.ncols, s);
+    else
+        st = launch_gemm(static_cast<const uint8_t*>(weights), static_cast<const uint8_t*>(act), rb.perm,
+                         rb.offsets, rb.tiles_gemm, out, dots, rb.err, sh.n_slots, sh.top_k, sh.n_experts, sh.nrows,
+                         sh.ncols, sh.tokens, s);
+    prof_mark(kProfMatmulEnd, s);
+    return st;
+}
+
+}  // namespace ft
+
+using namespace ft;
+
+extern "C" {
+
+int ft_abi_version(void) { return FT_MOE_ABI_VERSION; }
+
+const char* ft_last_error(void) { return g_last_error.c_str(); }
+
+int ft_quantize_q8_1(const void* x_fp16, void* act_q8_1, int64_t tokens, int64_t ncols, void* stream) {
+    g_last_error.clear();
+    if (tokens < 0) return fail(FT_ERR_ARG, "tokens must be >= 0");
+    if (ncols <= 0 || ncols % 32 != 0) return fail(FT_ERR_ARG, "ncols must be a positive multiple of 32");
+    int64_t n;
+    if (!mul_ok(tokens, ncols, &n) || n > INT64_MAX / 4) return fail(FT_ERR_SIZE, "tokens * ncols overflows");
+    if (tokens == 0) return FT_OK;
+    if (!x_fp16 || !act_q8_1) return fail(FT_ERR_ARG, "null pointer");
+    if (!aligned(x_fp16, 8) || !aligned(act_q8_1, 4))
+        return fail(FT_ERR_ALIGN, "x_fp16 must be 8-byte and act_q8_1 4-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    prof_mark(kProfQuantBegin, s);
+    const int st = launch_quantize_q8_1(x_fp16, act_q8_1, tokens, ncols, s);
+    prof_mark(kProfQuantEnd, s);
+    return st;
+}
+
+int ft_moe_route_offsets(const int32_t* topk_ids, int64_t tokens, int32_t top_k, int32_t n_experts, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, uint32_t* dev_err, void* stream) {
+    g_last_error.clear();
+    Shape sh{};
+    if (int st = check_route_args(tokens, top_k, n_experts, &sh)) return st;
+    if (!counts || !offsets || (sh.n_slots > 0 && (!topk_ids || !perm))) return fail(FT_ERR_ARG, "null pointer");
+    if (!aligned(topk_ids, 4) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(perm, 4))
+        return fail(FT_ERR_ALIGN, "int32 arrays must be 4-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const WsLayout L = ws_layout(sh.n_slots, sh.n_experts);
+    uint8_t* ws = nullptr;
+    if (int st = ws_acquire(L.total, s, &ws)) return st;
+    RouteBuffers rb{};
+    rb.counts = counts;
+    rb.offsets = offsets;
+    rb.perm = perm;
+    rb.hist = reinterpret_cast<int32_t*>(ws + L.hist);
+    rb.tiles_gemv = nullptr;
+    rb.tiles_gemm = nullptr;
+    rb.err = dev_err ? dev_err : reinterpret_cast<uint32_t*>(ws + L.err);
+    return launch_route(topk_ids, sh.n_slots, sh.n_experts, rb, 1, 1, nullptr, 0, s);
+}
+
+static int matmul_entry(const void* weights, const void* act, const int32_t* topk_ids, float* out, int32_t* dots,
+                        int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols,
+                        void* stream) {
+    g_last_error.clear();
+    Shape sh{};
+    if (int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh)) return st;
+    if (sh.n_slots == 0) return FT_OK;
+    if (!weights || !act || !topk_ids || (!out && !dots)) return fail(FT_ERR_ARG, "null pointer");
+    if (!aligned(weights, 16) || !aligned(act, 16))
+        return fail(FT_ERR_ALIGN, "weights and act must be 16-byte aligned");
+    if (!aligned(topk_ids, 4) || !aligned(out, 4) || !aligned(dots, 4))
+        return fail(FT_ERR_ALIGN, "topk_ids / out / dots must be 4-byte aligned");
+    if (dots) {
+        int64_t n;
+        if (!mul_ok(sh.n_slots * sh.nrows, sh.nb, &n) || n > INT32_MAX)
+            return fail(FT_ERR_SIZE, "dots array would exceed 2^31 elements");
+    }
+    return run_matmul(weights, act, topk_ids, out, dots, sh, static_cast<cudaStream_t>(stream));
+}
+
+int ft_moe_q4_0_q8_1(const void* weights, const void* act, const int32_t* topk_ids, float* out, int64_t tokens,
+                     int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols, void* stream) {
+    if (!out) {
+        g_last_error.clear();
+        Shape sh{};
+        if (int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh)) return st;
+        if (sh.n_slots == 0) return FT_OK;
+        return fail(FT_ERR_ARG, "null pointer");
+    }
+    return matmul_entry(weights, act, topk_ids, out, nullptr, tokens, top_k, n_experts, nrows, ncols, stream);
+}
+
+int ft_moe_block_dots(const void* weights, const void* act, const int32_t* topk_ids, int32_t* dots, int64_t tokens,
+                      int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols, void* stream) {
+    if (!dots) {
+        g_last_error.clear();
+        Shape sh{};
+        if (int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh)) return st;
+        if (sh.n_slots == 0) return FT_OK;
+        return fail(FT_ERR_ARG, "null pointer");
+    }
+    return matmul_entry(weights, act, topk_ids, nullptr, dots, tokens, top_k, n_experts, nrows, ncols, stream);
+}
+
+size_t ft_moe_workspace_bytes(int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols) {
+    Shape sh{};
+    std::string keep = g_last_error;
+    const int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh);
+    g_last_error = keep;
+    if (st) return 0;
+    return ws_layout(sh.n_slots, sh.n_experts).total;
+}
+
+int ft_moe_reserve(int64_t max_tokens, int32_t max_top_k, int32_t n_experts, int64_t nrows, int64_t ncols) {
+    g_last_error.clear();
+    Shape sh{};
+    if (int st = check_matmul_args(max_tokens, max_top_k, n_experts, nrows, ncols, &sh)) return st;
+    uint8_t* base = nullptr;
+    return ws_acquire(ws_layout(sh.n_slots, sh.n_experts).total, nullptr, &base);
+}
+
+int ft_moe_release(void) {
+    g_last_error.clear();
+    int dev;
+    if (int st = current_device(&dev)) return st;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    DeviceWs& w = g_ws[dev];
+    if (w.base) {
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+        e = cudaFree(w.base);
+        w.base = nullptr;
+        w.bytes = 0;
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+    }
+    return FT_OK;
+}
+
+int ft_moe_read_device_error(void* stream, uint32_t* flags_out) {
+    g_last_error.clear();
+    if (!flags_out) return fail(FT_ERR_ARG, "null pointer");
+    *flags_out = 0;
+    int dev;
+    if (int st = current_device(&dev)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    DeviceWs& w = g_ws[dev];
+    if (!w.base) return FT_OK;
+    uint32_t v = 0;
+    e = cudaMemcpy(&v, w.base, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+    e = cudaMemset(w.base, 0, sizeof(v));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+    *flags_out = v;
+    return v ? fail(FT_ERR_DEVICE_FLAG, "device error flags 0x%x", v) : FT_OK;
+}
+
+int ft_profile_enable(int32_t max_calls) {
+    g_last_error.clear();
+    if (max_calls < 0) return fail(FT_ERR_ARG, "max_calls must be >= 0");
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    Prof& P = g_prof;
+    if (P.ev) {
+        for (int i = 0; i < P.max_calls * 5; ++i) cudaEventDestroy(P.ev[i]);
+        delete[] P.ev;
+        P.ev = nullptr;
+    }
+    P.on = false;
+    P.max_calls = 0;
+    P.n_quant = P.n_mm = 0;
+    P.quant_open = P.mm_open = false;
+    P.launches = 0;
+    if (max_calls == 0) return FT_OK;
+    P.ev = new cudaEvent_t[static_cast<size_t>(max_calls) * 5];
+    for (int i = 0; i < max_calls * 5; ++i) {
+        const cudaError_t e = cudaEventCreate(&P.ev[i]);
+        if (e != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(P.ev[j]);
+            delete[] P.ev;
+            P.ev = nullptr;
+            return cuda_fail(e, "cudaEventCreate");
+        }
+    }
+    P.max_calls = max_calls;
+    P.on = true;
+    return FT_OK;
+}
+
+int ft_profile_read(double* quantize_ms, double* route_ms, double* matmul_ms, int64_t* n_calls,
+                    int64_t* n_launches) {
+    g_last_error.clear();
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    Prof& P = g_prof;
+    double q = 0, r = 0, m = 0;
+    for (int i = 0; i < P.n_quant; ++i) {
+        float ms = 0;
+        cudaError_t e = cudaEventSynchronize(P.ev[i * 5 + 1]);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, P.ev[i * 5 + 0], P.ev[i * 5 + 1]);
+        if (e != cudaSuccess) return cuda_fail(e, "reading quantizer events");
+        q += ms;
+    }
+    for (int i = 0; i < P.n_mm; ++i) {
+        float a = 0, b = 0;
+        cudaError_t e = cudaEventSynchronize(P.ev[i * 5 + 4]);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&a, P.ev[i * 5 + 2], P.ev[i * 5 + 3]);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&b, P.ev[i * 5 + 3], P.ev[i * 5 + 4]);
+        if (e != cudaSuccess) return cuda_fail(e, "reading matmul events");
+        r += a;
+        m += b;
+    }
+    if (quantize_ms) *quantize_ms = q;
+    if (route_ms) *route_ms = r;
+    if (matmul_ms) *matmul_ms = m;
+    if (n_calls) *n_calls = P.n_mm;
+    if (n_launches) *n_launches = P.launches;
+    P.n_quant = P.n_mm = 0;
+    P.quant_open = P.mm_open = false;
+    P.launches = 0;
+    return FT_OK;
+}
+
+int ft_moe_set_path(int32_t path) {
+    if (path != FT_PATH_AUTO && path != FT_PATH_GEMV && path != FT_PATH_GEMM) return -1;
+    const int prev = path_setting();
+    std::lock_guard<std::mutex> lk(g_path_mu);
+    g_path = path;
+    return prev;
+}
+
+int ft_moe_selected_path(int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols) {
+    Shape sh{};
+    std::string keep = g_last_error;
+    const int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh);
+    g_last_error = keep;
+    if (st) return -1;
+    return choose_path(sh, path_setting());
+}
+
+}  // extern "C"

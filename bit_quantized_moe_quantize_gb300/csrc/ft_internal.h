@@ -1,0 +1,75 @@
+// Host-side internals shared by the translation units of libft_moe.so.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ft {
+
+// Status plus a message recorded for ft_last_error().
+int fail(int status, const char* fmt, ...);
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
+
+// Sets the dynamic shared-memory limit of a kernel once per device and size.
+int set_smem_limit(const void* kernel, int bytes);
+
+// Profiling hooks (no-ops unless ft_profile_enable is active).
+enum ProfPoint { kProfQuantBegin, kProfQuantEnd, kProfRouteBegin, kProfMatmulBegin, kProfMatmulEnd };
+void prof_mark(ProfPoint p, cudaStream_t s);
+void prof_count_launch();
+
+// Checks cudaGetLastError() after a launch; on failure records the kernel
+// name and geometry and returns FT_ERR_LAUNCH.
+int check_launch(const char* kernel, dim3 grid, dim3 block, size_t smem);
+
+// ------------------------------------------------------------ quantizer
+int launch_quantize_q8_1(const void* x, void* act, int64_t tokens, int64_t ncols, cudaStream_t s);
+
+// ---------------------------------------------------------------- router
+constexpr int kRouteChunk = 256;          // slots per warp-chunk
+constexpr int kRouteWarps = 8;            // warp-chunks per CTA
+
+struct RouteBuffers {
+    int32_t* counts;       // [E]
+    int32_t* offsets;      // [E+1]
+    int32_t* perm;         // [S]
+    int32_t* hist;         // [nchunks][E] scratch
+    int32_t* tiles_gemv;   // [E+1] or nullptr
+    int32_t* tiles_gemm;   // [E+1] or nullptr
+    uint32_t* err;
+};
+
+inline int64_t route_chunks(int64_t n_slots) { return (n_slots + kRouteChunk - 1) / kRouteChunk; }
+
+// Launches the three routing kernels.  When zero_rows != nullptr the rows of
+// slots with a bad expert id are zeroed there (row_words 4-byte words each).
+int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const RouteBuffers& b,
+                 int32_t gemv_group, int32_t gemm_group, uint32_t* zero_rows, int64_t row_words, cudaStream_t s);
+
+// ------------------------------------------------------------------ GEMV
+struct GemvPlan {
+    int group;          // slots per tile (1, 2, 4 or 8)
+    int rows;           // weight rows per CTA tile
+    int lanes_per_row;  // 8, 16 or 32
+    int64_t grid_x;     // tile upper bound
+    int64_t row_tiles;
+    size_t smem;
+};
+
+GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols);
+
+int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act, const int32_t* perm,
+                const int32_t* offsets, const int32_t* tiles, float* out, int32_t* dots, uint32_t* err,
+                int64_t n_slots, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols, cudaStream_t s);
+
+// ------------------------------------------------------------------ GEMM
+constexpr int kGemmBN = 128;   // slots per tile
+constexpr int kGemmBM = 128;   // weight rows per tile
+
+int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
+                const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
+                int32_t n_experts, int64_t nrows, int64_t ncols, int64_t tokens, cudaStream_t s);
+
+}  // namespace ft

@@ -1,0 +1,241 @@
+// Router: stable counting sort of the flat (token, top-k) slots by expert id.
+//
+// Produces counts[E], offsets[E+1] with a leading 0 (nvfp4-megamoe-kernel
+// CURRENT_BUG.md, Bug 4: the grouped GEMM takes expert_offsets[1:E+1]) and
+// the padding-free permutation perm[S]: perm[offsets[e] + r] is the r-th slot
+// of expert e in ascending slot order.  Positions in [offsets[e],
+// offsets[e+1]) belong to e, the searchsorted(right=True) map of Bug 2, so
+// empty experts own no position.  The same pass also writes, per matmul path,
+// the prefix over experts of the number of slot tiles (ceil(count / group)),
+// which lets the matmul kernels enumerate their tiles on the device.
+//
+// Three launches, always, whatever the data: no host read-back, no
+// allocation, nothing that depends on device values on the host side, so
+// the router can be captured in a CUDA graph (CURRENT_BUG.md, "Cudagraph
+// Constraints").  No atomics on global counters: each warp owns a chunk of
+// 256 slots and a private histogram row, so every result is deterministic.
+//
+//   1. route_hist:    per chunk, histogram of expert ids -> hist[chunk][e]
+//   2. route_scan:    one CTA: counts, offsets, tile prefixes, and hist
+//                     rewritten in place as each chunk's first position per e
+//   3. route_scatter: per chunk, stable placement with __match_any_sync ranks
+#include "ft_common.cuh"
+#include "ft_internal.h"
+
+namespace ft {
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__global__ void __launch_bounds__(32 * kRouteWarps)
+    route_hist_kernel(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts, int64_t n_chunks,
+                      int32_t* __restrict__ hist, uint32_t* err) {
+    extern __shared__ int32_t sh_hist[];
+    const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+    const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
+    if (chunk >= n_chunks) return;
+    int32_t* row = sh_hist + static_cast<int64_t>(warp) * n_experts;
+    for (int32_t e = lane; e < n_experts; e += 32) row[e] = 0;
+    __syncwarp();
+    bool saw_bad = false;
+    for (int step = 0; step < kRouteChunk / 32; ++step) {
+        const int64_t s = chunk * kRouteChunk + step * 32 + lane;
+        const int32_t e = s < n_slots ? ids[s] : -1;
+        const bool valid = s < n_slots && e >= 0 && e < n_experts;
+        saw_bad |= (s < n_slots) && !valid;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
+        if (valid && lane == static_cast<uint32_t>(__ffs(peers) - 1)) row[e] += __popc(peers);
+        __syncwarp();
+    }
+    if (__any_sync(0xFFFFFFFFu, saw_bad) && lane == 0) atomicOr(err, FT_DEVERR_BAD_EXPERT_ID);
+    int32_t* grow = hist + chunk * n_experts;
+    for (int32_t e = lane; e < n_experts; e += 32) grow[e] = row[e];
+}
+
+// Exclusive scan of v[0..n) in shared memory by the whole CTA (blockDim 1024);
+// returns the total.  scratch holds 32 ints.
+__device__ int32_t block_exclusive_scan(int32_t* v, int32_t n, int32_t* scratch) {
+    const int32_t tid = threadIdx.x, nt = blockDim.x;
+    const int32_t per = (n + nt - 1) / nt;
+    const int32_t lo = min(n, tid * per), hi = min(n, lo + per);
+    int32_t local = 0;
+    for (int32_t i = lo; i < hi; ++i) local += v[i];
+    // inclusive warp scan of the per-thread sums
+    const uint32_t lane = lane_id(), warp = tid >> 5;
+    int32_t inc = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= static_cast<uint32_t>(o)) inc += y;
+    }
+    if (lane == 31) scratch[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const int32_t nw = nt >> 5;
+        int32_t w = lane < static_cast<uint32_t>(nw) ? scratch[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+            if (lane >= static_cast<uint32_t>(o)) w += y;
+        }
+        if (lane < static_cast<uint32_t>(nw)) scratch[lane] = w;   // inclusive over warps
+    }
+    __syncthreads();
+    const int32_t total = scratch[(nt >> 5) - 1];
+    int32_t run = inc - local + (warp > 0 ? scratch[warp - 1] : 0);
+    for (int32_t i = lo; i < hi; ++i) {
+        const int32_t x = v[i];
+        v[i] = run;
+        run += x;
+    }
+    __syncthreads();
+    return total;
+}
+
+// One CTA of 1024 threads.  Shared: part[P][E] + tot[E] + tiles[E] + 32.
+__global__ void __launch_bounds__(1024)
+    route_scan_kernel(int32_t* __restrict__ hist, int64_t n_chunks, int32_t n_experts, int32_t* __restrict__ counts,
+                      int32_t* __restrict__ offsets, int32_t* __restrict__ tiles_gemv, int32_t gemv_group,
+                      int32_t* __restrict__ tiles_gemm, int32_t gemm_group) {
+    extern __shared__ int32_t sh[];
+    const int32_t E = n_experts, nt = blockDim.x, tid = threadIdx.x;
+    const int32_t P = E >= nt ? 1 : nt / E;                 // parts per expert
+    int32_t* part = sh;                                     // [P][E]
+    int32_t* tot = part + static_cast<int64_t>(P) * E;      // [E]
+    int32_t* tl = tot + E;                                  // [E]
+    int32_t* scratch = tl + E;                              // [32]
+    const int64_t per = (n_chunks + P - 1) / P;
+
+    // pass 1: partial sums over chunk ranges
+    for (int32_t idx = tid; idx < P * E; idx += nt) {
+        const int32_t e = idx % E, p = idx / E;
+        const int64_t c0 = p * per, c1 = min(n_chunks, c0 + per);
+        int32_t acc = 0;
+        for (int64_t c = c0; c < c1; ++c) acc += hist[c * E + e];
+        part[p * E + e] = acc;
+    }
+    __syncthreads();
+    // per expert: exclusive prefix over parts, and the total
+    for (int32_t e = tid; e < E; e += nt) {
+        int32_t run = 0;
+        for (int32_t p = 0; p < P; ++p) {
+            const int32_t x = part[p * E + e];
+            part[p * E + e] = run;
+            run += x;
+        }
+        tot[e] = run;
+        counts[e] = run;
+    }
+    __syncthreads();
+    // tile counts per path, before tot is overwritten by its scan
+    if (tiles_gemv)
+        for (int32_t e = tid; e < E; e += nt) tl[e] = (tot[e] + gemv_group - 1) / gemv_group;
+    __syncthreads();
+    if (tiles_gemv) {
+        const int32_t t = block_exclusive_scan(tl, E, scratch);
+        for (int32_t e = tid; e < E; e += nt) tiles_gemv[e] = tl[e];
+        if (tid == 0) tiles_gemv[E] = t;
+    }
+    __syncthreads();
+    if (tiles_gemm)
+        for (int32_t e = tid; e < E; e += nt) tl[e] = (tot[e] + gemm_group - 1) / gemm_group;
+    __syncthreads();
+    if (tiles_gemm) {
+        const int32_t t = block_exclusive_scan(tl, E, scratch);
+        for (int32_t e = tid; e < E; e += nt) tiles_gemm[e] = tl[e];
+        if (tid == 0) tiles_gemm[E] = t;
+    }
+    __syncthreads();
+    const int32_t total = block_exclusive_scan(tot, E, scratch);
+    for (int32_t e = tid; e < E; e += nt) offsets[e] = tot[e];
+    if (tid == 0) offsets[E] = total;
+    __syncthreads();
+    // pass 2: hist[c][e] := first position of chunk c's slots of expert e
+    for (int32_t idx = tid; idx < P * E; idx += nt) {
+        const int32_t e = idx % E, p = idx / E;
+        const int64_t c0 = p * per, c1 = min(n_chunks, c0 + per);
+        int32_t run = tot[e] + part[p * E + e];
+        for (int64_t c = c0; c < c1; ++c) {
+            const int32_t x = hist[c * E + e];
+            hist[c * E + e] = run;
+            run += x;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(32 * kRouteWarps)
+    route_scatter_kernel(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts, int64_t n_chunks,
+                         const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ perm, uint32_t* __restrict__ zero_rows, int64_t row_words) {
+    extern __shared__ int32_t sh_cursor[];
+    const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+    // tail of perm: positions past the valid slots are -1
+    {
+        const int64_t n_valid = offsets[n_experts];
+        const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+        for (int64_t p = n_valid + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; p < n_slots;
+             p += stride)
+            perm[p] = -1;
+    }
+    const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
+    if (chunk >= n_chunks) return;
+    int32_t* cur = sh_cursor + static_cast<int64_t>(warp) * n_experts;
+    const int32_t* brow = base + chunk * n_experts;
+    for (int32_t e = lane; e < n_experts; e += 32) cur[e] = brow[e];
+    __syncwarp();
+    for (int step = 0; step < kRouteChunk / 32; ++step) {
+        const int64_t s = chunk * kRouteChunk + step * 32 + lane;
+        const int32_t e = s < n_slots ? ids[s] : -1;
+        const bool valid = s < n_slots && e >= 0 && e < n_experts;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
+        int32_t pos = 0;
+        if (valid) pos = cur[e] + __popc(peers & lanemask_lt());
+        __syncwarp();
+        if (valid && lane == static_cast<uint32_t>(__ffs(peers) - 1)) cur[e] += __popc(peers);
+        if (valid) perm[pos] = static_cast<int32_t>(s);
+        if (!valid && s < n_slots && zero_rows != nullptr) {
+            uint32_t* row = zero_rows + s * row_words;
+            for (int64_t r = 0; r < row_words; ++r) row[r] = 0u;
+        }
+        __syncwarp();
+    }
+}
+
+int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const RouteBuffers& b,
+                 int32_t gemv_group, int32_t gemm_group, uint32_t* zero_rows, int64_t row_words, cudaStream_t s) {
+    {
+        const int big = 160 * 1024;
+        if (int st = set_smem_limit(reinterpret_cast<const void*>(route_hist_kernel), big)) return st;
+        if (int st = set_smem_limit(reinterpret_cast<const void*>(route_scan_kernel), big)) return st;
+        if (int st = set_smem_limit(reinterpret_cast<const void*>(route_scatter_kernel), big)) return st;
+    }
+    const int64_t n_chunks = route_chunks(n_slots);
+    const int64_t ctas = (n_chunks + kRouteWarps - 1) / kRouteWarps;
+    const dim3 block(32 * kRouteWarps);
+    const size_t sm_rows = static_cast<size_t>(kRouteWarps) * n_experts * sizeof(int32_t);
+    if (ctas > 0) {
+        const dim3 grid(static_cast<unsigned>(ctas));
+        route_hist_kernel<<<grid, block, sm_rows, s>>>(ids, n_slots, n_experts, n_chunks, b.hist, b.err);
+        if (int st = check_launch("route_hist_kernel", grid, block, sm_rows)) return st;
+    }
+    {
+        const int32_t P = n_experts >= 1024 ? 1 : 1024 / n_experts;
+        const size_t sm = (static_cast<size_t>(P) * n_experts + 2 * static_cast<size_t>(n_experts) + 32) *
+                          sizeof(int32_t);
+        route_scan_kernel<<<1, 1024, sm, s>>>(b.hist, n_chunks, n_experts, b.counts, b.offsets, b.tiles_gemv,
+                                              gemv_group, b.tiles_gemm, gemm_group);
+        if (int st = check_launch("route_scan_kernel", dim3(1), dim3(1024), sm)) return st;
+    }
+    if (ctas > 0) {
+        const dim3 grid(static_cast<unsigned>(ctas));
+        route_scatter_kernel<<<grid, block, sm_rows, s>>>(ids, n_slots, n_experts, n_chunks, b.hist, b.offsets,
+                                                          b.perm, zero_rows, row_words);
+        if (int st = check_launch("route_scatter_kernel", grid, block, sm_rows)) return st;
+    }
+    return FT_OK;
+}
+
+}  // namespace ft

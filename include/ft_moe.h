@@ -1,0 +1,233 @@
+/*
+ * ft_moe.h - C ABI of the GB300 (sm_103a) routed Q4_0 x Q8_1 MoE expert matmul.
+ *
+ * What it computes.  For every flat (token, top-k) slot s = t * top_k + j of a
+ * batch, with expert e = topk_ids[s], and every weight row r of that expert:
+ *
+ *     out[s][r] = sum_b  d_w[e][r][b] * d_a[t][b] * sum_{i<32} (q_w[e][r][b][i] - 8) * q_a[t][b][i]
+ *
+ * the dot product of the routed expert's Q4_0 weight rows with the token's
+ * Q8_1 activation (moe_vec_q4_0_q8_1 over the flat (token, top-k) index:
+ * FreeToken PR #185, "launch GGUF MoE GEMV token axis on grid.x, not grid.z",
+ * sections "Problem" and "Fix"), in both the per-slot GEMV form and the
+ * expert-grouped GEMM form keyed by expert_offsets with a leading 0
+ * (nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 4).  The per-block integer dots
+ * are exact; the scale products are accumulated in fp32.
+ *
+ * Formats (GGUF blocks of 32 values, little-endian):
+ *   Q4_0, 18 bytes: fp16 d, then 16 bytes qs; value j < 16 is the low nibble
+ *         of qs[j], value j + 16 its high nibble; weight = (q - 8) * d.
+ *   Q8_1, 36 bytes: fp16 d, fp16 s, then 32 int8 q; activation = q * d and
+ *         s = d * sum(q) (stored for format fidelity; the dot does not use it).
+ *
+ * Layouts (all row-major, contiguous):
+ *   weights  [n_experts][nrows][ncols/32] Q4_0 blocks (18 B each)
+ *   act      [tokens][ncols/32] Q8_1 blocks (36 B each)
+ *   topk_ids [tokens][top_k] int32
+ *   out      [tokens][top_k][nrows] fp32
+ *
+ * Conventions shared by every entry point.
+ *   - Pointers are DEVICE pointers on the current CUDA device unless stated.
+ *     The caller owns every buffer it passes; the library owns only its
+ *     workspace (see ft_moe_reserve).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All work is stream-ordered; no entry point below synchronizes
+ *     except ft_moe_read_device_error and ft_moe_release.
+ *   - Every size product is computed in 64-bit; no launch places the slot or
+ *     token count on grid.y or grid.z, so tokens * top_k is not capped at
+ *     65535 (FreeToken PR #185, "Problem"; mlxcel PR #652, "Summary").
+ *   - Argument errors are reported before anything is launched.  After every
+ *     kernel launch the library checks the launch status and, on failure,
+ *     returns FT_ERR_LAUNCH with the kernel name and grid in ft_last_error()
+ *     (FreeToken PR #185: FT_MOE_VEC_LAUNCH_CHECK, "Fix").
+ *   - Expert ids outside [0, n_experts) never fault: the slot is left out of
+ *     the routing, its output row is zeroed and FT_DEVERR_BAD_EXPERT_ID is
+ *     raised in the device error word.
+ *   - Route + matmul issue a fixed number of launches, allocate nothing once
+ *     the workspace is reserved and read nothing back to the host, so they can
+ *     be captured in a CUDA graph (nvfp4-megamoe-kernel CURRENT_BUG.md,
+ *     "Cudagraph Constraints").
+ */
+#ifndef FT_MOE_H
+#define FT_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FT_MOE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define FT_API __attribute__((visibility("default")))
+#else
+#define FT_API
+#endif
+
+typedef enum {
+    FT_OK = 0,
+    FT_ERR_ARG = 1,          /* null pointer, bad count, bad top_k, ncols % 32 != 0 ...   */
+    FT_ERR_SIZE = 2,         /* a size product overflows, or exceeds a documented limit */
+    FT_ERR_ALIGN = 3,        /* a pointer misses its required alignment                 */
+    FT_ERR_LAUNCH = 4,       /* a kernel launch was rejected; see ft_last_error()       */
+    FT_ERR_WORKSPACE = 5,    /* workspace too small while the stream is being captured  */
+    FT_ERR_CUDA = 6,         /* a CUDA runtime call failed; see ft_last_error()         */
+    FT_ERR_DEVICE_FLAG = 7   /* ft_moe_read_device_error found a raised device flag     */
+} ft_status;
+
+/* Bits of the device error word. */
+#define FT_DEVERR_BAD_EXPERT_ID 0x1u   /* a topk id was outside [0, n_experts)           */
+#define FT_DEVERR_WAIT_TIMEOUT  0x2u   /* a bounded in-kernel wait gave up (never expected) */
+
+/* Path selection for ft_moe_q4_0_q8_1 (ft_moe_set_path). */
+#define FT_PATH_AUTO 0   /* chosen on the host from tokens*top_k, n_experts and the shape */
+#define FT_PATH_GEMV 1   /* per-slot GEMV on CUDA cores                                  */
+#define FT_PATH_GEMM 2   /* expert-grouped GEMM on the tcgen05 tensor cores              */
+
+/* Documented limits. */
+#define FT_MAX_EXPERTS 4096
+#define FT_MAX_NCOLS   65536
+
+/*
+ * ft_quantize_q8_1 - fp16 activations -> Q8_1 blocks (quantize_row_q8_1 on
+ * FreeToken PR #185, "Fix").  Per 32-block of a row, in IEEE fp32 with
+ * round-to-nearest: amax = max |x|, d = amax / 127, q = round-half-away(x / d)
+ * (0 when amax == 0), s = d * sum(q); d and s stored as fp16 (round to
+ * nearest even).  The result is bit-identical to the CPU oracle.
+ *
+ *   x_fp16    device, [tokens][ncols] fp16, 4-byte aligned
+ *   act_q8_1  device, [tokens][ncols/32] Q8_1 (36 B each), 4-byte aligned
+ *   tokens    >= 0 (0 is a no-op); ncols > 0, ncols % 32 == 0
+ * Errors: FT_ERR_ARG, FT_ERR_SIZE, FT_ERR_ALIGN, FT_ERR_LAUNCH.
+ */
+FT_API int ft_quantize_q8_1(const void* x_fp16, void* act_q8_1, int64_t tokens, int64_t ncols,
+                     void* stream);
+
+/*
+ * ft_moe_route_offsets - stable counting sort of the tokens*top_k slots by
+ * expert id (the expert_offsets of nvfp4-megamoe-kernel CURRENT_BUG.md,
+ * Bug 4, with the searchsorted(right=True) slot-to-expert map of Bug 2).
+ *
+ *   topk_ids  device, [tokens][top_k] int32
+ *   counts    device, [n_experts] int32 out: slots routed to each expert
+ *   offsets   device, [n_experts + 1] int32 out: offsets[0] = 0,
+ *             offsets[e+1] = offsets[e] + counts[e]; offsets[n_experts] is the
+ *             number of slots with a valid id
+ *   perm      device, [tokens*top_k] int32 out: perm[offsets[e] + r] is the
+ *             r-th slot (ascending slot order) routed to e; entries at and past
+ *             offsets[n_experts] are -1.  Unique, hence bit-comparable.
+ *   dev_err   device uint32 or NULL; bad ids OR FT_DEVERR_BAD_EXPERT_ID into
+ *             it (NULL: the library's own word, read by ft_moe_read_device_error)
+ * Needs 1 <= top_k <= n_experts <= FT_MAX_EXPERTS and tokens*top_k < 2^31.
+ * Uses the library workspace (reserved or grown on demand outside capture).
+ * Errors: FT_ERR_ARG, FT_ERR_SIZE, FT_ERR_WORKSPACE, FT_ERR_CUDA, FT_ERR_LAUNCH.
+ */
+FT_API int ft_moe_route_offsets(const int32_t* topk_ids, int64_t tokens, int32_t top_k,
+                         int32_t n_experts, int32_t* counts, int32_t* offsets, int32_t* perm,
+                         uint32_t* dev_err, void* stream);
+
+/*
+ * ft_moe_q4_0_q8_1 - the routed expert matmul defined at the top of this file.
+ * Routes internally (into the workspace), then runs the GEMV or the grouped
+ * GEMM path (FT_PATH_AUTO decides on the host, without reading the device).
+ *
+ *   weights   device, Q4_0 [n_experts][nrows][ncols/32]; 16-byte aligned
+ *   act       device, Q8_1 [tokens][ncols/32] (from ft_quantize_q8_1); 16-byte aligned
+ *   topk_ids  device, int32 [tokens][top_k]
+ *   out       device, fp32 [tokens][top_k][nrows]; every element is written
+ *             (rows of slots with a bad expert id are written as 0)
+ * Needs ncols % 32 == 0, 0 < ncols <= FT_MAX_NCOLS, nrows > 0,
+ * 1 <= top_k <= n_experts <= FT_MAX_EXPERTS, tokens*top_k < 2^31.
+ * The tensor-core path additionally needs ncols % 256 == 0; other shapes take
+ * the GEMV path (a forced FT_PATH_GEMM on such a shape returns FT_ERR_ARG).
+ * Errors: FT_ERR_ARG, FT_ERR_SIZE, FT_ERR_ALIGN, FT_ERR_WORKSPACE, FT_ERR_CUDA,
+ * FT_ERR_LAUNCH.
+ */
+FT_API int ft_moe_q4_0_q8_1(const void* weights, const void* act, const int32_t* topk_ids, float* out,
+                     int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows,
+                     int64_t ncols, void* stream);
+
+/*
+ * ft_moe_workspace_bytes - bytes of library workspace that one
+ * ft_moe_q4_0_q8_1 / ft_moe_route_offsets call of this shape needs.
+ * Returns 0 for invalid arguments.
+ */
+FT_API size_t ft_moe_workspace_bytes(int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows,
+                              int64_t ncols);
+
+/*
+ * ft_moe_reserve - allocate (cudaMalloc) the workspace of the current device
+ * for shapes up to these maxima.  Call it before capturing a stream; inside a
+ * capture the library never allocates and returns FT_ERR_WORKSPACE instead.
+ * Outside capture a call that needs more grows the workspace by itself
+ * (cudaFree + cudaMalloc, which synchronize the device).
+ * Errors: FT_ERR_ARG, FT_ERR_SIZE, FT_ERR_CUDA.
+ */
+FT_API int ft_moe_reserve(int64_t max_tokens, int32_t max_top_k, int32_t n_experts, int64_t nrows,
+                   int64_t ncols);
+
+/* ft_moe_release - free the current device's workspace (synchronizes). */
+FT_API int ft_moe_release(void);
+
+/*
+ * ft_moe_read_device_error - synchronize `stream`, read the library's device
+ * error word of the current device into *flags_out and clear it.  Returns
+ * FT_OK when no flag was raised, FT_ERR_DEVICE_FLAG otherwise.  Not for use
+ * inside a stream capture.
+ */
+FT_API int ft_moe_read_device_error(void* stream, uint32_t* flags_out);
+
+/*
+ * ft_moe_set_path - force the path of later ft_moe_q4_0_q8_1 calls in this
+ * process (FT_PATH_AUTO / FT_PATH_GEMV / FT_PATH_GEMM); returns the previous
+ * setting, or -1 for an unknown value.  The environment variable FT_MOE_PATH
+ * (auto|gemv|gemm) sets the initial value.
+ */
+FT_API int ft_moe_set_path(int32_t path);
+
+/* ft_moe_selected_path - the path ft_moe_q4_0_q8_1 would take for this shape
+ * under the current setting (FT_PATH_GEMV or FT_PATH_GEMM), or -1. */
+FT_API int ft_moe_selected_path(int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows,
+                         int64_t ncols);
+
+/*
+ * ft_moe_block_dots - diagnostic: run the selected path in a mode that writes
+ * every per-block integer dot instead of the scaled sum:
+ *   dots  device, int32 [tokens*top_k][nrows][ncols/32]
+ *         dots[s][r][b] = sum_i (q_w[e][r][b][i] - 8) * q_a[t][b][i]
+ *         (0 for slots with a bad id).
+ * Same arguments and errors as ft_moe_q4_0_q8_1, plus FT_ERR_SIZE when the
+ * dots array would exceed 2^31 elements.  For tests on small shapes.
+ */
+FT_API int ft_moe_block_dots(const void* weights, const void* act, const int32_t* topk_ids,
+                      int32_t* dots, int64_t tokens, int32_t top_k, int32_t n_experts,
+                      int64_t nrows, int64_t ncols, void* stream);
+
+/*
+ * Profiling.  ft_profile_enable(max_calls) starts recording, on the stream
+ * each call launches on, CUDA events around the quantizer kernel and around
+ * the routing and matmul kernels of each later call (up to max_calls calls;
+ * 0 stops recording).  It allocates the events, so call it outside stream
+ * capture.  ft_profile_read synchronizes on the recorded events and returns
+ * the summed kernel times (milliseconds), the number of calls recorded and the
+ * number of kernels this library launched since recording started, then
+ * resets the totals.  Per-process state, meant for benchmarks.
+ */
+FT_API int ft_profile_enable(int32_t max_calls);
+FT_API int ft_profile_read(double* quantize_ms, double* route_ms, double* matmul_ms, int64_t* n_calls,
+                           int64_t* n_launches);
+
+/* ft_last_error - message of the last failing call on this host thread
+ * (empty string if none).  The pointer stays valid until the next call on the
+ * same thread. */
+FT_API const char* ft_last_error(void);
+
+/* ft_abi_version - FT_MOE_ABI_VERSION of the loaded library. */
+FT_API int ft_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FT_MOE_H */

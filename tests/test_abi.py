@@ -1,0 +1,141 @@
+"""The C-ABI library loads on a host without a GPU, exports every symbol
+include/ft_moe.h declares, and rejects bad arguments on the host before any
+CUDA call (CPU only: nothing here launches a kernel)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_quantized_moe_quantize_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "ft_moe.h")).read()
+    return re.findall(r"FT_API\s+[\w\s\*]+?\b(ft_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(header_functions())
+    for required in ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1"):
+        assert required in names
+
+
+def test_exports_every_declared_symbol(lib):
+    from bit_quantized_moe_quantize_gb300 import _lib
+    names = header_functions()
+    assert names
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(_lib.EXPORTS)
+
+
+def test_library_is_native_and_current(lib):
+    from bit_quantized_moe_quantize_gb300 import build
+    assert build.is_current()
+    assert lib.ft_abi_version() == 1
+    with open(build.LIB, "rb") as f:
+        assert f.read(4) == b"\x7fELF"
+
+
+def test_no_load_time_cuda_dependency():
+    """The library links the CUDA runtime statically and reaches the driver
+    lazily, so it loads on machines without a GPU driver."""
+    from bit_quantized_moe_quantize_gb300 import build
+    ctypes.CDLL(build.LIB)   # would raise if libcuda.so.1 were a load-time need
+
+
+def _err(lib):
+    return lib.ft_last_error().decode()
+
+
+def test_quantize_rejects_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    assert lib.ft_quantize_q8_1(vp(0), vp(0), -1, 32, vp(0)) == 1
+    assert lib.ft_quantize_q8_1(vp(0), vp(0), 4, 33, vp(0)) == 1
+    assert "multiple of 32" in _err(lib)
+    assert lib.ft_quantize_q8_1(vp(0), vp(0), 4, 0, vp(0)) == 1
+    assert lib.ft_quantize_q8_1(vp(0), vp(0), 0, 64, vp(0)) == 0          # empty batch: no-op
+    assert lib.ft_quantize_q8_1(vp(0), vp(0), 4, 64, vp(0)) == 1          # null pointers
+    assert lib.ft_quantize_q8_1(vp(0x1002), vp(0x2000), 4, 64, vp(0)) == 3   # misaligned x
+    assert lib.ft_quantize_q8_1(vp(0), vp(0), 1 << 62, 64, vp(0)) == 2    # size overflow
+
+
+def test_route_rejects_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    f = lib.ft_moe_route_offsets
+    assert f(vp(0), 4, 0, 8, vp(0), vp(0), vp(0), vp(0), vp(0)) == 1      # top_k 0
+    assert f(vp(0), 4, 9, 8, vp(0), vp(0), vp(0), vp(0), vp(0)) == 1      # top_k > E
+    assert f(vp(0), 4, 2, 0, vp(0), vp(0), vp(0), vp(0), vp(0)) == 1      # no experts
+    assert f(vp(0), 4, 2, 5000, vp(0), vp(0), vp(0), vp(0), vp(0)) == 1   # > FT_MAX_EXPERTS
+    assert f(vp(0), 1 << 30, 8, 8, vp(0), vp(0), vp(0), vp(0), vp(0)) == 2   # slots >= 2^31
+    assert "2^31" in _err(lib)
+    assert f(vp(0), 4, 2, 8, vp(0), vp(0), vp(0), vp(0), vp(0)) == 1      # null pointers
+    assert f(vp(0x1001), 4, 2, 8, vp(0x2000), vp(0x3000), vp(0x4000), vp(0), vp(0)) == 3
+
+
+def test_matmul_rejects_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    f = lib.ft_moe_q4_0_q8_1
+    W, A, I, O = vp(0x10000), vp(0x20000), vp(0x30000), vp(0x40000)
+    assert f(W, A, I, O, 4, 2, 8, 128, 100, vp(0)) == 1        # ncols % 32
+    assert f(W, A, I, O, 4, 2, 8, 0, 256, vp(0)) == 1          # nrows
+    assert f(W, A, I, O, 4, 2, 8, 128, 1 << 20, vp(0)) == 2    # ncols over the limit
+    assert f(W, A, I, O, 4, 2, 4096, 1 << 20, 256, vp(0)) == 2  # E*N >= 2^31
+    assert f(W, A, I, O, 0, 2, 8, 128, 256, vp(0)) == 0        # no slots: no-op
+    assert f(vp(0), A, I, O, 4, 2, 8, 128, 256, vp(0)) == 1    # null weights
+    assert f(W, A, I, vp(0), 4, 2, 8, 128, 256, vp(0)) == 1    # null out
+    assert f(vp(0x10008), A, I, O, 4, 2, 8, 128, 256, vp(0)) == 3   # weights not 16-byte aligned
+    assert f(W, A, vp(0x30002), O, 4, 2, 8, 128, 256, vp(0)) == 3   # ids misaligned
+    d = lib.ft_moe_block_dots
+    assert d(W, A, I, vp(0), 4, 2, 8, 128, 256, vp(0)) == 1
+    assert d(W, A, I, O, 1 << 20, 8, 8, 4096, 4096, vp(0)) == 2     # dots > 2^31 elements
+
+
+def test_workspace_and_path_selection(lib):
+    ws = lib.ft_moe_workspace_bytes
+    small = ws(16, 2, 8, 128, 256)
+    big = ws(8192, 8, 128, 1408, 2816)
+    assert 0 < small < big
+    assert big >= 8192 * 8 * 4              # holds the permutation
+    assert ws(16, 2, 8, 128, 100) == 0      # invalid shape
+    prev = lib.ft_moe_set_path(0)
+    try:
+        sel = lib.ft_moe_selected_path
+        assert sel(1, 8, 128, 768, 2048) == 1            # decode: GEMV
+        assert sel(8191, 8, 128, 1408, 2816) == 2        # prefill: tensor cores
+        assert sel(8191, 8, 128, 1408, 2816 + 32) == 1   # ncols % 256 != 0: GEMV only
+        assert lib.ft_moe_set_path(2) == 0
+        assert sel(1, 8, 128, 768, 2048) == 2
+        assert lib.ft_moe_set_path(7) == -1
+        assert sel(1, 8, 128, 768, 100) == -1
+    finally:
+        lib.ft_moe_set_path(prev if prev >= 0 else 0)
+
+
+def test_last_error_is_per_call(lib):
+    vp = ctypes.c_void_p
+    assert lib.ft_quantize_q8_1(vp(0), vp(0), 4, 33, vp(0)) == 1
+    assert _err(lib)
+    assert lib.ft_quantize_q8_1(vp(0), vp(0), 0, 64, vp(0)) == 0
+    assert _err(lib) == ""
+
+
+def test_product_path_never_imports_the_oracle():
+    """The CUDA binding and the benchmark's GPU leg must not reach the oracle."""
+    pkg = os.path.join(ROOT, "bit_quantized_moe_quantize_gb300")
+    for fn in os.listdir(pkg):
+        if fn.endswith(".py"):
+            src = open(os.path.join(pkg, fn)).read()
+            assert "import oracle" not in src and "from oracle" not in src, fn
+    for fn in os.listdir(os.path.join(pkg, "csrc")):
+        src = open(os.path.join(pkg, "csrc", fn)).read()
+        assert "ft_oracle" not in src and "oracle_" not in src, fn

@@ -83,14 +83,35 @@ def workload(spec):
     return name, wl, T
 
 
-def make_inputs(wl, T, rank):
+def replica_workload(wl, rank):
+    """Rank r's replica: the same expert weights, its own batch of tokens."""
     from bit_quantized_moe_quantize_gb300 import synth
-    w = synth.make_weights(wl)
-    # each replica gets its own batch (same weights, different tokens)
-    wl_r = synth.Workload(**{**wl.__dict__, "seed": wl.seed + 7919 * rank}) if rank else wl
+    return synth.Workload(**{**wl.__dict__, "seed": wl.seed + 7919 * rank}) if rank else wl
+
+
+def make_inputs(wl, T, rank, with_weights=True):
+    from bit_quantized_moe_quantize_gb300 import synth
+    w = synth.make_weights(wl) if with_weights else None
+    wl_r = replica_workload(wl, rank)
     x = synth.make_activations(wl_r, T)
     ids = synth.make_topk_ids(wl_r, T)
     return w, x, ids
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank scalar over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job routed tokens/s: every rank's tokens over the slowest rank's step time."""
+    return tokens_per_rank * world / (ms_max / 1000.0)
 
 
 # ------------------------------------------------------------------ clocks
@@ -290,12 +311,8 @@ def ours(args):
     prof = ft.profile_read()
     ft.profile_enable(0)
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = T * world / (ms / 1000.0)
+    ms = max_over_ranks(statistics.mean(step_ms), dev)
+    value = job_throughput(T, world, ms)
 
     # e2e through the public API: pinned host input -> device -> result -> pinned host
     e2e = None
@@ -317,12 +334,8 @@ def ours(args):
             if j >= 0:
                 e_ev[j][1].record(stream)
         torch.cuda.synchronize()
-        e_ms = statistics.mean(a.elapsed_time(b) for a, b in e_ev)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": T * world / (e_ms / 1000.0), "unit": UNIT, "ms_per_step": e_ms,
+        e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e_ev), dev)
+        e2e = {"value": job_throughput(T, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": int(x.nbytes + ids.nbytes), "d2h_bytes_per_step": int(S * N * 4)}
         assert np.array_equal(ho.numpy(), out.cpu().numpy())
     if ft.read_device_error():

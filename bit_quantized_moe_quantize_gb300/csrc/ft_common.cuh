@@ -79,6 +79,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     }
 }
 
+// Warp-uniform bounded wait: every lane polls, and the warp fails together if
+// any lane gave up, so warp-collective instructions that follow never see a
+// diverged warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err) {
+    const bool ok = mbar_wait(bar, parity, err);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // ------------------------------------------------------------ async copies
 // 1-D bulk copy global -> shared, completion counted on an mbarrier.
 // dst, src 16-byte aligned; bytes a multiple of 16.

@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             const int32_t wy = static_cast<int32_t>(static_cast<int64_t>(ti.e) * a.nrows + ti.m0);
             for (int32_t ks = 0; ks < n_stages; ++ks, ++it) {
                 const uint32_t s = it % RAW_STAGES;
-                if (!mbar_wait(&raw_empty[s], ((it / RAW_STAGES) & 1u) ^ 1u, a.err)) { ok = false; break; }
+                if (!mbar_wait_warp(&raw_empty[s], ((it / RAW_STAGES) & 1u) ^ 1u, a.err)) { ok = false; break; }
                 uint8_t* wraw = smem + OFF_RAW + s * RAW_STAGE_BYTES;
                 uint8_t* araw = wraw + W_RAW_BYTES;
                 if (lane == 0) {
@@ -343,8 +343,8 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             const int64_t row = ti.m0 + row_l;
             for (int32_t b = 0; b < nb; ++b, ++bc) {
                 const uint32_t ab = bc % NACC, sc = bc % NSC;
-                if (!mbar_wait(&acc_full[ab], (bc / NACC) & 1u, a.err)) { ok = false; break; }
-                if (!mbar_wait(&sc_full[sc], (bc / NSC) & 1u, a.err)) { ok = false; break; }
+                if (!mbar_wait_warp(&acc_full[ab], (bc / NACC) & 1u, a.err)) { ok = false; break; }
+                if (!mbar_wait_warp(&sc_full[sc], (bc / NSC) & 1u, a.err)) { ok = false; break; }
                 tc_fence_after();
                 const float* dws = reinterpret_cast<const float*>(smem + OFF_SC + sc * SC_BYTES);
                 const float* das = dws + BM + colh * 64;

@@ -27,7 +27,7 @@ PATHS = {"auto": FT_PATH_AUTO, "gemv": FT_PATH_GEMV, "gemm": FT_PATH_GEMM}
 EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_moe_workspace_bytes",
            "ft_moe_reserve", "ft_moe_release", "ft_moe_read_device_error", "ft_moe_set_path",
            "ft_moe_selected_path", "ft_moe_block_dots", "ft_last_error", "ft_abi_version", "ft_profile_enable",
-           "ft_profile_read")
+           "ft_profile_read", "ft_moe_route_offsets_noalloc")
 
 
 class FtError(RuntimeError):
@@ -56,6 +56,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         i64, i32, vp, u32p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)
         L.ft_quantize_q8_1.argtypes = [vp, vp, i64, i64, vp]
         L.ft_moe_route_offsets.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp]
+        L.ft_moe_route_offsets_noalloc.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp]
         L.ft_moe_q4_0_q8_1.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_moe_block_dots.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_moe_workspace_bytes.argtypes = [i64, i32, i32, i64, i64]

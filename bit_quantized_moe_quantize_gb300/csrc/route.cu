@@ -19,6 +19,8 @@
 //   2. route_scan:    one CTA: counts, offsets, tile prefixes, and hist
 //                     rewritten in place as each chunk's first position per e
 //   3. route_scatter: per chunk, stable placement with __match_any_sync ranks
+#include <mutex>
+
 #include "ft_common.cuh"
 #include "ft_internal.h"
 
@@ -238,4 +240,74 @@ int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const R
     return FT_OK;
 }
 
+// --------------------------------------------------- allocation-free router
+// For callers that must not allocate device memory (see
+// ft_moe_route_offsets_noalloc in ft_moe.h): the histogram scratch is this
+// fixed array, plus one word that receives bad-id flags when the caller
+// passes no error word.  Host code must not use the array's name as a
+// pointer - on the host it is only a stand-in for the symbol - so its device
+// address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) int32_t g_route_noalloc_scratch[FT_ROUTE_NOALLOC_SCRATCH_WORDS + 64];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set-up on the
+// first call per device).
+int noalloc_scratch(int32_t** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(FT_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(FT_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_route_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return fail(FT_ERR_CUDA, "cudaGetSymbolAddress(route scratch): %s", cudaGetErrorString(e));
+        g_noalloc_addr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_noalloc_addr[dev];
+    return FT_OK;
+}
+}  // namespace
+
 }  // namespace ft
+
+extern "C" int ft_moe_route_offsets_noalloc(const int32_t* topk_ids, int64_t tokens, int32_t top_k,
+                                            int32_t n_experts, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                            uint32_t* dev_err, void* stream) {
+    using namespace ft;
+    if (tokens < 0) return fail(FT_ERR_ARG, "tokens must be >= 0 (got %lld)", (long long)tokens);
+    if (n_experts < 1 || n_experts > FT_MAX_EXPERTS)
+        return fail(FT_ERR_ARG, "n_experts must be in [1, %d] (got %d)", FT_MAX_EXPERTS, n_experts);
+    if (top_k < 1 || top_k > n_experts)
+        return fail(FT_ERR_ARG, "top_k must be in [1, n_experts=%d] (got %d)", n_experts, top_k);
+    if (tokens > INT32_MAX / top_k)
+        return fail(FT_ERR_SIZE, "tokens * top_k = %lld * %d must be < 2^31", (long long)tokens, top_k);
+    const int64_t n_slots = tokens * top_k;
+    const int64_t words = route_chunks(n_slots) * static_cast<int64_t>(n_experts);
+    if (words > FT_ROUTE_NOALLOC_SCRATCH_WORDS)
+        return fail(FT_ERR_SIZE,
+                    "ft_moe_route_offsets_noalloc: %lld slots and %d experts need %lld scratch words, more than the "
+                    "%d built into the library; use ft_moe_route_offsets",
+                    (long long)n_slots, n_experts, (long long)words, FT_ROUTE_NOALLOC_SCRATCH_WORDS);
+    if (!counts || !offsets || (n_slots > 0 && (!topk_ids || !perm))) return fail(FT_ERR_ARG, "null pointer");
+    if ((reinterpret_cast<uintptr_t>(topk_ids) | reinterpret_cast<uintptr_t>(counts) |
+         reinterpret_cast<uintptr_t>(offsets) | reinterpret_cast<uintptr_t>(perm)) & 3u)
+        return fail(FT_ERR_ALIGN, "int32 arrays must be 4-byte aligned");
+    int32_t* scratch = nullptr;
+    if (int st = noalloc_scratch(&scratch)) return st;
+    RouteBuffers rb{};
+    rb.counts = counts;
+    rb.offsets = offsets;
+    rb.perm = perm;
+    rb.hist = scratch;
+    rb.tiles_gemv = nullptr;
+    rb.tiles_gemm = nullptr;
+    rb.err = dev_err ? dev_err : reinterpret_cast<uint32_t*>(scratch + FT_ROUTE_NOALLOC_SCRATCH_WORDS);
+    return launch_route(topk_ids, n_slots, n_experts, rb, 1, 1, nullptr, 0, static_cast<cudaStream_t>(stream));
+}
+

@@ -129,6 +129,34 @@ FT_API int ft_moe_route_offsets(const int32_t* topk_ids, int64_t tokens, int32_t
                          uint32_t* dev_err, void* stream);
 
 /*
+ * ft_moe_route_offsets_noalloc - the same routing as ft_moe_route_offsets,
+ * for callers that are not allowed to allocate device memory: a runtime
+ * whose memory planner owns every byte of the GPU after start-up, a plugin
+ * running inside another framework's allocator, or a latency-critical loop
+ * that cannot afford cudaMalloc's implicit device synchronization.  This
+ * entry point has no counterpart on the pages; it exists only for them.
+ *
+ * Nothing is allocated, by this call or any earlier one: the per-chunk
+ * histogram scratch lives in one fixed array of FT_ROUTE_NOALLOC_SCRATCH_WORDS
+ * int32 (1 MiB) compiled into the library, which every GPU that loads the
+ * library holds until the process exits.  The scratch needs
+ * ceil(tokens*top_k / 256) * n_experts words; larger problems are rejected
+ * with FT_ERR_SIZE before anything runs (use ft_moe_route_offsets for them).
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array and nothing in it
+ * needs to start at zero (every histogram entry is written before it is
+ * read), so calls that overlap on the GPU - on different streams, or from
+ * different host threads - race with each other and must be serialized by
+ * the caller.  Arguments, outputs and the other errors are those of
+ * ft_moe_route_offsets; with dev_err == NULL bad-id flags are dropped.
+ */
+#define FT_ROUTE_NOALLOC_SCRATCH_WORDS (1 << 18)
+FT_API int ft_moe_route_offsets_noalloc(const int32_t* topk_ids, int64_t tokens, int32_t top_k,
+                                        int32_t n_experts, int32_t* counts, int32_t* offsets,
+                                        int32_t* perm, uint32_t* dev_err, void* stream);
+
+/*
  * ft_moe_q4_0_q8_1 - the routed expert matmul defined at the top of this file.
  * Routes internally (into the workspace), then runs the GEMV or the grouped
  * GEMM path (FT_PATH_AUTO decides on the host, without reading the device).

@@ -201,14 +201,15 @@ static int get_stream_capturing(cudaStream_t s, bool* capturing) {
 // -------------------------------------------------------------- workspace
 // Per device: one cudaMalloc'ed block.  Layout (each part 256-byte aligned):
 //   err word | counts[E] | offsets[E+1] | perm[S] | tiles_gemv[E+1] |
-//   tiles_gemm[E+1] | hist[nchunks][E]
+//   tiles_gemm[E+1] | hist[nchunks][E] | (tensor-core path only:)
+//   xh[S_pad][ncols] fp16 | da[S_pad][ncols/32] fp16
 struct WsLayout {
-    size_t err, counts, offsets, perm, tiles_gemv, tiles_gemm, hist, total;
+    size_t err, counts, offsets, perm, tiles_gemv, tiles_gemm, hist, xh, da, total;
 };
 
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
-static WsLayout ws_layout(int64_t n_slots, int32_t n_experts) {
+static WsLayout ws_layout(int64_t n_slots, int32_t n_experts, int64_t gemm_ncols = 0) {
     WsLayout L{};
     size_t o = 0;
     L.err = o;
@@ -225,6 +226,11 @@ static WsLayout ws_layout(int64_t n_slots, int32_t n_experts) {
     o = al256(o + 4 * (static_cast<size_t>(n_experts) + 1));
     L.hist = o;
     o = al256(o + 4 * static_cast<size_t>(route_chunks(n_slots)) * n_experts);
+    const size_t rows = gemm_ncols ? static_cast<size_t>(gemm_rows(n_slots)) : 0;
+    L.xh = o;
+    o = al256(o + 2 * rows * static_cast<size_t>(gemm_ncols));
+    L.da = o;
+    o = al256(o + 2 * rows * static_cast<size_t>(gemm_ncols / 32));
     L.total = o;
     return L;
 }
@@ -296,7 +302,11 @@ static int path_setting() {
     return g_path;
 }
 
-static bool gemm_shape_ok(const Shape& sh) { return sh.ncols % 256 == 0; }
+// The tensor-core path loads 8-block weight boxes (rows 16-byte aligned) of
+// 128 rows, so it needs ncols % 256 == 0 and at least 128 weight rows overall.
+static bool gemm_shape_ok(const Shape& sh) {
+    return sh.ncols % 256 == 0 && static_cast<int64_t>(sh.n_experts) * sh.nrows >= kGemmBM;
+}
 
 // Host-side choice from the shape only (no device read): the tensor-core path
 // pays off once experts see enough slots to fill a 128-column MMA tile.
@@ -312,8 +322,9 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
                       const Shape& sh, cudaStream_t s) {
     const int path = choose_path(sh, path_setting());
     if (path == FT_PATH_GEMM && !gemm_shape_ok(sh))
-        return fail(FT_ERR_ARG, "the tensor-core path needs ncols %% 256 == 0 (got %lld)", (long long)sh.ncols);
-    const WsLayout L = ws_layout(sh.n_slots, sh.n_experts);
+        return fail(FT_ERR_ARG, "the tensor-core path needs ncols %% 256 == 0 and n_experts * nrows >= 128 (got %lld, %lld)",
+                    (long long)sh.ncols, (long long)sh.n_experts * sh.nrows);
+    const WsLayout L = ws_layout(sh.n_slots, sh.n_experts, path == FT_PATH_GEMM ? sh.ncols : 0);
     uint8_t* ws = nullptr;
     if (int st = ws_acquire(L.total, s, &ws)) return st;
     RouteBuffers rb{};
@@ -342,7 +353,7 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     else
         st = launch_gemm(static_cast<const uint8_t*>(weights), static_cast<const uint8_t*>(act), rb.perm,
                          rb.offsets, rb.tiles_gemm, out, dots, rb.err, sh.n_slots, sh.top_k, sh.n_experts, sh.nrows,
-                         sh.ncols, sh.tokens, s);
+                         sh.ncols, reinterpret_cast<uint16_t*>(ws + L.xh), reinterpret_cast<uint16_t*>(ws + L.da), s);
     prof_mark(kProfMatmulEnd, s);
     return st;
 }
@@ -447,7 +458,7 @@ size_t ft_moe_workspace_bytes(int64_t tokens, int32_t top_k, int32_t n_experts, 
     const int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh);
     g_last_error = keep;
     if (st) return 0;
-    return ws_layout(sh.n_slots, sh.n_experts).total;
+    return ws_layout(sh.n_slots, sh.n_experts, gemm_shape_ok(sh) ? sh.ncols : 0).total;
 }
 
 int ft_moe_reserve(int64_t max_tokens, int32_t max_top_k, int32_t n_experts, int64_t nrows, int64_t ncols) {
@@ -455,7 +466,7 @@ int ft_moe_reserve(int64_t max_tokens, int32_t max_top_k, int32_t n_experts, int
     Shape sh{};
     if (int st = check_matmul_args(max_tokens, max_top_k, n_experts, nrows, ncols, &sh)) return st;
     uint8_t* base = nullptr;
-    return ws_acquire(ws_layout(sh.n_slots, sh.n_experts).total, nullptr, &base);
+    return ws_acquire(ws_layout(sh.n_slots, sh.n_experts, gemm_shape_ok(sh) ? sh.ncols : 0).total, nullptr, &base);
 }
 
 int ft_moe_release(void) {

@@ -68,8 +68,13 @@ int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act
 constexpr int kGemmBN = 128;   // slots per tile
 constexpr int kGemmBM = 128;   // weight rows per tile
 
+// xh: [S_pad][ncols] fp16 and da: [S_pad][ncols/32] fp16 workspace for the
+// routed activations in router order, S_pad = gemm_rows(S) (written by the
+// gather kernel, zero past the routed slots, read by TMA).
+inline int64_t gemm_rows(int64_t n_slots) { return (n_slots + kGemmBN - 1) / kGemmBN * kGemmBN; }
+
 int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
                 const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
-                int32_t n_experts, int64_t nrows, int64_t ncols, int64_t tokens, cudaStream_t s);
+                int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, cudaStream_t s);
 
 }  // namespace ft

@@ -7,22 +7,35 @@
 // "Key Architecture: Fixed-Layout Padding": tiles are cut from the router's
 // padding-free permutation, so no expert is padded to a fixed row count.
 //
-// Tile = (expert e, up to 128 routed slots of e, 128 weight rows of e).
-// A persistent grid (one CTA per SM) walks the tile list, whose length is
-// read on the device from the router's tile prefix; empty experts own no
-// tile.  Per CTA, warp-specialized:
-//   warp 12  producer: per stage of 8 Q4_0 blocks (K = 256) one 2-D TMA load
-//            of the 128 x 144-byte weight box, plus one 288-byte bulk copy per
-//            routed slot of its Q8_1 activation row segment (the gather);
-//   warps 8-11 unpack: Q4_0 nibbles -> fp16 (q - 8) and int8 q_a -> fp16,
-//            both exact, into the K-major 128-byte-swizzled operand layout,
-//            plus the fp32 block scales d_w (per row) and d_a (per slot);
-//   warp 13  MMA: per 32-value block, two tcgen05.mma kind::f16 (K = 16)
+// Two launches.  gather_act_kernel writes, in router order, each routed
+// slot's Q8_1 activation row as an fp16 row (exact: q in [-127, 127]) plus
+// its fp16 block scales, so that the GEMM's activation operand is a plain 2-D
+// array the TMA can load straight into the MMA's swizzled layout.
+//
+// moe_gemm_tc_kernel: tile = (expert e, up to 128 routed slots of e, 128
+// weight rows of e).  A persistent grid (one CTA per SM) walks the tile list,
+// whose length is read on the device from the router's tile prefix; empty
+// experts own no tile.  Per CTA, warp-specialized:
+//   warp 20  producer: per stage of 8 Q4_0 blocks (K = 256) a 2-D TMA load of
+//            the 128 x 144-byte weight box and of the 128 x 8 activation-scale
+//            box; per pair of blocks a 2-D TMA load of the 128 x 64 fp16
+//            activation box with 128-byte swizzle (the MMA's B layout);
+//   warps 16-19 unpack: Q4_0 nibbles -> fp16 (q - 8), exact, into the K-major
+//            128-byte-swizzled A layout (each thread one weight row, 16-byte
+//            shared loads that are bank-conflict free because a 144-byte row
+//            is an odd number of 16-byte chunks), plus the fp32 block scales
+//            d_w (per row) and d_a (per slot) for the drain;
+//   warp 21  MMA: per 32-value block, two tcgen05.mma kind::f16 (K = 16)
 //            M = 128, N = 128 into its own TMEM accumulator (4 buffers);
-//   warps 0-7 drain: tcgen05.ld the block's exact integer dot (fp32 holds it
-//            exactly: |dot| <= 32512), acc += dot * (d_w * d_a) in fp32
-//            registers, and at the end of the tile store the 128 x 128
-//            outputs to out[slot][row] (32 consecutive rows per warp store).
+//   warps 0-15 drain: each owns 16 TMEM lanes x 64 columns and loads them
+//            with the 16x256b shape, so a thread holds 2 rows x 16 columns
+//            and one shared load of scales serves four different column
+//            pairs of the warp (a 32x32b thread would need all of its
+//            columns' scales, the same for every lane); the block's
+//            exact integer dot (fp32 holds it exactly: |dot| <= 32512) is
+//            scaled as acc += d_w * (dot * d_a) with one packed fp32x2
+//            multiply and one packed fp32x2 FMA per column pair; at the end of
+//            the tile the outputs go to out[slot][row].
 //
 // Why fp16 operands: every operand value is a small integer (q_w - 8 in
 // [-8, 7], q_a in [-127, 127]), exact in fp16, and a 32-term block dot is
@@ -31,6 +44,7 @@
 // along K, so each block needs its own accumulator and a drain; the drain's
 // two fp32 operations per (row, slot, block) set this kernel's ceiling.
 #include <cuda.h>
+#include <type_traits>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
@@ -44,19 +58,26 @@ constexpr int BM = kGemmBM;                 // weight rows per tile
 constexpr int BN = kGemmBN;                 // slots per tile
 constexpr int KB = 8;                       // Q4_0 blocks per raw stage (K = 256)
 constexpr int RAW_STAGES = 2;
-constexpr int OP_SLOTS = 2;                 // operand slots of 2 blocks (K = 64, one 128-B swizzle atom)
+constexpr int OP_SLOTS = 4;                 // operand slots of 2 blocks (K = 64, one 128-B swizzle atom)
 constexpr int NACC = 4;                     // TMEM accumulators, 128 columns each
 constexpr int NSC = 8;                      // scale ring depth (blocks)
 constexpr int W_RAW_BYTES = BM * KB * Q4_0_BYTES;    // 18432
-constexpr int A_RAW_BYTES = BN * KB * Q8_1_BYTES;    // 36864
-constexpr int RAW_STAGE_BYTES = W_RAW_BYTES + A_RAW_BYTES;
+constexpr int DA_RAW_BYTES = BN * KB * 2;             // 2048: [slot][8] fp16 activation scales
+constexpr int RAW_STAGE_BYTES = W_RAW_BYTES + DA_RAW_BYTES;
 constexpr int OPA_BYTES = BM * 128;                  // 16384
 constexpr int OPB_BYTES = BN * 128;                  // 16384
 constexpr int OP_SLOT_BYTES = OPA_BYTES + OPB_BYTES;
-constexpr int SC_BYTES = (BM + BN) * 4;
-constexpr int N_DRAIN_WARPS = 8, N_UNPACK_WARPS = 4;
-constexpr int WARP_PRODUCER = 12, WARP_MMA = 13;
-constexpr int THREADS = 14 * 32;
+// Scales of one block, fp32: d_w[BM], then d_a in the drain's read order:
+// for each 64-column half and column-pair index q (0..3) a group of 16
+// floats {d_a[64 half + 8 i + 2 q + e] : i < 8, e < 2} at a 20-float (80 B)
+// pitch, so that the four 16-byte groups a warp's quads load at once fall
+// in four different bank groups.
+constexpr int DA_QPITCH = 20;
+constexpr int SC_BYTES = BM * 4 + 2 * 4 * DA_QPITCH * 4;   // 512 + 640
+constexpr int N_DRAIN_WARPS = 16, N_UNPACK_WARPS = 4;
+constexpr int UNPACK_THREADS = N_UNPACK_WARPS * 32;  // each converts BM / UNPACK_THREADS weight rows
+constexpr int WARP_PRODUCER = 20, WARP_MMA = 21;
+constexpr int THREADS = 22 * 32;                     // up to 6 warps per SM sub-partition: 80 registers
 constexpr uint32_t TMEM_COLS = 512;
 
 // smem offsets from a 1024-aligned base
@@ -64,14 +85,13 @@ constexpr int OFF_OP = 0;
 constexpr int OFF_RAW = OFF_OP + OP_SLOTS * OP_SLOT_BYTES;
 constexpr int OFF_SC = OFF_RAW + RAW_STAGES * RAW_STAGE_BYTES;
 constexpr int OFF_BAR = OFF_SC + NSC * SC_BYTES;
-constexpr int N_BARS = 2 * RAW_STAGES + 2 * OP_SLOTS + 2 * NACC + 2 * NSC;
+constexpr int N_BARS = 2 * RAW_STAGES + 2 * OP_SLOTS + 2 * NACC + NSC;
 constexpr int OFF_TMEM = OFF_BAR + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;     // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 }  // namespace gemm
 
 struct GemmArgs {
-    const uint8_t* act;
     const int32_t* perm;
     const int32_t* offsets;
     const int32_t* tiles;
@@ -139,7 +159,8 @@ __device__ __forceinline__ void i8x4_to_h2(uint32_t v, uint32_t& lo, uint32_t& h
 
 template <bool DUMP>
 __global__ void __launch_bounds__(gemm::THREADS, 1)
-    moe_gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const GemmArgs a) {
+    moe_gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                       const __grid_constant__ CUtensorMap smap, const GemmArgs a) {
     using namespace gemm;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -150,8 +171,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     uint64_t* op_empty = op_full + OP_SLOTS;
     uint64_t* acc_full = op_empty + OP_SLOTS;
     uint64_t* acc_empty = acc_full + NACC;
-    uint64_t* sc_full = acc_empty + NACC;
-    uint64_t* sc_empty = sc_full + NSC;
+    uint64_t* sc_empty = acc_empty + NACC;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
 
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
@@ -161,27 +181,34 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < RAW_STAGES; ++i) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], N_UNPACK_WARPS * 32);
+            mbar_init(&raw_empty[i], UNPACK_THREADS);
         }
         for (int i = 0; i < OP_SLOTS; ++i) {
-            mbar_init(&op_full[i], N_UNPACK_WARPS * 32);
+            mbar_init(&op_full[i], UNPACK_THREADS + 1);   // unpack threads + the producer's TMA
             mbar_init(&op_empty[i], 1);
         }
         for (int i = 0; i < NACC; ++i) {
-            mbar_init(&acc_full[i], 1);
+            // block bc's accumulator is ready once its MMAs completed (the commit)
+            // and the MMA thread has arrived after issuing them.  That second,
+            // explicit arrival releases what the MMA thread acquired from the
+            // operand barrier - the unpack threads' scale writes for the block -
+            // and, being made only after acc_empty was observed, can never fall
+            // into an earlier phase of the barrier.
+            mbar_init(&acc_full[i], 2);
             mbar_init(&acc_empty[i], N_DRAIN_WARPS);
         }
-        for (int i = 0; i < NSC; ++i) {
-            mbar_init(&sc_full[i], N_UNPACK_WARPS * 32);
-            mbar_init(&sc_empty[i], N_DRAIN_WARPS);
-        }
+        for (int i = 0; i < NSC; ++i) mbar_init(&sc_empty[i], N_DRAIN_WARPS);
         fence_mbar_init();
     }
     if (warp == WARP_MMA) {
         tmem_alloc(tmem_slot, TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == WARP_PRODUCER && lane == 0) prefetch_tmap(&wmap);
+    if (warp == WARP_PRODUCER && lane == 0) {
+        prefetch_tmap(&wmap);
+        prefetch_tmap(&xmap);
+        prefetch_tmap(&smap);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -191,102 +218,117 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
 
     if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------------ producer
-        uint32_t it = 0;
+        uint32_t it = 0, ou = 0;
         bool ok = true;
         for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
             const TileInfo ti = decode_tile(a, w);
-            int64_t arow[BN / 32];
-#pragma unroll
-            for (int j = 0; j < BN / 32; ++j) {
-                const int n = static_cast<int>(lane) + 32 * j;
-                arow[j] = n < ti.nvalid ? static_cast<int64_t>(a.perm[ti.p0 + n] / a.top_k) * nb * Q8_1_BYTES : 0;
-            }
             const int32_t wy = static_cast<int32_t>(static_cast<int64_t>(ti.e) * a.nrows + ti.m0);
-            for (int32_t ks = 0; ks < n_stages; ++ks, ++it) {
+            const int32_t py = static_cast<int32_t>(ti.p0);
+            for (int32_t ks = 0; ks < n_stages && ok; ++ks, ++it) {
                 const uint32_t s = it % RAW_STAGES;
                 if (!mbar_wait_warp(&raw_empty[s], ((it / RAW_STAGES) & 1u) ^ 1u, a.err)) { ok = false; break; }
                 uint8_t* wraw = smem + OFF_RAW + s * RAW_STAGE_BYTES;
-                uint8_t* araw = wraw + W_RAW_BYTES;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&raw_full[s], W_RAW_BYTES + ti.nvalid * (KB * Q8_1_BYTES));
+                    mbar_arrive_expect_tx(&raw_full[s], W_RAW_BYTES + DA_RAW_BYTES);
                     tma_load_2d(wraw, &wmap, ks * KB * Q4_0_BYTES, wy, &raw_full[s]);
+                    tma_load_2d(wraw + W_RAW_BYTES, &smap, ks * KB, py, &raw_full[s]);
+                }
+                for (int j = 0; j < KB / 2; ++j, ++ou) {
+                    const uint32_t os = ou % OP_SLOTS;
+                    if (!mbar_wait_warp(&op_empty[os], ((ou / OP_SLOTS) & 1u) ^ 1u, a.err)) { ok = false; break; }
+                    if (lane == 0) {
+                        uint8_t* opb = smem + OFF_OP + os * OP_SLOT_BYTES + OPA_BYTES;
+                        mbar_arrive_expect_tx(&op_full[os], OPB_BYTES);
+                        tma_load_2d(opb, &xmap, (ks * (KB / 2) + j) * 64, py, &op_full[os]);
+                    }
                 }
                 __syncwarp();
-#pragma unroll
-                for (int j = 0; j < BN / 32; ++j) {
-                    const int n = static_cast<int>(lane) + 32 * j;
-                    if (n < ti.nvalid)
-                        bulk_g2s(araw + n * (KB * Q8_1_BYTES),
-                                 a.act + arow[j] + static_cast<int64_t>(ks) * (KB * Q8_1_BYTES),
-                                 KB * Q8_1_BYTES, &raw_full[s]);
-                }
             }
         }
     } else if (warp >= N_DRAIN_WARPS && warp < N_DRAIN_WARPS + N_UNPACK_WARPS) {
         // -------------------------------------------------------------- unpack
-        const uint32_t u = threadIdx.x - N_DRAIN_WARPS * 32;   // weight row and slot index, 0..127
+        constexpr int RPT = BM / UNPACK_THREADS;                  // rows (and slots) per thread
+        const uint32_t u0 = threadIdx.x - N_DRAIN_WARPS * 32;     // rows u0, u0 + UNPACK_THREADS, ...
         uint32_t it = 0, ou = 0, bc = 0;
         bool ok = true;
         for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            const TileInfo ti = decode_tile(a, w);
-            const bool slot_ok = static_cast<int32_t>(u) < ti.nvalid;
             for (int32_t ks = 0; ks < n_stages && ok; ++ks, ++it) {
                 const uint32_t s = it % RAW_STAGES;
                 if (!mbar_wait(&raw_full[s], (it / RAW_STAGES) & 1u, a.err)) { ok = false; break; }
                 const uint8_t* wraw = smem + OFF_RAW + s * RAW_STAGE_BYTES;
-                const uint8_t* araw = wraw + W_RAW_BYTES;
+                // each slot's 8 activation scales of the stage (rows past the
+                // tile's routed slots hold the next expert's or zero-filled data
+                // and only reach output columns that are never stored)
+                uint32_t dav[RPT][4];                                     // 8 fp16 scales, packed in pairs
+#pragma unroll
+                for (int rr = 0; rr < RPT; ++rr) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(wraw + W_RAW_BYTES + (u0 + rr * UNPACK_THREADS) * (KB * 2));
+                    dav[rr][0] = x.x;
+                    dav[rr][1] = x.y;
+                    dav[rr][2] = x.z;
+                    dav[rr][3] = x.w;
+                }
+#pragma unroll
                 for (int j = 0; j < KB / 2; ++j, ++ou) {
                     const uint32_t os = ou % OP_SLOTS;
                     if (!mbar_wait(&op_empty[os], ((ou / OP_SLOTS) & 1u) ^ 1u, a.err)) { ok = false; break; }
                     uint8_t* opa = smem + OFF_OP + os * OP_SLOT_BYTES;
-                    uint8_t* opb = opa + OPA_BYTES;
+                    // the unit's 36 bytes of a row start at byte 36j = 16 * (2j) + 4j: words
+                    // j .. j+8 of a 3-chunk window starting at chunk 2j (9 chunks per row, so
+                    // 8 consecutive rows hit 8 different 16-byte bank groups)
+                    uint32_t wv[RPT][12];
+#pragma unroll
+                    for (int rr = 0; rr < RPT; ++rr) {
+                        const uint4* wrow =
+                            reinterpret_cast<const uint4*>(wraw + (u0 + rr * UNPACK_THREADS) * (KB * Q4_0_BYTES));
+#pragma unroll
+                        for (int c = 0; c < 3; ++c) {
+                            const uint4 q = wrow[2 * j + c];
+                            wv[rr][4 * c + 0] = q.x;
+                            wv[rr][4 * c + 1] = q.y;
+                            wv[rr][4 * c + 2] = q.z;
+                            wv[rr][4 * c + 3] = q.w;
+                        }
+                    }
+#pragma unroll
                     for (int h = 0; h < 2; ++h, ++bc) {
-                        const int bi = 2 * j + h;
                         const uint32_t sc = bc % NSC;
                         if (!mbar_wait(&sc_empty[sc], ((bc / NSC) & 1u) ^ 1u, a.err)) { ok = false; break; }
                         float* dws = reinterpret_cast<float*>(smem + OFF_SC + sc * SC_BYTES);
                         float* das = dws + BM;
-                        // weight row u, block bi: 18 bytes at a 2-byte aligned offset
-                        {
-                            const uint32_t off = u * (KB * Q4_0_BYTES) + bi * Q4_0_BYTES;
-                            const uint32_t sh = off & 2u;
-                            const uint32_t* wv = reinterpret_cast<const uint32_t*>(wraw + (off - sh));
-                            const uint32_t W0 = wv[0], W1 = wv[1], W2 = wv[2], W3 = wv[3], W4 = wv[4];
-                            const uint32_t sel = sh ? 0x7654u : 0x5432u;
-                            const uint32_t q[4] = {__byte_perm(W0, W1, sel), __byte_perm(W1, W2, sel),
-                                                   __byte_perm(W2, W3, sel), __byte_perm(W3, W4, sel)};
-                            dws[u] = __half2float(
-                                __ushort_as_half(static_cast<unsigned short>((W0 >> (sh * 8)) & 0xFFFFu)));
-                            uint32_t hv[16];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                nib4_to_h2(q[i] & 0x0F0F0F0Fu, hv[2 * i], hv[2 * i + 1]);            // values 4i..4i+3
-                                nib4_to_h2((q[i] >> 4) & 0x0F0F0F0Fu, hv[8 + 2 * i], hv[8 + 2 * i + 1]);  // 16+4i..
+                        for (int rr = 0; rr < RPT; ++rr) {
+                            const uint32_t u = u0 + rr * UNPACK_THREADS;
+                            uint32_t q[4], dbits;
+                            if (h == 0) {   // bytes 4j .. 4j+17 of the window: 2-byte aligned nibbles
+                                dbits = wv[rr][j] & 0xFFFFu;
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) q[i] = __byte_perm(wv[rr][j + i], wv[rr][j + i + 1], 0x5432u);
+                            } else {        // bytes 4j+18 .. 4j+35: word-aligned nibbles
+                                dbits = wv[rr][j + 4] >> 16;
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) q[i] = wv[rr][j + 5 + i];
                             }
+                            dws[u] = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
+                            {
+                                const uint32_t pair = dav[rr][j];             // scales of blocks 2j, 2j+1
+                                const unsigned short hb = static_cast<unsigned short>(h ? (pair >> 16) : (pair & 0xFFFFu));
+                                const uint32_t c = u & 63u;                   // slot u: half u/64, i, q, e
+                                das[(u >> 6) * (4 * DA_QPITCH) + ((c & 7u) >> 1) * DA_QPITCH + (c >> 3) * 2 + (c & 1u)] =
+                                    __half2float(__ushort_as_half(hb));
+                            }
+                            // 16-byte chunk c holds values 8c..8c+7: the low nibbles of q[0..3] are
+                            // values 0..15, the high nibbles values 16..31
 #pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                *reinterpret_cast<uint4*>(opa + sw128_off(u, 4 * h + c)) =
-                                    make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+                            for (int c = 0; c < 4; ++c) {
+                                const uint32_t qa = q[2 * (c & 1)], qb = q[2 * (c & 1) + 1];
+                                const uint32_t sh = (c >> 1) * 4u;
+                                uint32_t h0, h1, h2, h3;
+                                nib4_to_h2((qa >> sh) & 0x0F0F0F0Fu, h0, h1);
+                                nib4_to_h2((qb >> sh) & 0x0F0F0F0Fu, h2, h3);
+                                *reinterpret_cast<uint4*>(opa + sw128_off(u, 4 * h + c)) = make_uint4(h0, h1, h2, h3);
+                            }
                         }
-                        // slot u, block bi: 36 bytes, 4-byte aligned
-                        if (slot_ok) {
-                            const uint32_t* av =
-                                reinterpret_cast<const uint32_t*>(araw + u * (KB * Q8_1_BYTES) + bi * Q8_1_BYTES);
-                            das[u] = __half2float(__ushort_as_half(static_cast<unsigned short>(av[0] & 0xFFFFu)));
-                            uint32_t hv[16];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) i8x4_to_h2(av[1 + i], hv[2 * i], hv[2 * i + 1]);
-#pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                *reinterpret_cast<uint4*>(opb + sw128_off(u, 4 * h + c)) =
-                                    make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
-                        } else {
-                            das[u] = 0.0f;
-#pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                *reinterpret_cast<uint4*>(opb + sw128_off(u, 4 * h + c)) = make_uint4(0, 0, 0, 0);
-                        }
-                        mbar_arrive(&sc_full[sc]);
                     }
                     if (!ok) break;
                     fence_proxy_async_smem();
@@ -322,6 +364,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                                            k);
                             }
                             tc_commit(&acc_full[ab]);
+                            mbar_arrive(&acc_full[ab]);
                         }
                         tc_commit(&op_empty[os]);
                     }
@@ -331,74 +374,90 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         __syncwarp();
     } else {
         // --------------------------------------------------------------- drain
-        const uint32_t quarter = warp & 3u, colh = warp >> 2;
-        const uint32_t row_l = quarter * 32 + lane;                       // TMEM lane = weight row in tile
-        float acc[64];
+        // warp w: TMEM lanes 32 (w % 4) + 16 ((w / 4) % 2) .. +15, columns 64 (w / 8) .. +63,
+        // loaded as two 32-column halves of 16 registers (the drain's register budget)
+        const uint32_t lane0 = (warp & 3u) * 32u + ((warp >> 2) & 1u) * 16u;
+        const uint32_t col0 = (warp >> 3) * 64u;
+        const uint32_t q = lane & 3u;                      // column pair 2q, 2q+1 of each group of 8
+        const uint32_t r0 = lane0 + (lane >> 2);           // rows r0 and r0 + 8 of the tile
+        const uint32_t tlane = tmem_base + (lane0 << 16) + col0;
+        float2 acc[2][8];                                  // [row][column group]
 #pragma unroll
-        for (int c = 0; c < 64; ++c) acc[c] = 0.0f;
+        for (int i = 0; i < 8; ++i) acc[0][i] = acc[1][i] = make_float2(0.0f, 0.0f);
         uint32_t bc = 0;
         bool ok = true;
         for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
             const TileInfo ti = decode_tile(a, w);
-            const int64_t row = ti.m0 + row_l;
             for (int32_t b = 0; b < nb; ++b, ++bc) {
                 const uint32_t ab = bc % NACC, sc = bc % NSC;
                 if (!mbar_wait_warp(&acc_full[ab], (bc / NACC) & 1u, a.err)) { ok = false; break; }
-                if (!mbar_wait_warp(&sc_full[sc], (bc / NSC) & 1u, a.err)) { ok = false; break; }
                 tc_fence_after();
                 const float* dws = reinterpret_cast<const float*>(smem + OFF_SC + sc * SC_BYTES);
-                const float* das = dws + BM + colh * 64;
-                const float dw = dws[row_l];
-                const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + ab * BN + colh * 64;
+                const float4* dap =
+                    reinterpret_cast<const float4*>(dws + BM + (col0 >> 6) * (4 * DA_QPITCH) + q * DA_QPITCH);
+                const float dw0 = dws[r0], dw1 = dws[r0 + 8];
+                const float2 dw0x2 = make_float2(dw0, dw0), dw1x2 = make_float2(dw1, dw1);
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(taddr + part * 32, r);
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t d[16];
+                    tmem_ld_16x256b_x4(tlane + ab * BN + 32 * hh, d);
                     tmem_wait_ld();
+                    if (hh == 1) {                           // TMEM buffer ab fully read
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                    }
                     if constexpr (DUMP) {
-                        if (row < a.nrows) {
 #pragma unroll
-                            for (int c = 0; c < 32; ++c) {
-                                const int n = colh * 64 + part * 32 + c;
-                                if (n < ti.nvalid) {
+                        for (int ig = 0; ig < 4; ++ig)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int64_t row = ti.m0 + r0 + (e >> 1) * 8;
+                                const int n = col0 + 8 * (4 * hh + ig) + 2 * static_cast<int>(q) + (e & 1);
+                                if (row < a.nrows && n < ti.nvalid) {
                                     const int64_t s = a.perm[ti.p0 + n];
                                     a.dots[(s * a.nrows + row) * nb + b] =
-                                        static_cast<int32_t>(__uint_as_float(r[c]));
+                                        static_cast<int32_t>(__uint_as_float(d[4 * ig + e]));
                                 }
                             }
-                        }
                     } else {
+                        // acc += d_w * (dot * d_a): one packed multiply and one packed FMA per column pair
 #pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4) {
-                            const float4 d4 = *reinterpret_cast<const float4*>(das + part * 32 + 4 * c4);
-                            acc[part * 32 + 4 * c4 + 0] = fmaf(__uint_as_float(r[4 * c4 + 0]), dw * d4.x, acc[part * 32 + 4 * c4 + 0]);
-                            acc[part * 32 + 4 * c4 + 1] = fmaf(__uint_as_float(r[4 * c4 + 1]), dw * d4.y, acc[part * 32 + 4 * c4 + 1]);
-                            acc[part * 32 + 4 * c4 + 2] = fmaf(__uint_as_float(r[4 * c4 + 2]), dw * d4.z, acc[part * 32 + 4 * c4 + 2]);
-                            acc[part * 32 + 4 * c4 + 3] = fmaf(__uint_as_float(r[4 * c4 + 3]), dw * d4.w, acc[part * 32 + 4 * c4 + 3]);
+                        for (int k2 = 0; k2 < 2; ++k2) {
+                            const float4 v = dap[2 * hh + k2];   // d_a of columns 8i+2q+{0,1}, i = 4hh+2k2, +1
+#pragma unroll
+                            for (int ii = 0; ii < 2; ++ii) {
+                                const int ig = 2 * k2 + ii, i = 4 * hh + ig;
+                                const float2 da2 = ii ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
+                                const float2 t0 =
+                                    __fmul2_rn(make_float2(__uint_as_float(d[4 * ig]), __uint_as_float(d[4 * ig + 1])), da2);
+                                const float2 t1 = __fmul2_rn(
+                                    make_float2(__uint_as_float(d[4 * ig + 2]), __uint_as_float(d[4 * ig + 3])), da2);
+                                acc[0][i] = __ffma2_rn(t0, dw0x2, acc[0][i]);
+                                acc[1][i] = __ffma2_rn(t1, dw1x2, acc[1][i]);
+                            }
                         }
                     }
                 }
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&acc_empty[ab]);
-                    mbar_arrive(&sc_empty[sc]);
-                }
+                if (lane == 0) mbar_arrive(&sc_empty[sc]);   // scale slot sc free again
             }
             if (!ok) break;
             if constexpr (!DUMP) {
-                if (row < a.nrows) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const int n = colh * 64 + c;
+                for (int i = 0; i < 8; ++i) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int n = col0 + 8 * i + 2 * static_cast<int>(q) + e;
                         if (n < ti.nvalid) {
                             const int64_t s = a.perm[ti.p0 + n];
-                            a.out[s * a.nrows + row] = acc[c];
+                            float* o = a.out + s * a.nrows + ti.m0 + r0;
+                            if (ti.m0 + r0 < a.nrows) o[0] = e ? acc[0][i].y : acc[0][i].x;
+                            if (ti.m0 + r0 + 8 < a.nrows) o[8] = e ? acc[1][i].y : acc[1][i].x;
                         }
                     }
+                    acc[0][i] = acc[1][i] = make_float2(0.0f, 0.0f);
                 }
-#pragma unroll
-                for (int c = 0; c < 64; ++c) acc[c] = 0.0f;
             }
         }
     }
@@ -408,6 +467,45 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     if (warp == WARP_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// --------------------------------------------------------------- gather
+// One warp per router position p: slot s = perm[p] of token t = s / k.  Lane
+// b-strided over the K/32 blocks: 36 bytes of Q8_1 in, 64 bytes of fp16 out
+// (exact integers) and the block's fp16 scale d.  Positions past the routed slots
+// (bad ids, and the padding up to a multiple of 128 rows) are written as zeros.
+__global__ void __launch_bounds__(256)
+    gather_act_kernel(const uint8_t* __restrict__ act, const int32_t* __restrict__ perm,
+                      const int32_t* __restrict__ offsets, int32_t n_experts, int32_t top_k, int32_t nb,
+                      int64_t n_rows, uint4* __restrict__ xh, uint16_t* __restrict__ da) {
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int64_t n_valid = offsets[n_experts];
+    const uint32_t lane = lane_id();
+    for (int64_t p = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); p < n_rows;
+         p += warps) {
+        uint4* xrow = xh + p * nb * 4;      // 4 x 16 bytes per block
+        uint16_t* drow = da + p * nb;
+        if (p < n_valid) {
+            const int64_t t = perm[p] / top_k;
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(act + t * nb * Q8_1_BYTES);
+            for (int32_t b = lane; b < nb; b += 32) {
+                const uint32_t* blk = src + b * (Q8_1_BYTES / 4);
+                drow[b] = static_cast<uint16_t>(__ldg(blk) & 0xFFFFu);
+                uint32_t hv[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) i8x4_to_h2(__ldg(blk + 1 + i), hv[2 * i], hv[2 * i + 1]);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    xrow[b * 4 + c] = make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+            }
+        } else {
+            for (int32_t b = lane; b < nb; b += 32) {
+                drow[b] = 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) xrow[b * 4 + c] = make_uint4(0, 0, 0, 0);
+            }
+        }
     }
 }
 
@@ -425,27 +523,50 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
-int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
-                const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
-                int32_t n_experts, int64_t nrows, int64_t ncols, int64_t tokens, cudaStream_t s) {
-    using namespace gemm;
-    (void)tokens;
-    if (n_slots == 0) return FT_OK;
-    const int64_t nb = ncols / QK;
+static int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz,
+                     const char* what) {
     auto encode = get_encode_fn();
     if (!encode) return fail(FT_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    CUtensorMap wmap;
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(nb * Q4_0_BYTES), static_cast<cuuint64_t>(n_experts * nrows)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(nb * Q4_0_BYTES)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(KB * Q4_0_BYTES), static_cast<cuuint32_t>(BM)};
+    const cuuint64_t gdim[2] = {inner, outer};
+    const cuuint64_t gstride[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estride[2] = {1, 1};
-    CUresult cr = encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(weights), gdim, gstride, box,
-                         estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) return fail(FT_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(cr));
+    const CUresult cr = encode(map, dt, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return fail(FT_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed (%d)", what, static_cast<int>(cr));
+    return FT_OK;
+}
+
+int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
+                const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
+                int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, cudaStream_t s) {
+    using namespace gemm;
+    if (n_slots == 0) return FT_OK;
+    const int64_t nb = ncols / QK;
+    const int sms = sm_count();
+    const int64_t rows = gemm_rows(n_slots);
+    {
+        const int64_t want = (rows + 7) / 8;
+        const int64_t cap = static_cast<int64_t>(sms) * 16;
+        const dim3 grid(static_cast<unsigned>(want < cap ? want : cap));
+        gather_act_kernel<<<grid, 256, 0, s>>>(act, perm, offsets, n_experts, top_k, static_cast<int32_t>(nb), rows,
+                                               reinterpret_cast<uint4*>(xh), da);
+        if (int st = check_launch("gather_act_kernel", grid, dim3(256), 0)) return st;
+    }
+    CUtensorMap wmap, xmap, smap;
+    if (int st = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, weights, nb * Q4_0_BYTES, n_experts * nrows,
+                           nb * Q4_0_BYTES, KB * Q4_0_BYTES, BM, CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
+        return st;
+    if (int st = encode_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, ncols, rows, ncols * 2, 64, BN,
+                           CU_TENSOR_MAP_SWIZZLE_128B, "activations"))
+        return st;
+    if (int st = encode_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, da, nb, rows, nb * 2, KB, BN,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, "activation scales"))
+        return st;
 
     GemmArgs ga{};
-    ga.act = act;
     ga.perm = perm;
     ga.offsets = offsets;
     ga.tiles = tiles;
@@ -458,18 +579,17 @@ int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm,
     ga.n_experts = n_experts;
     ga.row_tiles = static_cast<int32_t>((nrows + BM - 1) / BM);
 
-    const int sms = sm_count();
     const int64_t slot_tiles_ub = (n_slots + BN - 1) / BN + (n_experts < n_slots ? n_experts : n_slots);
     const int64_t tiles_ub = slot_tiles_ub * ga.row_tiles;
     const dim3 grid(static_cast<unsigned>(tiles_ub < sms ? tiles_ub : sms));
     const dim3 block(THREADS);
     if (dots) {
         if (int st = set_smem_limit(reinterpret_cast<const void*>(moe_gemm_tc_kernel<true>), SMEM_BYTES)) return st;
-        moe_gemm_tc_kernel<true><<<grid, block, SMEM_BYTES, s>>>(wmap, ga);
+        moe_gemm_tc_kernel<true><<<grid, block, SMEM_BYTES, s>>>(wmap, xmap, smap, ga);
         return check_launch("moe_gemm_tc_kernel<dump>", grid, block, SMEM_BYTES);
     }
     if (int st = set_smem_limit(reinterpret_cast<const void*>(moe_gemm_tc_kernel<false>), SMEM_BYTES)) return st;
-    moe_gemm_tc_kernel<false><<<grid, block, SMEM_BYTES, s>>>(wmap, ga);
+    moe_gemm_tc_kernel<false><<<grid, block, SMEM_BYTES, s>>>(wmap, xmap, smap, ga);
     return check_launch("moe_gemm_tc_kernel", grid, block, SMEM_BYTES);
 }
 

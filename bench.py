@@ -45,9 +45,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (FreeToken PR #185, "Performance"); context only, other hardware.
 PAGES_T4_TOKENS_PER_S = {("prefill", 8191): 8191 / 0.7058, ("prefill", 4096): 4096 / 0.3461,
                          ("prefill", 2048): 2048 / 0.1740}
-# DRAM bytes per launch of the dominant kernel from one ncu capture, keyed by
-# the library source hash it was taken on (stale entries are not reported).
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the dominant kernel from one ncu
+# capture (profiles/moe_gemm_tc_prefill_8191.md), keyed by the library source
+# hash it was taken on, so a changed kernel reports null instead.
+NCU_TRAFFIC = {("moe_gemm_tc_kernel", "ffe0d2e9e4281bb3", "prefill:8191"): 666607872 + 341066752}
 
 
 def parse():
@@ -253,7 +254,6 @@ def ours(args):
     from bit_quantized_moe_quantize_gb300 import build
     build.build()
     ft.load()
-    ft.set_path("auto")
 
     name, wl, T = workload(args.workload)
     w, x, ids = make_inputs(wl, T, rank)

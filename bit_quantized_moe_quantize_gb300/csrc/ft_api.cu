@@ -342,7 +342,8 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     uint32_t* zero_rows = dots ? reinterpret_cast<uint32_t*>(dots) : reinterpret_cast<uint32_t*>(out);
     const int64_t row_words = dots ? sh.nrows * sh.nb : sh.nrows;
     prof_mark(kProfRouteBegin, s);
-    if (int st = launch_route(topk_ids, sh.n_slots, sh.n_experts, rb, gp.group, kGemmBN, zero_rows, row_words, s))
+    if (int st = launch_route(topk_ids, sh.n_slots, sh.n_experts, rb, gp.group, gemm_tile_width(sh.n_slots, sh.n_experts),
+                              zero_rows, row_words, s))
         return st;
     prof_mark(kProfMatmulBegin, s);
     int st;

@@ -50,11 +50,13 @@ int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const R
 
 // ------------------------------------------------------------------ GEMV
 struct GemvPlan {
-    int group;          // slots per tile (1, 2, 4 or 8)
-    int rows;           // weight rows per CTA tile
-    int lanes_per_row;  // 8, 16 or 32
-    int64_t grid_x;     // tile upper bound
-    int64_t row_tiles;
+    int group;            // slots per tile (1, 2, 4 or 8)
+    int rows;             // weight rows per stage (8 * rows per warp)
+    int lanes_per_row;    // rows per warp per stage (1, 2 or 4)
+    int stages;           // depth of the bulk-copy ring
+    int64_t grid_x;       // slot-tile upper bound
+    int64_t row_tiles;    // grid.y: CTAs per slot tile
+    int64_t rows_per_cta;
     size_t smem;
 };
 
@@ -71,6 +73,10 @@ constexpr int kGemmBM = 128;   // weight rows per tile
 // xh: [S_pad][ncols] fp16 and da: [S_pad][ncols/32] fp16 workspace for the
 // routed activations in router order, S_pad = gemm_rows(S) (written by the
 // gather kernel, zero past the routed slots, read by TMA).
+// Slot-tile width (32 or 128) the tensor-core path uses for this batch; the
+// router's GEMM tile prefix must be built with the same width.
+int gemm_tile_width(int64_t n_slots, int32_t n_experts);
+
 inline int64_t gemm_rows(int64_t n_slots) { return (n_slots + kGemmBN - 1) / kGemmBN * kGemmBN; }
 
 int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,

@@ -53,43 +53,50 @@
 
 namespace ft {
 
-namespace gemm {
-constexpr int BM = kGemmBM;                 // weight rows per tile
-constexpr int BN = kGemmBN;                 // slots per tile
-constexpr int KB = 8;                       // Q4_0 blocks per raw stage (K = 256)
-constexpr int RAW_STAGES = 2;
-constexpr int OP_SLOTS = 4;                 // operand slots of 2 blocks (K = 64, one 128-B swizzle atom)
-constexpr int NACC = 4;                     // TMEM accumulators, 128 columns each
-constexpr int NSC = 8;                      // scale ring depth (blocks)
-constexpr int W_RAW_BYTES = BM * KB * Q4_0_BYTES;    // 18432
-constexpr int DA_RAW_BYTES = BN * KB * 2;             // 2048: [slot][8] fp16 activation scales
-constexpr int RAW_STAGE_BYTES = W_RAW_BYTES + DA_RAW_BYTES;
-constexpr int OPA_BYTES = BM * 128;                  // 16384
-constexpr int OPB_BYTES = BN * 128;                  // 16384
-constexpr int OP_SLOT_BYTES = OPA_BYTES + OPB_BYTES;
-// Scales of one block, fp32: d_w[BM], then d_a in the drain's read order:
-// for each 64-column half and column-pair index q (0..3) a group of 16
-// floats {d_a[64 half + 8 i + 2 q + e] : i < 8, e < 2} at a 20-float (80 B)
-// pitch, so that the four 16-byte groups a warp's quads load at once fall
-// in four different bank groups.
-constexpr int DA_QPITCH = 20;
-constexpr int SC_BYTES = BM * 4 + 2 * 4 * DA_QPITCH * 4;   // 512 + 640
-constexpr int N_DRAIN_WARPS = 16, N_UNPACK_WARPS = 4;
-constexpr int UNPACK_THREADS = N_UNPACK_WARPS * 32;  // each converts BM / UNPACK_THREADS weight rows
-constexpr int WARP_PRODUCER = 20, WARP_MMA = 21;
-constexpr int THREADS = 22 * 32;                     // up to 6 warps per SM sub-partition: 80 registers
-constexpr uint32_t TMEM_COLS = 512;
-
-// smem offsets from a 1024-aligned base
-constexpr int OFF_OP = 0;
-constexpr int OFF_RAW = OFF_OP + OP_SLOTS * OP_SLOT_BYTES;
-constexpr int OFF_SC = OFF_RAW + RAW_STAGES * RAW_STAGE_BYTES;
-constexpr int OFF_BAR = OFF_SC + NSC * SC_BYTES;
-constexpr int N_BARS = 2 * RAW_STAGES + 2 * OP_SLOTS + 2 * NACC + NSC;
-constexpr int OFF_TMEM = OFF_BAR + N_BARS * 8;
-constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;     // + alignment slack
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-}  // namespace gemm
+// Compile-time configuration for a slot-tile width BN (32 for decode-sized
+// batches, 128 for prefill).
+template <int BN_>
+struct Gemm {
+    static constexpr int BN = BN_;                      // slots per tile
+    static constexpr int BM = kGemmBM;                  // weight rows per tile
+    static constexpr int KB = 8;                        // Q4_0 blocks per raw stage (K = 256)
+    static constexpr int RAW_STAGES = 2;
+    static constexpr int OP_SLOTS = 4;                  // operand slots of 2 blocks (K = 64, one 128-B swizzle atom)
+    static constexpr int NACC = 4;                      // TMEM accumulators, BN columns each
+    static constexpr int NSC = 8;                       // scale ring depth (blocks)
+    static constexpr int W_RAW_BYTES = BM * KB * Q4_0_BYTES;   // 18432
+    static constexpr int DA_RAW_BYTES = BN * KB * 2;           // [slot][8] fp16 activation scales
+    static constexpr int RAW_STAGE_BYTES = W_RAW_BYTES + DA_RAW_BYTES;
+    static constexpr int OPA_BYTES = BM * 128;
+    static constexpr int OPB_BYTES = BN * 128;
+    static constexpr int OP_SLOT_BYTES = OPA_BYTES + OPB_BYTES;
+    // drain: each warp owns 16 TMEM lanes x CW columns (CW / 32 loads of 16 registers)
+    static constexpr int CW = BN < 64 ? BN : 64;
+    static constexpr int N_DRAIN_WARPS = 8 * (BN / CW);
+    // Scales of one block, fp32: d_w[BM], then d_a in the drain's read order:
+    // for each CW-column group and column-pair index q (0..3) a group of CW/4
+    // floats {d_a[CW g + 8 i + 2 q + e] : i < CW/8, e < 2} at a pitch of
+    // CW/4 + 4 floats, so that the four 16-byte groups a warp's quads load at
+    // once fall in four different bank groups.
+    static constexpr int DA_QPITCH = CW / 4 + 4;
+    static constexpr int SC_BYTES = BM * 4 + (BN / CW) * 4 * DA_QPITCH * 4;
+    static constexpr int N_UNPACK_WARPS = 4;
+    static constexpr int UNPACK_THREADS = N_UNPACK_WARPS * 32;  // one weight row per thread
+    static constexpr int WARP_PRODUCER = N_DRAIN_WARPS + N_UNPACK_WARPS, WARP_MMA = WARP_PRODUCER + 1;
+    static constexpr int THREADS = (WARP_MMA + 1) * 32;
+    static constexpr uint32_t TMEM_COLS = NACC * BN;
+    // smem offsets from a 1024-aligned base
+    static constexpr int OFF_OP = 0;
+    static constexpr int OFF_RAW = OFF_OP + OP_SLOTS * OP_SLOT_BYTES;
+    static constexpr int OFF_SC = OFF_RAW + RAW_STAGES * RAW_STAGE_BYTES;
+    static constexpr int OFF_BAR = OFF_SC + NSC * SC_BYTES;
+    static constexpr int N_BARS = 2 * RAW_STAGES + 2 * OP_SLOTS + 2 * NACC + NSC;
+    static constexpr int OFF_TMEM = OFF_BAR + N_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;    // + alignment slack
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(OP_SLOT_BYTES % 1024 == 0 && OPA_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+    static_assert(BN % 32 == 0 && BN <= 256, "tile width");
+};
 
 struct GemmArgs {
     const int32_t* perm;
@@ -112,6 +119,7 @@ struct TileInfo {
     int64_t m0;
 };
 
+template <int BN>
 __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int64_t w) {
     TileInfo ti;
     const int64_t st = w / a.row_tiles;
@@ -123,9 +131,9 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int64_t w) {
         else hi = mid - 1;
     }
     ti.e = lo;
-    ti.p0 = static_cast<int64_t>(a.offsets[lo]) + (st - a.tiles[lo]) * gemm::BN;
-    ti.nvalid = static_cast<int32_t>(min(static_cast<int64_t>(gemm::BN), a.offsets[lo + 1] - ti.p0));
-    ti.m0 = mt * gemm::BM;
+    ti.p0 = static_cast<int64_t>(a.offsets[lo]) + (st - a.tiles[lo]) * BN;
+    ti.nvalid = static_cast<int32_t>(min(static_cast<int64_t>(BN), a.offsets[lo + 1] - ti.p0));
+    ti.m0 = mt * kGemmBM;
     return ti;
 }
 
@@ -157,11 +165,20 @@ __device__ __forceinline__ void i8x4_to_h2(uint32_t v, uint32_t& lo, uint32_t& h
     hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
-template <bool DUMP>
-__global__ void __launch_bounds__(gemm::THREADS, 1)
+template <int BN, bool DUMP>
+__global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
     moe_gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                        const __grid_constant__ CUtensorMap smap, const GemmArgs a) {
-    using namespace gemm;
+    using C = Gemm<BN>;
+    constexpr int BM = C::BM, KB = C::KB, RAW_STAGES = C::RAW_STAGES, OP_SLOTS = C::OP_SLOTS, NACC = C::NACC;
+    constexpr int NSC = C::NSC, W_RAW_BYTES = C::W_RAW_BYTES, DA_RAW_BYTES = C::DA_RAW_BYTES;
+    constexpr int RAW_STAGE_BYTES = C::RAW_STAGE_BYTES, OPA_BYTES = C::OPA_BYTES, OPB_BYTES = C::OPB_BYTES;
+    constexpr int OP_SLOT_BYTES = C::OP_SLOT_BYTES, CW = C::CW, N_DRAIN_WARPS = C::N_DRAIN_WARPS;
+    constexpr int DA_QPITCH = C::DA_QPITCH, SC_BYTES = C::SC_BYTES, N_UNPACK_WARPS = C::N_UNPACK_WARPS;
+    constexpr int UNPACK_THREADS = C::UNPACK_THREADS, WARP_PRODUCER = C::WARP_PRODUCER, WARP_MMA = C::WARP_MMA;
+    constexpr uint32_t TMEM_COLS = C::TMEM_COLS;
+    constexpr int OFF_OP = C::OFF_OP, OFF_RAW = C::OFF_RAW, OFF_SC = C::OFF_SC, OFF_BAR = C::OFF_BAR;
+    constexpr int OFF_TMEM = C::OFF_TMEM;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -221,7 +238,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         uint32_t it = 0, ou = 0;
         bool ok = true;
         for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            const TileInfo ti = decode_tile(a, w);
+            const TileInfo ti = decode_tile<BN>(a, w);
             const int32_t wy = static_cast<int32_t>(static_cast<int64_t>(ti.e) * a.nrows + ti.m0);
             const int32_t py = static_cast<int32_t>(ti.p0);
             for (int32_t ks = 0; ks < n_stages && ok; ++ks, ++it) {
@@ -262,7 +279,10 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                 uint32_t dav[RPT][4];                                     // 8 fp16 scales, packed in pairs
 #pragma unroll
                 for (int rr = 0; rr < RPT; ++rr) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(wraw + W_RAW_BYTES + (u0 + rr * UNPACK_THREADS) * (KB * 2));
+                    const uint32_t us = u0 + rr * UNPACK_THREADS;
+                    uint4 x = make_uint4(0, 0, 0, 0);
+                    if (us < static_cast<uint32_t>(BN))
+                        x = *reinterpret_cast<const uint4*>(wraw + W_RAW_BYTES + us * (KB * 2));
                     dav[rr][0] = x.x;
                     dav[rr][1] = x.y;
                     dav[rr][2] = x.z;
@@ -313,9 +333,11 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                             {
                                 const uint32_t pair = dav[rr][j];             // scales of blocks 2j, 2j+1
                                 const unsigned short hb = static_cast<unsigned short>(h ? (pair >> 16) : (pair & 0xFFFFu));
-                                const uint32_t c = u & 63u;                   // slot u: half u/64, i, q, e
-                                das[(u >> 6) * (4 * DA_QPITCH) + ((c & 7u) >> 1) * DA_QPITCH + (c >> 3) * 2 + (c & 1u)] =
-                                    __half2float(__ushort_as_half(hb));
+                                if (u < static_cast<uint32_t>(BN)) {
+                                    const uint32_t c = u % CW;                // slot u: group u/CW, i, q, e
+                                    das[(u / CW) * (4 * DA_QPITCH) + ((c & 7u) >> 1) * DA_QPITCH + (c >> 3) * 2 + (c & 1u)] =
+                                        __half2float(__ushort_as_half(hb));
+                                }
                             }
                             // 16-byte chunk c holds values 8c..8c+7: the low nibbles of q[0..3] are
                             // values 0..15, the high nibbles values 16..31
@@ -374,35 +396,36 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         __syncwarp();
     } else {
         // --------------------------------------------------------------- drain
-        // warp w: TMEM lanes 32 (w % 4) + 16 ((w / 4) % 2) .. +15, columns 64 (w / 8) .. +63,
-        // loaded as two 32-column halves of 16 registers (the drain's register budget)
+        // warp w: TMEM lanes 32 (w % 4) + 16 ((w / 4) % 2) .. +15, columns CW (w / 8) .. +CW-1,
+        // loaded as CW/32 halves of 16 registers (the drain's register budget)
+        constexpr int NH = CW / 32;
         const uint32_t lane0 = (warp & 3u) * 32u + ((warp >> 2) & 1u) * 16u;
-        const uint32_t col0 = (warp >> 3) * 64u;
+        const uint32_t col0 = (warp >> 3) * static_cast<uint32_t>(CW);
         const uint32_t q = lane & 3u;                      // column pair 2q, 2q+1 of each group of 8
         const uint32_t r0 = lane0 + (lane >> 2);           // rows r0 and r0 + 8 of the tile
         const uint32_t tlane = tmem_base + (lane0 << 16) + col0;
-        float2 acc[2][8];                                  // [row][column group]
+        float2 acc[2][CW / 8];                             // [row][column group]
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[0][i] = acc[1][i] = make_float2(0.0f, 0.0f);
+        for (int i = 0; i < CW / 8; ++i) acc[0][i] = acc[1][i] = make_float2(0.0f, 0.0f);
         uint32_t bc = 0;
         bool ok = true;
         for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            const TileInfo ti = decode_tile(a, w);
+            const TileInfo ti = decode_tile<BN>(a, w);
             for (int32_t b = 0; b < nb; ++b, ++bc) {
                 const uint32_t ab = bc % NACC, sc = bc % NSC;
                 if (!mbar_wait_warp(&acc_full[ab], (bc / NACC) & 1u, a.err)) { ok = false; break; }
                 tc_fence_after();
                 const float* dws = reinterpret_cast<const float*>(smem + OFF_SC + sc * SC_BYTES);
                 const float4* dap =
-                    reinterpret_cast<const float4*>(dws + BM + (col0 >> 6) * (4 * DA_QPITCH) + q * DA_QPITCH);
+                    reinterpret_cast<const float4*>(dws + BM + (col0 / CW) * (4 * DA_QPITCH) + q * DA_QPITCH);
                 const float dw0 = dws[r0], dw1 = dws[r0 + 8];
                 const float2 dw0x2 = make_float2(dw0, dw0), dw1x2 = make_float2(dw1, dw1);
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
+                for (int hh = 0; hh < NH; ++hh) {
                     uint32_t d[16];
                     tmem_ld_16x256b_x4(tlane + ab * BN + 32 * hh, d);
                     tmem_wait_ld();
-                    if (hh == 1) {                           // TMEM buffer ab fully read
+                    if (hh == NH - 1) {                      // TMEM buffer ab fully read
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&acc_empty[ab]);
@@ -445,7 +468,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             if (!ok) break;
             if constexpr (!DUMP) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < CW / 8; ++i) {
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int n = col0 + 8 * i + 2 * static_cast<int>(q) + e;
@@ -539,11 +562,12 @@ static int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
     return FT_OK;
 }
 
-int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
-                const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
-                int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, cudaStream_t s) {
-    using namespace gemm;
-    if (n_slots == 0) return FT_OK;
+template <int BN>
+static int launch_gemm_bn(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
+                          const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots,
+                          int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da,
+                          cudaStream_t s) {
+    using C = Gemm<BN>;
     const int64_t nb = ncols / QK;
     const int sms = sm_count();
     const int64_t rows = gemm_rows(n_slots);
@@ -557,12 +581,12 @@ int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm,
     }
     CUtensorMap wmap, xmap, smap;
     if (int st = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, weights, nb * Q4_0_BYTES, n_experts * nrows,
-                           nb * Q4_0_BYTES, KB * Q4_0_BYTES, BM, CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
+                           nb * Q4_0_BYTES, C::KB * Q4_0_BYTES, C::BM, CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
         return st;
     if (int st = encode_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, ncols, rows, ncols * 2, 64, BN,
                            CU_TENSOR_MAP_SWIZZLE_128B, "activations"))
         return st;
-    if (int st = encode_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, da, nb, rows, nb * 2, KB, BN,
+    if (int st = encode_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, da, nb, rows, nb * 2, C::KB, BN,
                            CU_TENSOR_MAP_SWIZZLE_NONE, "activation scales"))
         return st;
 
@@ -577,20 +601,38 @@ int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm,
     ga.nb = static_cast<int32_t>(nb);
     ga.top_k = top_k;
     ga.n_experts = n_experts;
-    ga.row_tiles = static_cast<int32_t>((nrows + BM - 1) / BM);
+    ga.row_tiles = static_cast<int32_t>((nrows + C::BM - 1) / C::BM);
 
     const int64_t slot_tiles_ub = (n_slots + BN - 1) / BN + (n_experts < n_slots ? n_experts : n_slots);
     const int64_t tiles_ub = slot_tiles_ub * ga.row_tiles;
     const dim3 grid(static_cast<unsigned>(tiles_ub < sms ? tiles_ub : sms));
-    const dim3 block(THREADS);
+    const dim3 block(C::THREADS);
     if (dots) {
-        if (int st = set_smem_limit(reinterpret_cast<const void*>(moe_gemm_tc_kernel<true>), SMEM_BYTES)) return st;
-        moe_gemm_tc_kernel<true><<<grid, block, SMEM_BYTES, s>>>(wmap, xmap, smap, ga);
-        return check_launch("moe_gemm_tc_kernel<dump>", grid, block, SMEM_BYTES);
+        if (int st = set_smem_limit(reinterpret_cast<const void*>(moe_gemm_tc_kernel<BN, true>), C::SMEM_BYTES))
+            return st;
+        moe_gemm_tc_kernel<BN, true><<<grid, block, C::SMEM_BYTES, s>>>(wmap, xmap, smap, ga);
+        return check_launch("moe_gemm_tc_kernel<dump>", grid, block, C::SMEM_BYTES);
     }
-    if (int st = set_smem_limit(reinterpret_cast<const void*>(moe_gemm_tc_kernel<false>), SMEM_BYTES)) return st;
-    moe_gemm_tc_kernel<false><<<grid, block, SMEM_BYTES, s>>>(wmap, xmap, smap, ga);
-    return check_launch("moe_gemm_tc_kernel", grid, block, SMEM_BYTES);
+    if (int st = set_smem_limit(reinterpret_cast<const void*>(moe_gemm_tc_kernel<BN, false>), C::SMEM_BYTES)) return st;
+    moe_gemm_tc_kernel<BN, false><<<grid, block, C::SMEM_BYTES, s>>>(wmap, xmap, smap, ga);
+    return check_launch("moe_gemm_tc_kernel", grid, block, C::SMEM_BYTES);
+}
+
+int gemm_tile_width(int64_t n_slots, int32_t n_experts) {
+    // narrow slot tiles while experts see few slots each: the drain then scales
+    // 32 instead of 128 columns per block
+    return static_cast<double>(n_slots) / n_experts < 96.0 ? 32 : kGemmBN;
+}
+
+int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
+                const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
+                int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, cudaStream_t s) {
+    if (n_slots == 0) return FT_OK;
+    if (gemm_tile_width(n_slots, n_experts) == 32)
+        return launch_gemm_bn<32>(weights, act, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,
+                                  ncols, xh, da, s);
+    return launch_gemm_bn<kGemmBN>(weights, act, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,
+                                   ncols, xh, da, s);
 }
 
 }  // namespace ft

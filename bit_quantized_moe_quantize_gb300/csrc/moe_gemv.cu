@@ -7,15 +7,17 @@
 // the flat (token, top-k) index belongs on grid.x, never on grid.z).  The
 // tile -> expert map is a binary search over the router's tile prefix, i.e.
 // searchsorted(right=True) (nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 2), so
-// empty experts own no tile.  grid.y walks weight-row tiles (kept <= 65535;
-// a CTA loops when there are more).  Extra CTAs of the upper bound exit.
+// empty experts own no tile.  grid.y splits the expert's rows into contiguous
+// ranges, sized from the SM count so that all CTAs stream at once (<= 65535).
+// Extra CTAs of the upper bound exit.
 //
-// Per CTA: one bulk copy (cp.async.bulk, mbarrier-tracked) stages the row
-// tile's Q4_0 bytes, which are contiguous because an expert's rows are; the
-// G activation rows are unpacked into shared memory as 16-byte aligned int8
-// blocks plus fp32 scales and exact block sums.  Each weight block is read
-// once from shared memory and dotted with all G slots, so weight bytes are
-// read from HBM once per (expert, row tile, slot group).
+// Per CTA: the G activation rows are staged once in shared memory as 16-byte
+// aligned int8 blocks plus fp32 scales and exact block sums; the row range's
+// Q4_0 bytes (contiguous, because an expert's rows are) stream through a ring
+// of up to four mbarrier-tracked bulk copies (cp.async.bulk) of ~40 KB, so
+// several copies are in flight while the previous stage is computed.  Each
+// weight block is read once from shared memory and dotted with all G slots,
+// so weight bytes leave HBM once per (expert, slot group).
 //
 // Arithmetic: per block, sum_i q_w[i] * q_a[i] with dp4a on the raw nibbles,
 // then minus 8 * sum_i q_a[i] (exact integer), so the block dot is bit-exact;
@@ -41,24 +43,21 @@ struct GemvArgs {
     int32_t nb;          // blocks per row
     int32_t top_k;
     int32_t n_experts;
-    int32_t rows;        // rows per tile
-    int32_t lanes_per_row;
-    int64_t row_tiles;
-    int32_t bulk;        // weight rows 16-byte aligned -> bulk copy
+    int32_t stages;      // depth of the weight ring (1..kMaxStages)
+    int64_t rows_per_cta;
+    int32_t bulk;        // weight rows 16-byte aligned -> bulk copies
 };
 
+constexpr int kMaxStages = 4;
+
 // Shared-memory carve-up (bytes), in this order:
-//   mbarrier (16) | slot ids int32[G] (pad 16) | qa [G][nb][32] | da f32 [G][nb]
-//   | suma i32 [G][nb] | weight tile [rows][nb][18] (+16 pad)
-__host__ __device__ inline size_t gemv_smem_bytes(int G, int nb, int rows) {
-    size_t o = 16;
-    o += ((static_cast<size_t>(G) * 4 + 15) / 16) * 16;
-    o += static_cast<size_t>(G) * nb * 32;
-    o += static_cast<size_t>(G) * nb * 4;
-    o += static_cast<size_t>(G) * nb * 4;
-    o = (o + 15) / 16 * 16;
-    o += static_cast<size_t>(rows) * nb * Q4_0_BYTES + 16;
-    return o;
+//   mbarriers [kMaxStages] (32) | slot ids int32[G] (pad 16) | qa [G][nb][32] |
+//   da f32 [G][nb] | suma i32 [G][nb] | weight ring [stages][R rows][nb][18] (+16 pad each)
+__host__ __device__ inline size_t gemv_act_bytes(int G, int nb) {
+    return (32 + ((static_cast<size_t>(G) * 4 + 15) / 16) * 16 + static_cast<size_t>(G) * nb * 40 + 15) / 16 * 16;
+}
+__host__ __device__ inline size_t gemv_stage_bytes(int R, int nb) {
+    return (static_cast<size_t>(R) * nb * Q4_0_BYTES + 16 + 15) / 16 * 16;
 }
 
 __device__ __forceinline__ int32_t find_expert(const int32_t* tiles, int32_t n_experts, int64_t t) {
@@ -72,147 +71,191 @@ __device__ __forceinline__ int32_t find_expert(const int32_t* tiles, int32_t n_e
     return lo;
 }
 
-template <int G, bool DUMP>
+// One 18-byte Q4_0 block at a 2-byte aligned shared-memory offset: fp32 d and
+// the 16 nibble bytes as four words (qs[4i..4i+3] in word i).
+__device__ __forceinline__ void load_q4_block(const uint8_t* base, uint32_t off, float& d, uint32_t (&q)[4]) {
+    const uint32_t sh = off & 2u;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off - sh));
+    const uint32_t W0 = w[0], W1 = w[1], W2 = w[2], W3 = w[3], W4 = w[4];
+    const uint32_t sel = sh ? 0x7654u : 0x5432u;
+    q[0] = __byte_perm(W0, W1, sel);
+    q[1] = __byte_perm(W1, W2, sel);
+    q[2] = __byte_perm(W2, W3, sel);
+    q[3] = __byte_perm(W3, W4, sel);
+    d = __half2float(__ushort_as_half(static_cast<unsigned short>((W0 >> (sh * 8)) & 0xFFFFu)));
+}
+
+// int32 -> fp32 for |v| < 2^22 with an integer add and a float subtract
+__device__ __forceinline__ float small_int_to_float(int v) {
+    return __int_as_float(v + 0x4B400000) - 12582912.0f;
+}
+
+// grid.x: slot tiles (G slots of one expert); grid.y: a contiguous range of that
+// expert's rows, streamed through a ring of `stages` bulk copies of R = 8 * RW
+// rows.  Warp w handles rows w*RW .. w*RW+RW-1 of each stage, lane l the blocks
+// b = l, l + 32, ... of those rows, and every activation block it loads from
+// shared memory serves RW rows.
+template <int G, int RW, bool DUMP>
 __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
+    constexpr int R = 8 * RW;
     extern __shared__ __align__(16) uint8_t smem[];
     const int64_t t = blockIdx.x;
     const int32_t E = a.n_experts;
     if (t >= a.tiles[E]) return;
+    const int64_t r_begin = static_cast<int64_t>(blockIdx.y) * a.rows_per_cta;
+    if (r_begin >= a.nrows) return;
+    const int64_t r_end = min(a.nrows, r_begin + a.rows_per_cta);
+    const int32_t n_st = static_cast<int32_t>((r_end - r_begin + R - 1) / R);
     const int32_t e = find_expert(a.tiles, E, t);
     const int64_t p0 = static_cast<int64_t>(a.offsets[e]) + (t - a.tiles[e]) * G;
     const int32_t ng = static_cast<int32_t>(min(static_cast<int64_t>(G), a.offsets[e + 1] - p0));
     const int32_t nb = a.nb;
+    const int NS = a.stages;
 
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    int32_t* slot = reinterpret_cast<int32_t*>(smem + 16);
-    size_t o = 16 + ((static_cast<size_t>(G) * 4 + 15) / 16) * 16;
+    int32_t* slot = reinterpret_cast<int32_t*>(smem + 32);
+    size_t o = 32 + ((static_cast<size_t>(G) * 4 + 15) / 16) * 16;
     uint8_t* qa = smem + o;
     o += static_cast<size_t>(G) * nb * 32;
     float* da = reinterpret_cast<float*>(smem + o);
     o += static_cast<size_t>(G) * nb * 4;
     int32_t* suma = reinterpret_cast<int32_t*>(smem + o);
-    o += static_cast<size_t>(G) * nb * 4;
-    o = (o + 15) / 16 * 16;
-    uint8_t* wt = smem + o;
+    uint8_t* ring = smem + gemv_act_bytes(G, nb);
+    const size_t stage_bytes = gemv_stage_bytes(R, nb);
 
     const int64_t row_bytes = static_cast<int64_t>(nb) * Q4_0_BYTES;
     const uint8_t* wexp = a.weights + static_cast<int64_t>(e) * a.nrows * row_bytes;
+    auto stage_rows = [&](int32_t st) { return static_cast<int32_t>(min(static_cast<int64_t>(R), r_end - (r_begin + st * R))); };
+    auto issue = [&](int32_t st) {   // one thread: bulk copy of stage st into its ring slot
+        const int32_t buf = st % NS;
+        const uint32_t bytes = static_cast<uint32_t>(stage_rows(st) * row_bytes);
+        mbar_arrive_expect_tx(&bar[buf], bytes);
+        bulk_g2s(ring + buf * stage_bytes, wexp + (r_begin + static_cast<int64_t>(st) * R) * row_bytes, bytes, &bar[buf]);
+    };
 
     if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
+        for (int i = 0; i < NS; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
     }
     if (threadIdx.x < G) slot[threadIdx.x] = threadIdx.x < ng ? a.perm[p0 + threadIdx.x] : 0;
     __syncthreads();
+    if (a.bulk && threadIdx.x == 0)
+        for (int32_t st = 0; st < min(NS, n_st); ++st) issue(st);
 
-    // unpack the G activation rows: int8 block, fp32 d, exact sum of q
+    // stage the G activation rows once: int8 block, fp32 d, exact sum of q
     for (int32_t i = threadIdx.x; i < ng * nb; i += blockDim.x) {
         const int32_t g = i / nb, b = i - g * nb;
         const int64_t tok = slot[g] / a.top_k;
         const uint32_t* src = reinterpret_cast<const uint32_t*>(a.act + (tok * nb + b) * Q8_1_BYTES);
         const uint32_t ds = __ldg(src);
-        uint4 q0 = make_uint4(__ldg(src + 1), __ldg(src + 2), __ldg(src + 3), __ldg(src + 4));
-        uint4 q1 = make_uint4(__ldg(src + 5), __ldg(src + 6), __ldg(src + 7), __ldg(src + 8));
+        const uint4 q0 = make_uint4(__ldg(src + 1), __ldg(src + 2), __ldg(src + 3), __ldg(src + 4));
+        const uint4 q1 = make_uint4(__ldg(src + 5), __ldg(src + 6), __ldg(src + 7), __ldg(src + 8));
         uint4* dst = reinterpret_cast<uint4*>(qa + (static_cast<size_t>(g) * nb + b) * 32);
         dst[0] = q0;
         dst[1] = q1;
         da[g * nb + b] = __half2float(__ushort_as_half(static_cast<unsigned short>(ds & 0xFFFFu)));
-        int s = 0;
-        s = __dp4a(static_cast<int>(q0.x), 0x01010101, s);
-        s = __dp4a(static_cast<int>(q0.y), 0x01010101, s);
-        s = __dp4a(static_cast<int>(q0.z), 0x01010101, s);
-        s = __dp4a(static_cast<int>(q0.w), 0x01010101, s);
-        s = __dp4a(static_cast<int>(q1.x), 0x01010101, s);
-        s = __dp4a(static_cast<int>(q1.y), 0x01010101, s);
-        s = __dp4a(static_cast<int>(q1.z), 0x01010101, s);
-        s = __dp4a(static_cast<int>(q1.w), 0x01010101, s);
-        suma[g * nb + b] = s;
+        int sm = 0;
+        sm = __dp4a(static_cast<int>(q0.x), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q0.y), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q0.z), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q0.w), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q1.x), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q1.y), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q1.z), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q1.w), 0x01010101, sm);
+        suma[g * nb + b] = sm;
     }
+    __syncthreads();
 
-    const int L = a.lanes_per_row;
-    const int rows_per_warp_pass = 32 / L;
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-    const int sub = static_cast<int>(lane) % L;
-    const int rsub = static_cast<int>(lane) / L;
-    uint32_t phase = 0;
-
-    for (int64_t y = blockIdx.y; y < a.row_tiles; y += gridDim.y) {
-        const int64_t r0 = y * a.rows;
-        const int32_t nr = static_cast<int32_t>(min(static_cast<int64_t>(a.rows), a.nrows - r0));
-        const uint8_t* src = wexp + r0 * row_bytes;
-        const uint32_t bytes = static_cast<uint32_t>(nr * row_bytes);
+    for (int32_t st = 0; st < n_st; ++st) {
+        const int32_t buf = st % NS;
+        const int32_t nr = stage_rows(st);
+        const int64_t r0 = r_begin + static_cast<int64_t>(st) * R;
+        uint8_t* wt = ring + buf * stage_bytes;
         if (a.bulk) {
-            if (threadIdx.x == 0) {
-                mbar_arrive_expect_tx(bar, bytes);
-                bulk_g2s(wt, src, bytes, bar);
-            }
+            if (!mbar_wait(&bar[buf], static_cast<uint32_t>((st / NS) & 1), a.err)) break;
         } else {
             // rows not 16-byte aligned: 2-byte loads (blocks are 2-byte aligned)
-            const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
+            const uint16_t* s16 = reinterpret_cast<const uint16_t*>(wexp + r0 * row_bytes);
             uint16_t* d16 = reinterpret_cast<uint16_t*>(wt);
-            for (uint32_t i = threadIdx.x; i < bytes / 2; i += blockDim.x) d16[i] = __ldg(s16 + i);
+            const uint32_t n16 = static_cast<uint32_t>(nr * row_bytes / 2);
+            for (uint32_t i = threadIdx.x; i < n16; i += blockDim.x) d16[i] = __ldg(s16 + i);
+            __syncthreads();
         }
-        __syncthreads();   // activations unpacked (first pass) / fallback tile written
-        if (a.bulk && !mbar_wait(bar, phase, a.err)) return;
-        phase ^= 1u;
 
-        for (int32_t rl = static_cast<int32_t>(warp) * rows_per_warp_pass + rsub; rl - rsub < nr;
-             rl += 8 * rows_per_warp_pass) {
-            const bool row_ok = rl < nr;
-            float acc[G];
+        const int32_t rl0 = static_cast<int32_t>(warp) * RW;   // this warp's first row in the stage
+        float acc[RW][G];
 #pragma unroll
-            for (int g = 0; g < G; ++g) acc[g] = 0.0f;
-            if (row_ok) {
-                const uint32_t rbase = static_cast<uint32_t>(rl) * static_cast<uint32_t>(row_bytes);
-                for (int b = sub; b < nb; b += L) {
-                    const uint32_t off = rbase + static_cast<uint32_t>(b) * Q4_0_BYTES;
-                    const uint32_t sh = off & 2u;
-                    const uint32_t* w = reinterpret_cast<const uint32_t*>(wt + (off - sh));
-                    const uint32_t W0 = w[0], W1 = w[1], W2 = w[2], W3 = w[3], W4 = w[4];
-                    const uint32_t sel = sh ? 0x7654u : 0x5432u;
-                    const uint32_t q0 = __byte_perm(W0, W1, sel), q1 = __byte_perm(W1, W2, sel);
-                    const uint32_t q2 = __byte_perm(W2, W3, sel), q3 = __byte_perm(W3, W4, sel);
-                    const float dw =
-                        __half2float(__ushort_as_half(static_cast<unsigned short>((W0 >> (sh * 8)) & 0xFFFFu)));
-                    const int l0 = q0 & 0x0F0F0F0F, l1 = q1 & 0x0F0F0F0F, l2 = q2 & 0x0F0F0F0F, l3 = q3 & 0x0F0F0F0F;
-                    const int h0 = (q0 >> 4) & 0x0F0F0F0F, h1 = (q1 >> 4) & 0x0F0F0F0F;
-                    const int h2 = (q2 >> 4) & 0x0F0F0F0F, h3 = (q3 >> 4) & 0x0F0F0F0F;
+        for (int j = 0; j < RW; ++j)
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        if (g < ng) {
-                            const uint4* av = reinterpret_cast<const uint4*>(qa + (static_cast<size_t>(g) * nb + b) * 32);
-                            const uint4 A0 = av[0], A1 = av[1];
-                            int dot = 0;
-                            dot = __dp4a(l0, static_cast<int>(A0.x), dot);
-                            dot = __dp4a(l1, static_cast<int>(A0.y), dot);
-                            dot = __dp4a(l2, static_cast<int>(A0.z), dot);
-                            dot = __dp4a(l3, static_cast<int>(A0.w), dot);
-                            dot = __dp4a(h0, static_cast<int>(A1.x), dot);
-                            dot = __dp4a(h1, static_cast<int>(A1.y), dot);
-                            dot = __dp4a(h2, static_cast<int>(A1.z), dot);
-                            dot = __dp4a(h3, static_cast<int>(A1.w), dot);
-                            dot -= 8 * suma[g * nb + b];
+            for (int g = 0; g < G; ++g) acc[j][g] = 0.0f;
+        if (rl0 < nr) {
+            for (int b = static_cast<int>(lane); b < nb; b += 32) {
+                int lo[RW][4], hi[RW][4];
+                float dw[RW];
+#pragma unroll
+                for (int j = 0; j < RW; ++j) {
+                    uint32_t q[4];
+                    const int rl = min(rl0 + j, nr - 1);       // rows past the stage repeat the last one
+                    load_q4_block(wt, static_cast<uint32_t>(rl * row_bytes + b * Q4_0_BYTES), dw[j], q);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        lo[j][i] = static_cast<int>(q[i] & 0x0F0F0F0Fu);
+                        hi[j][i] = static_cast<int>((q[i] >> 4) & 0x0F0F0F0Fu);
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    if (g < ng) {
+                        const uint4* av = reinterpret_cast<const uint4*>(qa + (static_cast<size_t>(g) * nb + b) * 32);
+                        const uint4 A0 = av[0], A1 = av[1];
+                        const float dag = da[g * nb + b];
+                        const int sa8 = 8 * suma[g * nb + b];
+#pragma unroll
+                        for (int j = 0; j < RW; ++j) {
+                            int dot = -sa8;
+                            dot = __dp4a(lo[j][0], static_cast<int>(A0.x), dot);
+                            dot = __dp4a(lo[j][1], static_cast<int>(A0.y), dot);
+                            dot = __dp4a(lo[j][2], static_cast<int>(A0.z), dot);
+                            dot = __dp4a(lo[j][3], static_cast<int>(A0.w), dot);
+                            dot = __dp4a(hi[j][0], static_cast<int>(A1.x), dot);
+                            dot = __dp4a(hi[j][1], static_cast<int>(A1.y), dot);
+                            dot = __dp4a(hi[j][2], static_cast<int>(A1.z), dot);
+                            dot = __dp4a(hi[j][3], static_cast<int>(A1.w), dot);
                             if constexpr (DUMP) {
-                                a.dots[(static_cast<int64_t>(slot[g]) * a.nrows + r0 + rl) * nb + b] = dot;
+                                if (rl0 + j < nr)
+                                    a.dots[(static_cast<int64_t>(slot[g]) * a.nrows + r0 + rl0 + j) * nb + b] = dot;
                             } else {
-                                acc[g] = fmaf(static_cast<float>(dot), dw * da[g * nb + b], acc[g]);
+                                acc[j][g] = fmaf(small_int_to_float(dot), dw[j] * dag, acc[j][g]);
                             }
                         }
                     }
                 }
             }
-            if constexpr (!DUMP) {
+        }
+        if constexpr (!DUMP) {
 #pragma unroll
-                for (int g = 0; g < G; ++g)
-                    for (int o2 = L >> 1; o2 > 0; o2 >>= 1) acc[g] += __shfl_xor_sync(0xFFFFFFFFu, acc[g], o2);
-                if (row_ok && sub == 0) {
+            for (int j = 0; j < RW; ++j)
 #pragma unroll
-                    for (int g = 0; g < G; ++g)
-                        if (g < ng) a.out[static_cast<int64_t>(slot[g]) * a.nrows + r0 + rl] = acc[g];
+                for (int g = 0; g < G; ++g) {
+                    float v = acc[j][g];
+#pragma unroll
+                    for (int o2 = 16; o2 > 0; o2 >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o2);
+                    acc[j][g] = v;
                 }
+            if (lane == 0) {
+#pragma unroll
+                for (int j = 0; j < RW; ++j)
+                    if (rl0 + j < nr) {
+#pragma unroll
+                        for (int g = 0; g < G; ++g)
+                            if (g < ng) a.out[static_cast<int64_t>(slot[g]) * a.nrows + r0 + rl0 + j] = acc[j][g];
+                    }
             }
         }
-        __syncthreads();   // tile consumed before the next copy overwrites it
+        __syncthreads();   // ring slot consumed
+        if (a.bulk && threadIdx.x == 0 && st + NS < n_st) issue(st + NS);
     }
 }
 
@@ -221,31 +264,54 @@ GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t nc
     const int64_t nb = ncols / QK;
     const double mean = static_cast<double>(n_slots) / n_experts;
     p.group = mean <= 1.0 ? 1 : mean <= 2.0 ? 2 : mean <= 4.0 ? 4 : 8;
-    p.lanes_per_row = nb >= 24 ? 32 : nb >= 12 ? 16 : 8;
     const int64_t row_bytes = nb * Q4_0_BYTES;
-    int64_t rows = 49152 / row_bytes;
-    rows = rows < 1 ? 1 : rows > 16 ? 16 : rows;
-    p.rows = static_cast<int>(rows);
-    p.row_tiles = (nrows + rows - 1) / rows;
-    p.smem = gemv_smem_bytes(p.group, static_cast<int>(nb), p.rows);
-    while (p.smem > 220 * 1024 && p.group > 1) {   // very long rows: fewer slots per tile
+    // rows per warp: a stage of 8 * RW rows of about 40 KB
+    const int64_t rw = 40960 / (8 * row_bytes);
+    p.lanes_per_row = rw >= 4 ? 4 : rw >= 2 ? 2 : 1;   // RW (rows per warp per stage)
+    p.rows = 8 * p.lanes_per_row;
+    const size_t act = gemv_act_bytes(p.group, static_cast<int>(nb));
+    const size_t stage = gemv_stage_bytes(p.rows, static_cast<int>(nb));
+    const size_t budget = 220 * 1024;
+    int stages = static_cast<int>(budget > act ? (budget - act) / stage : 0);
+    while (stages < 2 && p.group > 1) {                 // very long rows: fewer slots per tile
         p.group >>= 1;
-        p.smem = gemv_smem_bytes(p.group, static_cast<int>(nb), p.rows);
+        const size_t act2 = gemv_act_bytes(p.group, static_cast<int>(nb));
+        stages = static_cast<int>(budget > act2 ? (budget - act2) / stage : 0);
     }
+    p.stages = stages > kMaxStages ? kMaxStages : stages;
+    p.smem = gemv_act_bytes(p.group, static_cast<int>(nb)) + static_cast<size_t>(p.stages) * stage;
     const int64_t ub = (n_slots + p.group - 1) / p.group + (n_experts < n_slots ? n_experts : n_slots);
     p.grid_x = ub < n_slots ? ub : n_slots;
+    // spread each slot tile's rows over enough CTAs that every SM streams
+    const int64_t stages_total = (nrows + p.rows - 1) / p.rows;
+    const int64_t ctas_per_sm = p.smem <= 110 * 1024 ? 2 : 1;
+    const int64_t target = static_cast<int64_t>(sm_count()) * ctas_per_sm;
+    const int64_t min_tiles = (n_slots + p.group - 1) / p.group;     // at least this many slot tiles exist
+    int64_t y = min_tiles > 0 ? (target + min_tiles - 1) / min_tiles : 1;
+    y = y < 1 ? 1 : y > stages_total ? stages_total : y;
+    y = y > 65535 ? 65535 : y;
+    p.row_tiles = y;
+    p.rows_per_cta = (stages_total + y - 1) / y * p.rows;
     return p;
 }
 
-template <int G, bool DUMP>
+template <int G, int RW, bool DUMP>
 static int launch_gemv_t(const GemvPlan& plan, const GemvArgs& a, cudaStream_t s) {
-    const dim3 grid(static_cast<unsigned>(plan.grid_x),
-                    static_cast<unsigned>(plan.row_tiles < 65535 ? plan.row_tiles : 65535));
+    const dim3 grid(static_cast<unsigned>(plan.grid_x), static_cast<unsigned>(plan.row_tiles));
     const dim3 block(256);
-    if (int st = set_smem_limit(reinterpret_cast<const void*>(moe_gemv_kernel<G, DUMP>), static_cast<int>(plan.smem)))
+    if (int st = set_smem_limit(reinterpret_cast<const void*>(moe_gemv_kernel<G, RW, DUMP>), static_cast<int>(plan.smem)))
         return st;
-    moe_gemv_kernel<G, DUMP><<<grid, block, plan.smem, s>>>(a);
+    moe_gemv_kernel<G, RW, DUMP><<<grid, block, plan.smem, s>>>(a);
     return check_launch(DUMP ? "moe_gemv_kernel<dump>" : "moe_gemv_kernel", grid, block, plan.smem);
+}
+
+template <int G, bool DUMP>
+static int launch_gemv_rw(const GemvPlan& plan, const GemvArgs& a, cudaStream_t s) {
+    switch (plan.lanes_per_row) {
+        case 4: return launch_gemv_t<G, 4, DUMP>(plan, a, s);
+        case 2: return launch_gemv_t<G, 2, DUMP>(plan, a, s);
+        default: return launch_gemv_t<G, 1, DUMP>(plan, a, s);
+    }
 }
 
 int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act, const int32_t* perm,
@@ -265,17 +331,16 @@ int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act
     a.nb = static_cast<int32_t>(ncols / QK);
     a.top_k = top_k;
     a.n_experts = n_experts;
-    a.rows = plan.rows;
-    a.lanes_per_row = plan.lanes_per_row;
-    a.row_tiles = plan.row_tiles;
+    a.stages = plan.stages;
+    a.rows_per_cta = plan.rows_per_cta;
     a.bulk = ((a.nb * Q4_0_BYTES) % 16 == 0) && ((reinterpret_cast<uintptr_t>(weights) & 15u) == 0);
     (void)n_slots;
     const bool dump = dots != nullptr;
     switch (plan.group) {
-        case 1: return dump ? launch_gemv_t<1, true>(plan, a, s) : launch_gemv_t<1, false>(plan, a, s);
-        case 2: return dump ? launch_gemv_t<2, true>(plan, a, s) : launch_gemv_t<2, false>(plan, a, s);
-        case 4: return dump ? launch_gemv_t<4, true>(plan, a, s) : launch_gemv_t<4, false>(plan, a, s);
-        default: return dump ? launch_gemv_t<8, true>(plan, a, s) : launch_gemv_t<8, false>(plan, a, s);
+        case 1: return dump ? launch_gemv_rw<1, true>(plan, a, s) : launch_gemv_rw<1, false>(plan, a, s);
+        case 2: return dump ? launch_gemv_rw<2, true>(plan, a, s) : launch_gemv_rw<2, false>(plan, a, s);
+        case 4: return dump ? launch_gemv_rw<4, true>(plan, a, s) : launch_gemv_rw<4, false>(plan, a, s);
+        default: return dump ? launch_gemv_rw<8, true>(plan, a, s) : launch_gemv_rw<8, false>(plan, a, s);
     }
 }
 

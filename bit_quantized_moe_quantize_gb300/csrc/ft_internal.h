@@ -51,6 +51,7 @@ int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const R
 // ------------------------------------------------------------------ GEMV
 struct GemvPlan {
     int group;            // slots per tile (1, 2, 4 or 8)
+    int row_warps;        // row-per-lane kernel: compute warps of 32 rows each (0: the block-per-lane kernel)
     int rows;             // weight rows per stage (8 * rows per warp)
     int lanes_per_row;    // rows per warp per stage (1, 2 or 4)
     int stages;           // depth of the bulk-copy ring
@@ -70,15 +71,15 @@ int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act
 constexpr int kGemmBN = 128;   // slots per tile
 constexpr int kGemmBM = 128;   // weight rows per tile
 
-// xh: [S_pad][ncols] fp16 and da: [S_pad][ncols/32] fp16 workspace for the
-// routed activations in router order, S_pad = gemm_rows(S) (written by the
-// gather kernel, zero past the routed slots, read by TMA).
 // Slot-tile width (32 or 128) the tensor-core path uses for this batch; the
 // router's GEMM tile prefix must be built with the same width.
 int gemm_tile_width(int64_t n_slots, int32_t n_experts);
 
 inline int64_t gemm_rows(int64_t n_slots) { return (n_slots + kGemmBN - 1) / kGemmBN * kGemmBN; }
 
+// xh: [S_pad][ncols] fp16 and da: [S_pad][ncols/32] fp16 workspace for the
+// routed activations in router order, S_pad = gemm_rows(S) (written by the
+// gather kernel, zero past the routed slots, read by TMA).
 int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
                 const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
                 int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, cudaStream_t s);

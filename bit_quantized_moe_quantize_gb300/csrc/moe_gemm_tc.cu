@@ -1,5 +1,5 @@
-// Expert-grouped GEMM path of the routed Q4_0 x Q8_1 expert matmul (prefill),
-// on the sm_103a tensor cores (tcgen05 MMA into TMEM).
+// Expert-grouped GEMM path of the routed Q4_0 x Q8_1 expert matmul on the
+// sm_103a tensor cores (tcgen05 MMA into TMEM).
 //
 // The grouped form follows the expert_offsets layout of nvfp4-megamoe-kernel
 // CURRENT_BUG.md (Bug 4: offsets with a leading 0; Bug 2: position -> expert
@@ -7,35 +7,34 @@
 // "Key Architecture: Fixed-Layout Padding": tiles are cut from the router's
 // padding-free permutation, so no expert is padded to a fixed row count.
 //
-// Two launches.  gather_act_kernel writes, in router order, each routed
-// slot's Q8_1 activation row as an fp16 row (exact: q in [-127, 127]) plus
-// its fp16 block scales, so that the GEMM's activation operand is a plain 2-D
-// array the TMA can load straight into the MMA's swizzled layout.
+// gather_act_kernel writes, in router order, each routed slot's Q8_1
+// activation row as an fp16 row (exact: q in [-127, 127]) plus its fp16 block
+// scales, so that the GEMM's activation operand is a plain 2-D array the TMA
+// can load straight into the MMA's swizzled layout.
 //
-// moe_gemm_tc_kernel: tile = (expert e, up to 128 routed slots of e, 128
+// moe_gemm_tc_kernel: tile = (expert e, up to BN routed slots of e, 128
 // weight rows of e).  A persistent grid (one CTA per SM) walks the tile list,
 // whose length is read on the device from the router's tile prefix; empty
 // experts own no tile.  Per CTA, warp-specialized:
-//   warp 20  producer: per stage of 8 Q4_0 blocks (K = 256) a 2-D TMA load of
-//            the 128 x 144-byte weight box and of the 128 x 8 activation-scale
-//            box; per pair of blocks a 2-D TMA load of the 128 x 64 fp16
+//   producer: per stage of 8 Q4_0 blocks (K = 256) a 2-D TMA load of the
+//            128 x 144-byte weight box and of the BN x 8 activation-scale
+//            box; per pair of blocks a 2-D TMA load of the BN x 64 fp16
 //            activation box with 128-byte swizzle (the MMA's B layout);
-//   warps 16-19 unpack: Q4_0 nibbles -> fp16 (q - 8), exact, into the K-major
+//   unpack (4 warps): Q4_0 nibbles -> fp16 (q - 8), exact, into the K-major
 //            128-byte-swizzled A layout (each thread one weight row, 16-byte
 //            shared loads that are bank-conflict free because a 144-byte row
 //            is an odd number of 16-byte chunks), plus the fp32 block scales
 //            d_w (per row) and d_a (per slot) for the drain;
-//   warp 21  MMA: per 32-value block, two tcgen05.mma kind::f16 (K = 16)
-//            M = 128, N = 128 into its own TMEM accumulator (4 buffers);
-//   warps 0-15 drain: each owns 16 TMEM lanes x 64 columns and loads them
-//            with the 16x256b shape, so a thread holds 2 rows x 16 columns
-//            and one shared load of scales serves four different column
-//            pairs of the warp (a 32x32b thread would need all of its
-//            columns' scales, the same for every lane); the block's
-//            exact integer dot (fp32 holds it exactly: |dot| <= 32512) is
-//            scaled as acc += d_w * (dot * d_a) with one packed fp32x2
-//            multiply and one packed fp32x2 FMA per column pair; at the end of
-//            the tile the outputs go to out[slot][row].
+//   MMA:     per 32-value block, two tcgen05.mma kind::f16 (K = 16)
+//            M = 128, N = BN into its own TMEM accumulator (4 buffers);
+//   drain:   each warp owns 16 TMEM lanes x min(BN, 64) columns and loads
+//            them with the 16x256b shape, so a thread holds 2 rows x 16
+//            columns and one shared load of scales serves four different
+//            column pairs of the warp; the block's exact integer dot (fp32
+//            holds it exactly: |dot| <= 32512) is scaled as
+//            acc += d_w * (dot * d_a) with one packed fp32x2 multiply and one
+//            packed fp32x2 FMA per column pair; at the end of the tile the
+//            outputs go to out[slot][row].
 //
 // Why fp16 operands: every operand value is a small integer (q_w - 8 in
 // [-8, 7], q_a in [-127, 127]), exact in fp16, and a 32-term block dot is
@@ -43,13 +42,7 @@
 // while running at the fp16 tensor rate.  The scales change every 32 values
 // along K, so each block needs its own accumulator and a drain; the drain's
 // two fp32 operations per (row, slot, block) set this kernel's ceiling.
-#include <cuda.h>
-#include <type_traits>
-#include <cudaTypedefs.h>
-#include <cuda_fp16.h>
-
-#include "ft_common.cuh"
-#include "ft_internal.h"
+#include "gemm_common.cuh"
 
 namespace ft {
 
@@ -98,59 +91,9 @@ struct Gemm {
     static_assert(BN % 32 == 0 && BN <= 256, "tile width");
 };
 
-struct GemmArgs {
-    const int32_t* perm;
-    const int32_t* offsets;
-    const int32_t* tiles;
-    float* out;
-    int32_t* dots;
-    uint32_t* err;
-    int64_t nrows;
-    int32_t nb;
-    int32_t top_k;
-    int32_t n_experts;
-    int32_t row_tiles;
-};
-
-struct TileInfo {
-    int32_t e;
-    int64_t p0;
-    int32_t nvalid;
-    int64_t m0;
-};
-
-template <int BN>
-__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int64_t w) {
-    TileInfo ti;
-    const int64_t st = w / a.row_tiles;
-    const int64_t mt = w - st * a.row_tiles;
-    int32_t lo = 0, hi = a.n_experts - 1;
-    while (lo < hi) {
-        const int32_t mid = (lo + hi + 1) >> 1;
-        if (a.tiles[mid] <= st) lo = mid;
-        else hi = mid - 1;
-    }
-    ti.e = lo;
-    ti.p0 = static_cast<int64_t>(a.offsets[lo]) + (st - a.tiles[lo]) * BN;
-    ti.nvalid = static_cast<int32_t>(min(static_cast<int64_t>(BN), a.offsets[lo + 1] - ti.p0));
-    ti.m0 = mt * kGemmBM;
-    return ti;
-}
-
 // Byte offset of 16-byte chunk c of row r in a K-major 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) {
     return (r >> 3) * 1024u + (r & 7u) * 128u + ((c ^ (r & 7u)) << 4);
-}
-
-// Four packed nibble bytes -> two fp16x2 words holding (nibble - 8), in order.
-__device__ __forceinline__ void nib4_to_h2(uint32_t nib, uint32_t& lo, uint32_t& hi) {
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
-    uint32_t a = __byte_perm(nib, 0x64646464u, 0x4140u);
-    uint32_t b = __byte_perm(nib, 0x64646464u, 0x4342u);
-    __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
-    __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
-    lo = *reinterpret_cast<uint32_t*>(&ha);
-    hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
 // Four int8 bytes -> two fp16x2 words holding the same integers.
@@ -333,11 +276,7 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
                             {
                                 const uint32_t pair = dav[rr][j];             // scales of blocks 2j, 2j+1
                                 const unsigned short hb = static_cast<unsigned short>(h ? (pair >> 16) : (pair & 0xFFFFu));
-                                if (u < static_cast<uint32_t>(BN)) {
-                                    const uint32_t c = u % CW;                // slot u: group u/CW, i, q, e
-                                    das[(u / CW) * (4 * DA_QPITCH) + ((c & 7u) >> 1) * DA_QPITCH + (c >> 3) * 2 + (c & 1u)] =
-                                        __half2float(__ushort_as_half(hb));
-                                }
+                                if (u < static_cast<uint32_t>(BN)) das[da_index<CW>(u)] = __half2float(__ushort_as_half(hb));
                             }
                             // 16-byte chunk c holds values 8c..8c+7: the low nibbles of q[0..3] are
                             // values 0..15, the high nibbles values 16..31
@@ -494,40 +433,42 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
 }
 
 // --------------------------------------------------------------- gather
-// One warp per router position p: slot s = perm[p] of token t = s / k.  Lane
-// b-strided over the K/32 blocks: 36 bytes of Q8_1 in, 64 bytes of fp16 out
-// (exact integers) and the block's fp16 scale d.  Positions past the routed slots
-// (bad ids, and the padding up to a multiple of 128 rows) are written as zeros.
+// One warp per router position p: slot s = perm[p] of token t = s / k.  The
+// warp walks the token's Q8_1 row as consecutive 4-byte words (coalesced):
+// word 9b of the row is block b's (d, s) pair, words 9b+1 .. 9b+8 its 32 int8
+// values, which become 4 fp16 each (exact integers) at xh[p][32b + 4(w-1)].
+// Positions past the routed slots (bad ids, and the padding up to a multiple
+// of 128 rows) are written as zeros.
 __global__ void __launch_bounds__(256)
     gather_act_kernel(const uint8_t* __restrict__ act, const int32_t* __restrict__ perm,
                       const int32_t* __restrict__ offsets, int32_t n_experts, int32_t top_k, int32_t nb,
-                      int64_t n_rows, uint4* __restrict__ xh, uint16_t* __restrict__ da) {
+                      int64_t n_rows, uint2* __restrict__ xh, uint16_t* __restrict__ da) {
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int64_t n_valid = offsets[n_experts];
     const uint32_t lane = lane_id();
+    const int32_t words = nb * (Q8_1_BYTES / 4);
     for (int64_t p = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); p < n_rows;
          p += warps) {
-        uint4* xrow = xh + p * nb * 4;      // 4 x 16 bytes per block
+        uint2* xrow = xh + p * nb * 8;      // 8 x 8 bytes per block
         uint16_t* drow = da + p * nb;
         if (p < n_valid) {
             const int64_t t = perm[p] / top_k;
             const uint32_t* src = reinterpret_cast<const uint32_t*>(act + t * nb * Q8_1_BYTES);
-            for (int32_t b = lane; b < nb; b += 32) {
-                const uint32_t* blk = src + b * (Q8_1_BYTES / 4);
-                drow[b] = static_cast<uint16_t>(__ldg(blk) & 0xFFFFu);
-                uint32_t hv[16];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) i8x4_to_h2(__ldg(blk + 1 + i), hv[2 * i], hv[2 * i + 1]);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    xrow[b * 4 + c] = make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+#pragma unroll 4
+            for (int32_t j = lane; j < words; j += 32) {
+                const uint32_t v = __ldg(src + j);
+                const int32_t b = j / 9, r = j - 9 * b;
+                if (r == 0) {
+                    drow[b] = static_cast<uint16_t>(v & 0xFFFFu);
+                } else {
+                    uint32_t lo, hi;
+                    i8x4_to_h2(v, lo, hi);
+                    xrow[b * 8 + (r - 1)] = make_uint2(lo, hi);
+                }
             }
         } else {
-            for (int32_t b = lane; b < nb; b += 32) {
-                drow[b] = 0;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) xrow[b * 4 + c] = make_uint4(0, 0, 0, 0);
-            }
+            for (int32_t j = lane; j < nb * 8; j += 32) xrow[j] = make_uint2(0, 0);
+            for (int32_t b = lane; b < nb; b += 32) drow[b] = 0;
         }
     }
 }
@@ -546,7 +487,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
-static int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz,
                      const char* what) {
     auto encode = get_encode_fn();
@@ -562,23 +503,25 @@ static int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
     return FT_OK;
 }
 
+int launch_gather(const uint8_t* act, const int32_t* perm, const int32_t* offsets, int32_t n_experts, int32_t top_k,
+                  int64_t nb, int64_t n_slots, uint16_t* xh, uint16_t* da, cudaStream_t s) {
+    const int64_t rows = gemm_rows(n_slots);
+    const int64_t want = (rows + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
+    const dim3 grid(static_cast<unsigned>(want < cap ? want : cap));
+    gather_act_kernel<<<grid, 256, 0, s>>>(act, perm, offsets, n_experts, top_k, static_cast<int32_t>(nb), rows,
+                                           reinterpret_cast<uint2*>(xh), da);
+    return check_launch("gather_act_kernel", grid, dim3(256), 0);
+}
+
 template <int BN>
-static int launch_gemm_bn(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
-                          const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots,
-                          int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da,
-                          cudaStream_t s) {
+static int launch_gemm_bn(const uint8_t* weights, const int32_t* perm, const int32_t* offsets, const int32_t* tiles,
+                          float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k, int32_t n_experts,
+                          int64_t nrows, int64_t ncols, const uint16_t* xh, const uint16_t* da, cudaStream_t s) {
     using C = Gemm<BN>;
     const int64_t nb = ncols / QK;
     const int sms = sm_count();
     const int64_t rows = gemm_rows(n_slots);
-    {
-        const int64_t want = (rows + 7) / 8;
-        const int64_t cap = static_cast<int64_t>(sms) * 16;
-        const dim3 grid(static_cast<unsigned>(want < cap ? want : cap));
-        gather_act_kernel<<<grid, 256, 0, s>>>(act, perm, offsets, n_experts, top_k, static_cast<int32_t>(nb), rows,
-                                               reinterpret_cast<uint4*>(xh), da);
-        if (int st = check_launch("gather_act_kernel", grid, dim3(256), 0)) return st;
-    }
     CUtensorMap wmap, xmap, smap;
     if (int st = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, weights, nb * Q4_0_BYTES, n_experts * nrows,
                            nb * Q4_0_BYTES, C::KB * Q4_0_BYTES, C::BM, CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
@@ -628,10 +571,11 @@ int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm,
                 const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
                 int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, cudaStream_t s) {
     if (n_slots == 0) return FT_OK;
+    if (int st = launch_gather(act, perm, offsets, n_experts, top_k, ncols / QK, n_slots, xh, da, s)) return st;
     if (gemm_tile_width(n_slots, n_experts) == 32)
-        return launch_gemm_bn<32>(weights, act, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,
+        return launch_gemm_bn<32>(weights, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,
                                   ncols, xh, da, s);
-    return launch_gemm_bn<kGemmBN>(weights, act, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,
+    return launch_gemm_bn<kGemmBN>(weights, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,
                                    ncols, xh, da, s);
 }
 

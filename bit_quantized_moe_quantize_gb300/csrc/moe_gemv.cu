@@ -1,5 +1,8 @@
 // GEMV path of the routed Q4_0 x Q8_1 expert matmul (moe_vec_q4_0_q8_1 on
-// FreeToken PR #185), for batches with few slots per expert (decode).
+// FreeToken PR #185), for batches with few slots per expert (decode).  Two
+// kernels share the launch geometry below: moe_gemv_rows_kernel (one weight
+// row per lane, rows a multiple of 16 bytes, several slot tiles) and
+// moe_gemv_kernel (one block per lane; any row length, and one-token batches).
 //
 // Launch geometry.  grid.x enumerates slot tiles: each is up to G slots of
 // one expert taken from the router's permutation, so grid.x is bounded by
@@ -25,8 +28,7 @@
 // across lanes with shuffles.
 #include <cuda_fp16.h>
 
-#include "ft_common.cuh"
-#include "ft_internal.h"
+#include "gemm_common.cuh"
 
 namespace ft {
 
@@ -58,6 +60,17 @@ __host__ __device__ inline size_t gemv_act_bytes(int G, int nb) {
 }
 __host__ __device__ inline size_t gemv_stage_bytes(int R, int nb) {
     return (static_cast<size_t>(R) * nb * Q4_0_BYTES + 16 + 15) / 16 * 16;
+}
+
+// Row-per-lane kernel's shared memory: full/empty mbarriers [kMaxRowStages]
+// each | slot ids int32[G] | qa [G][nb][32] | aux float2 [G][nb] | ring of
+// boxes (128-byte aligned, 144 x 32 W bytes each).
+constexpr int kMaxRowStages = 8;
+__host__ __device__ inline size_t gemv_rows_qa_offset(int G) {
+    return (16 * kMaxRowStages + static_cast<size_t>(G) * 4 + 15) / 16 * 16;
+}
+__host__ __device__ inline size_t gemv_rows_ring_offset(int G, int nb) {
+    return (gemv_rows_qa_offset(G) + static_cast<size_t>(G) * nb * 40 + 127) / 128 * 128;
 }
 
 __device__ __forceinline__ int32_t find_expert(const int32_t* tiles, int32_t n_experts, int64_t t) {
@@ -259,11 +272,224 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Row-per-lane kernel, for rows that are a whole number of 16-byte chunks
+// (ncols % 256 == 0).  grid.x: slot tiles (G slots of one expert); grid.y:
+// groups of 32 W weight rows of that expert (looping past 65535 groups).
+// Warp w of the W compute warps owns rows 32 w .. 32 w + 31 of the group and
+// lane l one row, so each lane keeps the G partial sums of its row in
+// registers over the whole of K: no cross-lane reduction, and the output
+// store of a warp is 32 consecutive floats.  The weights stream through a
+// ring of TMA boxes of 8 Q4_0 blocks (144 bytes) x 32 W rows, refilled by a
+// producer warp; in shared memory a row of the box is 9 16-byte chunks, an
+// odd count, so the 32 lanes' 16-byte loads of their own rows never collide
+// on a bank.  The G slots' activations are staged once per CTA and every
+// read of them is the same address for the whole warp (a broadcast).
+template <int G, bool DUMP>
+__global__ void __launch_bounds__(160) moe_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                             const GemvArgs a) {
+    constexpr int KB = 8;                                 // blocks per box
+    constexpr int BOX_ROW = KB * Q4_0_BYTES;              // 144
+    const int32_t W = static_cast<int32_t>(blockDim.x >> 5) - 1;
+    const int64_t t = blockIdx.x;
+    const int32_t E = a.n_experts;
+    if (t >= a.tiles[E]) return;
+    const int32_t e = find_expert(a.tiles, E, t);
+    const int64_t p0 = static_cast<int64_t>(a.offsets[e]) + (t - a.tiles[e]) * G;
+    const int32_t ng = static_cast<int32_t>(min(static_cast<int64_t>(G), a.offsets[e + 1] - p0));
+    const int32_t nb = a.nb;
+    const int32_t n_ks = nb / KB;
+    const int NS = a.stages;
+    const int64_t n_groups = (a.nrows + 32 * W - 1) / (32 * W);
+    const int64_t my_groups = blockIdx.y < n_groups ? (n_groups - 1 - blockIdx.y) / gridDim.y + 1 : 0;
+    const int64_t n_it = my_groups * n_ks;                // boxes this CTA consumes, in order
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kMaxRowStages;
+    int32_t* slot = reinterpret_cast<int32_t*>(smem + 16 * kMaxRowStages);
+    uint4* qa = reinterpret_cast<uint4*>(smem + gemv_rows_qa_offset(G));         // [G][nb][2] uint4
+    float2* aux = reinterpret_cast<float2*>(qa + static_cast<size_t>(G) * nb * 2);  // [G][nb] {d_a, 8 sum q}
+    uint8_t* ring = smem + gemv_rows_ring_offset(G, nb);
+    const uint32_t stage_bytes = static_cast<uint32_t>(BOX_ROW * 32 * W);
+
+    const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], W);
+        }
+        fence_mbar_init();
+    }
+    if (threadIdx.x < G) slot[threadIdx.x] = threadIdx.x < ng ? a.perm[p0 + threadIdx.x] : 0;
+    __syncthreads();
+
+    // stage the G activation rows once: 32 int8 as two 16-byte chunks, and
+    // {d_a, 8 * sum q} so that each block dot starts from -8 sum q
+    for (int32_t i = threadIdx.x; i < G * nb; i += blockDim.x) {
+        const int32_t g = i / nb, b = i - g * nb;
+        uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
+        float d = 0.0f;
+        int sm = 0;
+        if (g < ng) {
+            const int64_t tok = slot[g] / a.top_k;
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(a.act + (tok * nb + b) * Q8_1_BYTES);
+            const uint32_t ds = __ldg(src);
+            q0 = make_uint4(__ldg(src + 1), __ldg(src + 2), __ldg(src + 3), __ldg(src + 4));
+            q1 = make_uint4(__ldg(src + 5), __ldg(src + 6), __ldg(src + 7), __ldg(src + 8));
+            d = __half2float(__ushort_as_half(static_cast<unsigned short>(ds & 0xFFFFu)));
+            sm = __dp4a(static_cast<int>(q0.x), 0x01010101, sm);
+            sm = __dp4a(static_cast<int>(q0.y), 0x01010101, sm);
+            sm = __dp4a(static_cast<int>(q0.z), 0x01010101, sm);
+            sm = __dp4a(static_cast<int>(q0.w), 0x01010101, sm);
+            sm = __dp4a(static_cast<int>(q1.x), 0x01010101, sm);
+            sm = __dp4a(static_cast<int>(q1.y), 0x01010101, sm);
+            sm = __dp4a(static_cast<int>(q1.z), 0x01010101, sm);
+            sm = __dp4a(static_cast<int>(q1.w), 0x01010101, sm);
+        }
+        qa[(static_cast<size_t>(g) * nb + b) * 2] = q0;
+        qa[(static_cast<size_t>(g) * nb + b) * 2 + 1] = q1;
+        aux[static_cast<size_t>(g) * nb + b] = make_float2(d, __int_as_float(8 * sm));
+    }
+    __syncthreads();
+
+    const int64_t erow0 = static_cast<int64_t>(e) * a.nrows;   // first weight row of the expert
+    if (static_cast<int32_t>(warp) == W) {
+        // ------------------------------------------------------------ producer
+        int64_t grp = blockIdx.y;
+        int32_t ks = 0;
+        for (int64_t it = 0; it < n_it; ++it) {
+            const int32_t s = static_cast<int32_t>(it % NS);
+            if (!mbar_wait_warp(&empty[s], static_cast<uint32_t>(((it / NS) & 1) ^ 1), a.err)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[s], stage_bytes);
+                tma_load_2d(ring + static_cast<size_t>(s) * stage_bytes, &wmap, ks * BOX_ROW,
+                            static_cast<int32_t>(erow0 + grp * 32 * W), &full[s]);
+            }
+            __syncwarp();
+            if (++ks == n_ks) {
+                ks = 0;
+                grp += gridDim.y;
+            }
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------------- compute
+    int64_t grp = blockIdx.y;
+    int32_t ks = 0;
+    float acc[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) acc[g] = 0.0f;
+    for (int64_t it = 0; it < n_it; ++it) {
+        const int32_t s = static_cast<int32_t>(it % NS);
+        if (!mbar_wait_warp(&full[s], static_cast<uint32_t>((it / NS) & 1), a.err)) break;
+        const uint4* rowp = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * stage_bytes +
+                                                           (warp * 32 + lane) * BOX_ROW);
+        uint32_t wv[36];
+#pragma unroll
+        for (int c = 0; c < 9; ++c) {
+            const uint4 v = rowp[c];
+            wv[4 * c] = v.x;
+            wv[4 * c + 1] = v.y;
+            wv[4 * c + 2] = v.z;
+            wv[4 * c + 3] = v.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);            // the box now lives in registers
+        const int64_t row = grp * 32 * W + warp * 32 + lane;   // row within the expert
+#pragma unroll
+        for (int j = 0; j < KB; ++j) {
+            // block j of the box starts at byte 18 j: word 9j/2 (j even, d in its
+            // low half) or the high half of word (18j - 2)/4 (j odd)
+            uint32_t q[4], dbits;
+            if ((j & 1) == 0) {
+                const int w0 = 9 * j / 2;
+                dbits = wv[w0] & 0xFFFFu;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) q[i] = __byte_perm(wv[w0 + i], wv[w0 + i + 1], 0x5432u);
+            } else {
+                const int w0 = (18 * j - 2) / 4;
+                dbits = wv[w0] >> 16;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) q[i] = wv[w0 + 1 + i];
+            }
+            const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
+            int lo[4], hi[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                lo[i] = static_cast<int>(q[i] & 0x0F0F0F0Fu);          // values 4i .. 4i+3
+                hi[i] = static_cast<int>((q[i] >> 4) & 0x0F0F0F0Fu);   // values 16+4i .. 16+4i+3
+            }
+            const int32_t b = ks * KB + j;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint4 A0 = qa[(static_cast<size_t>(g) * nb + b) * 2];
+                const uint4 A1 = qa[(static_cast<size_t>(g) * nb + b) * 2 + 1];
+                const float2 x = aux[static_cast<size_t>(g) * nb + b];
+                int dot = -__float_as_int(x.y);
+                dot = __dp4a(lo[0], static_cast<int>(A0.x), dot);
+                dot = __dp4a(lo[1], static_cast<int>(A0.y), dot);
+                dot = __dp4a(lo[2], static_cast<int>(A0.z), dot);
+                dot = __dp4a(lo[3], static_cast<int>(A0.w), dot);
+                dot = __dp4a(hi[0], static_cast<int>(A1.x), dot);
+                dot = __dp4a(hi[1], static_cast<int>(A1.y), dot);
+                dot = __dp4a(hi[2], static_cast<int>(A1.z), dot);
+                dot = __dp4a(hi[3], static_cast<int>(A1.w), dot);
+                if constexpr (DUMP) {
+                    if (g < ng && row < a.nrows) a.dots[(static_cast<int64_t>(slot[g]) * a.nrows + row) * nb + b] = dot;
+                } else {
+                    acc[g] = fmaf(small_int_to_float(dot), dw * x.x, acc[g]);
+                }
+            }
+        }
+        if (++ks == n_ks) {                                // end of the row group: store, next group
+            if constexpr (!DUMP) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    if (g < ng && row < a.nrows) a.out[static_cast<int64_t>(slot[g]) * a.nrows + row] = acc[g];
+                    acc[g] = 0.0f;
+                }
+            }
+            ks = 0;
+            grp += gridDim.y;
+        }
+    }
+}
+
 GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols) {
     GemvPlan p{};
     const int64_t nb = ncols / QK;
     const double mean = static_cast<double>(n_slots) / n_experts;
     p.group = mean <= 1.0 ? 1 : mean <= 2.0 ? 2 : mean <= 4.0 ? 4 : 8;
+    if (ncols % 256 == 0 && (p.group >= 2 || (n_slots + p.group - 1) / p.group >= 32)) {
+        // row-per-lane kernel: warps of 32 rows, as many per CTA (up to 4) as
+        // still leaves two CTAs per SM, and a ring as deep as ~110 KB allows.
+        // With a handful of single-slot tiles (one token) it would leave most
+        // SMs with one or two warps; the block-per-lane kernel below spreads
+        // such a batch over every SM instead.
+        const int64_t min_tiles = (n_slots + p.group - 1) / p.group;
+        const int64_t groups32 = (nrows + 31) / 32;
+        const int64_t sms = sm_count();
+        p.row_warps = 1;
+        for (int w = 4; w > 1; w >>= 1)
+            if (min_tiles * ((groups32 + w - 1) / w) >= 2 * sms) {
+                p.row_warps = w;
+                break;
+            }
+        const size_t ring0 = gemv_rows_ring_offset(p.group, static_cast<int>(nb));
+        const size_t stage = static_cast<size_t>(144) * 32 * p.row_warps;
+        const size_t budget = 110 * 1024;
+        int st = budget > ring0 ? static_cast<int>((budget - ring0) / stage) : 0;
+        st = st < 2 ? 2 : st > kMaxRowStages ? kMaxRowStages : st;
+        p.stages = st;
+        p.smem = ring0 + static_cast<size_t>(st) * stage;
+        const int64_t ub = (n_slots + p.group - 1) / p.group + (n_experts < n_slots ? n_experts : n_slots);
+        p.grid_x = ub < n_slots ? ub : n_slots;
+        const int64_t ng = (nrows + 32 * p.row_warps - 1) / (32 * p.row_warps);
+        p.row_tiles = ng < 65535 ? ng : 65535;
+        return p;
+    }
     const int64_t row_bytes = nb * Q4_0_BYTES;
     // rows per warp: a stage of 8 * RW rows of about 40 KB
     const int64_t rw = 40960 / (8 * row_bytes);
@@ -314,6 +540,16 @@ static int launch_gemv_rw(const GemvPlan& plan, const GemvArgs& a, cudaStream_t 
     }
 }
 
+template <int G, bool DUMP>
+static int launch_gemv_rows(const GemvPlan& plan, const CUtensorMap& wmap, const GemvArgs& a, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(plan.grid_x), static_cast<unsigned>(plan.row_tiles));
+    const dim3 block(32 * (plan.row_warps + 1));
+    if (int st = set_smem_limit(reinterpret_cast<const void*>(moe_gemv_rows_kernel<G, DUMP>), static_cast<int>(plan.smem)))
+        return st;
+    moe_gemv_rows_kernel<G, DUMP><<<grid, block, plan.smem, s>>>(wmap, a);
+    return check_launch(DUMP ? "moe_gemv_rows_kernel<dump>" : "moe_gemv_rows_kernel", grid, block, plan.smem);
+}
+
 int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act, const int32_t* perm,
                 const int32_t* offsets, const int32_t* tiles, float* out, int32_t* dots, uint32_t* err,
                 int64_t n_slots, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols, cudaStream_t s) {
@@ -336,6 +572,19 @@ int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act
     a.bulk = ((a.nb * Q4_0_BYTES) % 16 == 0) && ((reinterpret_cast<uintptr_t>(weights) & 15u) == 0);
     (void)n_slots;
     const bool dump = dots != nullptr;
+    if (plan.row_warps > 0) {
+        CUtensorMap wmap;
+        if (int st = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, weights, a.nb * Q4_0_BYTES,
+                               static_cast<uint64_t>(n_experts) * nrows, a.nb * Q4_0_BYTES, 144, 32 * plan.row_warps,
+                               CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
+            return st;
+        switch (plan.group) {
+            case 1: return dump ? launch_gemv_rows<1, true>(plan, wmap, a, s) : launch_gemv_rows<1, false>(plan, wmap, a, s);
+            case 2: return dump ? launch_gemv_rows<2, true>(plan, wmap, a, s) : launch_gemv_rows<2, false>(plan, wmap, a, s);
+            case 4: return dump ? launch_gemv_rows<4, true>(plan, wmap, a, s) : launch_gemv_rows<4, false>(plan, wmap, a, s);
+            default: return dump ? launch_gemv_rows<8, true>(plan, wmap, a, s) : launch_gemv_rows<8, false>(plan, wmap, a, s);
+        }
+    }
     switch (plan.group) {
         case 1: return dump ? launch_gemv_rw<1, true>(plan, a, s) : launch_gemv_rw<1, false>(plan, a, s);
         case 2: return dump ? launch_gemv_rw<2, true>(plan, a, s) : launch_gemv_rw<2, false>(plan, a, s);

@@ -172,7 +172,10 @@ def test_ragged_full_compare(path, oracle, E, k, K, N, T, seed, path_name):
     G.check_close(got, ref, wn, xn, f"ragged {E},{k},{K},{N},{T}/{path_name}")
 
 
-@pytest.mark.parametrize("E,k,K,N,T,seed", [(5, 2, 512, 200, 77, 11), (16, 4, 256, 64, 129, 13)])
+# the first two take the 32-wide tensor-core tiles (few slots per expert), the
+# last two the 128-wide tiles on widened weights (many slots per expert)
+@pytest.mark.parametrize("E,k,K,N,T,seed", [(5, 2, 512, 200, 77, 11), (16, 4, 256, 64, 129, 13),
+                                            (3, 3, 768, 130, 300, 12), (2, 1, 4096, 260, 400, 14)])
 @pytest.mark.parametrize("path_name", ["gemv", "gemm"])
 def test_ragged_block_dots(path, oracle, E, k, K, N, T, seed, path_name):
     w, x, ids = _custom(E, k, K, N, T, seed, zero_rows=True)
@@ -277,17 +280,19 @@ def test_deterministic(path, oracle):
         assert np.array_equal(r1, r2)
 
 
-def test_graph_capture_replay(path, oracle):
+@pytest.mark.parametrize("T", [300, 1000])
+def test_graph_capture_replay(path, oracle, T):
     """Quantize + route + matmul captured in a CUDA graph and replayed give the
-    eager result bit for bit (no allocation or host sync inside)."""
+    eager result bit for bit (no allocation or host sync inside).  T = 300
+    takes the 32-wide tensor-core tiles, T = 1000 the widened-weight ones."""
     import torch
-    w, x, ids = _custom(8, 2, 512, 256, 300, 60)
+    w, x, ids = _custom(8, 2, 512, 256, T, 60)
     dw, dx, di = G.dev(w), G.dev(x), G.dev(ids)
     for p in ("gemv", "gemm"):
         path.set_path(p)
-        path.reserve(300, 2, 8, 256, 512)
-        act = torch.empty((300, 16, 36), dtype=torch.uint8, device="cuda")
-        out = torch.empty((300, 2, 256), dtype=torch.float32, device="cuda")
+        path.reserve(T, 2, 8, 256, 512)
+        act = torch.empty((T, 16, 36), dtype=torch.uint8, device="cuda")
+        out = torch.empty((T, 2, 256), dtype=torch.float32, device="cuda")
         path.quantize_q8_1(dx, out=act)
         path.moe_q4_0_q8_1(dw, act, di, out=out)
         eager = G.host(out).copy()

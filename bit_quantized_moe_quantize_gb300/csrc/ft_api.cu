@@ -345,6 +345,12 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     if (int st = launch_route(topk_ids, sh.n_slots, sh.n_experts, rb, gp.group, gemm_tile_width(sh.n_slots, sh.n_experts),
                               zero_rows, row_words, s))
         return st;
+    if (path == FT_PATH_GEMM && sh.n_slots > 0) {
+        if (int st = launch_gather(static_cast<const uint8_t*>(act), rb.perm, rb.offsets, sh.n_experts, sh.top_k,
+                                   sh.nb, sh.n_slots, reinterpret_cast<uint16_t*>(ws + L.xh),
+                                   reinterpret_cast<uint16_t*>(ws + L.da), s))
+            return st;
+    }
     prof_mark(kProfMatmulBegin, s);
     int st;
     if (path == FT_PATH_GEMV)

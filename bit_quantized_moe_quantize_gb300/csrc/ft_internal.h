@@ -78,8 +78,10 @@ int gemm_tile_width(int64_t n_slots, int32_t n_experts);
 inline int64_t gemm_rows(int64_t n_slots) { return (n_slots + kGemmBN - 1) / kGemmBN * kGemmBN; }
 
 // xh: [S_pad][ncols] fp16 and da: [S_pad][ncols/32] fp16 workspace for the
-// routed activations in router order, S_pad = gemm_rows(S) (written by the
-// gather kernel, zero past the routed slots, read by TMA).
+// routed activations in router order, S_pad = gemm_rows(S): written by
+// launch_gather (zero past the routed slots), then read by the GEMM's TMA.
+int launch_gather(const uint8_t* act, const int32_t* perm, const int32_t* offsets, int32_t n_experts, int32_t top_k,
+                  int64_t nb, int64_t n_slots, uint16_t* xh, uint16_t* da, cudaStream_t s);
 int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
                 const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
                 int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, cudaStream_t s);

@@ -85,8 +85,4 @@ __device__ __forceinline__ uint32_t da_index(uint32_t c) {
 int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz, const char* what);
 
-// Routed activations in router order, as fp16 rows plus fp16 block scales.
-int launch_gather(const uint8_t* act, const int32_t* perm, const int32_t* offsets, int32_t n_experts, int32_t top_k,
-                  int64_t nb, int64_t n_slots, uint16_t* xh, uint16_t* da, cudaStream_t s);
-
 }  // namespace ft

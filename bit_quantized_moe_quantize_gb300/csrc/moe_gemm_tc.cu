@@ -570,8 +570,8 @@ int gemm_tile_width(int64_t n_slots, int32_t n_experts) {
 int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
                 const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
                 int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, cudaStream_t s) {
+    (void)act;   // read by launch_gather, which the caller runs first
     if (n_slots == 0) return FT_OK;
-    if (int st = launch_gather(act, perm, offsets, n_experts, top_k, ncols / QK, n_slots, xh, da, s)) return st;
     if (gemm_tile_width(n_slots, n_experts) == 32)
         return launch_gemm_bn<32>(weights, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,
                                   ncols, xh, da, s);

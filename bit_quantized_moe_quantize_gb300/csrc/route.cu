@@ -9,16 +9,22 @@
 // the prefix over experts of the number of slot tiles (ceil(count / group)),
 // which lets the matmul kernels enumerate their tiles on the device.
 //
-// Three launches, always, whatever the data: no host read-back, no
-// allocation, nothing that depends on device values on the host side, so
-// the router can be captured in a CUDA graph (CURRENT_BUG.md, "Cudagraph
-// Constraints").  No atomics on global counters: each warp owns a chunk of
-// 256 slots and a private histogram row, so every result is deterministic.
+// A fixed number of launches for a given shape, whatever the data: no host
+// read-back, no allocation, nothing that depends on device values on the
+// host side, so the router can be captured in a CUDA graph (CURRENT_BUG.md,
+// "Cudagraph Constraints").  No atomics on global counters: each warp owns a
+// chunk of 256 slots and a private histogram row, so every result is
+// deterministic.
 //
 //   1. route_hist:    per chunk, histogram of expert ids -> hist[chunk][e]
 //   2. route_scan:    one CTA: counts, offsets, tile prefixes, and hist
 //                     rewritten in place as each chunk's first position per e
 //   3. route_scatter: per chunk, stable placement with __match_any_sync ranks
+//
+// Batches of at most 32 chunks whose histograms fit in shared memory (decode)
+// run the same three steps inside one CTA (route_small_kernel), with the
+// histogram in shared memory: one launch instead of three, which is most of
+// the routing time when the batch is small.
 #include <mutex>
 
 #include "ft_common.cuh"
@@ -32,14 +38,11 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
-__global__ void __launch_bounds__(32 * kRouteWarps)
-    route_hist_kernel(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts, int64_t n_chunks,
-                      int32_t* __restrict__ hist, uint32_t* err) {
-    extern __shared__ int32_t sh_hist[];
-    const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-    const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
-    if (chunk >= n_chunks) return;
-    int32_t* row = sh_hist + static_cast<int64_t>(warp) * n_experts;
+// Step 1 for one warp and its chunk: histogram of the chunk's expert ids in
+// row[E] (shared memory), bad ids flagged in err.
+__device__ void route_hist_chunk(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts, int64_t chunk,
+                                 int32_t* row, uint32_t* err) {
+    const uint32_t lane = lane_id();
     for (int32_t e = lane; e < n_experts; e += 32) row[e] = 0;
     __syncwarp();
     bool saw_bad = false;
@@ -53,6 +56,18 @@ __global__ void __launch_bounds__(32 * kRouteWarps)
         __syncwarp();
     }
     if (__any_sync(0xFFFFFFFFu, saw_bad) && lane == 0) atomicOr(err, FT_DEVERR_BAD_EXPERT_ID);
+    __syncwarp();
+}
+
+__global__ void __launch_bounds__(32 * kRouteWarps)
+    route_hist_kernel(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts, int64_t n_chunks,
+                      int32_t* __restrict__ hist, uint32_t* err) {
+    extern __shared__ int32_t sh_hist[];
+    const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+    const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
+    if (chunk >= n_chunks) return;
+    int32_t* row = sh_hist + static_cast<int64_t>(warp) * n_experts;
+    route_hist_chunk(ids, n_slots, n_experts, chunk, row, err);
     int32_t* grow = hist + chunk * n_experts;
     for (int32_t e = lane; e < n_experts; e += 32) grow[e] = row[e];
 }
@@ -97,12 +112,11 @@ __device__ int32_t block_exclusive_scan(int32_t* v, int32_t n, int32_t* scratch)
     return total;
 }
 
-// One CTA of 1024 threads.  Shared: part[P][E] + tot[E] + tiles[E] + 32.
-__global__ void __launch_bounds__(1024)
-    route_scan_kernel(int32_t* __restrict__ hist, int64_t n_chunks, int32_t n_experts, int32_t* __restrict__ counts,
-                      int32_t* __restrict__ offsets, int32_t* __restrict__ tiles_gemv, int32_t gemv_group,
-                      int32_t* __restrict__ tiles_gemm, int32_t gemm_group) {
-    extern __shared__ int32_t sh[];
+// Step 2 by one CTA of 1024 threads on hist[n_chunks][E] (global or shared
+// memory).  sh: part[P][E] + tot[E] + tiles[E] + 32 ints.
+__device__ void route_scan_body(int32_t* hist, int64_t n_chunks, int32_t n_experts, int32_t* __restrict__ counts,
+                                int32_t* __restrict__ offsets, int32_t* __restrict__ tiles_gemv, int32_t gemv_group,
+                                int32_t* __restrict__ tiles_gemm, int32_t gemm_group, int32_t* sh) {
     const int32_t E = n_experts, nt = blockDim.x, tid = threadIdx.x;
     const int32_t P = E >= nt ? 1 : nt / E;                 // parts per expert
     int32_t* part = sh;                                     // [P][E]
@@ -168,26 +182,21 @@ __global__ void __launch_bounds__(1024)
     }
 }
 
-__global__ void __launch_bounds__(32 * kRouteWarps)
-    route_scatter_kernel(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts, int64_t n_chunks,
-                         const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
-                         int32_t* __restrict__ perm, uint32_t* __restrict__ zero_rows, int64_t row_words) {
-    extern __shared__ int32_t sh_cursor[];
-    const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-    // tail of perm: positions past the valid slots are -1
-    {
-        const int64_t n_valid = offsets[n_experts];
-        const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-        for (int64_t p = n_valid + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; p < n_slots;
-             p += stride)
-            perm[p] = -1;
-    }
-    const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
-    if (chunk >= n_chunks) return;
-    int32_t* cur = sh_cursor + static_cast<int64_t>(warp) * n_experts;
-    const int32_t* brow = base + chunk * n_experts;
-    for (int32_t e = lane; e < n_experts; e += 32) cur[e] = brow[e];
-    __syncwarp();
+// One CTA of 1024 threads.  Shared: part[P][E] + tot[E] + tiles[E] + 32.
+__global__ void __launch_bounds__(1024)
+    route_scan_kernel(int32_t* __restrict__ hist, int64_t n_chunks, int32_t n_experts, int32_t* __restrict__ counts,
+                      int32_t* __restrict__ offsets, int32_t* __restrict__ tiles_gemv, int32_t gemv_group,
+                      int32_t* __restrict__ tiles_gemm, int32_t gemm_group) {
+    extern __shared__ int32_t sh[];
+    route_scan_body(hist, n_chunks, n_experts, counts, offsets, tiles_gemv, gemv_group, tiles_gemm, gemm_group, sh);
+}
+
+// Step 3 for one warp and its chunk: cur[E] (shared memory) starts as the
+// chunk's first position per expert.
+__device__ void route_scatter_chunk(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts,
+                                    int64_t chunk, int32_t* cur, int32_t* __restrict__ perm,
+                                    uint32_t* __restrict__ zero_rows, int64_t row_words) {
+    const uint32_t lane = lane_id();
     for (int step = 0; step < kRouteChunk / 32; ++step) {
         const int64_t s = chunk * kRouteChunk + step * 32 + lane;
         const int32_t e = s < n_slots ? ids[s] : -1;
@@ -206,6 +215,51 @@ __global__ void __launch_bounds__(32 * kRouteWarps)
     }
 }
 
+// Positions past the valid slots are -1 (threads tid, tid + nt, ...).
+__device__ __forceinline__ void route_perm_tail(const int32_t* __restrict__ offsets, int32_t n_experts,
+                                                int64_t n_slots, int32_t* __restrict__ perm, int64_t tid, int64_t nt) {
+    const int64_t n_valid = offsets[n_experts];
+    for (int64_t p = n_valid + tid; p < n_slots; p += nt) perm[p] = -1;
+}
+
+__global__ void __launch_bounds__(32 * kRouteWarps)
+    route_scatter_kernel(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts, int64_t n_chunks,
+                         const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ perm, uint32_t* __restrict__ zero_rows, int64_t row_words) {
+    extern __shared__ int32_t sh_cursor[];
+    const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+    route_perm_tail(offsets, n_experts, n_slots, perm, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+                    static_cast<int64_t>(gridDim.x) * blockDim.x);
+    const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
+    if (chunk >= n_chunks) return;
+    int32_t* cur = sh_cursor + static_cast<int64_t>(warp) * n_experts;
+    const int32_t* brow = base + chunk * n_experts;
+    for (int32_t e = lane; e < n_experts; e += 32) cur[e] = brow[e];
+    __syncwarp();
+    route_scatter_chunk(ids, n_slots, n_experts, chunk, cur, perm, zero_rows, row_words);
+}
+
+// All three steps in one CTA of 1024 threads (32 warps, one chunk each) for
+// n_chunks <= 32.  Shared: hist[n_chunks][E], then the scan's part/tot/tiles.
+__global__ void __launch_bounds__(1024)
+    route_small_kernel(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts, int64_t n_chunks,
+                       int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                       int32_t* __restrict__ tiles_gemv, int32_t gemv_group, int32_t* __restrict__ tiles_gemm,
+                       int32_t gemm_group, uint32_t* err, uint32_t* __restrict__ zero_rows, int64_t row_words) {
+    extern __shared__ int32_t sh_small[];
+    int32_t* hist = sh_small;                                            // [n_chunks][E]
+    int32_t* scan_sh = sh_small + n_chunks * static_cast<int64_t>(n_experts);
+    const uint32_t warp = threadIdx.x >> 5;
+    if (warp < n_chunks) route_hist_chunk(ids, n_slots, n_experts, warp, hist + warp * n_experts, err);
+    __syncthreads();
+    route_scan_body(hist, n_chunks, n_experts, counts, offsets, tiles_gemv, gemv_group, tiles_gemm, gemm_group,
+                    scan_sh);
+    __syncthreads();
+    route_perm_tail(offsets, n_experts, n_slots, perm, threadIdx.x, blockDim.x);
+    if (warp < n_chunks) route_scatter_chunk(ids, n_slots, n_experts, warp, hist + warp * n_experts, perm, zero_rows,
+                                             row_words);
+}
+
 int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const RouteBuffers& b,
                  int32_t gemv_group, int32_t gemm_group, uint32_t* zero_rows, int64_t row_words, cudaStream_t s) {
     {
@@ -215,6 +269,17 @@ int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const R
         if (int st = set_smem_limit(reinterpret_cast<const void*>(route_scatter_kernel), big)) return st;
     }
     const int64_t n_chunks = route_chunks(n_slots);
+    const int32_t P = n_experts >= 1024 ? 1 : 1024 / n_experts;
+    const size_t scan_sm = (static_cast<size_t>(P) * n_experts + 2 * static_cast<size_t>(n_experts) + 32) *
+                           sizeof(int32_t);
+    if (n_chunks <= 32 && n_chunks * n_experts <= 16384) {
+        const size_t sm = static_cast<size_t>(n_chunks) * n_experts * sizeof(int32_t) + scan_sm;
+        if (int st = set_smem_limit(reinterpret_cast<const void*>(route_small_kernel), static_cast<int>(sm))) return st;
+        route_small_kernel<<<1, 1024, sm, s>>>(ids, n_slots, n_experts, n_chunks, b.counts, b.offsets, b.perm,
+                                               b.tiles_gemv, gemv_group, b.tiles_gemm, gemm_group, b.err, zero_rows,
+                                               row_words);
+        return check_launch("route_small_kernel", dim3(1), dim3(1024), sm);
+    }
     const int64_t ctas = (n_chunks + kRouteWarps - 1) / kRouteWarps;
     const dim3 block(32 * kRouteWarps);
     const size_t sm_rows = static_cast<size_t>(kRouteWarps) * n_experts * sizeof(int32_t);
@@ -223,14 +288,9 @@ int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const R
         route_hist_kernel<<<grid, block, sm_rows, s>>>(ids, n_slots, n_experts, n_chunks, b.hist, b.err);
         if (int st = check_launch("route_hist_kernel", grid, block, sm_rows)) return st;
     }
-    {
-        const int32_t P = n_experts >= 1024 ? 1 : 1024 / n_experts;
-        const size_t sm = (static_cast<size_t>(P) * n_experts + 2 * static_cast<size_t>(n_experts) + 32) *
-                          sizeof(int32_t);
-        route_scan_kernel<<<1, 1024, sm, s>>>(b.hist, n_chunks, n_experts, b.counts, b.offsets, b.tiles_gemv,
-                                              gemv_group, b.tiles_gemm, gemm_group);
-        if (int st = check_launch("route_scan_kernel", dim3(1), dim3(1024), sm)) return st;
-    }
+    route_scan_kernel<<<1, 1024, scan_sm, s>>>(b.hist, n_chunks, n_experts, b.counts, b.offsets, b.tiles_gemv,
+                                               gemv_group, b.tiles_gemm, gemm_group);
+    if (int st = check_launch("route_scan_kernel", dim3(1), dim3(1024), scan_sm)) return st;
     if (ctas > 0) {
         const dim3 grid(static_cast<unsigned>(ctas));
         route_scatter_kernel<<<grid, block, sm_rows, s>>>(ids, n_slots, n_experts, n_chunks, b.hist, b.offsets,

@@ -235,13 +235,16 @@ FT_API int ft_moe_block_dots(const void* weights, const void* act, const int32_t
 
 /*
  * Profiling.  ft_profile_enable(max_calls) starts recording, on the stream
- * each call launches on, CUDA events around the quantizer kernel and around
- * the routing and matmul kernels of each later call (up to max_calls calls;
- * 0 stops recording).  It allocates the events, so call it outside stream
- * capture.  ft_profile_read synchronizes on the recorded events and returns
- * the summed kernel times (milliseconds), the number of calls recorded and the
- * number of kernels this library launched since recording started, then
- * resets the totals.  Per-process state, meant for benchmarks.
+ * each call launches on, CUDA events around the quantizer kernel and, in each
+ * later matmul call, around its preparation (routing, plus on the tensor-core
+ * path the gather of the routed activations into the MMA operand layout) and
+ * around its matmul kernel (up to max_calls calls; 0 stops recording).  It
+ * allocates the events, so call it outside stream capture.  ft_profile_read
+ * synchronizes on the recorded events and returns the summed times
+ * (milliseconds) as quantize_ms, route_ms (the preparation) and matmul_ms
+ * (the matmul kernel alone), the number of calls recorded and the number of
+ * kernels this library launched since recording started, then resets the
+ * totals.  Per-process state, meant for benchmarks.
  */
 FT_API int ft_profile_enable(int32_t max_calls);
 FT_API int ft_profile_read(double* quantize_ms, double* route_ms, double* matmul_ms, int64_t* n_calls,

@@ -506,8 +506,8 @@ int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64
 int launch_gather(const uint8_t* act, const int32_t* perm, const int32_t* offsets, int32_t n_experts, int32_t top_k,
                   int64_t nb, int64_t n_slots, uint16_t* xh, uint16_t* da, cudaStream_t s) {
     const int64_t rows = gemm_rows(n_slots);
-    const int64_t want = (rows + 7) / 8;
-    const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
+    const int64_t want = (rows + 7) / 8;   // one warp per row, all rows at once
+    const int64_t cap = 0x7FFFFFFF;
     const dim3 grid(static_cast<unsigned>(want < cap ? want : cap));
     gather_act_kernel<<<grid, 256, 0, s>>>(act, perm, offsets, n_experts, top_k, static_cast<int32_t>(nb), rows,
                                            reinterpret_cast<uint2*>(xh), da);

@@ -68,9 +68,10 @@ int launch_quantize_q8_1(const void* x, void* act, int64_t tokens, int64_t ncols
     const int64_t n_blocks = tokens * (ncols / QK);
     if (n_blocks == 0) return FT_OK;
     const int threads = 256;
-    const int sms = sm_count();
+    // one thread per 8-byte load: every load of the batch is issued at once
+    // (grid.x up to 2^31 - 1; larger batches take the grid-stride loop)
     const int64_t want = (n_blocks * 8 + threads - 1) / threads;
-    const int64_t cap = static_cast<int64_t>(sms) * 16;
+    const int64_t cap = 0x7FFFFFFF;
     const dim3 grid(static_cast<unsigned>(want < cap ? want : cap));
     quantize_q8_1_kernel<<<grid, threads, 0, s>>>(static_cast<const uint2*>(x), static_cast<uint8_t*>(act),
                                                   n_blocks);

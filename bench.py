@@ -392,10 +392,8 @@ def ours(args):
                 "algorithmic": f"2*S*N*K = {flops:.4g} FLOP per launch", "kernel_ms": mm_ms}
     else:
         # the library's GEMV plan: one weight row per lane when rows are whole
-        # 16-byte chunks and the batch has several slot tiles, else one block per lane
-        mean = S / E
-        group = 1 if mean <= 1 else 2 if mean <= 2 else 4 if mean <= 4 else 8
-        kern = "moe_gemv_rows_kernel" if K % 256 == 0 and (group >= 2 or -(-S // group) >= 32) else "moe_gemv_kernel"
+        # 16-byte chunks, else one block per lane
+        kern = "moe_gemv_rows_kernel" if K % 256 == 0 else "moe_gemv_kernel"
         achieved = alg_bytes / (mm_ms / 1000.0) / 1e9
         roof = {"kernel": kern, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_note": f"copy bandwidth, of {peak_src}",

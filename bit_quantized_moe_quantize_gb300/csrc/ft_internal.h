@@ -51,7 +51,9 @@ int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const R
 // ------------------------------------------------------------------ GEMV
 struct GemvPlan {
     int group;            // slots per tile (1, 2, 4 or 8)
-    int row_warps;        // row-per-lane kernel: compute warps of 32 rows each (0: the block-per-lane kernel)
+    int row_warps;        // row-per-lane kernel: row groups of 32 per CTA (0: the block-per-lane kernel)
+    int ksplit;           // row-per-lane kernel: warps that share a row group
+    int64_t min_tiles;    // slot tiles the batch has at least (ceil(S / group))
     int rows;             // weight rows per stage (8 * rows per warp)
     int lanes_per_row;    // rows per warp per stage (1, 2 or 4)
     int stages;           // depth of the bulk-copy ring

@@ -46,9 +46,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 PAGES_T4_TOKENS_PER_S = {("prefill", 8191): 8191 / 0.7058, ("prefill", 4096): 4096 / 0.3461,
                          ("prefill", 2048): 2048 / 0.1740}
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
-# capture (profiles/moe_gemm_tc_prefill_8191.md), keyed by the library source
-# hash it was taken on, so a changed kernel reports null instead.
-NCU_TRAFFIC = {("moe_gemm_tc_kernel", "ffe0d2e9e4281bb3", "prefill:8191"): 666607872 + 341066752}
+# capture (profiles/moe_gemm_tc_prefill.md), keyed by the library source hash
+# it was taken on, so a changed kernel reports null instead.
+NCU_TRAFFIC = {("moe_gemm_tc_kernel", "4692f6fb6c110585", "prefill:8191"): 666574848 + 340576256}
 
 
 def parse():

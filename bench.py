@@ -46,9 +46,22 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 PAGES_T4_TOKENS_PER_S = {("prefill", 8191): 8191 / 0.7058, ("prefill", 4096): 4096 / 0.3461,
                          ("prefill", 2048): 2048 / 0.1740}
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
-# capture (profiles/moe_gemm_tc_prefill.md), keyed by the library source hash
-# it was taken on, so a changed kernel reports null instead.
-NCU_TRAFFIC = {("moe_gemm_tc_kernel", "4692f6fb6c110585", "prefill:8191"): 666574848 + 340576256}
+# capture (profiles/moe_gemm_tc_prefill.md), keyed by a hash of the sources that
+# kernel is built from, so a changed kernel reports null instead.
+GEMM_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemm_tc.cu", "bit_quantized_moe_quantize_gb300/csrc/gemm_common.cuh",
+                "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh", "bit_quantized_moe_quantize_gb300/csrc/ft_internal.h",
+                "include/ft_moe.h")
+NCU_TRAFFIC = {("moe_gemm_tc_kernel", "d712be8223232a55", "prefill:8191"): 666574848 + 340576256}
+
+
+def kernel_source_hash(files) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def parse():
@@ -399,8 +412,7 @@ def ours(args):
                 "frac": achieved / peaks["hbm_gbs"], "peak_note": f"copy bandwidth, of {peak_src}",
                 "algorithmic": f"unique expert weights + Q8_1 act + fp32 out = {alg_bytes} B per launch",
                 "kernel_ms": mm_ms}
-    from bit_quantized_moe_quantize_gb300 import build as _b
-    tr = NCU_TRAFFIC.get((kern, _b.source_hash(), args.workload))
+    tr = NCU_TRAFFIC.get((kern, kernel_source_hash(GEMM_SOURCES), args.workload)) if path == "gemm" else None
     roof["traffic"] = tr
 
     cpu = None

@@ -422,8 +422,6 @@ __global__ void __launch_bounds__(288) moe_gemv_rows_kernel(const __grid_constan
                 wv[4 * c + 2] = v.z;
                 wv[4 * c + 3] = v.w;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);            // the box now lives in registers
 #pragma unroll
             for (int j = 0; j < KB; ++j) {
                 // block j of the box starts at byte 18 j: word 9j/2 (j even, d in its
@@ -470,6 +468,12 @@ __global__ void __launch_bounds__(288) moe_gemv_rows_kernel(const __grid_constan
                     }
                 }
             }
+            // release the box only after its values have been used: an arrival
+            // right after the shared loads can reach the producer while the
+            // loaded values are still on their way to registers, and its next
+            // TMA write then overtakes them
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
         }
         if (!ok) break;
         if constexpr (!DUMP) {

@@ -511,7 +511,7 @@ GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t nc
     p.group = mean <= 1.0 ? 1 : mean <= 2.0 ? 2 : mean <= 4.0 ? 4 : 8;
     if (ncols % 256 == 0) {
         // row-per-lane kernel.  KS warps per row group so that the batch
-        // keeps ~16 compute warps per SM busy, then as many row groups per CTA
+        // keeps ~32 compute warps per SM busy, then as many row groups per CTA
         // (RW, RW * KS <= 8) as still leave two CTAs per SM; a ring of
         // 2 KS boxes when the K range is split, else as deep as ~110 KB allows;
         // grid.y sized so that every CTA is resident at once.
@@ -519,7 +519,10 @@ GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t nc
         const int64_t groups32 = (nrows + 31) / 32;
         const int64_t sms = sm_count();
         const int64_t n_ks = nb / 8;
-        const int64_t want = (16 * sms + min_tiles * groups32 - 1) / (min_tiles * groups32);
+        // (8-slot tiles hold ~134 registers per thread, so splitting them
+        // further halves the CTAs an SM holds: keep those at ~16 warps)
+        const int64_t target = (p.group >= 8 ? 16 : 32) * sms;
+        const int64_t want = (target + min_tiles * groups32 - 1) / (min_tiles * groups32);
         int ks = 1;
         while (ks < want && ks < 8 && 2 * ks <= n_ks) ks *= 2;
         int rw = 1;

@@ -56,6 +56,12 @@ struct Gemm {
     static constexpr int RAW_STAGES = 2;
     static constexpr int OP_SLOTS = 4;                  // operand slots of 2 blocks (K = 64, one 128-B swizzle atom)
     static constexpr int NACC = 4;                      // TMEM accumulators, BN columns each
+    // Narrow tiles hand accumulators between the MMA thread and the drain per
+    // 2-block unit (a pair of accumulators, one commit, one release), which
+    // halves the hand-offs when the drain's work per block is small; wide
+    // tiles hand them off per block, which keeps the drain fed more evenly.
+    static constexpr bool PAIRED = BN_ <= 32;
+    static constexpr int NBAR_ACC = PAIRED ? NACC / 2 : NACC;   // accumulator barriers
     static constexpr int NSC = 8;                       // scale ring depth (blocks)
     static constexpr int W_RAW_BYTES = BM * KB * Q4_0_BYTES;   // 18432
     static constexpr int DA_RAW_BYTES = BN * KB * 2;           // [slot][8] fp16 activation scales
@@ -83,7 +89,7 @@ struct Gemm {
     static constexpr int OFF_RAW = OFF_OP + OP_SLOTS * OP_SLOT_BYTES;
     static constexpr int OFF_SC = OFF_RAW + RAW_STAGES * RAW_STAGE_BYTES;
     static constexpr int OFF_BAR = OFF_SC + NSC * SC_BYTES;
-    static constexpr int N_BARS = 2 * RAW_STAGES + 2 * OP_SLOTS + 2 * NACC + NSC;
+    static constexpr int N_BARS = 2 * RAW_STAGES + 2 * OP_SLOTS + 2 * NBAR_ACC + NSC;
     static constexpr int OFF_TMEM = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;    // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -114,6 +120,8 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
                        const __grid_constant__ CUtensorMap smap, const GemmArgs a) {
     using C = Gemm<BN>;
     constexpr int BM = C::BM, KB = C::KB, RAW_STAGES = C::RAW_STAGES, OP_SLOTS = C::OP_SLOTS, NACC = C::NACC;
+    constexpr int NBAR_ACC = C::NBAR_ACC;
+    constexpr bool PAIRED = C::PAIRED;
     constexpr int NSC = C::NSC, W_RAW_BYTES = C::W_RAW_BYTES, DA_RAW_BYTES = C::DA_RAW_BYTES;
     constexpr int RAW_STAGE_BYTES = C::RAW_STAGE_BYTES, OPA_BYTES = C::OPA_BYTES, OPB_BYTES = C::OPB_BYTES;
     constexpr int OP_SLOT_BYTES = C::OP_SLOT_BYTES, CW = C::CW, N_DRAIN_WARPS = C::N_DRAIN_WARPS;
@@ -130,8 +138,8 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
     uint64_t* op_full = raw_empty + RAW_STAGES;
     uint64_t* op_empty = op_full + OP_SLOTS;
     uint64_t* acc_full = op_empty + OP_SLOTS;
-    uint64_t* acc_empty = acc_full + NACC;
-    uint64_t* sc_empty = acc_empty + NACC;
+    uint64_t* acc_empty = acc_full + NBAR_ACC;
+    uint64_t* sc_empty = acc_empty + NBAR_ACC;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
 
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
@@ -147,11 +155,11 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
             mbar_init(&op_full[i], UNPACK_THREADS + 1);   // unpack threads + the producer's TMA
             mbar_init(&op_empty[i], 1);
         }
-        for (int i = 0; i < NACC; ++i) {
-            // block bc's accumulator is ready once its MMAs completed (the commit)
+        for (int i = 0; i < NBAR_ACC; ++i) {
+            // an accumulator (pair) is ready once its MMAs completed (the commit)
             // and the MMA thread has arrived after issuing them.  That second,
             // explicit arrival releases what the MMA thread acquired from the
-            // operand barrier - the unpack threads' scale writes for the block -
+            // operand barrier - the unpack threads' scale writes for the blocks -
             // and, being made only after acc_empty was observed, can never fall
             // into an earlier phase of the barrier.
             mbar_init(&acc_full[i], 2);
@@ -301,7 +309,41 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
         }
     } else if (warp == WARP_MMA) {
         // ----------------------------------------------------------------- MMA
-        if (lane == 0) {
+        if (PAIRED && lane == 0) {
+            // one accumulator pair per 2-block unit
+            constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+            uint32_t ou = 0;
+            bool ok = true;
+            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                for (int32_t ks = 0; ks < n_stages && ok; ++ks) {
+                    for (int j = 0; j < KB / 2; ++j, ++ou) {
+                        const uint32_t os = ou % OP_SLOTS;
+                        if (!mbar_wait(&op_full[os], (ou / OP_SLOTS) & 1u, a.err)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t abase = smem_u32(smem + OFF_OP + os * OP_SLOT_BYTES);
+                        const uint32_t bbase = abase + OPA_BYTES;
+                        const uint32_t pa = ou % NBAR_ACC;
+                        if (!mbar_wait(&acc_empty[pa], ((ou / NBAR_ACC) & 1u) ^ 1u, a.err)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t d_tmem = tmem_base + (2 * pa + h) * BN;
+#pragma unroll
+                            for (int k = 0; k < 2; ++k) {
+                                const uint32_t koff = h * 64 + k * 32;
+                                tc_mma_f16(d_tmem, smem_desc_sw128(abase + koff), smem_desc_sw128(bbase + koff), idesc,
+                                           k);
+                            }
+                        }
+                        tc_commit(&acc_full[pa]);
+                        mbar_arrive(&acc_full[pa]);
+                        tc_commit(&op_empty[os]);
+                    }
+                }
+            }
+        }
+        if (!PAIRED && lane == 0) {
+            // one accumulator per block
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
             uint32_t ou = 0, bc = 0;
             bool ok = true;
@@ -346,79 +388,164 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
         float2 acc[2][CW / 8];                             // [row][column group]
 #pragma unroll
         for (int i = 0; i < CW / 8; ++i) acc[0][i] = acc[1][i] = make_float2(0.0f, 0.0f);
-        uint32_t bc = 0;
-        bool ok = true;
-        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            const TileInfo ti = decode_tile<BN>(a, w);
-            for (int32_t b = 0; b < nb; ++b, ++bc) {
-                const uint32_t ab = bc % NACC, sc = bc % NSC;
-                if (!mbar_wait_warp(&acc_full[ab], (bc / NACC) & 1u, a.err)) { ok = false; break; }
-                tc_fence_after();
-                const float* dws = reinterpret_cast<const float*>(smem + OFF_SC + sc * SC_BYTES);
-                const float4* dap =
-                    reinterpret_cast<const float4*>(dws + BM + (col0 / CW) * (4 * DA_QPITCH) + q * DA_QPITCH);
-                const float dw0 = dws[r0], dw1 = dws[r0 + 8];
-                const float2 dw0x2 = make_float2(dw0, dw0), dw1x2 = make_float2(dw1, dw1);
-#pragma unroll
-                for (int hh = 0; hh < NH; ++hh) {
-                    uint32_t d[16];
-                    tmem_ld_16x256b_x4(tlane + ab * BN + 32 * hh, d);
-                    tmem_wait_ld();
-                    if (hh == NH - 1) {                      // TMEM buffer ab fully read
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+        if constexpr (PAIRED) {
+            uint32_t bc = 0, uc = 0;                           // blocks and 2-block units drained
+            bool ok = true;
+            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                const TileInfo ti = decode_tile<BN>(a, w);
+                for (int32_t b = 0; b < nb; ++b, ++bc) {
+                    const uint32_t h = static_cast<uint32_t>(b) & 1u;   // block within its unit (nb is even)
+                    // the unit's accumulator pair, its phase, and the block's accumulator
+                    const uint32_t bi = uc % NBAR_ACC, ph = (uc / NBAR_ACC) & 1u;
+                    const uint32_t ab = 2 * bi + h, sc = bc % NSC;
+                    if (h == 0) {
+                        if (!mbar_wait_warp(&acc_full[bi], ph, a.err)) { ok = false; break; }
+                        tc_fence_after();
                     }
-                    if constexpr (DUMP) {
-#pragma unroll
-                        for (int ig = 0; ig < 4; ++ig)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int64_t row = ti.m0 + r0 + (e >> 1) * 8;
-                                const int n = col0 + 8 * (4 * hh + ig) + 2 * static_cast<int>(q) + (e & 1);
-                                if (row < a.nrows && n < ti.nvalid) {
-                                    const int64_t s = a.perm[ti.p0 + n];
-                                    a.dots[(s * a.nrows + row) * nb + b] =
-                                        static_cast<int32_t>(__uint_as_float(d[4 * ig + e]));
+                    const float* dws = reinterpret_cast<const float*>(smem + OFF_SC + sc * SC_BYTES);
+                    const float4* dap =
+                        reinterpret_cast<const float4*>(dws + BM + (col0 / CW) * (4 * DA_QPITCH) + q * DA_QPITCH);
+                    const float dw0 = dws[r0], dw1 = dws[r0 + 8];
+                    const float2 dw0x2 = make_float2(dw0, dw0), dw1x2 = make_float2(dw1, dw1);
+    #pragma unroll
+                    for (int hh = 0; hh < NH; ++hh) {
+                        uint32_t d[16];
+                        tmem_ld_16x256b_x4(tlane + ab * BN + 32 * hh, d);
+                        tmem_wait_ld();
+                        if (h == 1 && hh == NH - 1) {            // the unit's accumulator pair fully read
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&acc_empty[bi]);
+                        }
+                        if constexpr (DUMP) {
+    #pragma unroll
+                            for (int ig = 0; ig < 4; ++ig)
+    #pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int64_t row = ti.m0 + r0 + (e >> 1) * 8;
+                                    const int n = col0 + 8 * (4 * hh + ig) + 2 * static_cast<int>(q) + (e & 1);
+                                    if (row < a.nrows && n < ti.nvalid) {
+                                        const int64_t s = a.perm[ti.p0 + n];
+                                        a.dots[(s * a.nrows + row) * nb + b] =
+                                            static_cast<int32_t>(__uint_as_float(d[4 * ig + e]));
+                                    }
+                                }
+                        } else {
+                            // acc += d_w * (dot * d_a): one packed multiply and one packed FMA per column pair
+    #pragma unroll
+                            for (int k2 = 0; k2 < 2; ++k2) {
+                                const float4 v = dap[2 * hh + k2];   // d_a of columns 8i+2q+{0,1}, i = 4hh+2k2, +1
+    #pragma unroll
+                                for (int ii = 0; ii < 2; ++ii) {
+                                    const int ig = 2 * k2 + ii, i = 4 * hh + ig;
+                                    const float2 da2 = ii ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
+                                    const float2 t0 =
+                                        __fmul2_rn(make_float2(__uint_as_float(d[4 * ig]), __uint_as_float(d[4 * ig + 1])), da2);
+                                    const float2 t1 = __fmul2_rn(
+                                        make_float2(__uint_as_float(d[4 * ig + 2]), __uint_as_float(d[4 * ig + 3])), da2);
+                                    acc[0][i] = __ffma2_rn(t0, dw0x2, acc[0][i]);
+                                    acc[1][i] = __ffma2_rn(t1, dw1x2, acc[1][i]);
                                 }
                             }
-                    } else {
-                        // acc += d_w * (dot * d_a): one packed multiply and one packed FMA per column pair
-#pragma unroll
-                        for (int k2 = 0; k2 < 2; ++k2) {
-                            const float4 v = dap[2 * hh + k2];   // d_a of columns 8i+2q+{0,1}, i = 4hh+2k2, +1
-#pragma unroll
-                            for (int ii = 0; ii < 2; ++ii) {
-                                const int ig = 2 * k2 + ii, i = 4 * hh + ig;
-                                const float2 da2 = ii ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
-                                const float2 t0 =
-                                    __fmul2_rn(make_float2(__uint_as_float(d[4 * ig]), __uint_as_float(d[4 * ig + 1])), da2);
-                                const float2 t1 = __fmul2_rn(
-                                    make_float2(__uint_as_float(d[4 * ig + 2]), __uint_as_float(d[4 * ig + 3])), da2);
-                                acc[0][i] = __ffma2_rn(t0, dw0x2, acc[0][i]);
-                                acc[1][i] = __ffma2_rn(t1, dw1x2, acc[1][i]);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sc_empty[sc]);   // scale slot sc free again
+                    uc += h;
+                }
+                if (!ok) break;
+                if constexpr (!DUMP) {
+    #pragma unroll
+                    for (int i = 0; i < CW / 8; ++i) {
+    #pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int n = col0 + 8 * i + 2 * static_cast<int>(q) + e;
+                            if (n < ti.nvalid) {
+                                const int64_t s = a.perm[ti.p0 + n];
+                                float* o = a.out + s * a.nrows + ti.m0 + r0;
+                                if (ti.m0 + r0 < a.nrows) o[0] = e ? acc[0][i].y : acc[0][i].x;
+                                if (ti.m0 + r0 + 8 < a.nrows) o[8] = e ? acc[1][i].y : acc[1][i].x;
+                            }
+                        }
+                        acc[0][i] = acc[1][i] = make_float2(0.0f, 0.0f);
+                    }
+                }
+            }
+        } else {
+            uint32_t bc = 0;
+            bool ok = true;
+            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                const TileInfo ti = decode_tile<BN>(a, w);
+                for (int32_t b = 0; b < nb; ++b, ++bc) {
+                    const uint32_t ab = bc % NACC, sc = bc % NSC;
+                    if (!mbar_wait_warp(&acc_full[ab], (bc / NACC) & 1u, a.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const float* dws = reinterpret_cast<const float*>(smem + OFF_SC + sc * SC_BYTES);
+                    const float4* dap =
+                        reinterpret_cast<const float4*>(dws + BM + (col0 / CW) * (4 * DA_QPITCH) + q * DA_QPITCH);
+                    const float dw0 = dws[r0], dw1 = dws[r0 + 8];
+                    const float2 dw0x2 = make_float2(dw0, dw0), dw1x2 = make_float2(dw1, dw1);
+    #pragma unroll
+                    for (int hh = 0; hh < NH; ++hh) {
+                        uint32_t d[16];
+                        tmem_ld_16x256b_x4(tlane + ab * BN + 32 * hh, d);
+                        tmem_wait_ld();
+                        if (hh == NH - 1) {                      // TMEM buffer ab fully read
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                        }
+                        if constexpr (DUMP) {
+    #pragma unroll
+                            for (int ig = 0; ig < 4; ++ig)
+    #pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int64_t row = ti.m0 + r0 + (e >> 1) * 8;
+                                    const int n = col0 + 8 * (4 * hh + ig) + 2 * static_cast<int>(q) + (e & 1);
+                                    if (row < a.nrows && n < ti.nvalid) {
+                                        const int64_t s = a.perm[ti.p0 + n];
+                                        a.dots[(s * a.nrows + row) * nb + b] =
+                                            static_cast<int32_t>(__uint_as_float(d[4 * ig + e]));
+                                    }
+                                }
+                        } else {
+                            // acc += d_w * (dot * d_a): one packed multiply and one packed FMA per column pair
+    #pragma unroll
+                            for (int k2 = 0; k2 < 2; ++k2) {
+                                const float4 v = dap[2 * hh + k2];   // d_a of columns 8i+2q+{0,1}, i = 4hh+2k2, +1
+    #pragma unroll
+                                for (int ii = 0; ii < 2; ++ii) {
+                                    const int ig = 2 * k2 + ii, i = 4 * hh + ig;
+                                    const float2 da2 = ii ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
+                                    const float2 t0 =
+                                        __fmul2_rn(make_float2(__uint_as_float(d[4 * ig]), __uint_as_float(d[4 * ig + 1])), da2);
+                                    const float2 t1 = __fmul2_rn(
+                                        make_float2(__uint_as_float(d[4 * ig + 2]), __uint_as_float(d[4 * ig + 3])), da2);
+                                    acc[0][i] = __ffma2_rn(t0, dw0x2, acc[0][i]);
+                                    acc[1][i] = __ffma2_rn(t1, dw1x2, acc[1][i]);
+                                }
                             }
                         }
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sc_empty[sc]);   // scale slot sc free again
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sc_empty[sc]);   // scale slot sc free again
-            }
-            if (!ok) break;
-            if constexpr (!DUMP) {
-#pragma unroll
-                for (int i = 0; i < CW / 8; ++i) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int n = col0 + 8 * i + 2 * static_cast<int>(q) + e;
-                        if (n < ti.nvalid) {
-                            const int64_t s = a.perm[ti.p0 + n];
-                            float* o = a.out + s * a.nrows + ti.m0 + r0;
-                            if (ti.m0 + r0 < a.nrows) o[0] = e ? acc[0][i].y : acc[0][i].x;
-                            if (ti.m0 + r0 + 8 < a.nrows) o[8] = e ? acc[1][i].y : acc[1][i].x;
+                if (!ok) break;
+                if constexpr (!DUMP) {
+    #pragma unroll
+                    for (int i = 0; i < CW / 8; ++i) {
+    #pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int n = col0 + 8 * i + 2 * static_cast<int>(q) + e;
+                            if (n < ti.nvalid) {
+                                const int64_t s = a.perm[ti.p0 + n];
+                                float* o = a.out + s * a.nrows + ti.m0 + r0;
+                                if (ti.m0 + r0 < a.nrows) o[0] = e ? acc[0][i].y : acc[0][i].x;
+                                if (ti.m0 + r0 + 8 < a.nrows) o[8] = e ? acc[1][i].y : acc[1][i].x;
+                            }
                         }
+                        acc[0][i] = acc[1][i] = make_float2(0.0f, 0.0f);
                     }
-                    acc[0][i] = acc[1][i] = make_float2(0.0f, 0.0f);
                 }
             }
         }

@@ -689,9 +689,10 @@ static int launch_gemm_bn(const uint8_t* weights, const int32_t* perm, const int
 }
 
 int gemm_tile_width(int64_t n_slots, int32_t n_experts) {
-    // narrow slot tiles while experts see few slots each: the drain then scales
-    // 32 instead of 128 columns per block
-    return static_cast<double>(n_slots) / n_experts < 96.0 ? 32 : kGemmBN;
+    // narrow slot tiles while experts see few slots each (the drain then scales
+    // 32 instead of 128 columns per block); measured crossover between 32 and
+    // 64 slots per expert
+    return static_cast<double>(n_slots) / n_experts < 48.0 ? 32 : kGemmBN;
 }
 
 int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,

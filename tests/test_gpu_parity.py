@@ -280,11 +280,12 @@ def test_deterministic(path, oracle):
         assert np.array_equal(r1, r2)
 
 
-@pytest.mark.parametrize("T", [300, 1000])
+@pytest.mark.parametrize("T", [150, 1000])
 def test_graph_capture_replay(path, oracle, T):
     """Quantize + route + matmul captured in a CUDA graph and replayed give the
-    eager result bit for bit (no allocation or host sync inside).  T = 300
-    takes the 32-wide tensor-core tiles, T = 1000 the widened-weight ones."""
+    eager result bit for bit (no allocation or host sync inside).  T = 150
+    (37.5 slots per expert) takes the 32-wide tensor-core tiles, T = 1000 the
+    128-wide ones."""
     import torch
     w, x, ids = _custom(8, 2, 512, 256, T, 60)
     dw, dx, di = G.dev(w), G.dev(x), G.dev(ids)

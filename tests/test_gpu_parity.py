@@ -173,7 +173,7 @@ def test_ragged_full_compare(path, oracle, E, k, K, N, T, seed, path_name):
 
 
 # the first two take the 32-wide tensor-core tiles (few slots per expert), the
-# last two the 128-wide tiles on widened weights (many slots per expert)
+# last two the 128-wide tiles (many slots per expert)
 @pytest.mark.parametrize("E,k,K,N,T,seed", [(5, 2, 512, 200, 77, 11), (16, 4, 256, 64, 129, 13),
                                             (3, 3, 768, 130, 300, 12), (2, 1, 4096, 260, 400, 14)])
 @pytest.mark.parametrize("path_name", ["gemv", "gemm"])

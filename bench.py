@@ -51,7 +51,7 @@ PAGES_T4_TOKENS_PER_S = {("prefill", 8191): 8191 / 0.7058, ("prefill", 4096): 40
 GEMM_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemm_tc.cu", "bit_quantized_moe_quantize_gb300/csrc/gemm_common.cuh",
                 "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh", "bit_quantized_moe_quantize_gb300/csrc/ft_internal.h",
                 "include/ft_moe.h")
-NCU_TRAFFIC = {("moe_gemm_tc_kernel", "d712be8223232a55", "prefill:8191"): 666574848 + 340576256}
+NCU_TRAFFIC = {("moe_gemm_tc_kernel", "a5ed6a8ab5bf58e6", "prefill:8191"): 666685184 + 341326592}
 
 
 def kernel_source_hash(files) -> str:

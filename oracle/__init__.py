@@ -73,6 +73,7 @@ class Oracle:
         L.oracle_block_dot.restype = i32
         L.oracle_moe_q4_0_q8_1.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64]
         L.oracle_moe_sample.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp, vp, i64, vp]
+        L.oracle_moe_slots_q4_0_q8_1.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64]
         L.oracle_moe_block_dots.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.oracle_moe_dequant_bruteforce.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp]
         self.lib = L
@@ -147,6 +148,19 @@ class Oracle:
         E, N, K, T, k = self._shape(weights, act, ids)
         out = np.empty((T, k, N), dtype=np.float32)
         self.lib.oracle_moe_q4_0_q8_1(_p(weights), _p(act), _p(ids), _p(out), T, k, E, N, K)
+        return out
+
+    def moe_slots(self, weights, act_slots, topk_ids) -> np.ndarray:
+        """Per-slot activations: act_slots is Q8_1 [T*k][K/32], row s for slot s."""
+        weights = np.ascontiguousarray(weights, dtype=np.uint8)
+        act_slots = np.ascontiguousarray(act_slots, dtype=np.uint8)
+        ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+        E, N, nb, _ = weights.shape
+        T, k = ids.shape
+        assert act_slots.shape == (T * k, nb, 36), act_slots.shape
+        K = nb * QK
+        out = np.empty((T, k, N), dtype=np.float32)
+        self.lib.oracle_moe_slots_q4_0_q8_1(_p(weights), _p(act_slots), _p(ids), _p(out), T, k, E, N, K)
         return out
 
     def moe_sample(self, weights, act, topk_ids, slots, rows) -> np.ndarray:

@@ -260,6 +260,36 @@ void oracle_moe_q4_0_q8_1(const uint8_t* weights, const uint8_t* act, const int3
                                                 nrows, ncols, s, r);
 }
 
+/* Per-slot activations (the second expert layer's input, one Q8_1 row per
+ * routed slot, nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 6: L2 runs on the L1
+ * output after SiLU*up): out[s][r] as above with activation row s instead of
+ * row s / top_k. */
+void oracle_moe_slots_q4_0_q8_1(const uint8_t* weights, const uint8_t* act_slots, const int32_t* topk_ids,
+                                float* out, int64_t tokens, int32_t top_k, int32_t n_experts,
+                                int64_t nrows, int64_t ncols)
+{
+    int64_t nb = ncols / QK;
+    int64_t n_slots = tokens * top_k;
+    for (int64_t s = 0; s < n_slots; ++s) {
+        int32_t e = topk_ids[s];
+        const uint8_t* arow = act_slots + s * nb * Q8_1_BYTES;
+        for (int64_t r = 0; r < nrows; ++r) {
+            double y = 0.0;
+            if (e >= 0 && e < n_experts) {
+                const uint8_t* wrow = weights + ((int64_t)e * nrows + r) * nb * Q4_0_BYTES;
+                for (int64_t b = 0; b < nb; ++b) {
+                    const uint8_t* wb = wrow + b * Q4_0_BYTES;
+                    const uint8_t* ab = arow + b * Q8_1_BYTES;
+                    double dw = oracle_half_to_double(rd16(wb));
+                    double da = oracle_half_to_double(rd16(ab));
+                    y += dw * da * (double)oracle_block_dot(wb, ab);
+                }
+            }
+            out[s * nrows + r] = (float)y;
+        }
+    }
+}
+
 void oracle_moe_sample(const uint8_t* weights, const uint8_t* act, const int32_t* topk_ids,
                        int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows,
                        int64_t ncols, const int64_t* slots, const int64_t* rows, int64_t n,

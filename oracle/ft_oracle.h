@@ -19,6 +19,9 @@
  *                                                  dequant brute force, numpy
  *                                                  einsum of decoded operands,
  *                                                  split invariance
+ *   oracle_moe_slots_q4_0_q8_1                     pinned: numpy einsum of decoded
+ *                                                  operands; replicated token rows
+ *                                                  give oracle_moe_q4_0_q8_1 bit for bit
  *
  * Byte layouts (GGUF block formats; the pages serve GGUF Q4_0 checkpoints but
  * do not print the formats):
@@ -55,6 +58,10 @@ int32_t oracle_block_dot(const uint8_t* w_block, const uint8_t* a_block);
 void oracle_moe_q4_0_q8_1(const uint8_t* weights, const uint8_t* act, const int32_t* topk_ids,
                           float* out, int64_t tokens, int32_t top_k, int32_t n_experts,
                           int64_t nrows, int64_t ncols);
+
+void oracle_moe_slots_q4_0_q8_1(const uint8_t* weights, const uint8_t* act_slots, const int32_t* topk_ids,
+                                float* out, int64_t tokens, int32_t top_k, int32_t n_experts,
+                                int64_t nrows, int64_t ncols);
 
 void oracle_moe_sample(const uint8_t* weights, const uint8_t* act, const int32_t* topk_ids,
                        int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows,

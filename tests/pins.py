@@ -343,9 +343,33 @@ def pin_moe_bad_ids(o):
     assert y[0].any() and y[3].any()
 
 
+def pin_moe_slots_numpy_einsum(o):
+    """Per-slot activations (one Q8_1 row per routed slot): independent numpy
+    decode of both operands and einsum, with every slot's row different."""
+    for seed, T, k in [(60, 6, 2), (61, 3, 3)]:
+        w, x, ids = tiny_case(seed=seed, T=T * k, k=1)        # T*k distinct activation rows
+        ids = tiny_case(seed=seed + 100, T=T, k=k)[2]          # routing of T tokens x k slots
+        act_slots = o.quantize_q8_1(x)                          # [T*k, nb, 36]
+        W = numpy_decode_q4_0(w)                                # [E, N, K]
+        A = numpy_decode_q8_1(act_slots)                        # [T*k, K]
+        want = np.einsum("snk,sk->sn", W[ids.reshape(-1)], A).reshape(T, k, -1)
+        got = o.moe_slots(w, act_slots, ids).astype(np.float64)
+        tol = 1e-6 * np.abs(want) + 1e-9 * np.abs(want).max()
+        assert np.all(np.abs(got - want) <= tol)
+
+
+def pin_moe_slots_replicated_rows(o):
+    """Slot s given its token's row (row s // k) reproduces the per-token
+    matmul bit for bit."""
+    w, x, ids = tiny_case(seed=62, T=7, k=3)
+    act = o.quantize_q8_1(x)
+    act_slots = np.repeat(act, ids.shape[1], axis=0)
+    assert np.array_equal(o.moe_slots(w, act_slots, ids), o.moe(w, act, ids))
+
+
 ALL_PINS = [
     pin_fp16, pin_q4_0_hand, pin_q4_0_nearest_level, pin_q4_0_matches_generator, pin_q4_0_dequant,
     pin_q8_1_hand, pin_q8_1_numpy, pin_q8_1_error_bound, pin_route, pin_block_dot_hand,
     pin_moe_closed_form_vs_bruteforce, pin_moe_numpy_einsum, pin_moe_block_dots,
-    pin_moe_split_invariance, pin_moe_bad_ids,
+    pin_moe_split_invariance, pin_moe_bad_ids, pin_moe_slots_numpy_einsum, pin_moe_slots_replicated_rows,
 ]

@@ -27,7 +27,7 @@ PATHS = {"auto": FT_PATH_AUTO, "gemv": FT_PATH_GEMV, "gemm": FT_PATH_GEMM}
 EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_moe_workspace_bytes",
            "ft_moe_reserve", "ft_moe_release", "ft_moe_read_device_error", "ft_moe_set_path",
            "ft_moe_selected_path", "ft_moe_block_dots", "ft_last_error", "ft_abi_version", "ft_profile_enable",
-           "ft_profile_read", "ft_moe_route_offsets_noalloc")
+           "ft_profile_read", "ft_moe_route_offsets_noalloc", "ft_moe_q4_0_q8_1_slots")
 
 
 class FtError(RuntimeError):
@@ -58,6 +58,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.ft_moe_route_offsets.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp]
         L.ft_moe_route_offsets_noalloc.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp]
         L.ft_moe_q4_0_q8_1.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
+        L.ft_moe_q4_0_q8_1_slots.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_moe_block_dots.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_moe_workspace_bytes.argtypes = [i64, i32, i32, i64, i64]
         L.ft_moe_workspace_bytes.restype = ctypes.c_size_t
@@ -163,6 +164,29 @@ def moe_q4_0_q8_1(weights, act, topk_ids, out=None):
     po = _dev(out, torch.float32, "out")
     _check(load().ft_moe_q4_0_q8_1(ctypes.c_void_p(weights.data_ptr()), ctypes.c_void_p(act.data_ptr()),
                                    ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, E, N, K, _stream(weights)))
+    return out
+
+
+def moe_q4_0_q8_1_slots(weights, act_slots, topk_ids, out=None):
+    """Routed matmul with one activation row per slot: Q4_0 [E,N,K/32,18] x
+    Q8_1 [T*k,K/32,36] (row s for slot s = t*k + j) -> fp32 [T, k, N]
+    (ft_moe_q4_0_q8_1_slots)."""
+    torch = _torch()
+    _dev(weights, torch.uint8, "weights", 4)
+    _dev(act_slots, torch.uint8, "act_slots", 3)
+    _dev(topk_ids, torch.int32, "topk_ids", 2)
+    E, N, nb, wb = weights.shape
+    S, nb2, ab = act_slots.shape
+    T, k = topk_ids.shape
+    if wb != 18 or ab != 36 or nb != nb2 or S != T * k:
+        raise ValueError(f"shape mismatch: weights {tuple(weights.shape)} act_slots {tuple(act_slots.shape)} "
+                         f"topk_ids {tuple(topk_ids.shape)}")
+    if out is None:
+        out = torch.empty((T, k, N), dtype=torch.float32, device=weights.device)
+    po = _dev(out, torch.float32, "out")
+    _check(load().ft_moe_q4_0_q8_1_slots(ctypes.c_void_p(weights.data_ptr()), ctypes.c_void_p(act_slots.data_ptr()),
+                                         ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, E, N, nb * 32,
+                                         _stream(weights)))
     return out
 
 

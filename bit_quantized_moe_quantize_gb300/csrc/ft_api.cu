@@ -150,6 +150,7 @@ static bool mul_ok(int64_t a, int64_t b, int64_t* r) {
 struct Shape {
     int64_t tokens, n_slots, nrows, ncols, nb;
     int32_t top_k, n_experts;
+    int32_t act_div;   // activation row of slot s: s / act_div (top_k: one row per token; 1: one per slot)
 };
 
 // Checks the routing arguments; fills n_slots.
@@ -166,6 +167,7 @@ static int check_route_args(int64_t tokens, int32_t top_k, int32_t n_experts, Sh
     sh->top_k = top_k;
     sh->n_experts = n_experts;
     sh->n_slots = s;
+    sh->act_div = top_k;
     return FT_OK;
 }
 
@@ -346,7 +348,7 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
                               zero_rows, row_words, s))
         return st;
     if (path == FT_PATH_GEMM && sh.n_slots > 0) {
-        if (int st = launch_gather(static_cast<const uint8_t*>(act), rb.perm, rb.offsets, sh.n_experts, sh.top_k,
+        if (int st = launch_gather(static_cast<const uint8_t*>(act), rb.perm, rb.offsets, sh.n_experts, sh.act_div,
                                    sh.nb, sh.n_slots, reinterpret_cast<uint16_t*>(ws + L.xh),
                                    reinterpret_cast<uint16_t*>(ws + L.da), s))
             return st;
@@ -355,11 +357,11 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     int st;
     if (path == FT_PATH_GEMV)
         st = launch_gemv(gp, static_cast<const uint8_t*>(weights), static_cast<const uint8_t*>(act), rb.perm,
-                         rb.offsets, rb.tiles_gemv, out, dots, rb.err, sh.n_slots, sh.top_k, sh.n_experts, sh.nrows,
+                         rb.offsets, rb.tiles_gemv, out, dots, rb.err, sh.n_slots, sh.act_div, sh.n_experts, sh.nrows,
                          sh.ncols, s);
     else
         st = launch_gemm(static_cast<const uint8_t*>(weights), static_cast<const uint8_t*>(act), rb.perm,
-                         rb.offsets, rb.tiles_gemm, out, dots, rb.err, sh.n_slots, sh.top_k, sh.n_experts, sh.nrows,
+                         rb.offsets, rb.tiles_gemm, out, dots, rb.err, sh.n_slots, sh.act_div, sh.n_experts, sh.nrows,
                          sh.ncols, reinterpret_cast<uint16_t*>(ws + L.xh), reinterpret_cast<uint16_t*>(ws + L.da), s);
     prof_mark(kProfMatmulEnd, s);
     return st;
@@ -417,10 +419,11 @@ int ft_moe_route_offsets(const int32_t* topk_ids, int64_t tokens, int32_t top_k,
 
 static int matmul_entry(const void* weights, const void* act, const int32_t* topk_ids, float* out, int32_t* dots,
                         int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols,
-                        void* stream) {
+                        void* stream, bool act_per_slot = false) {
     g_last_error.clear();
     Shape sh{};
     if (int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh)) return st;
+    if (act_per_slot) sh.act_div = 1;
     if (sh.n_slots == 0) return FT_OK;
     if (!weights || !act || !topk_ids || (!out && !dots)) return fail(FT_ERR_ARG, "null pointer");
     if (!aligned(weights, 16) || !aligned(act, 16))
@@ -445,6 +448,20 @@ int ft_moe_q4_0_q8_1(const void* weights, const void* act, const int32_t* topk_i
         return fail(FT_ERR_ARG, "null pointer");
     }
     return matmul_entry(weights, act, topk_ids, out, nullptr, tokens, top_k, n_experts, nrows, ncols, stream);
+}
+
+int ft_moe_q4_0_q8_1_slots(const void* weights, const void* act_slots, const int32_t* topk_ids, float* out,
+                           int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols,
+                           void* stream) {
+    if (!out) {
+        g_last_error.clear();
+        Shape sh{};
+        if (int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh)) return st;
+        if (sh.n_slots == 0) return FT_OK;
+        return fail(FT_ERR_ARG, "null pointer");
+    }
+    return matmul_entry(weights, act_slots, topk_ids, out, nullptr, tokens, top_k, n_experts, nrows, ncols, stream,
+                        true);
 }
 
 int ft_moe_block_dots(const void* weights, const void* act, const int32_t* topk_ids, int32_t* dots, int64_t tokens,

@@ -178,6 +178,23 @@ FT_API int ft_moe_q4_0_q8_1(const void* weights, const void* act, const int32_t*
                      int64_t ncols, void* stream);
 
 /*
+ * ft_moe_q4_0_q8_1_slots - the same matmul with one activation row per routed
+ * slot instead of one per token: the input of the second expert layer, which
+ * runs on the first layer's output after SiLU*up, one row per routed slot
+ * (nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 6).
+ *   out[s][r] = sum_b d_w[e][r][b] * d_a[s][b] * sum_i (q_w - 8) * q_a[s][b][i],
+ *   e = topk_ids[s], s = t * top_k + j.
+ *
+ *   act_slots device, Q8_1 [tokens*top_k][ncols/32]; row s belongs to slot s;
+ *             16-byte aligned
+ * Every other argument, the layouts, the path choice, the workspace and the
+ * errors are those of ft_moe_q4_0_q8_1.
+ */
+FT_API int ft_moe_q4_0_q8_1_slots(const void* weights, const void* act_slots, const int32_t* topk_ids,
+                                  float* out, int64_t tokens, int32_t top_k, int32_t n_experts,
+                                  int64_t nrows, int64_t ncols, void* stream);
+
+/*
  * ft_moe_workspace_bytes - bytes of library workspace that one
  * ft_moe_q4_0_q8_1 / ft_moe_route_offsets call of this shape needs.
  * Returns 0 for invalid arguments.

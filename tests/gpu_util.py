@@ -73,3 +73,12 @@ def full_norms(oracle, weights, act, ids):
     xn = act_norms(oracle, act)                        # [T]
     idc = np.clip(ids, 0, E - 1)
     return wn[idc], np.broadcast_to(xn[:, None, None], (*ids.shape, N))
+
+
+def full_norms_slots(oracle, weights, act_slots, ids):
+    """As full_norms, with one activation row per slot (act_slots [T*k, nb, 36])."""
+    E, N, nb, _ = weights.shape
+    wn = np.linalg.norm(oracle.dequantize_q4_0(weights.reshape(E * N, nb, 18)), axis=-1).reshape(E, N)
+    xn = act_norms(oracle, act_slots).reshape(ids.shape)   # [T, k]
+    idc = np.clip(ids, 0, E - 1)
+    return wn[idc], np.broadcast_to(xn[:, :, None], (*ids.shape, N))

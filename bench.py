@@ -73,6 +73,8 @@ def parse():
     ap.add_argument("--workload", default="prefill:8191")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--per-slot", action="store_true",
+                    help="one activation row per routed slot (ft_moe_q4_0_q8_1_slots, the second expert layer)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of a CUDA-graph replay of the step")
     return ap.parse_args()
@@ -274,20 +276,26 @@ def ours(args):
     w, x, ids = make_inputs(wl, T, rank)
     E, k, K, N = wl.n_experts, wl.top_k, wl.ncols, wl.nrows
     S = T * k
+    if args.per_slot:                       # one fp16 activation row per slot
+        from bit_quantized_moe_quantize_gb300 import synth
+        x = synth.make_activations(replica_workload(wl, rank), S)
+    rows = S if args.per_slot else T
     path = {1: "gemv", 2: "gemm"}[ft.selected_path(T, k, E, N, K)]
 
     dw = torch.from_numpy(w).to(dev)
     dx = torch.from_numpy(x).to(dev)
     di = torch.from_numpy(ids).to(dev)
-    act = torch.empty((T, K // 32, 36), dtype=torch.uint8, device=dev)
+    act = torch.empty((rows, K // 32, 36), dtype=torch.uint8, device=dev)
     out = torch.empty((T, k, N), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ft.reserve(T, k, E, N, K)
     stream = torch.cuda.current_stream()
 
+    matmul = ft.moe_q4_0_q8_1_slots if args.per_slot else ft.moe_q4_0_q8_1
+
     def step():
         ft.quantize_q8_1(dx, out=act)
-        ft.moe_q4_0_q8_1(dw, act, di, out=out)
+        matmul(dw, act, di, out=out)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -395,7 +403,7 @@ def ours(args):
     flops = 2.0 * S * N * K
     counts = np.bincount(ids.reshape(-1), minlength=E)
     nb = K // 32
-    alg_bytes = int((counts > 0).sum()) * N * nb * 18 + T * nb * 36 + S * N * 4
+    alg_bytes = int((counts > 0).sum()) * N * nb * 18 + rows * nb * 36 + S * N * 4
     if path == "gemm":
         kern = "moe_gemm_tc_kernel"
         achieved = flops / (mm_ms / 1000.0) / 1e12
@@ -429,7 +437,8 @@ def ours(args):
         "vs_baseline_note": "pages' Tesla T4 moe_vec time for this token count (context, other hardware)"
         if base else None,
         "dtype": "q4_0 x q8_1: exact int block dots (f16 MMA / dp4a), f32 scaling",
-        "data": "synthetic", "config": {**config_of(name, wl, T, world), "path": path, "launch": launch_mode},
+        "data": "synthetic", "config": {**config_of(name, wl, T, world), "path": path, "launch": launch_mode,
+                                        "activations": "per slot" if args.per_slot else "per token"},
         "effective_tops": 2.0 * S * N * K * world / (ms / 1000.0) / 1e12,
         "kernels_ms_per_step": {"quantize": prof["quantize_ms"] / calls, "prepare": prof["route_ms"] / calls,
                                 "matmul": mm_ms,

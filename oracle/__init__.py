@@ -74,6 +74,7 @@ class Oracle:
         L.oracle_moe_q4_0_q8_1.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64]
         L.oracle_moe_sample.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp, vp, i64, vp]
         L.oracle_moe_slots_q4_0_q8_1.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64]
+        L.oracle_moe_ep_q4_0_q8_1.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i32, i64, i64]
         L.oracle_moe_block_dots.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.oracle_moe_dequant_bruteforce.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp]
         self.lib = L
@@ -161,6 +162,18 @@ class Oracle:
         K = nb * QK
         out = np.empty((T, k, N), dtype=np.float32)
         self.lib.oracle_moe_slots_q4_0_q8_1(_p(weights), _p(act_slots), _p(ids), _p(out), T, k, E, N, K)
+        return out
+
+    def moe_ep(self, weights_local, act, topk_ids, n_global, expert_start) -> np.ndarray:
+        """Expert-parallel shard: weights_local = experts [expert_start, expert_start + E_local)
+        of n_global; topk_ids hold global ids; non-local slots give zero rows."""
+        weights_local = np.ascontiguousarray(weights_local, dtype=np.uint8)
+        act = np.ascontiguousarray(act, dtype=np.uint8)
+        ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+        E_local, N, K, T, k = self._shape(weights_local, act, ids)
+        out = np.empty((T, k, N), dtype=np.float32)
+        self.lib.oracle_moe_ep_q4_0_q8_1(_p(weights_local), _p(act), _p(ids), _p(out), T, k, n_global,
+                                         expert_start, E_local, N, K)
         return out
 
     def moe_sample(self, weights, act, topk_ids, slots, rows) -> np.ndarray:

@@ -290,6 +290,40 @@ void oracle_moe_slots_q4_0_q8_1(const uint8_t* weights, const uint8_t* act_slots
     }
 }
 
+/* Expert-parallel shard (nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 8: global
+ * expert ids, remapped by the shard's first expert, non-local slots masked):
+ * weights_local holds experts [expert_start, expert_start + n_local) of
+ * n_global; a slot whose global id g lies in that range is computed with
+ * local expert g - expert_start, every other slot's row is 0. */
+void oracle_moe_ep_q4_0_q8_1(const uint8_t* weights_local, const uint8_t* act, const int32_t* topk_ids,
+                             float* out, int64_t tokens, int32_t top_k, int32_t n_global,
+                             int32_t expert_start, int32_t n_local, int64_t nrows, int64_t ncols)
+{
+    int64_t nb = ncols / QK;
+    int64_t n_slots = tokens * top_k;
+    (void)n_global;
+    for (int64_t s = 0; s < n_slots; ++s) {
+        int32_t g = topk_ids[s];
+        int64_t t = s / top_k;
+        const uint8_t* arow = act + t * nb * Q8_1_BYTES;
+        for (int64_t r = 0; r < nrows; ++r) {
+            double y = 0.0;
+            if (g >= expert_start && g < expert_start + n_local) {
+                int32_t e = g - expert_start;
+                const uint8_t* wrow = weights_local + ((int64_t)e * nrows + r) * nb * Q4_0_BYTES;
+                for (int64_t b = 0; b < nb; ++b) {
+                    const uint8_t* wb = wrow + b * Q4_0_BYTES;
+                    const uint8_t* ab = arow + b * Q8_1_BYTES;
+                    double dw = oracle_half_to_double(rd16(wb));
+                    double da = oracle_half_to_double(rd16(ab));
+                    y += dw * da * (double)oracle_block_dot(wb, ab);
+                }
+            }
+            out[s * nrows + r] = (float)y;
+        }
+    }
+}
+
 void oracle_moe_sample(const uint8_t* weights, const uint8_t* act, const int32_t* topk_ids,
                        int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows,
                        int64_t ncols, const int64_t* slots, const int64_t* rows, int64_t n,

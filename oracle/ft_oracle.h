@@ -22,6 +22,10 @@
  *   oracle_moe_slots_q4_0_q8_1                     pinned: numpy einsum of decoded
  *                                                  operands; replicated token rows
  *                                                  give oracle_moe_q4_0_q8_1 bit for bit
+ *   oracle_moe_ep_q4_0_q8_1                        pinned: the shards of a partition
+ *                                                  of the experts sum to
+ *                                                  oracle_moe_q4_0_q8_1 bit for bit;
+ *                                                  hand-checked masking
  *
  * Byte layouts (GGUF block formats; the pages serve GGUF Q4_0 checkpoints but
  * do not print the formats):
@@ -62,6 +66,10 @@ void oracle_moe_q4_0_q8_1(const uint8_t* weights, const uint8_t* act, const int3
 void oracle_moe_slots_q4_0_q8_1(const uint8_t* weights, const uint8_t* act_slots, const int32_t* topk_ids,
                                 float* out, int64_t tokens, int32_t top_k, int32_t n_experts,
                                 int64_t nrows, int64_t ncols);
+
+void oracle_moe_ep_q4_0_q8_1(const uint8_t* weights_local, const uint8_t* act, const int32_t* topk_ids,
+                             float* out, int64_t tokens, int32_t top_k, int32_t n_global,
+                             int32_t expert_start, int32_t n_local, int64_t nrows, int64_t ncols);
 
 void oracle_moe_sample(const uint8_t* weights, const uint8_t* act, const int32_t* topk_ids,
                        int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows,

@@ -367,9 +367,28 @@ def pin_moe_slots_replicated_rows(o):
     assert np.array_equal(o.moe_slots(w, act_slots, ids), o.moe(w, act, ids))
 
 
+def pin_moe_ep_shards_sum_to_full(o):
+    """A partition of the experts into shards: the shards' outputs (zero rows for
+    slots routed elsewhere) add up to the full matmul bit for bit, and a single
+    shard holding every expert is the full matmul."""
+    w, x, ids = tiny_case(seed=64, E=6, T=9, k=2)
+    act = o.quantize_q8_1(x)
+    full = o.moe(w, act, ids)
+    E = w.shape[0]
+    for bounds in [(0, 2, 6), (0, 1, 4, 6), (0, 6)]:
+        total = np.zeros_like(full)
+        for lo, hi in zip(bounds[:-1], bounds[1:]):
+            part = o.moe_ep(w[lo:hi], act, ids, E, lo)
+            local = (ids >= lo) & (ids < hi)
+            assert not part[~local].any()                     # non-local slots are zero rows
+            total += part
+        assert np.array_equal(total, full)
+
+
 ALL_PINS = [
     pin_fp16, pin_q4_0_hand, pin_q4_0_nearest_level, pin_q4_0_matches_generator, pin_q4_0_dequant,
     pin_q8_1_hand, pin_q8_1_numpy, pin_q8_1_error_bound, pin_route, pin_block_dot_hand,
     pin_moe_closed_form_vs_bruteforce, pin_moe_numpy_einsum, pin_moe_block_dots,
     pin_moe_split_invariance, pin_moe_bad_ids, pin_moe_slots_numpy_einsum, pin_moe_slots_replicated_rows,
+    pin_moe_ep_shards_sum_to_full,
 ]

@@ -9,11 +9,11 @@ synthetic-input generator used by the tests and the benchmark.
 """
 
 from ._lib import (FT_DEVERR_BAD_EXPERT_ID, FT_DEVERR_WAIT_TIMEOUT, FT_PATH_AUTO, FT_PATH_GEMM, FT_PATH_GEMV,
-                   FtError, block_dots, last_error, load, moe_q4_0_q8_1, moe_q4_0_q8_1_slots, profile_enable, profile_read, quantize_q8_1,
+                   FtError, block_dots, last_error, load, moe_q4_0_q8_1, moe_q4_0_q8_1_ep, moe_q4_0_q8_1_slots, profile_enable, profile_read, quantize_q8_1,
                    read_device_error, release, reserve, route_offsets, selected_path, set_path, workspace_bytes)
 
 __all__ = [
     "FT_DEVERR_BAD_EXPERT_ID", "FT_DEVERR_WAIT_TIMEOUT", "FT_PATH_AUTO", "FT_PATH_GEMM", "FT_PATH_GEMV", "FtError",
-    "block_dots", "last_error", "load", "moe_q4_0_q8_1", "moe_q4_0_q8_1_slots", "profile_enable", "profile_read", "quantize_q8_1", "read_device_error", "release", "reserve",
+    "block_dots", "last_error", "load", "moe_q4_0_q8_1", "moe_q4_0_q8_1_ep", "moe_q4_0_q8_1_slots", "profile_enable", "profile_read", "quantize_q8_1", "read_device_error", "release", "reserve",
     "route_offsets", "selected_path", "set_path", "workspace_bytes",
 ]

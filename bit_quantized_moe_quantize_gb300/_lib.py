@@ -27,7 +27,8 @@ PATHS = {"auto": FT_PATH_AUTO, "gemv": FT_PATH_GEMV, "gemm": FT_PATH_GEMM}
 EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_moe_workspace_bytes",
            "ft_moe_reserve", "ft_moe_release", "ft_moe_read_device_error", "ft_moe_set_path",
            "ft_moe_selected_path", "ft_moe_block_dots", "ft_last_error", "ft_abi_version", "ft_profile_enable",
-           "ft_profile_read", "ft_moe_route_offsets_noalloc", "ft_moe_q4_0_q8_1_slots")
+           "ft_profile_read", "ft_moe_route_offsets_noalloc", "ft_moe_q4_0_q8_1_slots",
+           "ft_moe_q4_0_q8_1_ep")
 
 
 class FtError(RuntimeError):
@@ -59,6 +60,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.ft_moe_route_offsets_noalloc.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp]
         L.ft_moe_q4_0_q8_1.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_moe_q4_0_q8_1_slots.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
+        L.ft_moe_q4_0_q8_1_ep.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp]
         L.ft_moe_block_dots.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_moe_workspace_bytes.argtypes = [i64, i32, i32, i64, i64]
         L.ft_moe_workspace_bytes.restype = ctypes.c_size_t
@@ -187,6 +189,22 @@ def moe_q4_0_q8_1_slots(weights, act_slots, topk_ids, out=None):
     _check(load().ft_moe_q4_0_q8_1_slots(ctypes.c_void_p(weights.data_ptr()), ctypes.c_void_p(act_slots.data_ptr()),
                                          ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, E, N, nb * 32,
                                          _stream(weights)))
+    return out
+
+
+def moe_q4_0_q8_1_ep(weights_local, act, topk_ids, n_experts_global, expert_start, out=None):
+    """Routed matmul on an expert-parallel shard (ft_moe_q4_0_q8_1_ep):
+    weights_local Q4_0 [E_local,N,K/32,18] holds experts [expert_start,
+    expert_start + E_local) of n_experts_global; topk_ids hold global ids;
+    rows of slots routed elsewhere are 0."""
+    torch = _torch()
+    E_local, N, K, T, k = _matmul_shape(weights_local, act, topk_ids)
+    if out is None:
+        out = torch.empty((T, k, N), dtype=torch.float32, device=weights_local.device)
+    po = _dev(out, torch.float32, "out")
+    _check(load().ft_moe_q4_0_q8_1_ep(ctypes.c_void_p(weights_local.data_ptr()), ctypes.c_void_p(act.data_ptr()),
+                                      ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, int(n_experts_global),
+                                      int(expert_start), E_local, N, K, _stream(weights_local)))
     return out
 
 

@@ -151,6 +151,11 @@ struct Shape {
     int64_t tokens, n_slots, nrows, ncols, nb;
     int32_t top_k, n_experts;
     int32_t act_div;   // activation row of slot s: s / act_div (top_k: one row per token; 1: one per slot)
+    // expert-parallel shard: ids are global in [0, n_global); this call holds
+    // experts [expert_start, expert_start + n_experts) (0 and n_experts otherwise)
+    int32_t expert_start, n_global;
+    // routed slots per held expert on average (what the tile plans go by)
+    double mean() const { return static_cast<double>(n_slots) / n_global; }
 };
 
 // Checks the routing arguments; fills n_slots.
@@ -168,6 +173,8 @@ static int check_route_args(int64_t tokens, int32_t top_k, int32_t n_experts, Sh
     sh->n_experts = n_experts;
     sh->n_slots = s;
     sh->act_div = top_k;
+    sh->expert_start = 0;
+    sh->n_global = n_experts;
     return FT_OK;
 }
 
@@ -316,8 +323,7 @@ static int choose_path(const Shape& sh, int setting) {
     if (setting == FT_PATH_GEMV) return FT_PATH_GEMV;
     if (setting == FT_PATH_GEMM) return FT_PATH_GEMM;
     if (!gemm_shape_ok(sh)) return FT_PATH_GEMV;
-    const double mean = static_cast<double>(sh.n_slots) / sh.n_experts;
-    return mean >= 16.0 ? FT_PATH_GEMM : FT_PATH_GEMV;
+    return sh.mean() >= 16.0 ? FT_PATH_GEMM : FT_PATH_GEMV;
 }
 
 static int run_matmul(const void* weights, const void* act, const int32_t* topk_ids, float* out, int32_t* dots,
@@ -338,13 +344,16 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     rb.tiles_gemm = reinterpret_cast<int32_t*>(ws + L.tiles_gemm);
     rb.err = reinterpret_cast<uint32_t*>(ws + L.err);
 
-    const GemvPlan gp = plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols);
+    const GemvPlan gp = plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols, sh.mean());
+    const int tile_width = gemm_tile_width(sh.mean());
     if (path == FT_PATH_GEMV && gp.smem > 227 * 1024)
         return fail(FT_ERR_SIZE, "GEMV tile needs %zu bytes of shared memory", gp.smem);
     uint32_t* zero_rows = dots ? reinterpret_cast<uint32_t*>(dots) : reinterpret_cast<uint32_t*>(out);
     const int64_t row_words = dots ? sh.nrows * sh.nb : sh.nrows;
     prof_mark(kProfRouteBegin, s);
-    if (int st = launch_route(topk_ids, sh.n_slots, sh.n_experts, rb, gp.group, gemm_tile_width(sh.n_slots, sh.n_experts),
+    rb.expert_start = sh.expert_start;
+    rb.n_global = sh.n_global;
+    if (int st = launch_route(topk_ids, sh.n_slots, sh.n_experts, rb, gp.group, tile_width,
                               zero_rows, row_words, s))
         return st;
     if (path == FT_PATH_GEMM && sh.n_slots > 0) {
@@ -362,7 +371,8 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     else
         st = launch_gemm(static_cast<const uint8_t*>(weights), static_cast<const uint8_t*>(act), rb.perm,
                          rb.offsets, rb.tiles_gemm, out, dots, rb.err, sh.n_slots, sh.act_div, sh.n_experts, sh.nrows,
-                         sh.ncols, reinterpret_cast<uint16_t*>(ws + L.xh), reinterpret_cast<uint16_t*>(ws + L.da), s);
+                         sh.ncols, reinterpret_cast<uint16_t*>(ws + L.xh), reinterpret_cast<uint16_t*>(ws + L.da),
+                         tile_width, s);
     prof_mark(kProfMatmulEnd, s);
     return st;
 }
@@ -419,11 +429,20 @@ int ft_moe_route_offsets(const int32_t* topk_ids, int64_t tokens, int32_t top_k,
 
 static int matmul_entry(const void* weights, const void* act, const int32_t* topk_ids, float* out, int32_t* dots,
                         int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols,
-                        void* stream, bool act_per_slot = false) {
+                        void* stream, bool act_per_slot = false, int32_t expert_start = 0, int32_t n_local = 0) {
     g_last_error.clear();
     Shape sh{};
+    // n_experts counts every expert the ids may name; an expert-parallel shard
+    // (n_local > 0) holds experts [expert_start, expert_start + n_local) of them
     if (int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh)) return st;
     if (act_per_slot) sh.act_div = 1;
+    if (n_local > 0) {
+        if (expert_start < 0 || static_cast<int64_t>(expert_start) + n_local > n_experts)
+            return fail(FT_ERR_ARG, "the shard's experts [%d, %lld) must lie in [0, n_experts_global=%d)", expert_start,
+                        (long long)expert_start + n_local, n_experts);
+        sh.expert_start = expert_start;
+        sh.n_experts = n_local;
+    }
     if (sh.n_slots == 0) return FT_OK;
     if (!weights || !act || !topk_ids || (!out && !dots)) return fail(FT_ERR_ARG, "null pointer");
     if (!aligned(weights, 16) || !aligned(act, 16))
@@ -448,6 +467,24 @@ int ft_moe_q4_0_q8_1(const void* weights, const void* act, const int32_t* topk_i
         return fail(FT_ERR_ARG, "null pointer");
     }
     return matmul_entry(weights, act, topk_ids, out, nullptr, tokens, top_k, n_experts, nrows, ncols, stream);
+}
+
+int ft_moe_q4_0_q8_1_ep(const void* weights_local, const void* act, const int32_t* topk_ids, float* out,
+                        int64_t tokens, int32_t top_k, int32_t n_experts_global, int32_t expert_start,
+                        int32_t n_experts_local, int64_t nrows, int64_t ncols, void* stream) {
+    if (n_experts_local < 1) {
+        g_last_error.clear();
+        return fail(FT_ERR_ARG, "n_experts_local must be >= 1 (got %d)", n_experts_local);
+    }
+    if (!out) {
+        g_last_error.clear();
+        Shape sh{};
+        if (int st = check_matmul_args(tokens, top_k, n_experts_global, nrows, ncols, &sh)) return st;
+        if (sh.n_slots == 0) return FT_OK;
+        return fail(FT_ERR_ARG, "null pointer");
+    }
+    return matmul_entry(weights_local, act, topk_ids, out, nullptr, tokens, top_k, n_experts_global, nrows, ncols,
+                        stream, false, expert_start, n_experts_local);
 }
 
 int ft_moe_q4_0_q8_1_slots(const void* weights, const void* act_slots, const int32_t* topk_ids, float* out,

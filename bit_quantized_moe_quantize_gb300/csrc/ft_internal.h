@@ -39,6 +39,12 @@ struct RouteBuffers {
     int32_t* tiles_gemv;   // [E+1] or nullptr
     int32_t* tiles_gemm;   // [E+1] or nullptr
     uint32_t* err;
+    // Expert-parallel shard: ids are global, the routed experts are
+    // [expert_start, expert_start + n_experts) of n_global (0 = n_experts);
+    // other valid ids are left out (zero rows, no error), ids outside
+    // [0, n_global) raise FT_DEVERR_BAD_EXPERT_ID.
+    int32_t expert_start;
+    int32_t n_global;
 };
 
 inline int64_t route_chunks(int64_t n_slots) { return (n_slots + kRouteChunk - 1) / kRouteChunk; }
@@ -63,7 +69,8 @@ struct GemvPlan {
     size_t smem;
 };
 
-GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols);
+// mean: routed slots per expert on average (decides the slots per tile)
+GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols, double mean);
 
 int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act, const int32_t* perm,
                 const int32_t* offsets, const int32_t* tiles, float* out, int32_t* dots, uint32_t* err,
@@ -75,7 +82,7 @@ constexpr int kGemmBM = 128;   // weight rows per tile
 
 // Slot-tile width (32 or 128) the tensor-core path uses for this batch; the
 // router's GEMM tile prefix must be built with the same width.
-int gemm_tile_width(int64_t n_slots, int32_t n_experts);
+int gemm_tile_width(double mean_slots_per_expert);
 
 inline int64_t gemm_rows(int64_t n_slots) { return (n_slots + kGemmBN - 1) / kGemmBN * kGemmBN; }
 
@@ -86,6 +93,7 @@ int launch_gather(const uint8_t* act, const int32_t* perm, const int32_t* offset
                   int64_t nb, int64_t n_slots, uint16_t* xh, uint16_t* da, cudaStream_t s);
 int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
                 const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
-                int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, cudaStream_t s);
+                int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, int tile_width,
+                cudaStream_t s);
 
 }  // namespace ft

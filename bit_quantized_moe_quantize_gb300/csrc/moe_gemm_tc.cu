@@ -688,19 +688,20 @@ static int launch_gemm_bn(const uint8_t* weights, const int32_t* perm, const int
     return check_launch("moe_gemm_tc_kernel", grid, block, C::SMEM_BYTES);
 }
 
-int gemm_tile_width(int64_t n_slots, int32_t n_experts) {
+int gemm_tile_width(double mean_slots_per_expert) {
     // narrow slot tiles while experts see few slots each (the drain then scales
     // 32 instead of 128 columns per block); measured crossover between 32 and
     // 64 slots per expert
-    return static_cast<double>(n_slots) / n_experts < 48.0 ? 32 : kGemmBN;
+    return mean_slots_per_expert < 48.0 ? 32 : kGemmBN;
 }
 
 int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
                 const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
-                int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, cudaStream_t s) {
+                int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, int tile_width,
+                cudaStream_t s) {
     (void)act;   // read by launch_gather, which the caller runs first
     if (n_slots == 0) return FT_OK;
-    if (gemm_tile_width(n_slots, n_experts) == 32)
+    if (tile_width == 32)
         return launch_gemm_bn<32>(weights, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,
                                   ncols, xh, da, s);
     return launch_gemm_bn<kGemmBN>(weights, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,

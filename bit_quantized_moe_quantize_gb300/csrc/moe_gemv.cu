@@ -504,10 +504,9 @@ __global__ void __launch_bounds__(288) moe_gemv_rows_kernel(const __grid_constan
     }
 }
 
-GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols) {
+GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols, double mean) {
     GemvPlan p{};
     const int64_t nb = ncols / QK;
-    const double mean = static_cast<double>(n_slots) / n_experts;
     p.group = mean <= 1.0 ? 1 : mean <= 2.0 ? 2 : mean <= 4.0 ? 4 : 8;
     if (ncols % 256 == 0) {
         // row-per-lane kernel.  KS warps per row group so that the batch
@@ -515,7 +514,10 @@ GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t nc
         // (RW, RW * KS <= 8) as still leave two CTAs per SM; a ring of
         // 2 KS boxes when the K range is split, else as deep as ~110 KB allows;
         // grid.y sized so that every CTA is resident at once.
-        const int64_t min_tiles = (n_slots + p.group - 1) / p.group;
+        // expected routed slots (an expert-parallel shard routes only its share)
+        const double expect = mean * n_experts < static_cast<double>(n_slots) ? mean * n_experts : n_slots;
+        const int64_t local = static_cast<int64_t>(expect + 0.999);
+        const int64_t min_tiles = local > 0 ? (local + p.group - 1) / p.group : 1;
         const int64_t groups32 = (nrows + 31) / 32;
         const int64_t sms = sm_count();
         const int64_t n_ks = nb / 8;

@@ -41,16 +41,18 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 // Step 1 for one warp and its chunk: histogram of the chunk's expert ids in
 // row[E] (shared memory), bad ids flagged in err.
 __device__ void route_hist_chunk(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts, int64_t chunk,
-                                 int32_t* row, uint32_t* err) {
+                                 int32_t* row, uint32_t* err, int32_t expert_start, int32_t n_global) {
     const uint32_t lane = lane_id();
     for (int32_t e = lane; e < n_experts; e += 32) row[e] = 0;
     __syncwarp();
     bool saw_bad = false;
     for (int step = 0; step < kRouteChunk / 32; ++step) {
         const int64_t s = chunk * kRouteChunk + step * 32 + lane;
-        const int32_t e = s < n_slots ? ids[s] : -1;
-        const bool valid = s < n_slots && e >= 0 && e < n_experts;
-        saw_bad |= (s < n_slots) && !valid;
+        const int32_t g = s < n_slots ? ids[s] : -1;              // global expert id
+        const int64_t el = static_cast<int64_t>(g) - expert_start;  // routed expert (this shard's numbering)
+        const bool valid = s < n_slots && el >= 0 && el < n_experts;
+        const int32_t e = static_cast<int32_t>(el);
+        saw_bad |= (s < n_slots) && (g < 0 || g >= n_global);     // only ids no shard owns are errors
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
         if (valid && lane == static_cast<uint32_t>(__ffs(peers) - 1)) row[e] += __popc(peers);
         __syncwarp();
@@ -61,13 +63,13 @@ __device__ void route_hist_chunk(const int32_t* __restrict__ ids, int64_t n_slot
 
 __global__ void __launch_bounds__(32 * kRouteWarps)
     route_hist_kernel(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts, int64_t n_chunks,
-                      int32_t* __restrict__ hist, uint32_t* err) {
+                      int32_t* __restrict__ hist, uint32_t* err, int32_t expert_start, int32_t n_global) {
     extern __shared__ int32_t sh_hist[];
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
     const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
     if (chunk >= n_chunks) return;
     int32_t* row = sh_hist + static_cast<int64_t>(warp) * n_experts;
-    route_hist_chunk(ids, n_slots, n_experts, chunk, row, err);
+    route_hist_chunk(ids, n_slots, n_experts, chunk, row, err, expert_start, n_global);
     int32_t* grow = hist + chunk * n_experts;
     for (int32_t e = lane; e < n_experts; e += 32) grow[e] = row[e];
 }
@@ -195,12 +197,13 @@ __global__ void __launch_bounds__(1024)
 // chunk's first position per expert.
 __device__ void route_scatter_chunk(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts,
                                     int64_t chunk, int32_t* cur, int32_t* __restrict__ perm,
-                                    uint32_t* __restrict__ zero_rows, int64_t row_words) {
+                                    uint32_t* __restrict__ zero_rows, int64_t row_words, int32_t expert_start) {
     const uint32_t lane = lane_id();
     for (int step = 0; step < kRouteChunk / 32; ++step) {
         const int64_t s = chunk * kRouteChunk + step * 32 + lane;
-        const int32_t e = s < n_slots ? ids[s] : -1;
-        const bool valid = s < n_slots && e >= 0 && e < n_experts;
+        const int64_t el = static_cast<int64_t>(s < n_slots ? ids[s] : -1) - expert_start;
+        const bool valid = s < n_slots && el >= 0 && el < n_experts;
+        const int32_t e = static_cast<int32_t>(el);
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
         int32_t pos = 0;
         if (valid) pos = cur[e] + __popc(peers & lanemask_lt());
@@ -225,7 +228,8 @@ __device__ __forceinline__ void route_perm_tail(const int32_t* __restrict__ offs
 __global__ void __launch_bounds__(32 * kRouteWarps)
     route_scatter_kernel(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts, int64_t n_chunks,
                          const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
-                         int32_t* __restrict__ perm, uint32_t* __restrict__ zero_rows, int64_t row_words) {
+                         int32_t* __restrict__ perm, uint32_t* __restrict__ zero_rows, int64_t row_words,
+                         int32_t expert_start) {
     extern __shared__ int32_t sh_cursor[];
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
     route_perm_tail(offsets, n_experts, n_slots, perm, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(32 * kRouteWarps)
     const int32_t* brow = base + chunk * n_experts;
     for (int32_t e = lane; e < n_experts; e += 32) cur[e] = brow[e];
     __syncwarp();
-    route_scatter_chunk(ids, n_slots, n_experts, chunk, cur, perm, zero_rows, row_words);
+    route_scatter_chunk(ids, n_slots, n_experts, chunk, cur, perm, zero_rows, row_words, expert_start);
 }
 
 // All three steps in one CTA of 1024 threads (32 warps, one chunk each) for
@@ -245,19 +249,22 @@ __global__ void __launch_bounds__(1024)
     route_small_kernel(const int32_t* __restrict__ ids, int64_t n_slots, int32_t n_experts, int64_t n_chunks,
                        int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                        int32_t* __restrict__ tiles_gemv, int32_t gemv_group, int32_t* __restrict__ tiles_gemm,
-                       int32_t gemm_group, uint32_t* err, uint32_t* __restrict__ zero_rows, int64_t row_words) {
+                       int32_t gemm_group, uint32_t* err, uint32_t* __restrict__ zero_rows, int64_t row_words,
+                       int32_t expert_start, int32_t n_global) {
     extern __shared__ int32_t sh_small[];
     int32_t* hist = sh_small;                                            // [n_chunks][E]
     int32_t* scan_sh = sh_small + n_chunks * static_cast<int64_t>(n_experts);
     const uint32_t warp = threadIdx.x >> 5;
-    if (warp < n_chunks) route_hist_chunk(ids, n_slots, n_experts, warp, hist + warp * n_experts, err);
+    if (warp < n_chunks)
+        route_hist_chunk(ids, n_slots, n_experts, warp, hist + warp * n_experts, err, expert_start, n_global);
     __syncthreads();
     route_scan_body(hist, n_chunks, n_experts, counts, offsets, tiles_gemv, gemv_group, tiles_gemm, gemm_group,
                     scan_sh);
     __syncthreads();
     route_perm_tail(offsets, n_experts, n_slots, perm, threadIdx.x, blockDim.x);
-    if (warp < n_chunks) route_scatter_chunk(ids, n_slots, n_experts, warp, hist + warp * n_experts, perm, zero_rows,
-                                             row_words);
+    if (warp < n_chunks)
+        route_scatter_chunk(ids, n_slots, n_experts, warp, hist + warp * n_experts, perm, zero_rows, row_words,
+                            expert_start);
 }
 
 int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const RouteBuffers& b,
@@ -269,6 +276,7 @@ int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const R
         if (int st = set_smem_limit(reinterpret_cast<const void*>(route_scatter_kernel), big)) return st;
     }
     const int64_t n_chunks = route_chunks(n_slots);
+    const int32_t start = b.expert_start, n_global = b.n_global > 0 ? b.n_global : n_experts;
     const int32_t P = n_experts >= 1024 ? 1 : 1024 / n_experts;
     const size_t scan_sm = (static_cast<size_t>(P) * n_experts + 2 * static_cast<size_t>(n_experts) + 32) *
                            sizeof(int32_t);
@@ -277,7 +285,7 @@ int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const R
         if (int st = set_smem_limit(reinterpret_cast<const void*>(route_small_kernel), static_cast<int>(sm))) return st;
         route_small_kernel<<<1, 1024, sm, s>>>(ids, n_slots, n_experts, n_chunks, b.counts, b.offsets, b.perm,
                                                b.tiles_gemv, gemv_group, b.tiles_gemm, gemm_group, b.err, zero_rows,
-                                               row_words);
+                                               row_words, start, n_global);
         return check_launch("route_small_kernel", dim3(1), dim3(1024), sm);
     }
     const int64_t ctas = (n_chunks + kRouteWarps - 1) / kRouteWarps;
@@ -285,7 +293,8 @@ int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const R
     const size_t sm_rows = static_cast<size_t>(kRouteWarps) * n_experts * sizeof(int32_t);
     if (ctas > 0) {
         const dim3 grid(static_cast<unsigned>(ctas));
-        route_hist_kernel<<<grid, block, sm_rows, s>>>(ids, n_slots, n_experts, n_chunks, b.hist, b.err);
+        route_hist_kernel<<<grid, block, sm_rows, s>>>(ids, n_slots, n_experts, n_chunks, b.hist, b.err, start,
+                                                       n_global);
         if (int st = check_launch("route_hist_kernel", grid, block, sm_rows)) return st;
     }
     route_scan_kernel<<<1, 1024, scan_sm, s>>>(b.hist, n_chunks, n_experts, b.counts, b.offsets, b.tiles_gemv,
@@ -294,7 +303,7 @@ int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const R
     if (ctas > 0) {
         const dim3 grid(static_cast<unsigned>(ctas));
         route_scatter_kernel<<<grid, block, sm_rows, s>>>(ids, n_slots, n_experts, n_chunks, b.hist, b.offsets,
-                                                          b.perm, zero_rows, row_words);
+                                                          b.perm, zero_rows, row_words, start);
         if (int st = check_launch("route_scatter_kernel", grid, block, sm_rows)) return st;
     }
     return FT_OK;

@@ -195,6 +195,29 @@ FT_API int ft_moe_q4_0_q8_1_slots(const void* weights, const void* act_slots, co
                                   int64_t nrows, int64_t ncols, void* stream);
 
 /*
+ * ft_moe_q4_0_q8_1_ep - the matmul on one expert-parallel shard: topk_ids
+ * hold global expert ids, the shard holds experts [expert_start,
+ * expert_start + n_experts_local) of n_experts_global, a slot routed to one
+ * of them is computed with local expert id - expert_start, and every other
+ * slot's output row is written as 0 (nvfp4-megamoe-kernel CURRENT_BUG.md,
+ * Bug 8: global ids remapped by experts_start_idx, non-local tokens masked),
+ * so the outputs of shards that partition the experts add up to the full
+ * result.  Only ids outside [0, n_experts_global) raise
+ * FT_DEVERR_BAD_EXPERT_ID.
+ *
+ *   weights_local  device, Q4_0 [n_experts_local][nrows][ncols/32]; 16-byte aligned
+ *   act, topk_ids, out, tokens, top_k, nrows, ncols as for ft_moe_q4_0_q8_1
+ * Needs 1 <= top_k <= n_experts_global <= FT_MAX_EXPERTS, n_experts_local >= 1,
+ * 0 <= expert_start and expert_start + n_experts_local <= n_experts_global.
+ * Errors as for ft_moe_q4_0_q8_1.  The path choice and the tile plans assume
+ * the slots spread evenly over the global experts.
+ */
+FT_API int ft_moe_q4_0_q8_1_ep(const void* weights_local, const void* act, const int32_t* topk_ids,
+                               float* out, int64_t tokens, int32_t top_k, int32_t n_experts_global,
+                               int32_t expert_start, int32_t n_experts_local, int64_t nrows,
+                               int64_t ncols, void* stream);
+
+/*
  * ft_moe_workspace_bytes - bytes of library workspace that one
  * ft_moe_q4_0_q8_1 / ft_moe_route_offsets call of this shape needs.
  * Returns 0 for invalid arguments.

@@ -77,6 +77,8 @@ class Oracle:
         L.oracle_moe_ep_q4_0_q8_1.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i32, i64, i64]
         L.oracle_moe_block_dots.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.oracle_moe_dequant_bruteforce.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp]
+        L.oracle_act_mul.argtypes = [vp, i64, i64, i32, vp]
+        L.oracle_act_mul_quantize_q8_1.argtypes = [vp, i64, i64, i32, vp]
         self.lib = L
         self.path = so_path
 
@@ -117,6 +119,40 @@ class Oracle:
         out = np.empty(nb * QK, dtype=np.float64)
         self.lib.oracle_dequantize_q8_1(_p(blocks), nb, _p(out))
         return out.reshape(*blocks.shape[:-2], blocks.shape[-2] * QK)
+
+    # gated activation ------------------------------------------------
+    ACT_SILU = 0
+    ACT_GELU_TANH = 1
+
+    def act_mul(self, h: np.ndarray, kind: int) -> np.ndarray:
+        """a = act(h[..., :I]) * h[..., I:] in fp64, rounded to fp32."""
+        h = np.ascontiguousarray(h, dtype=np.float32)
+        two_i = h.shape[-1]
+        assert two_i % 2 == 0
+        rows = h.size // two_i if two_i else 0
+        out = np.empty((*h.shape[:-1], two_i // 2), dtype=np.float32)
+        self.lib.oracle_act_mul(_p(h), rows, two_i // 2, int(kind), _p(out))
+        return out
+
+    def act_mul_quantize_q8_1(self, h: np.ndarray, kind: int) -> np.ndarray:
+        """Q8_1 rows [..., I/32, 36] of act_mul(h, kind)."""
+        h = np.ascontiguousarray(h, dtype=np.float32)
+        two_i = h.shape[-1]
+        assert two_i % (2 * QK) == 0
+        rows = h.size // two_i if two_i else 0
+        out = np.empty((*h.shape[:-1], two_i // 2 // QK, Q8_1_BYTES), dtype=np.uint8)
+        self.lib.oracle_act_mul_quantize_q8_1(_p(h), rows, two_i // 2, int(kind), _p(out))
+        return out
+
+    def moe_ffn(self, w13, w2, act, topk_ids, kind: int):
+        """Both expert layers of the routed MoE block, per slot: h = W13 x (gate |
+        up rows), a = Q8_1(act(gate) * up), out = W2 a -> [T, k, hidden] fp32,
+        with h and a returned too."""
+        h = self.moe(w13, act, topk_ids)
+        T, k = np.asarray(topk_ids).shape
+        a = self.act_mul_quantize_q8_1(h.reshape(T * k, -1), kind)
+        out = self.moe_slots(w2, a, topk_ids)
+        return out, h, a
 
     # route -----------------------------------------------------------
     def route(self, topk_ids: np.ndarray, n_experts: int):

@@ -138,6 +138,31 @@ void oracle_dequantize_q4_0(const uint8_t* blocks, int64_t n_blocks, double* out
  * per 32-block of an fp16 row, in fp32: amax = max |x|, d = amax / 127,
  * q = round(x / d) clamped to [-127, 127] (0 when amax == 0), s = d * sum q.
  * d and s are stored as fp16. */
+/* One Q8_1 block from 32 fp32 values, in single precision as quantize_row_q8_1
+ * defines it (FreeToken PR #185, "Fix"): d = amax / 127, q = round(x / d)
+ * clamped to [-127, 127], s = d * sum(q); d and s stored as fp16. */
+static void quantize_block_q8_1(const float* x, uint8_t* o)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < QK; ++i)
+        if (fabsf(x[i]) > amax) amax = fabsf(x[i]);
+    float d = amax / 127.0f;
+    int sum = 0;
+    for (int i = 0; i < QK; ++i) {
+        int q = 0;
+        if (amax != 0.0f) {
+            q = (int)roundf(x[i] / d);
+            if (q < -127) q = -127;
+            if (q > 127) q = 127;
+        }
+        sum += q;
+        o[4 + i] = (uint8_t)(int8_t)q;
+    }
+    float s = d * (float)sum;
+    wr16(o, oracle_float_to_half(d));
+    wr16(o + 2, oracle_float_to_half(s));
+}
+
 void oracle_quantize_q8_1(const uint16_t* x_fp16, int64_t tokens, int64_t ncols, uint8_t* out)
 {
     int64_t nb = ncols / QK;
@@ -146,25 +171,7 @@ void oracle_quantize_q8_1(const uint16_t* x_fp16, int64_t tokens, int64_t ncols,
             float x[QK];
             for (int i = 0; i < QK; ++i)
                 x[i] = (float)oracle_half_to_double(x_fp16[t * ncols + b * QK + i]);
-            float amax = 0.0f;
-            for (int i = 0; i < QK; ++i)
-                if (fabsf(x[i]) > amax) amax = fabsf(x[i]);
-            float d = amax / 127.0f;
-            int sum = 0;
-            uint8_t* o = out + (t * nb + b) * Q8_1_BYTES;
-            for (int i = 0; i < QK; ++i) {
-                int q = 0;
-                if (amax != 0.0f) {
-                    q = (int)roundf(x[i] / d);
-                    if (q < -127) q = -127;
-                    if (q > 127) q = 127;
-                }
-                sum += q;
-                o[4 + i] = (uint8_t)(int8_t)q;
-            }
-            float s = d * (float)sum;
-            wr16(o, oracle_float_to_half(d));
-            wr16(o + 2, oracle_float_to_half(s));
+            quantize_block_q8_1(x, out + (t * nb + b) * Q8_1_BYTES);
         }
     }
 }
@@ -177,6 +184,50 @@ void oracle_dequantize_q8_1(const uint8_t* blocks, int64_t n_blocks, double* out
         for (int i = 0; i < QK; ++i)
             out[b * QK + i] = (double)(int8_t)blk[4 + i] * d;
     }
+}
+
+/* ----------------------------------------------------- gated activation */
+
+/* The two gated activations that sit between the expert layers: GELU in its
+ * tanh form (flashinfer gelu_tanh_and_mul, called right after the routed
+ * matmul on FreeToken PR #185, "Problem") and SiLU (the "SiLU*up" step between
+ * the two expert layers on nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 6).
+ *   silu(g)      = g / (1 + exp(-g))
+ *   gelu_tanh(g) = g/2 * (1 + tanh(sqrt(2/pi) * (g + 0.044715 g^3)))
+ * Both in fp64. */
+static double act_fn(double g, int32_t kind)
+{
+    if (kind == ORACLE_ACT_SILU)
+        return g / (1.0 + exp(-g));
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    return 0.5 * g * (1.0 + tanh(c * (g + 0.044715 * g * g * g)));
+}
+
+/* a[r][i] = act(h[r][i]) * h[r][n_inter + i], computed in fp64 and rounded
+ * once to fp32: the first half of each row of h is the gate, the second half
+ * the up projection (the gate/up row order of the fused expert weight). */
+void oracle_act_mul(const float* h, int64_t rows, int64_t n_inter, int32_t kind, float* a)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* hr = h + r * 2 * n_inter;
+        for (int64_t i = 0; i < n_inter; ++i)
+            a[r * n_inter + i] = (float)(act_fn((double)hr[i], kind) * (double)hr[n_inter + i]);
+    }
+}
+
+/* oracle_act_mul followed by the Q8_1 quantizer on its fp32 result, one Q8_1
+ * row of n_inter / 32 blocks per row of h. */
+void oracle_act_mul_quantize_q8_1(const float* h, int64_t rows, int64_t n_inter, int32_t kind, uint8_t* out)
+{
+    int64_t nb = n_inter / QK;
+    float* a = (float*)malloc((size_t)(n_inter > 0 ? n_inter : 1) * sizeof(float));
+    if (!a) abort();
+    for (int64_t r = 0; r < rows; ++r) {
+        oracle_act_mul(h + r * 2 * n_inter, 1, n_inter, kind, a);
+        for (int64_t b = 0; b < nb; ++b)
+            quantize_block_q8_1(a + b * QK, out + (r * nb + b) * Q8_1_BYTES);
+    }
+    free(a);
 }
 
 /* ----------------------------------------------------------------- route */

@@ -26,6 +26,11 @@
  *                                                  of the experts sum to
  *                                                  oracle_moe_q4_0_q8_1 bit for bit;
  *                                                  hand-checked masking
+ *   oracle_act_mul / _quantize_q8_1                pinned: scipy expit and the exact
+ *                                                  GELU x*Phi(x) within the tanh
+ *                                                  form's error, f(x) - f(-x) = x,
+ *                                                  gate/up order, hand values; the
+ *                                                  quantizer replayed in numpy fp32
  *
  * Byte layouts (GGUF block formats; the pages serve GGUF Q4_0 checkpoints but
  * do not print the formats):
@@ -35,6 +40,7 @@
  *       s = d * sum(q).
  *   weights [E][N][K/32] Q4_0, activations [T][K/32] Q8_1,
  *   topk_ids [T][k] int32 (slot s = t*k + j), out [T][k][N] fp32.
+ *   gated activation: h [rows][2 * n_inter] fp32 (gate | up), a [rows][n_inter].
  */
 #ifndef FT_ORACLE_H
 #define FT_ORACLE_H
@@ -53,6 +59,11 @@ void oracle_dequantize_q4_0(const uint8_t* blocks, int64_t n_blocks, double* out
 
 void oracle_quantize_q8_1(const uint16_t* x_fp16, int64_t tokens, int64_t ncols, uint8_t* out);
 void oracle_dequantize_q8_1(const uint8_t* blocks, int64_t n_blocks, double* out);
+
+#define ORACLE_ACT_SILU 0
+#define ORACLE_ACT_GELU_TANH 1
+void oracle_act_mul(const float* h, int64_t rows, int64_t n_inter, int32_t kind, float* a);
+void oracle_act_mul_quantize_q8_1(const float* h, int64_t rows, int64_t n_inter, int32_t kind, uint8_t* out);
 
 int64_t oracle_route(const int32_t* topk_ids, int64_t n_slots, int32_t n_experts,
                      int32_t* counts, int32_t* offsets, int32_t* perm);

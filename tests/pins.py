@@ -385,10 +385,103 @@ def pin_moe_ep_shards_sum_to_full(o):
         assert np.array_equal(total, full)
 
 
+# ------------------------------------------------------- gated activation
+def _act_inputs(seed, rows=5, n_inter=96):
+    rng = np.random.default_rng(seed)
+    h = (rng.standard_normal((rows, 2 * n_inter)) * 3).astype(np.float32)
+    h[0, :8] = [0.0, -0.0, 1e-30, -1e-30, 40.0, -40.0, 1000.0, -1000.0]
+    h[1, :n_inter] = np.linspace(-12, 12, n_inter, dtype=np.float32)
+    return h
+
+
+def _ulp32(x):
+    return np.spacing(np.abs(x).astype(np.float32)).astype(np.float64)
+
+
+def pin_act_library(o):
+    """act_mul against library activations in fp64 (torch.nn.functional.silu and
+    gelu(approximate="tanh")), up half applied after: within one fp32 ulp, plus
+    1e-15 |g u| for the cancellation in 1 + tanh(.) deep in the negative tail,
+    where two fp64 tanh routines may differ by an ulp of 1."""
+    import torch
+    import torch.nn.functional as F
+    h = _act_inputs(11)
+    n = h.shape[1] // 2
+    g = torch.from_numpy(h[:, :n].astype(np.float64))
+    u = h[:, n:].astype(np.float64)
+    for kind, fn in ((o.ACT_SILU, F.silu), (o.ACT_GELU_TANH, lambda t: F.gelu(t, approximate="tanh"))):
+        ref = fn(g).numpy() * u
+        a = o.act_mul(h, kind).astype(np.float64)
+        tol = _ulp32(ref) + 1e-15 * np.abs(g.numpy() * u) + 1e-45
+        assert np.all(np.abs(a - ref) <= tol), kind
+        assert np.mean(a == ref.astype(np.float32)) > 0.98
+
+
+def pin_act_gelu_vs_erf(o):
+    """The tanh form stays within 5e-4 of the exact GELU x * Phi(x) (its known
+    approximation error is 4.7e-4); a dropped cubic term is off by 3e-2."""
+    from scipy.special import erf
+    g = np.linspace(-10, 10, 4001).astype(np.float32)
+    h = np.concatenate([g, np.ones_like(g)])[None, :]
+    a = o.act_mul(h, o.ACT_GELU_TANH)[0].astype(np.float64)
+    gd = g.astype(np.float64)
+    exact = 0.5 * gd * (1.0 + erf(gd / np.sqrt(2.0)))
+    assert np.abs(a - exact).max() < 5e-4
+
+
+def pin_act_odd_identity(o):
+    """Both activations satisfy f(x) - f(-x) = x (1 - sigmoid(x) = sigmoid(-x),
+    tanh odd); with up = 1 each output carries one fp32 rounding."""
+    g = np.concatenate([np.linspace(-30, 30, 601), [1e-3, 0.25, 7.5]]).astype(np.float32)
+    n = g.size
+    h = np.zeros((2, 2 * n), np.float32)
+    h[0, :n], h[1, :n] = g, -g
+    h[:, n:] = 1.0
+    for kind in (o.ACT_SILU, o.ACT_GELU_TANH):
+        a = o.act_mul(h, kind).astype(np.float64)
+        diff = a[0] - a[1]
+        assert np.all(np.abs(diff - g) <= _ulp32(a[0]) + _ulp32(a[1]) + 1e-45), kind
+
+
+def pin_act_hand(o):
+    """Gate/up order and hand values: silu(0) * u = 0, silu(g) -> g for large g,
+    silu(g) -> 0 for very negative g, silu(ln 3) = (3/4) ln 3, and the up half
+    multiplies (a gate of 0 zeroes the output whatever the up value)."""
+    h = np.array([[0.0, 50.0, -200.0, np.log(3.0), 5.0, 0.0, 2.0, 1.0,
+                   7.0, 2.0, 3.0, 4.0, 0.0, 9.0, 1.0, -3.0]], dtype=np.float32)
+    a = o.act_mul(h, o.ACT_SILU)[0]
+    assert a[0] == 0.0                                   # gate 0, up 7
+    assert a[1] == np.float32(100.0)                     # 50 * sigmoid(50) rounds to 50; times up 2
+    assert a[2] == 0.0 and np.signbit(a[2])              # -200 / (1 + e^200) = -0 (times up 3)
+    ln3 = np.float64(np.float32(np.log(3.0)))
+    assert abs(float(a[3]) - 4.0 * ln3 / (1.0 + 1.0 / 3.0 * np.exp(np.log(3.0) - ln3))) < 1e-6
+    assert a[4] == 0.0                                   # up 0
+    assert a[5] == 0.0                                   # gate 0, up 9
+    assert abs(float(a[6]) - 2.0 / (1.0 + np.exp(-2.0))) < 1e-6
+    assert abs(float(a[7]) + 3.0 / (1.0 + np.exp(-1.0))) < 1e-6
+
+
+def pin_act_quantize_numpy(o):
+    """act_mul_quantize_q8_1 is the fp32 Q8_1 replay applied to act_mul's output,
+    one row of I/32 blocks per row of h."""
+    h = _act_inputs(12, rows=6, n_inter=128)
+    h[2, :128] = 0.0                                      # a row of zero blocks
+    for kind in (o.ACT_SILU, o.ACT_GELU_TANH):
+        blk = o.act_mul_quantize_q8_1(h, kind)
+        assert blk.shape == (6, 4, 36)
+        d, s, q = _q8_numpy_fp32(o.act_mul(h, kind))
+        b = blk.reshape(-1, 36)
+        assert np.array_equal(b[:, 0:2].copy().view(np.uint16)[:, 0], d.view(np.uint16))
+        assert np.array_equal(b[:, 2:4].copy().view(np.uint16)[:, 0], s.view(np.uint16))
+        assert np.array_equal(b[:, 4:].view(np.int8).astype(np.int64), q)
+        assert not blk[2].any()
+
+
 ALL_PINS = [
     pin_fp16, pin_q4_0_hand, pin_q4_0_nearest_level, pin_q4_0_matches_generator, pin_q4_0_dequant,
     pin_q8_1_hand, pin_q8_1_numpy, pin_q8_1_error_bound, pin_route, pin_block_dot_hand,
     pin_moe_closed_form_vs_bruteforce, pin_moe_numpy_einsum, pin_moe_block_dots,
     pin_moe_split_invariance, pin_moe_bad_ids, pin_moe_slots_numpy_einsum, pin_moe_slots_replicated_rows,
-    pin_moe_ep_shards_sum_to_full,
+    pin_moe_ep_shards_sum_to_full, pin_act_library, pin_act_gelu_vs_erf, pin_act_odd_identity, pin_act_hand,
+    pin_act_quantize_numpy,
 ]

@@ -50,6 +50,12 @@ MUTANTS = {
     "route_unstable": ("perm[offsets[e] + cursor[e]] = (int32_t)s;",
                        "perm[offsets[e] + counts[e] - 1 - cursor[e]] = (int32_t)s;"),
     "fp16_truncates": ("double q = nearbyint(m * 2048.0);", "double q = floor(m * 2048.0);"),
+    "silu_sign": ("return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
+    "gelu_drops_cubic": ("(g + 0.044715 * g * g * g)", "(g)"),
+    "gelu_drops_half": ("return 0.5 * g * (1.0 + tanh(", "return g * (1.0 + tanh("),
+    "gate_up_swapped": ("(act_fn((double)hr[i], kind) * (double)hr[n_inter + i])",
+                        "(act_fn((double)hr[n_inter + i], kind) * (double)hr[i])"),
+    "act_kind_swapped": ("if (kind == ORACLE_ACT_SILU)", "if (kind != ORACLE_ACT_SILU)"),
     "bad_id_not_zeroed": ("    if (e < 0 || e >= n_experts)\n        return 0.0;\n",
                           "    if (e < 0 || e >= n_experts)\n        e = 0;\n"),
 }

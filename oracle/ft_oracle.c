@@ -193,14 +193,17 @@ void oracle_dequantize_q8_1(const uint8_t* blocks, int64_t n_blocks, double* out
  * matmul on FreeToken PR #185, "Problem") and SiLU (the "SiLU*up" step between
  * the two expert layers on nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 6).
  *   silu(g)      = g / (1 + exp(-g))
- *   gelu_tanh(g) = g/2 * (1 + tanh(sqrt(2/pi) * (g + 0.044715 g^3)))
- * Both in fp64. */
+ *   gelu_tanh(g) = g/2 * (1 + tanh(y)),  y = sqrt(2/pi) * (g + 0.044715 g^3)
+ * Both in fp64.  gelu_tanh is evaluated as g / (1 + exp(-2 y)), the same
+ * function since (1 + tanh(y)) / 2 = 1 / (1 + exp(-2 y)): written with tanh,
+ * 1 + tanh(y) cancels to nothing (or to a few ulps of 1) for g below about -6,
+ * where the exact value is tiny but not zero. */
 static double act_fn(double g, int32_t kind)
 {
     if (kind == ORACLE_ACT_SILU)
         return g / (1.0 + exp(-g));
-    const double c = sqrt(2.0 / 3.14159265358979323846);
-    return 0.5 * g * (1.0 + tanh(c * (g + 0.044715 * g * g * g)));
+    const double y = sqrt(2.0 / 3.14159265358979323846) * (g + 0.044715 * g * g * g);
+    return g / (1.0 + exp(-2.0 * y));
 }
 
 /* a[r][i] = act(h[r][i]) * h[r][n_inter + i], computed in fp64 and rounded

@@ -26,7 +26,8 @@
  *                                                  of the experts sum to
  *                                                  oracle_moe_q4_0_q8_1 bit for bit;
  *                                                  hand-checked masking
- *   oracle_act_mul / _quantize_q8_1                pinned: scipy expit and the exact
+ *   oracle_act_mul / _quantize_q8_1                pinned: 50-digit mpmath values, torch
+ *                                                  activations, the exact
  *                                                  GELU x*Phi(x) within the tanh
  *                                                  form's error, f(x) - f(-x) = x,
  *                                                  gate/up order, hand values; the

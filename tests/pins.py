@@ -414,7 +414,30 @@ def pin_act_library(o):
         a = o.act_mul(h, kind).astype(np.float64)
         tol = _ulp32(ref) + 1e-15 * np.abs(g.numpy() * u) + 1e-45
         assert np.all(np.abs(a - ref) <= tol), kind
-        assert np.mean(a == ref.astype(np.float32)) > 0.98
+        if kind == o.ACT_SILU:                  # no cancellation in either evaluation
+            assert np.mean(a == ref.astype(np.float32)) > 0.98
+
+
+def pin_act_tail_accuracy(o):
+    """Both activations against 50-digit evaluations of their definitions
+    (mpmath), tanh form as written for GELU: every fp32 result within one ulp,
+    including the negative tails where the exact values are tiny (GELU below
+    g = -6, where 1 + tanh(y) cancels in fp64; SiLU down to g = -80)."""
+    import mpmath
+    mpmath.mp.dps = 50
+    g = np.concatenate([np.linspace(-12, 12, 481), np.linspace(-80, -12, 69)]).astype(np.float32)
+    h = np.concatenate([g, np.full_like(g, 1.5)])[None, :]
+    c = mpmath.sqrt(mpmath.mpf(2) / mpmath.pi)
+    for kind in (o.ACT_SILU, o.ACT_GELU_TANH):
+        a = o.act_mul(h, kind)[0]
+        for gi, ai in zip(g.tolist(), a.tolist()):
+            x = mpmath.mpf(gi)
+            if kind == o.ACT_SILU:
+                ex = x / (1 + mpmath.exp(-x))
+            else:
+                ex = x / 2 * (1 + mpmath.tanh(c * (x + mpmath.mpf("0.044715") * x ** 3)))
+            ex = float(ex * mpmath.mpf(1.5))
+            assert abs(ai - ex) <= float(np.spacing(np.float32(abs(ex)))) + 1e-45, (kind, gi, ai, ex)
 
 
 def pin_act_gelu_vs_erf(o):
@@ -482,6 +505,6 @@ ALL_PINS = [
     pin_q8_1_hand, pin_q8_1_numpy, pin_q8_1_error_bound, pin_route, pin_block_dot_hand,
     pin_moe_closed_form_vs_bruteforce, pin_moe_numpy_einsum, pin_moe_block_dots,
     pin_moe_split_invariance, pin_moe_bad_ids, pin_moe_slots_numpy_einsum, pin_moe_slots_replicated_rows,
-    pin_moe_ep_shards_sum_to_full, pin_act_library, pin_act_gelu_vs_erf, pin_act_odd_identity, pin_act_hand,
+    pin_moe_ep_shards_sum_to_full, pin_act_library, pin_act_tail_accuracy, pin_act_gelu_vs_erf, pin_act_odd_identity, pin_act_hand,
     pin_act_quantize_numpy,
 ]

@@ -52,7 +52,8 @@ MUTANTS = {
     "fp16_truncates": ("double q = nearbyint(m * 2048.0);", "double q = floor(m * 2048.0);"),
     "silu_sign": ("return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
     "gelu_drops_cubic": ("(g + 0.044715 * g * g * g)", "(g)"),
-    "gelu_drops_half": ("return 0.5 * g * (1.0 + tanh(", "return g * (1.0 + tanh("),
+    "gelu_drops_factor_2": ("return g / (1.0 + exp(-2.0 * y));", "return g / (1.0 + exp(-y));"),
+    "gelu_tanh_form": ("return g / (1.0 + exp(-2.0 * y));", "return 0.5 * g * (1.0 + tanh(y));"),
     "gate_up_swapped": ("(act_fn((double)hr[i], kind) * (double)hr[n_inter + i])",
                         "(act_fn((double)hr[n_inter + i], kind) * (double)hr[i])"),
     "act_kind_swapped": ("if (kind == ORACLE_ACT_SILU)", "if (kind != ORACLE_ACT_SILU)"),

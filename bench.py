@@ -77,6 +77,9 @@ def parse():
                     help="one activation row per routed slot (ft_moe_q4_0_q8_1_slots, the second expert layer)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of a CUDA-graph replay of the step")
+    ap.add_argument("--ffn", choices=["silu", "gelu_tanh"], default=None,
+                    help="time both expert layers (ft_moe_ffn_q4_0_q8_1) with the workload's ncols as the hidden "
+                         "size and its nrows as the intermediate size")
     return ap.parse_args()
 
 
@@ -453,10 +456,120 @@ def ours(args):
     return 0
 
 
+# ------------------------------------------------------------ both layers
+def ffn(args):
+    """quantize + layer 1 (gate and up rows) + activation/requantize + layer 2
+    per step, CUDA-graph replayed; per-stage kernel times from an eager pass of
+    the same calls; roofline of the activation/requantize kernel (HBM)."""
+    import torch
+    rank, world, _ = dist_env()
+    if world > 1:
+        raise SystemExit("--ffn runs on one GPU")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import bit_quantized_moe_quantize_gb300 as ft
+    from bit_quantized_moe_quantize_gb300 import build, synth
+    build.build()
+    ft.load()
+    name, wl, T = workload(args.workload)
+    E, k, H, I = wl.n_experts, wl.top_k, wl.ncols, wl.nrows
+    S = T * k
+    kind = {"silu": ft.ACT_SILU, "gelu_tanh": ft.ACT_GELU_TANH}[args.ffn]
+    w13 = synth.make_weights(synth.custom_workload(E, k, H, 2 * I, wl.seed))
+    w2 = synth.make_weights(synth.custom_workload(E, k, I, H, wl.seed + 1000))
+    x = synth.make_activations(wl, T)
+    ids = synth.make_topk_ids(wl, T)
+    d13, d2 = torch.from_numpy(w13).to(dev), torch.from_numpy(w2).to(dev)
+    dx, di = torch.from_numpy(x).to(dev), torch.from_numpy(ids).to(dev)
+    act = torch.empty((T, H // 32, 36), dtype=torch.uint8, device=dev)
+    h = torch.empty((T, k, 2 * I), dtype=torch.float32, device=dev)
+    mid = torch.empty((S, I // 32, 36), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, k, H), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ft.reserve(T, k, E, max(2 * I, H), max(H, I))
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ft.quantize_q8_1(dx, out=act)
+        ft.moe_ffn_q4_0_q8_1(d13, d2, act, di, kind, out=out, h=h, act_mid=mid)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    run, launch_mode = step, "eager"
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                step()
+        stream.wait_stream(side)
+        run, launch_mode = graph.replay, "cuda graph"
+        for _ in range(3):
+            flush.zero_()
+            run()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    clocks.mark("begin")
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        run()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("end")
+    clk = clocks.stop()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    # per stage, eager, events on the launching stream (torch's current stream)
+    stages = {"quantize": lambda: ft.quantize_q8_1(dx, out=act),
+              "layer1": lambda: ft.moe_q4_0_q8_1(d13, act, di, out=h),
+              "act_requant": lambda: ft.act_mul_quantize_q8_1(h, kind, out=mid),
+              "layer2": lambda: ft.moe_q4_0_q8_1_slots(d2, mid, di, out=out)}
+    n_prof = max(3, min(args.steps, 30))
+    st_ms = {}
+    for key, fn in stages.items():
+        tl = []
+        for _ in range(n_prof):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            tl.append((a, b))
+        torch.cuda.synchronize()
+        st_ms[key] = statistics.mean(a.elapsed_time(b) for a, b in tl)
+    if ft.read_device_error():
+        raise RuntimeError("device error flag raised")
+    peaks, peak_src = load_peaks()
+    act_bytes = S * 2 * I * 4 + S * (I // 32) * 36
+    achieved = act_bytes / (st_ms["act_requant"] / 1000.0) / 1e9
+    flops = 2.0 * S * (2 * I) * H + 2.0 * S * H * I
+    line = {"metric": "routed tokens/s through both expert layers", "value": T / (ms / 1000.0), "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "dtype": "q4_0 x q8_1 exact int block dots, f32 scaling and activation", "data": "synthetic",
+            "config": {"workload": f"{name} E={E} k={k} hidden={H} inter={I} T={T} act={args.ffn}",
+                       "launch": launch_mode, "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)"},
+            "effective_tops": flops / (ms / 1000.0) / 1e12,
+            "stages_ms": st_ms,
+            "roofline": {"kernel": "act_mul_quantize_q8_1_kernel", "bound": "hbm", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "algorithmic": f"S*2I*4 + S*I/32*36 = {act_bytes} B per launch",
+                         "peak_note": f"copy bandwidth, of {peak_src}", "traffic": None},
+            "clocks": clk}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return reference_arm(args)
+    if args.ffn:
+        return ffn(args)
     return ours(args)
 
 

@@ -6,14 +6,18 @@ synthetic-input generator used by the tests and the benchmark.
 
     act = quantize_q8_1(x_fp16)                       # fp16 [T, K] -> Q8_1
     out = moe_q4_0_q8_1(weights_q4_0, act, topk_ids)  # fp32 [T, k, N]
+    a2 = act_mul_quantize_q8_1(out, ACT_SILU)         # Q8_1 of silu(gate) * up per slot
+    y, h, a2 = moe_ffn_q4_0_q8_1(w13, w2, act, topk_ids, ACT_SILU)   # both expert layers
 """
 
-from ._lib import (FT_DEVERR_BAD_EXPERT_ID, FT_DEVERR_WAIT_TIMEOUT, FT_PATH_AUTO, FT_PATH_GEMM, FT_PATH_GEMV,
-                   FtError, block_dots, last_error, load, moe_q4_0_q8_1, moe_q4_0_q8_1_ep, moe_q4_0_q8_1_slots, profile_enable, profile_read, quantize_q8_1,
-                   read_device_error, release, reserve, route_offsets, selected_path, set_path, workspace_bytes)
+from ._lib import (ACT_GELU_TANH, ACT_SILU, FT_DEVERR_BAD_EXPERT_ID, FT_DEVERR_WAIT_TIMEOUT, FT_PATH_AUTO,
+                   FT_PATH_GEMM, FT_PATH_GEMV, FtError, act_mul_quantize_q8_1, block_dots, last_error, load,
+                   moe_ffn_q4_0_q8_1, moe_q4_0_q8_1, moe_q4_0_q8_1_ep, moe_q4_0_q8_1_slots, profile_enable,
+                   profile_read, quantize_q8_1, read_device_error, release, reserve, route_offsets, selected_path,
+                   set_path, workspace_bytes)
 
 __all__ = [
-    "FT_DEVERR_BAD_EXPERT_ID", "FT_DEVERR_WAIT_TIMEOUT", "FT_PATH_AUTO", "FT_PATH_GEMM", "FT_PATH_GEMV", "FtError",
+    "ACT_GELU_TANH", "ACT_SILU", "act_mul_quantize_q8_1", "moe_ffn_q4_0_q8_1", "FT_DEVERR_BAD_EXPERT_ID", "FT_DEVERR_WAIT_TIMEOUT", "FT_PATH_AUTO", "FT_PATH_GEMM", "FT_PATH_GEMV", "FtError",
     "block_dots", "last_error", "load", "moe_q4_0_q8_1", "moe_q4_0_q8_1_ep", "moe_q4_0_q8_1_slots", "profile_enable", "profile_read", "quantize_q8_1", "read_device_error", "release", "reserve",
     "route_offsets", "selected_path", "set_path", "workspace_bytes",
 ]

@@ -28,7 +28,7 @@ EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_m
            "ft_moe_reserve", "ft_moe_release", "ft_moe_read_device_error", "ft_moe_set_path",
            "ft_moe_selected_path", "ft_moe_block_dots", "ft_last_error", "ft_abi_version", "ft_profile_enable",
            "ft_profile_read", "ft_moe_route_offsets_noalloc", "ft_moe_q4_0_q8_1_slots",
-           "ft_moe_q4_0_q8_1_ep")
+           "ft_moe_q4_0_q8_1_ep", "ft_act_mul_quantize_q8_1", "ft_moe_ffn_q4_0_q8_1")
 
 
 class FtError(RuntimeError):
@@ -62,6 +62,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.ft_moe_q4_0_q8_1_slots.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_moe_q4_0_q8_1_ep.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp]
         L.ft_moe_block_dots.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
+        L.ft_act_mul_quantize_q8_1.argtypes = [vp, vp, i64, i64, i32, vp]
+        L.ft_moe_ffn_q4_0_q8_1.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i64, i64, i32, vp]
         L.ft_moe_workspace_bytes.argtypes = [i64, i32, i32, i64, i64]
         L.ft_moe_workspace_bytes.restype = ctypes.c_size_t
         L.ft_moe_reserve.argtypes = [i64, i32, i32, i64, i64]
@@ -206,6 +208,50 @@ def moe_q4_0_q8_1_ep(weights_local, act, topk_ids, n_experts_global, expert_star
                                       ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, int(n_experts_global),
                                       int(expert_start), E_local, N, K, _stream(weights_local)))
     return out
+
+
+ACT_SILU = 0
+ACT_GELU_TANH = 1
+
+
+def act_mul_quantize_q8_1(h, act_kind, out=None):
+    """fp32 [..., 2I] (gate | up) -> Q8_1 uint8 [rows, I/32, 36] of act(gate) * up,
+    rows = h.numel() / 2I (ft_act_mul_quantize_q8_1)."""
+    torch = _torch()
+    ph = _dev(h, torch.float32, "h")
+    two_i = h.shape[-1]
+    if two_i % 64:
+        raise ValueError(f"the last dim of h must be 2 * n_inter with n_inter % 32 == 0 (got {two_i})")
+    rows = h.numel() // two_i
+    if out is None:
+        out = torch.empty((rows, two_i // 64, 36), dtype=torch.uint8, device=h.device)
+    po = _dev(out, torch.uint8, "out")
+    if out.numel() != rows * (two_i // 64) * 36:
+        raise ValueError(f"out must hold {rows} x {two_i // 64} Q8_1 blocks")
+    _check(load().ft_act_mul_quantize_q8_1(ph, po, rows, two_i // 2, int(act_kind), _stream(h)))
+    return out
+
+
+def moe_ffn_q4_0_q8_1(w13, w2, act, topk_ids, act_kind, out=None, h=None, act_mid=None):
+    """Both expert layers per slot (ft_moe_ffn_q4_0_q8_1): w13 Q4_0 [E, 2I, H/32, 18]
+    (gate rows, then up rows), w2 Q4_0 [E, H, I/32, 18], act Q8_1 [T, H/32, 36]
+    -> out fp32 [T, k, H]; returns (out, h [T, k, 2I] fp32, act_mid [T*k, I/32, 36])."""
+    torch = _torch()
+    E, two_i, H, T, k = _matmul_shape(w13, act, topk_ids)
+    _dev(w2, torch.uint8, "w2", 4)
+    if w2.shape[0] != E or w2.shape[1] != H or w2.shape[3] != 18 or 2 * w2.shape[2] * 32 != two_i:
+        raise ValueError(f"shape mismatch: w13 {tuple(w13.shape)} w2 {tuple(w2.shape)}")
+    I = two_i // 2
+    dev = w13.device
+    out = torch.empty((T, k, H), dtype=torch.float32, device=dev) if out is None else out
+    h = torch.empty((T, k, two_i), dtype=torch.float32, device=dev) if h is None else h
+    act_mid = torch.empty((T * k, I // 32, 36), dtype=torch.uint8, device=dev) if act_mid is None else act_mid
+    _check(load().ft_moe_ffn_q4_0_q8_1(ctypes.c_void_p(w13.data_ptr()), ctypes.c_void_p(w2.data_ptr()),
+                                       ctypes.c_void_p(act.data_ptr()), ctypes.c_void_p(topk_ids.data_ptr()),
+                                       _dev(h, torch.float32, "h"), _dev(act_mid, torch.uint8, "act_mid"),
+                                       _dev(out, torch.float32, "out"), T, k, E, H, I, int(act_kind),
+                                       _stream(w13)))
+    return out, h, act_mid
 
 
 def block_dots(weights, act, topk_ids, out=None):

@@ -501,6 +501,46 @@ int ft_moe_q4_0_q8_1_slots(const void* weights, const void* act_slots, const int
                         true);
 }
 
+int ft_act_mul_quantize_q8_1(const float* h, void* act_q8_1, int64_t rows, int64_t n_inter, int32_t act_kind,
+                             void* stream) {
+    g_last_error.clear();
+    if (rows < 0) return fail(FT_ERR_ARG, "rows must be >= 0 (got %lld)", (long long)rows);
+    if (n_inter <= 0 || n_inter % 32 != 0)
+        return fail(FT_ERR_ARG, "n_inter must be a positive multiple of 32 (got %lld)", (long long)n_inter);
+    if (act_kind != FT_ACT_SILU && act_kind != FT_ACT_GELU_TANH)
+        return fail(FT_ERR_ARG, "act_kind must be FT_ACT_SILU or FT_ACT_GELU_TANH (got %d)", act_kind);
+    int64_t n;
+    if (!mul_ok(rows, 2 * n_inter, &n) || n > INT64_MAX / 8) return fail(FT_ERR_SIZE, "rows * n_inter overflows");
+    if (rows == 0) return FT_OK;
+    if (!h || !act_q8_1) return fail(FT_ERR_ARG, "null pointer");
+    if (!aligned(h, 16) || !aligned(act_q8_1, 4))
+        return fail(FT_ERR_ALIGN, "h must be 16-byte and act_q8_1 4-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    prof_mark(kProfQuantBegin, s);
+    const int st = launch_act_mul_quantize_q8_1(h, act_q8_1, rows, n_inter, act_kind, s);
+    prof_mark(kProfQuantEnd, s);
+    return st;
+}
+
+int ft_moe_ffn_q4_0_q8_1(const void* w13, const void* w2, const void* act, const int32_t* topk_ids, float* h,
+                         void* act_mid, float* out, int64_t tokens, int32_t top_k, int32_t n_experts,
+                         int64_t hidden, int64_t n_inter, int32_t act_kind, void* stream) {
+    g_last_error.clear();
+    Shape sh{};
+    if (n_inter <= 0 || n_inter > INT64_MAX / 2) return fail(FT_ERR_ARG, "n_inter must be > 0");
+    if (int st = check_matmul_args(tokens, top_k, n_experts, 2 * n_inter, hidden, &sh)) return st;
+    if (int st = check_matmul_args(tokens, top_k, n_experts, hidden, n_inter, &sh)) return st;
+    if (act_kind != FT_ACT_SILU && act_kind != FT_ACT_GELU_TANH)
+        return fail(FT_ERR_ARG, "act_kind must be FT_ACT_SILU or FT_ACT_GELU_TANH (got %d)", act_kind);
+    if (sh.n_slots == 0) return FT_OK;
+    if (!h || !act_mid || !out) return fail(FT_ERR_ARG, "null pointer");
+    if (!aligned(h, 16) || !aligned(act_mid, 16)) return fail(FT_ERR_ALIGN, "h and act_mid must be 16-byte aligned");
+    if (int st = matmul_entry(w13, act, topk_ids, h, nullptr, tokens, top_k, n_experts, 2 * n_inter, hidden, stream))
+        return st;
+    if (int st = ft_act_mul_quantize_q8_1(h, act_mid, sh.n_slots, n_inter, act_kind, stream)) return st;
+    return matmul_entry(w2, act_mid, topk_ids, out, nullptr, tokens, top_k, n_experts, hidden, n_inter, stream, true);
+}
+
 int ft_moe_block_dots(const void* weights, const void* act, const int32_t* topk_ids, int32_t* dots, int64_t tokens,
                       int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols, void* stream) {
     if (!dots) {

@@ -1,22 +1,87 @@
 // Activation quantizer: fp16 rows -> Q8_1 blocks (quantize_row_q8_1 on
 // FreeToken PR #185, "Fix"; format restated in ft_moe.h).
 //
-// HBM-bound: 2 bytes read and 1.125 bytes written per value.  Eight lanes
-// own one 32-value block (four values each, one 8-byte load per lane); the
-// block's amax and integer sum are reduced with 3 shuffle steps inside the
-// 8-lane group.  The flat block index runs on grid.x with a grid-stride loop,
-// so neither tokens nor tokens * blocks is bound by a 65535 grid dimension
-// (the limit quantize_row_q8_1 tiles around on FreeToken PR #185, "Fix").
+// HBM-bound: 2 bytes read and 1.125 bytes written per value.  Two layouts of
+// the same arithmetic:
+//  - quantize_q8_1_block_kernel, for batches of at least two 256-thread CTAs
+//    per SM (and x 16-byte aligned): one thread owns a whole 32-value block (four 16-byte loads, 64
+//    bytes in flight per thread), so amax and the code sum need no shuffles;
+//  - quantize_q8_1_kernel, for small batches: eight lanes own one block (one
+//    8-byte load each, amax and sum reduced with 3 shuffle steps), which puts
+//    8x more threads on a batch of a few tokens.
+// The flat block index runs on grid.x with a grid-stride loop, so neither
+// tokens nor tokens * blocks is bound by a 65535 grid dimension (the limit
+// quantize_row_q8_1 tiles around on FreeToken PR #185, "Fix").
 //
-// Bit-exactness: amax is exact, d = amax / 127 and x / d are IEEE fp32
-// divisions (__fdiv_rn), q = roundf (half away from zero), s = d * sum(q) is
-// one fp32 multiply, and both are rounded to fp16 with __float2half_rn.
+// Bit-exactness: amax is exact, d = amax / 127 is an IEEE fp32 division
+// (__fdiv_rn), q = roundf(x / d) with the quotient of an IEEE division (see
+// q8_code), s = d * sum(q) is one fp32 multiply, and both are rounded to fp16
+// with __float2half_rn.
 #include <cuda_fp16.h>
 
 #include "ft_common.cuh"
 #include "ft_internal.h"
 
 namespace ft {
+
+// round(v / d) clamped to [-127, 127], exactly as the IEEE quotient rounds:
+// v * rcp(d) lies within 2^-23 |v / d| (<= 1.6e-5 for |v / d| <= 127.5) of
+// v / d, whose fp32 rounding moves it by at most 4e-6 more, so both round to
+// the same integer unless v * rcp(d) is within 4e-5 of a half integer; those
+// take the division.  rcp(d) is finite for d >= 1e-36 (else always divide).
+__device__ __forceinline__ int q8_code(float v, float d, float rd, bool fast) {
+    float y = fast ? __fmul_rn(v, rd) : __fdiv_rn(v, d);
+    const float t = fabsf(y);
+    if (fast && fabsf((t - truncf(t)) - 0.5f) < 4.0e-5f) y = __fdiv_rn(v, d);
+    return min(127, max(-127, static_cast<int>(roundf(y))));
+}
+
+__device__ __forceinline__ uint32_t q8_header(float d, int sum) {
+    const __half hd = __float2half_rn(d);
+    const __half hs = __float2half_rn(__fmul_rn(d, static_cast<float>(sum)));
+    return static_cast<uint32_t>(__half_as_ushort(hd)) | (static_cast<uint32_t>(__half_as_ushort(hs)) << 16);
+}
+
+__global__ void __launch_bounds__(256) quantize_q8_1_block_kernel(const uint4* __restrict__ x,
+                                                                  uint32_t* __restrict__ out, int64_t n_blocks) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; blk < n_blocks; blk += stride) {
+        uint4 raw[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) raw[c] = __ldg(x + blk * 4 + c);
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t w[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+                v[8 * c + 2 * i] = __low2float(h);
+                v[8 * c + 2 * i + 1] = __high2float(h);
+            }
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const float d = __fdiv_rn(amax, 127.0f);
+        const bool fast = d >= 1.0e-36f;
+        const float rd = fast ? __frcp_rn(d) : 0.0f;
+        uint32_t packed[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) packed[i] = 0;
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int qi = amax != 0.0f ? q8_code(v[i], d, rd, fast) : 0;
+            sum += qi;
+            packed[i >> 2] |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * (i & 3));
+        }
+        uint32_t* ob = out + blk * (Q8_1_BYTES / 4);
+        ob[0] = q8_header(d, sum);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ob[1 + i] = packed[i];
+    }
+}
 
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const uint2* __restrict__ x, uint8_t* __restrict__ out,
                                                             int64_t n_blocks) {
@@ -35,32 +100,21 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const uint2* __restr
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(group_mask, amax, o));
         const float d = __fdiv_rn(amax, 127.0f);
-        int q[4];
+        const bool fast = d >= 1.0e-36f;
+        const float rd = fast ? __frcp_rn(d) : 0.0f;
+        uint32_t packed = 0;
         int sum = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            int qi = 0;
-            if (amax != 0.0f) {
-                qi = static_cast<int>(roundf(__fdiv_rn(v[j], d)));
-                qi = min(127, max(-127, qi));
-            }
-            q[j] = qi;
+            const int qi = amax != 0.0f ? q8_code(v[j], d, rd, fast) : 0;
             sum += qi;
+            packed |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * j);
         }
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(group_mask, sum, o);
         uint8_t* ob = out + blk * Q8_1_BYTES;
-        const uint32_t packed = (static_cast<uint32_t>(q[0]) & 0xFFu) | ((static_cast<uint32_t>(q[1]) & 0xFFu) << 8) |
-                                ((static_cast<uint32_t>(q[2]) & 0xFFu) << 16) |
-                                ((static_cast<uint32_t>(q[3]) & 0xFFu) << 24);
         *reinterpret_cast<uint32_t*>(ob + 4 + 4 * sub) = packed;
-        if (sub == 0) {
-            const __half hd = __float2half_rn(d);
-            const __half hs = __float2half_rn(__fmul_rn(d, static_cast<float>(sum)));
-            const uint32_t ds = static_cast<uint32_t>(__half_as_ushort(hd)) |
-                                (static_cast<uint32_t>(__half_as_ushort(hs)) << 16);
-            *reinterpret_cast<uint32_t*>(ob) = ds;
-        }
+        if (sub == 0) *reinterpret_cast<uint32_t*>(ob) = q8_header(d, sum);
     }
 }
 
@@ -68,14 +122,123 @@ int launch_quantize_q8_1(const void* x, void* act, int64_t tokens, int64_t ncols
     const int64_t n_blocks = tokens * (ncols / QK);
     if (n_blocks == 0) return FT_OK;
     const int threads = 256;
-    // one thread per 8-byte load: every load of the batch is issued at once
-    // (grid.x up to 2^31 - 1; larger batches take the grid-stride loop)
-    const int64_t want = (n_blocks * 8 + threads - 1) / threads;
     const int64_t cap = 0x7FFFFFFF;
+    const bool x16 = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;   // 16-byte loads need it
+    if (x16 && n_blocks >= 2 * static_cast<int64_t>(threads) * sm_count()) {
+        // one thread per block, every block of the batch in flight at once
+        // (grid.x up to 2^31 - 1; larger batches take the grid-stride loop)
+        const int64_t want = (n_blocks + threads - 1) / threads;
+        const dim3 grid(static_cast<unsigned>(want < cap ? want : cap));
+        quantize_q8_1_block_kernel<<<grid, threads, 0, s>>>(static_cast<const uint4*>(x),
+                                                             static_cast<uint32_t*>(act), n_blocks);
+        return check_launch("quantize_q8_1_block_kernel", grid, dim3(threads), 0);
+    }
+    const int64_t want = (n_blocks * 8 + threads - 1) / threads;
     const dim3 grid(static_cast<unsigned>(want < cap ? want : cap));
     quantize_q8_1_kernel<<<grid, threads, 0, s>>>(static_cast<const uint2*>(x), static_cast<uint8_t*>(act),
                                                   n_blocks);
     return check_launch("quantize_q8_1_kernel", grid, dim3(threads), 0);
+}
+
+// ---------------------------------------------------------------------------
+// Gated activation + Q8_1 requantization: the step between the two expert
+// layers (gelu_tanh_and_mul right after the routed matmul on FreeToken PR
+// #185, "Problem"; SiLU*up between layer 1 and layer 2 on
+// nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 6).  h [rows][2 I] fp32, gate half
+// then up half -> [rows][I/32] Q8_1 of a = act(gate) * up.  a lives only in
+// registers: no fp32 or fp16 copy of it is written and read back by a
+// separate quantizer.
+//
+// Both activations are g * sigmoid(z) in fp32: z = g for SiLU, and
+// z = 2 sqrt(2/pi) (g + 0.044715 g^3) for the tanh form of GELU, since
+// (1 + tanh(y)) / 2 = 1 / (1 + exp(-2 y)); the sigmoid form has no
+// cancellation where tanh(y) approaches -1.  expf is CUDA's accurate
+// exponential; the result is within a few fp32 ulps of the exact activation,
+// so the Q8_1 codes equal those of the exactly computed a except where
+// a / d falls within that distance of a rounding boundary.
+//
+// HBM-bound: 8 bytes read and 1.125 bytes written per output value.  Eight
+// lanes own one block (four gate and four up values each, one 16-byte load
+// per half); each thread loads its kActUnroll units before it uses any, so
+// 32 * kActUnroll bytes per thread are in flight.
+
+constexpr int kActUnroll = 1;
+
+__device__ __forceinline__ float act_mul(float g, float up, int kind) {
+    const float z = kind == FT_ACT_SILU ? g : 1.5957691216057308f * fmaf(0.044715f * g, g * g, g);
+    return g * __frcp_rn(1.0f + expf(-z)) * up;
+}
+
+__global__ void __launch_bounds__(256) act_mul_quantize_q8_1_kernel(const float4* __restrict__ h,
+                                                                    uint8_t* __restrict__ out, int64_t n_blocks,
+                                                                    uint32_t nb_row, int kind) {
+    const int64_t total = n_blocks * 8;
+    const uint32_t lane = lane_id();
+    const uint32_t group_mask = 0xFFu << (lane & 24u);
+    const uint32_t sub = lane & 7u;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * (256 * kActUnroll) + threadIdx.x;
+    // block (row r, column block b) of the first unit; unit u is 32 u blocks on
+    int64_t r = (i0 >> 3) / nb_row;
+    uint32_t b = static_cast<uint32_t>((i0 >> 3) - r * nb_row);
+    float4 g[kActUnroll], up[kActUnroll];
+#pragma unroll
+    for (int u = 0; u < kActUnroll; ++u) {
+        if (i0 + u * 256 < total) {
+            // float4 index of the gate quad: row r holds 16 nb_row float4s
+            const int64_t gi = r * (16 * static_cast<int64_t>(nb_row)) + 8 * static_cast<int64_t>(b) + sub;
+            g[u] = __ldg(h + gi);
+            up[u] = __ldg(h + gi + 8 * static_cast<int64_t>(nb_row));
+        } else {
+            g[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            up[u] = g[u];
+        }
+        b += 32;
+        while (b >= nb_row) {
+            b -= nb_row;
+            ++r;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kActUnroll; ++u) {
+        const int64_t i = i0 + u * 256;
+        const float v[4] = {act_mul(g[u].x, up[u].x, kind), act_mul(g[u].y, up[u].y, kind),
+                            act_mul(g[u].z, up[u].z, kind), act_mul(g[u].w, up[u].w, kind)};
+        float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(group_mask, amax, o));
+        const float d = __fdiv_rn(amax, 127.0f);
+        const bool fast = d >= 1.0e-36f;
+        const float rd = fast ? __frcp_rn(d) : 0.0f;
+        uint32_t packed = 0;
+        int sum = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int qi = amax != 0.0f ? q8_code(v[j], d, rd, fast) : 0;
+            sum += qi;
+            packed |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * j);
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(group_mask, sum, o);
+        if (i < total) {
+            uint8_t* ob = out + (i >> 3) * Q8_1_BYTES;
+            *reinterpret_cast<uint32_t*>(ob + 4 + 4 * sub) = packed;
+            if (sub == 0) *reinterpret_cast<uint32_t*>(ob) = q8_header(d, sum);
+        }
+    }
+}
+
+int launch_act_mul_quantize_q8_1(const float* h, void* act, int64_t rows, int64_t n_inter, int kind,
+                                 cudaStream_t s) {
+    const int64_t nb_row = n_inter / QK;
+    const int64_t n_blocks = rows * nb_row;
+    if (n_blocks == 0) return FT_OK;
+    const int64_t per_cta = 256 * kActUnroll;
+    const int64_t want = (n_blocks * 8 + per_cta - 1) / per_cta;
+    if (want > 0x7FFFFFFF) return fail(FT_ERR_SIZE, "rows * n_inter too large for one launch");
+    const dim3 grid(static_cast<unsigned>(want));
+    act_mul_quantize_q8_1_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(h), static_cast<uint8_t*>(act),
+                                                      n_blocks, static_cast<uint32_t>(nb_row), kind);
+    return check_launch("act_mul_quantize_q8_1_kernel", grid, dim3(256), 0);
 }
 
 }  // namespace ft

@@ -86,6 +86,10 @@ typedef enum {
 #define FT_PATH_GEMV 1   /* per-slot GEMV on CUDA cores                                  */
 #define FT_PATH_GEMM 2   /* expert-grouped GEMM on the tcgen05 tensor cores              */
 
+/* Gated activations of ft_act_mul_quantize_q8_1 / ft_moe_ffn_q4_0_q8_1. */
+#define FT_ACT_SILU 0        /* silu(g) = g / (1 + exp(-g))                              */
+#define FT_ACT_GELU_TANH 1   /* g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3)))            */
+
 /* Documented limits. */
 #define FT_MAX_EXPERTS 4096
 #define FT_MAX_NCOLS   65536
@@ -216,6 +220,56 @@ FT_API int ft_moe_q4_0_q8_1_ep(const void* weights_local, const void* act, const
                                float* out, int64_t tokens, int32_t top_k, int32_t n_experts_global,
                                int32_t expert_start, int32_t n_experts_local, int64_t nrows,
                                int64_t ncols, void* stream);
+
+/*
+ * ft_act_mul_quantize_q8_1 - the step between the two expert layers, fused:
+ * the gated activation of the gate half of each row times its up half,
+ * requantized to Q8_1 (gelu_tanh_and_mul right after the routed matmul on
+ * FreeToken PR #185, "Problem"; SiLU*up between layer 1 and layer 2 on
+ * nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 6).  Per row r and column i < I:
+ *   a[r][i] = act(h[r][i]) * h[r][I + i]      (fp32, never stored)
+ * then each 32-block of a row is quantized as ft_quantize_q8_1 does.
+ * The activation is computed in fp32 to within a few ulps of the exact value
+ * (the CPU oracle takes it in fp64 and rounds once), so a Q8_1 code may differ
+ * by 1 from the oracle's where a / d lies that close to a rounding boundary.
+ *
+ *   h         device, fp32 [rows][2 * n_inter] (gate | up), 16-byte aligned
+ *   act_q8_1  device, Q8_1 [rows][n_inter / 32], 4-byte aligned
+ *   rows      >= 0 (0 is a no-op); n_inter > 0, n_inter % 32 == 0
+ *   act_kind  FT_ACT_SILU or FT_ACT_GELU_TANH
+ * Errors: FT_ERR_ARG, FT_ERR_SIZE, FT_ERR_ALIGN, FT_ERR_LAUNCH.
+ */
+FT_API int ft_act_mul_quantize_q8_1(const float* h, void* act_q8_1, int64_t rows, int64_t n_inter,
+                                    int32_t act_kind, void* stream);
+
+/*
+ * ft_moe_ffn_q4_0_q8_1 - both expert layers of the routed MoE block, per
+ * slot, in three steps on `stream` (layer 1 -> activation -> layer 2 on
+ * nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 6):
+ *   h       = ft_moe_q4_0_q8_1(w13, act)           gate and up rows in one matmul
+ *   act_mid = ft_act_mul_quantize_q8_1(h)          per slot row
+ *   out     = ft_moe_q4_0_q8_1_slots(w2, act_mid)
+ * The weighted sum over a token's top_k slots is left to the caller.
+ *
+ *   w13       device, Q4_0 [n_experts][2 * n_inter][hidden / 32]: rows
+ *             [0, n_inter) of an expert are its gate rows, [n_inter, 2 n_inter)
+ *             its up rows; 16-byte aligned
+ *   w2        device, Q4_0 [n_experts][hidden][n_inter / 32]; 16-byte aligned
+ *   act       device, Q8_1 [tokens][hidden / 32]; 16-byte aligned
+ *   topk_ids  device, int32 [tokens][top_k]
+ *   h         device, fp32 [tokens][top_k][2 * n_inter] out (scratch the
+ *             caller owns; holds the layer-1 result afterwards); 16-byte aligned
+ *   act_mid   device, Q8_1 [tokens * top_k][n_inter / 32] out (scratch the
+ *             caller owns; holds the layer-2 input afterwards); 16-byte aligned
+ *   out       device, fp32 [tokens][top_k][hidden] out
+ * Needs hidden and n_inter positive multiples of 32 and the limits of
+ * ft_moe_q4_0_q8_1 for both matmuls.  Slots with a bad expert id get zero h,
+ * act_mid and out rows.  Errors: those of the three steps.
+ */
+FT_API int ft_moe_ffn_q4_0_q8_1(const void* w13, const void* w2, const void* act, const int32_t* topk_ids,
+                                float* h, void* act_mid, float* out, int64_t tokens, int32_t top_k,
+                                int32_t n_experts, int64_t hidden, int64_t n_inter, int32_t act_kind,
+                                void* stream);
 
 /*
  * ft_moe_workspace_bytes - bytes of library workspace that one

@@ -139,3 +139,27 @@ def test_product_path_never_imports_the_oracle():
     for fn in os.listdir(os.path.join(pkg, "csrc")):
         src = open(os.path.join(pkg, "csrc", fn)).read()
         assert "ft_oracle" not in src and "oracle_" not in src, fn
+
+
+def test_activation_and_ffn_reject_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    f = lib.ft_act_mul_quantize_q8_1
+    H, A = vp(0x10000), vp(0x20000)
+    assert f(H, A, -1, 64, 0, vp(0)) == 1                     # rows < 0
+    assert f(H, A, 4, 48, 0, vp(0)) == 1                      # n_inter % 32
+    assert f(H, A, 4, 64, 2, vp(0)) == 1                      # unknown activation
+    assert "act_kind" in _err(lib)
+    assert f(H, A, 0, 64, 1, vp(0)) == 0                      # no rows: no-op
+    assert f(vp(0), A, 4, 64, 0, vp(0)) == 1                  # null h
+    assert f(vp(0x10008), A, 4, 64, 0, vp(0)) == 3            # h not 16-byte aligned
+    assert f(H, vp(0x20002), 4, 64, 0, vp(0)) == 3            # act not 4-byte aligned
+    assert f(H, A, 1 << 60, 64, 0, vp(0)) == 2                # size overflow
+    g = lib.ft_moe_ffn_q4_0_q8_1
+    W1, W2, X, I, Hh, M, O = (vp(0x10000 * i) for i in range(1, 8))
+    assert g(W1, W2, X, I, Hh, M, O, 4, 2, 8, 256, 100, 0, vp(0)) == 1  # n_inter % 32
+    assert g(W1, W2, X, I, Hh, M, O, 4, 2, 8, 250, 128, 0, vp(0)) == 1  # hidden % 32
+    assert g(W1, W2, X, I, Hh, M, O, 4, 2, 8, 256, 128, 5, vp(0)) == 1  # unknown activation
+    assert g(W1, W2, X, I, Hh, M, O, 0, 2, 8, 256, 128, 0, vp(0)) == 0  # no slots: no-op
+    assert g(W1, W2, X, I, vp(0), M, O, 4, 2, 8, 256, 128, 0, vp(0)) == 1    # null h
+    assert g(W1, W2, X, I, vp(0x50008), M, O, 4, 2, 8, 256, 128, 0, vp(0)) == 3   # h misaligned
+    assert g(W1, W2, X, I, Hh, vp(0x60004), O, 4, 2, 8, 256, 128, 0, vp(0)) == 3  # act_mid misaligned

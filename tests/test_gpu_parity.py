@@ -50,6 +50,47 @@ def test_quantize_bit_exact(ft, oracle, T, K, seed):
     assert np.array_equal(got, want)
 
 
+def _near_tie_rows():
+    """Every fp16 value in [-m, m] for several block maxima m, 31 per block plus
+    m itself: x / d lands on or next to half integers over and over."""
+    blocks = []
+    for m in (12.7, 1.0, 127.0, 0.3, 5e-3, 3e4):
+        m16 = np.float16(m)
+        allv = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16)
+        allv = allv[(allv > 0) & (allv <= m16)]
+        allv = np.concatenate([allv, -allv])
+        n = len(allv) // 31 * 31
+        b = allv[:n].reshape(-1, 31)
+        blocks.append(np.concatenate([b, np.full((len(b), 1), m16, dtype=np.float16)], axis=1))
+    v = np.concatenate(blocks)
+    v = v[: len(v) // 8 * 8]
+    return v.reshape(-1, 256)
+
+
+@pytest.mark.parametrize("copies", [1, 12], ids=["lane_groups", "block_per_thread"])
+def test_quantize_near_ties_bit_exact(ft, oracle, copies):
+    """The reciprocal-multiply quotient must round like the IEEE division on
+    every near tie; one copy (6992 blocks) runs the small-batch kernel, twelve
+    copies (past two 256-thread CTAs per SM of blocks) the one-thread-per-block
+    kernel."""
+    x = np.concatenate([_near_tie_rows()] * copies)
+    got = G.host(ft.quantize_q8_1(G.dev(x)))
+    assert np.array_equal(got, oracle.quantize_q8_1(x))
+
+
+def test_quantize_unaligned_input(ft, oracle):
+    """x only 8-byte aligned on a batch big enough for the one-thread-per-block
+    kernel: its 16-byte loads are not used, same bytes."""
+    import torch
+    x = np.random.default_rng(7).standard_normal((4096, 1024)).astype(np.float16)
+    buf = torch.empty(x.size + 4, dtype=torch.float16, device="cuda")
+    dx = buf[4:].view(4096, 1024)
+    dx.copy_(torch.from_numpy(x))
+    assert dx.data_ptr() % 16 == 8
+    got = G.host(ft.quantize_q8_1(dx))
+    assert np.array_equal(got, oracle.quantize_q8_1(x))
+
+
 @pytest.mark.parametrize("name,T", [("mixtral_8x7b", 32768), ("prefill", 8191)])
 def test_quantize_bit_exact_full_size(ft, oracle, name, T):
     x = G.case(name, T)["x"] if name != "mixtral_8x7b" else _mixtral_x(T)

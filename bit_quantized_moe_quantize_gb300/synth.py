@@ -69,7 +69,12 @@ WORKLOADS = {
 }
 
 # stream ids inside one workload seed
-_S_WEIGHTS, _S_ACT, _S_ROUTE, _S_OUTLIER, _S_RANK = 0, 1, 2, 3, 4
+_S_WEIGHTS, _S_ACT, _S_ROUTE, _S_OUTLIER, _S_RANK, _S_GGUF = 0, 1, 2, 3, 4, 5
+
+# the other GGUF weight types with 32-weight blocks: bytes per block, offset of
+# the code bytes, whether the block stores an fp16 m after d, GGML type number
+GGUF_TYPES = {"q4_0": (18, 2, False, 2), "q4_1": (20, 4, True, 3), "q5_0": (22, 2, False, 6),
+              "q5_1": (24, 4, True, 7), "q8_0": (34, 2, False, 8)}
 
 
 def _rng(seed: int, stream: int, *extra: int) -> np.random.Generator:
@@ -112,6 +117,37 @@ def make_weights(wl: Workload, chunk_rows: int = 1 << 16) -> np.ndarray:
         w = rng.standard_normal((r1 - r0, K), dtype=np.float32) * np.float32(wl.w_std)
         flat[r0:r1] = encode_q4_0(w)
     return out
+
+
+def make_weights_gguf(wl: Workload, wtype: str, chunk_rows: int = 1 << 16) -> np.ndarray:
+    """Expert weights as random valid blocks of a GGUF type, uint8 [E, N, K/32, bytes].
+
+    Q4_0 goes through make_weights.  For the others every code byte (nibbles,
+    5th-bit words, int8 codes) is uniform random, d = fp16(0.0005 + 0.002 |z|)
+    and, for the types with an offset, m = fp16(-d * L / 2 * (1 + 0.1 z'))
+    with L the number of levels, so that the weights centre near zero like
+    trained ones.  Random bytes are valid blocks of these formats; no weight
+    quantization is involved.
+    """
+    if wtype == "q4_0":
+        return make_weights(wl, chunk_rows)
+    bb, code0, has_m, tid = GGUF_TYPES[wtype]
+    E, N, K = wl.n_experts, wl.nrows, wl.ncols
+    nb = K // QK
+    out = np.empty((E * N, nb, bb), dtype=np.uint8)
+    rng = _rng(wl.seed, _S_GGUF, tid)
+    levels = {"q4_1": 16, "q5_1": 32}.get(wtype, 0)
+    for r0 in range(0, E * N, chunk_rows):
+        r1 = min(E * N, r0 + chunk_rows)
+        n = r1 - r0
+        d = (np.float32(0.0005) + np.float32(0.002) * np.abs(rng.standard_normal((n, nb), dtype=np.float32)))
+        out[r0:r1, :, 0:2] = d.astype(np.float16).view(np.uint8).reshape(n, nb, 2)
+        if has_m:
+            z = rng.standard_normal((n, nb), dtype=np.float32)
+            m = -d * np.float32(levels / 2) * (np.float32(1) + np.float32(0.1) * z)
+            out[r0:r1, :, 2:4] = m.astype(np.float16).view(np.uint8).reshape(n, nb, 2)
+        out[r0:r1, :, code0:] = rng.integers(0, 256, size=(n, nb, bb - code0), dtype=np.uint8)
+    return out.reshape(E, N, nb, bb)
 
 
 def make_activations(wl: Workload, tokens: int) -> np.ndarray:

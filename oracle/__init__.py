@@ -78,6 +78,12 @@ class Oracle:
         L.oracle_moe_block_dots.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.oracle_moe_dequant_bruteforce.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.oracle_act_mul.argtypes = [vp, i64, i64, i32, vp]
+        L.oracle_gguf_block_bytes.argtypes = [i32]
+        L.oracle_gguf_block_bytes.restype = i32
+        L.oracle_dequantize_gguf.argtypes = [i32, vp, i64, vp]
+        L.oracle_gguf_block_dot.argtypes = [i32, vp, vp]
+        L.oracle_gguf_block_dot.restype = i32
+        L.oracle_moe_gguf_q8_1.argtypes = [i32, vp, vp, vp, vp, i64, i32, i32, i64, i64]
         L.oracle_act_mul_quantize_q8_1.argtypes = [vp, i64, i64, i32, vp]
         self.lib = L
         self.path = so_path
@@ -119,6 +125,43 @@ class Oracle:
         out = np.empty(nb * QK, dtype=np.float64)
         self.lib.oracle_dequantize_q8_1(_p(blocks), nb, _p(out))
         return out.reshape(*blocks.shape[:-2], blocks.shape[-2] * QK)
+
+    # other GGUF weight types -----------------------------------------
+    GGUF = {"q4_0": 2, "q4_1": 3, "q5_0": 6, "q5_1": 7, "q8_0": 8}
+
+    def gguf_block_bytes(self, wtype) -> int:
+        return int(self.lib.oracle_gguf_block_bytes(self.GGUF.get(wtype, wtype)))
+
+    def dequantize_gguf(self, wtype, blocks: np.ndarray) -> np.ndarray:
+        t = self.GGUF.get(wtype, wtype)
+        bb = self.gguf_block_bytes(t)
+        blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+        assert blocks.shape[-1] == bb
+        nb = blocks.size // bb
+        out = np.empty(nb * QK, dtype=np.float64)
+        self.lib.oracle_dequantize_gguf(t, _p(blocks), nb, _p(out))
+        return out.reshape(*blocks.shape[:-2], blocks.shape[-2] * QK)
+
+    def gguf_block_dot(self, wtype, w_block: np.ndarray, a_block: np.ndarray) -> int:
+        t = self.GGUF.get(wtype, wtype)
+        w = np.ascontiguousarray(w_block, dtype=np.uint8)
+        a = np.ascontiguousarray(a_block, dtype=np.uint8)
+        assert w.size == self.gguf_block_bytes(t) and a.size == Q8_1_BYTES
+        return int(self.lib.oracle_gguf_block_dot(t, _p(w), _p(a)))
+
+    def moe_gguf(self, wtype, weights, act, topk_ids) -> np.ndarray:
+        """weights [E, N, K/32, bytes of the type] x Q8_1 act [T, K/32, 36] -> fp32 [T, k, N]."""
+        t = self.GGUF.get(wtype, wtype)
+        w = np.ascontiguousarray(weights, dtype=np.uint8)
+        a = np.ascontiguousarray(act, dtype=np.uint8)
+        ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+        E, N, nb, bb = w.shape
+        assert bb == self.gguf_block_bytes(t)
+        T, k = ids.shape
+        assert a.shape == (T, nb, Q8_1_BYTES)
+        out = np.empty((T, k, N), dtype=np.float32)
+        self.lib.oracle_moe_gguf_q8_1(t, _p(w), _p(a), _p(ids), _p(out), T, k, E, N, nb * QK)
+        return out
 
     # gated activation ------------------------------------------------
     ACT_SILU = 0

@@ -186,6 +186,110 @@ void oracle_dequantize_q8_1(const uint8_t* blocks, int64_t n_blocks, double* out
     }
 }
 
+/* ------------------------------------------ other 32-value GGUF weight types */
+
+/* The other GGUF weight types whose blocks hold 32 weights, as matmul weights
+ * against the same Q8_1 activations (the 19 per-type launchers of
+ * moe_vec.cuh on FreeToken PR #185, "Notes"; the pages exercise only Q4_0 and
+ * do not print the formats, restated in ft_oracle.h).  Each weight is
+ * w_i = q_i * d + c with an integer level q_i and an offset c (0 or m), so a
+ * block's contribution is
+ *     d * d_a * sum_i q_i * q_a[i]  +  c * d_a * sum_i q_a[i],
+ * and the second term takes d_a * sum(q_a) as the activation block's stored
+ * fp16 s (the quantity Q8_1 stores s for). */
+int32_t oracle_gguf_block_bytes(int32_t type)
+{
+    switch (type) {
+        case ORACLE_GGUF_Q4_0: return 18;
+        case ORACLE_GGUF_Q4_1: return 20;
+        case ORACLE_GGUF_Q5_0: return 22;
+        case ORACLE_GGUF_Q5_1: return 24;
+        case ORACLE_GGUF_Q8_0: return 34;
+        default: return 0;
+    }
+}
+
+/* Integer level q_i of weight i of a block. */
+static int gguf_level(const uint8_t* blk, int32_t type, int i)
+{
+    int nib, hi5;
+    uint32_t qh;
+    switch (type) {
+        case ORACLE_GGUF_Q4_0:
+            return q4_0_nibble(blk, i) - 8;
+        case ORACLE_GGUF_Q4_1:
+            return i < 16 ? (blk[4 + i] & 0x0f) : (blk[4 + i - 16] >> 4);
+        case ORACLE_GGUF_Q5_0:
+        case ORACLE_GGUF_Q5_1: {
+            const uint8_t* h = blk + (type == ORACLE_GGUF_Q5_0 ? 2 : 4);
+            const uint8_t* qs = h + 4;
+            qh = (uint32_t)h[0] | ((uint32_t)h[1] << 8) | ((uint32_t)h[2] << 16) | ((uint32_t)h[3] << 24);
+            nib = i < 16 ? (qs[i] & 0x0f) : (qs[i - 16] >> 4);
+            hi5 = (int)((qh >> i) & 1u);
+            return (nib | (hi5 << 4)) - (type == ORACLE_GGUF_Q5_0 ? 16 : 0);
+        }
+        case ORACLE_GGUF_Q8_0:
+            return (int)(int8_t)blk[2 + i];
+        default:
+            abort();
+    }
+}
+
+/* Offset c of a block: the fp16 m of Q4_1 / Q5_1, else 0. */
+static double gguf_offset(const uint8_t* blk, int32_t type)
+{
+    if (type == ORACLE_GGUF_Q4_1 || type == ORACLE_GGUF_Q5_1)
+        return oracle_half_to_double(rd16(blk + 2));
+    return 0.0;
+}
+
+void oracle_dequantize_gguf(int32_t type, const uint8_t* blocks, int64_t n_blocks, double* out)
+{
+    const int32_t bytes = oracle_gguf_block_bytes(type);
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        const uint8_t* blk = blocks + b * bytes;
+        double d = oracle_half_to_double(rd16(blk));
+        double c = gguf_offset(blk, type);
+        for (int i = 0; i < QK; ++i)
+            out[b * QK + i] = (double)gguf_level(blk, type, i) * d + c;
+    }
+}
+
+int32_t oracle_gguf_block_dot(int32_t type, const uint8_t* w_block, const uint8_t* a_block)
+{
+    int32_t acc = 0;
+    for (int i = 0; i < QK; ++i)
+        acc += gguf_level(w_block, type, i) * (int32_t)(int8_t)a_block[4 + i];
+    return acc;
+}
+
+void oracle_moe_gguf_q8_1(int32_t type, const uint8_t* weights, const uint8_t* act, const int32_t* topk_ids,
+                          float* out, int64_t tokens, int32_t top_k, int32_t n_experts,
+                          int64_t nrows, int64_t ncols)
+{
+    const int64_t nb = ncols / QK;
+    const int32_t bytes = oracle_gguf_block_bytes(type);
+    const int64_t n_slots = tokens * top_k;
+    for (int64_t s = 0; s < n_slots; ++s) {
+        const int32_t e = topk_ids[s];
+        const int64_t t = s / top_k;
+        for (int64_t r = 0; r < nrows; ++r) {
+            double y = 0.0;
+            if (e >= 0 && e < n_experts) {
+                for (int64_t b = 0; b < nb; ++b) {
+                    const uint8_t* wb = weights + (((int64_t)e * nrows + r) * nb + b) * bytes;
+                    const uint8_t* ab = act + (t * nb + b) * Q8_1_BYTES;
+                    double dw = oracle_half_to_double(rd16(wb));
+                    double da = oracle_half_to_double(rd16(ab));
+                    double sa = oracle_half_to_double(rd16(ab + 2));
+                    y += dw * da * (double)oracle_gguf_block_dot(type, wb, ab) + gguf_offset(wb, type) * sa;
+                }
+            }
+            out[s * nrows + r] = (float)y;
+        }
+    }
+}
+
 /* ----------------------------------------------------- gated activation */
 
 /* The two gated activations that sit between the expert layers: GELU in its

@@ -26,6 +26,11 @@
  *                                                  of the experts sum to
  *                                                  oracle_moe_q4_0_q8_1 bit for bit;
  *                                                  hand-checked masking
+ *   oracle_dequantize_gguf / _gguf_block_dot /     pinned: hand blocks per type, an
+ *   oracle_moe_gguf_q8_1                           independent numpy decode + einsum,
+ *                                                  Q4_0 equal to oracle_moe_q4_0_q8_1
+ *                                                  bit for bit, the offset term within
+ *                                                  the fp16 rounding of s
  *   oracle_act_mul / _quantize_q8_1                pinned: 50-digit mpmath values, torch
  *                                                  activations, the exact
  *                                                  GELU x*Phi(x) within the tanh
@@ -42,6 +47,14 @@
  *   weights [E][N][K/32] Q4_0, activations [T][K/32] Q8_1,
  *   topk_ids [T][k] int32 (slot s = t*k + j), out [T][k][N] fp32.
  *   gated activation: h [rows][2 * n_inter] fp32 (gate | up), a [rows][n_inter].
+ * Other GGUF weight types with 32-weight blocks (weight i = q_i d + c):
+ *   Q4_1 20 B: fp16 d, fp16 m, 16 B qs (nibbles as Q4_0); q_i = nibble, c = m
+ *   Q5_0 22 B: fp16 d, 4 B qh (little-endian), 16 B qs; q_i = nibble_i |
+ *       (bit i of qh) << 4, minus 16; c = 0
+ *   Q5_1 24 B: fp16 d, fp16 m, 4 B qh, 16 B qs; q_i = nibble_i | (bit i) << 4;
+ *       c = m
+ *   Q8_0 34 B: fp16 d, 32 int8 q; c = 0
+ *   weights [E][N][K/32] blocks of the type.
  */
 #ifndef FT_ORACLE_H
 #define FT_ORACLE_H
@@ -60,6 +73,19 @@ void oracle_dequantize_q4_0(const uint8_t* blocks, int64_t n_blocks, double* out
 
 void oracle_quantize_q8_1(const uint16_t* x_fp16, int64_t tokens, int64_t ncols, uint8_t* out);
 void oracle_dequantize_q8_1(const uint8_t* blocks, int64_t n_blocks, double* out);
+
+/* GGUF weight types with 32-weight blocks (GGML type numbers). */
+#define ORACLE_GGUF_Q4_0 2
+#define ORACLE_GGUF_Q4_1 3
+#define ORACLE_GGUF_Q5_0 6
+#define ORACLE_GGUF_Q5_1 7
+#define ORACLE_GGUF_Q8_0 8
+int32_t oracle_gguf_block_bytes(int32_t type);
+void oracle_dequantize_gguf(int32_t type, const uint8_t* blocks, int64_t n_blocks, double* out);
+int32_t oracle_gguf_block_dot(int32_t type, const uint8_t* w_block, const uint8_t* a_block);
+void oracle_moe_gguf_q8_1(int32_t type, const uint8_t* weights, const uint8_t* act, const int32_t* topk_ids,
+                          float* out, int64_t tokens, int32_t top_k, int32_t n_experts,
+                          int64_t nrows, int64_t ncols);
 
 #define ORACLE_ACT_SILU 0
 #define ORACLE_ACT_GELU_TANH 1

@@ -500,11 +500,124 @@ def pin_act_quantize_numpy(o):
         assert not blk[2].any()
 
 
+# ------------------------------------------------- other GGUF weight types
+def numpy_decode_gguf(wtype, w):
+    """Independent vectorised decode of the 32-weight GGUF types [..., nb, bytes]
+    -> (levels int64 [..., nb, 32], d fp64 [..., nb], offset fp64 [..., nb])."""
+    w = np.ascontiguousarray(w)
+    d = w[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    zero = np.zeros_like(d)
+    if wtype == "q8_0":
+        return w[..., 2:34].copy().view(np.int8).astype(np.int64), d, zero
+    has_m = wtype in ("q4_1", "q5_1")
+    m = w[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64) if has_m else zero
+    if wtype == "q4_1":
+        qs = w[..., 4:20].astype(np.int64)
+        return np.concatenate([qs & 15, qs >> 4], axis=-1), d, m
+    h0 = 4 if has_m else 2
+    qh = w[..., h0:h0 + 4].copy().view("<u4")[..., 0].astype(np.int64)
+    qs = w[..., h0 + 4:h0 + 20].astype(np.int64)
+    nib = np.concatenate([qs & 15, qs >> 4], axis=-1)
+    bits = (qh[..., None] >> np.arange(32)) & 1
+    lev = nib | (bits << 4)
+    return (lev - 16 if wtype == "q5_0" else lev), d, m
+
+
+def _gguf_random(wtype, E=3, N=5, K=96, seed=0):
+    from bit_quantized_moe_quantize_gb300 import synth
+    return synth.make_weights_gguf(synth.custom_workload(E, 2, K, N, seed), wtype)
+
+
+def pin_gguf_hand(o):
+    """Hand-assembled blocks of each type, decoded and dotted by hand."""
+    a = q8_block(0x3C00, 0x0000, [1] * 32)                  # d_a = 1, q_a = 1, s = 0 (stored)
+    # Q8_0: d = 1, codes -128, 127, 0, ..., 5
+    b = np.zeros(34, np.uint8)
+    b[0], b[1] = 0x00, 0x3C
+    q = np.zeros(32, np.int8)
+    q[:3] = [-128, 127, 0]
+    q[31] = 5
+    b[2:] = q.view(np.uint8)
+    assert o.dequantize_gguf("q8_0", b[None]).tolist() == q.astype(float).tolist()
+    assert o.gguf_block_dot("q8_0", b, a) == 4
+    # Q4_1: d = 0.5, m = -2; low nibble j, high nibble 15 - j -> w_j = j/2 - 2, w_{j+16} = (15-j)/2 - 2
+    b = np.zeros(20, np.uint8)
+    b[0:2] = [0x00, 0x38]
+    b[2:4] = [0x00, 0xC0]
+    b[4:] = [j | ((15 - j) << 4) for j in range(16)]
+    want = [j / 2 - 2 for j in range(16)] + [(15 - j) / 2 - 2 for j in range(16)]
+    assert o.dequantize_gguf("q4_1", b[None]).tolist() == want
+    assert o.gguf_block_dot("q4_1", b, a) == 2 * sum(range(16))        # levels, not values
+    # Q5_0: d = 1, all nibbles 0, qh bits 1 and 16 set -> levels 0 at i = 1, 16, else -16
+    b = np.zeros(22, np.uint8)
+    b[0:2] = [0x00, 0x3C]
+    b[2:6] = [0x02, 0x00, 0x01, 0x00]
+    lev = [-16] * 32
+    lev[1] = lev[16] = 0
+    assert o.dequantize_gguf("q5_0", b[None]).tolist() == [float(v) for v in lev]
+    assert o.gguf_block_dot("q5_0", b, a) == -16 * 30
+    # Q5_1: d = 0.25, m = 1; nibbles 15 everywhere, qh = 0x80000000 -> level 31 at i = 31, else 15
+    b = np.zeros(24, np.uint8)
+    b[0:2] = [0x00, 0x34]
+    b[2:4] = [0x00, 0x3C]
+    b[4:8] = [0x00, 0x00, 0x00, 0x80]
+    b[8:] = 0xFF
+    want = [15 * 0.25 + 1] * 31 + [31 * 0.25 + 1]
+    assert o.dequantize_gguf("q5_1", b[None]).tolist() == want
+    assert o.gguf_block_dot("q5_1", b, a) == 15 * 31 + 31
+
+
+def pin_gguf_numpy_decode(o):
+    for wtype in ("q4_1", "q5_0", "q5_1", "q8_0"):
+        w = _gguf_random(wtype, seed=3)
+        lev, d, m = numpy_decode_gguf(wtype, w)
+        want = lev * d[..., None] + m[..., None]
+        got = o.dequantize_gguf(wtype, w)
+        assert np.array_equal(got, want.reshape(got.shape)), wtype
+
+
+def pin_gguf_moe_numpy(o):
+    """The matmul of each type against a numpy restatement: per block
+    d_w d_a sum(q_w q_a) + m s_a with s_a the stored fp16 s, in fp64; and
+    against the plain dequantized dot within the fp16 rounding of s."""
+    from bit_quantized_moe_quantize_gb300 import synth
+    rng = np.random.default_rng(4)
+    E, k, K, N, T = 4, 2, 128, 6, 5
+    x = rng.standard_normal((T, K)).astype(np.float16)
+    act = o.quantize_q8_1(x)
+    ids = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    qa = act[..., 4:].view(np.int8).astype(np.int64)
+    da = act[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    sa = act[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
+    xa = numpy_decode_q8_1(act)
+    for wtype in ("q4_1", "q5_0", "q5_1", "q8_0"):
+        w = _gguf_random(wtype, E=E, N=N, K=K, seed=5)
+        lev, d, m = numpy_decode_gguf(wtype, w)                  # [E, N, nb, 32], [E, N, nb]
+        got = o.moe_gguf(wtype, w, act, ids).astype(np.float64)
+        wv = (lev * d[..., None] + m[..., None]).reshape(E, N, K)
+        for t in range(T):
+            for j in range(k):
+                e = ids[t, j]
+                dots = np.einsum("rbi,bi->rb", lev[e], qa[t])
+                want = (d[e] * da[t] * dots + m[e] * sa[t]).sum(axis=1)
+                assert np.allclose(got[t, j], want, rtol=1e-6, atol=1e-9), wtype
+                plain = wv[e] @ xa[t]
+                slack = (np.abs(m[e]) * (np.abs(sa[t]) * 2.0 ** -11 + 2.0 ** -24)).sum(axis=1)
+                assert np.all(np.abs(want - plain) <= slack + 1e-12), wtype
+
+
+def pin_gguf_q4_0_is_the_q4_0_matmul(o):
+    w, x, ids = tiny_case(seed=9)
+    act = o.quantize_q8_1(x)
+    assert np.array_equal(o.moe_gguf("q4_0", w, act, ids), o.moe(w, act, ids))
+
+
 ALL_PINS = [
     pin_fp16, pin_q4_0_hand, pin_q4_0_nearest_level, pin_q4_0_matches_generator, pin_q4_0_dequant,
     pin_q8_1_hand, pin_q8_1_numpy, pin_q8_1_error_bound, pin_route, pin_block_dot_hand,
     pin_moe_closed_form_vs_bruteforce, pin_moe_numpy_einsum, pin_moe_block_dots,
     pin_moe_split_invariance, pin_moe_bad_ids, pin_moe_slots_numpy_einsum, pin_moe_slots_replicated_rows,
     pin_moe_ep_shards_sum_to_full, pin_act_library, pin_act_tail_accuracy, pin_act_gelu_vs_erf, pin_act_odd_identity, pin_act_hand,
-    pin_act_quantize_numpy,
+    pin_act_quantize_numpy, pin_gguf_hand, pin_gguf_numpy_decode, pin_gguf_moe_numpy,
+    pin_gguf_q4_0_is_the_q4_0_matmul,
 ]

@@ -28,7 +28,7 @@ EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_m
            "ft_moe_reserve", "ft_moe_release", "ft_moe_read_device_error", "ft_moe_set_path",
            "ft_moe_selected_path", "ft_moe_block_dots", "ft_last_error", "ft_abi_version", "ft_profile_enable",
            "ft_profile_read", "ft_moe_route_offsets_noalloc", "ft_moe_q4_0_q8_1_slots",
-           "ft_moe_q4_0_q8_1_ep", "ft_act_mul_quantize_q8_1", "ft_moe_ffn_q4_0_q8_1")
+           "ft_moe_q4_0_q8_1_ep", "ft_act_mul_quantize_q8_1", "ft_moe_ffn_q4_0_q8_1", "ft_moe_gguf_q8_1")
 
 
 class FtError(RuntimeError):
@@ -63,6 +63,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.ft_moe_q4_0_q8_1_ep.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp]
         L.ft_moe_block_dots.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_act_mul_quantize_q8_1.argtypes = [vp, vp, i64, i64, i32, vp]
+        L.ft_moe_gguf_q8_1.argtypes = [i32, vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_moe_ffn_q4_0_q8_1.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i64, i64, i32, vp]
         L.ft_moe_workspace_bytes.argtypes = [i64, i32, i32, i64, i64]
         L.ft_moe_workspace_bytes.restype = ctypes.c_size_t
@@ -207,6 +208,32 @@ def moe_q4_0_q8_1_ep(weights_local, act, topk_ids, n_experts_global, expert_star
     _check(load().ft_moe_q4_0_q8_1_ep(ctypes.c_void_p(weights_local.data_ptr()), ctypes.c_void_p(act.data_ptr()),
                                       ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, int(n_experts_global),
                                       int(expert_start), E_local, N, K, _stream(weights_local)))
+    return out
+
+
+# GGUF weight types with 32-weight blocks: GGML type number, bytes per block
+WEIGHT_TYPES = {"q4_0": (2, 18), "q4_1": (3, 20), "q5_0": (6, 22), "q5_1": (7, 24), "q8_0": (8, 34)}
+
+
+def moe_gguf_q8_1(wtype, weights, act, topk_ids, out=None):
+    """Routed matmul with weights of a 32-weight GGUF type (ft_moe_gguf_q8_1):
+    weights uint8 [E, N, K/32, bytes of the type] x Q8_1 [T, K/32, 36] -> fp32 [T, k, N]."""
+    torch = _torch()
+    tid, bb = WEIGHT_TYPES[wtype]
+    _dev(weights, torch.uint8, "weights", 4)
+    _dev(act, torch.uint8, "act", 3)
+    _dev(topk_ids, torch.int32, "topk_ids", 2)
+    E, N, nb, wb = weights.shape
+    T, nb2, ab = act.shape
+    if wb != bb or ab != 36 or nb != nb2 or topk_ids.shape[0] != T:
+        raise ValueError(f"shape mismatch for {wtype}: weights {tuple(weights.shape)} act {tuple(act.shape)} "
+                         f"topk_ids {tuple(topk_ids.shape)}")
+    k = topk_ids.shape[1]
+    if out is None:
+        out = torch.empty((T, k, N), dtype=torch.float32, device=weights.device)
+    po = _dev(out, torch.float32, "out")
+    _check(load().ft_moe_gguf_q8_1(tid, ctypes.c_void_p(weights.data_ptr()), ctypes.c_void_p(act.data_ptr()),
+                                   ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, E, N, nb * 32, _stream(weights)))
     return out
 
 

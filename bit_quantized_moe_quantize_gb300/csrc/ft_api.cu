@@ -154,6 +154,7 @@ struct Shape {
     // expert-parallel shard: ids are global in [0, n_global); this call holds
     // experts [expert_start, expert_start + n_experts) (0 and n_experts otherwise)
     int32_t expert_start, n_global;
+    int32_t wtype;     // FT_TYPE_* of the weights
     // routed slots per held expert on average (what the tile plans go by)
     double mean() const { return static_cast<double>(n_slots) / n_global; }
 };
@@ -175,6 +176,7 @@ static int check_route_args(int64_t tokens, int32_t top_k, int32_t n_experts, Sh
     sh->act_div = top_k;
     sh->expert_start = 0;
     sh->n_global = n_experts;
+    sh->wtype = FT_TYPE_Q4_0;
     return FT_OK;
 }
 
@@ -188,7 +190,7 @@ static int check_matmul_args(int64_t tokens, int32_t top_k, int32_t n_experts, i
     int64_t en, wbytes, obytes;
     if (!mul_ok(n_experts, nrows, &en) || en > INT32_MAX)
         return fail(FT_ERR_SIZE, "n_experts * nrows must be < 2^31");
-    if (!mul_ok(en, (ncols / 32) * 18, &wbytes)) return fail(FT_ERR_SIZE, "weight size overflows int64");
+    if (!mul_ok(en, (ncols / 32) * 34, &wbytes)) return fail(FT_ERR_SIZE, "weight size overflows int64");
     if (!mul_ok(sh->n_slots, nrows, &obytes) || obytes > INT64_MAX / 4)
         return fail(FT_ERR_SIZE, "output size overflows int64");
     sh->nrows = nrows;
@@ -321,6 +323,7 @@ static bool gemm_shape_ok(const Shape& sh) {
 // pays off once experts see enough slots to fill a 128-column MMA tile.
 static int choose_path(const Shape& sh, int setting) {
     if (setting == FT_PATH_GEMV) return FT_PATH_GEMV;
+    if (sh.wtype != FT_TYPE_Q4_0) return setting == FT_PATH_GEMM ? FT_PATH_GEMM : FT_PATH_GEMV;
     if (setting == FT_PATH_GEMM) return FT_PATH_GEMM;
     if (!gemm_shape_ok(sh)) return FT_PATH_GEMV;
     return sh.mean() >= 16.0 ? FT_PATH_GEMM : FT_PATH_GEMV;
@@ -329,6 +332,8 @@ static int choose_path(const Shape& sh, int setting) {
 static int run_matmul(const void* weights, const void* act, const int32_t* topk_ids, float* out, int32_t* dots,
                       const Shape& sh, cudaStream_t s) {
     const int path = choose_path(sh, path_setting());
+    if (path == FT_PATH_GEMM && sh.wtype != FT_TYPE_Q4_0)
+        return fail(FT_ERR_ARG, "the tensor-core path takes Q4_0 weights only (weight type %d)", sh.wtype);
     if (path == FT_PATH_GEMM && !gemm_shape_ok(sh))
         return fail(FT_ERR_ARG, "the tensor-core path needs ncols %% 256 == 0 and n_experts * nrows >= 128 (got %lld, %lld)",
                     (long long)sh.ncols, (long long)sh.n_experts * sh.nrows);
@@ -344,10 +349,12 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     rb.tiles_gemm = reinterpret_cast<int32_t*>(ws + L.tiles_gemm);
     rb.err = reinterpret_cast<uint32_t*>(ws + L.err);
 
-    const GemvPlan gp = plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols, sh.mean());
+    const GemvPlan gp = plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols, sh.mean(),
+                                  weight_block_bytes(sh.wtype));
     const int tile_width = gemm_tile_width(sh.mean());
-    if (path == FT_PATH_GEMV && gp.smem > 227 * 1024)
-        return fail(FT_ERR_SIZE, "GEMV tile needs %zu bytes of shared memory", gp.smem);
+    if (path == FT_PATH_GEMV && (gp.smem > 227 * 1024 || gp.stages < 1))
+        return fail(FT_ERR_SIZE, "GEMV tile needs %zu bytes of shared memory (%d ring stages of %lld-column rows fit)",
+                    gp.smem, gp.stages, (long long)sh.ncols);
     uint32_t* zero_rows = dots ? reinterpret_cast<uint32_t*>(dots) : reinterpret_cast<uint32_t*>(out);
     const int64_t row_words = dots ? sh.nrows * sh.nb : sh.nrows;
     prof_mark(kProfRouteBegin, s);
@@ -367,7 +374,7 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     if (path == FT_PATH_GEMV)
         st = launch_gemv(gp, static_cast<const uint8_t*>(weights), static_cast<const uint8_t*>(act), rb.perm,
                          rb.offsets, rb.tiles_gemv, out, dots, rb.err, sh.n_slots, sh.act_div, sh.n_experts, sh.nrows,
-                         sh.ncols, s);
+                         sh.ncols, s, sh.wtype);
     else
         st = launch_gemm(static_cast<const uint8_t*>(weights), static_cast<const uint8_t*>(act), rb.perm,
                          rb.offsets, rb.tiles_gemm, out, dots, rb.err, sh.n_slots, sh.act_div, sh.n_experts, sh.nrows,
@@ -429,13 +436,16 @@ int ft_moe_route_offsets(const int32_t* topk_ids, int64_t tokens, int32_t top_k,
 
 static int matmul_entry(const void* weights, const void* act, const int32_t* topk_ids, float* out, int32_t* dots,
                         int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols,
-                        void* stream, bool act_per_slot = false, int32_t expert_start = 0, int32_t n_local = 0) {
+                        void* stream, bool act_per_slot = false, int32_t expert_start = 0, int32_t n_local = 0,
+                        int32_t wtype = FT_TYPE_Q4_0) {
     g_last_error.clear();
     Shape sh{};
     // n_experts counts every expert the ids may name; an expert-parallel shard
     // (n_local > 0) holds experts [expert_start, expert_start + n_local) of them
     if (int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh)) return st;
     if (act_per_slot) sh.act_div = 1;
+    if (weight_block_bytes(wtype) == 0) return fail(FT_ERR_ARG, "unknown weight type %d", wtype);
+    sh.wtype = wtype;
     if (n_local > 0) {
         if (expert_start < 0 || static_cast<int64_t>(expert_start) + n_local > n_experts)
             return fail(FT_ERR_ARG, "the shard's experts [%d, %lld) must lie in [0, n_experts_global=%d)", expert_start,
@@ -539,6 +549,23 @@ int ft_moe_ffn_q4_0_q8_1(const void* w13, const void* w2, const void* act, const
         return st;
     if (int st = ft_act_mul_quantize_q8_1(h, act_mid, sh.n_slots, n_inter, act_kind, stream)) return st;
     return matmul_entry(w2, act_mid, topk_ids, out, nullptr, tokens, top_k, n_experts, hidden, n_inter, stream, true);
+}
+
+int ft_moe_gguf_q8_1(int32_t wtype, const void* weights, const void* act, const int32_t* topk_ids, float* out,
+                     int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols, void* stream) {
+    if (weight_block_bytes(wtype) == 0) {
+        g_last_error.clear();
+        return fail(FT_ERR_ARG, "unknown weight type %d", wtype);
+    }
+    if (!out) {
+        g_last_error.clear();
+        Shape sh{};
+        if (int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh)) return st;
+        if (sh.n_slots == 0) return FT_OK;
+        return fail(FT_ERR_ARG, "null pointer");
+    }
+    return matmul_entry(weights, act, topk_ids, out, nullptr, tokens, top_k, n_experts, nrows, ncols, stream, false,
+                        0, 0, wtype);
 }
 
 int ft_moe_block_dots(const void* weights, const void* act, const int32_t* topk_ids, int32_t* dots, int64_t tokens,

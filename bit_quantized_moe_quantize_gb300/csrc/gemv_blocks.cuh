@@ -1,0 +1,361 @@
+// The block-per-lane GEMV kernel of the routed expert matmul, templated on the
+// weight block type (GGUF Q4_0, Q4_1, Q5_0, Q5_1, Q8_0: the per-type
+// launchers of moe_vec.cuh on FreeToken PR #185, "Notes"), with its shared
+// arguments and launch helpers.  moe_gemv.cu instantiates it for Q4_0 next to
+// the row-per-lane kernel; moe_gemv_gguf.cu for the other types.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "gemm_common.cuh"
+
+namespace ft {
+
+
+struct GemvArgs {
+    const uint8_t* weights;
+    const uint8_t* act;
+    const int32_t* perm;
+    const int32_t* offsets;
+    const int32_t* tiles;
+    float* out;
+    int32_t* dots;
+    uint32_t* err;
+    int64_t nrows;
+    int32_t nb;          // blocks per row
+    int32_t top_k;
+    int32_t n_experts;
+    int32_t stages;      // depth of the weight ring (1..kMaxStages)
+    int64_t rows_per_cta;
+    int32_t bulk;        // weight rows 16-byte aligned -> bulk copies
+    int32_t row_warps;   // row-per-lane kernel: row groups of 32 per CTA
+    int32_t ksplit;      // row-per-lane kernel: warps sharing a row group, each on every ksplit-th box
+};
+
+constexpr int kMaxStages = 4;
+
+// Shared-memory carve-up (bytes), in this order:
+//   mbarriers [kMaxStages] (32) | slot ids int32[G] (pad 16) | qa [G][nb][32] |
+//   da f32 [G][nb] | suma i32 [G][nb] | weight ring [stages][R rows][nb][18] (+16 pad each)
+__host__ __device__ inline size_t gemv_act_bytes(int G, int nb) {
+    return (32 + ((static_cast<size_t>(G) * 4 + 15) / 16) * 16 + static_cast<size_t>(G) * nb * 40 + 15) / 16 * 16;
+}
+__host__ __device__ inline size_t gemv_stage_bytes(int R, int nb, int block_bytes = Q4_0_BYTES) {
+    return (static_cast<size_t>(R) * nb * block_bytes + 16 + 15) / 16 * 16;
+}
+
+__device__ __forceinline__ int32_t find_expert(const int32_t* tiles, int32_t n_experts, int64_t t) {
+    // largest e in [0, E) with tiles[e] <= t  (tiles[E] > t is guaranteed by the caller)
+    int32_t lo = 0, hi = n_experts - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (tiles[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// One 18-byte Q4_0 block at a 2-byte aligned shared-memory offset: fp32 d and
+// the 16 nibble bytes as four words (qs[4i..4i+3] in word i).
+__device__ __forceinline__ void load_q4_block(const uint8_t* base, uint32_t off, float& d, uint32_t (&q)[4]) {
+    const uint32_t sh = off & 2u;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (off - sh));
+    const uint32_t W0 = w[0], W1 = w[1], W2 = w[2], W3 = w[3], W4 = w[4];
+    const uint32_t sel = sh ? 0x7654u : 0x5432u;
+    q[0] = __byte_perm(W0, W1, sel);
+    q[1] = __byte_perm(W1, W2, sel);
+    q[2] = __byte_perm(W2, W3, sel);
+    q[3] = __byte_perm(W3, W4, sel);
+    d = __half2float(__ushort_as_half(static_cast<unsigned short>((W0 >> (sh * 8)) & 0xFFFFu)));
+}
+
+// NW words starting at a 2-byte aligned shared-memory offset (reads one word
+// past them: every ring stage carries 16 bytes of padding)
+template <int NW>
+__device__ __forceinline__ void load_words(const uint8_t* base, uint32_t off, uint32_t (&w)[NW]) {
+    const uint32_t sh = off & 2u;
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(base + (off - sh));
+    uint32_t raw[NW + 1];
+#pragma unroll
+    for (int i = 0; i <= NW; ++i) raw[i] = p[i];
+    const uint32_t sel = sh ? 0x5432u : 0x3210u;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = __byte_perm(raw[i], raw[i + 1], sel);
+}
+
+__device__ __forceinline__ float half_at(const uint8_t* base, uint32_t off) {
+    return __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(base + off)));
+}
+
+// bits 0..3 of x -> bit 4 of bytes 0..3
+__device__ __forceinline__ uint32_t spread4(uint32_t x) {
+    return ((x & 1u) << 4) | ((x & 2u) << 11) | ((x & 4u) << 18) | ((x & 8u) << 25);
+}
+
+// Weight block types of the block-per-lane kernel (GGUF, 32 weights each;
+// weight i = q_i d + c): per type its bytes, the level offset subtracted from
+// the stored level (Q4_0: 8, Q5_0: 16) and whether the block stores an fp16
+// m (c = m, Q4_1 / Q5_1; else c = 0).
+template <int WT>
+struct WBlock;
+template <> struct WBlock<FT_TYPE_Q4_0> { static constexpr int bytes = 18, level0 = 8; static constexpr bool has_m = false; };
+template <> struct WBlock<FT_TYPE_Q4_1> { static constexpr int bytes = 20, level0 = 0; static constexpr bool has_m = true; };
+template <> struct WBlock<FT_TYPE_Q5_0> { static constexpr int bytes = 22, level0 = 16; static constexpr bool has_m = false; };
+template <> struct WBlock<FT_TYPE_Q5_1> { static constexpr int bytes = 24, level0 = 0; static constexpr bool has_m = true; };
+template <> struct WBlock<FT_TYPE_Q8_0> { static constexpr int bytes = 34, level0 = 0; static constexpr bool has_m = false; };
+
+// One weight block at a 2-byte aligned shared-memory offset: fp32 d and m,
+// and its 32 stored levels as int8 lanes of eight words, weights 0..15 in
+// lo[0..3] and 16..31 in hi[0..3] (the order of the Q8_1 codes they meet).
+template <int WT>
+__device__ __forceinline__ void decode_block(const uint8_t* base, uint32_t off, float& d, float& m, int (&lo)[4],
+                                             int (&hi)[4]) {
+    m = 0.0f;
+    if constexpr (WT == FT_TYPE_Q4_0) {
+        uint32_t q[4];
+        load_q4_block(base, off, d, q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo[i] = static_cast<int>(q[i] & 0x0F0F0F0Fu);
+            hi[i] = static_cast<int>((q[i] >> 4) & 0x0F0F0F0Fu);
+        }
+    } else if constexpr (WT == FT_TYPE_Q4_1) {
+        uint32_t w[5];
+        load_words<5>(base, off, w);
+        d = __half2float(__ushort_as_half(static_cast<unsigned short>(w[0] & 0xFFFFu)));
+        m = __half2float(__ushort_as_half(static_cast<unsigned short>(w[0] >> 16)));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo[i] = static_cast<int>(w[1 + i] & 0x0F0F0F0Fu);
+            hi[i] = static_cast<int>((w[1 + i] >> 4) & 0x0F0F0F0Fu);
+        }
+    } else if constexpr (WT == FT_TYPE_Q5_0 || WT == FT_TYPE_Q5_1) {
+        constexpr uint32_t H0 = WT == FT_TYPE_Q5_0 ? 2 : 4;   // offset of the 5th-bit word
+        d = half_at(base, off);
+        if constexpr (WT == FT_TYPE_Q5_1) m = half_at(base, off + 2);
+        uint32_t qh[1], qs[4];
+        load_words<1>(base, off + H0, qh);
+        load_words<4>(base, off + H0 + 4, qs);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo[i] = static_cast<int>((qs[i] & 0x0F0F0F0Fu) | spread4(qh[0] >> (4 * i)));
+            hi[i] = static_cast<int>(((qs[i] >> 4) & 0x0F0F0F0Fu) | spread4(qh[0] >> (16 + 4 * i)));
+        }
+    } else {
+        static_assert(WT == FT_TYPE_Q8_0, "weight type");
+        d = half_at(base, off);
+        uint32_t q[8];
+        load_words<8>(base, off + 2, q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo[i] = static_cast<int>(q[i]);
+            hi[i] = static_cast<int>(q[4 + i]);
+        }
+    }
+}
+
+// int32 -> fp32 for |v| < 2^22 with an integer add and a float subtract
+__device__ __forceinline__ float small_int_to_float(int v) {
+    return __int_as_float(v + 0x4B400000) - 12582912.0f;
+}
+
+// grid.x: slot tiles (G slots of one expert); grid.y: a contiguous range of that
+// expert's rows, streamed through a ring of `stages` bulk copies of R = 8 * RW
+// rows.  Warp w handles rows w*RW .. w*RW+RW-1 of each stage, lane l the blocks
+// b = l, l + 32, ... of those rows, and every activation block it loads from
+// shared memory serves RW rows.  WT is the weight block type: per block
+//   d_w d_a (sum_i q_i q_a[i] - level0 * sum_i q_a[i])  +  m s_a
+// with q_i the stored level, the m term only for the types that store m
+// (s_a: the activation block's fp16 s, the sum the Q8_1 format stores for it).
+template <int WT, int G, int RW, bool DUMP>
+__global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
+    constexpr int R = 8 * RW;
+    constexpr int WB = WBlock<WT>::bytes;
+    constexpr bool HAS_M = WBlock<WT>::has_m;
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int64_t t = blockIdx.x;
+    const int32_t E = a.n_experts;
+    if (t >= a.tiles[E]) return;
+    const int64_t r_begin = static_cast<int64_t>(blockIdx.y) * a.rows_per_cta;
+    if (r_begin >= a.nrows) return;
+    const int64_t r_end = min(a.nrows, r_begin + a.rows_per_cta);
+    const int32_t n_st = static_cast<int32_t>((r_end - r_begin + R - 1) / R);
+    const int32_t e = find_expert(a.tiles, E, t);
+    const int64_t p0 = static_cast<int64_t>(a.offsets[e]) + (t - a.tiles[e]) * G;
+    const int32_t ng = static_cast<int32_t>(min(static_cast<int64_t>(G), a.offsets[e + 1] - p0));
+    const int32_t nb = a.nb;
+    const int NS = a.stages;
+
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    int32_t* slot = reinterpret_cast<int32_t*>(smem + 32);
+    size_t o = 32 + ((static_cast<size_t>(G) * 4 + 15) / 16) * 16;
+    uint8_t* qa = smem + o;
+    o += static_cast<size_t>(G) * nb * 32;
+    float* da = reinterpret_cast<float*>(smem + o);
+    o += static_cast<size_t>(G) * nb * 4;
+    int32_t* suma = reinterpret_cast<int32_t*>(smem + o);
+    uint8_t* ring = smem + gemv_act_bytes(G, nb);
+    const size_t stage_bytes = gemv_stage_bytes(R, nb, WB);
+
+    const int64_t row_bytes = static_cast<int64_t>(nb) * WB;
+    const uint8_t* wexp = a.weights + static_cast<int64_t>(e) * a.nrows * row_bytes;
+    auto stage_rows = [&](int32_t st) { return static_cast<int32_t>(min(static_cast<int64_t>(R), r_end - (r_begin + st * R))); };
+    auto issue = [&](int32_t st) {   // one thread: bulk copy of stage st into its ring slot
+        const int32_t buf = st % NS;
+        const uint32_t bytes = static_cast<uint32_t>(stage_rows(st) * row_bytes);
+        mbar_arrive_expect_tx(&bar[buf], bytes);
+        bulk_g2s(ring + buf * stage_bytes, wexp + (r_begin + static_cast<int64_t>(st) * R) * row_bytes, bytes, &bar[buf]);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x < G) slot[threadIdx.x] = threadIdx.x < ng ? a.perm[p0 + threadIdx.x] : 0;
+    __syncthreads();
+    if (a.bulk && threadIdx.x == 0)
+        for (int32_t st = 0; st < min(NS, n_st); ++st) issue(st);
+
+    // stage the G activation rows once: int8 block, fp32 d, exact sum of q
+    for (int32_t i = threadIdx.x; i < ng * nb; i += blockDim.x) {
+        const int32_t g = i / nb, b = i - g * nb;
+        const int64_t tok = slot[g] / a.top_k;
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(a.act + (tok * nb + b) * Q8_1_BYTES);
+        const uint32_t ds = __ldg(src);
+        const uint4 q0 = make_uint4(__ldg(src + 1), __ldg(src + 2), __ldg(src + 3), __ldg(src + 4));
+        const uint4 q1 = make_uint4(__ldg(src + 5), __ldg(src + 6), __ldg(src + 7), __ldg(src + 8));
+        uint4* dst = reinterpret_cast<uint4*>(qa + (static_cast<size_t>(g) * nb + b) * 32);
+        dst[0] = q0;
+        dst[1] = q1;
+        da[g * nb + b] = __half2float(__ushort_as_half(static_cast<unsigned short>(ds & 0xFFFFu)));
+        if constexpr (HAS_M) {   // the offset term needs s, not the code sum
+            suma[g * nb + b] = __float_as_int(__half2float(__ushort_as_half(static_cast<unsigned short>(ds >> 16))));
+            continue;
+        }
+        int sm = 0;
+        sm = __dp4a(static_cast<int>(q0.x), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q0.y), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q0.z), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q0.w), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q1.x), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q1.y), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q1.z), 0x01010101, sm);
+        sm = __dp4a(static_cast<int>(q1.w), 0x01010101, sm);
+        suma[g * nb + b] = sm;
+    }
+    __syncthreads();
+
+    const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+    for (int32_t st = 0; st < n_st; ++st) {
+        const int32_t buf = st % NS;
+        const int32_t nr = stage_rows(st);
+        const int64_t r0 = r_begin + static_cast<int64_t>(st) * R;
+        uint8_t* wt = ring + buf * stage_bytes;
+        if (a.bulk) {
+            if (!mbar_wait(&bar[buf], static_cast<uint32_t>((st / NS) & 1), a.err)) break;
+        } else {
+            // rows not 16-byte aligned: 2-byte loads (blocks are 2-byte aligned)
+            const uint16_t* s16 = reinterpret_cast<const uint16_t*>(wexp + r0 * row_bytes);
+            uint16_t* d16 = reinterpret_cast<uint16_t*>(wt);
+            const uint32_t n16 = static_cast<uint32_t>(nr * row_bytes / 2);
+            for (uint32_t i = threadIdx.x; i < n16; i += blockDim.x) d16[i] = __ldg(s16 + i);
+            __syncthreads();
+        }
+
+        const int32_t rl0 = static_cast<int32_t>(warp) * RW;   // this warp's first row in the stage
+        float acc[RW][G];
+#pragma unroll
+        for (int j = 0; j < RW; ++j)
+#pragma unroll
+            for (int g = 0; g < G; ++g) acc[j][g] = 0.0f;
+        if (rl0 < nr) {
+            for (int b = static_cast<int>(lane); b < nb; b += 32) {
+                int lo[RW][4], hi[RW][4];
+                float dw[RW], mw[RW];
+#pragma unroll
+                for (int j = 0; j < RW; ++j) {
+                    const int rl = min(rl0 + j, nr - 1);       // rows past the stage repeat the last one
+                    decode_block<WT>(wt, static_cast<uint32_t>(rl * row_bytes + b * WB), dw[j], mw[j], lo[j], hi[j]);
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    if (g < ng) {
+                        const uint4* av = reinterpret_cast<const uint4*>(qa + (static_cast<size_t>(g) * nb + b) * 32);
+                        const uint4 A0 = av[0], A1 = av[1];
+                        const float dag = da[g * nb + b];
+                        const int sa0 = HAS_M ? 0 : WBlock<WT>::level0 * suma[g * nb + b];
+                        const float sag = HAS_M ? __int_as_float(suma[g * nb + b]) : 0.0f;
+#pragma unroll
+                        for (int j = 0; j < RW; ++j) {
+                            int dot = -sa0;
+                            dot = __dp4a(lo[j][0], static_cast<int>(A0.x), dot);
+                            dot = __dp4a(lo[j][1], static_cast<int>(A0.y), dot);
+                            dot = __dp4a(lo[j][2], static_cast<int>(A0.z), dot);
+                            dot = __dp4a(lo[j][3], static_cast<int>(A0.w), dot);
+                            dot = __dp4a(hi[j][0], static_cast<int>(A1.x), dot);
+                            dot = __dp4a(hi[j][1], static_cast<int>(A1.y), dot);
+                            dot = __dp4a(hi[j][2], static_cast<int>(A1.z), dot);
+                            dot = __dp4a(hi[j][3], static_cast<int>(A1.w), dot);
+                            if constexpr (DUMP) {
+                                if (rl0 + j < nr)
+                                    a.dots[(static_cast<int64_t>(slot[g]) * a.nrows + r0 + rl0 + j) * nb + b] = dot;
+                            } else {
+                                acc[j][g] = fmaf(small_int_to_float(dot), dw[j] * dag, acc[j][g]);
+                                if constexpr (HAS_M) acc[j][g] = fmaf(mw[j], sag, acc[j][g]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if constexpr (!DUMP) {
+#pragma unroll
+            for (int j = 0; j < RW; ++j)
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float v = acc[j][g];
+#pragma unroll
+                    for (int o2 = 16; o2 > 0; o2 >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o2);
+                    acc[j][g] = v;
+                }
+            if (lane == 0) {
+#pragma unroll
+                for (int j = 0; j < RW; ++j)
+                    if (rl0 + j < nr) {
+#pragma unroll
+                        for (int g = 0; g < G; ++g)
+                            if (g < ng) a.out[static_cast<int64_t>(slot[g]) * a.nrows + r0 + rl0 + j] = acc[j][g];
+                    }
+            }
+        }
+        __syncthreads();   // ring slot consumed
+        if (a.bulk && threadIdx.x == 0 && st + NS < n_st) issue(st + NS);
+    }
+}
+
+
+template <int WT, int G, int RW, bool DUMP>
+static int launch_gemv_t(const GemvPlan& plan, const GemvArgs& a, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(plan.grid_x), static_cast<unsigned>(plan.row_tiles));
+    const dim3 block(256);
+    if (int st = set_smem_limit(reinterpret_cast<const void*>(moe_gemv_kernel<WT, G, RW, DUMP>),
+                                static_cast<int>(plan.smem)))
+        return st;
+    moe_gemv_kernel<WT, G, RW, DUMP><<<grid, block, plan.smem, s>>>(a);
+    return check_launch(DUMP ? "moe_gemv_kernel<dump>" : "moe_gemv_kernel", grid, block, plan.smem);
+}
+
+template <int WT, int G, bool DUMP>
+static int launch_gemv_rw(const GemvPlan& plan, const GemvArgs& a, cudaStream_t s) {
+    switch (plan.lanes_per_row) {
+        case 4: return launch_gemv_t<WT, G, 4, DUMP>(plan, a, s);
+        case 2: return launch_gemv_t<WT, G, 2, DUMP>(plan, a, s);
+        default: return launch_gemv_t<WT, G, 1, DUMP>(plan, a, s);
+    }
+}
+
+
+// The block-per-lane kernel for a weight type other than Q4_0 (moe_gemv_gguf.cu).
+int launch_gemv_gguf(int wtype, const GemvPlan& plan, const GemvArgs& a, cudaStream_t s);
+
+}  // namespace ft

@@ -86,6 +86,22 @@ typedef enum {
 #define FT_PATH_GEMV 1   /* per-slot GEMV on CUDA cores                                  */
 #define FT_PATH_GEMM 2   /* expert-grouped GEMM on the tcgen05 tensor cores              */
 
+/* Weight block types of ft_moe_gguf_q8_1: the GGUF types whose blocks hold
+ * 32 weights (GGML type numbers).  Weight i of a block = q_i * d + c:
+ *   Q4_0 18 B: fp16 d, 16 B nibbles (weight j<16: low nibble of byte j, j+16:
+ *        its high nibble); q_i = nibble - 8, c = 0
+ *   Q4_1 20 B: fp16 d, fp16 m, 16 B nibbles as Q4_0; q_i = nibble, c = m
+ *   Q5_0 22 B: fp16 d, 4 B qh (little-endian uint32), 16 B nibbles;
+ *        q_i = (nibble_i | (bit i of qh) << 4) - 16, c = 0
+ *   Q5_1 24 B: fp16 d, fp16 m, 4 B qh, 16 B nibbles; q_i = nibble_i |
+ *        (bit i of qh) << 4, c = m
+ *   Q8_0 34 B: fp16 d, 32 int8 q_i, c = 0 */
+#define FT_TYPE_Q4_0 2
+#define FT_TYPE_Q4_1 3
+#define FT_TYPE_Q5_0 6
+#define FT_TYPE_Q5_1 7
+#define FT_TYPE_Q8_0 8
+
 /* Gated activations of ft_act_mul_quantize_q8_1 / ft_moe_ffn_q4_0_q8_1. */
 #define FT_ACT_SILU 0        /* silu(g) = g / (1 + exp(-g))                              */
 #define FT_ACT_GELU_TANH 1   /* g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3)))            */
@@ -220,6 +236,28 @@ FT_API int ft_moe_q4_0_q8_1_ep(const void* weights_local, const void* act, const
                                float* out, int64_t tokens, int32_t top_k, int32_t n_experts_global,
                                int32_t expert_start, int32_t n_experts_local, int64_t nrows,
                                int64_t ncols, void* stream);
+
+/*
+ * ft_moe_gguf_q8_1 - the routed matmul with expert weights of any GGUF type
+ * whose blocks hold 32 weights (FT_TYPE_*; the per-type launchers of
+ * moe_vec.cuh on FreeToken PR #185, "Notes"):
+ *   out[s][r] = sum_b d_w d_a sum_i q_i q_a[i] + c s_a
+ * per weight block b of row r of expert topk_ids[s] and activation block b of
+ * the slot's token, with q_i, c as in the FT_TYPE_* list and s_a the
+ * activation block's stored fp16 s (c = 0 for Q4_0, Q5_0, Q8_0).
+ *
+ *   wtype     FT_TYPE_Q4_0 (exactly ft_moe_q4_0_q8_1), FT_TYPE_Q4_1,
+ *             FT_TYPE_Q5_0, FT_TYPE_Q5_1 or FT_TYPE_Q8_0
+ *   weights   device, [n_experts][nrows][ncols/32] blocks of wtype; 16-byte aligned
+ *   act, topk_ids, out, tokens, top_k, n_experts, nrows, ncols as for
+ *   ft_moe_q4_0_q8_1.
+ * Types other than Q4_0 always take the GEMV path (one weight block per
+ * lane); ft_moe_set_path(FT_PATH_GEMM) makes them fail with FT_ERR_ARG.
+ * Errors as for ft_moe_q4_0_q8_1, plus FT_ERR_ARG for an unknown wtype.
+ */
+FT_API int ft_moe_gguf_q8_1(int32_t wtype, const void* weights, const void* act, const int32_t* topk_ids,
+                            float* out, int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows,
+                            int64_t ncols, void* stream);
 
 /*
  * ft_act_mul_quantize_q8_1 - the step between the two expert layers, fused:

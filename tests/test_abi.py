@@ -163,3 +163,16 @@ def test_activation_and_ffn_reject_bad_arguments(lib):
     assert g(W1, W2, X, I, vp(0), M, O, 4, 2, 8, 256, 128, 0, vp(0)) == 1    # null h
     assert g(W1, W2, X, I, vp(0x50008), M, O, 4, 2, 8, 256, 128, 0, vp(0)) == 3   # h misaligned
     assert g(W1, W2, X, I, Hh, vp(0x60004), O, 4, 2, 8, 256, 128, 0, vp(0)) == 3  # act_mid misaligned
+
+
+def test_gguf_matmul_rejects_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    f = lib.ft_moe_gguf_q8_1
+    W, A, I, O = vp(0x10000), vp(0x20000), vp(0x30000), vp(0x40000)
+    assert f(5, W, A, I, O, 4, 2, 8, 128, 256, vp(0)) == 1       # unknown type
+    assert "weight type" in _err(lib)
+    assert f(0, W, A, I, O, 4, 2, 8, 128, 256, vp(0)) == 1       # unknown type
+    assert f(8, W, A, I, O, 4, 2, 8, 128, 100, vp(0)) == 1       # ncols % 32
+    assert f(3, W, A, I, O, 0, 2, 8, 128, 256, vp(0)) == 0       # no slots: no-op
+    assert f(6, W, A, I, vp(0), 4, 2, 8, 128, 256, vp(0)) == 1   # null out
+    assert f(7, vp(0x10008), A, I, O, 4, 2, 8, 128, 256, vp(0)) == 3   # weights misaligned

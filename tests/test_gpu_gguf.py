@@ -1,0 +1,116 @@
+"""GPU parity of ft_moe_gguf_q8_1: the routed matmul with expert weights of the
+other GGUF types whose blocks hold 32 weights (Q4_1, Q5_0, Q5_1, Q8_0; the
+per-type launchers of moe_vec.cuh on FreeToken PR #185, "Notes").
+
+Against the oracle's matmul of the same type within the matmul tolerance
+(max |err| <= 1e-3 ||w_row|| ||x||, relative L2 <= 1e-4, ||w_row|| of the
+dequantized weight row); Q4_0 through the same entry point bit for bit equal
+to ft_moe_q4_0_q8_1; bad ids; rows not 16-byte aligned; a full-size decode
+step of the 8-expert 14336 x 4096 layer; the shapes the path rejects."""
+
+import numpy as np
+import pytest
+
+import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+TYPES = ["q4_1", "q5_0", "q5_1", "q8_0"]
+
+
+@pytest.fixture(scope="module")
+def ft():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bit_quantized_moe_quantize_gb300 as ft
+    from bit_quantized_moe_quantize_gb300 import build
+    build.build()
+    ft.load()
+    prev = ft.set_path("auto")
+    yield ft
+    ft.set_path(prev)
+
+
+def _case(wtype, E, k, K, N, T, seed, routing="uniform"):
+    from bit_quantized_moe_quantize_gb300 import synth
+    wl = synth.custom_workload(E, k, K, N, seed, routing=routing)
+    return synth.make_weights_gguf(wl, wtype), synth.make_activations(wl, T), synth.make_topk_ids(wl, T)
+
+
+def _check(ft, oracle, wtype, w, x, ids, what):
+    act = oracle.quantize_q8_1(x)
+    ref = oracle.moe_gguf(wtype, w, act, ids)
+    got = G.host(ft.moe_gguf_q8_1(wtype, G.dev(w), G.dev(act), G.dev(ids)))
+    E, N, nb, bb = w.shape
+    wn = np.linalg.norm(oracle.dequantize_gguf(wtype, w.reshape(E * N, nb, bb)), axis=-1).reshape(E, N)
+    xn = G.act_norms(oracle, act)
+    idc = np.clip(ids, 0, E - 1)
+    G.check_close(got, ref, wn[idc], np.broadcast_to(xn[:, None, None], (*ids.shape, N)), what)
+    return got, ref
+
+
+# (E, k, K, N, T): tiny; 3 blocks per row (rows of 60-102 bytes, not 16-byte
+# aligned: 2-byte copies instead of bulk copies); 8-slot tiles; a top-8 decode
+# step with Zipf routing
+CASES = [(8, 2, 256, 128, 16, 90, "uniform"), (5, 2, 96, 50, 77, 91, "uniform"),
+         (8, 2, 512, 256, 1000, 92, "uniform"), (128, 8, 2048, 768, 8, 93, "zipf")]
+
+
+@pytest.mark.parametrize("wtype", TYPES)
+@pytest.mark.parametrize("E,k,K,N,T,seed,routing", CASES)
+def test_gguf_matches_oracle(ft, oracle, wtype, E, k, K, N, T, seed, routing):
+    w, x, ids = _case(wtype, E, k, K, N, T, seed, routing)
+    _check(ft, oracle, wtype, w, x, ids, f"{wtype} {E},{k},{K},{N},{T}")
+
+
+@pytest.mark.parametrize("wtype", TYPES)
+def test_gguf_full_size_decode(ft, oracle, wtype):
+    """One token of the 8-expert top-2 layer with 14336 rows of 4096 columns,
+    every output against the oracle."""
+    w, x, ids = _case(wtype, 8, 2, 4096, 14336, 1, 94)
+    _check(ft, oracle, wtype, w, x, ids, f"{wtype} full-size decode")
+
+
+def test_gguf_q4_0_is_the_q4_0_entry(ft, oracle):
+    import torch
+    from bit_quantized_moe_quantize_gb300 import synth
+    wl = synth.custom_workload(8, 2, 512, 256, 95)
+    w, x, ids = synth.make_weights(wl), synth.make_activations(wl, 300), synth.make_topk_ids(wl, 300)
+    act = G.dev(oracle.quantize_q8_1(x))
+    dw, di = G.dev(w), G.dev(ids)
+    a = ft.moe_gguf_q8_1("q4_0", dw, act, di)
+    b = ft.moe_q4_0_q8_1(dw, act, di)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("wtype", ["q5_1", "q8_0"])
+def test_gguf_bad_ids_zero_rows(ft, oracle, wtype):
+    w, x, ids = _case(wtype, 8, 2, 256, 128, 40, 96)
+    ids = ids.copy()
+    ids[2, 0] = -3
+    ids[9, 1] = 8
+    ft.read_device_error()
+    got, ref = _check(ft, oracle, wtype, w, x, ids, f"{wtype} bad ids")
+    assert not got[2, 0].any() and not got[9, 1].any()
+    assert ft.read_device_error() & ft.FT_DEVERR_BAD_EXPERT_ID
+
+
+def test_gguf_rejects_what_the_path_cannot_run(ft, oracle):
+    import torch
+    w, x, ids = _case("q8_0", 8, 2, 256, 128, 4, 97)
+    act = G.dev(oracle.quantize_q8_1(x))
+    dw, di = G.dev(w), G.dev(ids)
+    prev = ft.set_path("gemm")
+    try:
+        with pytest.raises(ft.FtError, match="Q4_0 weights only"):
+            ft.moe_gguf_q8_1("q8_0", dw, act, di)
+    finally:
+        ft.set_path(prev)
+    # rows of 32768 Q8_0 columns: one ring stage of 8 rows does not fit in shared memory
+    big = torch.zeros((2, 8, 1024, 34), dtype=torch.uint8, device="cuda")
+    xb = torch.zeros((1, 1024, 36), dtype=torch.uint8, device="cuda")
+    ib = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    with pytest.raises(ft.FtError, match="shared memory"):
+        ft.moe_gguf_q8_1("q8_0", big, xb, ib)

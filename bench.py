@@ -49,9 +49,8 @@ PAGES_T4_TOKENS_PER_S = {("prefill", 8191): 8191 / 0.7058, ("prefill", 4096): 40
 # capture (profiles/moe_gemm_tc_prefill.md), keyed by a hash of the sources that
 # kernel is built from, so a changed kernel reports null instead.
 GEMM_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemm_tc.cu", "bit_quantized_moe_quantize_gb300/csrc/gemm_common.cuh",
-                "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh", "bit_quantized_moe_quantize_gb300/csrc/ft_internal.h",
-                "include/ft_moe.h")
-NCU_TRAFFIC = {("moe_gemm_tc_kernel", "a5ed6a8ab5bf58e6", "prefill:8191"): 666685184 + 341326592}
+                "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh", "bit_quantized_moe_quantize_gb300/csrc/ft_internal.h")
+NCU_TRAFFIC = {("moe_gemm_tc_kernel", "5966128ff74c2e7f", "prefill:8191"): 666817280 + 340600320}
 
 
 def kernel_source_hash(files) -> str:

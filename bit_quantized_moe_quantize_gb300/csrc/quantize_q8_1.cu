@@ -15,7 +15,7 @@
 //
 // Bit-exactness: amax is exact, d = amax / 127 is an IEEE fp32 division
 // (__fdiv_rn), q = roundf(x / d) with the quotient of an IEEE division (see
-// q8_code), s = d * sum(q) is one fp32 multiply, and both are rounded to fp16
+// q8_codes), s = d * sum(q) is one fp32 multiply, and both are rounded to fp16
 // with __float2half_rn.
 #include <cuda_fp16.h>
 
@@ -24,22 +24,50 @@
 
 namespace ft {
 
-// round(v / d) clamped to [-127, 127], exactly as the IEEE quotient rounds:
-// v * rcp(d) lies within 2^-23 |v / d| (<= 1.6e-5 for |v / d| <= 127.5) of
-// v / d, whose fp32 rounding moves it by at most 4e-6 more, so both round to
-// the same integer unless v * rcp(d) is within 4e-5 of a half integer; those
-// take the division.  rcp(d) is finite for d >= 1e-36 (else always divide).
-__device__ __forceinline__ int q8_code(float v, float d, float rd, bool fast) {
-    float y = fast ? __fmul_rn(v, rd) : __fdiv_rn(v, d);
-    const float t = fabsf(y);
-    if (fast && fabsf((t - truncf(t)) - 0.5f) < 4.0e-5f) y = __fdiv_rn(v, d);
-    return min(127, max(-127, static_cast<int>(roundf(y))));
+// Codes of N values of one block: round(v / d) clamped to [-127, 127],
+// exactly as the IEEE quotient rounds.  v * rcp(d) lies within
+// 2^-23 |v / d| (<= 1.6e-5 for |v / d| <= 127.5) of v / d, whose fp32
+// rounding moves it by at most 4e-6 more, so both round to the same integer
+// unless v * rcp(d) is within 4e-5 of a half integer.  All N values go
+// through the reciprocal; only if one of them lands that near a tie (or
+// d < 1e-36, where rcp(d) may overflow) do those take the division: one
+// rarely taken branch per N values.  amax == 0 gives all-zero codes.
+template <int N>
+__device__ __forceinline__ void q8_codes(const float (&v)[N], float amax, float d, int (&q)[N]) {
+    const bool fast = d >= 1.0e-36f;
+    const float rd = __frcp_rn(d);
+    float y[N];
+    bool slow = !fast;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        y[j] = __fmul_rn(v[j], rd);
+        const float t = fabsf(y[j]);
+        slow |= fabsf((t - truncf(t)) - 0.5f) < 4.0e-5f;
+    }
+    if (slow) {
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            const float t = fabsf(y[j]);
+            if (!fast || fabsf((t - truncf(t)) - 0.5f) < 4.0e-5f) y[j] = __fdiv_rn(v[j], d);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+        q[j] = amax != 0.0f ? min(127, max(-127, static_cast<int>(roundf(y[j])))) : 0;
 }
 
 __device__ __forceinline__ uint32_t q8_header(float d, int sum) {
     const __half hd = __float2half_rn(d);
     const __half hs = __float2half_rn(__fmul_rn(d, static_cast<float>(sum)));
     return static_cast<uint32_t>(__half_as_ushort(hd)) | (static_cast<uint32_t>(__half_as_ushort(hs)) << 16);
+}
+
+// value i (0..31) of a block held as four 16-byte words of fp16
+__device__ __forceinline__ float half_of(const uint4 (&raw)[4], int i) {
+    const uint4 r = raw[i >> 3];
+    const uint32_t w = (i & 6) == 0 ? r.x : (i & 6) == 2 ? r.y : (i & 6) == 4 ? r.z : r.w;
+    const __half2 h = *reinterpret_cast<const __half2*>(&w);
+    return (i & 1) ? __high2float(h) : __low2float(h);
 }
 
 __global__ void __launch_bounds__(256) quantize_q8_1_block_kernel(const uint4* __restrict__ x,
@@ -49,32 +77,48 @@ __global__ void __launch_bounds__(256) quantize_q8_1_block_kernel(const uint4* _
         uint4 raw[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) raw[c] = __ldg(x + blk * 4 + c);
-        float v[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint32_t w[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
-                v[8 * c + 2 * i] = __low2float(h);
-                v[8 * c + 2 * i + 1] = __high2float(h);
-            }
-        }
         float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(half_of(raw, i)));
         const float d = __fdiv_rn(amax, 127.0f);
+        // q8_codes, written out over the raw halves (no 32-value array): the
+        // codes from the reciprocal first; if any value lands near a tie (or
+        // d < 1e-36), the block is redone with the division for those values
         const bool fast = d >= 1.0e-36f;
-        const float rd = fast ? __frcp_rn(d) : 0.0f;
+        const float rd = __frcp_rn(d);
         uint32_t packed[8];
+        int sum = 0;
+        bool slow = !fast;
 #pragma unroll
         for (int i = 0; i < 8; ++i) packed[i] = 0;
-        int sum = 0;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            const int qi = amax != 0.0f ? q8_code(v[i], d, rd, fast) : 0;
+            const float y = __fmul_rn(half_of(raw, i), rd);
+            const float t = fabsf(y);
+            slow |= fabsf((t - truncf(t)) - 0.5f) < 4.0e-5f;
+            const int qi = amax != 0.0f ? min(127, max(-127, static_cast<int>(roundf(y)))) : 0;
             sum += qi;
             packed[i >> 2] |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * (i & 3));
+        }
+        if (slow) {
+            // reloaded (from L1 / L2) rather than kept: holding the 32 values
+            // across the common path would double the registers
+            uint4 raw2[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) raw2[c] = __ldg(x + blk * 4 + c);
+            sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) packed[i] = 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float v = half_of(raw2, i);
+                float y = __fmul_rn(v, rd);
+                const float t = fabsf(y);
+                if (!fast || fabsf((t - truncf(t)) - 0.5f) < 4.0e-5f) y = __fdiv_rn(v, d);
+                const int qi = amax != 0.0f ? min(127, max(-127, static_cast<int>(roundf(y)))) : 0;
+                sum += qi;
+                packed[i >> 2] |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * (i & 3));
+            }
         }
         uint32_t* ob = out + blk * (Q8_1_BYTES / 4);
         ob[0] = q8_header(d, sum);
@@ -100,15 +144,14 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const uint2* __restr
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(group_mask, amax, o));
         const float d = __fdiv_rn(amax, 127.0f);
-        const bool fast = d >= 1.0e-36f;
-        const float rd = fast ? __frcp_rn(d) : 0.0f;
+        int q[4];
+        q8_codes<4>(v, amax, d, q);
         uint32_t packed = 0;
         int sum = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int qi = amax != 0.0f ? q8_code(v[j], d, rd, fast) : 0;
-            sum += qi;
-            packed |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * j);
+            sum += q[j];
+            packed |= (static_cast<uint32_t>(q[j]) & 0xFFu) << (8 * j);
         }
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(group_mask, sum, o);
@@ -152,10 +195,12 @@ int launch_quantize_q8_1(const void* x, void* act, int64_t tokens, int64_t ncols
 // Both activations are g * sigmoid(z) in fp32: z = g for SiLU, and
 // z = 2 sqrt(2/pi) (g + 0.044715 g^3) for the tanh form of GELU, since
 // (1 + tanh(y)) / 2 = 1 / (1 + exp(-2 y)); the sigmoid form has no
-// cancellation where tanh(y) approaches -1.  expf is CUDA's accurate
-// exponential; the result is within a few fp32 ulps of the exact activation,
-// so the Q8_1 codes equal those of the exactly computed a except where
-// a / d falls within that distance of a rounding boundary.
+// cancellation where tanh(y) approaches -1.  The exponential and the
+// division are the fast hardware forms (__expf, __fdividef): relative error
+// about 1e-6 for |z| <= 20, so a code can differ from that of the exactly
+// computed a only where a / d lies within ~1e-4 of a rounding boundary, and
+// where the exact a is below 2^-126 |g| (exp(-z) past 2^126) the result is 0,
+// in blocks whose fp16 scale is 0 anyway or whose codes there are 0.
 //
 // HBM-bound: 8 bytes read and 1.125 bytes written per output value.  Eight
 // lanes own one block (four gate and four up values each, one 16-byte load
@@ -166,7 +211,7 @@ constexpr int kActUnroll = 1;
 
 __device__ __forceinline__ float act_mul(float g, float up, int kind) {
     const float z = kind == FT_ACT_SILU ? g : 1.5957691216057308f * fmaf(0.044715f * g, g * g, g);
-    return g * __frcp_rn(1.0f + expf(-z)) * up;
+    return __fdividef(g, 1.0f + __expf(-z)) * up;
 }
 
 __global__ void __launch_bounds__(256) act_mul_quantize_q8_1_kernel(const float4* __restrict__ h,
@@ -207,15 +252,14 @@ __global__ void __launch_bounds__(256) act_mul_quantize_q8_1_kernel(const float4
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(group_mask, amax, o));
         const float d = __fdiv_rn(amax, 127.0f);
-        const bool fast = d >= 1.0e-36f;
-        const float rd = fast ? __frcp_rn(d) : 0.0f;
+        int q[4];
+        q8_codes<4>(v, amax, d, q);
         uint32_t packed = 0;
         int sum = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int qi = amax != 0.0f ? q8_code(v[j], d, rd, fast) : 0;
-            sum += qi;
-            packed |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * j);
+            sum += q[j];
+            packed |= (static_cast<uint32_t>(q[j]) & 0xFFu) << (8 * j);
         }
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(group_mask, sum, o);

@@ -74,7 +74,9 @@ _S_WEIGHTS, _S_ACT, _S_ROUTE, _S_OUTLIER, _S_RANK, _S_GGUF = 0, 1, 2, 3, 4, 5
 # the other GGUF weight types with 32-weight blocks: bytes per block, offset of
 # the code bytes, whether the block stores an fp16 m after d, GGML type number
 GGUF_TYPES = {"q4_0": (18, 2, False, 2), "q4_1": (20, 4, True, 3), "q5_0": (22, 2, False, 6),
-              "q5_1": (24, 4, True, 7), "q8_0": (34, 2, False, 8)}
+              "q5_1": (24, 4, True, 7), "q8_0": (34, 2, False, 8),
+              "q4_k": (144, 4, False, 12), "q5_k": (176, 4, False, 13)}
+KQUANTS = ("q4_k", "q5_k")     # 256 weights per (super-)block; the others hold 32
 
 
 def _rng(seed: int, stream: int, *extra: int) -> np.random.Generator:
@@ -120,20 +122,23 @@ def make_weights(wl: Workload, chunk_rows: int = 1 << 16) -> np.ndarray:
 
 
 def make_weights_gguf(wl: Workload, wtype: str, chunk_rows: int = 1 << 16) -> np.ndarray:
-    """Expert weights as random valid blocks of a GGUF type, uint8 [E, N, K/32, bytes].
+    """Expert weights as random valid blocks of a GGUF type, uint8
+    [E, N, K/32, bytes] (K/256 super-blocks for the K-quants).
 
     Q4_0 goes through make_weights.  For the others every code byte (nibbles,
-    5th-bit words, int8 codes) is uniform random, d = fp16(0.0005 + 0.002 |z|)
-    and, for the types with an offset, m = fp16(-d * L / 2 * (1 + 0.1 z'))
-    with L the number of levels, so that the weights centre near zero like
-    trained ones.  Random bytes are valid blocks of these formats; no weight
-    quantization is involved.
+    5th-bit words, int8 codes, packed 6-bit sub-block scales and mins) is
+    uniform random, d = fp16(0.0005 + 0.002 |z|) and, for the types with an
+    offset, m = fp16(-d * L / 2 * (1 + 0.1 z')) with L the number of levels,
+    so that the weights centre near zero like trained ones; the K-quants take
+    0.05 of that d and dmin = fp16(d L / 2 |1 + 0.1 z'|) (the 6-bit sub-block
+    scale and min multiply both).  Random bytes are valid blocks
+    of these formats; no weight quantization is involved.
     """
     if wtype == "q4_0":
         return make_weights(wl, chunk_rows)
     bb, code0, has_m, tid = GGUF_TYPES[wtype]
     E, N, K = wl.n_experts, wl.nrows, wl.ncols
-    nb = K // QK
+    nb = K // (256 if wtype in KQUANTS else QK)
     out = np.empty((E * N, nb, bb), dtype=np.uint8)
     rng = _rng(wl.seed, _S_GGUF, tid)
     levels = {"q4_1": 16, "q5_1": 32}.get(wtype, 0)
@@ -141,6 +146,11 @@ def make_weights_gguf(wl: Workload, wtype: str, chunk_rows: int = 1 << 16) -> np
         r1 = min(E * N, r0 + chunk_rows)
         n = r1 - r0
         d = (np.float32(0.0005) + np.float32(0.002) * np.abs(rng.standard_normal((n, nb), dtype=np.float32)))
+        if wtype in KQUANTS:      # super-block scales of the 6-bit sub-block scales and mins
+            d = d * np.float32(0.05)
+            half_levels = np.float32(8 if wtype == "q4_k" else 16)
+            dmin = d * half_levels * np.abs(np.float32(1) + np.float32(0.1) * rng.standard_normal((n, nb), dtype=np.float32))
+            out[r0:r1, :, 2:4] = dmin.astype(np.float16).view(np.uint8).reshape(n, nb, 2)
         out[r0:r1, :, 0:2] = d.astype(np.float16).view(np.uint8).reshape(n, nb, 2)
         if has_m:
             z = rng.standard_normal((n, nb), dtype=np.float32)

@@ -127,7 +127,8 @@ class Oracle:
         return out.reshape(*blocks.shape[:-2], blocks.shape[-2] * QK)
 
     # other GGUF weight types -----------------------------------------
-    GGUF = {"q4_0": 2, "q4_1": 3, "q5_0": 6, "q5_1": 7, "q8_0": 8}
+    GGUF = {"q4_0": 2, "q4_1": 3, "q5_0": 6, "q5_1": 7, "q8_0": 8, "q4_k": 12, "q5_k": 13}
+    KQUANTS = (12, 13)
 
     def gguf_block_bytes(self, wtype) -> int:
         return int(self.lib.oracle_gguf_block_bytes(self.GGUF.get(wtype, wtype)))
@@ -138,9 +139,10 @@ class Oracle:
         blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
         assert blocks.shape[-1] == bb
         nb = blocks.size // bb
-        out = np.empty(nb * QK, dtype=np.float64)
+        per = 256 if t in self.KQUANTS else QK
+        out = np.empty(nb * per, dtype=np.float64)
         self.lib.oracle_dequantize_gguf(t, _p(blocks), nb, _p(out))
-        return out.reshape(*blocks.shape[:-2], blocks.shape[-2] * QK)
+        return out.reshape(*blocks.shape[:-2], blocks.shape[-2] * per)
 
     def gguf_block_dot(self, wtype, w_block: np.ndarray, a_block: np.ndarray) -> int:
         t = self.GGUF.get(wtype, wtype)
@@ -157,10 +159,11 @@ class Oracle:
         ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
         E, N, nb, bb = w.shape
         assert bb == self.gguf_block_bytes(t)
+        per = 256 if t in self.KQUANTS else QK
         T, k = ids.shape
-        assert a.shape == (T, nb, Q8_1_BYTES)
+        assert a.shape == (T, nb * per // QK, Q8_1_BYTES)
         out = np.empty((T, k, N), dtype=np.float32)
-        self.lib.oracle_moe_gguf_q8_1(t, _p(w), _p(a), _p(ids), _p(out), T, k, E, N, nb * QK)
+        self.lib.oracle_moe_gguf_q8_1(t, _p(w), _p(a), _p(ids), _p(out), T, k, E, N, nb * per)
         return out
 
     # gated activation ------------------------------------------------

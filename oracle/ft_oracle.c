@@ -196,7 +196,9 @@ void oracle_dequantize_q8_1(const uint8_t* blocks, int64_t n_blocks, double* out
  * block's contribution is
  *     d * d_a * sum_i q_i * q_a[i]  +  c * d_a * sum_i q_a[i],
  * and the second term takes d_a * sum(q_a) as the activation block's stored
- * fp16 s (the quantity Q8_1 stores s for). */
+ * fp16 s (the quantity Q8_1 stores s for).  The K-quants (below) are written
+ * as w = d sc q - dmin m per 32-weight sub-block; their min term is taken with
+ * the exact d_a * sum(q_a). */
 int32_t oracle_gguf_block_bytes(int32_t type)
 {
     switch (type) {
@@ -205,6 +207,8 @@ int32_t oracle_gguf_block_bytes(int32_t type)
         case ORACLE_GGUF_Q5_0: return 22;
         case ORACLE_GGUF_Q5_1: return 24;
         case ORACLE_GGUF_Q8_0: return 34;
+        case ORACLE_GGUF_Q4_K: return 144;
+        case ORACLE_GGUF_Q5_K: return 176;
         default: return 0;
     }
 }
@@ -243,9 +247,57 @@ static double gguf_offset(const uint8_t* blk, int32_t type)
     return 0.0;
 }
 
+/* K-quant super-blocks (Q4_K 144 B, Q5_K 176 B) hold 256 weights as eight
+ * sub-blocks of 32: fp16 d, fp16 dmin, 12 bytes of packed 6-bit scale/min
+ * pairs, then (Q5_K only) 32 bytes qh of 5th bits, then 128 bytes of
+ * nibbles.  Sub-block j uses nibble byte 32 * (j / 2) + l, its low nibble for
+ * even j and its high nibble for odd j, and (Q5_K) bit j of qh[l] as the 5th
+ * bit; weight l = d * sc_j * q_l - dmin * m_j.  The pair (sc_j, m_j): for
+ * j < 4 the low 6 bits of bytes j and j + 4; for j >= 4 the low nibble of byte
+ * j + 4 with the top two bits of byte j - 4 above it, and the high nibble of
+ * byte j + 4 with the top two bits of byte j above it. */
+static int is_kquant(int32_t type) { return type == ORACLE_GGUF_Q4_K || type == ORACLE_GGUF_Q5_K; }
+
+static void kquant_scale_min(const uint8_t* sc12, int j, int* sc, int* m)
+{
+    if (j < 4) {
+        *sc = sc12[j] & 63;
+        *m = sc12[j + 4] & 63;
+    } else {
+        *sc = (sc12[j + 4] & 0x0f) | ((sc12[j - 4] >> 6) << 4);
+        *m = (sc12[j + 4] >> 4) | ((sc12[j] >> 6) << 4);
+    }
+}
+
+/* Sub-block j of a K-quant super-block: its 32 levels, d * sc_j and dmin * m_j. */
+static void kquant_sub(const uint8_t* sb, int32_t type, int j, int* lev, double* dsc, double* dmn)
+{
+    int sc, m;
+    kquant_scale_min(sb + 4, j, &sc, &m);
+    *dsc = oracle_half_to_double(rd16(sb)) * sc;
+    *dmn = oracle_half_to_double(rd16(sb + 2)) * m;
+    const uint8_t* qs = sb + (type == ORACLE_GGUF_Q5_K ? 48 : 16) + 32 * (j / 2);
+    for (int l = 0; l < QK; ++l) {
+        lev[l] = (j % 2 == 0) ? (qs[l] & 0x0f) : (qs[l] >> 4);
+        if (type == ORACLE_GGUF_Q5_K)
+            lev[l] |= ((sb[16 + l] >> j) & 1) << 4;
+    }
+}
+
 void oracle_dequantize_gguf(int32_t type, const uint8_t* blocks, int64_t n_blocks, double* out)
 {
     const int32_t bytes = oracle_gguf_block_bytes(type);
+    if (is_kquant(type)) {
+        for (int64_t b = 0; b < n_blocks; ++b)
+            for (int j = 0; j < 8; ++j) {
+                int lev[QK];
+                double dsc, dmn;
+                kquant_sub(blocks + b * bytes, type, j, lev, &dsc, &dmn);
+                for (int l = 0; l < QK; ++l)
+                    out[b * 256 + j * QK + l] = dsc * lev[l] - dmn;
+            }
+        return;
+    }
     for (int64_t b = 0; b < n_blocks; ++b) {
         const uint8_t* blk = blocks + b * bytes;
         double d = oracle_half_to_double(rd16(blk));
@@ -275,7 +327,24 @@ void oracle_moe_gguf_q8_1(int32_t type, const uint8_t* weights, const uint8_t* a
         const int64_t t = s / top_k;
         for (int64_t r = 0; r < nrows; ++r) {
             double y = 0.0;
-            if (e >= 0 && e < n_experts) {
+            if (e >= 0 && e < n_experts && is_kquant(type)) {
+                /* sub-block b of the row = sub-block b % 8 of super-block b / 8:
+                 * d sc d_a sum(q q_a) - dmin m d_a sum(q_a), the exact sum of q_a */
+                const uint8_t* row = weights + ((int64_t)e * nrows + r) * (nb / 8) * bytes;
+                for (int64_t b = 0; b < nb; ++b) {
+                    int lev[QK];
+                    double dsc, dmn;
+                    kquant_sub(row + (b / 8) * bytes, type, (int)(b % 8), lev, &dsc, &dmn);
+                    const uint8_t* ab = act + (t * nb + b) * Q8_1_BYTES;
+                    const double da = oracle_half_to_double(rd16(ab));
+                    int32_t dot = 0, suma = 0;
+                    for (int l = 0; l < QK; ++l) {
+                        dot += lev[l] * (int32_t)(int8_t)ab[4 + l];
+                        suma += (int32_t)(int8_t)ab[4 + l];
+                    }
+                    y += dsc * da * (double)dot - dmn * da * (double)suma;
+                }
+            } else if (e >= 0 && e < n_experts) {
                 for (int64_t b = 0; b < nb; ++b) {
                     const uint8_t* wb = weights + (((int64_t)e * nrows + r) * nb + b) * bytes;
                     const uint8_t* ab = act + (t * nb + b) * Q8_1_BYTES;

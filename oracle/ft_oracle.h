@@ -54,6 +54,11 @@
  *   Q5_1 24 B: fp16 d, fp16 m, 4 B qh, 16 B qs; q_i = nibble_i | (bit i) << 4;
  *       c = m
  *   Q8_0 34 B: fp16 d, 32 int8 q; c = 0
+ * K-quants, 256 weights per super-block, eight sub-blocks of 32 (weight l of
+ * sub-block j = d * sc_j * q_l - dmin * m_j, 6-bit sc_j and m_j):
+ *   Q4_K 144 B: fp16 d, fp16 dmin, 12 B scales/mins, 128 B nibbles
+ *   Q5_K 176 B: fp16 d, fp16 dmin, 12 B scales/mins, 32 B qh, 128 B nibbles
+ *   (oracle_dequantize_gguf counts super-blocks for these; ncols % 256 == 0)
  *   weights [E][N][K/32] blocks of the type.
  */
 #ifndef FT_ORACLE_H
@@ -80,6 +85,8 @@ void oracle_dequantize_q8_1(const uint8_t* blocks, int64_t n_blocks, double* out
 #define ORACLE_GGUF_Q5_0 6
 #define ORACLE_GGUF_Q5_1 7
 #define ORACLE_GGUF_Q8_0 8
+#define ORACLE_GGUF_Q4_K 12
+#define ORACLE_GGUF_Q5_K 13
 int32_t oracle_gguf_block_bytes(int32_t type);
 void oracle_dequantize_gguf(int32_t type, const uint8_t* blocks, int64_t n_blocks, double* out);
 int32_t oracle_gguf_block_dot(int32_t type, const uint8_t* w_block, const uint8_t* a_block);

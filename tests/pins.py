@@ -612,6 +612,109 @@ def pin_gguf_q4_0_is_the_q4_0_matmul(o):
     assert np.array_equal(o.moe_gguf("q4_0", w, act, ids), o.moe(w, act, ids))
 
 
+# -------------------------------------------------------------- K-quants
+def numpy_decode_kquant(wtype, w):
+    """Independent vectorised decode of Q4_K / Q5_K super-blocks [..., nsb, bytes]
+    -> fp64 [..., nsb * 256]."""
+    w = np.ascontiguousarray(w)
+    d = w[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    dmin = w[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
+    sc12 = w[..., 4:16].astype(np.int64)
+    lo_sc, lo_m = sc12[..., 0:4] & 63, sc12[..., 4:8] & 63
+    hi_sc = (sc12[..., 8:12] & 15) | ((sc12[..., 0:4] >> 6) << 4)
+    hi_m = (sc12[..., 8:12] >> 4) | ((sc12[..., 4:8] >> 6) << 4)
+    sc = np.concatenate([lo_sc, hi_sc], axis=-1)                 # [..., 8]
+    m = np.concatenate([lo_m, hi_m], axis=-1)
+    q0 = 48 if wtype == "q5_k" else 16
+    qs = w[..., q0:q0 + 128].astype(np.int64).reshape(*w.shape[:-1], 4, 32)
+    lev = np.stack([qs & 15, qs >> 4], axis=-2).reshape(*w.shape[:-1], 8, 32)   # sub-block j = 2 c + half
+    if wtype == "q5_k":
+        qh = w[..., 16:48].astype(np.int64)                       # [..., 32]
+        bits = (qh[..., None, :] >> np.arange(8)[:, None]) & 1    # [..., 8, 32]
+        lev = lev | (bits << 4)
+    vals = d[..., None, None] * sc[..., None] * lev - (dmin[..., None] * m)[..., None]
+    return vals.reshape(*w.shape[:-2], w.shape[-2] * 256)
+
+
+def _kq_scales_bytes(sc, m):
+    """Pack eight 6-bit (scale, min) pairs by hand into the 12 scale bytes."""
+    b = [0] * 12
+    for j in range(4):
+        b[j] = (sc[j] & 63) | ((sc[j + 4] >> 4) << 6)
+        b[j + 4] = (m[j] & 63) | ((m[j + 4] >> 4) << 6)
+        b[j + 8] = (sc[j + 4] & 15) | ((m[j + 4] & 15) << 4)
+    return b
+
+
+def pin_kquant_hand(o):
+    """A hand-packed Q4_K and Q5_K super-block: every sub-block's scale and min
+    (the low four through byte j, the high four split over nibbles and top bits),
+    nibble halves and 5th bits."""
+    sc = [1, 2, 3, 4, 33, 34, 35, 50]
+    m = [5, 6, 7, 8, 17, 18, 40, 63]
+    for wtype, size in (("q4_k", 144), ("q5_k", 176)):
+        b = np.zeros(size, np.uint8)
+        b[0:2] = [0x00, 0x3C]                 # d = 1
+        b[2:4] = [0x00, 0x38]                 # dmin = 0.5
+        b[4:16] = _kq_scales_bytes(sc, m)
+        q0 = 48 if wtype == "q5_k" else 16
+        lev_lo = np.arange(32) % 16
+        lev_hi = (np.arange(32) * 7) % 16
+        for c in range(4):
+            b[q0 + 32 * c:q0 + 32 * c + 32] = lev_lo | (lev_hi << 4)
+        if wtype == "q5_k":
+            b[16:48] = 0b10100101             # 5th bit set in sub-blocks 0, 2, 5, 7
+        got = o.dequantize_gguf(wtype, b[None]).reshape(8, 32)
+        for j in range(8):
+            lev = (lev_lo if j % 2 == 0 else lev_hi).copy()
+            if wtype == "q5_k" and j in (0, 2, 5, 7):
+                lev += 16
+            assert np.array_equal(got[j], 1.0 * sc[j] * lev - 0.5 * m[j]), (wtype, j)
+
+
+def pin_kquant_numpy_decode(o):
+    for wtype in ("q4_k", "q5_k"):
+        w = _gguf_random(wtype, K=512, seed=6)
+        assert np.array_equal(o.dequantize_gguf(wtype, w), numpy_decode_kquant(wtype, w)), wtype
+
+
+def pin_kquant_moe_numpy(o):
+    """Each K-quant matmul against the plain dequantized dot in fp64 (its min
+    term uses the exact d_a * sum(q_a), so the two agree to rounding)."""
+    rng = np.random.default_rng(8)
+    E, k, K, N, T = 3, 2, 512, 5, 4
+    act = o.quantize_q8_1(rng.standard_normal((T, K)).astype(np.float16))
+    ids = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    xa = numpy_decode_q8_1(act)
+    for wtype in ("q4_k", "q5_k"):
+        w = _gguf_random(wtype, E=E, N=N, K=K, seed=9)
+        wv = numpy_decode_kquant(wtype, w).reshape(E, N, K)
+        got = o.moe_gguf(wtype, w, act, ids).astype(np.float64)
+        for t in range(T):
+            for j in range(k):
+                want = wv[ids[t, j]] @ xa[t]
+                scale = np.abs(wv[ids[t, j]]) @ np.abs(xa[t])
+                assert np.all(np.abs(got[t, j] - want) <= 1e-6 * scale + 1e-12), wtype
+
+
+def pin_kquant_unit_scales_are_q4_1(o):
+    """A Q4_K super-block whose sub-block scales and mins are all 1 holds eight
+    Q4_1 blocks with d' = d and m' = -dmin (nibbles re-laid in Q4_1 order)."""
+    rng = np.random.default_rng(10)
+    b = np.zeros(144, np.uint8)
+    b[0:2] = np.array([0.0625], np.float16).view(np.uint8)
+    b[2:4] = np.array([0.375], np.float16).view(np.uint8)
+    b[4:16] = _kq_scales_bytes([1] * 8, [1] * 8)
+    b[16:] = rng.integers(0, 256, 128, dtype=np.uint8)
+    q41 = np.zeros((8, 20), np.uint8)
+    for j in range(8):
+        lev = (b[16 + 32 * (j // 2):16 + 32 * (j // 2) + 32] >> (4 * (j % 2))) & 15
+        q41[j, 0:2] = b[0:2]
+        q41[j, 2:4] = np.array([-0.375], np.float16).view(np.uint8)
+        q41[j, 4:] = lev[:16] | (lev[16:] << 4)
+    assert np.array_equal(o.dequantize_gguf("q4_k", b[None]), o.dequantize_gguf("q4_1", q41))
+
+
 ALL_PINS = [
     pin_fp16, pin_q4_0_hand, pin_q4_0_nearest_level, pin_q4_0_matches_generator, pin_q4_0_dequant,
     pin_q8_1_hand, pin_q8_1_numpy, pin_q8_1_error_bound, pin_route, pin_block_dot_hand,
@@ -619,5 +722,6 @@ ALL_PINS = [
     pin_moe_split_invariance, pin_moe_bad_ids, pin_moe_slots_numpy_einsum, pin_moe_slots_replicated_rows,
     pin_moe_ep_shards_sum_to_full, pin_act_library, pin_act_tail_accuracy, pin_act_gelu_vs_erf, pin_act_odd_identity, pin_act_hand,
     pin_act_quantize_numpy, pin_gguf_hand, pin_gguf_numpy_decode, pin_gguf_moe_numpy,
-    pin_gguf_q4_0_is_the_q4_0_matmul,
+    pin_gguf_q4_0_is_the_q4_0_matmul, pin_kquant_hand, pin_kquant_numpy_decode, pin_kquant_moe_numpy,
+    pin_kquant_unit_scales_are_q4_1,
 ]

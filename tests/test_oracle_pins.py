@@ -64,6 +64,12 @@ MUTANTS = {
     "q4_1_m_read_as_d": ("return oracle_half_to_double(rd16(blk + 2));", "return oracle_half_to_double(rd16(blk));"),
     "q4_1_nibble_order": ("return i < 16 ? (blk[4 + i] & 0x0f) : (blk[4 + i - 16] >> 4);",
                           "return i < 16 ? (blk[4 + i] >> 4) : (blk[4 + i - 16] & 0x0f);"),
+    "kquant_scale_high_bits": ("*sc = (sc12[j + 4] & 0x0f) | ((sc12[j - 4] >> 6) << 4);",
+                               "*sc = (sc12[j + 4] & 0x0f) | ((sc12[j] >> 6) << 4);"),
+    "kquant_min_sign": ("- dmn * da * (double)suma;", "+ dmn * da * (double)suma;"),
+    "kquant_nibble_half": ("lev[l] = (j % 2 == 0) ? (qs[l] & 0x0f) : (qs[l] >> 4);",
+                           "lev[l] = (j % 2 == 0) ? (qs[l] >> 4) : (qs[l] & 0x0f);"),
+    "q5k_bit_index": ("lev[l] |= ((sb[16 + l] >> j) & 1) << 4;", "lev[l] |= ((sb[16 + l] >> (j / 2)) & 1) << 4;"),
     "bad_id_not_zeroed": ("    if (e < 0 || e >= n_experts)\n        return 0.0;\n",
                           "    if (e < 0 || e >= n_experts)\n        e = 0;\n"),
 }

@@ -211,21 +211,23 @@ def moe_q4_0_q8_1_ep(weights_local, act, topk_ids, n_experts_global, expert_star
     return out
 
 
-# GGUF weight types with 32-weight blocks: GGML type number, bytes per block
-WEIGHT_TYPES = {"q4_0": (2, 18), "q4_1": (3, 20), "q5_0": (6, 22), "q5_1": (7, 24), "q8_0": (8, 34)}
+# GGUF weight types: GGML type number, bytes per stored block, weights per block
+WEIGHT_TYPES = {"q4_0": (2, 18, 32), "q4_1": (3, 20, 32), "q5_0": (6, 22, 32), "q5_1": (7, 24, 32),
+                "q8_0": (8, 34, 32), "q4_k": (12, 144, 256), "q5_k": (13, 176, 256)}
 
 
 def moe_gguf_q8_1(wtype, weights, act, topk_ids, out=None):
-    """Routed matmul with weights of a 32-weight GGUF type (ft_moe_gguf_q8_1):
-    weights uint8 [E, N, K/32, bytes of the type] x Q8_1 [T, K/32, 36] -> fp32 [T, k, N]."""
+    """Routed matmul with weights of a GGUF type (ft_moe_gguf_q8_1): weights uint8
+    [E, N, K/32 (K/256 for the K-quants), bytes of the type] x Q8_1 [T, K/32, 36]
+    -> fp32 [T, k, N]."""
     torch = _torch()
-    tid, bb = WEIGHT_TYPES[wtype]
+    tid, bb, per = WEIGHT_TYPES[wtype]
     _dev(weights, torch.uint8, "weights", 4)
     _dev(act, torch.uint8, "act", 3)
     _dev(topk_ids, torch.int32, "topk_ids", 2)
     E, N, nb, wb = weights.shape
     T, nb2, ab = act.shape
-    if wb != bb or ab != 36 or nb != nb2 or topk_ids.shape[0] != T:
+    if wb != bb or ab != 36 or nb * per != nb2 * 32 or topk_ids.shape[0] != T:
         raise ValueError(f"shape mismatch for {wtype}: weights {tuple(weights.shape)} act {tuple(act.shape)} "
                          f"topk_ids {tuple(topk_ids.shape)}")
     k = topk_ids.shape[1]
@@ -233,7 +235,7 @@ def moe_gguf_q8_1(wtype, weights, act, topk_ids, out=None):
         out = torch.empty((T, k, N), dtype=torch.float32, device=weights.device)
     po = _dev(out, torch.float32, "out")
     _check(load().ft_moe_gguf_q8_1(tid, ctypes.c_void_p(weights.data_ptr()), ctypes.c_void_p(act.data_ptr()),
-                                   ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, E, N, nb * 32, _stream(weights)))
+                                   ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, E, N, nb * per, _stream(weights)))
     return out
 
 

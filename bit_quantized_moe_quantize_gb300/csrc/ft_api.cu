@@ -349,8 +349,7 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     rb.tiles_gemm = reinterpret_cast<int32_t*>(ws + L.tiles_gemm);
     rb.err = reinterpret_cast<uint32_t*>(ws + L.err);
 
-    const GemvPlan gp = plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols, sh.mean(),
-                                  weight_block_bytes(sh.wtype));
+    const GemvPlan gp = plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols, sh.mean(), sh.wtype);
     const int tile_width = gemm_tile_width(sh.mean());
     if (path == FT_PATH_GEMV && (gp.smem > 227 * 1024 || gp.stages < 1))
         return fail(FT_ERR_SIZE, "GEMV tile needs %zu bytes of shared memory (%d ring stages of %lld-column rows fit)",
@@ -445,6 +444,9 @@ static int matmul_entry(const void* weights, const void* act, const int32_t* top
     if (int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh)) return st;
     if (act_per_slot) sh.act_div = 1;
     if (weight_block_bytes(wtype) == 0) return fail(FT_ERR_ARG, "unknown weight type %d", wtype);
+    if (ncols % weight_block_values(wtype) != 0)
+        return fail(FT_ERR_ARG, "weight type %d needs ncols %% %d == 0 (got %lld)", wtype, weight_block_values(wtype),
+                    (long long)ncols);
     sh.wtype = wtype;
     if (n_local > 0) {
         if (expert_start < 0 || static_cast<int64_t>(expert_start) + n_local > n_experts)

@@ -72,9 +72,11 @@ struct GemvPlan {
 
 // mean: routed slots per expert on average (decides the slots per tile)
 GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols, double mean,
-                   int block_bytes = 18);
-// bytes of one 32-weight block of a FT_TYPE_* weight type (0: unknown type)
+                   int wtype = FT_TYPE_Q4_0);
+// bytes of one stored block of a FT_TYPE_* weight type (0: unknown type) and
+// the weights it holds (32, or 256 for the K-quant super-blocks)
 int weight_block_bytes(int wtype);
+int weight_block_values(int wtype);
 
 int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act, const int32_t* perm,
                 const int32_t* offsets, const int32_t* tiles, float* out, int32_t* dots, uint32_t* err,

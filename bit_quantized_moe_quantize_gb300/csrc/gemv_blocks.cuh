@@ -92,24 +92,44 @@ __device__ __forceinline__ uint32_t spread4(uint32_t x) {
     return ((x & 1u) << 4) | ((x & 2u) << 11) | ((x & 4u) << 18) | ((x & 8u) << 25);
 }
 
-// Weight block types of the block-per-lane kernel (GGUF, 32 weights each;
-// weight i = q_i d + c): per type its bytes, the level offset subtracted from
-// the stored level (Q4_0: 8, Q5_0: 16) and whether the block stores an fp16
-// m (c = m, Q4_1 / Q5_1; else c = 0).
+// Weight block types of the block-per-lane kernel (GGUF): per type its bytes
+// per stored block, the 32-weight sub-blocks a stored block holds (8 for the
+// K-quant super-blocks), the level offset subtracted from the stored level
+// (Q4_0: 8, Q5_0: 16), whether the block stores an fp16 m (c = m, Q4_1 / Q5_1:
+// the offset term is m s_a) and whether a sub-block carries a min
+// (K-quants: - dmin m_j d_a sum(q_a), with the exact sum of the codes).
 template <int WT>
 struct WBlock;
-template <> struct WBlock<FT_TYPE_Q4_0> { static constexpr int bytes = 18, level0 = 8; static constexpr bool has_m = false; };
-template <> struct WBlock<FT_TYPE_Q4_1> { static constexpr int bytes = 20, level0 = 0; static constexpr bool has_m = true; };
-template <> struct WBlock<FT_TYPE_Q5_0> { static constexpr int bytes = 22, level0 = 16; static constexpr bool has_m = false; };
-template <> struct WBlock<FT_TYPE_Q5_1> { static constexpr int bytes = 24, level0 = 0; static constexpr bool has_m = true; };
-template <> struct WBlock<FT_TYPE_Q8_0> { static constexpr int bytes = 34, level0 = 0; static constexpr bool has_m = false; };
+template <> struct WBlock<FT_TYPE_Q4_0> { static constexpr int bytes = 18, per = 1, level0 = 8; static constexpr bool has_m = false, has_min = false; };
+template <> struct WBlock<FT_TYPE_Q4_1> { static constexpr int bytes = 20, per = 1, level0 = 0; static constexpr bool has_m = true, has_min = false; };
+template <> struct WBlock<FT_TYPE_Q5_0> { static constexpr int bytes = 22, per = 1, level0 = 16; static constexpr bool has_m = false, has_min = false; };
+template <> struct WBlock<FT_TYPE_Q5_1> { static constexpr int bytes = 24, per = 1, level0 = 0; static constexpr bool has_m = true, has_min = false; };
+template <> struct WBlock<FT_TYPE_Q8_0> { static constexpr int bytes = 34, per = 1, level0 = 0; static constexpr bool has_m = false, has_min = false; };
+template <> struct WBlock<FT_TYPE_Q4_K> { static constexpr int bytes = 144, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = true; };
+template <> struct WBlock<FT_TYPE_Q5_K> { static constexpr int bytes = 176, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = true; };
 
-// One weight block at a 2-byte aligned shared-memory offset: fp32 d and m,
+// 6-bit scale and min of sub-block j of a K-quant super-block from its 12
+// packed bytes (w[0..2] = bytes 0..11): j < 4 the low 6 bits of bytes j and
+// j + 4; j >= 4 the low / high nibble of byte j + 4 with the top two bits of
+// byte j - 4 / j above it.
+__device__ __forceinline__ void kquant_scale_min(const uint32_t (&w)[3], int j, int& sc, int& mn) {
+    auto byte = [&](int i) { return static_cast<int>((w[i >> 2] >> (8 * (i & 3))) & 0xFFu); };
+    if (j < 4) {
+        sc = byte(j) & 63;
+        mn = byte(j + 4) & 63;
+    } else {
+        sc = (byte(j + 4) & 15) | ((byte(j - 4) >> 6) << 4);
+        mn = (byte(j + 4) >> 4) | ((byte(j) >> 6) << 4);
+    }
+}
+
+// One 32-weight block (sub-block j of the stored block at a 2-byte aligned
+// shared-memory offset): fp32 d and m (the K-quants: d sc_j and dmin m_j),
 // and its 32 stored levels as int8 lanes of eight words, weights 0..15 in
 // lo[0..3] and 16..31 in hi[0..3] (the order of the Q8_1 codes they meet).
 template <int WT>
-__device__ __forceinline__ void decode_block(const uint8_t* base, uint32_t off, float& d, float& m, int (&lo)[4],
-                                             int (&hi)[4]) {
+__device__ __forceinline__ void decode_block(const uint8_t* base, uint32_t off, int j, float& d, float& m,
+                                             int (&lo)[4], int (&hi)[4]) {
     m = 0.0f;
     if constexpr (WT == FT_TYPE_Q4_0) {
         uint32_t q[4];
@@ -141,6 +161,29 @@ __device__ __forceinline__ void decode_block(const uint8_t* base, uint32_t off, 
             lo[i] = static_cast<int>((qs[i] & 0x0F0F0F0Fu) | spread4(qh[0] >> (4 * i)));
             hi[i] = static_cast<int>(((qs[i] >> 4) & 0x0F0F0F0Fu) | spread4(qh[0] >> (16 + 4 * i)));
         }
+    } else if constexpr (WT == FT_TYPE_Q4_K || WT == FT_TYPE_Q5_K) {
+        constexpr uint32_t Q0 = WT == FT_TYPE_Q5_K ? 48 : 16;   // offset of the nibbles
+        uint32_t hd[1], sc12[3], qs[8];
+        load_words<1>(base, off, hd);
+        load_words<3>(base, off + 4, sc12);
+        load_words<8>(base, off + Q0 + 32 * (j >> 1), qs);
+        int sc, mn;
+        kquant_scale_min(sc12, j, sc, mn);
+        d = __half2float(__ushort_as_half(static_cast<unsigned short>(hd[0] & 0xFFFFu))) * static_cast<float>(sc);
+        m = __half2float(__ushort_as_half(static_cast<unsigned short>(hd[0] >> 16))) * static_cast<float>(mn);
+        const int sh = 4 * (j & 1);
+        uint32_t qh[8];
+        if constexpr (WT == FT_TYPE_Q5_K) load_words<8>(base, off + 16, qh);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t l = (qs[i] >> sh) & 0x0F0F0F0Fu, h = (qs[4 + i] >> sh) & 0x0F0F0F0Fu;
+            if constexpr (WT == FT_TYPE_Q5_K) {   // bit j of each qh byte -> bit 4 of the level byte
+                l |= ((qh[i] >> j) & 0x01010101u) << 4;
+                h |= ((qh[4 + i] >> j) & 0x01010101u) << 4;
+            }
+            lo[i] = static_cast<int>(l);
+            hi[i] = static_cast<int>(h);
+        }
     } else {
         static_assert(WT == FT_TYPE_Q8_0, "weight type");
         d = half_at(base, off);
@@ -171,7 +214,9 @@ template <int WT, int G, int RW, bool DUMP>
 __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
     constexpr int R = 8 * RW;
     constexpr int WB = WBlock<WT>::bytes;
+    constexpr int PER = WBlock<WT>::per;
     constexpr bool HAS_M = WBlock<WT>::has_m;
+    constexpr bool HAS_MIN = WBlock<WT>::has_min;
     extern __shared__ __align__(16) uint8_t smem[];
     const int64_t t = blockIdx.x;
     const int32_t E = a.n_experts;
@@ -195,9 +240,9 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
     o += static_cast<size_t>(G) * nb * 4;
     int32_t* suma = reinterpret_cast<int32_t*>(smem + o);
     uint8_t* ring = smem + gemv_act_bytes(G, nb);
-    const size_t stage_bytes = gemv_stage_bytes(R, nb, WB);
+    const size_t stage_bytes = gemv_stage_bytes(R, nb, WB / PER);
 
-    const int64_t row_bytes = static_cast<int64_t>(nb) * WB;
+    const int64_t row_bytes = static_cast<int64_t>(nb / PER) * WB;
     const uint8_t* wexp = a.weights + static_cast<int64_t>(e) * a.nrows * row_bytes;
     auto stage_rows = [&](int32_t st) { return static_cast<int32_t>(min(static_cast<int64_t>(R), r_end - (r_begin + st * R))); };
     auto issue = [&](int32_t st) {   // one thread: bulk copy of stage st into its ring slot
@@ -275,7 +320,8 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
 #pragma unroll
                 for (int j = 0; j < RW; ++j) {
                     const int rl = min(rl0 + j, nr - 1);       // rows past the stage repeat the last one
-                    decode_block<WT>(wt, static_cast<uint32_t>(rl * row_bytes + b * WB), dw[j], mw[j], lo[j], hi[j]);
+                    decode_block<WT>(wt, static_cast<uint32_t>(rl * row_bytes + (b / PER) * WB), b % PER, dw[j], mw[j],
+                                     lo[j], hi[j]);
                 }
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
@@ -284,7 +330,9 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
                         const uint4 A0 = av[0], A1 = av[1];
                         const float dag = da[g * nb + b];
                         const int sa0 = HAS_M ? 0 : WBlock<WT>::level0 * suma[g * nb + b];
-                        const float sag = HAS_M ? __int_as_float(suma[g * nb + b]) : 0.0f;
+                        // offset term's activation factor: s_a (Q4_1, Q5_1) or -d_a sum(q_a) (K-quants)
+                        const float sag = HAS_M ? __int_as_float(suma[g * nb + b])
+                                                : HAS_MIN ? -dag * small_int_to_float(suma[g * nb + b]) : 0.0f;
 #pragma unroll
                         for (int j = 0; j < RW; ++j) {
                             int dot = -sa0;
@@ -301,7 +349,7 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
                                     a.dots[(static_cast<int64_t>(slot[g]) * a.nrows + r0 + rl0 + j) * nb + b] = dot;
                             } else {
                                 acc[j][g] = fmaf(small_int_to_float(dot), dw[j] * dag, acc[j][g]);
-                                if constexpr (HAS_M) acc[j][g] = fmaf(mw[j], sag, acc[j][g]);
+                                if constexpr (HAS_M || HAS_MIN) acc[j][g] = fmaf(mw[j], sag, acc[j][g]);
                             }
                         }
                     }

@@ -280,16 +280,23 @@ int weight_block_bytes(int wtype) {
         case FT_TYPE_Q5_0: return WBlock<FT_TYPE_Q5_0>::bytes;
         case FT_TYPE_Q5_1: return WBlock<FT_TYPE_Q5_1>::bytes;
         case FT_TYPE_Q8_0: return WBlock<FT_TYPE_Q8_0>::bytes;
+        case FT_TYPE_Q4_K: return WBlock<FT_TYPE_Q4_K>::bytes;
+        case FT_TYPE_Q5_K: return WBlock<FT_TYPE_Q5_K>::bytes;
         default: return 0;
     }
 }
 
-GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols, double mean,
-                   int block_bytes) {
+int weight_block_values(int wtype) {
+    return wtype == FT_TYPE_Q4_K || wtype == FT_TYPE_Q5_K ? 256 : weight_block_bytes(wtype) ? 32 : 0;
+}
+
+GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols, double mean, int wtype) {
+    // row bytes per 32 weights (whole: 144 / 8 and 176 / 8 for the K-quants)
+    const int block_bytes = weight_block_bytes(wtype) * 32 / weight_block_values(wtype);
     GemvPlan p{};
     const int64_t nb = ncols / QK;
     p.group = mean <= 1.0 ? 1 : mean <= 2.0 ? 2 : mean <= 4.0 ? 4 : 8;
-    if (ncols % 256 == 0 && block_bytes == Q4_0_BYTES) {
+    if (ncols % 256 == 0 && wtype == FT_TYPE_Q4_0) {
         // row-per-lane kernel (Q4_0 only).  KS warps per row group so that the batch
         // keeps ~32 compute warps per SM busy, then as many row groups per CTA
         // (RW, RW * KS <= 8) as still leave two CTAs per SM; a ring of
@@ -435,7 +442,7 @@ int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act
     a.n_experts = n_experts;
     a.stages = plan.stages;
     a.rows_per_cta = plan.rows_per_cta;
-    a.bulk = ((static_cast<int64_t>(a.nb) * weight_block_bytes(wtype)) % 16 == 0) &&
+    a.bulk = ((ncols / weight_block_values(wtype) * weight_block_bytes(wtype)) % 16 == 0) &&
              ((reinterpret_cast<uintptr_t>(weights) & 15u) == 0);
     a.row_warps = plan.row_warps;
     a.ksplit = plan.ksplit;

@@ -101,6 +101,16 @@ typedef enum {
 #define FT_TYPE_Q5_0 6
 #define FT_TYPE_Q5_1 7
 #define FT_TYPE_Q8_0 8
+/* K-quants: 256 weights per super-block, eight sub-blocks of 32; weight l of
+ * sub-block j = d * sc_j * q_l - dmin * m_j with 6-bit sc_j, m_j packed in 12
+ * bytes (j < 4: low 6 bits of bytes j and j + 4; j >= 4: low / high nibble of
+ * byte j + 4 with the top two bits of byte j - 4 / j above it).  Sub-block j
+ * takes nibble byte 32 * (j / 2) + l, low nibble for even j, high for odd j.
+ *   Q4_K 144 B: fp16 d, fp16 dmin, 12 B scales/mins, 128 B nibbles
+ *   Q5_K 176 B: fp16 d, fp16 dmin, 12 B scales/mins, 32 B qh (bit j of qh[l]
+ *        is the 5th bit of weight l of sub-block j), 128 B nibbles */
+#define FT_TYPE_Q4_K 12
+#define FT_TYPE_Q5_K 13
 
 /* Gated activations of ft_act_mul_quantize_q8_1 / ft_moe_ffn_q4_0_q8_1. */
 #define FT_ACT_SILU 0        /* silu(g) = g / (1 + exp(-g))                              */
@@ -238,17 +248,20 @@ FT_API int ft_moe_q4_0_q8_1_ep(const void* weights_local, const void* act, const
                                int64_t ncols, void* stream);
 
 /*
- * ft_moe_gguf_q8_1 - the routed matmul with expert weights of any GGUF type
- * whose blocks hold 32 weights (FT_TYPE_*; the per-type launchers of
- * moe_vec.cuh on FreeToken PR #185, "Notes"):
+ * ft_moe_gguf_q8_1 - the routed matmul with expert weights of a GGUF type
+ * (FT_TYPE_*; the per-type launchers of moe_vec.cuh on FreeToken PR #185,
+ * "Notes"):
  *   out[s][r] = sum_b d_w d_a sum_i q_i q_a[i] + c s_a
- * per weight block b of row r of expert topk_ids[s] and activation block b of
- * the slot's token, with q_i, c as in the FT_TYPE_* list and s_a the
- * activation block's stored fp16 s (c = 0 for Q4_0, Q5_0, Q8_0).
+ * per 32-weight block b of row r of expert topk_ids[s] and activation block b
+ * of the slot's token, with q_i, c as in the FT_TYPE_* list and s_a the
+ * activation block's stored fp16 s (c = 0 for Q4_0, Q5_0, Q8_0); for the
+ * K-quants, per sub-block b, d sc_b d_a sum_i q_i q_a[i] - dmin m_b d_a sum_i q_a[i].
  *
  *   wtype     FT_TYPE_Q4_0 (exactly ft_moe_q4_0_q8_1), FT_TYPE_Q4_1,
- *             FT_TYPE_Q5_0, FT_TYPE_Q5_1 or FT_TYPE_Q8_0
- *   weights   device, [n_experts][nrows][ncols/32] blocks of wtype; 16-byte aligned
+ *             FT_TYPE_Q5_0, FT_TYPE_Q5_1, FT_TYPE_Q8_0, FT_TYPE_Q4_K or
+ *             FT_TYPE_Q5_K (the K-quants need ncols % 256 == 0)
+ *   weights   device, [n_experts][nrows][ncols/32] blocks of wtype
+ *             ([ncols/256] super-blocks for the K-quants); 16-byte aligned
  *   act, topk_ids, out, tokens, top_k, n_experts, nrows, ncols as for
  *   ft_moe_q4_0_q8_1.
  * Types other than Q4_0 always take the GEMV path (one weight block per

@@ -176,3 +176,6 @@ def test_gguf_matmul_rejects_bad_arguments(lib):
     assert f(3, W, A, I, O, 0, 2, 8, 128, 256, vp(0)) == 0       # no slots: no-op
     assert f(6, W, A, I, vp(0), 4, 2, 8, 128, 256, vp(0)) == 1   # null out
     assert f(7, vp(0x10008), A, I, O, 4, 2, 8, 128, 256, vp(0)) == 3   # weights misaligned
+    assert f(12, W, A, I, O, 4, 2, 8, 128, 160, vp(0)) == 1      # Q4_K: ncols % 256
+    assert "ncols % 256" in _err(lib)
+    assert f(13, W, A, I, O, 4, 2, 8, 128, 288, vp(0)) == 1      # Q5_K: ncols % 256

@@ -75,8 +75,8 @@ _S_WEIGHTS, _S_ACT, _S_ROUTE, _S_OUTLIER, _S_RANK, _S_GGUF = 0, 1, 2, 3, 4, 5
 # the code bytes, whether the block stores an fp16 m after d, GGML type number
 GGUF_TYPES = {"q4_0": (18, 2, False, 2), "q4_1": (20, 4, True, 3), "q5_0": (22, 2, False, 6),
               "q5_1": (24, 4, True, 7), "q8_0": (34, 2, False, 8),
-              "q4_k": (144, 4, False, 12), "q5_k": (176, 4, False, 13)}
-KQUANTS = ("q4_k", "q5_k")     # 256 weights per (super-)block; the others hold 32
+              "q4_k": (144, 4, False, 12), "q5_k": (176, 4, False, 13), "q6_k": (210, 0, False, 14)}
+KQUANTS = ("q4_k", "q5_k", "q6_k")     # 256 weights per (super-)block; the others hold 32
 
 
 def _rng(seed: int, stream: int, *extra: int) -> np.random.Generator:
@@ -131,7 +131,8 @@ def make_weights_gguf(wl: Workload, wtype: str, chunk_rows: int = 1 << 16) -> np
     offset, m = fp16(-d * L / 2 * (1 + 0.1 z')) with L the number of levels,
     so that the weights centre near zero like trained ones; the K-quants take
     0.05 of that d and dmin = fp16(d L / 2 |1 + 0.1 z'|) (the 6-bit sub-block
-    scale and min multiply both).  Random bytes are valid blocks
+    scale and min multiply both); Q6_K takes random int8 scales and
+    d = fp16(0.00002 (0.5 + |z|)).  Random bytes are valid blocks
     of these formats; no weight quantization is involved.
     """
     if wtype == "q4_0":
@@ -145,6 +146,11 @@ def make_weights_gguf(wl: Workload, wtype: str, chunk_rows: int = 1 << 16) -> np
     for r0 in range(0, E * N, chunk_rows):
         r1 = min(E * N, r0 + chunk_rows)
         n = r1 - r0
+        if wtype == "q6_k":     # random code and scale bytes, fp16 d last
+            out[r0:r1, :, 0:208] = rng.integers(0, 256, size=(n, nb, 208), dtype=np.uint8)
+            d6 = np.float32(0.00002) * (np.float32(0.5) + np.abs(rng.standard_normal((n, nb), dtype=np.float32)))
+            out[r0:r1, :, 208:210] = d6.astype(np.float16).view(np.uint8).reshape(n, nb, 2)
+            continue
         d = (np.float32(0.0005) + np.float32(0.002) * np.abs(rng.standard_normal((n, nb), dtype=np.float32)))
         if wtype in KQUANTS:      # super-block scales of the 6-bit sub-block scales and mins
             d = d * np.float32(0.05)

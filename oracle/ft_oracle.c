@@ -209,6 +209,7 @@ int32_t oracle_gguf_block_bytes(int32_t type)
         case ORACLE_GGUF_Q8_0: return 34;
         case ORACLE_GGUF_Q4_K: return 144;
         case ORACLE_GGUF_Q5_K: return 176;
+        case ORACLE_GGUF_Q6_K: return 210;
         default: return 0;
     }
 }
@@ -256,7 +257,31 @@ static double gguf_offset(const uint8_t* blk, int32_t type)
  * j < 4 the low 6 bits of bytes j and j + 4; for j >= 4 the low nibble of byte
  * j + 4 with the top two bits of byte j - 4 above it, and the high nibble of
  * byte j + 4 with the top two bits of byte j above it. */
-static int is_kquant(int32_t type) { return type == ORACLE_GGUF_Q4_K || type == ORACLE_GGUF_Q5_K; }
+static int is_kquant(int32_t type)
+{
+    return type == ORACLE_GGUF_Q4_K || type == ORACLE_GGUF_Q5_K || type == ORACLE_GGUF_Q6_K;
+}
+
+/* Q6_K, 210 B per 256 weights: 128 B ql (low nibbles), 64 B qh (2-bit high
+ * parts), 16 int8 scales, fp16 d last.  The super-block is two halves of 128
+ * weights; sub-block j = 4 h + k (k < 4) of half h takes, for weight l < 32,
+ * nibble byte 64 h + 32 (k % 2) + l (low nibble for k < 2, high for k >= 2),
+ * bits 2k, 2k + 1 of byte 128 + 32 h + l as bits 4, 5, and level
+ * q = that 6-bit value - 32; weights l < 16 use scale 8 h + 2 k, l >= 16 scale
+ * 8 h + 2 k + 1: weight = d * scale * q. */
+static void q6k_sub(const uint8_t* sb, int j, int* lev, double* dsc_lo, double* dsc_hi)
+{
+    const int h = j / 4, k = j % 4;
+    const double d = oracle_half_to_double(rd16(sb + 208));
+    *dsc_lo = d * (double)(int8_t)sb[192 + 8 * h + 2 * k];
+    *dsc_hi = d * (double)(int8_t)sb[192 + 8 * h + 2 * k + 1];
+    for (int l = 0; l < QK; ++l) {
+        const uint8_t ql = sb[64 * h + 32 * (k % 2) + l];
+        const int lo4 = k < 2 ? (ql & 0x0f) : (ql >> 4);
+        const int hi2 = (sb[128 + 32 * h + l] >> (2 * k)) & 3;
+        lev[l] = (lo4 | (hi2 << 4)) - 32;
+    }
+}
 
 static void kquant_scale_min(const uint8_t* sc12, int j, int* sc, int* m)
 {
@@ -287,6 +312,17 @@ static void kquant_sub(const uint8_t* sb, int32_t type, int j, int* lev, double*
 void oracle_dequantize_gguf(int32_t type, const uint8_t* blocks, int64_t n_blocks, double* out)
 {
     const int32_t bytes = oracle_gguf_block_bytes(type);
+    if (type == ORACLE_GGUF_Q6_K) {
+        for (int64_t b = 0; b < n_blocks; ++b)
+            for (int j = 0; j < 8; ++j) {
+                int lev[QK];
+                double dlo, dhi;
+                q6k_sub(blocks + b * bytes, j, lev, &dlo, &dhi);
+                for (int l = 0; l < QK; ++l)
+                    out[b * 256 + j * QK + l] = (l < 16 ? dlo : dhi) * lev[l];
+            }
+        return;
+    }
     if (is_kquant(type)) {
         for (int64_t b = 0; b < n_blocks; ++b)
             for (int j = 0; j < 8; ++j) {
@@ -334,6 +370,20 @@ void oracle_moe_gguf_q8_1(int32_t type, const uint8_t* weights, const uint8_t* a
                 for (int64_t b = 0; b < nb; ++b) {
                     int lev[QK];
                     double dsc, dmn;
+                    if (type == ORACLE_GGUF_Q6_K) {
+                        /* two 16-weight scale groups per 32-block: d sc_lo d_a sum_lo + d sc_hi d_a sum_hi */
+                        double dlo, dhi;
+                        q6k_sub(row + (b / 8) * bytes, (int)(b % 8), lev, &dlo, &dhi);
+                        const uint8_t* ab6 = act + (t * nb + b) * Q8_1_BYTES;
+                        const double da6 = oracle_half_to_double(rd16(ab6));
+                        int32_t dlo_i = 0, dhi_i = 0;
+                        for (int l = 0; l < QK; ++l) {
+                            if (l < 16) dlo_i += lev[l] * (int32_t)(int8_t)ab6[4 + l];
+                            else dhi_i += lev[l] * (int32_t)(int8_t)ab6[4 + l];
+                        }
+                        y += dlo * da6 * (double)dlo_i + dhi * da6 * (double)dhi_i;
+                        continue;
+                    }
                     kquant_sub(row + (b / 8) * bytes, type, (int)(b % 8), lev, &dsc, &dmn);
                     const uint8_t* ab = act + (t * nb + b) * Q8_1_BYTES;
                     const double da = oracle_half_to_double(rd16(ab));

@@ -58,6 +58,8 @@
  * sub-block j = d * sc_j * q_l - dmin * m_j, 6-bit sc_j and m_j):
  *   Q4_K 144 B: fp16 d, fp16 dmin, 12 B scales/mins, 128 B nibbles
  *   Q5_K 176 B: fp16 d, fp16 dmin, 12 B scales/mins, 32 B qh, 128 B nibbles
+ *   Q6_K 210 B: 128 B low nibbles, 64 B 2-bit high parts, 16 int8 scales (one
+ *       per 16 weights), fp16 d; level = 6-bit value - 32, weight = d scale q
  *   (oracle_dequantize_gguf counts super-blocks for these; ncols % 256 == 0)
  *   weights [E][N][K/32] blocks of the type.
  */
@@ -87,6 +89,7 @@ void oracle_dequantize_q8_1(const uint8_t* blocks, int64_t n_blocks, double* out
 #define ORACLE_GGUF_Q8_0 8
 #define ORACLE_GGUF_Q4_K 12
 #define ORACLE_GGUF_Q5_K 13
+#define ORACLE_GGUF_Q6_K 14
 int32_t oracle_gguf_block_bytes(int32_t type);
 void oracle_dequantize_gguf(int32_t type, const uint8_t* blocks, int64_t n_blocks, double* out);
 int32_t oracle_gguf_block_dot(int32_t type, const uint8_t* w_block, const uint8_t* a_block);

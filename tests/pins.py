@@ -715,6 +715,68 @@ def pin_kquant_unit_scales_are_q4_1(o):
     assert np.array_equal(o.dequantize_gguf("q4_k", b[None]), o.dequantize_gguf("q4_1", q41))
 
 
+def numpy_decode_q6k(w):
+    """Independent vectorised decode of Q6_K super-blocks [..., nsb, 210] -> fp64 [..., nsb * 256]."""
+    w = np.ascontiguousarray(w)
+    lead = w.shape[:-1]
+    d = w[..., 208:210].copy().view(np.float16)[..., 0].astype(np.float64)
+    sc = w[..., 192:208].copy().view(np.int8).astype(np.float64)           # [..., 16]
+    ql = w[..., 0:128].astype(np.int64).reshape(*lead, 2, 2, 32)            # half, k % 2, l
+    qh = w[..., 128:192].astype(np.int64).reshape(*lead, 2, 32)             # half, l
+    out = np.empty((*lead, 2, 4, 32), dtype=np.float64)
+    for k in range(4):
+        lo4 = (ql[..., k % 2, :] >> (4 * (k // 2))) & 15
+        hi2 = (qh >> (2 * k)) & 3
+        q = (lo4 | (hi2 << 4)) - 32                                          # [..., 2, 32]
+        s_lo = sc[..., [2 * k, 8 + 2 * k]]                                   # [..., 2]
+        s_hi = sc[..., [2 * k + 1, 8 + 2 * k + 1]]
+        scale = np.concatenate([np.repeat(s_lo[..., None], 16, -1), np.repeat(s_hi[..., None], 16, -1)], -1)
+        out[..., k, :] = d[..., None, None] * scale * q
+    return out.reshape(*w.shape[:-2], w.shape[-2] * 256)
+
+
+def pin_q6k_hand(o):
+    """A hand-built Q6_K super-block: level = low nibble | 2 high bits << 4, - 32,
+    one int8 scale per 16 weights (negative ones included), d stored last."""
+    b = np.zeros(210, np.uint8)
+    b[208:210] = [0x00, 0x3C]                                    # d = 1
+    scales = np.array([1, -2, 3, 4, 5, 6, -7, 8, 9, 10, 11, 12, 13, -14, 15, 127], np.int8)
+    b[192:208] = scales.view(np.uint8)
+    l = np.arange(32)
+    b[0:32] = (l % 16) | (((l + 3) % 16) << 4)                    # half 0, k = 0 low / k = 2 high
+    b[32:64] = (l % 7) | ((l % 5) << 4)                           # half 0, k = 1 low / k = 3 high
+    b[128:160] = 0b11100100                                       # 2-bit parts 0, 1, 2, 3 for k = 0..3
+    got = o.dequantize_gguf("q6_k", b[None]).reshape(8, 32)
+    lo4 = {0: l % 16, 1: l % 7, 2: (l + 3) % 16, 3: l % 5}
+    for k in range(4):
+        q = (lo4[k] | (k << 4)) - 32
+        want = np.where(l < 16, scales[2 * k], scales[2 * k + 1]).astype(np.float64) * q
+        assert np.array_equal(got[k], want), k
+    # half 1 is all zero bytes: level -32 everywhere, scales 8..15
+    for k in range(4):
+        want = np.where(l < 16, scales[8 + 2 * k], scales[8 + 2 * k + 1]).astype(np.float64) * -32
+        assert np.array_equal(got[4 + k], want), 4 + k
+
+
+def pin_q6k_numpy(o):
+    """Decode against the numpy decoder; the matmul against the plain dequantized dot."""
+    w = _gguf_random("q6_k", K=512, seed=11)
+    assert np.array_equal(o.dequantize_gguf("q6_k", w), numpy_decode_q6k(w))
+    rng = np.random.default_rng(12)
+    E, k, K, N, T = 3, 2, 512, 5, 4
+    act = o.quantize_q8_1(rng.standard_normal((T, K)).astype(np.float16))
+    ids = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    xa = numpy_decode_q8_1(act)
+    w = _gguf_random("q6_k", E=E, N=N, K=K, seed=13)
+    wv = numpy_decode_q6k(w).reshape(E, N, K)
+    got = o.moe_gguf("q6_k", w, act, ids).astype(np.float64)
+    for t in range(T):
+        for j in range(k):
+            want = wv[ids[t, j]] @ xa[t]
+            scale = np.abs(wv[ids[t, j]]) @ np.abs(xa[t])
+            assert np.all(np.abs(got[t, j] - want) <= 1e-6 * scale + 1e-12)
+
+
 ALL_PINS = [
     pin_fp16, pin_q4_0_hand, pin_q4_0_nearest_level, pin_q4_0_matches_generator, pin_q4_0_dequant,
     pin_q8_1_hand, pin_q8_1_numpy, pin_q8_1_error_bound, pin_route, pin_block_dot_hand,
@@ -723,5 +785,5 @@ ALL_PINS = [
     pin_moe_ep_shards_sum_to_full, pin_act_library, pin_act_tail_accuracy, pin_act_gelu_vs_erf, pin_act_odd_identity, pin_act_hand,
     pin_act_quantize_numpy, pin_gguf_hand, pin_gguf_numpy_decode, pin_gguf_moe_numpy,
     pin_gguf_q4_0_is_the_q4_0_matmul, pin_kquant_hand, pin_kquant_numpy_decode, pin_kquant_moe_numpy,
-    pin_kquant_unit_scales_are_q4_1,
+    pin_kquant_unit_scales_are_q4_1, pin_q6k_hand, pin_q6k_numpy,
 ]

@@ -70,6 +70,11 @@ MUTANTS = {
     "kquant_nibble_half": ("lev[l] = (j % 2 == 0) ? (qs[l] & 0x0f) : (qs[l] >> 4);",
                            "lev[l] = (j % 2 == 0) ? (qs[l] >> 4) : (qs[l] & 0x0f);"),
     "q5k_bit_index": ("lev[l] |= ((sb[16 + l] >> j) & 1) << 4;", "lev[l] |= ((sb[16 + l] >> (j / 2)) & 1) << 4;"),
+    "q6k_offset_31": ("lev[l] = (lo4 | (hi2 << 4)) - 32;", "lev[l] = (lo4 | (hi2 << 4)) - 31;"),
+    "q6k_high_bits": ("const int hi2 = (sb[128 + 32 * h + l] >> (2 * k)) & 3;",
+                      "const int hi2 = (sb[128 + 32 * h + l] >> k) & 3;"),
+    "q6k_scale_group": ("if (l < 16) dlo_i += lev[l] * (int32_t)(int8_t)ab6[4 + l];",
+                        "if (l < 15) dlo_i += lev[l] * (int32_t)(int8_t)ab6[4 + l];"),
     "bad_id_not_zeroed": ("    if (e < 0 || e >= n_experts)\n        return 0.0;\n",
                           "    if (e < 0 || e >= n_experts)\n        e = 0;\n"),
 }

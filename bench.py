@@ -47,19 +47,25 @@ PAGES_T4_TOKENS_PER_S = {("prefill", 8191): 8191 / 0.7058, ("prefill", 4096): 40
                          ("prefill", 2048): 2048 / 0.1740}
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
 # capture (profiles/moe_gemm_tc_prefill.md), keyed by a hash of the sources that
-# kernel is built from, so a changed kernel reports null instead.
+# kernel is built from (its own files and the tile constants it takes from the
+# internal header), so a changed kernel reports null instead.
 GEMM_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemm_tc.cu", "bit_quantized_moe_quantize_gb300/csrc/gemm_common.cuh",
-                "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh", "bit_quantized_moe_quantize_gb300/csrc/ft_internal.h")
-NCU_TRAFFIC = {("moe_gemm_tc_kernel", "5966128ff74c2e7f", "prefill:8191"): 666817280 + 340600320}
+                "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh")
+GEMM_CONSTANTS = ("bit_quantized_moe_quantize_gb300/csrc/ft_internal.h", "kGemm")
+NCU_TRAFFIC = {("moe_gemm_tc_kernel", "1d61a05e410c8baf", "prefill:8191"): 666817280 + 340600320}
 
 
-def kernel_source_hash(files) -> str:
+def kernel_source_hash(files, constants=GEMM_CONSTANTS) -> str:
     import hashlib
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(os.path.basename(f).encode())
             h.update(fh.read())
+    if constants:
+        path, key = constants
+        with open(os.path.join(ROOT, path)) as fh:
+            h.update("".join(line for line in fh if key in line).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,6 +1,6 @@
 // The block-per-lane GEMV kernel of the routed expert matmul, templated on the
-// weight block type (GGUF Q4_0, Q4_1, Q5_0, Q5_1, Q8_0: the per-type
-// launchers of moe_vec.cuh on FreeToken PR #185, "Notes"), with its shared
+// weight block type (GGUF Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K: the
+// per-type launchers of moe_vec.cuh on FreeToken PR #185, "Notes"), with its shared
 // arguments and launch helpers.  moe_gemv.cu instantiates it for Q4_0 next to
 // the row-per-lane kernel; moe_gemv_gguf.cu for the other types.
 #pragma once
@@ -36,7 +36,7 @@ constexpr int kMaxStages = 4;
 
 // Shared-memory carve-up (bytes), in this order:
 //   mbarriers [kMaxStages] (32) | slot ids int32[G] (pad 16) | qa [G][nb][32] |
-//   da f32 [G][nb] | suma i32 [G][nb] | weight ring [stages][R rows][nb][18] (+16 pad each)
+//   da f32 [G][nb] | suma i32 [G][nb] | weight ring [stages][R rows][row bytes] (+16 pad each)
 __host__ __device__ inline size_t gemv_act_bytes(int G, int nb) {
     return (32 + ((static_cast<size_t>(G) * 4 + 15) / 16) * 16 + static_cast<size_t>(G) * nb * 40 + 15) / 16 * 16;
 }
@@ -97,16 +97,19 @@ __device__ __forceinline__ uint32_t spread4(uint32_t x) {
 // K-quant super-blocks), the level offset subtracted from the stored level
 // (Q4_0: 8, Q5_0: 16), whether the block stores an fp16 m (c = m, Q4_1 / Q5_1:
 // the offset term is m s_a) and whether a sub-block carries a min
-// (K-quants: - dmin m_j d_a sum(q_a), with the exact sum of the codes).
+// (K-quants: - dmin m_j d_a sum(q_a), with the exact sum of the codes), and
+// whether the block's two 16-weight halves carry their own scales (Q6_K:
+// d sc_lo and d sc_hi come back in d and m).
 template <int WT>
 struct WBlock;
-template <> struct WBlock<FT_TYPE_Q4_0> { static constexpr int bytes = 18, per = 1, level0 = 8; static constexpr bool has_m = false, has_min = false; };
-template <> struct WBlock<FT_TYPE_Q4_1> { static constexpr int bytes = 20, per = 1, level0 = 0; static constexpr bool has_m = true, has_min = false; };
-template <> struct WBlock<FT_TYPE_Q5_0> { static constexpr int bytes = 22, per = 1, level0 = 16; static constexpr bool has_m = false, has_min = false; };
-template <> struct WBlock<FT_TYPE_Q5_1> { static constexpr int bytes = 24, per = 1, level0 = 0; static constexpr bool has_m = true, has_min = false; };
-template <> struct WBlock<FT_TYPE_Q8_0> { static constexpr int bytes = 34, per = 1, level0 = 0; static constexpr bool has_m = false, has_min = false; };
-template <> struct WBlock<FT_TYPE_Q4_K> { static constexpr int bytes = 144, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = true; };
-template <> struct WBlock<FT_TYPE_Q5_K> { static constexpr int bytes = 176, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = true; };
+template <> struct WBlock<FT_TYPE_Q4_0> { static constexpr int bytes = 18, per = 1, level0 = 8; static constexpr bool has_m = false, has_min = false, split = false; };
+template <> struct WBlock<FT_TYPE_Q4_1> { static constexpr int bytes = 20, per = 1, level0 = 0; static constexpr bool has_m = true, has_min = false, split = false; };
+template <> struct WBlock<FT_TYPE_Q5_0> { static constexpr int bytes = 22, per = 1, level0 = 16; static constexpr bool has_m = false, has_min = false, split = false; };
+template <> struct WBlock<FT_TYPE_Q5_1> { static constexpr int bytes = 24, per = 1, level0 = 0; static constexpr bool has_m = true, has_min = false, split = false; };
+template <> struct WBlock<FT_TYPE_Q8_0> { static constexpr int bytes = 34, per = 1, level0 = 0; static constexpr bool has_m = false, has_min = false, split = false; };
+template <> struct WBlock<FT_TYPE_Q4_K> { static constexpr int bytes = 144, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = true, split = false; };
+template <> struct WBlock<FT_TYPE_Q5_K> { static constexpr int bytes = 176, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = true, split = false; };
+template <> struct WBlock<FT_TYPE_Q6_K> { static constexpr int bytes = 210, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = false, split = true; };
 
 // 6-bit scale and min of sub-block j of a K-quant super-block from its 12
 // packed bytes (w[0..2] = bytes 0..11): j < 4 the low 6 bits of bytes j and
@@ -184,6 +187,27 @@ __device__ __forceinline__ void decode_block(const uint8_t* base, uint32_t off, 
             lo[i] = static_cast<int>(l);
             hi[i] = static_cast<int>(h);
         }
+    } else if constexpr (WT == FT_TYPE_Q6_K) {
+        // sub-block j = 4 h + k: low nibbles from byte 64 h + 32 (k % 2) + l
+        // (high nibble for k >= 2), 2-bit high parts from bits 2k of byte
+        // 128 + 32 h + l, level - 32; int8 scales 8 h + 2k (weights < 16) and
+        // 8 h + 2k + 1; fp16 d last
+        const int h = j >> 2, k = j & 3;
+        uint32_t ql[8], qh[8];
+        load_words<8>(base, off + 64 * h + 32 * (k & 1), ql);
+        load_words<8>(base, off + 128 + 32 * h, qh);
+        const unsigned short scw = *reinterpret_cast<const unsigned short*>(base + off + 192 + 8 * h + 2 * k);
+        const float d6 = half_at(base, off + 208);
+        d = d6 * static_cast<float>(static_cast<int8_t>(scw & 0xFFu));
+        m = d6 * static_cast<float>(static_cast<int8_t>(scw >> 8));
+        const int sh = 4 * (k >> 1);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t l = ((ql[i] >> sh) & 0x0F0F0F0Fu) | (((qh[i] >> (2 * k)) & 0x03030303u) << 4);
+            const uint32_t hh = ((ql[4 + i] >> sh) & 0x0F0F0F0Fu) | (((qh[4 + i] >> (2 * k)) & 0x03030303u) << 4);
+            lo[i] = static_cast<int>(__vsub4(l, 0x20202020u));   // per byte: level - 32 as int8
+            hi[i] = static_cast<int>(__vsub4(hh, 0x20202020u));
+        }
     } else {
         static_assert(WT == FT_TYPE_Q8_0, "weight type");
         d = half_at(base, off);
@@ -217,6 +241,8 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
     constexpr int PER = WBlock<WT>::per;
     constexpr bool HAS_M = WBlock<WT>::has_m;
     constexpr bool HAS_MIN = WBlock<WT>::has_min;
+    constexpr bool SPLIT = WBlock<WT>::split;
+    static_assert(!(SPLIT && DUMP), "block dots are a Q4_0 diagnostic");
     extern __shared__ __align__(16) uint8_t smem[];
     const int64_t t = blockIdx.x;
     const int32_t E = a.n_experts;
@@ -240,9 +266,10 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
     o += static_cast<size_t>(G) * nb * 4;
     int32_t* suma = reinterpret_cast<int32_t*>(smem + o);
     uint8_t* ring = smem + gemv_act_bytes(G, nb);
-    const size_t stage_bytes = gemv_stage_bytes(R, nb, WB / PER);
-
     const int64_t row_bytes = static_cast<int64_t>(nb / PER) * WB;
+    // R rows + 16 bytes of padding, 16-byte granular (Q6_K's 210-byte blocks
+    // make a row no whole number of bytes per 32 weights)
+    const size_t stage_bytes = (static_cast<size_t>(R) * row_bytes + 16 + 15) / 16 * 16;
     const uint8_t* wexp = a.weights + static_cast<int64_t>(e) * a.nrows * row_bytes;
     auto stage_rows = [&](int32_t st) { return static_cast<int32_t>(min(static_cast<int64_t>(R), r_end - (r_begin + st * R))); };
     auto issue = [&](int32_t st) {   // one thread: bulk copy of stage st into its ring slot
@@ -335,6 +362,19 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
                                                 : HAS_MIN ? -dag * small_int_to_float(suma[g * nb + b]) : 0.0f;
 #pragma unroll
                         for (int j = 0; j < RW; ++j) {
+                            if constexpr (SPLIT) {   // two scale groups of 16 weights
+                                int dl = __dp4a(lo[j][0], static_cast<int>(A0.x), 0);
+                                dl = __dp4a(lo[j][1], static_cast<int>(A0.y), dl);
+                                dl = __dp4a(lo[j][2], static_cast<int>(A0.z), dl);
+                                dl = __dp4a(lo[j][3], static_cast<int>(A0.w), dl);
+                                int dh = __dp4a(hi[j][0], static_cast<int>(A1.x), 0);
+                                dh = __dp4a(hi[j][1], static_cast<int>(A1.y), dh);
+                                dh = __dp4a(hi[j][2], static_cast<int>(A1.z), dh);
+                                dh = __dp4a(hi[j][3], static_cast<int>(A1.w), dh);
+                                acc[j][g] = fmaf(small_int_to_float(dl), dw[j] * dag, acc[j][g]);
+                                acc[j][g] = fmaf(small_int_to_float(dh), mw[j] * dag, acc[j][g]);
+                                continue;
+                            }
                             int dot = -sa0;
                             dot = __dp4a(lo[j][0], static_cast<int>(A0.x), dot);
                             dot = __dp4a(lo[j][1], static_cast<int>(A0.y), dot);

@@ -282,17 +282,21 @@ int weight_block_bytes(int wtype) {
         case FT_TYPE_Q8_0: return WBlock<FT_TYPE_Q8_0>::bytes;
         case FT_TYPE_Q4_K: return WBlock<FT_TYPE_Q4_K>::bytes;
         case FT_TYPE_Q5_K: return WBlock<FT_TYPE_Q5_K>::bytes;
+        case FT_TYPE_Q6_K: return WBlock<FT_TYPE_Q6_K>::bytes;
         default: return 0;
     }
 }
 
 int weight_block_values(int wtype) {
-    return wtype == FT_TYPE_Q4_K || wtype == FT_TYPE_Q5_K ? 256 : weight_block_bytes(wtype) ? 32 : 0;
+    return wtype == FT_TYPE_Q4_K || wtype == FT_TYPE_Q5_K || wtype == FT_TYPE_Q6_K ? 256
+           : weight_block_bytes(wtype)                                            ? 32
+                                                                                  : 0;
 }
 
 GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols, double mean, int wtype) {
-    // row bytes per 32 weights (whole: 144 / 8 and 176 / 8 for the K-quants)
-    const int block_bytes = weight_block_bytes(wtype) * 32 / weight_block_values(wtype);
+    // row bytes per 32 weights (144 / 8, 176 / 8 for Q4_K, Q5_K; Q6_K's 210 / 8
+    // rounded up, enough for sizing the ring)
+    const int block_bytes = (weight_block_bytes(wtype) * 32 + weight_block_values(wtype) - 1) / weight_block_values(wtype);
     GemvPlan p{};
     const int64_t nb = ncols / QK;
     p.group = mean <= 1.0 ? 1 : mean <= 2.0 ? 2 : mean <= 4.0 ? 4 : 8;

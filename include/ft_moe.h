@@ -111,6 +111,12 @@ typedef enum {
  *        is the 5th bit of weight l of sub-block j), 128 B nibbles */
 #define FT_TYPE_Q4_K 12
 #define FT_TYPE_Q5_K 13
+/*   Q6_K 210 B: 128 B low nibbles, 64 B 2-bit high parts, 16 int8 scales (one
+ *        per 16 weights), fp16 d last.  Sub-block j = 4 h + k takes nibble byte
+ *        64 h + 32 (k % 2) + l (high nibble for k >= 2) and bits 2k, 2k + 1 of
+ *        byte 128 + 32 h + l; level = that 6-bit value - 32; weight l uses
+ *        scale 8 h + 2 k (l < 16) or 8 h + 2 k + 1: weight = d * scale * level */
+#define FT_TYPE_Q6_K 14
 
 /* Gated activations of ft_act_mul_quantize_q8_1 / ft_moe_ffn_q4_0_q8_1. */
 #define FT_ACT_SILU 0        /* silu(g) = g / (1 + exp(-g))                              */
@@ -255,11 +261,12 @@ FT_API int ft_moe_q4_0_q8_1_ep(const void* weights_local, const void* act, const
  * per 32-weight block b of row r of expert topk_ids[s] and activation block b
  * of the slot's token, with q_i, c as in the FT_TYPE_* list and s_a the
  * activation block's stored fp16 s (c = 0 for Q4_0, Q5_0, Q8_0); for the
- * K-quants, per sub-block b, d sc_b d_a sum_i q_i q_a[i] - dmin m_b d_a sum_i q_a[i].
+ * K-quants, per sub-block b, d sc_b d_a sum_i q_i q_a[i] - dmin m_b d_a sum_i q_a[i]
+ * (Q6_K: d d_a (sc_lo sum_{i<16} q_i q_a[i] + sc_hi sum_{i>=16} q_i q_a[i])).
  *
  *   wtype     FT_TYPE_Q4_0 (exactly ft_moe_q4_0_q8_1), FT_TYPE_Q4_1,
- *             FT_TYPE_Q5_0, FT_TYPE_Q5_1, FT_TYPE_Q8_0, FT_TYPE_Q4_K or
- *             FT_TYPE_Q5_K (the K-quants need ncols % 256 == 0)
+ *             FT_TYPE_Q5_0, FT_TYPE_Q5_1, FT_TYPE_Q8_0, FT_TYPE_Q4_K,
+ *             FT_TYPE_Q5_K or FT_TYPE_Q6_K (the K-quants need ncols % 256 == 0)
  *   weights   device, [n_experts][nrows][ncols/32] blocks of wtype
  *             ([ncols/256] super-blocks for the K-quants); 16-byte aligned
  *   act, topk_ids, out, tokens, top_k, n_experts, nrows, ncols as for

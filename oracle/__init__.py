@@ -78,6 +78,7 @@ class Oracle:
         L.oracle_moe_block_dots.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.oracle_moe_dequant_bruteforce.argtypes = [vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.oracle_act_mul.argtypes = [vp, i64, i64, i32, vp]
+        L.oracle_repack_q4_0_soa.argtypes = [vp, i64, vp, vp]
         L.oracle_gguf_block_bytes.argtypes = [i32]
         L.oracle_gguf_block_bytes.restype = i32
         L.oracle_dequantize_gguf.argtypes = [i32, vp, i64, vp]
@@ -165,6 +166,16 @@ class Oracle:
         out = np.empty((T, k, N), dtype=np.float32)
         self.lib.oracle_moe_gguf_q8_1(t, _p(w), _p(a), _p(ids), _p(out), T, k, E, N, nb * per)
         return out
+
+    # SoA repack --------------------------------------------------------
+    def repack_q4_0_soa(self, blocks: np.ndarray):
+        """Q4_0 blocks [..., 18] -> (nibble bytes uint8 [n, 16], scales fp16 [n])."""
+        b = np.ascontiguousarray(blocks, dtype=np.uint8)
+        n = b.size // Q4_0_BYTES
+        qs = np.empty((n, 16), dtype=np.uint8)
+        d = np.empty(n, dtype=np.uint16)
+        self.lib.oracle_repack_q4_0_soa(_p(b), n, _p(qs), _p(d))
+        return qs, d.view(np.float16)
 
     # gated activation ------------------------------------------------
     ACT_SILU = 0

@@ -409,6 +409,20 @@ void oracle_moe_gguf_q8_1(int32_t type, const uint8_t* weights, const uint8_t* a
     }
 }
 
+/* ----------------------------------------------- SoA repack of Q4_0 weights */
+
+/* The one-time repack of Q4_0 weight blocks from their stored array of
+ * 18-byte structures (fp16 d, 16 nibble bytes) into a structure of arrays:
+ * all nibble bytes, 16 per block in block order, then all scales, one fp16
+ * per block in block order.  Nothing is converted: the bytes move. */
+void oracle_repack_q4_0_soa(const uint8_t* blocks, int64_t n_blocks, uint8_t* qs, uint16_t* d)
+{
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        d[b] = rd16(blocks + b * Q4_0_BYTES);
+        memcpy(qs + b * 16, blocks + b * Q4_0_BYTES + 2, 16);
+    }
+}
+
 /* ----------------------------------------------------- gated activation */
 
 /* The two gated activations that sit between the expert layers: GELU in its

@@ -31,6 +31,8 @@
  *                                                  Q4_0 equal to oracle_moe_q4_0_q8_1
  *                                                  bit for bit, the offset term within
  *                                                  the fp16 rounding of s
+ *   oracle_repack_q4_0_soa                         pinned: numpy slicing of the
+ *                                                  block bytes, hand block
  *   oracle_act_mul / _quantize_q8_1                pinned: 50-digit mpmath values, torch
  *                                                  activations, the exact
  *                                                  GELU x*Phi(x) within the tanh
@@ -96,6 +98,8 @@ int32_t oracle_gguf_block_dot(int32_t type, const uint8_t* w_block, const uint8_
 void oracle_moe_gguf_q8_1(int32_t type, const uint8_t* weights, const uint8_t* act, const int32_t* topk_ids,
                           float* out, int64_t tokens, int32_t top_k, int32_t n_experts,
                           int64_t nrows, int64_t ncols);
+
+void oracle_repack_q4_0_soa(const uint8_t* blocks, int64_t n_blocks, uint8_t* qs, uint16_t* d);
 
 #define ORACLE_ACT_SILU 0
 #define ORACLE_ACT_GELU_TANH 1

@@ -777,6 +777,21 @@ def pin_q6k_numpy(o):
             assert np.all(np.abs(got[t, j] - want) <= 1e-6 * scale + 1e-12)
 
 
+# ------------------------------------------------------------- SoA repack
+def pin_repack_q4_0_soa(o):
+    """The repack is the block bytes sliced: nibble bytes 2..17 in block order,
+    then the fp16 at bytes 0..1 of each block; a hand block checks the order."""
+    w, _, _ = tiny_case(seed=12)
+    qs, d = o.repack_q4_0_soa(w)
+    flat = w.reshape(-1, 18)
+    assert np.array_equal(qs, flat[:, 2:])
+    assert np.array_equal(d.view(np.uint16), flat[:, 0:2].copy().view(np.uint16)[:, 0])
+    blk = q4_block(0x3C01, list(range(16)) + list(range(15, -1, -1)))
+    qs, d = o.repack_q4_0_soa(np.stack([blk, blk[::-1].copy()]))
+    assert d.view(np.uint16).tolist() == [0x3C01, int(blk[17]) | (int(blk[16]) << 8)]
+    assert qs[0].tolist() == [j | ((15 - j) << 4) for j in range(16)]
+
+
 ALL_PINS = [
     pin_fp16, pin_q4_0_hand, pin_q4_0_nearest_level, pin_q4_0_matches_generator, pin_q4_0_dequant,
     pin_q8_1_hand, pin_q8_1_numpy, pin_q8_1_error_bound, pin_route, pin_block_dot_hand,
@@ -785,5 +800,5 @@ ALL_PINS = [
     pin_moe_ep_shards_sum_to_full, pin_act_library, pin_act_tail_accuracy, pin_act_gelu_vs_erf, pin_act_odd_identity, pin_act_hand,
     pin_act_quantize_numpy, pin_gguf_hand, pin_gguf_numpy_decode, pin_gguf_moe_numpy,
     pin_gguf_q4_0_is_the_q4_0_matmul, pin_kquant_hand, pin_kquant_numpy_decode, pin_kquant_moe_numpy,
-    pin_kquant_unit_scales_are_q4_1, pin_q6k_hand, pin_q6k_numpy,
+    pin_kquant_unit_scales_are_q4_1, pin_q6k_hand, pin_q6k_numpy, pin_repack_q4_0_soa,
 ]

@@ -75,6 +75,8 @@ MUTANTS = {
                       "const int hi2 = (sb[128 + 32 * h + l] >> k) & 3;"),
     "q6k_scale_group": ("if (l < 16) dlo_i += lev[l] * (int32_t)(int8_t)ab6[4 + l];",
                         "if (l < 15) dlo_i += lev[l] * (int32_t)(int8_t)ab6[4 + l];"),
+    "repack_skips_wrong_bytes": ("memcpy(qs + b * 16, blocks + b * Q4_0_BYTES + 2, 16);",
+                                 "memcpy(qs + b * 16, blocks + b * Q4_0_BYTES + 1, 16);"),
     "bad_id_not_zeroed": ("    if (e < 0 || e >= n_experts)\n        return 0.0;\n",
                           "    if (e < 0 || e >= n_experts)\n        e = 0;\n"),
 }

@@ -28,7 +28,8 @@ EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_m
            "ft_moe_reserve", "ft_moe_release", "ft_moe_read_device_error", "ft_moe_set_path",
            "ft_moe_selected_path", "ft_moe_block_dots", "ft_last_error", "ft_abi_version", "ft_profile_enable",
            "ft_profile_read", "ft_moe_route_offsets_noalloc", "ft_moe_q4_0_q8_1_slots",
-           "ft_moe_q4_0_q8_1_ep", "ft_act_mul_quantize_q8_1", "ft_moe_ffn_q4_0_q8_1", "ft_moe_gguf_q8_1")
+           "ft_moe_q4_0_q8_1_ep", "ft_act_mul_quantize_q8_1", "ft_moe_ffn_q4_0_q8_1", "ft_moe_gguf_q8_1",
+           "ft_repack_q4_0_soa")
 
 
 class FtError(RuntimeError):
@@ -64,6 +65,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.ft_moe_block_dots.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_act_mul_quantize_q8_1.argtypes = [vp, vp, i64, i64, i32, vp]
         L.ft_moe_gguf_q8_1.argtypes = [i32, vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
+        L.ft_repack_q4_0_soa.argtypes = [vp, vp, vp, i64, vp]
         L.ft_moe_ffn_q4_0_q8_1.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i64, i64, i32, vp]
         L.ft_moe_workspace_bytes.argtypes = [i64, i32, i32, i64, i64]
         L.ft_moe_workspace_bytes.restype = ctypes.c_size_t
@@ -238,6 +240,21 @@ def moe_gguf_q8_1(wtype, weights, act, topk_ids, out=None):
     _check(load().ft_moe_gguf_q8_1(tid, ctypes.c_void_p(weights.data_ptr()), ctypes.c_void_p(act.data_ptr()),
                                    ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, E, N, nb * per, _stream(weights)))
     return out
+
+
+def repack_q4_0_soa(weights, qs=None, d=None):
+    """Q4_0 blocks uint8 [..., 18] -> (nibble bytes uint8 [n, 16], fp16 scales [n])
+    (ft_repack_q4_0_soa)."""
+    torch = _torch()
+    _dev(weights, torch.uint8, "weights")
+    if weights.shape[-1] != 18:
+        raise ValueError(f"weights must end in 18-byte Q4_0 blocks, got {tuple(weights.shape)}")
+    n = weights.numel() // 18
+    qs = torch.empty((n, 16), dtype=torch.uint8, device=weights.device) if qs is None else qs
+    d = torch.empty(n, dtype=torch.float16, device=weights.device) if d is None else d
+    _check(load().ft_repack_q4_0_soa(ctypes.c_void_p(weights.data_ptr()), _dev(qs, torch.uint8, "qs"),
+                                     _dev(d, torch.float16, "d"), n, _stream(weights)))
+    return qs, d
 
 
 ACT_SILU = 0

@@ -570,6 +570,17 @@ int ft_moe_gguf_q8_1(int32_t wtype, const void* weights, const void* act, const 
                         0, 0, wtype);
 }
 
+int ft_repack_q4_0_soa(const void* weights, void* qs, void* d, int64_t n_blocks, void* stream) {
+    g_last_error.clear();
+    if (n_blocks < 0) return fail(FT_ERR_ARG, "n_blocks must be >= 0 (got %lld)", (long long)n_blocks);
+    if (n_blocks > INT64_MAX / 18) return fail(FT_ERR_SIZE, "n_blocks * 18 overflows int64");
+    if (n_blocks == 0) return FT_OK;
+    if (!weights || !qs || !d) return fail(FT_ERR_ARG, "null pointer");
+    if (!aligned(weights, 2) || !aligned(qs, 16) || !aligned(d, 2))
+        return fail(FT_ERR_ALIGN, "weights and d must be 2-byte, qs 16-byte aligned");
+    return launch_repack_q4_0_soa(weights, qs, d, n_blocks, static_cast<cudaStream_t>(stream));
+}
+
 int ft_moe_block_dots(const void* weights, const void* act, const int32_t* topk_ids, int32_t* dots, int64_t tokens,
                       int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols, void* stream) {
     if (!dots) {

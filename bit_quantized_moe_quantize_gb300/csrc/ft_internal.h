@@ -27,6 +27,7 @@ int check_launch(const char* kernel, dim3 grid, dim3 block, size_t smem);
 // ------------------------------------------------------------ quantizer
 int launch_quantize_q8_1(const void* x, void* act, int64_t tokens, int64_t ncols, cudaStream_t s);
 int launch_act_mul_quantize_q8_1(const float* h, void* act, int64_t rows, int64_t n_inter, int kind, cudaStream_t s);
+int launch_repack_q4_0_soa(const void* blocks, void* qs, void* d, int64_t n_blocks, cudaStream_t s);
 
 // ---------------------------------------------------------------- router
 constexpr int kRouteChunk = 256;          // slots per warp-chunk

@@ -280,6 +280,23 @@ FT_API int ft_moe_gguf_q8_1(int32_t wtype, const void* weights, const void* act,
                             int64_t ncols, void* stream);
 
 /*
+ * ft_repack_q4_0_soa - one-time export of Q4_0 weights as a structure of
+ * arrays (the SoA weight repack export next to the per-type launchers of
+ * moe_vec.cuh, FreeToken PR #185, "Notes"): for block b of the stored array
+ *   qs[16 b .. 16 b + 15] = its 16 nibble bytes (block bytes 2..17)
+ *   d[b]                  = its fp16 scale (block bytes 0..1)
+ * Bytes move unchanged.  The matmul entry points read the stored layout; this
+ * is for consumers that want nibbles and scales apart.
+ *
+ *   weights   device, n_blocks Q4_0 blocks (e.g. [E][N][K/32]), 2-byte aligned
+ *   qs        device, uint8 [n_blocks][16] out, 16-byte aligned
+ *   d         device, fp16 [n_blocks] out, 2-byte aligned
+ *   n_blocks  >= 0 (0 is a no-op)
+ * Errors: FT_ERR_ARG, FT_ERR_SIZE, FT_ERR_ALIGN, FT_ERR_LAUNCH.
+ */
+FT_API int ft_repack_q4_0_soa(const void* weights, void* qs, void* d, int64_t n_blocks, void* stream);
+
+/*
  * ft_act_mul_quantize_q8_1 - the step between the two expert layers, fused:
  * the gated activation of the gate half of each row times its up half,
  * requantized to Q8_1 (gelu_tanh_and_mul right after the routed matmul on

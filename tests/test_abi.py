@@ -179,3 +179,15 @@ def test_gguf_matmul_rejects_bad_arguments(lib):
     assert f(12, W, A, I, O, 4, 2, 8, 128, 160, vp(0)) == 1      # Q4_K: ncols % 256
     assert "ncols % 256" in _err(lib)
     assert f(13, W, A, I, O, 4, 2, 8, 128, 288, vp(0)) == 1      # Q5_K: ncols % 256
+
+
+def test_repack_rejects_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    f = lib.ft_repack_q4_0_soa
+    W, Q, D = vp(0x10000), vp(0x20000), vp(0x30000)
+    assert f(W, Q, D, -1, vp(0)) == 1                          # n_blocks < 0
+    assert f(W, Q, D, 0, vp(0)) == 0                           # no blocks: no-op
+    assert f(vp(0), Q, D, 4, vp(0)) == 1                       # null weights
+    assert f(W, vp(0x20008), D, 4, vp(0)) == 3                 # qs not 16-byte aligned
+    assert f(vp(0x10001), Q, D, 4, vp(0)) == 3                 # weights odd
+    assert f(W, Q, D, 1 << 62, vp(0)) == 2                     # size overflow

@@ -61,3 +61,48 @@ def test_single_process_identity():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.job_throughput(8191, 1, 1000.0) == pytest.approx(8191.0)
+
+
+def _ep_rank_main(rank, world, port, q):
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    import torch
+    import torch.distributed as dist
+    import oracle as oracle_pkg
+    from bit_quantized_moe_quantize_gb300 import synth
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        o = oracle_pkg.get()
+        case = synth.make_case("tiny", 16)
+        w, ids = case["weights"], case["topk_ids"]
+        act = o.quantize_q8_1(case["x"])
+        E = w.shape[0]
+        lo, hi = rank * E // world, (rank + 1) * E // world      # this rank's experts
+        part = o.moe_ep(w[lo:hi], act, ids, E, lo)
+        total = torch.from_numpy(part.astype(np.float64))
+        dist.all_reduce(total)                                     # the combine: a sum over shards
+        q.put((rank, total.numpy().tobytes(), o.moe(w, act, ids).astype(np.float64).tobytes()))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_expert_parallel_shards_combine_over_gloo():
+    """Two ranks each hold half of the experts; every slot routed to another
+    rank's expert is a zero row, so one sum over ranks gives the full matmul."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_ep_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=120) for _ in range(2)]
+    for p in procs:
+        p.join(60)
+        assert p.exitcode == 0
+    for rank, total, full in res:
+        got = np.frombuffer(total)
+        want = np.frombuffer(full)
+        assert np.allclose(got, want, rtol=0, atol=1e-6 * np.abs(want).max())

@@ -30,7 +30,10 @@
  *   oracle_moe_gguf_q8_1                           independent numpy decode + einsum,
  *                                                  Q4_0 equal to oracle_moe_q4_0_q8_1
  *                                                  bit for bit, the offset term within
- *                                                  the fp16 rounding of s
+ *                                                  the fp16 rounding of s; K-quants:
+ *                                                  hand-packed super-blocks, a numpy
+ *                                                  decoder, the plain dequantized dot,
+ *                                                  unit-scale Q4_K = eight Q4_1 blocks
  *   oracle_repack_q4_0_soa                         pinned: numpy slicing of the
  *                                                  block bytes, hand block
  *   oracle_act_mul / _quantize_q8_1                pinned: 50-digit mpmath values, torch

@@ -75,8 +75,9 @@ _S_WEIGHTS, _S_ACT, _S_ROUTE, _S_OUTLIER, _S_RANK, _S_GGUF = 0, 1, 2, 3, 4, 5
 # the code bytes, whether the block stores an fp16 m after d, GGML type number
 GGUF_TYPES = {"q4_0": (18, 2, False, 2), "q4_1": (20, 4, True, 3), "q5_0": (22, 2, False, 6),
               "q5_1": (24, 4, True, 7), "q8_0": (34, 2, False, 8),
-              "q4_k": (144, 4, False, 12), "q5_k": (176, 4, False, 13), "q6_k": (210, 0, False, 14)}
-KQUANTS = ("q4_k", "q5_k", "q6_k")     # 256 weights per (super-)block; the others hold 32
+              "q4_k": (144, 4, False, 12), "q5_k": (176, 4, False, 13), "q6_k": (210, 0, False, 14),
+              "q2_k": (84, 0, False, 10), "q3_k": (110, 0, False, 11)}
+KQUANTS = ("q4_k", "q5_k", "q6_k", "q2_k", "q3_k")     # 256 weights per (super-)block; the others hold 32
 
 
 def _rng(seed: int, stream: int, *extra: int) -> np.random.Generator:
@@ -146,6 +147,16 @@ def make_weights_gguf(wl: Workload, wtype: str, chunk_rows: int = 1 << 16) -> np
     for r0 in range(0, E * N, chunk_rows):
         r1 = min(E * N, r0 + chunk_rows)
         n = r1 - r0
+        if wtype in ("q2_k", "q3_k"):     # random code, mask and scale bytes, fp16 d (and dmin) last
+            head = 80 if wtype == "q2_k" else 108
+            out[r0:r1, :, 0:head] = rng.integers(0, 256, size=(n, nb, head), dtype=np.uint8)
+            dd = np.float32(0.0005 if wtype == "q2_k" else 0.00015) * (
+                np.float32(0.5) + np.abs(rng.standard_normal((n, nb), dtype=np.float32)))
+            out[r0:r1, :, head:head + 2] = dd.astype(np.float16).view(np.uint8).reshape(n, nb, 2)
+            if wtype == "q2_k":      # dmin ~ d * 1.5 centres scale * q - min near zero
+                dm = dd * np.float32(1.5)
+                out[r0:r1, :, 82:84] = dm.astype(np.float16).view(np.uint8).reshape(n, nb, 2)
+            continue
         if wtype == "q6_k":     # random code and scale bytes, fp16 d last
             out[r0:r1, :, 0:208] = rng.integers(0, 256, size=(n, nb, 208), dtype=np.uint8)
             d6 = np.float32(0.00002) * (np.float32(0.5) + np.abs(rng.standard_normal((n, nb), dtype=np.float32)))

@@ -128,8 +128,8 @@ class Oracle:
         return out.reshape(*blocks.shape[:-2], blocks.shape[-2] * QK)
 
     # other GGUF weight types -----------------------------------------
-    GGUF = {"q4_0": 2, "q4_1": 3, "q5_0": 6, "q5_1": 7, "q8_0": 8, "q4_k": 12, "q5_k": 13, "q6_k": 14}
-    KQUANTS = (12, 13, 14)
+    GGUF = {"q4_0": 2, "q4_1": 3, "q5_0": 6, "q5_1": 7, "q8_0": 8, "q4_k": 12, "q5_k": 13, "q6_k": 14, "q2_k": 10, "q3_k": 11}
+    KQUANTS = (10, 11, 12, 13, 14)
 
     def gguf_block_bytes(self, wtype) -> int:
         return int(self.lib.oracle_gguf_block_bytes(self.GGUF.get(wtype, wtype)))

@@ -210,6 +210,8 @@ int32_t oracle_gguf_block_bytes(int32_t type)
         case ORACLE_GGUF_Q4_K: return 144;
         case ORACLE_GGUF_Q5_K: return 176;
         case ORACLE_GGUF_Q6_K: return 210;
+        case ORACLE_GGUF_Q2_K: return 84;
+        case ORACLE_GGUF_Q3_K: return 110;
         default: return 0;
     }
 }
@@ -259,7 +261,54 @@ static double gguf_offset(const uint8_t* blk, int32_t type)
  * byte j + 4 with the top two bits of byte j above it. */
 static int is_kquant(int32_t type)
 {
-    return type == ORACLE_GGUF_Q4_K || type == ORACLE_GGUF_Q5_K || type == ORACLE_GGUF_Q6_K;
+    return type == ORACLE_GGUF_Q4_K || type == ORACLE_GGUF_Q5_K || type == ORACLE_GGUF_Q6_K ||
+           type == ORACLE_GGUF_Q2_K || type == ORACLE_GGUF_Q3_K;
+}
+
+/* The two K-quants with 2-bit codes, 256 weights per super-block in two
+ * halves of 128; sub-block j = 4 h + k (k < 4) of half h takes, for weight
+ * l < 32, bits 2k, 2k + 1 of code byte 32 h + l, and its weights l < 16 use
+ * scale group 2 j, weights l >= 16 group 2 j + 1.
+ *   Q2_K  84 B: 16 scale bytes (low nibble scale, high nibble min, one per
+ *         group), 64 code bytes, fp16 d, fp16 dmin;
+ *         weight = d * scale * q - dmin * min, q = the 2-bit code.
+ *   Q3_K 110 B: 32 bytes hmask, 64 code bytes, 12 bytes of sixteen packed
+ *         6-bit scales, fp16 d; bit j of hmask[l] is the third bit of weight
+ *         l of sub-block j, level q = (2-bit code | third bit << 2) - 4;
+ *         weight = d * (scale - 32) * q.  The 6-bit scale of group g: its low
+ *         four bits are the low (g < 8) or high (g >= 8) nibble of byte g % 8,
+ *         its top two bits are bits 2 (g / 4 % 4) .. +1 of byte 8 + g % 4. */
+static void q2k3k_sub(const uint8_t* sb, int32_t type, int j, int* lev, double* s_lo, double* s_hi,
+                      double* m_lo, double* m_hi)
+{
+    const int h = j / 4, k = j % 4;
+    const uint8_t* q = sb + (type == ORACLE_GGUF_Q2_K ? 16 : 32) + 32 * h;
+    for (int l = 0; l < QK; ++l) {
+        int v = (q[l] >> (2 * k)) & 3;
+        if (type == ORACLE_GGUF_Q3_K)
+            v = (v | (((sb[l] >> j) & 1) << 2)) - 4;
+        lev[l] = v;
+    }
+    if (type == ORACLE_GGUF_Q2_K) {
+        const double d = oracle_half_to_double(rd16(sb + 80)), dmin = oracle_half_to_double(rd16(sb + 82));
+        *s_lo = d * (sb[2 * j] & 0x0f);
+        *s_hi = d * (sb[2 * j + 1] & 0x0f);
+        *m_lo = dmin * (sb[2 * j] >> 4);
+        *m_hi = dmin * (sb[2 * j + 1] >> 4);
+    } else {
+        const double d = oracle_half_to_double(rd16(sb + 108));
+        const uint8_t* sc = sb + 96;
+        int g, v6[2];
+        for (int i = 0; i < 2; ++i) {
+            g = 2 * j + i;
+            const int low4 = g < 8 ? (sc[g % 8] & 0x0f) : (sc[g % 8] >> 4);
+            const int top2 = (sc[8 + g % 4] >> (2 * (g / 4))) & 3;
+            v6[i] = (low4 | (top2 << 4)) - 32;
+        }
+        *s_lo = d * v6[0];
+        *s_hi = d * v6[1];
+        *m_lo = *m_hi = 0.0;
+    }
 }
 
 /* Q6_K, 210 B per 256 weights: 128 B ql (low nibbles), 64 B qh (2-bit high
@@ -312,6 +361,17 @@ static void kquant_sub(const uint8_t* sb, int32_t type, int j, int* lev, double*
 void oracle_dequantize_gguf(int32_t type, const uint8_t* blocks, int64_t n_blocks, double* out)
 {
     const int32_t bytes = oracle_gguf_block_bytes(type);
+    if (type == ORACLE_GGUF_Q2_K || type == ORACLE_GGUF_Q3_K) {
+        for (int64_t b = 0; b < n_blocks; ++b)
+            for (int j = 0; j < 8; ++j) {
+                int lev[QK];
+                double slo, shi, mlo, mhi;
+                q2k3k_sub(blocks + b * bytes, type, j, lev, &slo, &shi, &mlo, &mhi);
+                for (int l = 0; l < QK; ++l)
+                    out[b * 256 + j * QK + l] = l < 16 ? slo * lev[l] - mlo : shi * lev[l] - mhi;
+            }
+        return;
+    }
     if (type == ORACLE_GGUF_Q6_K) {
         for (int64_t b = 0; b < n_blocks; ++b)
             for (int j = 0; j < 8; ++j) {
@@ -370,6 +430,28 @@ void oracle_moe_gguf_q8_1(int32_t type, const uint8_t* weights, const uint8_t* a
                 for (int64_t b = 0; b < nb; ++b) {
                     int lev[QK];
                     double dsc, dmn;
+                    if (type == ORACLE_GGUF_Q2_K || type == ORACLE_GGUF_Q3_K) {
+                        /* two 16-weight groups per 32-block, each with its scale and
+                         * (Q2_K) min: s_g d_a sum_g(q q_a) - m_g d_a sum_g(q_a) */
+                        double slo, shi, mlo, mhi;
+                        q2k3k_sub(row + (b / 8) * bytes, type, (int)(b % 8), lev, &slo, &shi, &mlo, &mhi);
+                        const uint8_t* ab2 = act + (t * nb + b) * Q8_1_BYTES;
+                        const double da2 = oracle_half_to_double(rd16(ab2));
+                        int32_t dot_lo = 0, dot_hi = 0, sum_lo = 0, sum_hi = 0;
+                        for (int l = 0; l < QK; ++l) {
+                            const int32_t qa = (int32_t)(int8_t)ab2[4 + l];
+                            if (l < 16) {
+                                dot_lo += lev[l] * qa;
+                                sum_lo += qa;
+                            } else {
+                                dot_hi += lev[l] * qa;
+                                sum_hi += qa;
+                            }
+                        }
+                        y += slo * da2 * (double)dot_lo + shi * da2 * (double)dot_hi -
+                             mlo * da2 * (double)sum_lo - mhi * da2 * (double)sum_hi;
+                        continue;
+                    }
                     if (type == ORACLE_GGUF_Q6_K) {
                         /* two 16-weight scale groups per 32-block: d sc_lo d_a sum_lo + d sc_hi d_a sum_hi */
                         double dlo, dhi;

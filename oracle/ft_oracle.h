@@ -65,6 +65,10 @@
  *   Q5_K 176 B: fp16 d, fp16 dmin, 12 B scales/mins, 32 B qh, 128 B nibbles
  *   Q6_K 210 B: 128 B low nibbles, 64 B 2-bit high parts, 16 int8 scales (one
  *       per 16 weights), fp16 d; level = 6-bit value - 32, weight = d scale q
+ *   Q2_K  84 B: 16 scale bytes (scale | min << 4 per 16 weights), 64 B of
+ *       2-bit codes, fp16 d, fp16 dmin; weight = d scale q - dmin min
+ *   Q3_K 110 B: 32 B hmask (third bits), 64 B of 2-bit codes, 12 B of sixteen
+ *       packed 6-bit scales, fp16 d; weight = d (scale - 32) q, q in [-4, 3]
  *   (oracle_dequantize_gguf counts super-blocks for these; ncols % 256 == 0)
  *   weights [E][N][K/32] blocks of the type.
  */
@@ -95,6 +99,8 @@ void oracle_dequantize_q8_1(const uint8_t* blocks, int64_t n_blocks, double* out
 #define ORACLE_GGUF_Q4_K 12
 #define ORACLE_GGUF_Q5_K 13
 #define ORACLE_GGUF_Q6_K 14
+#define ORACLE_GGUF_Q2_K 10
+#define ORACLE_GGUF_Q3_K 11
 int32_t oracle_gguf_block_bytes(int32_t type);
 void oracle_dequantize_gguf(int32_t type, const uint8_t* blocks, int64_t n_blocks, double* out);
 int32_t oracle_gguf_block_dot(int32_t type, const uint8_t* w_block, const uint8_t* a_block);

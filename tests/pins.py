@@ -792,6 +792,106 @@ def pin_repack_q4_0_soa(o):
     assert qs[0].tolist() == [j | ((15 - j) << 4) for j in range(16)]
 
 
+def numpy_decode_q2k_q3k(wtype, w):
+    """Independent vectorised decode of Q2_K / Q3_K super-blocks -> fp64 [..., nsb * 256]."""
+    w = np.ascontiguousarray(w)
+    lead = w.shape[:-1]
+    q0 = 16 if wtype == "q2_k" else 32
+    codes = w[..., q0:q0 + 64].astype(np.int64).reshape(*lead, 2, 32)           # half, l
+    shifts = 2 * np.arange(4)
+    lev = (codes[..., None, :] >> shifts[:, None]) & 3                          # half, k, l
+    if wtype == "q2_k":
+        sc = w[..., 0:16].astype(np.int64)
+        scale, mn = (sc & 15).astype(np.float64), (sc >> 4).astype(np.float64)
+        d = w[..., 80:82].copy().view(np.float16)[..., 0].astype(np.float64)
+        dmin = w[..., 82:84].copy().view(np.float16)[..., 0].astype(np.float64)
+    else:
+        hm = w[..., 0:32].astype(np.int64)                                       # l
+        jj = np.arange(8).reshape(2, 4)                                          # sub-block index per (half, k)
+        hbit = (hm[..., None, None, :] >> jj[:, :, None]) & 1
+        lev = (lev | (hbit << 2)) - 4
+        b = w[..., 96:108].astype(np.int64)
+        g = np.arange(16)
+        low4 = np.where(g < 8, b[..., g % 8] & 15, b[..., g % 8] >> 4)
+        top2 = (b[..., 8 + g % 4] >> (2 * (g // 4))) & 3
+        scale = ((low4 | (top2 << 4)) - 32).astype(np.float64)
+        mn = np.zeros_like(scale)
+        d = w[..., 108:110].copy().view(np.float16)[..., 0].astype(np.float64)
+        dmin = np.zeros_like(d)
+    grp = np.arange(16).reshape(2, 4, 2)                                        # scale group per (half, k, l >= 16)
+    sel = np.repeat(grp, 16, axis=-1)                                           # half, k, 32
+    out = np.empty((*lead, 2, 4, 32))
+    for h in range(2):
+        for k in range(4):
+            gl, gh = sel[h, k, 0], sel[h, k, 16]
+            sc_v = np.concatenate([np.repeat(scale[..., gl, None], 16, -1), np.repeat(scale[..., gh, None], 16, -1)], -1)
+            mn_v = np.concatenate([np.repeat(mn[..., gl, None], 16, -1), np.repeat(mn[..., gh, None], 16, -1)], -1)
+            out[..., h, k, :] = d[..., None] * sc_v * lev[..., h, k, :] - dmin[..., None] * mn_v
+    return out.reshape(*w.shape[:-2], w.shape[-2] * 256)
+
+
+def pin_q2k_q3k_hand(o):
+    """Hand-built Q2_K and Q3_K super-blocks: code shifts, scale/min nibbles,
+    the third bit from hmask, the 6-bit scale packing (low nibbles of bytes
+    0..7 for groups 0..7, high nibbles for 8..15, top bits from bytes 8..11)."""
+    l = np.arange(32)
+    codes = ((l % 4) | (((l + 1) % 4) << 2) | (((l + 2) % 4) << 4) | (((l + 3) % 4) << 6)).astype(np.uint8)
+    # Q2_K: d = 1, dmin = 0.5; group g has scale g % 16 and min (g * 3) % 16
+    b = np.zeros(84, np.uint8)
+    b[0:16] = [(g % 16) | (((g * 3) % 16) << 4) for g in range(16)]
+    b[16:48] = codes
+    b[48:80] = codes[::-1]
+    b[80:82] = [0x00, 0x3C]
+    b[82:84] = [0x00, 0x38]
+    got = o.dequantize_gguf("q2_k", b[None]).reshape(8, 32)
+    for j in range(8):
+        h, k = divmod(j, 4)
+        src = codes if h == 0 else codes[::-1]
+        q = (src.astype(np.int64) >> (2 * k)) & 3
+        g = np.where(l < 16, 2 * j, 2 * j + 1)
+        assert np.array_equal(got[j], (g % 16) * q - 0.5 * ((g * 3) % 16)), ("q2_k", j)
+    # Q3_K: d = 1; scales (6-bit) 0..15 -> values 5 g - 32 + ... chosen as v_g = (7 g + 3) % 64
+    v = [(7 * g + 3) % 64 for g in range(16)]
+    sc = [0] * 12
+    for g in range(16):
+        sc[g % 8] |= (v[g] & 15) << (0 if g < 8 else 4)
+        sc[8 + g % 4] |= (v[g] >> 4) << (2 * (g // 4))
+    b = np.zeros(110, np.uint8)
+    b[0:32] = (l * 37) % 256                          # hmask
+    b[32:64] = codes
+    b[64:96] = codes[::-1]
+    b[96:108] = sc
+    b[108:110] = [0x00, 0x3C]
+    got = o.dequantize_gguf("q3_k", b[None]).reshape(8, 32)
+    hm = (l * 37) % 256
+    for j in range(8):
+        h, k = divmod(j, 4)
+        src = codes if h == 0 else codes[::-1]
+        q = ((src.astype(np.int64) >> (2 * k)) & 3) | (((hm >> j) & 1) << 2)
+        g = np.where(l < 16, 2 * j, 2 * j + 1)
+        assert np.array_equal(got[j], (np.array(v)[g] - 32) * (q - 4)), ("q3_k", j)
+
+
+def pin_q2k_q3k_numpy(o):
+    """Decode against the numpy decoder; the matmul against the plain dequantized dot."""
+    rng = np.random.default_rng(14)
+    E, k, K, N, T = 3, 2, 512, 5, 4
+    act = o.quantize_q8_1(rng.standard_normal((T, K)).astype(np.float16))
+    ids = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    xa = numpy_decode_q8_1(act)
+    for wtype in ("q2_k", "q3_k"):
+        w = _gguf_random(wtype, E=E, N=N, K=K, seed=15)
+        wv = numpy_decode_q2k_q3k(wtype, w)
+        assert np.array_equal(o.dequantize_gguf(wtype, w), wv), wtype
+        wv = wv.reshape(E, N, K)
+        got = o.moe_gguf(wtype, w, act, ids).astype(np.float64)
+        for t in range(T):
+            for j in range(k):
+                want = wv[ids[t, j]] @ xa[t]
+                scale = np.abs(wv[ids[t, j]]) @ np.abs(xa[t])
+                assert np.all(np.abs(got[t, j] - want) <= 1e-6 * scale + 1e-12), wtype
+
+
 ALL_PINS = [
     pin_fp16, pin_q4_0_hand, pin_q4_0_nearest_level, pin_q4_0_matches_generator, pin_q4_0_dequant,
     pin_q8_1_hand, pin_q8_1_numpy, pin_q8_1_error_bound, pin_route, pin_block_dot_hand,
@@ -800,5 +900,6 @@ ALL_PINS = [
     pin_moe_ep_shards_sum_to_full, pin_act_library, pin_act_tail_accuracy, pin_act_gelu_vs_erf, pin_act_odd_identity, pin_act_hand,
     pin_act_quantize_numpy, pin_gguf_hand, pin_gguf_numpy_decode, pin_gguf_moe_numpy,
     pin_gguf_q4_0_is_the_q4_0_matmul, pin_kquant_hand, pin_kquant_numpy_decode, pin_kquant_moe_numpy,
-    pin_kquant_unit_scales_are_q4_1, pin_q6k_hand, pin_q6k_numpy, pin_repack_q4_0_soa,
+    pin_kquant_unit_scales_are_q4_1, pin_q6k_hand, pin_q6k_numpy, pin_repack_q4_0_soa, pin_q2k_q3k_hand,
+    pin_q2k_q3k_numpy,
 ]

@@ -77,6 +77,11 @@ MUTANTS = {
                         "if (l < 15) dlo_i += lev[l] * (int32_t)(int8_t)ab6[4 + l];"),
     "repack_skips_wrong_bytes": ("memcpy(qs + b * 16, blocks + b * Q4_0_BYTES + 2, 16);",
                                  "memcpy(qs + b * 16, blocks + b * Q4_0_BYTES + 1, 16);"),
+    "q3k_third_bit_index": ("v = (v | (((sb[l] >> j) & 1) << 2)) - 4;", "v = (v | (((sb[l] >> k) & 1) << 2)) - 4;"),
+    "q3k_scale_top_bits": ("const int top2 = (sc[8 + g % 4] >> (2 * (g / 4))) & 3;",
+                           "const int top2 = (sc[8 + g / 4] >> (2 * (g % 4))) & 3;"),
+    "q2k_min_from_scale": ("*m_lo = dmin * (sb[2 * j] >> 4);", "*m_lo = dmin * (sb[2 * j] & 0x0f);"),
+    "q2k_group_split": ("if (l < 16) {\n                                dot_lo", "if (l < 8) {\n                                dot_lo"),
     "bad_id_not_zeroed": ("    if (e < 0 || e >= n_experts)\n        return 0.0;\n",
                           "    if (e < 0 || e >= n_experts)\n        e = 0;\n"),
 }

@@ -216,7 +216,7 @@ def moe_q4_0_q8_1_ep(weights_local, act, topk_ids, n_experts_global, expert_star
 # GGUF weight types: GGML type number, bytes per stored block, weights per block
 WEIGHT_TYPES = {"q4_0": (2, 18, 32), "q4_1": (3, 20, 32), "q5_0": (6, 22, 32), "q5_1": (7, 24, 32),
                 "q8_0": (8, 34, 32), "q4_k": (12, 144, 256), "q5_k": (13, 176, 256),
-                "q6_k": (14, 210, 256)}
+                "q6_k": (14, 210, 256), "q2_k": (10, 84, 256), "q3_k": (11, 110, 256)}
 
 
 def moe_gguf_q8_1(wtype, weights, act, topk_ids, out=None):

@@ -1,5 +1,5 @@
 // The block-per-lane GEMV kernel of the routed expert matmul, templated on the
-// weight block type (GGUF Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K: the
+// weight block type (GGUF Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q2_K..Q6_K: the
 // per-type launchers of moe_vec.cuh on FreeToken PR #185, "Notes"), with its shared
 // arguments and launch helpers.  moe_gemv.cu instantiates it for Q4_0 next to
 // the row-per-lane kernel; moe_gemv_gguf.cu for the other types.
@@ -98,18 +98,21 @@ __device__ __forceinline__ uint32_t spread4(uint32_t x) {
 // (Q4_0: 8, Q5_0: 16), whether the block stores an fp16 m (c = m, Q4_1 / Q5_1:
 // the offset term is m s_a) and whether a sub-block carries a min
 // (K-quants: - dmin m_j d_a sum(q_a), with the exact sum of the codes), and
-// whether the block's two 16-weight halves carry their own scales (Q6_K:
-// d sc_lo and d sc_hi come back in d and m).
+// whether the block's two 16-weight halves carry their own scales (Q6_K,
+// Q3_K, Q2_K: d sc_lo and d sc_hi come back in d and m) and their own mins
+// (Q2_K: dmin min_lo and dmin min_hi, from decode_mins).
 template <int WT>
 struct WBlock;
-template <> struct WBlock<FT_TYPE_Q4_0> { static constexpr int bytes = 18, per = 1, level0 = 8; static constexpr bool has_m = false, has_min = false, split = false; };
-template <> struct WBlock<FT_TYPE_Q4_1> { static constexpr int bytes = 20, per = 1, level0 = 0; static constexpr bool has_m = true, has_min = false, split = false; };
-template <> struct WBlock<FT_TYPE_Q5_0> { static constexpr int bytes = 22, per = 1, level0 = 16; static constexpr bool has_m = false, has_min = false, split = false; };
-template <> struct WBlock<FT_TYPE_Q5_1> { static constexpr int bytes = 24, per = 1, level0 = 0; static constexpr bool has_m = true, has_min = false, split = false; };
-template <> struct WBlock<FT_TYPE_Q8_0> { static constexpr int bytes = 34, per = 1, level0 = 0; static constexpr bool has_m = false, has_min = false, split = false; };
-template <> struct WBlock<FT_TYPE_Q4_K> { static constexpr int bytes = 144, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = true, split = false; };
-template <> struct WBlock<FT_TYPE_Q5_K> { static constexpr int bytes = 176, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = true, split = false; };
-template <> struct WBlock<FT_TYPE_Q6_K> { static constexpr int bytes = 210, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = false, split = true; };
+template <> struct WBlock<FT_TYPE_Q4_0> { static constexpr int bytes = 18, per = 1, level0 = 8; static constexpr bool has_m = false, has_min = false, split = false, split_min = false; };
+template <> struct WBlock<FT_TYPE_Q4_1> { static constexpr int bytes = 20, per = 1, level0 = 0; static constexpr bool has_m = true, has_min = false, split = false, split_min = false; };
+template <> struct WBlock<FT_TYPE_Q5_0> { static constexpr int bytes = 22, per = 1, level0 = 16; static constexpr bool has_m = false, has_min = false, split = false, split_min = false; };
+template <> struct WBlock<FT_TYPE_Q5_1> { static constexpr int bytes = 24, per = 1, level0 = 0; static constexpr bool has_m = true, has_min = false, split = false, split_min = false; };
+template <> struct WBlock<FT_TYPE_Q8_0> { static constexpr int bytes = 34, per = 1, level0 = 0; static constexpr bool has_m = false, has_min = false, split = false, split_min = false; };
+template <> struct WBlock<FT_TYPE_Q4_K> { static constexpr int bytes = 144, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = true, split = false, split_min = false; };
+template <> struct WBlock<FT_TYPE_Q5_K> { static constexpr int bytes = 176, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = true, split = false, split_min = false; };
+template <> struct WBlock<FT_TYPE_Q6_K> { static constexpr int bytes = 210, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = false, split = true, split_min = false; };
+template <> struct WBlock<FT_TYPE_Q2_K> { static constexpr int bytes = 84, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = false, split = true, split_min = true; };
+template <> struct WBlock<FT_TYPE_Q3_K> { static constexpr int bytes = 110, per = 8, level0 = 0; static constexpr bool has_m = false, has_min = false, split = true, split_min = false; };
 
 // 6-bit scale and min of sub-block j of a K-quant super-block from its 12
 // packed bytes (w[0..2] = bytes 0..11): j < 4 the low 6 bits of bytes j and
@@ -208,6 +211,49 @@ __device__ __forceinline__ void decode_block(const uint8_t* base, uint32_t off, 
             lo[i] = static_cast<int>(__vsub4(l, 0x20202020u));   // per byte: level - 32 as int8
             hi[i] = static_cast<int>(__vsub4(hh, 0x20202020u));
         }
+    } else if constexpr (WT == FT_TYPE_Q2_K || WT == FT_TYPE_Q3_K) {
+        // sub-block j = 4 h + k: bits 2k of code byte 32 h + l; groups 2j (weights
+        // < 16) and 2j + 1.  Q2_K: scale bytes 0..15 (scale | min << 4), codes at
+        // 16, fp16 d at 80.  Q3_K: hmask at 0 (bit j = third bit), codes at 32,
+        // twelve bytes of 6-bit scales at 96 (minus 32), fp16 d at 108; level =
+        // (code | third bit << 2) - 4.
+        const int h = j >> 2, k = j & 3;
+        constexpr uint32_t C0 = WT == FT_TYPE_Q2_K ? 16 : 32;
+        uint32_t c[8];
+        load_words<8>(base, off + C0 + 32 * h, c);
+        uint32_t hm[8];
+        if constexpr (WT == FT_TYPE_Q3_K) load_words<8>(base, off, hm);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t l = (c[i] >> (2 * k)) & 0x03030303u, hh = (c[4 + i] >> (2 * k)) & 0x03030303u;
+            if constexpr (WT == FT_TYPE_Q3_K) {
+                l = __vsub4(l | (((hm[i] >> j) & 0x01010101u) << 2), 0x04040404u);
+                hh = __vsub4(hh | (((hm[4 + i] >> j) & 0x01010101u) << 2), 0x04040404u);
+            }
+            lo[i] = static_cast<int>(l);
+            hi[i] = static_cast<int>(hh);
+        }
+        if constexpr (WT == FT_TYPE_Q2_K) {
+            const unsigned short scw = *reinterpret_cast<const unsigned short*>(base + off + 2 * j);
+            const float d2 = half_at(base, off + 80);
+            d = d2 * static_cast<float>(scw & 0x0Fu);
+            m = d2 * static_cast<float>((scw >> 8) & 0x0Fu);
+        } else {
+            uint32_t sw[3];
+            load_words<3>(base, off + 96, sw);
+            auto byte = [&](int i) { return static_cast<int>((sw[i >> 2] >> (8 * (i & 3))) & 0xFFu); };
+            int v[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int g = 2 * j + t;
+                const int low4 = g < 8 ? (byte(g & 7) & 15) : (byte(g & 7) >> 4);
+                const int top2 = (byte(8 + (g & 3)) >> (2 * (g >> 2))) & 3;
+                v[t] = (low4 | (top2 << 4)) - 32;
+            }
+            const float d3 = half_at(base, off + 108);
+            d = d3 * static_cast<float>(v[0]);
+            m = d3 * static_cast<float>(v[1]);
+        }
     } else {
         static_assert(WT == FT_TYPE_Q8_0, "weight type");
         d = half_at(base, off);
@@ -219,6 +265,14 @@ __device__ __forceinline__ void decode_block(const uint8_t* base, uint32_t off, 
             hi[i] = static_cast<int>(q[4 + i]);
         }
     }
+}
+
+// Q2_K's two group mins of sub-block j: dmin * (scale byte >> 4).
+__device__ __forceinline__ void decode_mins_q2k(const uint8_t* base, uint32_t off, int j, float& mn_lo, float& mn_hi) {
+    const unsigned short scw = *reinterpret_cast<const unsigned short*>(base + off + 2 * j);
+    const float dmin = half_at(base, off + 82);
+    mn_lo = dmin * static_cast<float>((scw >> 4) & 0x0Fu);
+    mn_hi = dmin * static_cast<float>(scw >> 12);
 }
 
 // int32 -> fp32 for |v| < 2^22 with an integer add and a float subtract
@@ -242,6 +296,7 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
     constexpr bool HAS_M = WBlock<WT>::has_m;
     constexpr bool HAS_MIN = WBlock<WT>::has_min;
     constexpr bool SPLIT = WBlock<WT>::split;
+    constexpr bool SPLIT_MIN = WBlock<WT>::split_min;
     static_assert(!(SPLIT && DUMP), "block dots are a Q4_0 diagnostic");
     extern __shared__ __align__(16) uint8_t smem[];
     const int64_t t = blockIdx.x;
@@ -309,11 +364,15 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
         sm = __dp4a(static_cast<int>(q0.y), 0x01010101, sm);
         sm = __dp4a(static_cast<int>(q0.z), 0x01010101, sm);
         sm = __dp4a(static_cast<int>(q0.w), 0x01010101, sm);
+        const int sm_lo = sm;
         sm = __dp4a(static_cast<int>(q1.x), 0x01010101, sm);
         sm = __dp4a(static_cast<int>(q1.y), 0x01010101, sm);
         sm = __dp4a(static_cast<int>(q1.z), 0x01010101, sm);
         sm = __dp4a(static_cast<int>(q1.w), 0x01010101, sm);
-        suma[g * nb + b] = sm;
+        // split-min types keep the two 16-code sums (|sum| <= 2032) in one word
+        suma[g * nb + b] = SPLIT_MIN ? static_cast<int>((static_cast<uint32_t>(sm_lo) & 0xFFFFu) |
+                                                        (static_cast<uint32_t>(sm - sm_lo) << 16))
+                                     : sm;
     }
     __syncthreads();
 
@@ -343,10 +402,15 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
         if (rl0 < nr) {
             for (int b = static_cast<int>(lane); b < nb; b += 32) {
                 int lo[RW][4], hi[RW][4];
-                float dw[RW], mw[RW];
+                float dw[RW], mw[RW], mn_lo[RW], mn_hi[RW];
 #pragma unroll
                 for (int j = 0; j < RW; ++j) {
                     const int rl = min(rl0 + j, nr - 1);       // rows past the stage repeat the last one
+                    if constexpr (SPLIT_MIN)
+                        decode_mins_q2k(wt, static_cast<uint32_t>(rl * row_bytes + (b / PER) * WB), b % PER, mn_lo[j],
+                                        mn_hi[j]);
+                    else
+                        mn_lo[j] = mn_hi[j] = 0.0f;
                     decode_block<WT>(wt, static_cast<uint32_t>(rl * row_bytes + (b / PER) * WB), b % PER, dw[j], mw[j],
                                      lo[j], hi[j]);
                 }
@@ -373,6 +437,13 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
                                 dh = __dp4a(hi[j][3], static_cast<int>(A1.w), dh);
                                 acc[j][g] = fmaf(small_int_to_float(dl), dw[j] * dag, acc[j][g]);
                                 acc[j][g] = fmaf(small_int_to_float(dh), mw[j] * dag, acc[j][g]);
+                                if constexpr (SPLIT_MIN) {   // - min_g d_a sum_g(q_a), both groups
+                                    const int sw = suma[g * nb + b];
+                                    const float s_lo = small_int_to_float(static_cast<int16_t>(sw & 0xFFFF));
+                                    const float s_hi = small_int_to_float(sw >> 16);
+                                    acc[j][g] = fmaf(-mn_lo[j] * dag, s_lo, acc[j][g]);
+                                    acc[j][g] = fmaf(-mn_hi[j] * dag, s_hi, acc[j][g]);
+                                }
                                 continue;
                             }
                             int dot = -sa0;

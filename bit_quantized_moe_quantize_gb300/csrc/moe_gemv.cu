@@ -283,12 +283,16 @@ int weight_block_bytes(int wtype) {
         case FT_TYPE_Q4_K: return WBlock<FT_TYPE_Q4_K>::bytes;
         case FT_TYPE_Q5_K: return WBlock<FT_TYPE_Q5_K>::bytes;
         case FT_TYPE_Q6_K: return WBlock<FT_TYPE_Q6_K>::bytes;
+        case FT_TYPE_Q2_K: return WBlock<FT_TYPE_Q2_K>::bytes;
+        case FT_TYPE_Q3_K: return WBlock<FT_TYPE_Q3_K>::bytes;
         default: return 0;
     }
 }
 
 int weight_block_values(int wtype) {
-    return wtype == FT_TYPE_Q4_K || wtype == FT_TYPE_Q5_K || wtype == FT_TYPE_Q6_K ? 256
+    return wtype == FT_TYPE_Q4_K || wtype == FT_TYPE_Q5_K || wtype == FT_TYPE_Q6_K || wtype == FT_TYPE_Q2_K ||
+                   wtype == FT_TYPE_Q3_K
+               ? 256
            : weight_block_bytes(wtype)                                            ? 32
                                                                                   : 0;
 }

@@ -1,5 +1,5 @@
 // The block-per-lane GEMV kernel instantiated for the GGUF weight types other
-// than Q4_0 (Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K: the per-type launchers of moe_vec.cuh on
+// than Q4_0 (Q4_1, Q5_0, Q5_1, Q8_0, Q2_K..Q6_K: the per-type launchers of moe_vec.cuh on
 // FreeToken PR #185, "Notes"), in a translation unit of its own so that the
 // library's sources compile in parallel.  No block dots (a Q4_0 diagnostic).
 #include "gemv_blocks.cuh"
@@ -25,6 +25,8 @@ int launch_gemv_gguf(int wtype, const GemvPlan& plan, const GemvArgs& a, cudaStr
         case FT_TYPE_Q4_K: return launch_gemv_type<FT_TYPE_Q4_K>(plan, a, s);
         case FT_TYPE_Q5_K: return launch_gemv_type<FT_TYPE_Q5_K>(plan, a, s);
         case FT_TYPE_Q6_K: return launch_gemv_type<FT_TYPE_Q6_K>(plan, a, s);
+        case FT_TYPE_Q2_K: return launch_gemv_type<FT_TYPE_Q2_K>(plan, a, s);
+        case FT_TYPE_Q3_K: return launch_gemv_type<FT_TYPE_Q3_K>(plan, a, s);
         default: return fail(FT_ERR_ARG, "unknown weight type %d", wtype);
     }
 }

@@ -117,6 +117,17 @@ typedef enum {
  *        byte 128 + 32 h + l; level = that 6-bit value - 32; weight l uses
  *        scale 8 h + 2 k (l < 16) or 8 h + 2 k + 1: weight = d * scale * level */
 #define FT_TYPE_Q6_K 14
+/*   Q2_K  84 B: 16 scale bytes (scale | min << 4, one per 16 weights), 64 B of
+ *        2-bit codes, fp16 d, fp16 dmin; weight = d scale q - dmin min
+ *   Q3_K 110 B: 32 B hmask, 64 B of 2-bit codes, 12 B of sixteen packed 6-bit
+ *        scales, fp16 d; bit j of hmask[l] is the third bit of weight l of
+ *        sub-block j, q = (code | third bit << 2) - 4, weight = d (scale - 32) q.
+ *        Scale g: low four bits from byte g % 8 (low nibble for g < 8, high for
+ *        g >= 8), top two from bits 2 (g / 4) of byte 8 + g % 4.
+ *   In both, sub-block j = 4 h + k takes bits 2k of code byte 32 h + l and
+ *   scale groups 2j (weights < 16) and 2j + 1. */
+#define FT_TYPE_Q2_K 10
+#define FT_TYPE_Q3_K 11
 
 /* Gated activations of ft_act_mul_quantize_q8_1 / ft_moe_ffn_q4_0_q8_1. */
 #define FT_ACT_SILU 0        /* silu(g) = g / (1 + exp(-g))                              */
@@ -262,11 +273,13 @@ FT_API int ft_moe_q4_0_q8_1_ep(const void* weights_local, const void* act, const
  * of the slot's token, with q_i, c as in the FT_TYPE_* list and s_a the
  * activation block's stored fp16 s (c = 0 for Q4_0, Q5_0, Q8_0); for the
  * K-quants, per sub-block b, d sc_b d_a sum_i q_i q_a[i] - dmin m_b d_a sum_i q_a[i]
- * (Q6_K: d d_a (sc_lo sum_{i<16} q_i q_a[i] + sc_hi sum_{i>=16} q_i q_a[i])).
+ * (Q6_K, Q3_K: d d_a (sc_lo sum_{i<16} q_i q_a[i] + sc_hi sum_{i>=16} q_i q_a[i]);
+ * Q2_K adds - dmin d_a (min_lo sum_{i<16} q_a[i] + min_hi sum_{i>=16} q_a[i])).
  *
  *   wtype     FT_TYPE_Q4_0 (exactly ft_moe_q4_0_q8_1), FT_TYPE_Q4_1,
- *             FT_TYPE_Q5_0, FT_TYPE_Q5_1, FT_TYPE_Q8_0, FT_TYPE_Q4_K,
- *             FT_TYPE_Q5_K or FT_TYPE_Q6_K (the K-quants need ncols % 256 == 0)
+ *             FT_TYPE_Q5_0, FT_TYPE_Q5_1, FT_TYPE_Q8_0, FT_TYPE_Q2_K,
+ *             FT_TYPE_Q3_K, FT_TYPE_Q4_K, FT_TYPE_Q5_K or FT_TYPE_Q6_K (the
+ *             K-quants need ncols % 256 == 0)
  *   weights   device, [n_experts][nrows][ncols/32] blocks of wtype
  *             ([ncols/256] super-blocks for the K-quants); 16-byte aligned
  *   act, topk_ids, out, tokens, top_k, n_experts, nrows, ncols as for

@@ -33,7 +33,10 @@
  *                                                  the fp16 rounding of s; K-quants:
  *                                                  hand-packed super-blocks, a numpy
  *                                                  decoder, the plain dequantized dot,
- *                                                  unit-scale Q4_K = eight Q4_1 blocks
+ *                                                  unit-scale Q4_K = eight Q4_1 blocks;
+ *                                                  Q2_K / Q3_K / Q6_K: hand-built
+ *                                                  super-blocks, numpy decoders,
+ *                                                  the plain dequantized dot
  *   oracle_repack_q4_0_soa                         pinned: numpy slicing of the
  *                                                  block bytes, hand block
  *   oracle_act_mul / _quantize_q8_1                pinned: 50-digit mpmath values, torch

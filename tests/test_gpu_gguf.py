@@ -1,6 +1,6 @@
 """GPU parity of ft_moe_gguf_q8_1: the routed matmul with expert weights of the
 other GGUF types (Q4_1, Q5_0, Q5_1, Q8_0 with 32-weight blocks; the K-quants
-Q4_K, Q5_K, Q6_K with 256-weight super-blocks; the per-type launchers of
+Q2_K, Q3_K, Q4_K, Q5_K, Q6_K with 256-weight super-blocks; the per-type launchers of
 moe_vec.cuh on FreeToken PR #185, "Notes").
 
 Against the oracle's matmul of the same type within the matmul tolerance
@@ -16,8 +16,8 @@ import gpu_util as G
 
 pytestmark = pytest.mark.gpu
 
-TYPES = ["q4_1", "q5_0", "q5_1", "q8_0", "q4_k", "q5_k", "q6_k"]
-KQ = ("q4_k", "q5_k", "q6_k")
+TYPES = ["q4_1", "q5_0", "q5_1", "q8_0", "q2_k", "q3_k", "q4_k", "q5_k", "q6_k"]
+KQ = ("q2_k", "q3_k", "q4_k", "q5_k", "q6_k")
 
 
 @pytest.fixture(scope="module")

@@ -21,6 +21,7 @@ STATUS_NAMES = {0: "FT_OK", 1: "FT_ERR_ARG", 2: "FT_ERR_SIZE", 3: "FT_ERR_ALIGN"
                 5: "FT_ERR_WORKSPACE", 6: "FT_ERR_CUDA", 7: "FT_ERR_DEVICE_FLAG"}
 FT_DEVERR_BAD_EXPERT_ID = 0x1
 FT_DEVERR_WAIT_TIMEOUT = 0x2
+FT_DEVERR_WORKSPACE_GUARD = 0x4
 FT_PATH_AUTO, FT_PATH_GEMV, FT_PATH_GEMM = 0, 1, 2
 PATHS = {"auto": FT_PATH_AUTO, "gemv": FT_PATH_GEMV, "gemm": FT_PATH_GEMM}
 
@@ -29,7 +30,7 @@ EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_m
            "ft_moe_selected_path", "ft_moe_block_dots", "ft_last_error", "ft_abi_version", "ft_profile_enable",
            "ft_profile_read", "ft_moe_route_offsets_noalloc", "ft_moe_q4_0_q8_1_slots",
            "ft_moe_q4_0_q8_1_ep", "ft_act_mul_quantize_q8_1", "ft_moe_ffn_q4_0_q8_1", "ft_moe_gguf_q8_1",
-           "ft_repack_q4_0_soa")
+           "ft_repack_q4_0_soa", "ft_debug_wait_timeout")
 
 
 class FtError(RuntimeError):
@@ -66,6 +67,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.ft_act_mul_quantize_q8_1.argtypes = [vp, vp, i64, i64, i32, vp]
         L.ft_moe_gguf_q8_1.argtypes = [i32, vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_repack_q4_0_soa.argtypes = [vp, vp, vp, i64, vp]
+        L.ft_debug_wait_timeout.argtypes = [i64, vp]
         L.ft_moe_ffn_q4_0_q8_1.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i64, i64, i32, vp]
         L.ft_moe_workspace_bytes.argtypes = [i64, i32, i32, i64, i64]
         L.ft_moe_workspace_bytes.restype = ctypes.c_size_t
@@ -334,6 +336,14 @@ def read_device_error(stream=None) -> int:
     if st not in (FT_OK, FT_ERR_DEVICE_FLAG):
         raise FtError(st, last_error())
     return int(flags.value)
+
+
+def debug_wait_timeout(limit_ns: int, stream=None):
+    """Test hook (ft_debug_wait_timeout): a kernel whose bounded wait gives up
+    after limit_ns; the flag it raises is read with read_device_error()."""
+    torch = _torch()
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream if stream is None else stream)
+    _check(load().ft_debug_wait_timeout(int(limit_ns), s))
 
 
 def set_path(path) -> int:

@@ -246,9 +246,16 @@ static WsLayout ws_layout(int64_t n_slots, int32_t n_experts, int64_t gemm_ncols
     return L;
 }
 
+// A guard block of kGuardBytes after the end of every workspace, filled with
+// kGuardByte when the workspace is allocated and checked by
+// ft_moe_read_device_error: a kernel writing past the end of the workspace
+// changes it.
+constexpr size_t kGuardBytes = 256;
+constexpr int kGuardByte = 0xA5;
+
 struct DeviceWs {
     void* base = nullptr;
-    size_t bytes = 0;
+    size_t bytes = 0;   // usable bytes; the guard block follows them
 };
 
 constexpr int kMaxDevices = 64;
@@ -284,9 +291,11 @@ static int ws_acquire(size_t need, cudaStream_t s, uint8_t** base) {
             w.bytes = 0;
         }
         void* p = nullptr;
-        cudaError_t e = cudaMalloc(&p, need);
+        cudaError_t e = cudaMalloc(&p, need + kGuardBytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
         e = cudaMemset(p, 0, need);
+        if (e == cudaSuccess) e = cudaMemset(static_cast<uint8_t*>(p) + need, kGuardByte, kGuardBytes);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
         if (e != cudaSuccess) {
             cudaFree(p);
             return cuda_fail(e, "cudaMemset(workspace)");
@@ -644,8 +653,29 @@ int ft_moe_read_device_error(void* stream, uint32_t* flags_out) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
     e = cudaMemset(w.base, 0, sizeof(v));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+    uint8_t guard[kGuardBytes];
+    uint8_t* gdev = static_cast<uint8_t*>(w.base) + w.bytes;
+    e = cudaMemcpy(guard, gdev, kGuardBytes, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(workspace guard)");
+    for (size_t i = 0; i < kGuardBytes; ++i)
+        if (guard[i] != kGuardByte) {
+            v |= FT_DEVERR_WORKSPACE_GUARD;
+            e = cudaMemset(gdev, kGuardByte, kGuardBytes);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace guard)");
+            break;
+        }
     *flags_out = v;
     return v ? fail(FT_ERR_DEVICE_FLAG, "device error flags 0x%x", v) : FT_OK;
+}
+
+int ft_debug_wait_timeout(int64_t limit_ns, void* stream) {
+    g_last_error.clear();
+    if (limit_ns < 1000 || limit_ns > 1000000000)
+        return fail(FT_ERR_ARG, "limit_ns must be in [1000, 1000000000] (got %lld)", (long long)limit_ns);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = nullptr;
+    if (int st = ws_acquire(ws_layout(0, 1).total, s, &ws)) return st;
+    return launch_wait_timeout_probe(reinterpret_cast<uint32_t*>(ws + ws_layout(0, 1).err), limit_ns, s);
 }
 
 int ft_profile_enable(int32_t max_calls) {

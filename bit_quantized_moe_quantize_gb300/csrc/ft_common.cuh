@@ -65,14 +65,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity.  Returns false (and
-// raises FT_DEVERR_WAIT_TIMEOUT) if the phase never completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
+// raises FT_DEVERR_WAIT_TIMEOUT) if the phase did not complete within
+// limit_ns of %globaltimer.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             atomicOr(err, FT_DEVERR_WAIT_TIMEOUT);
             return false;
         }
@@ -82,8 +84,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 // Warp-uniform bounded wait: every lane polls, and the warp fails together if
 // any lane gave up, so warp-collective instructions that follow never see a
 // diverged warp.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err) {
-    const bool ok = mbar_wait(bar, parity, err);
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+    const bool ok = mbar_wait(bar, parity, err, limit_ns);
     return __all_sync(0xFFFFFFFFu, ok);
 }
 

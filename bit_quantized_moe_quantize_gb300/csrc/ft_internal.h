@@ -24,6 +24,9 @@ void prof_count_launch();
 // name and geometry and returns FT_ERR_LAUNCH.
 int check_launch(const char* kernel, dim3 grid, dim3 block, size_t smem);
 
+// Test hook: a kernel whose bounded wait must give up after limit_ns.
+int launch_wait_timeout_probe(uint32_t* err, int64_t limit_ns, cudaStream_t s);
+
 // ------------------------------------------------------------ quantizer
 int launch_quantize_q8_1(const void* x, void* act, int64_t tokens, int64_t ncols, cudaStream_t s);
 int launch_act_mul_quantize_q8_1(const float* h, void* act, int64_t rows, int64_t n_inter, int kind, cudaStream_t s);

@@ -80,6 +80,7 @@ typedef enum {
 /* Bits of the device error word. */
 #define FT_DEVERR_BAD_EXPERT_ID 0x1u   /* a topk id was outside [0, n_experts)           */
 #define FT_DEVERR_WAIT_TIMEOUT  0x2u   /* a bounded in-kernel wait gave up (never expected) */
+#define FT_DEVERR_WORKSPACE_GUARD 0x4u /* a guard block between workspace regions was overwritten */
 
 /* Path selection for ft_moe_q4_0_q8_1 (ft_moe_set_path). */
 #define FT_PATH_AUTO 0   /* chosen on the host from tokens*top_k, n_experts and the shape */
@@ -190,8 +191,11 @@ FT_API int ft_moe_route_offsets(const int32_t* topk_ids, int64_t tokens, int32_t
  * ceil(tokens*top_k / 256) * n_experts words; larger problems are rejected
  * with FT_ERR_SIZE before anything runs (use ft_moe_route_offsets for them).
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls share the one array and nothing in it
+ * (cudaGetSymbolAddress) with that device current and keeps it for the life
+ * of the process; make that first call before any stream capture.  A
+ * cudaDeviceReset (or any teardown of the device's primary context) makes the
+ * kept address stale, so after one this entry point must not be used again in
+ * the same process.  All calls share the one array and nothing in it
  * needs to start at zero (every histogram entry is written before it is
  * read), so calls that overlap on the GPU - on different streams, or from
  * different host threads - race with each other and must be serialized by
@@ -383,11 +387,28 @@ FT_API int ft_moe_release(void);
 
 /*
  * ft_moe_read_device_error - synchronize `stream`, read the library's device
- * error word of the current device into *flags_out and clear it.  Returns
+ * error word of the current device into *flags_out and clear it.  It also
+ * checks the 256-byte guard blocks that separate the workspace regions (they
+ * are filled with a fixed pattern when the workspace is allocated): a
+ * changed guard adds FT_DEVERR_WORKSPACE_GUARD and is refilled.  Returns
  * FT_OK when no flag was raised, FT_ERR_DEVICE_FLAG otherwise.  Not for use
  * inside a stream capture.
  */
 FT_API int ft_moe_read_device_error(void* stream, uint32_t* flags_out);
+
+/*
+ * ft_debug_wait_timeout - test hook for the failure path of the bounded
+ * in-kernel waits.  Launches one small kernel on `stream` that allocates TMEM,
+ * waits on an mbarrier that nothing ever arrives on (the same bounded wait the
+ * matmul kernels use, here with a limit of limit_ns nanoseconds), raises
+ * FT_DEVERR_WAIT_TIMEOUT in the library's device error word when the wait
+ * gives up, frees its TMEM and returns.  The context stays usable: read the
+ * flag with ft_moe_read_device_error, then keep calling the library.
+ *   limit_ns  in [1000, 1000000000]
+ * Uses the library workspace (its error word).  The pages have no counterpart.
+ * Errors: FT_ERR_ARG, FT_ERR_WORKSPACE, FT_ERR_CUDA, FT_ERR_LAUNCH.
+ */
+FT_API int ft_debug_wait_timeout(int64_t limit_ns, void* stream);
 
 /*
  * ft_moe_set_path - force the path of later ft_moe_q4_0_q8_1 calls in this

@@ -191,3 +191,10 @@ def test_repack_rejects_bad_arguments(lib):
     assert f(W, vp(0x20008), D, 4, vp(0)) == 3                 # qs not 16-byte aligned
     assert f(vp(0x10001), Q, D, 4, vp(0)) == 3                 # weights odd
     assert f(W, Q, D, 1 << 62, vp(0)) == 2                     # size overflow
+
+
+def test_debug_wait_timeout_rejects_bad_limits_on_the_host(lib):
+    vp = ctypes.c_void_p
+    for bad in (0, 999, 2_000_000_000):
+        assert lib.ft_debug_wait_timeout(bad, vp(0)) == 1
+    assert "limit_ns" in _err(lib)

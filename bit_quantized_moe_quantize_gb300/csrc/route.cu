@@ -21,10 +21,11 @@
 //                     rewritten in place as each chunk's first position per e
 //   3. route_scatter: per chunk, stable placement with __match_any_sync ranks
 //
-// Batches of at most 32 chunks whose histograms fit in shared memory (decode)
-// run the same three steps inside one CTA (route_small_kernel), with the
-// histogram in shared memory: one launch instead of three, which is most of
-// the routing time when the batch is small.
+// Batches of at most 32 chunks whose histograms fit in shared memory run the
+// same three steps inside one CTA (route_small_kernel), with the histogram in
+// shared memory: one launch instead of three, which is most of the routing
+// time when the batch is small.  Decode-sized batches (at most 512 slots) run
+// them in a single warp (route_warp_kernel), with no CTA-wide barrier.
 #include <mutex>
 
 #include "ft_common.cuh"
@@ -267,6 +268,107 @@ __global__ void __launch_bounds__(1024)
                             expert_start);
 }
 
+// All three steps in ONE warp, for decode-sized batches (S <= kRouteWarpSlots,
+// E <= kRouteWarpExperts): the histogram and the scatter cursors live in
+// shared memory, the scans are warp scans over each lane's contiguous range
+// of experts, and nothing waits on a CTA-wide barrier.  The slot ids stay in
+// registers between the histogram and the scatter.  Same outputs, bit for
+// bit, as the multi-warp kernels.
+constexpr int kRouteWarpSlots = 512;
+constexpr int kRouteWarpExperts = 2048;
+
+__device__ __forceinline__ int32_t warp_inclusive_scan(int32_t v) {
+    const uint32_t lane = lane_id();
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= static_cast<uint32_t>(o)) v += y;
+    }
+    return v;
+}
+
+__global__ void __launch_bounds__(32)
+    route_warp_kernel(const int32_t* __restrict__ ids, int32_t n_slots, int32_t n_experts,
+                      int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                      int32_t* __restrict__ tiles_gemv, int32_t gemv_group, int32_t* __restrict__ tiles_gemm,
+                      int32_t gemm_group, uint32_t* err, uint32_t* __restrict__ zero_rows, int64_t row_words,
+                      int32_t expert_start, int32_t n_global) {
+    extern __shared__ int32_t sh_warp[];
+    int32_t* cnt = sh_warp;                 // [E]
+    int32_t* cur = sh_warp + n_experts;     // [E]
+    constexpr int STEPS = kRouteWarpSlots / 32;
+    const uint32_t lane = lane_id();
+    for (int32_t e = lane; e < n_experts; e += 32) cnt[e] = 0;
+    __syncwarp();
+    int32_t el[STEPS];
+    bool saw_bad = false;
+#pragma unroll
+    for (int step = 0; step < STEPS; ++step) {
+        const int32_t s = step * 32 + static_cast<int32_t>(lane);
+        el[step] = -1;
+        if (step * 32 < n_slots) {                                   // warp-uniform
+            const int32_t g = s < n_slots ? ids[s] : -1;
+            const int64_t x = static_cast<int64_t>(g) - expert_start;
+            const bool valid = s < n_slots && x >= 0 && x < n_experts;
+            saw_bad |= (s < n_slots) && (g < 0 || g >= n_global);
+            el[step] = valid ? static_cast<int32_t>(x) : -1;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, el[step]);
+            if (valid && lane == static_cast<uint32_t>(__ffs(peers) - 1)) cnt[el[step]] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    if (__any_sync(0xFFFFFFFFu, saw_bad) && lane == 0) atomicOr(err, FT_DEVERR_BAD_EXPERT_ID);
+    // exclusive scans over experts: lane l owns the contiguous range [lo, hi)
+    const int32_t per = (n_experts + 31) / 32;
+    const int32_t lo = min(n_experts, static_cast<int32_t>(lane) * per), hi = min(n_experts, lo + per);
+    int32_t sc = 0, sv = 0, sm = 0;
+    for (int32_t e = lo; e < hi; ++e) {
+        const int32_t c = cnt[e];
+        sc += c;
+        sv += (c + gemv_group - 1) / gemv_group;
+        sm += (c + gemm_group - 1) / gemm_group;
+    }
+    int32_t rc = warp_inclusive_scan(sc) - sc, rv = warp_inclusive_scan(sv) - sv, rm = warp_inclusive_scan(sm) - sm;
+    for (int32_t e = lo; e < hi; ++e) {
+        const int32_t c = cnt[e];
+        counts[e] = c;
+        offsets[e] = rc;
+        cur[e] = rc;
+        if (tiles_gemv) tiles_gemv[e] = rv;
+        if (tiles_gemm) tiles_gemm[e] = rm;
+        rc += c;
+        rv += (c + gemv_group - 1) / gemv_group;
+        rm += (c + gemm_group - 1) / gemm_group;
+    }
+    if (lane == 31) {
+        offsets[n_experts] = rc;
+        if (tiles_gemv) tiles_gemv[n_experts] = rv;
+        if (tiles_gemm) tiles_gemm[n_experts] = rm;
+    }
+    const int32_t n_valid = __shfl_sync(0xFFFFFFFFu, rc, 31);
+    __syncwarp();
+    // stable scatter: equal ids ranked by lane within each step of 32 slots
+#pragma unroll
+    for (int step = 0; step < STEPS; ++step) {
+        const int32_t s = step * 32 + static_cast<int32_t>(lane);
+        if (step * 32 < n_slots) {
+            const bool valid = el[step] >= 0;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, el[step]);
+            int32_t pos = 0;
+            if (valid) pos = cur[el[step]] + __popc(peers & lanemask_lt());
+            __syncwarp();
+            if (valid && lane == static_cast<uint32_t>(__ffs(peers) - 1)) cur[el[step]] += __popc(peers);
+            if (valid) perm[pos] = s;
+            if (!valid && s < n_slots && zero_rows != nullptr) {
+                uint32_t* row = zero_rows + static_cast<int64_t>(s) * row_words;
+                for (int64_t r = 0; r < row_words; ++r) row[r] = 0u;
+            }
+            __syncwarp();
+        }
+    }
+    for (int32_t p = n_valid + static_cast<int32_t>(lane); p < n_slots; p += 32) perm[p] = -1;
+}
+
 int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const RouteBuffers& b,
                  int32_t gemv_group, int32_t gemm_group, uint32_t* zero_rows, int64_t row_words, cudaStream_t s) {
     {
@@ -280,6 +382,13 @@ int launch_route(const int32_t* ids, int64_t n_slots, int32_t n_experts, const R
     const int32_t P = n_experts >= 1024 ? 1 : 1024 / n_experts;
     const size_t scan_sm = (static_cast<size_t>(P) * n_experts + 2 * static_cast<size_t>(n_experts) + 32) *
                            sizeof(int32_t);
+    if (n_slots <= kRouteWarpSlots && n_experts <= kRouteWarpExperts) {
+        const size_t sm = 2 * static_cast<size_t>(n_experts) * sizeof(int32_t);
+        route_warp_kernel<<<1, 32, sm, s>>>(ids, static_cast<int32_t>(n_slots), n_experts, b.counts, b.offsets, b.perm,
+                                            b.tiles_gemv, gemv_group, b.tiles_gemm, gemm_group, b.err, zero_rows,
+                                            row_words, start, n_global);
+        return check_launch("route_warp_kernel", dim3(1), dim3(32), sm);
+    }
     if (n_chunks <= 32 && n_chunks * n_experts <= 16384) {
         const size_t sm = static_cast<size_t>(n_chunks) * n_experts * sizeof(int32_t) + scan_sm;
         if (int st = set_smem_limit(reinterpret_cast<const void*>(route_small_kernel), static_cast<int>(sm))) return st;

@@ -496,9 +496,11 @@ def ours(args):
 
 # ------------------------------------------------------------ both layers
 def ffn(args):
-    """quantize + layer 1 (gate and up rows) + activation/requantize + layer 2
-    per step, CUDA-graph replayed; per-stage kernel times from an eager pass of
-    the same calls; roofline of the activation/requantize kernel (HBM)."""
+    """quantize + layer 1 (gate and up rows) with the activation/requantize
+    fused into it + layer 2 per step, CUDA-graph replayed; per-stage times
+    from an eager pass of the same calls, with the unfused layer 1 and
+    activation step beside them; roofline of the fused layer 1 (tensor pipe
+    on the tensor-core path, HBM on the GEMV path)."""
     import torch
     rank, world, _ = dist_env()
     if world > 1:
@@ -523,12 +525,12 @@ def ffn(args):
     mid = torch.empty((S, I // 32, 36), dtype=torch.uint8, device=dev)
     out = torch.empty((T, k, H), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    ft.reserve(T, k, E, max(2 * I, H), max(H, I))
+    ft.ffn_reserve(T, k, E, H, I)
     stream = torch.cuda.current_stream()
 
     def step():
         ft.quantize_q8_1(dx, out=act)
-        ft.moe_ffn_q4_0_q8_1(d13, d2, act, di, kind, out=out, h=h, act_mid=mid)
+        ft.moe_ffn_q4_0_q8_1(d13, d2, act, di, kind, out=out, act_mid=mid, keep_h=False)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -564,9 +566,10 @@ def ffn(args):
 
     # per stage, eager, events on the launching stream (torch's current stream)
     stages = {"quantize": lambda: ft.quantize_q8_1(dx, out=act),
-              "layer1": lambda: ft.moe_q4_0_q8_1(d13, act, di, out=h),
-              "act_requant": lambda: ft.act_mul_quantize_q8_1(h, kind, out=mid),
-              "layer2": lambda: ft.moe_q4_0_q8_1_slots(d2, mid, di, out=out)}
+              "layer1_act_fused": lambda: ft.moe_q4_0_q8_1_act(d13, act, di, kind, out=mid),
+              "layer2": lambda: ft.moe_q4_0_q8_1_slots(d2, mid, di, out=out),
+              "unfused_layer1": lambda: ft.moe_q4_0_q8_1(d13, act, di, out=h),
+              "unfused_act_requant": lambda: ft.act_mul_quantize_q8_1(h, kind, out=mid)}
     n_prof = max(3, min(args.steps, 30))
     st_ms = {}
     for key, fn in stages.items():
@@ -583,9 +586,23 @@ def ffn(args):
     if ft.read_device_error():
         raise RuntimeError("device error flag raised")
     peaks, peak_src = load_peaks()
-    act_bytes = S * 2 * I * 4 + S * (I // 32) * 36
-    achieved = act_bytes / (st_ms["act_requant"] / 1000.0) / 1e9
     flops = 2.0 * S * (2 * I) * H + 2.0 * S * H * I
+    l1_flops = 2.0 * S * (2 * I) * H
+    tc = ft.selected_path(T, k, E, 2 * I, H) == ft.FT_PATH_GEMM
+    if tc:
+        achieved = l1_flops / (st_ms["layer1_act_fused"] / 1000.0) / 1e12
+        roof = {"kernel": "moe_gemm_tc_kernel<act>", "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "algorithmic": f"2*S*2I*H = {l1_flops:.4g} FLOP per call (route and gather included in the time)",
+                "peak_note": f"dense bf16 tensor peak, of {peak_src}", "traffic": None}
+    else:
+        l1_bytes = E * 2 * I * (H // 32) * 18 + T * (H // 32) * 36 + S * (I // 32) * 36
+        achieved = l1_bytes / (st_ms["layer1_act_fused"] / 1000.0) / 1e9
+        roof = {"kernel": "moe_gemv_rows_kernel + act_mul_quantize_q8_1_kernel", "bound": "hbm",
+                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"],
+                "algorithmic": f"all expert weights + act + act_mid = {l1_bytes} B per call",
+                "peak_note": f"copy bandwidth, of {peak_src}", "traffic": None}
     line = {"metric": "routed tokens/s through both expert layers", "value": T / (ms / 1000.0), "unit": UNIT,
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "dtype": "q4_0 x q8_1 exact int block dots, f32 scaling and activation", "data": "synthetic",
@@ -593,10 +610,7 @@ def ffn(args):
                        "launch": launch_mode, "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)"},
             "effective_tops": flops / (ms / 1000.0) / 1e12,
             "stages_ms": st_ms,
-            "roofline": {"kernel": "act_mul_quantize_q8_1_kernel", "bound": "hbm", "achieved": achieved,
-                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "algorithmic": f"S*2I*4 + S*I/32*36 = {act_bytes} B per launch",
-                         "peak_note": f"copy bandwidth, of {peak_src}", "traffic": None},
+            "roofline": roof,
             "clocks": clk}
     print(json.dumps(line), flush=True)
     return 0

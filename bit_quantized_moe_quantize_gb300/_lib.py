@@ -30,7 +30,7 @@ EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_m
            "ft_moe_selected_path", "ft_moe_block_dots", "ft_last_error", "ft_abi_version", "ft_profile_enable",
            "ft_profile_read", "ft_moe_route_offsets_noalloc", "ft_moe_q4_0_q8_1_slots",
            "ft_moe_q4_0_q8_1_ep", "ft_act_mul_quantize_q8_1", "ft_moe_ffn_q4_0_q8_1", "ft_moe_gguf_q8_1",
-           "ft_repack_q4_0_soa", "ft_debug_wait_timeout")
+           "ft_repack_q4_0_soa", "ft_debug_wait_timeout", "ft_moe_q4_0_q8_1_act", "ft_moe_ffn_reserve")
 
 
 class FtError(RuntimeError):
@@ -69,6 +69,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.ft_repack_q4_0_soa.argtypes = [vp, vp, vp, i64, vp]
         L.ft_debug_wait_timeout.argtypes = [i64, vp]
         L.ft_moe_ffn_q4_0_q8_1.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i64, i64, i32, vp]
+        L.ft_moe_q4_0_q8_1_act.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, i32, vp]
+        L.ft_moe_ffn_reserve.argtypes = [i64, i32, i32, i64, i64]
         L.ft_moe_workspace_bytes.argtypes = [i64, i32, i32, i64, i64]
         L.ft_moe_workspace_bytes.restype = ctypes.c_size_t
         L.ft_moe_reserve.argtypes = [i64, i32, i32, i64, i64]
@@ -281,10 +283,31 @@ def act_mul_quantize_q8_1(h, act_kind, out=None):
     return out
 
 
-def moe_ffn_q4_0_q8_1(w13, w2, act, topk_ids, act_kind, out=None, h=None, act_mid=None):
+def moe_q4_0_q8_1_act(w13, act, topk_ids, act_kind, out=None):
+    """Layer 1 with the gated activation fused (ft_moe_q4_0_q8_1_act): w13 Q4_0
+    [E, 2I, H/32, 18] (gate rows, then up rows), act Q8_1 [T, H/32, 36] ->
+    Q8_1 uint8 [T*k, I/32, 36] of act(gate) * up per slot."""
+    torch = _torch()
+    E, two_i, H, T, k = _matmul_shape(w13, act, topk_ids)
+    if two_i % 64:
+        raise ValueError(f"w13 must hold 2 * n_inter rows with n_inter % 32 == 0 (got {two_i})")
+    I = two_i // 2
+    if out is None:
+        out = torch.empty((T * k, I // 32, 36), dtype=torch.uint8, device=w13.device)
+    po = _dev(out, torch.uint8, "out")
+    if out.numel() != T * k * (I // 32) * 36:
+        raise ValueError(f"out must hold {T * k} x {I // 32} Q8_1 blocks")
+    _check(load().ft_moe_q4_0_q8_1_act(ctypes.c_void_p(w13.data_ptr()), ctypes.c_void_p(act.data_ptr()),
+                                       ctypes.c_void_p(topk_ids.data_ptr()), po, T, k, E, I, H, int(act_kind),
+                                       _stream(w13)))
+    return out
+
+
+def moe_ffn_q4_0_q8_1(w13, w2, act, topk_ids, act_kind, out=None, h=None, act_mid=None, keep_h=True):
     """Both expert layers per slot (ft_moe_ffn_q4_0_q8_1): w13 Q4_0 [E, 2I, H/32, 18]
     (gate rows, then up rows), w2 Q4_0 [E, H, I/32, 18], act Q8_1 [T, H/32, 36]
-    -> out fp32 [T, k, H]; returns (out, h [T, k, 2I] fp32, act_mid [T*k, I/32, 36])."""
+    -> out fp32 [T, k, H]; returns (out, h [T, k, 2I] fp32, act_mid [T*k, I/32, 36]).
+    keep_h=False (and h None): layer 1 with the activation fused, h is None."""
     torch = _torch()
     E, two_i, H, T, k = _matmul_shape(w13, act, topk_ids)
     _dev(w2, torch.uint8, "w2", 4)
@@ -293,14 +316,21 @@ def moe_ffn_q4_0_q8_1(w13, w2, act, topk_ids, act_kind, out=None, h=None, act_mi
     I = two_i // 2
     dev = w13.device
     out = torch.empty((T, k, H), dtype=torch.float32, device=dev) if out is None else out
-    h = torch.empty((T, k, two_i), dtype=torch.float32, device=dev) if h is None else h
+    if h is None and keep_h:
+        h = torch.empty((T, k, two_i), dtype=torch.float32, device=dev)
     act_mid = torch.empty((T * k, I // 32, 36), dtype=torch.uint8, device=dev) if act_mid is None else act_mid
+    ph = ctypes.c_void_p(0) if h is None else _dev(h, torch.float32, "h")
     _check(load().ft_moe_ffn_q4_0_q8_1(ctypes.c_void_p(w13.data_ptr()), ctypes.c_void_p(w2.data_ptr()),
                                        ctypes.c_void_p(act.data_ptr()), ctypes.c_void_p(topk_ids.data_ptr()),
-                                       _dev(h, torch.float32, "h"), _dev(act_mid, torch.uint8, "act_mid"),
+                                       ph, _dev(act_mid, torch.uint8, "act_mid"),
                                        _dev(out, torch.float32, "out"), T, k, E, H, I, int(act_kind),
                                        _stream(w13)))
     return out, h, act_mid
+
+
+def ffn_reserve(max_tokens, max_top_k, n_experts, hidden, n_inter):
+    """Workspace for both expert layers up to these sizes (ft_moe_ffn_reserve)."""
+    _check(load().ft_moe_ffn_reserve(max_tokens, max_top_k, n_experts, hidden, n_inter))
 
 
 def block_dots(weights, act, topk_ids, out=None):

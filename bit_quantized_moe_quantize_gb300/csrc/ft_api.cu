@@ -213,14 +213,15 @@ static int get_stream_capturing(cudaStream_t s, bool* capturing) {
 // Per device: one cudaMalloc'ed block.  Layout (each part 256-byte aligned):
 //   err word | counts[E] | offsets[E+1] | perm[S] | tiles_gemv[E+1] |
 //   tiles_gemm[E+1] | hist[nchunks][E] | (tensor-core path only:)
-//   xh[S_pad][ncols] fp16 | da[S_pad][ncols/32] fp16
+//   xh[S_pad][ncols] fp16 | da[S_pad][ncols/32] fp16 | (layer 1 with the
+//   activation fused, on the GEMV path:) h[S][2 n_inter] fp32
 struct WsLayout {
-    size_t err, counts, offsets, perm, tiles_gemv, tiles_gemm, hist, xh, da, total;
+    size_t err, counts, offsets, perm, tiles_gemv, tiles_gemm, hist, xh, da, h, total;
 };
 
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
-static WsLayout ws_layout(int64_t n_slots, int32_t n_experts, int64_t gemm_ncols = 0) {
+static WsLayout ws_layout(int64_t n_slots, int32_t n_experts, int64_t gemm_ncols = 0, size_t h_bytes = 0) {
     WsLayout L{};
     size_t o = 0;
     L.err = o;
@@ -242,6 +243,8 @@ static WsLayout ws_layout(int64_t n_slots, int32_t n_experts, int64_t gemm_ncols
     o = al256(o + 2 * rows * static_cast<size_t>(gemm_ncols));
     L.da = o;
     o = al256(o + 2 * rows * static_cast<size_t>(gemm_ncols / 32));
+    L.h = o;
+    o = al256(o + h_bytes);
     L.total = o;
     return L;
 }
@@ -338,17 +341,32 @@ static int choose_path(const Shape& sh, int setting) {
     return sh.mean() >= 16.0 ? FT_PATH_GEMM : FT_PATH_GEMV;
 }
 
+// Slots above which the GEMV path is never chosen by itself (the tensor-core
+// path takes over at 16 routed slots per expert on average).
+static int64_t gemv_max_slots(const Shape& sh) {
+    if (path_setting() == FT_PATH_GEMV || !gemm_shape_ok(sh) || sh.wtype != FT_TYPE_Q4_0) return sh.n_slots;
+    const int64_t lim = 16 * static_cast<int64_t>(sh.n_global);
+    return sh.n_slots < lim ? sh.n_slots : lim;
+}
+
+// af != nullptr: layer 1 with the gated activation fused (sh.nrows = 2
+// af->n_inter, out unused): the tensor-core path applies it in its epilogue;
+// the GEMV path writes the layer-1 result to workspace and runs the
+// activation/requantize step on it.
 static int run_matmul(const void* weights, const void* act, const int32_t* topk_ids, float* out, int32_t* dots,
-                      const Shape& sh, cudaStream_t s) {
+                      const Shape& sh, cudaStream_t s, const ActFuse* af = nullptr) {
     const int path = choose_path(sh, path_setting());
     if (path == FT_PATH_GEMM && sh.wtype != FT_TYPE_Q4_0)
         return fail(FT_ERR_ARG, "the tensor-core path takes Q4_0 weights only (weight type %d)", sh.wtype);
     if (path == FT_PATH_GEMM && !gemm_shape_ok(sh))
         return fail(FT_ERR_ARG, "the tensor-core path needs ncols %% 256 == 0 and n_experts * nrows >= 128 (got %lld, %lld)",
                     (long long)sh.ncols, (long long)sh.n_experts * sh.nrows);
-    const WsLayout L = ws_layout(sh.n_slots, sh.n_experts, path == FT_PATH_GEMM ? sh.ncols : 0);
+    const bool h_in_ws = af && path == FT_PATH_GEMV;
+    const WsLayout L = ws_layout(sh.n_slots, sh.n_experts, path == FT_PATH_GEMM ? sh.ncols : 0,
+                                 h_in_ws ? 4 * static_cast<size_t>(sh.n_slots) * sh.nrows : 0);
     uint8_t* ws = nullptr;
     if (int st = ws_acquire(L.total, s, &ws)) return st;
+    if (h_in_ws) out = reinterpret_cast<float*>(ws + L.h);
     RouteBuffers rb{};
     rb.counts = reinterpret_cast<int32_t*>(ws + L.counts);
     rb.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
@@ -363,8 +381,13 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     if (path == FT_PATH_GEMV && (gp.smem > 227 * 1024 || gp.stages < 1))
         return fail(FT_ERR_SIZE, "GEMV tile needs %zu bytes of shared memory (%d ring stages of %lld-column rows fit)",
                     gp.smem, gp.stages, (long long)sh.ncols);
-    uint32_t* zero_rows = dots ? reinterpret_cast<uint32_t*>(dots) : reinterpret_cast<uint32_t*>(out);
-    const int64_t row_words = dots ? sh.nrows * sh.nb : sh.nrows;
+    // rows of slots with a bad expert id are zeroed by the router: block dots,
+    // outputs, or (fused on the tensor-core path) the slot's Q8_1 row
+    const bool fused_tc = af && path == FT_PATH_GEMM;
+    uint32_t* zero_rows = dots       ? reinterpret_cast<uint32_t*>(dots)
+                          : fused_tc ? reinterpret_cast<uint32_t*>(af->act_mid)
+                                     : reinterpret_cast<uint32_t*>(out);
+    const int64_t row_words = dots ? sh.nrows * sh.nb : fused_tc ? af->n_inter / 32 * 9 : sh.nrows;   // 9 words per Q8_1 block
     prof_mark(kProfRouteBegin, s);
     rb.expert_start = sh.expert_start;
     rb.n_global = sh.n_global;
@@ -379,15 +402,18 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     }
     prof_mark(kProfMatmulBegin, s);
     int st;
-    if (path == FT_PATH_GEMV)
+    if (path == FT_PATH_GEMV) {
         st = launch_gemv(gp, static_cast<const uint8_t*>(weights), static_cast<const uint8_t*>(act), rb.perm,
                          rb.offsets, rb.tiles_gemv, out, dots, rb.err, sh.n_slots, sh.act_div, sh.n_experts, sh.nrows,
                          sh.ncols, s, sh.wtype);
-    else
+        if (st == FT_OK && h_in_ws)
+            st = launch_act_mul_quantize_q8_1(out, af->act_mid, sh.n_slots, af->n_inter, af->kind, s);
+    } else {
         st = launch_gemm(static_cast<const uint8_t*>(weights), static_cast<const uint8_t*>(act), rb.perm,
-                         rb.offsets, rb.tiles_gemm, out, dots, rb.err, sh.n_slots, sh.act_div, sh.n_experts, sh.nrows,
-                         sh.ncols, reinterpret_cast<uint16_t*>(ws + L.xh), reinterpret_cast<uint16_t*>(ws + L.da),
-                         tile_width, s);
+                         rb.offsets, rb.tiles_gemm, fused_tc ? nullptr : out, dots, rb.err, sh.n_slots, sh.act_div,
+                         sh.n_experts, sh.nrows, sh.ncols, reinterpret_cast<uint16_t*>(ws + L.xh),
+                         reinterpret_cast<uint16_t*>(ws + L.da), tile_width, s, af);
+    }
     prof_mark(kProfMatmulEnd, s);
     return st;
 }
@@ -543,6 +569,25 @@ int ft_act_mul_quantize_q8_1(const float* h, void* act_q8_1, int64_t rows, int64
     return st;
 }
 
+int ft_moe_q4_0_q8_1_act(const void* w13, const void* act, const int32_t* topk_ids, void* act_mid, int64_t tokens,
+                         int32_t top_k, int32_t n_experts, int64_t n_inter, int64_t hidden, int32_t act_kind,
+                         void* stream) {
+    g_last_error.clear();
+    Shape sh{};
+    if (n_inter <= 0 || n_inter % 32 != 0 || n_inter > INT64_MAX / 4)
+        return fail(FT_ERR_ARG, "n_inter must be a positive multiple of 32 (got %lld)", (long long)n_inter);
+    if (int st = check_matmul_args(tokens, top_k, n_experts, 2 * n_inter, hidden, &sh)) return st;
+    if (act_kind != FT_ACT_SILU && act_kind != FT_ACT_GELU_TANH)
+        return fail(FT_ERR_ARG, "act_kind must be FT_ACT_SILU or FT_ACT_GELU_TANH (got %d)", act_kind);
+    if (sh.n_slots == 0) return FT_OK;
+    if (!w13 || !act || !topk_ids || !act_mid) return fail(FT_ERR_ARG, "null pointer");
+    if (!aligned(w13, 16) || !aligned(act, 16)) return fail(FT_ERR_ALIGN, "w13 and act must be 16-byte aligned");
+    if (!aligned(topk_ids, 4) || !aligned(act_mid, 4))
+        return fail(FT_ERR_ALIGN, "topk_ids and act_mid must be 4-byte aligned");
+    const ActFuse af{static_cast<uint8_t*>(act_mid), n_inter, act_kind};
+    return run_matmul(w13, act, topk_ids, nullptr, nullptr, sh, static_cast<cudaStream_t>(stream), &af);
+}
+
 int ft_moe_ffn_q4_0_q8_1(const void* w13, const void* w2, const void* act, const int32_t* topk_ids, float* h,
                          void* act_mid, float* out, int64_t tokens, int32_t top_k, int32_t n_experts,
                          int64_t hidden, int64_t n_inter, int32_t act_kind, void* stream) {
@@ -554,12 +599,36 @@ int ft_moe_ffn_q4_0_q8_1(const void* w13, const void* w2, const void* act, const
     if (act_kind != FT_ACT_SILU && act_kind != FT_ACT_GELU_TANH)
         return fail(FT_ERR_ARG, "act_kind must be FT_ACT_SILU or FT_ACT_GELU_TANH (got %d)", act_kind);
     if (sh.n_slots == 0) return FT_OK;
-    if (!h || !act_mid || !out) return fail(FT_ERR_ARG, "null pointer");
+    if (!act_mid || !out) return fail(FT_ERR_ARG, "null pointer");
     if (!aligned(h, 16) || !aligned(act_mid, 16)) return fail(FT_ERR_ALIGN, "h and act_mid must be 16-byte aligned");
-    if (int st = matmul_entry(w13, act, topk_ids, h, nullptr, tokens, top_k, n_experts, 2 * n_inter, hidden, stream))
+    if (h) {
+        if (int st = matmul_entry(w13, act, topk_ids, h, nullptr, tokens, top_k, n_experts, 2 * n_inter, hidden,
+                                  stream))
+            return st;
+        if (int st = ft_act_mul_quantize_q8_1(h, act_mid, sh.n_slots, n_inter, act_kind, stream)) return st;
+    } else if (int st = ft_moe_q4_0_q8_1_act(w13, act, topk_ids, act_mid, tokens, top_k, n_experts, n_inter, hidden,
+                                             act_kind, stream)) {
         return st;
-    if (int st = ft_act_mul_quantize_q8_1(h, act_mid, sh.n_slots, n_inter, act_kind, stream)) return st;
+    }
     return matmul_entry(w2, act_mid, topk_ids, out, nullptr, tokens, top_k, n_experts, hidden, n_inter, stream, true);
+}
+
+int ft_moe_ffn_reserve(int64_t max_tokens, int32_t max_top_k, int32_t n_experts, int64_t hidden, int64_t n_inter) {
+    g_last_error.clear();
+    Shape s1{}, s2{};
+    if (n_inter <= 0 || n_inter > INT64_MAX / 4) return fail(FT_ERR_ARG, "n_inter must be > 0");
+    if (int st = check_matmul_args(max_tokens, max_top_k, n_experts, 2 * n_inter, hidden, &s1)) return st;
+    if (int st = check_matmul_args(max_tokens, max_top_k, n_experts, hidden, n_inter, &s2)) return st;
+    // layer 1 on the tensor-core path, layer 1 fused on the GEMV path (its
+    // result in workspace, at most the slots that path is chosen for), layer 2
+    size_t need = ws_layout(s1.n_slots, n_experts, gemm_shape_ok(s1) ? hidden : 0).total;
+    const size_t fused_gemv =
+        ws_layout(s1.n_slots, n_experts, 0, 4 * static_cast<size_t>(gemv_max_slots(s1)) * 2 * n_inter).total;
+    const size_t l2 = ws_layout(s2.n_slots, n_experts, gemm_shape_ok(s2) ? n_inter : 0).total;
+    need = need > fused_gemv ? need : fused_gemv;
+    need = need > l2 ? need : l2;
+    uint8_t* base = nullptr;
+    return ws_acquire(need, nullptr, &base);
 }
 
 int ft_moe_gguf_q8_1(int32_t wtype, const void* weights, const void* act, const int32_t* topk_ids, float* out,

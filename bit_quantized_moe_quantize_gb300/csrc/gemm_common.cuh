@@ -24,6 +24,12 @@ struct GemmArgs {
     int32_t top_k;
     int32_t n_experts;
     int32_t row_tiles;
+    // layer 1 with the gated activation in the epilogue (act_mid != nullptr):
+    // the weight rows are n_inter gate rows then n_inter up rows per expert,
+    // and the epilogue writes Q8_1 rows of act(gate) * up to act_mid
+    uint8_t* act_mid;
+    int64_t n_inter;
+    int32_t act_kind;
 };
 
 struct TileInfo {

@@ -43,6 +43,7 @@
 // along K, so each block needs its own accumulator and a drain; the drain's
 // two fp32 operations per (row, slot, block) set this kernel's ceiling.
 #include "gemm_common.cuh"
+#include "q8_1_math.cuh"
 
 namespace ft {
 
@@ -83,13 +84,23 @@ struct Gemm {
     static constexpr int UNPACK_THREADS = N_UNPACK_WARPS * 32;  // one weight row per thread
     static constexpr int WARP_PRODUCER = N_DRAIN_WARPS + N_UNPACK_WARPS, WARP_MMA = WARP_PRODUCER + 1;
     static constexpr int THREADS = (WARP_MMA + 1) * 32;
+    static constexpr int N_EPI_WARPS = 2;                        // fused layer 1: quantizing warps after the MMA warp
+    static constexpr int THREADS_FUSED = THREADS + N_EPI_WARPS * 32;
     static constexpr uint32_t TMEM_COLS = NACC * BN;
     // smem offsets from a 1024-aligned base
     static constexpr int OFF_OP = 0;
     static constexpr int OFF_RAW = OFF_OP + OP_SLOTS * OP_SLOT_BYTES;
     static constexpr int OFF_SC = OFF_RAW + RAW_STAGES * RAW_STAGE_BYTES;
-    static constexpr int OFF_BAR = OFF_SC + NSC * SC_BYTES;
-    static constexpr int N_BARS = 2 * RAW_STAGES + 2 * OP_SLOTS + 2 * NBAR_ACC + NSC;
+    // Fused layer-1 epilogue: the up rows' sums as float2 [64 rows][BN / 2 + 4]
+    // (the 4 extra float2 per row keep a warp's float2 stores conflict-free),
+    // then, in the same bytes, act(gate) * up as float [BN slots][64 + 4]
+    // (rows 16-byte aligned, one 128-byte run per quarter-warp read)
+    static constexpr int EPI_P2 = BN / 2 + 4;
+    static constexpr int EPI_AP = 64 + 4;
+    static constexpr int EPI_BYTES = 64 * EPI_P2 * 8 > BN * EPI_AP * 4 ? 64 * EPI_P2 * 8 : BN * EPI_AP * 4;
+    static constexpr int OFF_EPI = OFF_SC + NSC * SC_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
+    static constexpr int N_BARS = 2 * RAW_STAGES + 2 * OP_SLOTS + 2 * NBAR_ACC + NSC + 4;
     static constexpr int OFF_TMEM = OFF_BAR + N_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;    // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -114,8 +125,119 @@ __device__ __forceinline__ void i8x4_to_h2(uint32_t v, uint32_t& lo, uint32_t& h
     hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
-template <int BN, bool DUMP>
-__global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
+// Fused layer-1 epilogue.  A tile's 128 rows are 64 gate rows i0 .. i0+63
+// (TMEM lanes 0..63) and the matching up rows (lanes 64..127), so gate row m
+// and up row m sit in the same thread position of drain warps w and w + 2.
+// At the end of a tile (tc counts the CTA's earlier tiles: the phase of the
+// epilogue barriers) the drain warps
+//   1. (up warps) store their sums, float2 [row][slot];
+//   2. (gate warps) read the up value of each of their sums and replace the
+//      sum g by act(g) * up; once every gate warp has read, they store those
+//      values slot-major ([slot][row]) in the same bytes;
+// and go on with the next tile, while two epilogue warps
+//   3. quantize (slot, 32-row block) units, eight lanes per unit with four
+//      values each - the lane layout and arithmetic of the separate
+//      activation/requantize step - and write the Q8_1 block of columns
+//      i0 + 32 j .. +31 of the slot's act_mid row.
+// The up warps wait before step 1 until step 3 of the previous tile is done
+// with the bytes.  Every wait is bounded; false: one gave up.
+template <int BN>
+__device__ __forceinline__ bool fused_act_drain(float2 (&acc)[2][Gemm<BN>::CW / 8], const GemmArgs& a,
+                                                uint8_t* epi, uint64_t* ebar, uint32_t tc, uint32_t warp,
+                                                uint32_t lane) {
+    using C = Gemm<BN>;
+    constexpr int CW = C::CW, P2 = C::EPI_P2, AP = C::EPI_AP;
+    uint64_t* up_ready = ebar;        // step 1 done (up warps)
+    uint64_t* up_read = ebar + 1;     // up values read (gate warps)
+    uint64_t* a_ready = ebar + 2;     // step 2 done (gate warps)
+    uint64_t* a_done = ebar + 3;      // step 3 done (epilogue warps)
+    const uint32_t ph = tc & 1u;
+    const uint32_t lane0 = (warp & 3u) * 32u + ((warp >> 2) & 1u) * 16u;
+    const uint32_t col0 = (warp >> 3) * static_cast<uint32_t>(CW);
+    const uint32_t q = lane & 3u, r0 = lane0 + (lane >> 2);
+    float2* ub = reinterpret_cast<float2*>(epi);
+    float* ab = reinterpret_cast<float*>(epi);
+    if ((warp & 3u) >= 2u) {
+        if (!mbar_wait_warp(a_done, ph ^ 1u, a.err)) return false;
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+            for (int i = 0; i < CW / 8; ++i) ub[(r0 - 64 + 8 * hr) * P2 + (col0 >> 1) + 4 * i + q] = acc[hr][i];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(up_ready);
+        return true;
+    }
+    if (!mbar_wait_warp(up_ready, ph, a.err)) return false;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+        for (int i = 0; i < CW / 8; ++i) {
+            const float2 u = ub[(r0 + 8 * hr) * P2 + (col0 >> 1) + 4 * i + q];
+            acc[hr][i].x = act_mul(acc[hr][i].x, u.x, a.act_kind);
+            acc[hr][i].y = act_mul(acc[hr][i].y, u.y, a.act_kind);
+        }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(up_read);
+    if (!mbar_wait_warp(up_read, ph, a.err)) return false;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+        for (int i = 0; i < CW / 8; ++i) {
+            const uint32_t n = col0 + 8 * i + 2 * q;
+            ab[n * AP + r0 + 8 * hr] = acc[hr][i].x;
+            ab[(n + 1) * AP + r0 + 8 * hr] = acc[hr][i].y;
+        }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(a_ready);
+    return true;
+}
+
+// Step 3 for one tile, by epilogue warp ew (0 or 1).
+template <int BN>
+__device__ __forceinline__ bool fused_act_quantize(const GemmArgs& a, const TileInfo& ti, const uint8_t* epi,
+                                                   uint64_t* ebar, uint32_t tc, uint32_t ew, uint32_t lane) {
+    using C = Gemm<BN>;
+    constexpr int AP = C::EPI_AP;
+    const float* ab = reinterpret_cast<const float*>(epi);
+    if (!mbar_wait_warp(ebar + 2, tc & 1u, a.err)) return false;
+    const uint32_t grp = lane >> 3, sub = lane & 7u;
+    const uint32_t gmask = 0xFFu << (lane & 24u);
+    const int64_t i0 = ti.m0 / 2, nbi = a.n_inter / QK;
+#pragma unroll 1
+    for (int it = 0; it < 2 * BN / (4 * C::N_EPI_WARPS); ++it) {
+        const uint32_t u = (static_cast<uint32_t>(it) * C::N_EPI_WARPS + ew) * 4u + grp;
+        const uint32_t n = u >> 1, j = u & 1u;
+        const float4 x = *reinterpret_cast<const float4*>(ab + n * AP + 32 * j + 4 * sub);
+        const float v[4] = {x.x, x.y, x.z, x.w};
+        float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, o));
+        const float d = __fdiv_rn(amax, 127.0f);
+        int qv[4];
+        q8_codes<4>(v, amax, d, qv);
+        uint32_t packed = 0;
+        int sum = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            sum += qv[k];
+            packed |= (static_cast<uint32_t>(qv[k]) & 0xFFu) << (8 * k);
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(gmask, sum, o);
+        if (static_cast<int32_t>(n) < ti.nvalid && i0 + 32 * static_cast<int64_t>(j) < a.n_inter) {
+            const int64_t slot = a.perm[ti.p0 + n];
+            uint8_t* ob = a.act_mid + (slot * nbi + i0 / QK + j) * Q8_1_BYTES;
+            *reinterpret_cast<uint32_t*>(ob + 4 + 4 * sub) = packed;
+            if (sub == 0) *reinterpret_cast<uint32_t*>(ob) = q8_header(d, sum);
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(ebar + 3);
+    return true;
+}
+
+template <int BN, bool DUMP, bool FUSE>
+__global__ void __launch_bounds__(FUSE ? Gemm<BN>::THREADS_FUSED : Gemm<BN>::THREADS, 1)
     moe_gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                        const __grid_constant__ CUtensorMap smap, const GemmArgs a) {
     using C = Gemm<BN>;
@@ -130,6 +252,7 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
     constexpr uint32_t TMEM_COLS = C::TMEM_COLS;
     constexpr int OFF_OP = C::OFF_OP, OFF_RAW = C::OFF_RAW, OFF_SC = C::OFF_SC, OFF_BAR = C::OFF_BAR;
     constexpr int OFF_TMEM = C::OFF_TMEM;
+    static_assert(!(DUMP && FUSE), "block dots come from the plain matmul");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -140,6 +263,7 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
     uint64_t* acc_full = op_empty + OP_SLOTS;
     uint64_t* acc_empty = acc_full + NBAR_ACC;
     uint64_t* sc_empty = acc_empty + NBAR_ACC;
+    uint64_t* epi_bar = sc_empty + NSC;          // fused epilogue: up_ready, up_read, a_ready, a_done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
 
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
@@ -166,6 +290,8 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
             mbar_init(&acc_empty[i], N_DRAIN_WARPS);
         }
         for (int i = 0; i < NSC; ++i) mbar_init(&sc_empty[i], N_DRAIN_WARPS);
+        for (int i = 0; i < 3; ++i) mbar_init(&epi_bar[i], N_DRAIN_WARPS / 2);
+        mbar_init(&epi_bar[3], C::N_EPI_WARPS);
         fence_mbar_init();
     }
     if (warp == WARP_MMA) {
@@ -190,7 +316,10 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
         bool ok = true;
         for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
             const TileInfo ti = decode_tile<BN>(a, w);
-            const int32_t wy = static_cast<int32_t>(static_cast<int64_t>(ti.e) * a.nrows + ti.m0);
+            // fused layer 1: gate rows i0 .. i0+63 and up rows n_inter + i0 .. (i0 = m0 / 2)
+            const int64_t row0 = static_cast<int64_t>(ti.e) * a.nrows + (FUSE ? ti.m0 / 2 : ti.m0);
+            const int32_t wy = static_cast<int32_t>(row0);
+            const int32_t wy_up = static_cast<int32_t>(FUSE ? row0 + a.n_inter : 0);
             const int32_t py = static_cast<int32_t>(ti.p0);
             for (int32_t ks = 0; ks < n_stages && ok; ++ks, ++it) {
                 const uint32_t s = it % RAW_STAGES;
@@ -199,6 +328,9 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&raw_full[s], W_RAW_BYTES + DA_RAW_BYTES);
                     tma_load_2d(wraw, &wmap, ks * KB * Q4_0_BYTES, wy, &raw_full[s]);
+                    if constexpr (FUSE)
+                        tma_load_2d(wraw + (BM / 2) * KB * Q4_0_BYTES, &wmap, ks * KB * Q4_0_BYTES, wy_up,
+                                    &raw_full[s]);
                     tma_load_2d(wraw + W_RAW_BYTES, &smap, ks * KB, py, &raw_full[s]);
                 }
                 for (int j = 0; j < KB / 2; ++j, ++ou) {
@@ -375,6 +507,15 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
             }
         }
         __syncwarp();
+    } else if (warp > WARP_MMA) {
+        // ---------------------------------------- fused layer 1: quantizing warps
+        if constexpr (FUSE) {
+            uint32_t tc = 0;
+            for (int64_t w = blockIdx.x; w < total; w += gridDim.x, ++tc) {
+                const TileInfo ti = decode_tile<BN>(a, w);
+                if (!fused_act_quantize<BN>(a, ti, smem + C::OFF_EPI, epi_bar, tc, warp - WARP_MMA - 1, lane)) break;
+            }
+        }
     } else {
         // --------------------------------------------------------------- drain
         // warp w: TMEM lanes 32 (w % 4) + 16 ((w / 4) % 2) .. +15, columns CW (w / 8) .. +CW-1,
@@ -386,12 +527,13 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
         const uint32_t r0 = lane0 + (lane >> 2);           // rows r0 and r0 + 8 of the tile
         const uint32_t tlane = tmem_base + (lane0 << 16) + col0;
         float2 acc[2][CW / 8];                             // [row][column group]
+        uint32_t tc = 0;                                   // tiles drained
 #pragma unroll
         for (int i = 0; i < CW / 8; ++i) acc[0][i] = acc[1][i] = make_float2(0.0f, 0.0f);
         if constexpr (PAIRED) {
             uint32_t bc = 0, uc = 0;                           // blocks and 2-block units drained
             bool ok = true;
-            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++tc) {
                 const TileInfo ti = decode_tile<BN>(a, w);
                 for (int32_t b = 0; b < nb; ++b, ++bc) {
                     const uint32_t h = static_cast<uint32_t>(b) & 1u;   // block within its unit (nb is even)
@@ -454,7 +596,11 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
                     uc += h;
                 }
                 if (!ok) break;
-                if constexpr (!DUMP) {
+                if constexpr (FUSE) {
+                    if (!fused_act_drain<BN>(acc, a, smem + C::OFF_EPI, epi_bar, tc, warp, lane)) break;
+    #pragma unroll
+                    for (int i = 0; i < CW / 8; ++i) acc[0][i] = acc[1][i] = make_float2(0.0f, 0.0f);
+                } else if constexpr (!DUMP) {
     #pragma unroll
                     for (int i = 0; i < CW / 8; ++i) {
     #pragma unroll
@@ -474,7 +620,7 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
         } else {
             uint32_t bc = 0;
             bool ok = true;
-            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++tc) {
                 const TileInfo ti = decode_tile<BN>(a, w);
                 for (int32_t b = 0; b < nb; ++b, ++bc) {
                     const uint32_t ab = bc % NACC, sc = bc % NSC;
@@ -531,7 +677,11 @@ __global__ void __launch_bounds__(Gemm<BN>::THREADS, 1)
                     if (lane == 0) mbar_arrive(&sc_empty[sc]);   // scale slot sc free again
                 }
                 if (!ok) break;
-                if constexpr (!DUMP) {
+                if constexpr (FUSE) {
+                    if (!fused_act_drain<BN>(acc, a, smem + C::OFF_EPI, epi_bar, tc, warp, lane)) break;
+    #pragma unroll
+                    for (int i = 0; i < CW / 8; ++i) acc[0][i] = acc[1][i] = make_float2(0.0f, 0.0f);
+                } else if constexpr (!DUMP) {
     #pragma unroll
                     for (int i = 0; i < CW / 8; ++i) {
     #pragma unroll
@@ -641,17 +791,31 @@ int launch_gather(const uint8_t* act, const int32_t* perm, const int32_t* offset
     return check_launch("gather_act_kernel", grid, dim3(256), 0);
 }
 
+template <int BN, bool DUMP, bool FUSE>
+static int launch_gemm_kernel(const CUtensorMap& wmap, const CUtensorMap& xmap, const CUtensorMap& smap,
+                              const GemmArgs& ga, dim3 grid, cudaStream_t s, const char* name) {
+    using C = Gemm<BN>;
+    const void* k = reinterpret_cast<const void*>(moe_gemm_tc_kernel<BN, DUMP, FUSE>);
+    if (int st = set_smem_limit(k, C::SMEM_BYTES)) return st;
+    constexpr int threads = FUSE ? C::THREADS_FUSED : C::THREADS;
+    moe_gemm_tc_kernel<BN, DUMP, FUSE><<<grid, threads, C::SMEM_BYTES, s>>>(wmap, xmap, smap, ga);
+    return check_launch(name, grid, dim3(threads), C::SMEM_BYTES);
+}
+
 template <int BN>
 static int launch_gemm_bn(const uint8_t* weights, const int32_t* perm, const int32_t* offsets, const int32_t* tiles,
                           float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k, int32_t n_experts,
-                          int64_t nrows, int64_t ncols, const uint16_t* xh, const uint16_t* da, cudaStream_t s) {
+                          int64_t nrows, int64_t ncols, const uint16_t* xh, const uint16_t* da, const ActFuse* af,
+                          cudaStream_t s) {
     using C = Gemm<BN>;
     const int64_t nb = ncols / QK;
     const int sms = sm_count();
     const int64_t rows = gemm_rows(n_slots);
+    // the fused layer 1 loads its 128 rows as two boxes of 64 (gate, up)
+    const uint32_t box_rows = af ? C::BM / 2 : C::BM;
     CUtensorMap wmap, xmap, smap;
     if (int st = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, weights, nb * Q4_0_BYTES, n_experts * nrows,
-                           nb * Q4_0_BYTES, C::KB * Q4_0_BYTES, C::BM, CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
+                           nb * Q4_0_BYTES, C::KB * Q4_0_BYTES, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
         return st;
     if (int st = encode_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, ncols, rows, ncols * 2, 64, BN,
                            CU_TENSOR_MAP_SWIZZLE_128B, "activations"))
@@ -671,21 +835,20 @@ static int launch_gemm_bn(const uint8_t* weights, const int32_t* perm, const int
     ga.nb = static_cast<int32_t>(nb);
     ga.top_k = top_k;
     ga.n_experts = n_experts;
-    ga.row_tiles = static_cast<int32_t>((nrows + C::BM - 1) / C::BM);
+    ga.row_tiles = static_cast<int32_t>(af ? (af->n_inter + C::BM / 2 - 1) / (C::BM / 2)
+                                           : (nrows + C::BM - 1) / C::BM);
+    if (af) {
+        ga.act_mid = af->act_mid;
+        ga.n_inter = af->n_inter;
+        ga.act_kind = af->kind;
+    }
 
     const int64_t slot_tiles_ub = (n_slots + BN - 1) / BN + (n_experts < n_slots ? n_experts : n_slots);
     const int64_t tiles_ub = slot_tiles_ub * ga.row_tiles;
     const dim3 grid(static_cast<unsigned>(tiles_ub < sms ? tiles_ub : sms));
-    const dim3 block(C::THREADS);
-    if (dots) {
-        if (int st = set_smem_limit(reinterpret_cast<const void*>(moe_gemm_tc_kernel<BN, true>), C::SMEM_BYTES))
-            return st;
-        moe_gemm_tc_kernel<BN, true><<<grid, block, C::SMEM_BYTES, s>>>(wmap, xmap, smap, ga);
-        return check_launch("moe_gemm_tc_kernel<dump>", grid, block, C::SMEM_BYTES);
-    }
-    if (int st = set_smem_limit(reinterpret_cast<const void*>(moe_gemm_tc_kernel<BN, false>), C::SMEM_BYTES)) return st;
-    moe_gemm_tc_kernel<BN, false><<<grid, block, C::SMEM_BYTES, s>>>(wmap, xmap, smap, ga);
-    return check_launch("moe_gemm_tc_kernel", grid, block, C::SMEM_BYTES);
+    if (dots) return launch_gemm_kernel<BN, true, false>(wmap, xmap, smap, ga, grid, s, "moe_gemm_tc_kernel<dump>");
+    if (af) return launch_gemm_kernel<BN, false, true>(wmap, xmap, smap, ga, grid, s, "moe_gemm_tc_kernel<act>");
+    return launch_gemm_kernel<BN, false, false>(wmap, xmap, smap, ga, grid, s, "moe_gemm_tc_kernel");
 }
 
 int gemm_tile_width(double mean_slots_per_expert) {
@@ -698,14 +861,16 @@ int gemm_tile_width(double mean_slots_per_expert) {
 int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
                 const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
                 int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, int tile_width,
-                cudaStream_t s) {
+                cudaStream_t s, const ActFuse* af) {
     (void)act;   // read by launch_gather, which the caller runs first
     if (n_slots == 0) return FT_OK;
+    if (af && (dots || af->n_inter * 2 != nrows))
+        return fail(FT_ERR_ARG, "the fused activation needs nrows = 2 n_inter and no block dots");
     if (tile_width == 32)
         return launch_gemm_bn<32>(weights, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,
-                                  ncols, xh, da, s);
+                                  ncols, xh, da, af, s);
     return launch_gemm_bn<kGemmBN>(weights, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,
-                                   ncols, xh, da, s);
+                                   ncols, xh, da, af, s);
 }
 
 }  // namespace ft

@@ -335,12 +335,44 @@ FT_API int ft_act_mul_quantize_q8_1(const float* h, void* act_q8_1, int64_t rows
                                     int32_t act_kind, void* stream);
 
 /*
+ * ft_moe_q4_0_q8_1_act - layer 1 of the routed MoE block with the gated
+ * activation and the Q8_1 requantization fused into it (gelu_tanh_and_mul
+ * right after the routed matmul on FreeToken PR #185, "Problem"; SiLU*up
+ * between layer 1 and layer 2 on nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 6):
+ *   act_mid = ft_act_mul_quantize_q8_1(ft_moe_q4_0_q8_1(w13, act))
+ * without the fp32 layer-1 result in memory on the tensor-core path: each
+ * tile there holds 64 gate rows and the 64 matching up rows of one expert,
+ * and its epilogue writes the Q8_1 blocks of act(gate) * up for its slots.
+ * On the GEMV path the layer-1 result goes to library workspace
+ * (tokens * top_k * 2 n_inter fp32) and the activation step reads it there.
+ * The per-element arithmetic is that of the two calls it replaces, so the
+ * result equals theirs bit for bit on the same path.
+ *
+ *   w13       device, Q4_0 [n_experts][2 * n_inter][hidden / 32]: rows
+ *             [0, n_inter) of an expert are its gate rows, [n_inter, 2 n_inter)
+ *             its up rows; 16-byte aligned
+ *   act       device, Q8_1 [tokens][hidden / 32]; 16-byte aligned
+ *   topk_ids  device, int32 [tokens][top_k]
+ *   act_mid   device, Q8_1 [tokens * top_k][n_inter / 32] out; 4-byte aligned
+ *   n_inter   positive multiple of 32; the limits of ft_moe_q4_0_q8_1 apply
+ *             to the matmul with nrows = 2 n_inter, ncols = hidden
+ *   act_kind  FT_ACT_SILU or FT_ACT_GELU_TANH
+ * Slots with a bad expert id get zero act_mid rows (and the device error
+ * flag).  Errors: those of ft_moe_q4_0_q8_1 and ft_act_mul_quantize_q8_1.
+ */
+FT_API int ft_moe_q4_0_q8_1_act(const void* w13, const void* act, const int32_t* topk_ids, void* act_mid,
+                                int64_t tokens, int32_t top_k, int32_t n_experts, int64_t n_inter, int64_t hidden,
+                                int32_t act_kind, void* stream);
+
+/*
  * ft_moe_ffn_q4_0_q8_1 - both expert layers of the routed MoE block, per
- * slot, in three steps on `stream` (layer 1 -> activation -> layer 2 on
- * nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 6):
+ * slot, on `stream` (layer 1 -> activation -> layer 2 on
+ * nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 6).  With h != NULL, three steps:
  *   h       = ft_moe_q4_0_q8_1(w13, act)           gate and up rows in one matmul
  *   act_mid = ft_act_mul_quantize_q8_1(h)          per slot row
  *   out     = ft_moe_q4_0_q8_1_slots(w2, act_mid)
+ * with h == NULL, two: act_mid = ft_moe_q4_0_q8_1_act(w13, act), then the
+ * same layer 2 (act_mid and out equal those of the three steps bit for bit).
  * The weighted sum over a token's top_k slots is left to the caller.
  *
  *   w13       device, Q4_0 [n_experts][2 * n_inter][hidden / 32]: rows
@@ -350,7 +382,8 @@ FT_API int ft_act_mul_quantize_q8_1(const float* h, void* act_q8_1, int64_t rows
  *   act       device, Q8_1 [tokens][hidden / 32]; 16-byte aligned
  *   topk_ids  device, int32 [tokens][top_k]
  *   h         device, fp32 [tokens][top_k][2 * n_inter] out (scratch the
- *             caller owns; holds the layer-1 result afterwards); 16-byte aligned
+ *             caller owns; holds the layer-1 result afterwards); 16-byte
+ *             aligned; or NULL: layer 1 with the activation fused
  *   act_mid   device, Q8_1 [tokens * top_k][n_inter / 32] out (scratch the
  *             caller owns; holds the layer-2 input afterwards); 16-byte aligned
  *   out       device, fp32 [tokens][top_k][hidden] out
@@ -362,6 +395,15 @@ FT_API int ft_moe_ffn_q4_0_q8_1(const void* w13, const void* w2, const void* act
                                 float* h, void* act_mid, float* out, int64_t tokens, int32_t top_k,
                                 int32_t n_experts, int64_t hidden, int64_t n_inter, int32_t act_kind,
                                 void* stream);
+
+/*
+ * ft_moe_ffn_reserve - ft_moe_reserve for both expert layers: allocates the
+ * current device's workspace for ft_moe_ffn_q4_0_q8_1 (h given or NULL) and
+ * ft_moe_q4_0_q8_1_act at up to these sizes, so that they can be captured
+ * in a CUDA graph.  Errors: FT_ERR_ARG, FT_ERR_SIZE, FT_ERR_CUDA.
+ */
+FT_API int ft_moe_ffn_reserve(int64_t max_tokens, int32_t max_top_k, int32_t n_experts, int64_t hidden,
+                              int64_t n_inter);
 
 /*
  * ft_moe_workspace_bytes - bytes of library workspace that one

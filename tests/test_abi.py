@@ -160,9 +160,31 @@ def test_activation_and_ffn_reject_bad_arguments(lib):
     assert g(W1, W2, X, I, Hh, M, O, 4, 2, 8, 250, 128, 0, vp(0)) == 1  # hidden % 32
     assert g(W1, W2, X, I, Hh, M, O, 4, 2, 8, 256, 128, 5, vp(0)) == 1  # unknown activation
     assert g(W1, W2, X, I, Hh, M, O, 0, 2, 8, 256, 128, 0, vp(0)) == 0  # no slots: no-op
-    assert g(W1, W2, X, I, vp(0), M, O, 4, 2, 8, 256, 128, 0, vp(0)) == 1    # null h
+    assert g(W1, W2, X, I, Hh, vp(0), O, 4, 2, 8, 256, 128, 0, vp(0)) == 1   # null act_mid
+    assert g(W1, W2, X, I, vp(0), M, vp(0), 4, 2, 8, 256, 128, 0, vp(0)) == 1  # null out (h NULL: fused)
     assert g(W1, W2, X, I, vp(0x50008), M, O, 4, 2, 8, 256, 128, 0, vp(0)) == 3   # h misaligned
     assert g(W1, W2, X, I, Hh, vp(0x60004), O, 4, 2, 8, 256, 128, 0, vp(0)) == 3  # act_mid misaligned
+
+
+def test_fused_layer1_rejects_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    f = lib.ft_moe_q4_0_q8_1_act
+    W, X, I, M = (vp(0x10000 * i) for i in range(1, 5))
+    assert f(W, X, I, M, 4, 2, 8, 100, 256, 0, vp(0)) == 1       # n_inter % 32
+    assert f(W, X, I, M, 4, 2, 8, 0, 256, 0, vp(0)) == 1         # n_inter = 0
+    assert f(W, X, I, M, 4, 2, 8, 128, 250, 0, vp(0)) == 1       # hidden % 32
+    assert f(W, X, I, M, 4, 2, 8, 128, 256, 7, vp(0)) == 1       # unknown activation
+    assert "act_kind" in _err(lib)
+    assert f(W, X, I, M, 4, 9, 8, 128, 256, 0, vp(0)) == 1       # top_k > n_experts
+    assert f(W, X, I, M, 0, 2, 8, 128, 256, 0, vp(0)) == 0       # no slots: no-op
+    assert f(W, X, I, vp(0), 4, 2, 8, 128, 256, 0, vp(0)) == 1   # null act_mid
+    assert f(vp(0x10008), X, I, M, 4, 2, 8, 128, 256, 0, vp(0)) == 3   # w13 misaligned
+    assert f(W, X, I, vp(0x40002), 4, 2, 8, 128, 256, 0, vp(0)) == 3   # act_mid not 4-byte aligned
+    assert f(W, X, I, M, 1 << 40, 8, 8, 128, 256, 0, vp(0)) == 2       # tokens * top_k >= 2^31
+    r = lib.ft_moe_ffn_reserve
+    assert r(16, 2, 8, 256, 0) == 1                                # n_inter = 0
+    assert r(16, 2, 8, 250, 128) == 1                              # hidden % 32
+    assert r(16, 9, 8, 256, 128) == 1                              # top_k > n_experts
 
 
 def test_gguf_matmul_rejects_bad_arguments(lib):

@@ -201,3 +201,120 @@ def test_ffn_equals_the_three_steps(ft, oracle):
     out2 = ft.moe_q4_0_q8_1_slots(dw2, mid2, dids)
     torch.cuda.synchronize()
     assert torch.equal(h, h2) and torch.equal(mid, mid2) and torch.equal(out, out2)
+
+
+# Layer 1 with the activation fused into it (ft_moe_q4_0_q8_1_act): on the
+# tensor-core path each tile holds 64 gate rows and the matching 64 up rows
+# and its epilogue writes the Q8_1 blocks; on the GEMV path the layer-1 result
+# goes through workspace.  (E, k, hidden, n_inter, T, seed, path):
+# 128-slot tiles (n_inter a multiple of 64, and n_inter % 64 == 32 so the
+# last tile holds one Q8_1 block), 32-slot tiles (n_inter = 96, and n_inter =
+# 32: half a tile), a ragged slot count, and the GEMV path.
+FUSED_CASES = [
+    (16, 4, 2048, 768, 300, 90, "gemm"),
+    (8, 2, 512, 160, 200, 91, "gemm"),
+    (32, 4, 256, 96, 200, 92, "gemm"),
+    (8, 2, 256, 32, 64, 93, "gemm"),
+    (6, 3, 768, 224, 157, 94, "gemm"),
+    (128, 8, 2048, 768, 4, 95, "gemv"),
+    (8, 2, 512, 160, 37, 96, "gemv"),
+]
+
+
+def _mid_ref(oracle, w13, act, ids, kind):
+    """The oracle's layer-2 input: its layer-1 result through its activation step."""
+    h = oracle.moe(w13, act, ids)
+    return oracle.act_mul_quantize_q8_1(h.reshape(-1, h.shape[-1]), kind)
+
+
+@pytest.mark.parametrize("kind", [0, 1], ids=["silu", "gelu_tanh"])
+@pytest.mark.parametrize("E,k,H,I,T,seed,path", FUSED_CASES)
+def test_fused_layer1_equals_matmul_then_activation(ft, oracle, kind, E, k, H, I, T, seed, path):
+    """Bit for bit the two calls it replaces, on the same path; and within the
+    requantization's bounds of the oracle."""
+    import torch
+    w13, _, x, ids = _ffn_case(E, k, H, I, T, seed)
+    act = oracle.quantize_q8_1(x)
+    dw, da, di = G.dev(w13), G.dev(act), G.dev(ids)
+    ft.set_path(path)
+    try:
+        mid = ft.moe_q4_0_q8_1_act(dw, da, di, kind)
+        mid2 = ft.act_mul_quantize_q8_1(ft.moe_q4_0_q8_1(dw, da, di), kind)
+        torch.cuda.synchronize()
+        assert torch.equal(mid, mid2.view(mid.shape)), "fused layer 1 differs from matmul + activation"
+        assert ft.read_device_error() == 0
+    finally:
+        ft.set_path("auto")
+    mid_ref = _mid_ref(oracle, w13, act, ids, kind)
+    check_requantized(G.host(mid), mid_ref, None, min_equal=0.98, tie_window=None,
+                      what=f"fused {E},{k},{H},{I},{T}/{kind}/{path}")
+
+
+@pytest.mark.parametrize("path", ["gemm", "gemv"])
+def test_fused_layer1_bad_ids_and_canaries(ft, oracle, path):
+    """Bad expert ids give zero act_mid rows and the error flag; the bytes
+    before and after act_mid keep their pattern."""
+    import torch
+    E, k, H, I, T = 8, 2, 512, 160, 120
+    w13, _, x, ids = _ffn_case(E, k, H, I, T, 97)
+    ids = ids.copy()
+    ids[3, 1] = -1
+    ids[60, 0] = E
+    act = oracle.quantize_q8_1(x)
+    n = T * k * (I // 32) * 36
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 0x5A, dtype=torch.uint8, device="cuda")
+    mid = buf[guard:guard + n].view(T * k, I // 32, 36)
+    ft.set_path(path)
+    try:
+        ft.moe_q4_0_q8_1_act(G.dev(w13), G.dev(act), G.dev(ids), 0, out=mid)
+        torch.cuda.synchronize()
+        assert ft.read_device_error() == ft.FT_DEVERR_BAD_EXPERT_ID
+    finally:
+        ft.set_path("auto")
+    b = G.host(buf)
+    assert (b[:guard] == 0x5A).all() and (b[-guard:] == 0x5A).all(), "wrote outside act_mid"
+    got = G.host(mid)
+    valid = ((ids >= 0) & (ids < E)).reshape(-1)
+    assert not got[~valid].any()
+    mid_ref = _mid_ref(oracle, w13, act, ids, 0)
+    check_requantized(got[valid], mid_ref[valid], None, min_equal=0.98, tie_window=None, what=f"bad ids/{path}")
+
+
+@pytest.mark.parametrize("kind", [0, 1], ids=["silu", "gelu_tanh"])
+def test_ffn_fused_matches_oracle_and_the_unfused_chain(ft, oracle, kind):
+    import torch
+    w13, w2, x, ids = _ffn_case(16, 4, 2048, 768, 300, 98)
+    act = G.dev(oracle.quantize_q8_1(x))
+    dw13, dw2, dids = G.dev(w13), G.dev(w2), G.dev(ids)
+    out, h, mid = ft.moe_ffn_q4_0_q8_1(dw13, dw2, act, dids, kind, keep_h=False)
+    assert h is None
+    out2, _, mid2 = ft.moe_ffn_q4_0_q8_1(dw13, dw2, act, dids, kind)
+    torch.cuda.synchronize()
+    assert torch.equal(mid, mid2) and torch.equal(out, out2)
+
+
+def test_fused_layer1_full_size(ft, oracle):
+    """The 8192-token prefill batch of a 128-expert top-8 layer with hidden
+    2048 and 768 intermediate columns (Zipf routing): the fused layer 1 equals
+    matmul + activation bit for bit over all 65536 slot rows, and a seeded
+    sample of 64 slot rows matches the oracle within the requantization's
+    bounds."""
+    import torch
+    from bit_quantized_moe_quantize_gb300 import synth
+    E, k, H, I, T = 128, 8, 2048, 768, 8192
+    wl1 = synth.custom_workload(E, k, H, 2 * I, 3, routing="zipf")
+    w13, x, ids = synth.make_weights(wl1), synth.make_activations(wl1, T), synth.make_topk_ids(wl1, T)
+    dx = G.dev(x)
+    act = ft.quantize_q8_1(dx)
+    dw, di = G.dev(w13), G.dev(ids)
+    mid = ft.moe_q4_0_q8_1_act(dw, act, di, 0)
+    mid2 = ft.act_mul_quantize_q8_1(ft.moe_q4_0_q8_1(dw, act, di), 0)
+    torch.cuda.synchronize()
+    assert torch.equal(mid, mid2.view(mid.shape))
+    assert ft.read_device_error() == 0
+    pick = np.sort(np.random.default_rng(99).choice(T, 8, replace=False))
+    act_h = G.host(act)
+    ref = _mid_ref(oracle, w13, act_h[pick], ids[pick], 0)
+    got = G.host(mid).reshape(T, k, I // 32, 36)[pick].reshape(-1, I // 32, 36)
+    check_requantized(got, ref, None, min_equal=0.98, tie_window=None, what="fused full size")

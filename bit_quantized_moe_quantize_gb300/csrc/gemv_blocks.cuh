@@ -285,9 +285,9 @@ __device__ __forceinline__ float small_int_to_float(int v) {
 // rows.  Warp w handles rows w*RW .. w*RW+RW-1 of each stage, lane l the blocks
 // b = l, l + 32, ... of those rows, and every activation block it loads from
 // shared memory serves RW rows.  WT is the weight block type: per block
-//   d_w d_a (sum_i q_i q_a[i] - level0 * sum_i q_a[i])  +  m s_a
-// with q_i the stored level, the m term only for the types that store m
-// (s_a: the activation block's fp16 s, the sum the Q8_1 format stores for it).
+//   d_w d_a (sum_i q_i q_a[i] - level0 * sum_i q_a[i])  +  m d_a sum_i q_a[i]
+// with q_i the stored level, the m term only for the types that store m, and
+// the exact sum of the activation codes (never the Q8_1 block's rounded s).
 template <int WT, int G, int RW, bool DUMP>
 __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
     constexpr int R = 8 * RW;
@@ -355,10 +355,6 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
         dst[0] = q0;
         dst[1] = q1;
         da[g * nb + b] = __half2float(__ushort_as_half(static_cast<unsigned short>(ds & 0xFFFFu)));
-        if constexpr (HAS_M) {   // the offset term needs s, not the code sum
-            suma[g * nb + b] = __float_as_int(__half2float(__ushort_as_half(static_cast<unsigned short>(ds >> 16))));
-            continue;
-        }
         int sm = 0;
         sm = __dp4a(static_cast<int>(q0.x), 0x01010101, sm);
         sm = __dp4a(static_cast<int>(q0.y), 0x01010101, sm);
@@ -420,10 +416,12 @@ __global__ void __launch_bounds__(256) moe_gemv_kernel(const GemvArgs a) {
                         const uint4* av = reinterpret_cast<const uint4*>(qa + (static_cast<size_t>(g) * nb + b) * 32);
                         const uint4 A0 = av[0], A1 = av[1];
                         const float dag = da[g * nb + b];
-                        const int sa0 = HAS_M ? 0 : WBlock<WT>::level0 * suma[g * nb + b];
-                        // offset term's activation factor: s_a (Q4_1, Q5_1) or -d_a sum(q_a) (K-quants)
-                        const float sag = HAS_M ? __int_as_float(suma[g * nb + b])
-                                                : HAS_MIN ? -dag * small_int_to_float(suma[g * nb + b]) : 0.0f;
+                        const int sa0 = WBlock<WT>::level0 * suma[g * nb + b];
+                        // offset term's activation factor, with the exact code sum:
+                        // d_a sum(q_a) (Q4_1, Q5_1) or -d_a sum(q_a) (K-quant mins)
+                        const float sag = HAS_M     ? dag * small_int_to_float(suma[g * nb + b])
+                                          : HAS_MIN ? -dag * small_int_to_float(suma[g * nb + b])
+                                                    : 0.0f;
 #pragma unroll
                         for (int j = 0; j < RW; ++j) {
                             if constexpr (SPLIT) {   // two scale groups of 16 weights

@@ -272,10 +272,11 @@ FT_API int ft_moe_q4_0_q8_1_ep(const void* weights_local, const void* act, const
  * ft_moe_gguf_q8_1 - the routed matmul with expert weights of a GGUF type
  * (FT_TYPE_*; the per-type launchers of moe_vec.cuh on FreeToken PR #185,
  * "Notes"):
- *   out[s][r] = sum_b d_w d_a sum_i q_i q_a[i] + c s_a
+ *   out[s][r] = sum_b d_w d_a sum_i q_i q_a[i] + c d_a sum_i q_a[i]
  * per 32-weight block b of row r of expert topk_ids[s] and activation block b
- * of the slot's token, with q_i, c as in the FT_TYPE_* list and s_a the
- * activation block's stored fp16 s (c = 0 for Q4_0, Q5_0, Q8_0); for the
+ * of the slot's token, with q_i, c as in the FT_TYPE_* list (c = 0 for Q4_0,
+ * Q5_0, Q8_0) and the exact sum of the activation codes (the dequantized
+ * activation is d_a q_a; the stored fp16 s, that sum rounded, is not used); for the
  * K-quants, per sub-block b, d sc_b d_a sum_i q_i q_a[i] - dmin m_b d_a sum_i q_a[i]
  * (Q6_K, Q3_K: d d_a (sc_lo sum_{i<16} q_i q_a[i] + sc_hi sum_{i>=16} q_i q_a[i]);
  * Q2_K adds - dmin d_a (min_lo sum_{i<16} q_a[i] + min_hi sum_{i>=16} q_a[i])).

@@ -14,12 +14,16 @@
  * CURRENT_BUG.md, Bugs 2 and 4).  The pages do not print the block formats;
  * they are the GGUF Q4_0 / Q8_1 formats restated in ft_oracle.h.
  *
- * Readings where the pages are silent (all listed in the design notes):
+ * Readings where the pages are silent:
  *   - "round" is round-half-away-from-zero (C roundf);
  *   - Q8_1 divides by the fp32 scale amax/127, not by its fp16 value;
  *   - s = fp16(d32 * (float)sum(q)) with d32 the fp32 scale;
  *   - the dot uses the exact integer sum of (q_w - 8) * q_a per block and
  *     never the rounded s;
+ *   - for every weight type with an offset (the m of Q4_1 / Q5_1, the mins of
+ *     the K-quants) the offset term is m * d_a * sum(q_a): the dequantized
+ *     activation is d_a * q_a, so its block sum is d_a times the exact sum of
+ *     the codes; the stored s, that sum rounded to fp16, is never used;
  *   - slots whose expert id is out of range are left out of the routing and
  *     produce zero output rows.
  *
@@ -478,12 +482,15 @@ void oracle_moe_gguf_q8_1(int32_t type, const uint8_t* weights, const uint8_t* a
                 }
             } else if (e >= 0 && e < n_experts) {
                 for (int64_t b = 0; b < nb; ++b) {
+                    /* d_w d_a sum(q q_a) + m d_a sum(q_a), the exact sum of q_a */
                     const uint8_t* wb = weights + (((int64_t)e * nrows + r) * nb + b) * bytes;
                     const uint8_t* ab = act + (t * nb + b) * Q8_1_BYTES;
                     double dw = oracle_half_to_double(rd16(wb));
                     double da = oracle_half_to_double(rd16(ab));
-                    double sa = oracle_half_to_double(rd16(ab + 2));
-                    y += dw * da * (double)oracle_gguf_block_dot(type, wb, ab) + gguf_offset(wb, type) * sa;
+                    int32_t suma = 0;
+                    for (int l = 0; l < QK; ++l) suma += (int32_t)(int8_t)ab[4 + l];
+                    y += dw * da * (double)oracle_gguf_block_dot(type, wb, ab) +
+                         gguf_offset(wb, type) * da * (double)suma;
                 }
             }
             out[s * nrows + r] = (float)y;

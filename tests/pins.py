@@ -578,8 +578,9 @@ def pin_gguf_numpy_decode(o):
 
 def pin_gguf_moe_numpy(o):
     """The matmul of each type against a numpy restatement: per block
-    d_w d_a sum(q_w q_a) + m s_a with s_a the stored fp16 s, in fp64; and
-    against the plain dequantized dot within the fp16 rounding of s."""
+    d_w d_a sum(q_w q_a) + m d_a sum(q_a) with the exact code sum, in fp64;
+    and against the plain dot of the dequantized weights and activations,
+    which that is term for term (fp64 rounding only)."""
     from bit_quantized_moe_quantize_gb300 import synth
     rng = np.random.default_rng(4)
     E, k, K, N, T = 4, 2, 128, 6, 5
@@ -588,7 +589,7 @@ def pin_gguf_moe_numpy(o):
     ids = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
     qa = act[..., 4:].view(np.int8).astype(np.int64)
     da = act[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
-    sa = act[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
+    suma = qa.sum(axis=-1).astype(np.float64)                    # [T, nb]
     xa = numpy_decode_q8_1(act)
     for wtype in ("q4_1", "q5_0", "q5_1", "q8_0"):
         w = _gguf_random(wtype, E=E, N=N, K=K, seed=5)
@@ -599,11 +600,10 @@ def pin_gguf_moe_numpy(o):
             for j in range(k):
                 e = ids[t, j]
                 dots = np.einsum("rbi,bi->rb", lev[e], qa[t])
-                want = (d[e] * da[t] * dots + m[e] * sa[t]).sum(axis=1)
+                want = (d[e] * da[t] * dots + m[e] * da[t] * suma[t]).sum(axis=1)
                 assert np.allclose(got[t, j], want, rtol=1e-6, atol=1e-9), wtype
                 plain = wv[e] @ xa[t]
-                slack = (np.abs(m[e]) * (np.abs(sa[t]) * 2.0 ** -11 + 2.0 ** -24)).sum(axis=1)
-                assert np.all(np.abs(want - plain) <= slack + 1e-12), wtype
+                assert np.allclose(want, plain, rtol=1e-12, atol=1e-12), wtype
 
 
 def pin_gguf_q4_0_is_the_q4_0_matmul(o):

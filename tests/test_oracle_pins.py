@@ -59,7 +59,9 @@ MUTANTS = {
     "act_kind_swapped": ("if (kind == ORACLE_ACT_SILU)", "if (kind != ORACLE_ACT_SILU)"),
     "q5_high_bit_index": ("hi5 = (int)((qh >> i) & 1u);", "hi5 = (int)((qh >> (i % 16)) & 1u);"),
     "q5_0_offset_15": ("(type == ORACLE_GGUF_Q5_0 ? 16 : 0)", "(type == ORACLE_GGUF_Q5_0 ? 15 : 0)"),
-    "gguf_offset_term_dropped": ("+ gguf_offset(wb, type) * sa;", ";"),
+    "gguf_offset_term_dropped": (" +\n                         gguf_offset(wb, type) * da * (double)suma;", ";"),
+    "gguf_offset_uses_stored_s": ("gguf_offset(wb, type) * da * (double)suma;",
+                                  "gguf_offset(wb, type) * oracle_half_to_double(rd16(ab + 2));"),
     "q8_0_unsigned": ("return (int)(int8_t)blk[2 + i];", "return (int)blk[2 + i];"),
     "q4_1_m_read_as_d": ("return oracle_half_to_double(rd16(blk + 2));", "return oracle_half_to_double(rd16(blk));"),
     "q4_1_nibble_order": ("return i < 16 ? (blk[4 + i] & 0x0f) : (blk[4 + i - 16] >> 4);",

@@ -82,6 +82,9 @@ def parse():
                     help="one activation row per routed slot (ft_moe_q4_0_q8_1_slots, the second expert layer)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of a CUDA-graph replay of the step")
+    ap.add_argument("--wtype", default="q4_0",
+                    choices=["q4_0", "q4_1", "q5_0", "q5_1", "q8_0", "q4_k", "q5_k", "q6_k", "q2_k", "q3_k"],
+                    help="GGUF type of the expert weights (other than q4_0: ft_moe_gguf_q8_1, GEMV path)")
     ap.add_argument("--ffn", choices=["silu", "gelu_tanh"], default=None,
                     help="time both expert layers (ft_moe_ffn_q4_0_q8_1) with the workload's ncols as the hidden "
                          "size and its nrows as the intermediate size")
@@ -311,12 +314,18 @@ def ours(args):
     name, wl, T = workload(args.workload)
     w, x, ids = make_inputs(wl, T, rank)
     E, k, K, N = wl.n_experts, wl.top_k, wl.ncols, wl.nrows
+    wtype = args.wtype
+    if wtype != "q4_0":
+        if args.per_slot or args.impl == "reference":
+            raise SystemExit("--wtype takes the per-token matmul of our arm only")
+        from bit_quantized_moe_quantize_gb300 import synth
+        w = synth.make_weights_gguf(wl, wtype)
     S = T * k
     if args.per_slot:                       # one fp16 activation row per slot
         from bit_quantized_moe_quantize_gb300 import synth
         x = synth.make_activations(replica_workload(wl, rank), S)
     rows = S if args.per_slot else T
-    path = {1: "gemv", 2: "gemm"}[ft.selected_path(T, k, E, N, K)]
+    path = {1: "gemv", 2: "gemm"}[ft.selected_path(T, k, E, N, K)] if wtype == "q4_0" else "gemv"
 
     dw = torch.from_numpy(w).to(dev)
     dx = torch.from_numpy(x).to(dev)
@@ -328,6 +337,9 @@ def ours(args):
     stream = torch.cuda.current_stream()
 
     matmul = ft.moe_q4_0_q8_1_slots if args.per_slot else ft.moe_q4_0_q8_1
+    if wtype != "q4_0":
+        def matmul(dw_, act_, di_, out=None):
+            return ft.moe_gguf_q8_1(wtype, dw_, act_, di_, out=out)
 
     def step():
         ft.quantize_q8_1(dx, out=act)
@@ -439,7 +451,8 @@ def ours(args):
     flops = 2.0 * S * N * K
     counts = np.bincount(ids.reshape(-1), minlength=E)
     nb = K // 32
-    alg_bytes = int((counts > 0).sum()) * N * nb * 18 + rows * nb * 36 + S * N * 4
+    _, wbytes, wper = ft.WEIGHT_TYPES[wtype]
+    alg_bytes = int((counts > 0).sum()) * N * (K // wper) * wbytes + rows * nb * 36 + S * N * 4
     if path == "gemm":
         kern = "moe_gemm_tc_kernel"
         achieved = flops / (mm_ms / 1000.0) / 1e12
@@ -449,8 +462,9 @@ def ours(args):
                 "algorithmic": f"2*S*N*K = {flops:.4g} FLOP per launch", "kernel_ms": mm_ms}
     else:
         # the library's GEMV plan: one weight row per lane when rows are whole
-        # 16-byte chunks, else one block per lane
-        kern = "moe_gemv_rows_kernel" if K % 256 == 0 else "moe_gemv_kernel"
+        # 256-weight runs (all types but Q6_K, Q2_K, Q3_K), else one block per lane
+        rows_ok = K % 256 == 0 and wtype not in ("q6_k", "q2_k", "q3_k")
+        kern = "moe_gemv_rows_kernel" if rows_ok else "moe_gemv_kernel"
         achieved = alg_bytes / (mm_ms / 1000.0) / 1e9
         roof = {"kernel": kern, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_note": f"copy bandwidth, of {peak_src}",
@@ -460,7 +474,7 @@ def ours(args):
     roof["traffic"] = tr
 
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and world == 1 and wtype == "q4_0":
         cores = host_cores()
         tps, n, dt = oracle_tokens_per_s(wl, w, x, ids, budget_s=10.0, threads=cores)
         tps1, n1, dt1 = oracle_tokens_per_s(wl, w, x, ids, budget_s=6.0)
@@ -477,9 +491,10 @@ def ours(args):
         "vs_baseline": (value / base) if base else None,
         "vs_baseline_note": "pages' Tesla T4 moe_vec time for this token count (context, other hardware)"
         if base else None,
-        "dtype": "q4_0 x q8_1: exact int block dots (f16 MMA / dp4a), f32 scaling",
+        "dtype": f"{wtype} x q8_1: exact int block dots (f16 MMA / dp4a), f32 scaling",
         "data": "synthetic", "config": {**config_of(name, wl, T, world), "path": path, "launch": launch_mode,
-                                        "activations": "per slot" if args.per_slot else "per token"},
+                                        "activations": "per slot" if args.per_slot else "per token",
+                                        "weights": wtype},
         "effective_tops": 2.0 * S * N * K * world / (ms / 1000.0) / 1e12,
         "kernels_ms_per_step": {"quantize": prof["quantize_ms"] / calls, "prepare": prof["route_ms"] / calls,
                                 "matmul": mm_ms,

@@ -81,6 +81,10 @@ GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t nc
 // the weights it holds (32, or 256 for the K-quant super-blocks)
 int weight_block_bytes(int wtype);
 int weight_block_values(int wtype);
+// Row-per-lane GEMV kernel: bytes of a row's 256 weights of a FT_TYPE_* type
+// and their pitch in a shared-memory box (0: the type does not run there).
+int row_box_bytes(int wtype);
+int row_box_pitch(int wtype);
 
 int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act, const int32_t* perm,
                 const int32_t* offsets, const int32_t* tiles, float* out, int32_t* dots, uint32_t* err,

@@ -53,10 +53,14 @@ def _check(ft, oracle, wtype, w, x, ids, what):
 
 
 # (E, k, K, N, T): tiny; 3 blocks per row (rows of 60-102 bytes, not 16-byte
-# aligned: 2-byte copies instead of bulk copies); 8-slot tiles; a top-8 decode
-# step with Zipf routing
+# aligned: 2-byte copies instead of bulk copies, block-per-lane kernel);
+# 8-slot tiles; a top-8 decode step with Zipf routing; rows of 1280 weights
+# and a ragged row count (row-per-lane kernel with 2- and 4-slot tiles and
+# the K range split); the block-per-lane kernel on 800-weight rows
 CASES = [(8, 2, 256, 128, 16, 90, "uniform"), (5, 2, 96, 50, 77, 91, "uniform"),
-         (8, 2, 512, 256, 1000, 92, "uniform"), (128, 8, 2048, 768, 8, 93, "zipf")]
+         (8, 2, 512, 256, 1000, 92, "uniform"), (128, 8, 2048, 768, 8, 93, "zipf"),
+         (16, 2, 1280, 200, 24, 98, "uniform"), (4, 2, 1280, 72, 7, 99, "uniform"),
+         (6, 2, 800, 100, 20, 100, "uniform")]
 
 
 @pytest.mark.parametrize("wtype", TYPES)
@@ -112,9 +116,10 @@ def test_gguf_rejects_what_the_path_cannot_run(ft, oracle):
             ft.moe_gguf_q8_1("q8_0", dw, act, di)
     finally:
         ft.set_path(prev)
-    # rows of 32768 Q8_0 columns: one ring stage of 8 rows does not fit in shared memory
-    big = torch.zeros((2, 8, 1024, 34), dtype=torch.uint8, device="cuda")
-    xb = torch.zeros((1, 1024, 36), dtype=torch.uint8, device="cuda")
+    # rows of 32736 Q8_0 columns (not a whole number of 256-weight runs, so the
+    # block-per-lane kernel): one ring stage of 8 rows does not fit in shared memory
+    big = torch.zeros((2, 8, 1023, 34), dtype=torch.uint8, device="cuda")
+    xb = torch.zeros((1, 1023, 36), dtype=torch.uint8, device="cuda")
     ib = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
     with pytest.raises(ft.FtError, match="shared memory"):
         ft.moe_gguf_q8_1("q8_0", big, xb, ib)

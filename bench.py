@@ -80,6 +80,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--per-slot", action="store_true",
                     help="one activation row per routed slot (ft_moe_q4_0_q8_1_slots, the second expert layer)")
+    ap.add_argument("--two-calls", action="store_true",
+                    help="time ft_quantize_q8_1 + ft_moe_q4_0_q8_1 instead of the single entry point ft_moe_q4_0_fp16")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of a CUDA-graph replay of the step")
     ap.add_argument("--wtype", default="q4_0",
@@ -341,7 +343,14 @@ def ours(args):
         def matmul(dw_, act_, di_, out=None):
             return ft.moe_gguf_q8_1(wtype, dw_, act_, di_, out=out)
 
+    # the hot path from fp16 activations: one call (one launch for a decode
+    # batch), or the quantizer and the matmul called one after the other
+    one_call = not args.two_calls and not args.per_slot and wtype == "q4_0"
+
     def step():
+        if one_call:
+            ft.moe_q4_0_fp16(dw, dx, di, out=out)
+            return
         ft.quantize_q8_1(dx, out=act)
         matmul(dw, act, di, out=out)
 
@@ -453,6 +462,9 @@ def ours(args):
     nb = K // 32
     _, wbytes, wper = ft.WEIGHT_TYPES[wtype]
     alg_bytes = int((counts > 0).sum()) * N * (K // wper) * wbytes + rows * nb * 36 + S * N * 4
+    fused = one_call and path == "gemv" and launches_per_step == 1
+    if fused:   # one launch reads the fp16 rows instead of Q8_1 blocks
+        alg_bytes += rows * K * 2 - rows * nb * 36
     if path == "gemm":
         kern = "moe_gemm_tc_kernel"
         achieved = flops / (mm_ms / 1000.0) / 1e12
@@ -464,11 +476,12 @@ def ours(args):
         # the library's GEMV plan: one weight row per lane when rows are whole
         # 256-weight runs (all types but Q6_K, Q2_K, Q3_K), else one block per lane
         rows_ok = K % 256 == 0 and wtype not in ("q6_k", "q2_k", "q3_k")
-        kern = "moe_gemv_rows_kernel" if rows_ok else "moe_gemv_kernel"
+        kern = ("moe_gemv_rows_kernel<fused>" if fused else "moe_gemv_rows_kernel") if rows_ok else "moe_gemv_kernel"
         achieved = alg_bytes / (mm_ms / 1000.0) / 1e9
         roof = {"kernel": kern, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_note": f"copy bandwidth, of {peak_src}",
-                "algorithmic": f"unique expert weights + Q8_1 act + fp32 out = {alg_bytes} B per launch",
+                "algorithmic": f"unique expert weights + {'fp16 x' if fused else 'Q8_1 act'} + fp32 out = "
+                               f"{alg_bytes} B per launch",
                 "kernel_ms": mm_ms}
     tr = NCU_TRAFFIC.get((kern, kernel_source_hash(GEMM_SOURCES), args.workload)) if path == "gemm" else None
     roof["traffic"] = tr
@@ -494,6 +507,7 @@ def ours(args):
         "dtype": f"{wtype} x q8_1: exact int block dots (f16 MMA / dp4a), f32 scaling",
         "data": "synthetic", "config": {**config_of(name, wl, T, world), "path": path, "launch": launch_mode,
                                         "activations": "per slot" if args.per_slot else "per token",
+                                        "entry": "ft_moe_q4_0_fp16" if one_call else "ft_quantize_q8_1 + matmul",
                                         "weights": wtype},
         "effective_tops": 2.0 * S * N * K * world / (ms / 1000.0) / 1e12,
         "kernels_ms_per_step": {"quantize": prof["quantize_ms"] / calls, "prepare": prof["route_ms"] / calls,

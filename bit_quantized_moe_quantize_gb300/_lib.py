@@ -30,7 +30,8 @@ EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_m
            "ft_moe_selected_path", "ft_moe_block_dots", "ft_last_error", "ft_abi_version", "ft_profile_enable",
            "ft_profile_read", "ft_moe_route_offsets_noalloc", "ft_moe_q4_0_q8_1_slots",
            "ft_moe_q4_0_q8_1_ep", "ft_act_mul_quantize_q8_1", "ft_moe_ffn_q4_0_q8_1", "ft_moe_gguf_q8_1",
-           "ft_repack_q4_0_soa", "ft_debug_wait_timeout", "ft_moe_q4_0_q8_1_act", "ft_moe_ffn_reserve")
+           "ft_repack_q4_0_soa", "ft_debug_wait_timeout", "ft_moe_q4_0_q8_1_act", "ft_moe_ffn_reserve",
+           "ft_moe_q4_0_fp16")
 
 
 class FtError(RuntimeError):
@@ -62,6 +63,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.ft_moe_route_offsets_noalloc.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp, vp]
         L.ft_moe_q4_0_q8_1.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_moe_q4_0_q8_1_slots.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
+        L.ft_moe_q4_0_fp16.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_moe_q4_0_q8_1_ep.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, vp]
         L.ft_moe_block_dots.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_act_mul_quantize_q8_1.argtypes = [vp, vp, i64, i64, i32, vp]
@@ -280,6 +282,27 @@ def act_mul_quantize_q8_1(h, act_kind, out=None):
     if out.numel() != rows * (two_i // 64) * 36:
         raise ValueError(f"out must hold {rows} x {two_i // 64} Q8_1 blocks")
     _check(load().ft_act_mul_quantize_q8_1(ph, po, rows, two_i // 2, int(act_kind), _stream(h)))
+    return out
+
+
+def moe_q4_0_fp16(weights, x, topk_ids, out=None):
+    """The whole hot path from fp16 rows (ft_moe_q4_0_fp16): Q4_0 [E, N, K/32, 18]
+    x fp16 [T, K] -> fp32 [T, k, N]; one launch for decode-sized batches."""
+    torch = _torch()
+    _dev(weights, torch.uint8, "weights", 4)
+    px = _dev(x, torch.float16, "x", 2)
+    _dev(topk_ids, torch.int32, "topk_ids", 2)
+    E, N, nb, wb = weights.shape
+    T, K = x.shape
+    if wb != 18 or nb * 32 != K or topk_ids.shape[0] != T:
+        raise ValueError(f"shape mismatch: weights {tuple(weights.shape)} x {tuple(x.shape)} "
+                         f"topk_ids {tuple(topk_ids.shape)}")
+    k = topk_ids.shape[1]
+    if out is None:
+        out = torch.empty((T, k, N), dtype=torch.float32, device=weights.device)
+    po = _dev(out, torch.float32, "out")
+    _check(load().ft_moe_q4_0_fp16(ctypes.c_void_p(weights.data_ptr()), px, ctypes.c_void_p(topk_ids.data_ptr()),
+                                   po, T, k, E, N, K, _stream(weights)))
     return out
 
 

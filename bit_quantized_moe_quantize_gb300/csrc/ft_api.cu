@@ -214,14 +214,16 @@ static int get_stream_capturing(cudaStream_t s, bool* capturing) {
 //   err word | counts[E] | offsets[E+1] | perm[S] | tiles_gemv[E+1] |
 //   tiles_gemm[E+1] | hist[nchunks][E] | (tensor-core path only:)
 //   xh[S_pad][ncols] fp16 | da[S_pad][ncols/32] fp16 | (layer 1 with the
-//   activation fused, on the GEMV path:) h[S][2 n_inter] fp32
+//   activation fused, on the GEMV path:) h[S][2 n_inter] fp32 | (the fp16
+//   entry point, unless it runs in one launch:) act[T][ncols/32] Q8_1
 struct WsLayout {
-    size_t err, counts, offsets, perm, tiles_gemv, tiles_gemm, hist, xh, da, h, total;
+    size_t err, counts, offsets, perm, tiles_gemv, tiles_gemm, hist, xh, da, h, act, total;
 };
 
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
-static WsLayout ws_layout(int64_t n_slots, int32_t n_experts, int64_t gemm_ncols = 0, size_t h_bytes = 0) {
+static WsLayout ws_layout(int64_t n_slots, int32_t n_experts, int64_t gemm_ncols = 0, size_t h_bytes = 0,
+                          size_t act_bytes = 0) {
     WsLayout L{};
     size_t o = 0;
     L.err = o;
@@ -245,6 +247,8 @@ static WsLayout ws_layout(int64_t n_slots, int32_t n_experts, int64_t gemm_ncols
     o = al256(o + 2 * rows * static_cast<size_t>(gemm_ncols / 32));
     L.h = o;
     o = al256(o + h_bytes);
+    L.act = o;
+    o = al256(o + act_bytes);
     L.total = o;
     return L;
 }
@@ -353,8 +357,16 @@ static int64_t gemv_max_slots(const Shape& sh) {
 // af->n_inter, out unused): the tensor-core path applies it in its epilogue;
 // the GEMV path writes the layer-1 result to workspace and runs the
 // activation/requantize step on it.
+// Bytes of the Q8_1 activation rows of a call (T rows of ncols / 32 blocks).
+static size_t act_rows_bytes(const Shape& sh) {
+    return static_cast<size_t>(sh.tokens) * static_cast<size_t>(sh.nb) * 36;
+}
+
+// x16 != nullptr: the activations come as fp16 rows [tokens][ncols] (act is
+// unused): a decode-sized batch on the GEMV path runs as one launch that
+// routes and quantizes per CTA; anything else quantizes into workspace first.
 static int run_matmul(const void* weights, const void* act, const int32_t* topk_ids, float* out, int32_t* dots,
-                      const Shape& sh, cudaStream_t s, const ActFuse* af = nullptr) {
+                      const Shape& sh, cudaStream_t s, const ActFuse* af = nullptr, const void* x16 = nullptr) {
     const int path = choose_path(sh, path_setting());
     if (path == FT_PATH_GEMM && sh.wtype != FT_TYPE_Q4_0)
         return fail(FT_ERR_ARG, "the tensor-core path takes Q4_0 weights only (weight type %d)", sh.wtype);
@@ -362,10 +374,31 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
         return fail(FT_ERR_ARG, "the tensor-core path needs ncols %% 256 == 0 and n_experts * nrows >= 128 (got %lld, %lld)",
                     (long long)sh.ncols, (long long)sh.n_experts * sh.nrows);
     const bool h_in_ws = af && path == FT_PATH_GEMV;
+    const GemvPlan gp = plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols, sh.mean(), sh.wtype);
+    const bool one_launch = x16 && !af && !dots && path == FT_PATH_GEMV && sh.wtype == FT_TYPE_Q4_0 &&
+                            sh.act_div == sh.top_k && sh.n_global == sh.n_experts && aligned(x16, 16) &&
+                            gp.smem <= 227 * 1024 && gemv_fused_ok(gp, sh.n_slots, sh.n_experts, sh.ncols);
     const WsLayout L = ws_layout(sh.n_slots, sh.n_experts, path == FT_PATH_GEMM ? sh.ncols : 0,
-                                 h_in_ws ? 4 * static_cast<size_t>(sh.n_slots) * sh.nrows : 0);
+                                 h_in_ws ? 4 * static_cast<size_t>(sh.n_slots) * sh.nrows : 0,
+                                 x16 && !one_launch ? act_rows_bytes(sh) : 0);
     uint8_t* ws = nullptr;
     if (int st = ws_acquire(L.total, s, &ws)) return st;
+    if (one_launch) {
+        prof_mark(kProfRouteBegin, s);
+        prof_mark(kProfMatmulBegin, s);
+        const int st = launch_gemv_fused(gp, static_cast<const uint8_t*>(weights), static_cast<const uint16_t*>(x16),
+                                         topk_ids, out, reinterpret_cast<uint32_t*>(ws + L.err), sh.n_slots,
+                                         sh.top_k, sh.n_experts, sh.nrows, sh.ncols, s);
+        prof_mark(kProfMatmulEnd, s);
+        return st;
+    }
+    if (x16) {
+        prof_mark(kProfQuantBegin, s);
+        const int st = launch_quantize_q8_1(x16, ws + L.act, sh.tokens, sh.ncols, s);
+        prof_mark(kProfQuantEnd, s);
+        if (st) return st;
+        act = ws + L.act;
+    }
     if (h_in_ws) out = reinterpret_cast<float*>(ws + L.h);
     RouteBuffers rb{};
     rb.counts = reinterpret_cast<int32_t*>(ws + L.counts);
@@ -376,7 +409,6 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     rb.tiles_gemm = reinterpret_cast<int32_t*>(ws + L.tiles_gemm);
     rb.err = reinterpret_cast<uint32_t*>(ws + L.err);
 
-    const GemvPlan gp = plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols, sh.mean(), sh.wtype);
     const int tile_width = gemm_tile_width(sh.mean());
     if (path == FT_PATH_GEMV && (gp.smem > 227 * 1024 || gp.stages < 1))
         return fail(FT_ERR_SIZE, "GEMV tile needs %zu bytes of shared memory (%d ring stages of %lld-column rows fit)",
@@ -514,6 +546,19 @@ int ft_moe_q4_0_q8_1(const void* weights, const void* act, const int32_t* topk_i
         return fail(FT_ERR_ARG, "null pointer");
     }
     return matmul_entry(weights, act, topk_ids, out, nullptr, tokens, top_k, n_experts, nrows, ncols, stream);
+}
+
+int ft_moe_q4_0_fp16(const void* weights, const void* x_fp16, const int32_t* topk_ids, float* out, int64_t tokens,
+                     int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols, void* stream) {
+    g_last_error.clear();
+    Shape sh{};
+    if (int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh)) return st;
+    if (sh.n_slots == 0) return FT_OK;
+    if (!weights || !x_fp16 || !topk_ids || !out) return fail(FT_ERR_ARG, "null pointer");
+    if (!aligned(weights, 16)) return fail(FT_ERR_ALIGN, "weights must be 16-byte aligned");
+    if (!aligned(x_fp16, 8) || !aligned(topk_ids, 4) || !aligned(out, 4))
+        return fail(FT_ERR_ALIGN, "x_fp16 must be 8-byte, topk_ids and out 4-byte aligned");
+    return run_matmul(weights, nullptr, topk_ids, out, nullptr, sh, static_cast<cudaStream_t>(stream), nullptr, x_fp16);
 }
 
 int ft_moe_q4_0_q8_1_ep(const void* weights_local, const void* act, const int32_t* topk_ids, float* out,
@@ -677,7 +722,7 @@ size_t ft_moe_workspace_bytes(int64_t tokens, int32_t top_k, int32_t n_experts, 
     const int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh);
     g_last_error = keep;
     if (st) return 0;
-    return ws_layout(sh.n_slots, sh.n_experts, gemm_shape_ok(sh) ? sh.ncols : 0).total;
+    return ws_layout(sh.n_slots, sh.n_experts, gemm_shape_ok(sh) ? sh.ncols : 0, 0, act_rows_bytes(sh)).total;
 }
 
 int ft_moe_reserve(int64_t max_tokens, int32_t max_top_k, int32_t n_experts, int64_t nrows, int64_t ncols) {
@@ -685,7 +730,8 @@ int ft_moe_reserve(int64_t max_tokens, int32_t max_top_k, int32_t n_experts, int
     Shape sh{};
     if (int st = check_matmul_args(max_tokens, max_top_k, n_experts, nrows, ncols, &sh)) return st;
     uint8_t* base = nullptr;
-    return ws_acquire(ws_layout(sh.n_slots, sh.n_experts, gemm_shape_ok(sh) ? sh.ncols : 0).total, nullptr, &base);
+    return ws_acquire(ws_layout(sh.n_slots, sh.n_experts, gemm_shape_ok(sh) ? sh.ncols : 0, 0, act_rows_bytes(sh)).total,
+                      nullptr, &base);
 }
 
 int ft_moe_release(void) {

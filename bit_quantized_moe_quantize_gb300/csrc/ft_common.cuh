@@ -64,6 +64,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Barrier `id` (1..15) over the first `threads` threads of the CTA (a
+// multiple of 32): __syncthreads for a subset of the warps, used only where
+// none of them can leave before reaching it.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // Bounded wait for the phase with the given parity.  Returns false (and
 // raises FT_DEVERR_WAIT_TIMEOUT) if the phase did not complete within
 // limit_ns of %globaltimer.

@@ -91,6 +91,15 @@ int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act
                 int64_t n_slots, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols, cudaStream_t s,
                 int wtype = FT_TYPE_Q4_0);
 
+// The decode step in one launch (moe_decode.cu): the row-per-lane GEMV with
+// the routing and the activation quantizer done per CTA, from fp16 x
+// [tokens][ncols] and the ids; Q4_0 weights.  gemv_fused_ok: whether the plan
+// and sizes allow it (and it pays off).
+bool gemv_fused_ok(const GemvPlan& plan, int64_t n_slots, int32_t n_experts, int64_t ncols);
+int launch_gemv_fused(const GemvPlan& plan, const uint8_t* weights, const uint16_t* x, const int32_t* ids,
+                      float* out, uint32_t* err, int64_t n_slots, int32_t top_k, int32_t n_experts, int64_t nrows,
+                      int64_t ncols, cudaStream_t s);
+
 // ------------------------------------------------------------------ GEMM
 constexpr int kGemmBN = 128;   // slots per tile
 constexpr int kGemmBM = 128;   // weight rows per tile

@@ -30,6 +30,11 @@ struct GemvArgs {
     int32_t bulk;        // weight rows 16-byte aligned -> bulk copies
     int32_t row_warps;   // row-per-lane kernel: row groups of 32 per CTA
     int32_t ksplit;      // row-per-lane kernel: warps sharing a row group, each on every ksplit-th box
+    // decode step in one launch (row-per-lane kernel, FUSED): the kernel routes
+    // the n_slots ids itself and quantizes the fp16 rows x [tokens][nb * 32]
+    const uint16_t* x;
+    const int32_t* ids;
+    int64_t n_slots;
 };
 
 constexpr int kMaxStages = 4;

@@ -36,6 +36,7 @@
 #include <cuda_fp16.h>
 
 #include "gemv_blocks.cuh"
+#include "q8_1_math.cuh"
 
 namespace ft {
 
@@ -66,11 +67,12 @@ struct RowPart {
 };
 
 // Shared memory: mbarriers full/empty [kMaxRowStages] and red_full/red_empty
-// [2] | slot ids int32[G] | qa [G][nb][32] | aux float2 [G][nb] | partial sums
-// [2][ksplit-1][row warps][32][G] fp32 | ring of boxes (128-byte aligned,
-// PITCH x 32 * row warps bytes each).
+// [2] | slot ids int32[G] | 4 words (the one-launch routing's result) | qa
+// [G][nb][32] | aux float2 [G][nb] | partial sums [2][ksplit-1][row
+// warps][32][G] fp32 | ring of boxes (128-byte aligned, PITCH x 32 * row
+// warps bytes each).
 __host__ __device__ inline size_t gemv_rows_qa_offset(int G) {
-    return (8 * (2 * kMaxRowStages + 4) + static_cast<size_t>(G) * 4 + 15) / 16 * 16;
+    return (8 * (2 * kMaxRowStages + 4) + static_cast<size_t>(G) * 4 + 16 + 15) / 16 * 16;
 }
 __host__ __device__ inline size_t gemv_rows_red_offset(int G, int nb) {
     return gemv_rows_qa_offset(G) + static_cast<size_t>(G) * nb * 40;
@@ -151,7 +153,101 @@ __device__ __forceinline__ void decode_win(const uint32_t (&w)[NW], int o, int j
     }
 }
 
-template <int WT, int G, bool DUMP>
+// Limits of the one-launch decode step (FUSED): its routing scratch, ids
+// [n_slots] | counts [E], lives in the weight ring before the first box
+// arrives.
+constexpr int kFuseMaxSlots = 512;
+constexpr int kFuseMaxExperts = 1024;
+__host__ __device__ inline size_t gemv_fused_scratch_bytes(int64_t n_slots, int32_t n_experts) {
+    return 4 * (static_cast<size_t>(n_slots) + n_experts);
+}
+
+// The routing of the one-launch decode step, done by each CTA for itself:
+// the stable counting sort of the router restricted to what slot tile t
+// needs.  All threads load the ids and count them per expert (ids outside
+// [0, E) are left out; the CTAs of slot-tile column 0 zero their output rows
+// over the row groups they own, and one raises the device error flag); warp 0
+// scans ceil(count / G) over the experts to find the expert e owning tile t
+// (tiles in expert order, searchsorted(right=True) as with the router's
+// prefix), then lists that expert's slots of ranks [r0, r0 + G) in ascending
+// slot order.  Returns false where t is past the last tile (uniform).
+template <int G>
+__device__ __forceinline__ bool fused_route(const GemvArgs& a, int32_t t, int32_t* scratch, int32_t* slot,
+                                            int64_t my_groups, int32_t rows_per_group, int32_t& e, int32_t& ng) {
+    const int32_t S = static_cast<int32_t>(a.n_slots), E = a.n_experts;
+    int32_t* ids = scratch;
+    int32_t* cnt = scratch + S;
+    int32_t* info = slot + G;                             // outside the ring the weights arrive in
+    for (int32_t i = threadIdx.x; i < S; i += blockDim.x) ids[i] = __ldg(a.ids + i);
+    for (int32_t i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+    bool bad = false;
+    for (int32_t i = threadIdx.x; i < S; i += blockDim.x) {
+        const int32_t id = ids[i];
+        if (id >= 0 && id < E) atomicAdd(&cnt[id], 1);
+        else bad = true;
+    }
+    bad = __syncthreads_or(bad);
+    if (bad && blockIdx.x == 0) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.err, FT_DEVERR_BAD_EXPERT_ID);
+        for (int32_t s = 0; s < S; ++s) {
+            const int32_t id = ids[s];
+            if (id >= 0 && id < E) continue;
+            for (int64_t gi = 0; gi < my_groups; ++gi) {
+                const int64_t r0 = (blockIdx.y + gi * gridDim.y) * rows_per_group;
+                for (int32_t r = threadIdx.x; r < rows_per_group; r += blockDim.x)
+                    if (r0 + r < a.nrows) a.out[static_cast<int64_t>(s) * a.nrows + r0 + r] = 0.0f;
+            }
+        }
+    }
+    if (threadIdx.x < 32) {
+        const uint32_t lane = threadIdx.x;
+        int32_t base = 0, fe = -1, fr0 = 0;
+        for (int32_t c0 = 0; c0 < E; c0 += 32) {
+            const int32_t ee = c0 + static_cast<int32_t>(lane);
+            const int32_t n = ee < E ? (cnt[ee] + G - 1) / G : 0;
+            int32_t inc = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                if (static_cast<int>(lane) >= o) inc += y;
+            }
+            const int32_t excl = base + inc - n;
+            if (n > 0 && t >= excl && t < excl + n) {
+                fe = ee;
+                fr0 = (t - excl) * G;
+            }
+            base += __shfl_sync(0xFFFFFFFFu, inc, 31);
+        }
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, fe >= 0);
+        if (m) {
+            const int src = __ffs(m) - 1;
+            fe = __shfl_sync(0xFFFFFFFFu, fe, src);
+            fr0 = __shfl_sync(0xFFFFFFFFu, fr0, src);
+            if (lane < G) slot[lane] = 0;
+            __syncwarp();
+            int32_t rank0 = 0;
+            for (int32_t c0 = 0; c0 < S; c0 += 32) {
+                const int32_t s = c0 + static_cast<int32_t>(lane);
+                const bool hit = s < S && ids[s] == fe;
+                const uint32_t bm = __ballot_sync(0xFFFFFFFFu, hit);
+                const int32_t rank = rank0 + __popc(bm & ((1u << lane) - 1u));
+                if (hit && rank >= fr0 && rank < fr0 + G) slot[rank - fr0] = s;
+                rank0 += __popc(bm);
+            }
+        }
+        if (lane == 0) {
+            info[0] = m ? fe : -1;
+            info[1] = m ? min(G, cnt[fe] - fr0) : 0;
+        }
+    }
+    __syncthreads();
+    e = info[0];
+    ng = info[1];
+    return e >= 0;
+}
+
+template <int WT, int G, bool DUMP, bool FUSED>
 __global__ void __launch_bounds__(288) moe_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap,
                                                              const GemvArgs a) {
     using BX = RowBox<WT>;
@@ -162,12 +258,17 @@ __global__ void __launch_bounds__(288) moe_gemv_rows_kernel(const __grid_constan
     static_assert(!DUMP || WT == FT_TYPE_Q4_0, "block dots are a Q4_0 diagnostic");
     const int32_t RW = a.row_warps, KS = a.ksplit;
     const int32_t n_compute = RW * KS;
+    static_assert(!(DUMP && FUSED), "block dots come from the routed form");
     const int64_t t = blockIdx.x;
     const int32_t E = a.n_experts;
-    if (t >= a.tiles[E]) return;
-    const int32_t e = find_expert(a.tiles, E, t);
-    const int64_t p0 = static_cast<int64_t>(a.offsets[e]) + (t - a.tiles[e]) * G;
-    const int32_t ng = static_cast<int32_t>(min(static_cast<int64_t>(G), a.offsets[e + 1] - p0));
+    int32_t e = 0, ng = 0;
+    int64_t p0 = 0;
+    if constexpr (!FUSED) {
+        if (t >= a.tiles[E]) return;
+        e = find_expert(a.tiles, E, t);
+        p0 = static_cast<int64_t>(a.offsets[e]) + (t - a.tiles[e]) * G;
+        ng = static_cast<int32_t>(min(static_cast<int64_t>(G), a.offsets[e + 1] - p0));
+    }
     const int32_t nb = a.nb;
     const int32_t n_ks = nb / 8;                          // boxes per row
     const int NS = a.stages;
@@ -185,7 +286,6 @@ __global__ void __launch_bounds__(288) moe_gemv_rows_kernel(const __grid_constan
     float* red = reinterpret_cast<float*>(smem_rows + gemv_rows_red_offset(G, nb));   // [2][KS-1][RW][32][G]
     uint8_t* ring = smem_rows + gemv_rows_ring_offset(G, nb, RW, KS);
     const uint32_t stage_bytes = static_cast<uint32_t>(PITCH * 32 * RW);
-
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
@@ -198,13 +298,77 @@ __global__ void __launch_bounds__(288) moe_gemv_rows_kernel(const __grid_constan
         }
         fence_mbar_init();
     }
-    if (threadIdx.x < G) slot[threadIdx.x] = threadIdx.x < ng ? a.perm[p0 + threadIdx.x] : 0;
-    __syncthreads();
+    if constexpr (FUSED) {
+        // the routing's barriers also publish the mbarriers; the producer then
+        // starts streaming at once while the compute warps quantize
+        if (!fused_route<G>(a, static_cast<int32_t>(t), reinterpret_cast<int32_t*>(ring), slot, my_groups, 32 * RW,
+                            e, ng))
+            return;
+    } else {
+        if (threadIdx.x < G) slot[threadIdx.x] = threadIdx.x < ng ? a.perm[p0 + threadIdx.x] : 0;
+        __syncthreads();
+    }
 
     // stage the G activation rows once: 32 int8 as two 16-byte chunks and
     // aux = {d_a, level0 * sum q (int bits: the dot starts from its negative)}
     // for Q4_0 / Q5_0, {d_a, d_a * sum q} for the types with an offset term
-    for (int32_t i = threadIdx.x; i < G * nb; i += blockDim.x) {
+    if constexpr (FUSED) {
+        // the one-launch decode step quantizes the slots' fp16 rows itself with
+        // the quantizer's arithmetic and lane layout (eight lanes per block,
+        // four values each), so the same codes; d rounded to fp16 as stored
+        const uint32_t sub = lane & 7u, gmask = 0xFFu << (lane & 24u);
+        const int32_t n_items = G * nb;
+        // each warp takes 4 blocks at a time (one per 8 lanes), FU of them in a
+        // batch whose loads are all issued before any is used
+        constexpr int FU = 4;
+        for (int32_t base = static_cast<int32_t>(warp) * 4 * FU;
+             base < n_items && static_cast<int32_t>(warp) < n_compute; base += n_compute * 4 * FU) {
+            uint2 raw[FU];
+#pragma unroll
+            for (int u = 0; u < FU; ++u) {
+                const int32_t i = base + 4 * u + static_cast<int32_t>(lane >> 3);
+                const int32_t g = i / nb, b = i - g * nb;
+                raw[u] = make_uint2(0, 0);
+                if (i < n_items && g < ng) {
+                    const int64_t tok = slot[g] / a.top_k;
+                    raw[u] = __ldg(reinterpret_cast<const uint2*>(a.x + (tok * nb + b) * QK) + sub);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < FU; ++u) {
+                const int32_t i = base + 4 * u + static_cast<int32_t>(lane >> 3);
+                const int32_t g = i / nb, b = i - g * nb;
+                const bool live = i < n_items && g < ng;
+                const __half2 h01 = *reinterpret_cast<const __half2*>(&raw[u].x);
+                const __half2 h23 = *reinterpret_cast<const __half2*>(&raw[u].y);
+                const float v[4] = {__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23)};
+                float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, o));
+                const float d32 = __fdiv_rn(amax, 127.0f);
+                int q[4];
+                q8_codes<4>(v, amax, d32, q);
+                uint32_t packed = 0;
+                int sm = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    sm += q[j];
+                    packed |= (static_cast<uint32_t>(q[j]) & 0xFFu) << (8 * j);
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) sm += __shfl_xor_sync(gmask, sm, o);
+                if (i < n_items) {
+                    reinterpret_cast<uint32_t*>(qa)[(static_cast<size_t>(g) * nb + b) * 8 + sub] = packed;
+                    if (sub == 0) {
+                        const float d = live ? __half2float(__float2half_rn(d32)) : 0.0f;
+                        const float y = OFFSET ? d * small_int_to_float(sm) : __int_as_float(LEVEL0 * sm);
+                        aux[static_cast<size_t>(g) * nb + b] = make_float2(d, y);
+                    }
+                }
+            }
+        }
+    }
+    for (int32_t i = threadIdx.x; i < G * nb && !FUSED; i += blockDim.x) {
         const int32_t g = i / nb, b = i - g * nb;
         uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
         float d = 0.0f;
@@ -230,7 +394,11 @@ __global__ void __launch_bounds__(288) moe_gemv_rows_kernel(const __grid_constan
         const float y = OFFSET ? d * small_int_to_float(sm) : __int_as_float(LEVEL0 * sm);
         aux[static_cast<size_t>(g) * nb + b] = make_float2(d, y);
     }
-    __syncthreads();
+    if constexpr (FUSED) {
+        if (static_cast<int32_t>(warp) < n_compute) named_bar_sync(1, static_cast<uint32_t>(n_compute) * 32u);
+    } else {
+        __syncthreads();
+    }
 
     const int64_t erow0 = static_cast<int64_t>(e) * a.nrows;   // first weight row of the expert
     if (static_cast<int32_t>(warp) == n_compute) {
@@ -354,9 +522,9 @@ __global__ void __launch_bounds__(288) moe_gemv_rows_kernel(const __grid_constan
 // CTAs of a kernel that fit on one SM at once (cached; moe_gemv.cu).
 int resident_ctas(const void* kernel, int threads, size_t smem);
 
-template <int WT, int G, bool DUMP>
+template <int WT, int G, bool DUMP, bool FUSED = false>
 static int launch_gemv_rows(const GemvPlan& plan, const CUtensorMap& wmap, const GemvArgs& a, cudaStream_t s) {
-    const void* kernel = reinterpret_cast<const void*>(moe_gemv_rows_kernel<WT, G, DUMP>);
+    const void* kernel = reinterpret_cast<const void*>(moe_gemv_rows_kernel<WT, G, DUMP, FUSED>);
     if (int st = set_smem_limit(kernel, static_cast<int>(plan.smem))) return st;
     const int threads = 32 * (plan.row_warps * plan.ksplit + 1);
     // grid.y: row blocks per slot tile, few enough that every CTA is resident
@@ -369,8 +537,9 @@ static int launch_gemv_rows(const GemvPlan& plan, const CUtensorMap& wmap, const
     y = y < 1 ? 1 : y > 65535 ? 65535 : y;
     const dim3 grid(static_cast<unsigned>(plan.grid_x), static_cast<unsigned>(y));
     const dim3 block(threads);
-    moe_gemv_rows_kernel<WT, G, DUMP><<<grid, block, plan.smem, s>>>(wmap, a);
-    return check_launch(DUMP ? "moe_gemv_rows_kernel<dump>" : "moe_gemv_rows_kernel", grid, block, plan.smem);
+    moe_gemv_rows_kernel<WT, G, DUMP, FUSED><<<grid, block, plan.smem, s>>>(wmap, a);
+    return check_launch(DUMP ? "moe_gemv_rows_kernel<dump>" : FUSED ? "moe_gemv_rows_kernel<fused>" : "moe_gemv_rows_kernel",
+                        grid, block, plan.smem);
 }
 
 template <int WT>

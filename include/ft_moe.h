@@ -229,6 +229,29 @@ FT_API int ft_moe_q4_0_q8_1(const void* weights, const void* act, const int32_t*
                      int64_t ncols, void* stream);
 
 /*
+ * ft_moe_q4_0_fp16 - the whole hot path from fp16 activations: exactly
+ *   ft_moe_q4_0_q8_1(weights, ft_quantize_q8_1(x_fp16), topk_ids, out)
+ * (quantize_row_q8_1 then moe_vec_q4_0_q8_1 over the flat slots, FreeToken
+ * PR #185, "Fix" and "Problem").  A decode-sized batch on the GEMV path (at
+ * most 512 slots, 1024 experts, ncols % 256 == 0, x_fp16 16-byte aligned,
+ * and at most 256 activation blocks per CTA's slot group) runs as one
+ * kernel launch in which every CTA routes the slots and quantizes the
+ * activation rows it needs itself (the stable slot order and
+ * the quantizer's arithmetic, so the out bits are those of the two calls);
+ * any other batch quantizes into library workspace (counted by
+ * ft_moe_workspace_bytes and ft_moe_reserve) and takes the usual path.
+ *
+ *   x_fp16    device, fp16 [tokens][ncols], 8-byte aligned
+ *   weights, topk_ids, out, tokens, top_k, n_experts, nrows, ncols as for
+ *   ft_moe_q4_0_q8_1.
+ * Bad expert ids: zero output rows and the device error flag, as there.
+ * Errors: those of ft_quantize_q8_1 and ft_moe_q4_0_q8_1.
+ */
+FT_API int ft_moe_q4_0_fp16(const void* weights, const void* x_fp16, const int32_t* topk_ids, float* out,
+                            int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols,
+                            void* stream);
+
+/*
  * ft_moe_q4_0_q8_1_slots - the same matmul with one activation row per routed
  * slot instead of one per token: the input of the second expert layer, which
  * runs on the first layer's output after SiLU*up, one row per routed slot

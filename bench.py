@@ -52,7 +52,7 @@ PAGES_T4_TOKENS_PER_S = {("prefill", 8191): 8191 / 0.7058, ("prefill", 4096): 40
 GEMM_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemm_tc.cu", "bit_quantized_moe_quantize_gb300/csrc/gemm_common.cuh",
                 "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh")
 GEMM_CONSTANTS = ("bit_quantized_moe_quantize_gb300/csrc/ft_internal.h", "kGemm")
-NCU_TRAFFIC = {("moe_gemm_tc_kernel", "1d61a05e410c8baf", "prefill:8191"): 666817280 + 340600320}
+NCU_TRAFFIC = {("moe_gemm_tc_kernel", "f14bdd613c5afc3d", "prefill:8191"): 666726144 + 340649472}
 
 
 def kernel_source_hash(files, constants=GEMM_CONSTANTS) -> str:
@@ -485,6 +485,24 @@ def ours(args):
                 "kernel_ms": mm_ms}
     tr = NCU_TRAFFIC.get((kern, kernel_source_hash(GEMM_SOURCES), args.workload)) if path == "gemm" else None
     roof["traffic"] = tr
+    if path == "gemv":
+        # the same number of bytes streamed by a plain read kernel (L2 flushed
+        # before each): what the memory system delivers at this size at all
+        nread = min(alg_bytes, dw.numel()) // 16 * 16
+        rl = []
+        for _ in range(n_prof):
+            flush.zero_()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            ft.debug_stream_read(dw, nread)
+            a1.record(stream)
+            rl.append((a0, a1))
+        torch.cuda.synchronize()
+        read_ms = statistics.mean(x.elapsed_time(y) for x, y in rl)
+        read_gbs = nread / (read_ms / 1000.0) / 1e9
+        roof["same_size_read"] = {"bytes": nread, "ms": read_ms, "gbs": read_gbs,
+                                  "frac": roof["achieved"] / read_gbs,
+                                  "note": "ft_debug_stream_read of the same bytes: plain 16-byte loads, L2 flushed"}
 
     cpu = None
     if not args.no_cpu_baseline and world == 1 and wtype == "q4_0":

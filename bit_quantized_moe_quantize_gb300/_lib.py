@@ -31,7 +31,7 @@ EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_m
            "ft_profile_read", "ft_moe_route_offsets_noalloc", "ft_moe_q4_0_q8_1_slots",
            "ft_moe_q4_0_q8_1_ep", "ft_act_mul_quantize_q8_1", "ft_moe_ffn_q4_0_q8_1", "ft_moe_gguf_q8_1",
            "ft_repack_q4_0_soa", "ft_debug_wait_timeout", "ft_moe_q4_0_q8_1_act", "ft_moe_ffn_reserve",
-           "ft_moe_q4_0_fp16")
+           "ft_moe_q4_0_fp16", "ft_debug_stream_read")
 
 
 class FtError(RuntimeError):
@@ -70,6 +70,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.ft_moe_gguf_q8_1.argtypes = [i32, vp, vp, vp, vp, i64, i32, i32, i64, i64, vp]
         L.ft_repack_q4_0_soa.argtypes = [vp, vp, vp, i64, vp]
         L.ft_debug_wait_timeout.argtypes = [i64, vp]
+        L.ft_debug_stream_read.argtypes = [vp, i64, vp]
         L.ft_moe_ffn_q4_0_q8_1.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i64, i64, i32, vp]
         L.ft_moe_q4_0_q8_1_act.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, i32, vp]
         L.ft_moe_ffn_reserve.argtypes = [i64, i32, i32, i64, i64]
@@ -389,6 +390,18 @@ def read_device_error(stream=None) -> int:
     if st not in (FT_OK, FT_ERR_DEVICE_FLAG):
         raise FtError(st, last_error())
     return int(flags.value)
+
+
+def debug_stream_read(buf, nbytes=None, stream=None):
+    """Measurement hook (ft_debug_stream_read): stream the first nbytes (default:
+    all, rounded down to 16) of a CUDA tensor through the SMs, nothing written."""
+    torch = _torch()
+    if not isinstance(buf, torch.Tensor) or not buf.is_cuda or not buf.is_contiguous():
+        raise TypeError("buf must be a contiguous CUDA tensor")
+    n = buf.numel() * buf.element_size() if nbytes is None else int(nbytes)
+    n -= n % 16
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream if stream is None else stream)
+    _check(load().ft_debug_stream_read(ctypes.c_void_p(buf.data_ptr()), n, s))
 
 
 def debug_wait_timeout(limit_ns: int, stream=None):

@@ -783,6 +783,20 @@ int ft_moe_read_device_error(void* stream, uint32_t* flags_out) {
     return v ? fail(FT_ERR_DEVICE_FLAG, "device error flags 0x%x", v) : FT_OK;
 }
 
+int ft_debug_stream_read(const void* buf, int64_t bytes, void* stream) {
+    g_last_error.clear();
+    if (bytes < 0 || bytes % 16 != 0)
+        return fail(FT_ERR_ARG, "bytes must be a non-negative multiple of 16 (got %lld)", (long long)bytes);
+    if (bytes == 0) return FT_OK;
+    if (!buf) return fail(FT_ERR_ARG, "null pointer");
+    if (!aligned(buf, 16)) return fail(FT_ERR_ALIGN, "buf must be 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = nullptr;
+    if (int st = ws_acquire(ws_layout(0, 1).total, s, &ws)) return st;
+    // the sink is the workspace's error word: written only on an impossible sum
+    return launch_stream_read(buf, bytes / 16, reinterpret_cast<uint32_t*>(ws + ws_layout(0, 1).counts), s);
+}
+
 int ft_debug_wait_timeout(int64_t limit_ns, void* stream) {
     g_last_error.clear();
     if (limit_ns < 1000 || limit_ns > 1000000000)

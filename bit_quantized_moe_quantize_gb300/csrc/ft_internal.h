@@ -26,6 +26,8 @@ int check_launch(const char* kernel, dim3 grid, dim3 block, size_t smem);
 
 // Test hook: a kernel whose bounded wait must give up after limit_ns.
 int launch_wait_timeout_probe(uint32_t* err, int64_t limit_ns, cudaStream_t s);
+// Measurement hook: a plain streaming read of n16 16-byte words of buf.
+int launch_stream_read(const void* buf, int64_t n16, uint32_t* sink, cudaStream_t s);
 
 // ------------------------------------------------------------ quantizer
 int launch_quantize_q8_1(const void* x, void* act, int64_t tokens, int64_t ncols, cudaStream_t s);

@@ -477,6 +477,19 @@ FT_API int ft_moe_read_device_error(void* stream, uint32_t* flags_out);
 FT_API int ft_debug_wait_timeout(int64_t limit_ns, void* stream);
 
 /*
+ * ft_debug_stream_read - measurement hook: a plain streaming read of `bytes`
+ * bytes of `buf` on `stream` (four independent 16-byte loads in flight per
+ * thread, four 512-thread CTAs per SM, nothing written), so that a caller can
+ * time how long the memory system takes to deliver a buffer of that size at
+ * all; a bandwidth-bound kernel reading the same number of bytes is judged
+ * against that time as well as against the copy peak of large buffers.
+ *   buf    device, 16-byte aligned; bytes a multiple of 16 (0 is a no-op)
+ * Uses the library workspace.  The pages have no counterpart.
+ * Errors: FT_ERR_ARG, FT_ERR_ALIGN, FT_ERR_WORKSPACE, FT_ERR_CUDA, FT_ERR_LAUNCH.
+ */
+FT_API int ft_debug_stream_read(const void* buf, int64_t bytes, void* stream);
+
+/*
  * ft_moe_set_path - force the path of later ft_moe_q4_0_q8_1 calls in this
  * process (FT_PATH_AUTO / FT_PATH_GEMV / FT_PATH_GEMM); returns the previous
  * setting, or -1 for an unknown value.  The environment variable FT_MOE_PATH

@@ -215,6 +215,16 @@ def test_repack_rejects_bad_arguments(lib):
     assert f(W, Q, D, 1 << 62, vp(0)) == 2                     # size overflow
 
 
+def test_debug_stream_read_rejects_bad_arguments_on_the_host(lib):
+    vp = ctypes.c_void_p
+    f = lib.ft_debug_stream_read
+    assert f(vp(0x10000), 100, vp(0)) == 1          # not a multiple of 16
+    assert f(vp(0x10000), -16, vp(0)) == 1          # negative
+    assert f(vp(0x10000), 0, vp(0)) == 0            # nothing to read: no-op
+    assert f(vp(0), 64, vp(0)) == 1                 # null buffer
+    assert f(vp(0x10008), 64, vp(0)) == 3           # not 16-byte aligned
+
+
 def test_debug_wait_timeout_rejects_bad_limits_on_the_host(lib):
     vp = ctypes.c_void_p
     for bad in (0, 999, 2_000_000_000):

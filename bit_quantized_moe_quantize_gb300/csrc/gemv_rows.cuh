@@ -248,7 +248,7 @@ __device__ __forceinline__ bool fused_route(const GemvArgs& a, int32_t t, int32_
 }
 
 template <int WT, int G, bool DUMP, bool FUSED>
-__global__ void __launch_bounds__(288) moe_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap,
+__global__ void __launch_bounds__(288, G >= 8 ? 1 : 2) moe_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap,
                                                              const GemvArgs a) {
     using BX = RowBox<WT>;
     constexpr int PITCH = BX::PITCH;

@@ -86,7 +86,7 @@ def parse():
                     help="time eager launches instead of a CUDA-graph replay of the step")
     ap.add_argument("--wtype", default="q4_0",
                     choices=["q4_0", "q4_1", "q5_0", "q5_1", "q8_0", "q4_k", "q5_k", "q6_k", "q2_k", "q3_k"],
-                    help="GGUF type of the expert weights (other than q4_0: ft_moe_gguf_q8_1, GEMV path)")
+                    help="GGUF type of the expert weights (other than q4_0: ft_moe_gguf_q8_1; GEMV path, tensor cores too for q4_k)")
     ap.add_argument("--ffn", choices=["silu", "gelu_tanh"], default=None,
                     help="time both expert layers (ft_moe_ffn_q4_0_q8_1) with the workload's ncols as the hidden "
                          "size and its nrows as the intermediate size")
@@ -327,7 +327,8 @@ def ours(args):
         from bit_quantized_moe_quantize_gb300 import synth
         x = synth.make_activations(replica_workload(wl, rank), S)
     rows = S if args.per_slot else T
-    path = {1: "gemv", 2: "gemm"}[ft.selected_path(T, k, E, N, K)] if wtype == "q4_0" else "gemv"
+    # the tensor-core path takes Q4_0 and Q4_K weights (the same shape rule)
+    path = {1: "gemv", 2: "gemm"}[ft.selected_path(T, k, E, N, K)] if wtype in ("q4_0", "q4_k") else "gemv"
 
     dw = torch.from_numpy(w).to(dev)
     dx = torch.from_numpy(x).to(dev)
@@ -466,7 +467,7 @@ def ours(args):
     if fused:   # one launch reads the fp16 rows instead of Q8_1 blocks
         alg_bytes += rows * K * 2 - rows * nb * 36
     if path == "gemm":
-        kern = "moe_gemm_tc_kernel"
+        kern = "moe_gemm_tc_kernel" if wtype == "q4_0" else f"moe_gemm_tc_kernel<{wtype}>"
         achieved = flops / (mm_ms / 1000.0) / 1e12
         roof = {"kernel": kern, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],

@@ -213,17 +213,18 @@ static int get_stream_capturing(cudaStream_t s, bool* capturing) {
 // Per device: one cudaMalloc'ed block.  Layout (each part 256-byte aligned):
 //   err word | counts[E] | offsets[E+1] | perm[S] | tiles_gemv[E+1] |
 //   tiles_gemm[E+1] | hist[nchunks][E] | (tensor-core path only:)
-//   xh[S_pad][ncols] fp16 | da[S_pad][ncols/32] fp16 | (layer 1 with the
+//   xh[S_pad][ncols] fp16 | da[S_pad][ncols/32] fp16 | (Q4_K weights there:)
+//   sa[S_pad][ncols/32] fp32 | (layer 1 with the
 //   activation fused, on the GEMV path:) h[S][2 n_inter] fp32 | (the fp16
 //   entry point, unless it runs in one launch:) act[T][ncols/32] Q8_1
 struct WsLayout {
-    size_t err, counts, offsets, perm, tiles_gemv, tiles_gemm, hist, xh, da, h, act, total;
+    size_t err, counts, offsets, perm, tiles_gemv, tiles_gemm, hist, xh, da, sa, h, act, total;
 };
 
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static WsLayout ws_layout(int64_t n_slots, int32_t n_experts, int64_t gemm_ncols = 0, size_t h_bytes = 0,
-                          size_t act_bytes = 0) {
+                          size_t act_bytes = 0, bool gemm_sums = false) {
     WsLayout L{};
     size_t o = 0;
     L.err = o;
@@ -245,6 +246,8 @@ static WsLayout ws_layout(int64_t n_slots, int32_t n_experts, int64_t gemm_ncols
     o = al256(o + 2 * rows * static_cast<size_t>(gemm_ncols));
     L.da = o;
     o = al256(o + 2 * rows * static_cast<size_t>(gemm_ncols / 32));
+    L.sa = o;
+    o = al256(o + (gemm_sums ? 4 * rows * static_cast<size_t>(gemm_ncols / 32) : 0));
     L.h = o;
     o = al256(o + h_bytes);
     L.act = o;
@@ -337,9 +340,11 @@ static bool gemm_shape_ok(const Shape& sh) {
 
 // Host-side choice from the shape only (no device read): the tensor-core path
 // pays off once experts see enough slots to fill a 128-column MMA tile.
+static bool gemm_type_ok(int wtype) { return wtype == FT_TYPE_Q4_0 || wtype == FT_TYPE_Q4_K; }
+
 static int choose_path(const Shape& sh, int setting) {
     if (setting == FT_PATH_GEMV) return FT_PATH_GEMV;
-    if (sh.wtype != FT_TYPE_Q4_0) return setting == FT_PATH_GEMM ? FT_PATH_GEMM : FT_PATH_GEMV;
+    if (!gemm_type_ok(sh.wtype)) return setting == FT_PATH_GEMM ? FT_PATH_GEMM : FT_PATH_GEMV;
     if (setting == FT_PATH_GEMM) return FT_PATH_GEMM;
     if (!gemm_shape_ok(sh)) return FT_PATH_GEMV;
     return sh.mean() >= 16.0 ? FT_PATH_GEMM : FT_PATH_GEMV;
@@ -368,8 +373,9 @@ static size_t act_rows_bytes(const Shape& sh) {
 static int run_matmul(const void* weights, const void* act, const int32_t* topk_ids, float* out, int32_t* dots,
                       const Shape& sh, cudaStream_t s, const ActFuse* af = nullptr, const void* x16 = nullptr) {
     const int path = choose_path(sh, path_setting());
-    if (path == FT_PATH_GEMM && sh.wtype != FT_TYPE_Q4_0)
-        return fail(FT_ERR_ARG, "the tensor-core path takes Q4_0 weights only (weight type %d)", sh.wtype);
+    if (path == FT_PATH_GEMM && !gemm_type_ok(sh.wtype))
+        return fail(FT_ERR_ARG, "the tensor-core path takes Q4_0 and Q4_K weights only (weight type %d)", sh.wtype);
+    const bool gemm_sums = path == FT_PATH_GEMM && sh.wtype == FT_TYPE_Q4_K;
     if (path == FT_PATH_GEMM && !gemm_shape_ok(sh))
         return fail(FT_ERR_ARG, "the tensor-core path needs ncols %% 256 == 0 and n_experts * nrows >= 128 (got %lld, %lld)",
                     (long long)sh.ncols, (long long)sh.n_experts * sh.nrows);
@@ -380,7 +386,7 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
                             gp.smem <= 227 * 1024 && gemv_fused_ok(gp, sh.n_slots, sh.n_experts, sh.ncols);
     const WsLayout L = ws_layout(sh.n_slots, sh.n_experts, path == FT_PATH_GEMM ? sh.ncols : 0,
                                  h_in_ws ? 4 * static_cast<size_t>(sh.n_slots) * sh.nrows : 0,
-                                 x16 && !one_launch ? act_rows_bytes(sh) : 0);
+                                 x16 && !one_launch ? act_rows_bytes(sh) : 0, gemm_sums);
     uint8_t* ws = nullptr;
     if (int st = ws_acquire(L.total, s, &ws)) return st;
     if (one_launch) {
@@ -429,7 +435,8 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
     if (path == FT_PATH_GEMM && sh.n_slots > 0) {
         if (int st = launch_gather(static_cast<const uint8_t*>(act), rb.perm, rb.offsets, sh.n_experts, sh.act_div,
                                    sh.nb, sh.n_slots, reinterpret_cast<uint16_t*>(ws + L.xh),
-                                   reinterpret_cast<uint16_t*>(ws + L.da), s))
+                                   reinterpret_cast<uint16_t*>(ws + L.da), s,
+                                   gemm_sums ? reinterpret_cast<float*>(ws + L.sa) : nullptr))
             return st;
     }
     prof_mark(kProfMatmulBegin, s);
@@ -444,7 +451,8 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
         st = launch_gemm(static_cast<const uint8_t*>(weights), static_cast<const uint8_t*>(act), rb.perm,
                          rb.offsets, rb.tiles_gemm, fused_tc ? nullptr : out, dots, rb.err, sh.n_slots, sh.act_div,
                          sh.n_experts, sh.nrows, sh.ncols, reinterpret_cast<uint16_t*>(ws + L.xh),
-                         reinterpret_cast<uint16_t*>(ws + L.da), tile_width, s, af);
+                         reinterpret_cast<uint16_t*>(ws + L.da), tile_width, s, af,
+                         gemm_sums ? reinterpret_cast<const float*>(ws + L.sa) : nullptr);
     }
     prof_mark(kProfMatmulEnd, s);
     return st;
@@ -722,7 +730,9 @@ size_t ft_moe_workspace_bytes(int64_t tokens, int32_t top_k, int32_t n_experts, 
     const int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh);
     g_last_error = keep;
     if (st) return 0;
-    return ws_layout(sh.n_slots, sh.n_experts, gemm_shape_ok(sh) ? sh.ncols : 0, 0, act_rows_bytes(sh)).total;
+    return ws_layout(sh.n_slots, sh.n_experts, gemm_shape_ok(sh) ? sh.ncols : 0, 0, act_rows_bytes(sh),
+                     gemm_shape_ok(sh))
+        .total;
 }
 
 int ft_moe_reserve(int64_t max_tokens, int32_t max_top_k, int32_t n_experts, int64_t nrows, int64_t ncols) {
@@ -730,7 +740,9 @@ int ft_moe_reserve(int64_t max_tokens, int32_t max_top_k, int32_t n_experts, int
     Shape sh{};
     if (int st = check_matmul_args(max_tokens, max_top_k, n_experts, nrows, ncols, &sh)) return st;
     uint8_t* base = nullptr;
-    return ws_acquire(ws_layout(sh.n_slots, sh.n_experts, gemm_shape_ok(sh) ? sh.ncols : 0, 0, act_rows_bytes(sh)).total,
+    return ws_acquire(ws_layout(sh.n_slots, sh.n_experts, gemm_shape_ok(sh) ? sh.ncols : 0, 0, act_rows_bytes(sh),
+                                gemm_shape_ok(sh))
+                          .total,
                       nullptr, &base);
 }
 

@@ -115,8 +115,9 @@ inline int64_t gemm_rows(int64_t n_slots) { return (n_slots + kGemmBN - 1) / kGe
 // xh: [S_pad][ncols] fp16 and da: [S_pad][ncols/32] fp16 workspace for the
 // routed activations in router order, S_pad = gemm_rows(S): written by
 // launch_gather (zero past the routed slots), then read by the GEMM's TMA.
+// sa != nullptr (Q4_K weights): also the exact d_a * sum(q_a) of every block, [S_pad][ncols/32] fp32.
 int launch_gather(const uint8_t* act, const int32_t* perm, const int32_t* offsets, int32_t n_experts, int32_t top_k,
-                  int64_t nb, int64_t n_slots, uint16_t* xh, uint16_t* da, cudaStream_t s);
+                  int64_t nb, int64_t n_slots, uint16_t* xh, uint16_t* da, cudaStream_t s, float* sa = nullptr);
 // Layer 1 with the gated activation fused into the epilogue: the weights
 // hold n_inter gate rows then n_inter up rows per expert (nrows = 2 n_inter),
 // and instead of out the kernel writes act_mid [S][n_inter / 32] Q8_1 rows of
@@ -130,6 +131,6 @@ struct ActFuse {
 int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
                 const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
                 int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, int tile_width,
-                cudaStream_t s, const ActFuse* af = nullptr);
+                cudaStream_t s, const ActFuse* af = nullptr, const float* sa = nullptr);
 
 }  // namespace ft

@@ -62,10 +62,13 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int64_t w) {
     return ti;
 }
 
-// Four packed nibble bytes -> two fp16x2 words holding (nibble - 8), in order.
-// 0x64nn is the fp16 1024 + nn, so one subtraction of 1032 gives nn - 8 exactly.
+// Four packed nibble bytes -> two fp16x2 words holding (nibble - OFF), in order
+// (OFF 8 for Q4_0, 0 for the K-quants' levels).  0x64nn is the fp16 1024 + nn,
+// so one subtraction of 1024 + OFF gives nn - OFF exactly.
+template <int OFF = 8>
 __device__ __forceinline__ void nib4_to_h2(uint32_t nib, uint32_t& lo, uint32_t& hi) {
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+    static_assert(OFF >= 0 && OFF < 256, "level offset");
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6400 + OFF), __ushort_as_half(0x6400 + OFF));
     uint32_t a = __byte_perm(nib, 0x64646464u, 0x4140u);
     uint32_t b = __byte_perm(nib, 0x64646464u, 0x4342u);
     __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);

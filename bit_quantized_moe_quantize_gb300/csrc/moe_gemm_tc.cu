@@ -43,14 +43,19 @@
 // along K, so each block needs its own accumulator and a drain; the drain's
 // two fp32 operations per (row, slot, block) set this kernel's ceiling.
 #include "gemm_common.cuh"
+#include "gemv_blocks.cuh"   // kquant_scale_min
 #include "q8_1_math.cuh"
 
 namespace ft {
 
 // Compile-time configuration for a slot-tile width BN (32 for decode-sized
-// batches, 128 for prefill).
-template <int BN_>
+// batches, 128 for prefill) and the weight type: Q4_0 (KQ_ false) or Q4_K
+// (KQ_ true: a raw stage is one 144-byte super-block per row, the same box as
+// eight Q4_0 blocks; each block also carries a min d_min m_j per row and the
+// activation block's d_a sum(q_a) per slot, one more fp32 term in the drain).
+template <int BN_, bool KQ_ = false>
 struct Gemm {
+    static constexpr bool KQ = KQ_;
     static constexpr int BN = BN_;                      // slots per tile
     static constexpr int BM = kGemmBM;                  // weight rows per tile
     static constexpr int KB = 8;                        // Q4_0 blocks per raw stage (K = 256)
@@ -66,7 +71,8 @@ struct Gemm {
     static constexpr int NSC = 8;                       // scale ring depth (blocks)
     static constexpr int W_RAW_BYTES = BM * KB * Q4_0_BYTES;   // 18432
     static constexpr int DA_RAW_BYTES = BN * KB * 2;           // [slot][8] fp16 activation scales
-    static constexpr int RAW_STAGE_BYTES = W_RAW_BYTES + DA_RAW_BYTES;
+    static constexpr int SA_RAW_BYTES = KQ ? BN * KB * 4 : 0;   // [slot][8] fp32 d_a sum(q_a) (Q4_K)
+    static constexpr int RAW_STAGE_BYTES = W_RAW_BYTES + DA_RAW_BYTES + SA_RAW_BYTES;
     static constexpr int OPA_BYTES = BM * 128;
     static constexpr int OPB_BYTES = BN * 128;
     static constexpr int OP_SLOT_BYTES = OPA_BYTES + OPB_BYTES;
@@ -79,7 +85,9 @@ struct Gemm {
     // CW/4 + 4 floats, so that the four 16-byte groups a warp's quads load at
     // once fall in four different bank groups.
     static constexpr int DA_QPITCH = CW / 4 + 4;
-    static constexpr int SC_BYTES = BM * 4 + (BN / CW) * 4 * DA_QPITCH * 4;
+    static constexpr int DA_FLOATS = (BN / CW) * 4 * DA_QPITCH;
+    // Q4_K adds the mins d_min m_j [BM] and the slots' d_a sum(q_a) (d_a's layout)
+    static constexpr int SC_BYTES = (BM * 4 + DA_FLOATS * 4) * (KQ ? 2 : 1);
     static constexpr int N_UNPACK_WARPS = 4;
     static constexpr int UNPACK_THREADS = N_UNPACK_WARPS * 32;  // one weight row per thread
     static constexpr int WARP_PRODUCER = N_DRAIN_WARPS + N_UNPACK_WARPS, WARP_MMA = WARP_PRODUCER + 1;
@@ -97,7 +105,7 @@ struct Gemm {
     // (rows 16-byte aligned, one 128-byte run per quarter-warp read)
     static constexpr int EPI_P2 = BN / 2 + 4;
     static constexpr int EPI_AP = 64 + 4;
-    static constexpr int EPI_BYTES = 64 * EPI_P2 * 8 > BN * EPI_AP * 4 ? 64 * EPI_P2 * 8 : BN * EPI_AP * 4;
+    static constexpr int EPI_BYTES = KQ ? 0 : 64 * EPI_P2 * 8 > BN * EPI_AP * 4 ? 64 * EPI_P2 * 8 : BN * EPI_AP * 4;
     static constexpr int OFF_EPI = OFF_SC + NSC * SC_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
     static constexpr int N_BARS = 2 * RAW_STAGES + 2 * OP_SLOTS + 2 * NBAR_ACC + NSC + 4;
@@ -236,11 +244,14 @@ __device__ __forceinline__ bool fused_act_quantize(const GemmArgs& a, const Tile
     return true;
 }
 
-template <int BN, bool DUMP, bool FUSE>
+template <int BN, bool DUMP, bool FUSE, bool KQ>
 __global__ void __launch_bounds__(FUSE ? Gemm<BN>::THREADS_FUSED : Gemm<BN>::THREADS, 1)
     moe_gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
-                       const __grid_constant__ CUtensorMap smap, const GemmArgs a) {
-    using C = Gemm<BN>;
+                       const __grid_constant__ CUtensorMap smap, const __grid_constant__ CUtensorMap amap,
+                       const GemmArgs a) {
+    using C = Gemm<BN, KQ>;
+    static_assert(!(KQ && (DUMP || FUSE)), "Q4_K takes the plain matmul only");
+    constexpr int SA_RAW_BYTES = C::SA_RAW_BYTES, DA_FLOATS = C::DA_FLOATS;
     constexpr int BM = C::BM, KB = C::KB, RAW_STAGES = C::RAW_STAGES, OP_SLOTS = C::OP_SLOTS, NACC = C::NACC;
     constexpr int NBAR_ACC = C::NBAR_ACC;
     constexpr bool PAIRED = C::PAIRED;
@@ -326,8 +337,10 @@ __global__ void __launch_bounds__(FUSE ? Gemm<BN>::THREADS_FUSED : Gemm<BN>::THR
                 if (!mbar_wait_warp(&raw_empty[s], ((it / RAW_STAGES) & 1u) ^ 1u, a.err)) { ok = false; break; }
                 uint8_t* wraw = smem + OFF_RAW + s * RAW_STAGE_BYTES;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&raw_full[s], W_RAW_BYTES + DA_RAW_BYTES);
+                    mbar_arrive_expect_tx(&raw_full[s], W_RAW_BYTES + DA_RAW_BYTES + SA_RAW_BYTES);
                     tma_load_2d(wraw, &wmap, ks * KB * Q4_0_BYTES, wy, &raw_full[s]);
+                    if constexpr (KQ)   // the slots' d_a sum(q_a) of the stage's 8 blocks
+                        tma_load_2d(wraw + W_RAW_BYTES + DA_RAW_BYTES, &amap, ks * KB, py, &raw_full[s]);
                     if constexpr (FUSE)
                         tma_load_2d(wraw + (BM / 2) * KB * Q4_0_BYTES, &wmap, ks * KB * Q4_0_BYTES, wy_up,
                                     &raw_full[s]);
@@ -376,6 +389,56 @@ __global__ void __launch_bounds__(FUSE ? Gemm<BN>::THREADS_FUSED : Gemm<BN>::THR
                     const uint32_t os = ou % OP_SLOTS;
                     if (!mbar_wait(&op_empty[os], ((ou / OP_SLOTS) & 1u) ^ 1u, a.err)) { ok = false; break; }
                     uint8_t* opa = smem + OFF_OP + os * OP_SLOT_BYTES;
+                    if constexpr (KQ) {
+                        // Q4_K: the row's stage is one super-block: chunk 0 = fp16 d, fp16
+                        // d_min, 12 bytes of 6-bit scale/min pairs; sub-blocks 2j and 2j+1 are
+                        // the low and high nibbles of the 32 bytes in chunks 1 + 2j, 2 + 2j
+                        // (levels 0..15, no offset); per block d sc_j, d_min m_j per row and
+                        // d_a, d_a sum(q_a) per slot go to the scale ring
+#pragma unroll
+                        for (int h = 0; h < 2; ++h, ++bc) {
+                            const uint32_t sc = bc % NSC;
+                            if (!mbar_wait(&sc_empty[sc], ((bc / NSC) & 1u) ^ 1u, a.err)) { ok = false; break; }
+                            float* dws = reinterpret_cast<float*>(smem + OFF_SC + sc * SC_BYTES);
+                            float* das = dws + BM;
+                            float* mws = das + DA_FLOATS;
+                            float* sas = mws + BM;
+#pragma unroll
+                            for (int rr = 0; rr < RPT; ++rr) {
+                                const uint32_t u = u0 + rr * UNPACK_THREADS;
+                                const uint4* wrow = reinterpret_cast<const uint4*>(wraw + u * (KB * Q4_0_BYTES));
+                                const uint4 hd = wrow[0], qc0 = wrow[1 + 2 * j], qc1 = wrow[2 + 2 * j];
+                                const uint32_t sc12[3] = {hd.y, hd.z, hd.w};
+                                int scv, mnv;
+                                kquant_scale_min(sc12, 2 * j + h, scv, mnv);
+                                dws[u] = __half2float(__ushort_as_half(static_cast<unsigned short>(hd.x & 0xFFFFu))) *
+                                         static_cast<float>(scv);
+                                mws[u] = __half2float(__ushort_as_half(static_cast<unsigned short>(hd.x >> 16))) *
+                                         static_cast<float>(mnv);
+                                if (u < static_cast<uint32_t>(BN)) {
+                                    const uint32_t pair = dav[rr][j];         // d_a of blocks 2j, 2j+1
+                                    const unsigned short hb =
+                                        static_cast<unsigned short>(h ? (pair >> 16) : (pair & 0xFFFFu));
+                                    das[da_index<CW>(u)] = __half2float(__ushort_as_half(hb));
+                                    sas[da_index<CW>(u)] = *reinterpret_cast<const float*>(
+                                        wraw + W_RAW_BYTES + DA_RAW_BYTES + u * (KB * 4) + (2 * j + h) * 4);
+                                }
+                                const uint32_t w8[8] = {qc0.x, qc0.y, qc0.z, qc0.w, qc1.x, qc1.y, qc1.z, qc1.w};
+                                // 16-byte chunk c of the block holds values 8c..8c+7: bytes 8c..8c+7
+#pragma unroll
+                                for (int c = 0; c < 4; ++c) {
+                                    uint32_t h0, h1, h2, h3;
+                                    nib4_to_h2<0>((w8[2 * c] >> (4 * h)) & 0x0F0F0F0Fu, h0, h1);
+                                    nib4_to_h2<0>((w8[2 * c + 1] >> (4 * h)) & 0x0F0F0F0Fu, h2, h3);
+                                    *reinterpret_cast<uint4*>(opa + sw128_off(u, 4 * h + c)) = make_uint4(h0, h1, h2, h3);
+                                }
+                            }
+                        }
+                        if (!ok) break;
+                        fence_proxy_async_smem();
+                        mbar_arrive(&op_full[os]);
+                        continue;
+                    }
                     // the unit's 36 bytes of a row start at byte 36j = 16 * (2j) + 4j: words
                     // j .. j+8 of a 3-chunk window starting at chunk 2j (9 chunks per row, so
                     // 8 consecutive rows hit 8 different 16-byte bank groups)
@@ -549,6 +612,12 @@ __global__ void __launch_bounds__(FUSE ? Gemm<BN>::THREADS_FUSED : Gemm<BN>::THR
                         reinterpret_cast<const float4*>(dws + BM + (col0 / CW) * (4 * DA_QPITCH) + q * DA_QPITCH);
                     const float dw0 = dws[r0], dw1 = dws[r0 + 8];
                     const float2 dw0x2 = make_float2(dw0, dw0), dw1x2 = make_float2(dw1, dw1);
+                    // Q4_K: - d_min m_j per row, and d_a sum(q_a) in d_a's layout
+                    const float* mws = dws + BM + DA_FLOATS;
+                    const float4* sap =
+                        reinterpret_cast<const float4*>(mws + BM + (col0 / CW) * (4 * DA_QPITCH) + q * DA_QPITCH);
+                    const float2 nm0x2 = KQ ? make_float2(-mws[r0], -mws[r0]) : make_float2(0.0f, 0.0f);
+                    const float2 nm1x2 = KQ ? make_float2(-mws[r0 + 8], -mws[r0 + 8]) : make_float2(0.0f, 0.0f);
     #pragma unroll
                     for (int hh = 0; hh < NH; ++hh) {
                         uint32_t d[16];
@@ -587,6 +656,12 @@ __global__ void __launch_bounds__(FUSE ? Gemm<BN>::THREADS_FUSED : Gemm<BN>::THR
                                         make_float2(__uint_as_float(d[4 * ig + 2]), __uint_as_float(d[4 * ig + 3])), da2);
                                     acc[0][i] = __ffma2_rn(t0, dw0x2, acc[0][i]);
                                     acc[1][i] = __ffma2_rn(t1, dw1x2, acc[1][i]);
+                                    if constexpr (KQ) {
+                                        const float4 sv = sap[2 * hh + k2];
+                                        const float2 sa2 = ii ? make_float2(sv.z, sv.w) : make_float2(sv.x, sv.y);
+                                        acc[0][i] = __ffma2_rn(sa2, nm0x2, acc[0][i]);
+                                        acc[1][i] = __ffma2_rn(sa2, nm1x2, acc[1][i]);
+                                    }
                                 }
                             }
                         }
@@ -631,6 +706,12 @@ __global__ void __launch_bounds__(FUSE ? Gemm<BN>::THREADS_FUSED : Gemm<BN>::THR
                         reinterpret_cast<const float4*>(dws + BM + (col0 / CW) * (4 * DA_QPITCH) + q * DA_QPITCH);
                     const float dw0 = dws[r0], dw1 = dws[r0 + 8];
                     const float2 dw0x2 = make_float2(dw0, dw0), dw1x2 = make_float2(dw1, dw1);
+                    // Q4_K: - d_min m_j per row, and d_a sum(q_a) in d_a's layout
+                    const float* mws = dws + BM + DA_FLOATS;
+                    const float4* sap =
+                        reinterpret_cast<const float4*>(mws + BM + (col0 / CW) * (4 * DA_QPITCH) + q * DA_QPITCH);
+                    const float2 nm0x2 = KQ ? make_float2(-mws[r0], -mws[r0]) : make_float2(0.0f, 0.0f);
+                    const float2 nm1x2 = KQ ? make_float2(-mws[r0 + 8], -mws[r0 + 8]) : make_float2(0.0f, 0.0f);
     #pragma unroll
                     for (int hh = 0; hh < NH; ++hh) {
                         uint32_t d[16];
@@ -669,6 +750,12 @@ __global__ void __launch_bounds__(FUSE ? Gemm<BN>::THREADS_FUSED : Gemm<BN>::THR
                                         make_float2(__uint_as_float(d[4 * ig + 2]), __uint_as_float(d[4 * ig + 3])), da2);
                                     acc[0][i] = __ffma2_rn(t0, dw0x2, acc[0][i]);
                                     acc[1][i] = __ffma2_rn(t1, dw1x2, acc[1][i]);
+                                    if constexpr (KQ) {
+                                        const float4 sv = sap[2 * hh + k2];
+                                        const float2 sa2 = ii ? make_float2(sv.z, sv.w) : make_float2(sv.x, sv.y);
+                                        acc[0][i] = __ffma2_rn(sa2, nm0x2, acc[0][i]);
+                                        acc[1][i] = __ffma2_rn(sa2, nm1x2, acc[1][i]);
+                                    }
                                 }
                             }
                         }
@@ -750,6 +837,46 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// The gather for Q4_K weights: the same fp16 rows and fp16 scales, plus the
+// exact d_a * sum(q_a) of every block as fp32 (|sum| <= 4064 and d_a an fp16,
+// so the product is exact), the activation factor of the K-quant min term.
+// One warp per router position; lane l takes blocks l, l + 32, ... whole.
+__global__ void __launch_bounds__(256)
+    gather_act_sums_kernel(const uint8_t* __restrict__ act, const int32_t* __restrict__ perm,
+                           const int32_t* __restrict__ offsets, int32_t n_experts, int32_t top_k, int32_t nb,
+                           int64_t n_rows, uint2* __restrict__ xh, uint16_t* __restrict__ da, float* __restrict__ sa) {
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int64_t n_valid = offsets[n_experts];
+    const uint32_t lane = lane_id();
+    for (int64_t p = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); p < n_rows;
+         p += warps) {
+        uint2* xrow = xh + p * nb * 8;      // 8 x 8 bytes per block
+        for (int32_t b = lane; b < nb; b += 32) {
+            uint32_t w[9];
+            if (p < n_valid) {
+                const int64_t t = perm[p] / top_k;
+                const uint32_t* src = reinterpret_cast<const uint32_t*>(act + (t * nb + b) * Q8_1_BYTES);
+#pragma unroll
+                for (int i = 0; i < 9; ++i) w[i] = __ldg(src + i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 9; ++i) w[i] = 0;
+            }
+            int sum = 0;
+#pragma unroll
+            for (int i = 1; i < 9; ++i) {
+                sum = __dp4a(static_cast<int>(w[i]), 0x01010101, sum);
+                uint32_t lo, hi;
+                i8x4_to_h2(w[i], lo, hi);
+                xrow[b * 8 + (i - 1)] = make_uint2(lo, hi);
+            }
+            const unsigned short dbits = static_cast<unsigned short>(w[0] & 0xFFFFu);
+            da[p * nb + b] = dbits;
+            sa[p * nb + b] = __half2float(__ushort_as_half(dbits)) * static_cast<float>(sum);
+        }
+    }
+}
+
 // ------------------------------------------------------------------- host
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -781,24 +908,30 @@ int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64
 }
 
 int launch_gather(const uint8_t* act, const int32_t* perm, const int32_t* offsets, int32_t n_experts, int32_t top_k,
-                  int64_t nb, int64_t n_slots, uint16_t* xh, uint16_t* da, cudaStream_t s) {
+                  int64_t nb, int64_t n_slots, uint16_t* xh, uint16_t* da, cudaStream_t s, float* sa) {
     const int64_t rows = gemm_rows(n_slots);
     const int64_t want = (rows + 7) / 8;   // one warp per row, all rows at once
     const int64_t cap = 0x7FFFFFFF;
     const dim3 grid(static_cast<unsigned>(want < cap ? want : cap));
+    if (sa) {
+        gather_act_sums_kernel<<<grid, 256, 0, s>>>(act, perm, offsets, n_experts, top_k, static_cast<int32_t>(nb),
+                                                    rows, reinterpret_cast<uint2*>(xh), da, sa);
+        return check_launch("gather_act_sums_kernel", grid, dim3(256), 0);
+    }
     gather_act_kernel<<<grid, 256, 0, s>>>(act, perm, offsets, n_experts, top_k, static_cast<int32_t>(nb), rows,
                                            reinterpret_cast<uint2*>(xh), da);
     return check_launch("gather_act_kernel", grid, dim3(256), 0);
 }
 
-template <int BN, bool DUMP, bool FUSE>
+template <int BN, bool DUMP, bool FUSE, bool KQ = false>
 static int launch_gemm_kernel(const CUtensorMap& wmap, const CUtensorMap& xmap, const CUtensorMap& smap,
-                              const GemmArgs& ga, dim3 grid, cudaStream_t s, const char* name) {
-    using C = Gemm<BN>;
-    const void* k = reinterpret_cast<const void*>(moe_gemm_tc_kernel<BN, DUMP, FUSE>);
+                              const CUtensorMap& amap, const GemmArgs& ga, dim3 grid, cudaStream_t s,
+                              const char* name) {
+    using C = Gemm<BN, KQ>;
+    const void* k = reinterpret_cast<const void*>(moe_gemm_tc_kernel<BN, DUMP, FUSE, KQ>);
     if (int st = set_smem_limit(k, C::SMEM_BYTES)) return st;
     constexpr int threads = FUSE ? C::THREADS_FUSED : C::THREADS;
-    moe_gemm_tc_kernel<BN, DUMP, FUSE><<<grid, threads, C::SMEM_BYTES, s>>>(wmap, xmap, smap, ga);
+    moe_gemm_tc_kernel<BN, DUMP, FUSE, KQ><<<grid, threads, C::SMEM_BYTES, s>>>(wmap, xmap, smap, amap, ga);
     return check_launch(name, grid, dim3(threads), C::SMEM_BYTES);
 }
 
@@ -806,7 +939,7 @@ template <int BN>
 static int launch_gemm_bn(const uint8_t* weights, const int32_t* perm, const int32_t* offsets, const int32_t* tiles,
                           float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k, int32_t n_experts,
                           int64_t nrows, int64_t ncols, const uint16_t* xh, const uint16_t* da, const ActFuse* af,
-                          cudaStream_t s) {
+                          cudaStream_t s, const float* sa) {
     using C = Gemm<BN>;
     const int64_t nb = ncols / QK;
     const int sms = sm_count();
@@ -823,6 +956,11 @@ static int launch_gemm_bn(const uint8_t* weights, const int32_t* perm, const int
     if (int st = encode_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, da, nb, rows, nb * 2, C::KB, BN,
                            CU_TENSOR_MAP_SWIZZLE_NONE, "activation scales"))
         return st;
+    CUtensorMap amap = smap;   // Q4_K: the slots' d_a sum(q_a), [rows][nb] fp32
+    if (sa)
+        if (int st = encode_2d(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sa, nb, rows, nb * 4, C::KB, BN,
+                               CU_TENSOR_MAP_SWIZZLE_NONE, "activation sums"))
+            return st;
 
     GemmArgs ga{};
     ga.perm = perm;
@@ -846,9 +984,10 @@ static int launch_gemm_bn(const uint8_t* weights, const int32_t* perm, const int
     const int64_t slot_tiles_ub = (n_slots + BN - 1) / BN + (n_experts < n_slots ? n_experts : n_slots);
     const int64_t tiles_ub = slot_tiles_ub * ga.row_tiles;
     const dim3 grid(static_cast<unsigned>(tiles_ub < sms ? tiles_ub : sms));
-    if (dots) return launch_gemm_kernel<BN, true, false>(wmap, xmap, smap, ga, grid, s, "moe_gemm_tc_kernel<dump>");
-    if (af) return launch_gemm_kernel<BN, false, true>(wmap, xmap, smap, ga, grid, s, "moe_gemm_tc_kernel<act>");
-    return launch_gemm_kernel<BN, false, false>(wmap, xmap, smap, ga, grid, s, "moe_gemm_tc_kernel");
+    if (sa) return launch_gemm_kernel<BN, false, false, true>(wmap, xmap, smap, amap, ga, grid, s, "moe_gemm_tc_kernel<q4_k>");
+    if (dots) return launch_gemm_kernel<BN, true, false>(wmap, xmap, smap, amap, ga, grid, s, "moe_gemm_tc_kernel<dump>");
+    if (af) return launch_gemm_kernel<BN, false, true>(wmap, xmap, smap, amap, ga, grid, s, "moe_gemm_tc_kernel<act>");
+    return launch_gemm_kernel<BN, false, false>(wmap, xmap, smap, amap, ga, grid, s, "moe_gemm_tc_kernel");
 }
 
 int gemm_tile_width(double mean_slots_per_expert) {
@@ -861,16 +1000,17 @@ int gemm_tile_width(double mean_slots_per_expert) {
 int launch_gemm(const uint8_t* weights, const uint8_t* act, const int32_t* perm, const int32_t* offsets,
                 const int32_t* tiles, float* out, int32_t* dots, uint32_t* err, int64_t n_slots, int32_t top_k,
                 int32_t n_experts, int64_t nrows, int64_t ncols, uint16_t* xh, uint16_t* da, int tile_width,
-                cudaStream_t s, const ActFuse* af) {
+                cudaStream_t s, const ActFuse* af, const float* sa) {
     (void)act;   // read by launch_gather, which the caller runs first
     if (n_slots == 0) return FT_OK;
     if (af && (dots || af->n_inter * 2 != nrows))
         return fail(FT_ERR_ARG, "the fused activation needs nrows = 2 n_inter and no block dots");
+    if (sa && (dots || af)) return fail(FT_ERR_ARG, "Q4_K weights take the plain matmul only");
     if (tile_width == 32)
         return launch_gemm_bn<32>(weights, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,
-                                  ncols, xh, da, af, s);
+                                  ncols, xh, da, af, s, sa);
     return launch_gemm_bn<kGemmBN>(weights, perm, offsets, tiles, out, dots, err, n_slots, top_k, n_experts, nrows,
-                                   ncols, xh, da, af, s);
+                                   ncols, xh, da, af, s, sa);
 }
 
 }  // namespace ft

@@ -105,6 +105,44 @@ def test_gguf_bad_ids_zero_rows(ft, oracle, wtype):
     assert ft.read_device_error() & ft.FT_DEVERR_BAD_EXPERT_ID
 
 
+# Q4_K on the tensor-core path: (E, k, K, N, T, seed, routing) - 32-wide slot
+# tiles, 128-wide tiles with ragged slot counts and a ragged row count, Zipf
+# routing with empty experts, and a prefill-sized batch that the host sends to
+# the tensor cores by itself
+Q4K_GEMM = [(8, 2, 512, 256, 100, 101, "uniform"), (16, 4, 1024, 200, 700, 102, "uniform"),
+            (128, 8, 2048, 768, 64, 103, "zipf"), (6, 2, 768, 136, 333, 104, "uniform")]
+
+
+@pytest.mark.parametrize("E,k,K,N,T,seed,routing", Q4K_GEMM)
+def test_q4_k_on_the_tensor_cores(ft, oracle, E, k, K, N, T, seed, routing):
+    w, x, ids = _case("q4_k", E, k, K, N, T, seed, routing)
+    prev = ft.set_path("gemm")
+    try:
+        got, ref = _check(ft, oracle, "q4_k", w, x, ids, f"q4_k gemm {E},{k},{K},{N},{T}")
+    finally:
+        ft.set_path(prev)
+    assert ft.read_device_error() == 0
+
+
+def test_q4_k_tensor_cores_full_size(ft, oracle):
+    """The 128-expert top-8 prefill layer (1408 x 2816) at 2048 tokens with Q4_K
+    weights: the host picks the tensor cores; every output of 16 seeded tokens
+    against the oracle's matmul of the same type on those tokens."""
+    from bit_quantized_moe_quantize_gb300 import synth
+    E, k, K, N, T = 128, 8, 2816, 1408, 2048
+    wl = synth.custom_workload(E, k, K, N, 105)
+    w, x, ids = synth.make_weights_gguf(wl, "q4_k"), synth.make_activations(wl, T), synth.make_topk_ids(wl, T)
+    assert ft.selected_path(T, k, E, N, K) == ft.FT_PATH_GEMM
+    act = oracle.quantize_q8_1(x)
+    got = G.host(ft.moe_gguf_q8_1("q4_k", G.dev(w), G.dev(act), G.dev(ids)))
+    assert ft.read_device_error() == 0
+    toks = np.sort(np.random.default_rng(106).choice(T, 16, replace=False))
+    ref = oracle.moe_gguf("q4_k", w, act[toks], ids[toks])
+    wn = np.linalg.norm(oracle.dequantize_gguf("q4_k", w.reshape(E * N, -1, 144)), axis=-1).reshape(E, N)
+    xn = G.act_norms(oracle, act[toks])
+    G.check_close(got[toks], ref, wn[ids[toks]], np.broadcast_to(xn[:, None, None], (16, k, N)), "q4_k gemm full size")
+
+
 def test_gguf_rejects_what_the_path_cannot_run(ft, oracle):
     import torch
     w, x, ids = _case("q8_0", 8, 2, 256, 128, 4, 97)
@@ -112,7 +150,7 @@ def test_gguf_rejects_what_the_path_cannot_run(ft, oracle):
     dw, di = G.dev(w), G.dev(ids)
     prev = ft.set_path("gemm")
     try:
-        with pytest.raises(ft.FtError, match="Q4_0 weights only"):
+        with pytest.raises(ft.FtError, match="Q4_0 and Q4_K weights only"):
             ft.moe_gguf_q8_1("q8_0", dw, act, di)
     finally:
         ft.set_path(prev)

@@ -312,8 +312,11 @@ FT_API int ft_moe_q4_0_q8_1_ep(const void* weights_local, const void* act, const
  *             ([ncols/256] super-blocks for the K-quants); 16-byte aligned
  *   act, topk_ids, out, tokens, top_k, n_experts, nrows, ncols as for
  *   ft_moe_q4_0_q8_1.
- * Types other than Q4_0 always take the GEMV path (one weight block per
- * lane); ft_moe_set_path(FT_PATH_GEMM) makes them fail with FT_ERR_ARG.
+ * Q4_0 and Q4_K take either path by the rule of ft_moe_q4_0_q8_1 (Q4_K on the
+ * tensor cores: one 144-byte super-block per row and stage, its sub-block
+ * scales and mins applied in the drain); the other types always take the
+ * GEMV path, and ft_moe_set_path(FT_PATH_GEMM) makes them fail with
+ * FT_ERR_ARG.
  * Errors as for ft_moe_q4_0_q8_1, plus FT_ERR_ARG for an unknown wtype.
  */
 FT_API int ft_moe_gguf_q8_1(int32_t wtype, const void* weights, const void* act, const int32_t* topk_ids,

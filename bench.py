@@ -89,6 +89,9 @@ def parse():
     ap.add_argument("--wtype", default="q4_0",
                     choices=["q4_0", "q4_1", "q5_0", "q5_1", "q8_0", "q4_k", "q5_k", "q6_k", "q2_k", "q3_k"],
                     help="GGUF type of the expert weights (other than q4_0: ft_moe_gguf_q8_1; GEMV path, tensor cores too for q4_k)")
+    ap.add_argument("--path", choices=["auto", "gemv", "gemm", "gemv_dp4a"], default="auto",
+                    help="force the library's path (ft_moe_set_path); gemv_dp4a: the GEMV path without the "
+                         "mma.sync 8-slot tiles")
     ap.add_argument("--ffn", choices=["silu", "gelu_tanh"], default=None,
                     help="time both expert layers (ft_moe_ffn_q4_0_q8_1) with the workload's ncols as the hidden "
                          "size and its nrows as the intermediate size")
@@ -330,6 +333,8 @@ def ours(args):
         x = synth.make_activations(replica_workload(wl, rank), S)
     rows = S if args.per_slot else T
     # the tensor-core path takes Q4_0 and Q4_K weights (the same shape rule)
+    path_setting = args.path
+    ft.set_path(path_setting)
     path = {1: "gemv", 2: "gemm"}[ft.selected_path(T, k, E, N, K)] if wtype in ("q4_0", "q4_k") else "gemv"
 
     dw = torch.from_numpy(w).to(dev)
@@ -532,6 +537,11 @@ def ours(args):
         # 256-weight runs (all types but Q6_K, Q2_K, Q3_K), else one block per lane
         rows_ok = K % 256 == 0 and wtype not in ("q6_k", "q2_k", "q3_k")
         kern = ("moe_gemv_rows_kernel<fused>" if fused else "moe_gemv_rows_kernel") if rows_ok else "moe_gemv_kernel"
+        # 8-slot Q4_0 tiles (more than 4 slots per expert on average) run on the
+        # mma.sync kernel when its fp16 activation tile and two boxes fit
+        if (rows_ok and not fused and wtype == "q4_0" and S / E > 4.0 and path_setting != "gemv_dp4a"
+                and nb * 576 + 2 * 144 * 32 <= 227 * 1024):
+            kern = "moe_gemv_mma_kernel"
         achieved = alg_bytes / (mm_ms / 1000.0) / 1e9
         roof = {"kernel": kern, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_note": f"copy bandwidth, of {peak_src}",
@@ -578,7 +588,8 @@ def ours(args):
         "vs_baseline_note": "pages' Tesla T4 moe_vec time for this token count (context, other hardware)"
         if base else None,
         "dtype": f"{wtype} x q8_1: exact int block dots (f16 MMA / dp4a), f32 scaling",
-        "data": "synthetic", "config": {**config_of(name, wl, T, world), "path": path, "launch": launch_mode,
+        "data": "synthetic", "config": {**config_of(name, wl, T, world), "path": path, "path_setting": path_setting,
+                                        "launch": launch_mode,
                                         "activations": "per slot" if args.per_slot else "per token",
                                         "entry": "ft_moe_q4_0_fp16" if one_call else "ft_quantize_q8_1 + matmul",
                                         "weights": wtype},

@@ -12,7 +12,7 @@ synthetic-input generator used by the tests and the benchmark.
 """
 
 from ._lib import (ACT_GELU_TANH, ACT_SILU, FT_DEVERR_BAD_EXPERT_ID, FT_DEVERR_WAIT_TIMEOUT,
-                   FT_DEVERR_WORKSPACE_GUARD, FT_PATH_AUTO, FT_PATH_GEMM, FT_PATH_GEMV, FtError,
+                   FT_DEVERR_WORKSPACE_GUARD, FT_PATH_AUTO, FT_PATH_GEMM, FT_PATH_GEMV, FT_PATH_GEMV_DP4A, FtError,
                    act_mul_quantize_q8_1, block_dots, debug_stream_read, debug_wait_timeout, ffn_reserve, last_error, load,
                    moe_ffn_q4_0_q8_1, moe_gguf_q8_1, moe_q4_0_fp16, moe_q4_0_q8_1, moe_q4_0_q8_1_act, moe_q4_0_q8_1_ep,
                    moe_q4_0_q8_1_slots, profile_enable,
@@ -20,7 +20,7 @@ from ._lib import (ACT_GELU_TANH, ACT_SILU, FT_DEVERR_BAD_EXPERT_ID, FT_DEVERR_W
                    set_path, workspace_bytes, WEIGHT_TYPES)
 
 __all__ = [
-    "ACT_GELU_TANH", "ACT_SILU", "WEIGHT_TYPES", "moe_gguf_q8_1", "repack_q4_0_soa", "act_mul_quantize_q8_1", "moe_ffn_q4_0_q8_1", "moe_q4_0_q8_1_act", "ffn_reserve", "moe_q4_0_fp16", "FT_DEVERR_BAD_EXPERT_ID", "FT_DEVERR_WAIT_TIMEOUT", "FT_DEVERR_WORKSPACE_GUARD", "debug_wait_timeout", "debug_stream_read", "FT_PATH_AUTO", "FT_PATH_GEMM", "FT_PATH_GEMV", "FtError",
+    "ACT_GELU_TANH", "ACT_SILU", "WEIGHT_TYPES", "moe_gguf_q8_1", "repack_q4_0_soa", "act_mul_quantize_q8_1", "moe_ffn_q4_0_q8_1", "moe_q4_0_q8_1_act", "ffn_reserve", "moe_q4_0_fp16", "FT_DEVERR_BAD_EXPERT_ID", "FT_DEVERR_WAIT_TIMEOUT", "FT_DEVERR_WORKSPACE_GUARD", "debug_wait_timeout", "debug_stream_read", "FT_PATH_AUTO", "FT_PATH_GEMM", "FT_PATH_GEMV", "FT_PATH_GEMV_DP4A", "FtError",
     "block_dots", "last_error", "load", "moe_q4_0_q8_1", "moe_q4_0_q8_1_ep", "moe_q4_0_q8_1_slots", "profile_enable", "profile_read", "quantize_q8_1", "read_device_error", "release", "reserve",
     "route_offsets", "selected_path", "set_path", "workspace_bytes",
 ]

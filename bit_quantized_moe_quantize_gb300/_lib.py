@@ -22,8 +22,8 @@ STATUS_NAMES = {0: "FT_OK", 1: "FT_ERR_ARG", 2: "FT_ERR_SIZE", 3: "FT_ERR_ALIGN"
 FT_DEVERR_BAD_EXPERT_ID = 0x1
 FT_DEVERR_WAIT_TIMEOUT = 0x2
 FT_DEVERR_WORKSPACE_GUARD = 0x4
-FT_PATH_AUTO, FT_PATH_GEMV, FT_PATH_GEMM = 0, 1, 2
-PATHS = {"auto": FT_PATH_AUTO, "gemv": FT_PATH_GEMV, "gemm": FT_PATH_GEMM}
+FT_PATH_AUTO, FT_PATH_GEMV, FT_PATH_GEMM, FT_PATH_GEMV_DP4A = 0, 1, 2, 3
+PATHS = {"auto": FT_PATH_AUTO, "gemv": FT_PATH_GEMV, "gemm": FT_PATH_GEMM, "gemv_dp4a": FT_PATH_GEMV_DP4A}
 
 EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_moe_workspace_bytes",
            "ft_moe_reserve", "ft_moe_release", "ft_moe_read_device_error", "ft_moe_set_path",

@@ -328,6 +328,7 @@ static int path_setting() {
         const char* v = std::getenv("FT_MOE_PATH");
         if (v && std::strcmp(v, "gemv") == 0) g_path = FT_PATH_GEMV;
         if (v && std::strcmp(v, "gemm") == 0) g_path = FT_PATH_GEMM;
+        if (v && std::strcmp(v, "gemv_dp4a") == 0) g_path = FT_PATH_GEMV_DP4A;
     }
     return g_path;
 }
@@ -343,7 +344,7 @@ static bool gemm_shape_ok(const Shape& sh) {
 static bool gemm_type_ok(int wtype) { return wtype == FT_TYPE_Q4_0 || wtype == FT_TYPE_Q4_K; }
 
 static int choose_path(const Shape& sh, int setting) {
-    if (setting == FT_PATH_GEMV) return FT_PATH_GEMV;
+    if (setting == FT_PATH_GEMV || setting == FT_PATH_GEMV_DP4A) return FT_PATH_GEMV;
     if (!gemm_type_ok(sh.wtype)) return setting == FT_PATH_GEMM ? FT_PATH_GEMM : FT_PATH_GEMV;
     if (setting == FT_PATH_GEMM) return FT_PATH_GEMM;
     if (!gemm_shape_ok(sh)) return FT_PATH_GEMV;
@@ -353,7 +354,8 @@ static int choose_path(const Shape& sh, int setting) {
 // Slots above which the GEMV path is never chosen by itself (the tensor-core
 // path takes over at 16 routed slots per expert on average).
 static int64_t gemv_max_slots(const Shape& sh) {
-    if (path_setting() == FT_PATH_GEMV || !gemm_shape_ok(sh) || sh.wtype != FT_TYPE_Q4_0) return sh.n_slots;
+    const int setting = path_setting();
+    if (setting == FT_PATH_GEMV || setting == FT_PATH_GEMV_DP4A || !gemm_shape_ok(sh) || sh.wtype != FT_TYPE_Q4_0) return sh.n_slots;
     const int64_t lim = 16 * static_cast<int64_t>(sh.n_global);
     return sh.n_slots < lim ? sh.n_slots : lim;
 }
@@ -380,7 +382,11 @@ static int run_matmul(const void* weights, const void* act, const int32_t* topk_
         return fail(FT_ERR_ARG, "the tensor-core path needs ncols %% 256 == 0 and n_experts * nrows >= 128 (got %lld, %lld)",
                     (long long)sh.ncols, (long long)sh.n_experts * sh.nrows);
     const bool h_in_ws = af && path == FT_PATH_GEMV;
-    const GemvPlan gp = plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols, sh.mean(), sh.wtype);
+    const GemvPlan gp = plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols, sh.mean(), sh.wtype,
+                                  path_setting() != FT_PATH_GEMV_DP4A);
+    // the one-launch decode step is the row-per-lane kernel: not where the
+    // routed matmul runs mma.sync tiles (its result must equal quantize +
+    // matmul bit for bit; gemv_fused_ok rejects such plans)
     const bool one_launch = x16 && !af && !dots && path == FT_PATH_GEMV && sh.wtype == FT_TYPE_Q4_0 &&
                             sh.act_div == sh.top_k && sh.n_global == sh.n_experts && aligned(x16, 16) &&
                             gp.smem <= 227 * 1024 && gemv_fused_ok(gp, sh.n_slots, sh.n_experts, sh.ncols);
@@ -884,7 +890,7 @@ int ft_profile_read(double* quantize_ms, double* route_ms, double* matmul_ms, in
 }
 
 int ft_moe_set_path(int32_t path) {
-    if (path != FT_PATH_AUTO && path != FT_PATH_GEMV && path != FT_PATH_GEMM) return -1;
+    if (path != FT_PATH_AUTO && path != FT_PATH_GEMV && path != FT_PATH_GEMM && path != FT_PATH_GEMV_DP4A) return -1;
     const int prev = path_setting();
     std::lock_guard<std::mutex> lk(g_path_mu);
     g_path = path;

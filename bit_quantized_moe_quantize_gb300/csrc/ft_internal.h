@@ -74,11 +74,16 @@ struct GemvPlan {
     int64_t row_tiles;    // grid.y: CTAs per slot tile
     int64_t rows_per_cta;
     size_t smem;
+    // Q4_0 tiles of `mma` groups of 8 slots on mma.sync (moe_gemv_mma.cu; 0:
+    // the dp4a kernels); row_warps (warps of 16 rows there), stages and smem
+    // then describe that kernel
+    int mma;
 };
 
-// mean: routed slots per expert on average (decides the slots per tile)
+// mean: routed slots per expert on average (decides the slots per tile);
+// mma: Q4_0 tiles with more than 4 slots may run on the mma.sync kernel
 GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols, double mean,
-                   int wtype = FT_TYPE_Q4_0);
+                   int wtype = FT_TYPE_Q4_0, bool mma = true);
 // bytes of one stored block of a FT_TYPE_* weight type (0: unknown type) and
 // the weights it holds (32, or 256 for the K-quant super-blocks)
 int weight_block_bytes(int wtype);

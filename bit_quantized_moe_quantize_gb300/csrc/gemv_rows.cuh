@@ -556,4 +556,10 @@ static int launch_gemv_rows_type(const GemvPlan& plan, const CUtensorMap& wmap, 
 int launch_gemv_rows_gguf(int wtype, const GemvPlan& plan, const CUtensorMap& wmap, const GemvArgs& a,
                           cudaStream_t s);
 
+// Q4_0 tiles of nt groups of 8 slots on mma.sync (moe_gemv_mma.cu): shared
+// memory of a CTA of row_warps row warps with a ring of `stages` boxes (row
+// blocks of 32 * row_warps rows, wmap's box), and the launch (dump: block dots).
+size_t gemv_mma_smem(int nb, int nt, int row_warps, int stages);
+int launch_gemv_mma(const GemvPlan& plan, const CUtensorMap& wmap, const GemvArgs& a, bool dump, cudaStream_t s);
+
 }  // namespace ft

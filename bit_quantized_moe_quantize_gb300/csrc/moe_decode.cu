@@ -17,7 +17,7 @@ namespace ft {
 constexpr int64_t kFuseMaxStagedBlocks = 256;
 
 bool gemv_fused_ok(const GemvPlan& plan, int64_t n_slots, int32_t n_experts, int64_t ncols) {
-    if (plan.row_warps <= 0 || n_slots > kFuseMaxSlots || n_experts > kFuseMaxExperts) return false;
+    if (plan.row_warps <= 0 || plan.mma || n_slots > kFuseMaxSlots || n_experts > kFuseMaxExperts) return false;
     if (static_cast<int64_t>(plan.group) * (ncols / QK) > kFuseMaxStagedBlocks) return false;
     const size_t ring = static_cast<size_t>(plan.stages) * RowBox<FT_TYPE_Q4_0>::PITCH * 32 * plan.row_warps;
     return gemv_fused_scratch_bytes(n_slots, n_experts) <= ring;

@@ -84,7 +84,8 @@ int row_box_pitch(int wtype) {
     }
 }
 
-GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols, double mean, int wtype) {
+GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t ncols, double mean, int wtype,
+                   bool mma) {
     // row bytes per 32 weights (144 / 8, 176 / 8 for Q4_K, Q5_K; Q6_K's 210 / 8
     // rounded up, enough for sizing the ring)
     const int block_bytes = (weight_block_bytes(wtype) * 32 + weight_block_values(wtype) - 1) / weight_block_values(wtype);
@@ -137,6 +138,45 @@ GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t nc
         p.rows_per_cta = (nrows + 32 * rw - 1) / (32 * rw);   // row blocks per slot tile
         p.min_tiles = min_tiles;
         p.row_tiles = 0;
+        if (mma && wtype == FT_TYPE_Q4_0 && mean > 4.0) {
+            // tiles on mma.sync: 16 slots (two groups of 8) where their fp16
+            // activation tile leaves room for a ring, else 8.  One CTA per SM
+            // of RW warps of 16 rows (fewer when the batch has fewer row blocks
+            // than SMs), RW chosen for a ring of at least 3 boxes where one exists
+            const size_t cap = 227 * 1024;
+            const int64_t groups16 = (nrows + 15) / 16;
+            for (int nt = 2; nt >= 1; --nt) {
+                const int64_t tiles = (local + 8 * nt - 1) / (8 * nt);
+                int best_rw = 0, best_st = 0;
+                static const int kRowWarps[] = {16, 12, 8, 4, 2, 1};
+                for (int need = 3; need >= 2 && best_rw == 0; --need)
+                    for (int mrw : kRowWarps) {
+                        // fewer rows per block only where the row blocks would not cover the SMs
+                        if (mrw > 1 && tiles * ((groups16 + mrw - 1) / mrw) < sms) continue;
+                        const size_t r0 = gemv_mma_smem(static_cast<int>(nb), nt, mrw, 0);
+                        const size_t stg = static_cast<size_t>(row_box_pitch(wtype)) * 16 * mrw;
+                        int st = cap > r0 ? static_cast<int>((cap - r0) / stg) : 0;
+                        st = st > kMaxRowStages ? kMaxRowStages : st;
+                        if (st >= need) {
+                            best_rw = mrw;
+                            best_st = st;
+                            break;
+                        }
+                    }
+                if (best_rw == 0) continue;
+                p.mma = nt;
+                p.group = 8 * nt;
+                p.row_warps = best_rw;
+                p.ksplit = 1;
+                p.stages = best_st;
+                p.smem = gemv_mma_smem(static_cast<int>(nb), nt, best_rw, best_st);
+                p.min_tiles = tiles > 0 ? tiles : 1;
+                const int64_t ub2 = (n_slots + p.group - 1) / p.group + (n_experts < n_slots ? n_experts : n_slots);
+                p.grid_x = ub2 < n_slots ? ub2 : n_slots;
+                p.rows_per_cta = (nrows + 16 * best_rw - 1) / (16 * best_rw);
+                break;
+            }
+        }
         return p;
     }
     const int64_t row_bytes = nb * block_bytes;
@@ -231,11 +271,13 @@ int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act
         const int bytes = row_box_bytes(wtype), pitch = row_box_pitch(wtype);
         const uint64_t row_bytes = static_cast<uint64_t>(a.nb / 8) * bytes;
         CUtensorMap wmap;
+        // (rows per box: 32 per row warp, 16 on the mma.sync kernel)
         if (int st = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, weights, row_bytes / 2,
-                               static_cast<uint64_t>(n_experts) * nrows, row_bytes, pitch / 2, 32 * plan.row_warps,
-                               CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
+                               static_cast<uint64_t>(n_experts) * nrows, row_bytes, pitch / 2,
+                               (plan.mma ? 16 : 32) * plan.row_warps, CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
             return st;
         if (wtype != FT_TYPE_Q4_0) return launch_gemv_rows_gguf(wtype, plan, wmap, a, s);
+        if (plan.mma) return launch_gemv_mma(plan, wmap, a, dump, s);
         switch (plan.group) {
             case 1: return dump ? launch_gemv_rows<FT_TYPE_Q4_0, 1, true>(plan, wmap, a, s) : launch_gemv_rows<FT_TYPE_Q4_0, 1, false>(plan, wmap, a, s);
             case 2: return dump ? launch_gemv_rows<FT_TYPE_Q4_0, 2, true>(plan, wmap, a, s) : launch_gemv_rows<FT_TYPE_Q4_0, 2, false>(plan, wmap, a, s);

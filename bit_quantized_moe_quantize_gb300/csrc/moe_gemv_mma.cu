@@ -1,0 +1,432 @@
+// GEMV tiles of 8 or 16 slots of the routed Q4_0 x Q8_1 expert matmul
+// (moe_vec_q4_0_q8_1 on FreeToken PR #185, "Problem" and "Notes") on the
+// warp-level tensor-core instruction mma.sync.m16n8k16 (fp16 operands, fp32
+// accumulation), for decode batches with more than 4 slots per expert.
+//
+// Why: with 8 slots per tile the row-per-lane kernel (gemv_rows.cuh) spends
+// 8 dp4a, three shared loads and two float ops per weight block and slot, and
+// is bound by instruction issue well below the memory roofline.  Here one
+// m16n8k16 pair forms 16 rows x 8 slots x 32 weights of block dots at once;
+// the per-block scales stay in the epilogue of every block (the accumulator
+// is in registers, so reading it back costs nothing, where tcgen05 would need
+// a tensor-memory round trip per 32-weight block).  A tile of NT = 2 slot
+// groups (16 slots) shares the weight fragments between two MMA pairs, so an
+// expert with up to 16 slots streams its weights once.
+//
+// Exactness.  Both operands hold small integers exactly: A = 1024 + q (low
+// nibbles) and 1024 + 16 q (high nibbles), formed by OR-ing the nibble into the
+// fp16 pattern of 1024; B = the activation codes, divided by 16 for the high
+// nibbles (a power of two: exact).  Every product is an integer and every
+// partial sum stays below 2^23, so the fp32 accumulation is exact whatever its
+// order.  The accumulator starts at -(1032 S_lo + 72 S_hi) with S_lo, S_hi the
+// sums of the block's first and last 16 codes, which removes the 1024 offsets
+// and the Q4_0 level 8; the result is the integer block dot
+// sum_i (q_i - 8) q_a[i], the same integer the dp4a kernels form.  It is then
+// scaled as there, acc = fma(dot, d_w * d_a, acc), blocks in order, so the
+// outputs equal the row-per-lane kernel's bit for bit wherever that kernel
+// does not split K.
+//
+// Fragment layout (m16n8k16, A row-major 16 x 16, B 16 x 8, per the PTX ISA):
+// lane = 4 g + t holds A rows g, g + 8 at k = 2t, 2t+1 (regs 0, 1) and
+// 2t+8, 2t+9 (regs 2, 3); B column (slot) g at k = 2t, 2t+1 and 2t+8, 2t+9;
+// C rows g, g + 8 at columns (slots) 2t, 2t+1.  Which of a block's 32 weights
+// sits at which k is free as long as A and B agree: lane t takes the four
+// nibble bytes P_t of the block (an aligned 32-bit word of the shared box:
+// bytes 4t..4t+3 for odd blocks, whose nibbles start 4-byte aligned; for even
+// blocks 4t-2..4t+1, and 0, 1, 14, 15 for t = 0, joined from two words with a
+// byte permute), the low nibbles of bytes 0, 2 / 1, 3 of that word at k = 2t,
+// 2t+1 / 2t+8, 2t+9 of the first MMA, the high nibbles likewise in the second.
+// The activation side is staged in that order as the lane's 8 codes (biased
+// to unsigned bytes), 8 bytes per lane, block and slot group (one
+// conflict-free 8-byte load), and turned into fp16 pairs with a byte permute
+// and one fp16 op per pair: half the shared memory of staged fp16 pairs,
+// which leaves room for 16 row warps and a 3-box ring.
+//
+// Work split.  The grid is one CTA per SM.  A work item is (slot tile, block
+// of 16 RW rows), numbered tile-major; there are tiles x row blocks of them
+// (the tile count is read on the device).  Each CTA takes one contiguous
+// range, cut by weight: an item whose tile uses its second slot group counts
+// 5, any other 3 (about their measured costs), so the SMs finish together
+// whatever the routing, and a CTA restages the activations only where its
+// range enters a new tile (items handed out one by one from a global counter
+// balance better but restage at nearly every item, which measured slower).
+// Weights stream as in the row-per-lane kernel: TMA boxes of 256 weights
+// (8 blocks, 144 bytes per row) x 16 RW rows through an mbarrier ring filled
+// by one producer warp, which runs ahead of the staging.  Warp r owns rows
+// 16 r .. 16 r + 15 of each box (one m16 tile), so a CTA keeps up to 16 row
+// warps busy on one staged activation tile.
+#include <cuda_fp16.h>
+
+#include "gemv_rows.cuh"
+
+namespace ft {
+
+// Shared memory: mbarriers full/empty [kMaxRowStages] | work range int64[2] |
+// qb [nb][NT][32 lanes] uint2 (codes + 128 at P_t: first / last 16) | xc
+// [nb][NT][4] float4 (the
+// accumulator's start for lane t: minus the offset sums of slots 2t, 2t+1,
+// twice, as the MMA's C quad) | xd [nb][NT][4] float2 (d_a of slots 2t, 2t+1)
+// | ring (128-byte aligned)
+__host__ __device__ inline size_t gemv_mma_qb_offset() { return 8 * 2 * kMaxRowStages + 16; }
+__host__ __device__ inline size_t gemv_mma_ring_offset(int nb, int nt) {
+    return (gemv_mma_qb_offset() + static_cast<size_t>(nb) * nt * (256 + 64 + 32) + 127) / 128 * 128;
+}
+size_t gemv_mma_smem(int nb, int nt, int row_warps, int stages) {
+    return gemv_mma_ring_offset(nb, nt) + static_cast<size_t>(stages) * RowBox<FT_TYPE_Q4_0>::PITCH * 16 * row_warps;
+}
+
+// D = A B + C on m16n8k16, fp16 operands, fp32 accumulators (not volatile: a
+// pure function of its operands, which the compiler may schedule freely, so
+// independent MMAs overlap their latencies)
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1, float c0,
+                                          float c1, float c2, float c3) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
+}
+
+__device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// The nibble word P_t of block j (compile-time) of a box row.
+template <int J>
+__device__ __forceinline__ uint32_t nibble_word(const uint8_t* row, uint32_t t) {
+    if constexpr (J & 1) {
+        return lds32(row + 18 * J + 2 + 4 * t);
+    } else {
+        const uint32_t x = lds32(row + 18 * J + 4 * t);
+        const uint32_t y = lds32(row + 18 * J + (t ? 4 * t : 16));
+        return __byte_perm(x, y, t ? 0x3210u : 0x5432u);
+    }
+}
+
+// Activation codes of the staging item (slot, block b, lane t): the 4 bytes
+// at positions P_t of the block's first 16 codes (hi: of its last 16).
+__device__ __forceinline__ uint32_t code_word(const uint8_t* codes, int32_t b, uint32_t t) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(codes);
+    if (b & 1) return __ldg(w + t);
+    if (t == 0) return __byte_perm(__ldg(w), __ldg(w + 3), 0x7610u);
+    return __byte_perm(__ldg(w + t - 1), __ldg(w + t), 0x5432u);
+}
+
+// B fragments from four codes biased by 128 (bytes u = q + 128): bytes 0, 2
+// (k = 2t, 2t+1) and 1, 3 (k = 2t+8, 2t+9) as fp16 pairs.  A byte under the
+// fp16 pattern of 1024 is 1024 + u exactly; minus 1152 it is q (lo), times
+// 1/16 minus 72 it is q / 16 (hi); both exact in fp16.
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<const __half2*>(&u); }
+__device__ __forceinline__ void codes_lo(uint32_t u, uint32_t& b0, uint32_t& b1) {
+    const __half2 k = __float2half2_rn(1152.0f);
+    b0 = h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x4240u)), k));
+    b1 = h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x4341u)), k));
+}
+__device__ __forceinline__ void codes_hi(uint32_t u, uint32_t& b0, uint32_t& b1) {
+    const __half2 s = __float2half2_rn(0.0625f), k = __float2half2_rn(-72.0f);
+    b0 = h2_bits(__hfma2(bits_h2(__byte_perm(u, 0x64646464u, 0x4240u)), s, k));
+    b1 = h2_bits(__hfma2(bits_h2(__byte_perm(u, 0x64646464u, 0x4341u)), s, k));
+}
+
+
+// Enter slot tile `tile` (compute warps, n_threads of them): stage its
+// activations as B fragments and offset sums, and return its slot count and
+// the slot ids of this thread's output columns (-1: none).
+template <int NT>
+__device__ __forceinline__ void mma_stage_tile(const GemvArgs& a, int64_t tile, uint2* qb, float4* xc, float2* xd,
+                                               int32_t n_threads, int32_t& ng, int32_t (&sid)[NT][2]) {
+    constexpr int G = 8 * NT;
+    const int32_t nb = a.nb;
+    const int32_t e = find_expert(a.tiles, a.n_experts, tile);
+    const int64_t p0 = static_cast<int64_t>(a.offsets[e]) + (tile - a.tiles[e]) * G;
+    ng = static_cast<int32_t>(min(static_cast<int64_t>(G), a.offsets[e + 1] - p0));
+    const uint32_t lane = lane_id(), g = lane >> 2, tq = lane & 3u;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int32_t n = nt * 8 + static_cast<int32_t>(2 * tq) + c;
+            sid[nt][c] = n < ng ? __ldg(a.perm + p0 + n) : -1;
+        }
+    // item i = ((b NT + group) 32 + lane), lane = 4 g + t: slot (group, g)'s
+    // codes at P_t of block b; the four lanes of a slot add up the block's
+    // code sums with two shuffles
+    for (int32_t i = static_cast<int32_t>(threadIdx.x); i < nb * NT * 32; i += n_threads) {
+        const int32_t bn = i >> 5, b = bn / NT, n = (bn - b * NT) * 8 + static_cast<int32_t>(g);
+        uint32_t wl = 0, wh = 0;
+        float d = 0.0f;
+        if (n < ng) {
+            const int64_t tok = __ldg(a.perm + p0 + n) / a.top_k;
+            const uint8_t* blk = a.act + (tok * nb + b) * Q8_1_BYTES;
+            d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(blk))));
+            wl = code_word(blk + 4, b, tq);
+            wh = code_word(blk + 20, b, tq);
+        }
+        qb[i] = make_uint2(wl ^ 0x80808080u, wh ^ 0x80808080u);
+        int sl = __dp4a(static_cast<int>(wl), 0x01010101, 0), sh = __dp4a(static_cast<int>(wh), 0x01010101, 0);
+        sl += __shfl_xor_sync(0xFFFFFFFFu, sl, 1);
+        sh += __shfl_xor_sync(0xFFFFFFFFu, sh, 1);
+        sl += __shfl_xor_sync(0xFFFFFFFFu, sl, 2);
+        sh += __shfl_xor_sync(0xFFFFFFFFu, sh, 2);
+        if (tq == 0) {
+            float* c = reinterpret_cast<float*>(xc + static_cast<size_t>(bn) * 4 + (g >> 1));
+            const float c0 = -static_cast<float>(1032 * sl + 72 * sh);
+            c[g & 1] = c0;
+            c[2 + (g & 1)] = c0;
+            reinterpret_cast<float*>(xd + static_cast<size_t>(bn) * 4 + (g >> 1))[g & 1] = d;
+        }
+    }
+}
+
+// Item weights of the work split: an item of a tile whose second slot group
+// holds slots costs about 1.7 times one whose tile has 8 slots or fewer
+// (measured: 53 against 31 us per CTA item on the Mixtral-shaped layer).
+constexpr int64_t kMmaW1 = 3, kMmaW2 = 5;
+
+// The CTA's contiguous range [w0, w1) of the work items (tile-major
+// (tile, row block)), cut so that every CTA gets the same item weight: CTA c
+// takes the items whose weight interval starts in [c W / grid, (c + 1) W /
+// grid), W the total.  One warp scans the experts' slot counts (tiles of
+// expert e: ceil(count / G), all full but the last) twice: once for W, once to
+// place the two bounds.  Written to range[0..1].
+template <int NT>
+__device__ void mma_work_range(const GemvArgs& a, int64_t n_rb, int64_t* range) {
+    constexpr int G = 8 * NT;
+    constexpr int64_t W1 = NT > 1 ? kMmaW1 : 1, W2 = NT > 1 ? kMmaW2 : 1;
+    const int32_t E = a.n_experts;
+    const uint32_t lane = lane_id();
+    auto expert = [&](int32_t e, int64_t& tl, int64_t& wt, int64_t& ulast) {
+        const int64_t c = e < E ? static_cast<int64_t>(a.offsets[e + 1] - a.offsets[e]) : 0;
+        tl = (c + G - 1) / G;
+        ulast = c - G * (tl - 1) > 8 ? W2 : W1;
+        wt = tl > 0 ? (tl - 1) * W2 + ulast : 0;
+    };
+    int64_t tot = 0;
+    for (int32_t e0 = 0; e0 < E; e0 += 32) {
+        int64_t tl, wt, ul;
+        expert(e0 + static_cast<int32_t>(lane), tl, wt, ul);
+        tot += wt;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
+    const int64_t W = tot * n_rb;
+    const int64_t P[2] = {W * blockIdx.x / gridDim.x, W * (blockIdx.x + 1) / gridDim.x};
+    int64_t wbase = 0, ibase = 0;                  // weight and items before the chunk
+    if (lane < 2) range[lane] = static_cast<int64_t>(a.tiles[E]) * n_rb;   // P == W: past the last item
+    __syncwarp();
+    for (int32_t e0 = 0; e0 < E; e0 += 32) {
+        int64_t tl, wt, ul;
+        expert(e0 + static_cast<int32_t>(lane), tl, wt, ul);
+        int64_t wi = wt * n_rb, ii = tl * n_rb;    // inclusive prefix over the chunk
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xFFFFFFFFu, wi, o), z = __shfl_up_sync(0xFFFFFFFFu, ii, o);
+            if (static_cast<int>(lane) >= o) {
+                wi += y;
+                ii += z;
+            }
+        }
+        const int64_t ws = wbase + wi - wt * n_rb, is = ibase + ii - tl * n_rb;   // this expert's start
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            if (wt > 0 && P[k] >= ws && P[k] < ws + wt * n_rb) {
+                const int64_t q = P[k] - ws, full = (tl - 1) * W2 * n_rb;
+                int64_t item;
+                if (q < full) {
+                    const int64_t t = q / (W2 * n_rb), q2 = q - t * W2 * n_rb;
+                    item = is + t * n_rb + (q2 + W2 - 1) / W2;
+                } else {
+                    item = is + (tl - 1) * n_rb + (q - full + ul - 1) / ul;
+                }
+                range[k] = item;
+            }
+        }
+        wbase += __shfl_sync(0xFFFFFFFFu, wi, 31);
+        ibase += __shfl_sync(0xFFFFFFFFu, ii, 31);
+    }
+}
+
+template <int NT, bool DUMP>
+__global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                              const GemvArgs a) {
+    constexpr int PITCH = RowBox<FT_TYPE_Q4_0>::PITCH;   // 144: 8 blocks of 18 bytes
+    const int32_t RW = a.row_warps;                       // warps of 16 rows
+    const int32_t E = a.n_experts;
+    const int32_t nb = a.nb;
+    const int32_t n_ks = nb / 8;                          // boxes per row
+    const int NS = a.stages;
+    const int64_t n_rb = (a.nrows + 16 * RW - 1) / (16 * RW);
+
+    extern __shared__ __align__(128) uint8_t smem_mma[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_mma);
+    uint64_t* empty = full + kMaxRowStages;
+    int64_t* range = reinterpret_cast<int64_t*>(empty + kMaxRowStages);
+    uint2* qb = reinterpret_cast<uint2*>(smem_mma + gemv_mma_qb_offset());          // [nb][NT][32]
+    float4* xc = reinterpret_cast<float4*>(qb + static_cast<size_t>(nb) * NT * 32);  // [nb][NT][4]
+    float2* xd = reinterpret_cast<float2*>(xc + static_cast<size_t>(nb) * NT * 4);   // [nb][NT][4]
+    uint8_t* ring = smem_mma + gemv_mma_ring_offset(nb, NT);
+    const uint32_t stage_bytes = static_cast<uint32_t>(PITCH * 16 * RW);
+    const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], RW);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 0) mma_work_range<NT>(a, n_rb, range);
+    __syncthreads();
+    const int64_t w0 = range[0], w1 = range[1];
+    if (w0 >= w1) return;
+
+    if (static_cast<int32_t>(warp) == RW) {
+        // ------------------------------------------------------------ producer
+        int64_t w = w0, tile = -1, erow0 = 0;
+        int32_t ks = 0;
+        const int64_t n_it = (w1 - w0) * n_ks;
+        for (int64_t it = 0; it < n_it; ++it) {
+            const int64_t tl = w / n_rb;
+            if (tl != tile) {
+                tile = tl;
+                erow0 = static_cast<int64_t>(find_expert(a.tiles, E, tl)) * a.nrows;
+            }
+            const int32_t s = static_cast<int32_t>(it % NS);
+            if (!mbar_wait_warp(&empty[s], static_cast<uint32_t>(((it / NS) & 1) ^ 1), a.err)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[s], stage_bytes);
+                tma_load_2d(ring + static_cast<size_t>(s) * stage_bytes, &wmap, ks * (PITCH / 2),
+                            static_cast<int32_t>(erow0 + (w - tl * n_rb) * 16 * RW), &full[s]);
+            }
+            __syncwarp();
+            if (++ks == n_ks) {
+                ks = 0;
+                ++w;
+            }
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------------- compute
+    // A warp whose bounded wait gave up stops waiting and computing but still
+    // takes every tile change's barriers, so no other warp waits on it.
+    const int32_t r = static_cast<int32_t>(warp);
+    const uint32_t g = lane >> 2, tq = lane & 3u;
+    const uint32_t n_threads = static_cast<uint32_t>(RW) * 32u;
+    int64_t cur = -1, it = 0;
+    int32_t ng = 0, sid[NT][2];
+    bool ok = true;
+    for (int64_t w = w0; w < w1; ++w) {
+        const int64_t tile = w / n_rb, rb = w - tile * n_rb;
+        if (tile != cur) {
+            if (cur >= 0) named_bar_sync(1, n_threads);  // every warp is done with the previous tile
+            mma_stage_tile<NT>(a, tile, qb, xc, xd, static_cast<int32_t>(n_threads), ng, sid);
+            named_bar_sync(1, n_threads);
+            cur = tile;
+        }
+        if (!ok) continue;
+        const int64_t row0 = rb * 16 * RW + r * 16;        // first row of the warp within the expert
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[nt][c] = 0.0f;
+        // one box: 8 blocks x rows g, g + 8 of the warp's 16, against the
+        // first (USE = 1) or both (USE = 2) slot groups
+        auto box_pass = [&](const uint8_t* ra, int32_t ks, auto USE_) {
+            constexpr int USE = decltype(USE_)::value;
+            const uint8_t* rb8 = ra + 8 * PITCH;
+            auto block = [&](auto J) {
+                constexpr int j = decltype(J)::value;
+                const int32_t b = ks * 8 + j;
+                const uint32_t wa = nibble_word<j>(ra, tq), wb = nibble_word<j>(rb8, tq);
+                const float dwa = __half2float(*reinterpret_cast<const __half*>(ra + 18 * j));
+                const float dwb = __half2float(*reinterpret_cast<const __half*>(rb8 + 18 * j));
+                const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+                const uint32_t alo[4] = {(wa & 0x000F000Fu) | 0x64006400u, (wb & 0x000F000Fu) | 0x64006400u,
+                                         (wa8 & 0x000F000Fu) | 0x64006400u, (wb8 & 0x000F000Fu) | 0x64006400u};
+                const uint32_t ahi[4] = {(wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
+                                         (wa8 & 0x00F000F0u) | 0x64006400u, (wb8 & 0x00F000F0u) | 0x64006400u};
+#pragma unroll
+                for (int nt = 0; nt < USE; ++nt) {
+                    const size_t bn = static_cast<size_t>(b) * NT + nt;
+                    const uint2 Q = qb[bn * 32 + lane];
+                    const float4 C = xc[bn * 4 + tq];
+                    const float2 D = xd[bn * 4 + tq];
+                    uint32_t bl0, bl1, bh0, bh1;
+                    codes_lo(Q.x, bl0, bl1);
+                    codes_hi(Q.y, bh0, bh1);
+                    float d0[4], d1[4];
+                    mma_16816(d0, alo, bl0, bl1, C.x, C.y, C.z, C.w);
+                    mma_16816(d1, ahi, bh0, bh1, d0[0], d0[1], d0[2], d0[3]);
+                    if constexpr (DUMP) {
+                        (void)D;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const int32_t sl = sid[nt][c & 1];
+                            const int64_t row = row0 + g + (c < 2 ? 0 : 8);
+                            if (sl >= 0 && row < a.nrows)
+                                a.dots[(static_cast<int64_t>(sl) * a.nrows + row) * nb + b] = __float2int_rn(d1[c]);
+                        }
+                    } else {
+                        acc[nt][0] = fmaf(d1[0], dwa * D.x, acc[nt][0]);
+                        acc[nt][1] = fmaf(d1[1], dwa * D.y, acc[nt][1]);
+                        acc[nt][2] = fmaf(d1[2], dwb * D.x, acc[nt][2]);
+                        acc[nt][3] = fmaf(d1[3], dwb * D.y, acc[nt][3]);
+                    }
+                }
+            };
+            block(std::integral_constant<int, 0>{});
+            block(std::integral_constant<int, 1>{});
+            block(std::integral_constant<int, 2>{});
+            block(std::integral_constant<int, 3>{});
+            block(std::integral_constant<int, 4>{});
+            block(std::integral_constant<int, 5>{});
+            block(std::integral_constant<int, 6>{});
+            block(std::integral_constant<int, 7>{});
+        };
+        const bool two = NT > 1 && ng > 8;                // the second slot group holds slots
+        for (int32_t ks = 0; ks < n_ks; ++ks, ++it) {
+            const int32_t s = static_cast<int32_t>(it % NS);
+            if (!mbar_wait_warp(&full[s], static_cast<uint32_t>((it / NS) & 1), a.err)) {
+                ok = false;
+                break;
+            }
+            const uint8_t* ra = ring + static_cast<size_t>(s) * stage_bytes + static_cast<size_t>(r * 16 + g) * PITCH;
+            if (two)
+                box_pass(ra, ks, std::integral_constant<int, NT>{});
+            else
+                box_pass(ra, ks, std::integral_constant<int, 1>{});
+            // release the box once its values are in registers and used (as in
+            // the row-per-lane kernel: the next TMA write must not overtake them)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        if (!ok || DUMP) continue;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int32_t sl = sid[nt][c & 1];
+                const int64_t row = row0 + g + (c < 2 ? 0 : 8);
+                if (sl >= 0 && row < a.nrows) a.out[static_cast<int64_t>(sl) * a.nrows + row] = acc[nt][c];
+            }
+    }
+}
+
+template <int NT, bool DUMP>
+static int launch_gemv_mma_nt(const GemvPlan& plan, const CUtensorMap& wmap, const GemvArgs& a, cudaStream_t s) {
+    const void* kernel = reinterpret_cast<const void*>(moe_gemv_mma_kernel<NT, DUMP>);
+    if (int st = set_smem_limit(kernel, static_cast<int>(plan.smem))) return st;
+    const int threads = 32 * (plan.row_warps + 1);
+    // one CTA per SM (or as many as fit); each takes an equal share of the work
+    const dim3 grid(static_cast<unsigned>(sm_count() * resident_ctas(kernel, threads, plan.smem)));
+    const dim3 block(threads);
+    moe_gemv_mma_kernel<NT, DUMP><<<grid, block, plan.smem, s>>>(wmap, a);
+    return check_launch(DUMP ? "moe_gemv_mma_kernel<dump>" : "moe_gemv_mma_kernel", grid, block, plan.smem);
+}
+
+int launch_gemv_mma(const GemvPlan& plan, const CUtensorMap& wmap, const GemvArgs& a, bool dump, cudaStream_t s) {
+    if (plan.mma == 2) return dump ? launch_gemv_mma_nt<2, true>(plan, wmap, a, s) : launch_gemv_mma_nt<2, false>(plan, wmap, a, s);
+    return dump ? launch_gemv_mma_nt<1, true>(plan, wmap, a, s) : launch_gemv_mma_nt<1, false>(plan, wmap, a, s);
+}
+
+}  // namespace ft

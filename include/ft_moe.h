@@ -86,6 +86,8 @@ typedef enum {
 #define FT_PATH_AUTO 0   /* chosen on the host from tokens*top_k, n_experts and the shape */
 #define FT_PATH_GEMV 1   /* per-slot GEMV on CUDA cores                                  */
 #define FT_PATH_GEMM 2   /* expert-grouped GEMM on the tcgen05 tensor cores              */
+#define FT_PATH_GEMV_DP4A 3 /* the GEMV path, every slot tile on the dp4a CUDA-core kernels
+                               (no mma.sync tiles; for comparison and tests)                */
 
 /* Weight block types of ft_moe_gguf_q8_1: the GGUF types whose blocks hold
  * 32 weights (GGML type numbers).  Weight i of a block = q_i * d + c:
@@ -494,9 +496,9 @@ FT_API int ft_debug_stream_read(const void* buf, int64_t bytes, void* stream);
 
 /*
  * ft_moe_set_path - force the path of later ft_moe_q4_0_q8_1 calls in this
- * process (FT_PATH_AUTO / FT_PATH_GEMV / FT_PATH_GEMM); returns the previous
- * setting, or -1 for an unknown value.  The environment variable FT_MOE_PATH
- * (auto|gemv|gemm) sets the initial value.
+ * process (FT_PATH_AUTO / FT_PATH_GEMV / FT_PATH_GEMM / FT_PATH_GEMV_DP4A);
+ * returns the previous setting, or -1 for an unknown value.  The environment
+ * variable FT_MOE_PATH (auto|gemv|gemm|gemv_dp4a) sets the initial value.
  */
 FT_API int ft_moe_set_path(int32_t path);
 

@@ -1,12 +1,14 @@
 """GPU parity of ft_moe_q4_0_fp16, the hot path from fp16 activations.
 
 A decode-sized batch (at most 512 slots and 1024 experts, ncols % 256 == 0,
-x 16-byte aligned) runs as ONE launch in which every CTA routes the slots and
-quantizes its rows itself; the result must equal ft_quantize_q8_1 followed by
-ft_moe_q4_0_q8_1 bit for bit (same GEMV plan, same arithmetic), and match the
-oracle within the matmul tolerance.  Outside those limits the entry point
-quantizes into workspace and takes the usual path: still bit-equal to the two
-calls.  Bad ids give zero rows and the device error flag on both forms.
+x 16-byte aligned, at most 4 slots per expert on average) runs as ONE launch
+in which every CTA routes the slots and quantizes its rows itself; the result
+must equal ft_quantize_q8_1 followed by ft_moe_q4_0_q8_1 bit for bit (same
+GEMV plan, same arithmetic), and match the oracle within the matmul
+tolerance.  Outside those limits (among them batches whose tiles run on the
+mma.sync kernel) the entry point quantizes into workspace and takes the usual
+path: still bit-equal to the two calls.  Bad ids give zero rows and the
+device error flag on both forms.
 """
 
 import numpy as np
@@ -50,16 +52,16 @@ def _two_calls(ft, w, x, ids):
 
 
 # (E, k, K, N, T, seed, routing): one token of the 8-expert layer (G = 1,
-# K-split), 32 tokens over 1024 columns (8-slot tiles), the 128-expert top-8 layer at 1, 8 and
-# 64 tokens (64 x 8 = 512 slots: the limit), a ragged small layer, 1024
-# experts (the limit)
+# K-split), 16 tokens over 1024 columns (4-slot tiles), the 128-expert top-8
+# layer at 1, 8 and 64 tokens (64 x 8 = 512 slots: the limit), a ragged small
+# layer, 1024 experts (the limit)
 ONE_LAUNCH = [
     (8, 2, 4096, 14336, 1, 4, "uniform"),
-    (8, 2, 1024, 14336, 32, 4, "uniform"),
+    (8, 2, 1024, 14336, 16, 4, "uniform"),
     (128, 8, 2048, 768, 1, 3, "zipf"),
     (128, 8, 2048, 768, 8, 3, "zipf"),
     (128, 8, 2048, 768, 64, 3, "zipf"),
-    (5, 2, 512, 200, 13, 40, "uniform"),
+    (5, 2, 512, 200, 10, 40, "uniform"),
     (1024, 4, 256, 64, 40, 41, "uniform"),
 ]
 
@@ -100,10 +102,10 @@ def test_bad_ids_zero_rows(ft, oracle, misaligned):
     """Both forms (one launch; x 8-byte aligned only: quantize + route +
     matmul): rows of bad slots are zero, the flag is raised, the rest match."""
     import torch
-    w, x, ids = _custom(8, 2, 1024, 300, 24, 42)
+    w, x, ids = _custom(16, 2, 1024, 300, 24, 42)
     ids = ids.copy()
     ids[0, 0] = -1
-    ids[7, 1] = 8
+    ids[7, 1] = 16
     ids[23, 1] = 1 << 20
     dw, di = G.dev(w), G.dev(ids)
     if misaligned:
@@ -134,7 +136,8 @@ def test_bad_ids_zero_rows(ft, oracle, misaligned):
     (128, 8, 2816, 1408, 2048, "auto"),      # prefill: quantize into workspace, tensor cores
     (8, 2, 256, 128, 300, "gemv"),           # 600 slots: past the one-launch limit
     (8, 2, 800, 100, 9, "auto"),             # ncols % 256 != 0: block-per-lane GEMV
-    (8, 2, 4096, 14336, 32, "auto"),         # 8-slot tiles of 4096 columns: too much to quantize per CTA
+    (8, 2, 4096, 14336, 32, "auto"),         # 8-slot tiles of 4096 columns: mma.sync tiles
+    (8, 2, 1024, 14336, 32, "auto"),         # 8-slot tiles of 1024 columns: mma.sync tiles
     (2000, 2, 256, 64, 4, "auto"),           # more experts than the one-launch limit
     (8, 2, 512, 256, 16, "gemm"),            # forced tensor cores
 ])

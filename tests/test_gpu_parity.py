@@ -203,7 +203,7 @@ RAGGED = [
 
 
 @pytest.mark.parametrize("E,k,K,N,T,seed", RAGGED)
-@pytest.mark.parametrize("path_name", ["gemv", "gemm"])
+@pytest.mark.parametrize("path_name", ["gemv", "gemv_dp4a", "gemm"])
 def test_ragged_full_compare(path, oracle, E, k, K, N, T, seed, path_name):
     w, x, ids = _custom(E, k, K, N, T, seed, zero_rows=True)
     act = oracle.quantize_q8_1(x)
@@ -217,7 +217,7 @@ def test_ragged_full_compare(path, oracle, E, k, K, N, T, seed, path_name):
 # last two the 128-wide tiles (many slots per expert)
 @pytest.mark.parametrize("E,k,K,N,T,seed", [(5, 2, 512, 200, 77, 11), (16, 4, 256, 64, 129, 13),
                                             (3, 3, 768, 130, 300, 12), (2, 1, 4096, 260, 400, 14)])
-@pytest.mark.parametrize("path_name", ["gemv", "gemm"])
+@pytest.mark.parametrize("path_name", ["gemv", "gemv_dp4a", "gemm"])
 def test_ragged_block_dots(path, oracle, E, k, K, N, T, seed, path_name):
     w, x, ids = _custom(E, k, K, N, T, seed, zero_rows=True)
     act = oracle.quantize_q8_1(x)
@@ -236,6 +236,70 @@ def test_gemv_odd_row_lengths(path, oracle, K):
     assert np.array_equal(_dots(path, w, act, ids, "auto"), oracle.moe_block_dots(w, act, ids))
 
 
+# 8-slot GEMV tiles on the mma.sync kernel ("gemv"; "gemv_dp4a" keeps them on
+# the dp4a row kernel): exact block dots, outputs within the tolerance of the
+# oracle; ragged row counts (not a multiple of 32 rows per warp), one and
+# several boxes per row, experts with a second, partial tile, a bad id.  Both
+# kernels form the same integer block dots and scale them in the same order,
+# so where the dp4a kernel does not split K (one box per row, K = 256, or
+# enough row groups: the full Mixtral-shaped layer) they agree bit for bit.
+MMA_CASES = [
+    # E, k, K, N, T, seed, bit-identical to the dp4a kernel: 5..8 slots per expert on average
+    (8, 2, 4096, 14336 // 8, 32, 70, False),
+    (8, 2, 256, 77, 20, 71, True),
+    (4, 4, 768, 300, 7, 72, False),
+    (16, 4, 2048, 520, 30, 73, False),
+    (3, 2, 512, 1000, 11, 74, False),
+    (6, 3, 256, 4000, 13, 75, True),
+]
+
+
+@pytest.mark.parametrize("E,k,K,N,T,seed,same", MMA_CASES)
+def test_gemv_mma_tiles(path, oracle, E, k, K, N, T, seed, same):
+    w, x, ids = _custom(E, k, K, N, T, seed, zero_rows=True)
+    ids = ids.copy()
+    ids[T // 2, 0] = E                                    # a bad id: zero row, flag
+    act = oracle.quantize_q8_1(x)
+    mean = T * k / E
+    assert 4.0 < mean <= 8.0
+    path.read_device_error()
+    a = _run(path, w, act, ids, "gemv")
+    assert path.read_device_error() & path.FT_DEVERR_BAD_EXPERT_ID
+    assert not a[T // 2, 0].any()
+    ref = oracle.moe(w, act, ids)
+    wn, xn = G.full_norms(oracle, w, act, ids)
+    G.check_close(a, ref, wn, xn, f"mma {E},{k},{K},{N},{T}")
+    assert np.array_equal(_dots(path, w, act, ids, "gemv"), oracle.moe_block_dots(w, act, ids))
+    b = _run(path, w, act, ids, "gemv_dp4a")
+    if same:
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    else:
+        G.check_close(a, b, wn, xn, f"mma vs dp4a {E},{k},{K},{N},{T}")
+
+
+@pytest.mark.parametrize("T", [24, 32])
+def test_gemv_mma_full_size_matches_dp4a(path, oracle, T):
+    """The Mixtral-shaped layer at 6 and 8 slots per expert: the mma.sync tiles
+    and the dp4a row kernel (unsplit K at this size) give the same bits, and
+    sampled outputs match the oracle."""
+    from bit_quantized_moe_quantize_gb300 import synth
+    wl = synth.WORKLOADS["mixtral_8x7b"]
+    w = G.weights_of("mixtral_8x7b")
+    x = synth.make_activations(wl, T)
+    ids = synth.make_topk_ids(wl, T)
+    act = oracle.quantize_q8_1(x)
+    a = _run(path, w, act, ids, "gemv")
+    b = _run(path, w, act, ids, "gemv_dp4a")
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    S, N = T * wl.top_k, wl.nrows
+    rng = np.random.default_rng(2000 + T)
+    slots, rows = rng.integers(0, S, 2000), rng.integers(0, N, 2000)
+    ref = oracle.moe_sample(w, act, ids, slots, rows)
+    wn = G.row_norms_w(oracle, w, ids.reshape(-1)[slots], rows)
+    xn = G.act_norms(oracle, act)[slots // wl.top_k]
+    G.check_close(a.reshape(S, N)[slots, rows], ref, wn, xn, f"mixtral T={T}")
+
+
 def test_gemm_rejects_unaligned_k(path):
     from bit_quantized_moe_quantize_gb300 import FtError
     w, x, ids = _custom(4, 2, 288, 40, 9, 31)
@@ -252,7 +316,7 @@ def test_bad_ids_zero_rows_and_flag(path, oracle):
     ids[4, 1] = 4
     act = oracle.quantize_q8_1(x)
     ref = oracle.moe(w, act, ids)
-    for p in ("gemv", "gemm"):
+    for p in ("gemv", "gemv_dp4a", "gemm"):
         path.read_device_error()
         out = G.dev(np.full((6, 2, 128), np.nan, np.float32))
         path.set_path(p)

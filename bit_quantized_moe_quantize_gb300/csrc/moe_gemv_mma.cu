@@ -42,19 +42,22 @@
 // and one fp16 op per pair: half the shared memory of staged fp16 pairs,
 // which leaves room for 16 row warps and a 3-box ring.
 //
-// Work split.  The grid is one CTA per SM.  A work item is (slot tile, block
-// of 16 RW rows), numbered tile-major; there are tiles x row blocks of them
+// Work split.  The grid is one CTA per SM.  A work unit is (slot tile, group
+// of 16 rows), numbered tile-major; there are tiles x ceil(rows / 16) of them
 // (the tile count is read on the device).  Each CTA takes one contiguous
-// range, cut by weight: an item whose tile uses its second slot group counts
-// 5, any other 3 (about their measured costs), so the SMs finish together
-// whatever the routing, and a CTA restages the activations only where its
-// range enters a new tile (items handed out one by one from a global counter
-// balance better but restage at nearly every item, which measured slower).
-// Weights stream as in the row-per-lane kernel: TMA boxes of 256 weights
-// (8 blocks, 144 bytes per row) x 16 RW rows through an mbarrier ring filled
-// by one producer warp, which runs ahead of the staging.  Warp r owns rows
-// 16 r .. 16 r + 15 of each box (one m16 tile), so a CTA keeps up to 16 row
-// warps busy on one staged activation tile.
+// range, cut by weight: a unit whose tile uses its second slot group counts
+// 3, any other 2 (about their costs), so the SMs finish together whatever
+// the routing; where the tiles are few, each tile gets its share of the CTAs
+// so that no CTA stages two tiles.  The CTA walks its range in row blocks of RW groups
+// (one TMA box high), cut short at the end of a tile and of the range (the
+// warps without a group there skip that block), and restages the activations
+// only where the range enters a new tile (units handed out one by one from a
+// global counter balance as well but restage at nearly every block, which
+// measured slower).  Weights stream as in the row-per-lane kernel: TMA boxes
+// of 256 weights (8 blocks, 144 bytes per row) x 16 RW rows through an
+// mbarrier ring filled by one producer warp, which runs ahead of the staging.
+// Warp r owns rows 16 r .. 16 r + 15 of each box (one m16 tile), so a CTA
+// keeps up to 16 row warps busy on one staged activation tile.
 #include <cuda_fp16.h>
 
 #include "gemv_rows.cuh"
@@ -177,46 +180,56 @@ __device__ __forceinline__ void mma_stage_tile(const GemvArgs& a, int64_t tile, 
     }
 }
 
-// Item weights of the work split: an item of a tile whose second slot group
-// holds slots costs about 1.7 times one whose tile has 8 slots or fewer
-// (measured: 53 against 31 us per CTA item on the Mixtral-shaped layer).
-constexpr int64_t kMmaW1 = 3, kMmaW2 = 5;
+// Unit weights of the work split: a row group of a tile whose second slot
+// group holds slots counts 3, one of a tile with 8 slots or fewer 2 (their
+// costs, roughly: the second group's MMAs and scaling are most of a unit).
+constexpr int64_t kMmaW1 = 2, kMmaW2 = 3;
 
-// The CTA's contiguous range [w0, w1) of the work items (tile-major
-// (tile, row block)), cut so that every CTA gets the same item weight: CTA c
-// takes the items whose weight interval starts in [c W / grid, (c + 1) W /
-// grid), W the total.  One warp scans the experts' slot counts (tiles of
-// expert e: ceil(count / G), all full but the last) twice: once for W, once to
-// place the two bounds.  Written to range[0..1].
+// The CTA's contiguous range [w0, w1) of the work units (tile-major (tile,
+// 16-row group), n_u units per tile), written to range[0..1].  A unit weighs
+// W1 or W2 by its tile's slot groups, W in all.  Where every tile's share of
+// the grid, grid * (tile weight) / W, is at least one CTA, each tile gets
+// that share rounded (cumulatively, so the counts add up to the grid) and
+// its units are cut evenly among them: no CTA stages two tiles.  Otherwise
+// (many small tiles) CTA c takes the units whose weight interval starts in
+// [c W / grid, (c + 1) W / grid).  One warp scans the experts' slot counts
+// (tiles of expert e: ceil(count / G), all full but the last).
 template <int NT>
-__device__ void mma_work_range(const GemvArgs& a, int64_t n_rb, int64_t* range) {
+__device__ void mma_work_range(const GemvArgs& a, int64_t n_u, int64_t* range) {
     constexpr int G = 8 * NT;
     constexpr int64_t W1 = NT > 1 ? kMmaW1 : 1, W2 = NT > 1 ? kMmaW2 : 1;
     const int32_t E = a.n_experts;
     const uint32_t lane = lane_id();
+    const int64_t grid = gridDim.x, c = blockIdx.x;
     auto expert = [&](int32_t e, int64_t& tl, int64_t& wt, int64_t& ulast) {
-        const int64_t c = e < E ? static_cast<int64_t>(a.offsets[e + 1] - a.offsets[e]) : 0;
-        tl = (c + G - 1) / G;
-        ulast = c - G * (tl - 1) > 8 ? W2 : W1;
+        const int64_t n = e < E ? static_cast<int64_t>(a.offsets[e + 1] - a.offsets[e]) : 0;
+        tl = (n + G - 1) / G;
+        ulast = n - G * (tl - 1) > 8 ? W2 : W1;
         wt = tl > 0 ? (tl - 1) * W2 + ulast : 0;
     };
     int64_t tot = 0;
+    bool light = false;                            // some tile weighs W1 per unit
     for (int32_t e0 = 0; e0 < E; e0 += 32) {
         int64_t tl, wt, ul;
         expert(e0 + static_cast<int32_t>(lane), tl, wt, ul);
         tot += wt;
+        light |= tl > 0 && ul == W1;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
-    const int64_t W = tot * n_rb;
-    const int64_t P[2] = {W * blockIdx.x / gridDim.x, W * (blockIdx.x + 1) / gridDim.x};
-    int64_t wbase = 0, ibase = 0;                  // weight and items before the chunk
-    if (lane < 2) range[lane] = static_cast<int64_t>(a.tiles[E]) * n_rb;   // P == W: past the last item
+    light = __any_sync(0xFFFFFFFFu, light);
+    const int64_t W = tot * n_u;
+    const bool per_tile = W > 0 && grid * n_u * (light ? W1 : W2) >= W;
+    // CTAs before weight x, per tile mode: round(grid x / W)
+    auto ctas_before = [&](int64_t x) { return (2 * grid * x + W) / (2 * W); };
+    const int64_t P[2] = {W * c / grid, W * (c + 1) / grid};
+    int64_t wbase = 0, ibase = 0;                  // weight and units before the chunk
+    if (lane < 2) range[lane] = static_cast<int64_t>(a.tiles[E]) * n_u;   // past the last unit
     __syncwarp();
     for (int32_t e0 = 0; e0 < E; e0 += 32) {
         int64_t tl, wt, ul;
         expert(e0 + static_cast<int32_t>(lane), tl, wt, ul);
-        int64_t wi = wt * n_rb, ii = tl * n_rb;    // inclusive prefix over the chunk
+        int64_t wi = wt * n_u, ii = tl * n_u;    // inclusive prefix over the chunk
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int64_t y = __shfl_up_sync(0xFFFFFFFFu, wi, o), z = __shfl_up_sync(0xFFFFFFFFu, ii, o);
@@ -225,19 +238,33 @@ __device__ void mma_work_range(const GemvArgs& a, int64_t n_rb, int64_t* range) 
                 ii += z;
             }
         }
-        const int64_t ws = wbase + wi - wt * n_rb, is = ibase + ii - tl * n_rb;   // this expert's start
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            if (wt > 0 && P[k] >= ws && P[k] < ws + wt * n_rb) {
-                const int64_t q = P[k] - ws, full = (tl - 1) * W2 * n_rb;
-                int64_t item;
-                if (q < full) {
-                    const int64_t t = q / (W2 * n_rb), q2 = q - t * W2 * n_rb;
-                    item = is + t * n_rb + (q2 + W2 - 1) / W2;
-                } else {
-                    item = is + (tl - 1) * n_rb + (q - full + ul - 1) / ul;
+        const int64_t ws = wbase + wi - wt * n_u, is = ibase + ii - tl * n_u;   // this expert's start
+        if (per_tile) {
+            if (wt > 0 && c >= ctas_before(ws) && c < ctas_before(ws + wt * n_u)) {
+                for (int64_t j = 0; j < tl; ++j) {
+                    const int64_t c0 = ctas_before(ws + j * W2 * n_u);
+                    const int64_t c1 = j + 1 < tl ? ctas_before(ws + (j + 1) * W2 * n_u) : ctas_before(ws + wt * n_u);
+                    if (c >= c0 && c < c1) {
+                        const int64_t k = c1 - c0, cc = c - c0;
+                        range[0] = is + j * n_u + n_u * cc / k;
+                        range[1] = is + j * n_u + n_u * (cc + 1) / k;
+                    }
                 }
-                range[k] = item;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if (wt > 0 && P[k] >= ws && P[k] < ws + wt * n_u) {
+                    const int64_t q = P[k] - ws, full = (tl - 1) * W2 * n_u;
+                    int64_t unit;
+                    if (q < full) {
+                        const int64_t t = q / (W2 * n_u), q2 = q - t * W2 * n_u;
+                        unit = is + t * n_u + (q2 + W2 - 1) / W2;
+                    } else {
+                        unit = is + (tl - 1) * n_u + (q - full + ul - 1) / ul;
+                    }
+                    range[k] = unit;
+                }
             }
         }
         wbase += __shfl_sync(0xFFFFFFFFu, wi, 31);
@@ -254,7 +281,7 @@ __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_const
     const int32_t nb = a.nb;
     const int32_t n_ks = nb / 8;                          // boxes per row
     const int NS = a.stages;
-    const int64_t n_rb = (a.nrows + 16 * RW - 1) / (16 * RW);
+    const int64_t n_g = (a.nrows + 15) / 16;              // 16-row groups of a tile
 
     extern __shared__ __align__(128) uint8_t smem_mma[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem_mma);
@@ -273,34 +300,34 @@ __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_const
         }
         fence_mbar_init();
     }
-    if (warp == 0) mma_work_range<NT>(a, n_rb, range);
+    if (warp == 0) mma_work_range<NT>(a, n_g, range);
     __syncthreads();
     const int64_t w0 = range[0], w1 = range[1];
     if (w0 >= w1) return;
 
     if (static_cast<int32_t>(warp) == RW) {
         // ------------------------------------------------------------ producer
-        int64_t w = w0, tile = -1, erow0 = 0;
-        int32_t ks = 0;
-        const int64_t n_it = (w1 - w0) * n_ks;
-        for (int64_t it = 0; it < n_it; ++it) {
-            const int64_t tl = w / n_rb;
+        // the boxes of each row block in K order; a row block is the next RW
+        // groups of the range, cut at the end of its tile and of the range
+        int64_t it = 0, tile = -1, erow0 = 0;
+        for (int64_t u = w0; u < w1;) {
+            const int64_t tl = u / n_g, g0 = u - tl * n_g;
+            const int64_t cnt = min(static_cast<int64_t>(RW), min(n_g - g0, w1 - u));
             if (tl != tile) {
                 tile = tl;
                 erow0 = static_cast<int64_t>(find_expert(a.tiles, E, tl)) * a.nrows;
             }
-            const int32_t s = static_cast<int32_t>(it % NS);
-            if (!mbar_wait_warp(&empty[s], static_cast<uint32_t>(((it / NS) & 1) ^ 1), a.err)) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&full[s], stage_bytes);
-                tma_load_2d(ring + static_cast<size_t>(s) * stage_bytes, &wmap, ks * (PITCH / 2),
-                            static_cast<int32_t>(erow0 + (w - tl * n_rb) * 16 * RW), &full[s]);
+            for (int32_t ks = 0; ks < n_ks; ++ks, ++it) {
+                const int32_t s = static_cast<int32_t>(it % NS);
+                if (!mbar_wait_warp(&empty[s], static_cast<uint32_t>(((it / NS) & 1) ^ 1), a.err)) return;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[s], stage_bytes);
+                    tma_load_2d(ring + static_cast<size_t>(s) * stage_bytes, &wmap, ks * (PITCH / 2),
+                                static_cast<int32_t>(erow0 + g0 * 16), &full[s]);
+                }
+                __syncwarp();
             }
-            __syncwarp();
-            if (++ks == n_ks) {
-                ks = 0;
-                ++w;
-            }
+            u += cnt;
         }
         return;
     }
@@ -314,8 +341,10 @@ __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_const
     int64_t cur = -1, it = 0;
     int32_t ng = 0, sid[NT][2];
     bool ok = true;
-    for (int64_t w = w0; w < w1; ++w) {
-        const int64_t tile = w / n_rb, rb = w - tile * n_rb;
+    for (int64_t u = w0; u < w1;) {
+        const int64_t tile = u / n_g, g0 = u - tile * n_g;
+        const int64_t cnt = min(static_cast<int64_t>(RW), min(n_g - g0, w1 - u));
+        u += cnt;
         if (tile != cur) {
             if (cur >= 0) named_bar_sync(1, n_threads);  // every warp is done with the previous tile
             mma_stage_tile<NT>(a, tile, qb, xc, xd, static_cast<int32_t>(n_threads), ng, sid);
@@ -323,7 +352,8 @@ __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_const
             cur = tile;
         }
         if (!ok) continue;
-        const int64_t row0 = rb * 16 * RW + r * 16;        // first row of the warp within the expert
+        const bool mine = r < cnt;                         // the block has a group for this warp
+        const int64_t row0 = (g0 + r) * 16;                // first row of the warp within the expert
         float acc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -391,16 +421,18 @@ __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_const
                 break;
             }
             const uint8_t* ra = ring + static_cast<size_t>(s) * stage_bytes + static_cast<size_t>(r * 16 + g) * PITCH;
-            if (two)
-                box_pass(ra, ks, std::integral_constant<int, NT>{});
-            else
-                box_pass(ra, ks, std::integral_constant<int, 1>{});
+            if (mine) {
+                if (two)
+                    box_pass(ra, ks, std::integral_constant<int, NT>{});
+                else
+                    box_pass(ra, ks, std::integral_constant<int, 1>{});
+            }
             // release the box once its values are in registers and used (as in
             // the row-per-lane kernel: the next TMA write must not overtake them)
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
-        if (!ok || DUMP) continue;
+        if (!ok || DUMP || !mine) continue;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll

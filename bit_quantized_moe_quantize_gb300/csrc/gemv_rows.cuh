@@ -557,9 +557,11 @@ int launch_gemv_rows_gguf(int wtype, const GemvPlan& plan, const CUtensorMap& wm
                           cudaStream_t s);
 
 // Q4_0 tiles of nt groups of 8 slots on mma.sync (moe_gemv_mma.cu): shared
-// memory of a CTA of row_warps row warps with a ring of `stages` boxes (row
-// blocks of 32 * row_warps rows, wmap's box), and the launch (dump: block dots).
+// memory of a CTA of row_warps warps of 16 rows with a ring of `stages` boxes,
+// and the launch (dump: block dots); wmap's box is 16 * row_warps rows high,
+// wmap16's 16 rows (for the short row blocks at the ends of a CTA's range).
 size_t gemv_mma_smem(int nb, int nt, int row_warps, int stages);
-int launch_gemv_mma(const GemvPlan& plan, const CUtensorMap& wmap, const GemvArgs& a, bool dump, cudaStream_t s);
+int launch_gemv_mma(const GemvPlan& plan, const CUtensorMap& wmap, const CUtensorMap& wmap16, const GemvArgs& a,
+                    bool dump, cudaStream_t s);
 
 }  // namespace ft

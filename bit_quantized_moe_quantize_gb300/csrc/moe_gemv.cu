@@ -277,7 +277,14 @@ int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act
                                (plan.mma ? 16 : 32) * plan.row_warps, CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
             return st;
         if (wtype != FT_TYPE_Q4_0) return launch_gemv_rows_gguf(wtype, plan, wmap, a, s);
-        if (plan.mma) return launch_gemv_mma(plan, wmap, a, dump, s);
+        if (plan.mma) {
+            CUtensorMap wmap16;
+            if (int st = encode_2d(&wmap16, CU_TENSOR_MAP_DATA_TYPE_UINT16, weights, row_bytes / 2,
+                                   static_cast<uint64_t>(n_experts) * nrows, row_bytes, pitch / 2, 16,
+                                   CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
+                return st;
+            return launch_gemv_mma(plan, wmap, wmap16, a, dump, s);
+        }
         switch (plan.group) {
             case 1: return dump ? launch_gemv_rows<FT_TYPE_Q4_0, 1, true>(plan, wmap, a, s) : launch_gemv_rows<FT_TYPE_Q4_0, 1, false>(plan, wmap, a, s);
             case 2: return dump ? launch_gemv_rows<FT_TYPE_Q4_0, 2, true>(plan, wmap, a, s) : launch_gemv_rows<FT_TYPE_Q4_0, 2, false>(plan, wmap, a, s);

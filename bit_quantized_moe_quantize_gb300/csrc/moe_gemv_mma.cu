@@ -274,6 +274,7 @@ __device__ void mma_work_range(const GemvArgs& a, int64_t n_u, int64_t* range) {
 
 template <int NT, bool DUMP>
 __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                              const __grid_constant__ CUtensorMap wmap16,
                                                               const GemvArgs a) {
     constexpr int PITCH = RowBox<FT_TYPE_Q4_0>::PITCH;   // 144: 8 blocks of 18 bytes
     const int32_t RW = a.row_warps;                       // warps of 16 rows
@@ -321,9 +322,18 @@ __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_const
                 const int32_t s = static_cast<int32_t>(it % NS);
                 if (!mbar_wait_warp(&empty[s], static_cast<uint32_t>(((it / NS) & 1) ^ 1), a.err)) return;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[s], stage_bytes);
-                    tma_load_2d(ring + static_cast<size_t>(s) * stage_bytes, &wmap, ks * (PITCH / 2),
-                                static_cast<int32_t>(erow0 + g0 * 16), &full[s]);
+                    uint8_t* dst = ring + static_cast<size_t>(s) * stage_bytes;
+                    if (cnt == RW) {
+                        mbar_arrive_expect_tx(&full[s], stage_bytes);
+                        tma_load_2d(dst, &wmap, ks * (PITCH / 2), static_cast<int32_t>(erow0 + g0 * 16), &full[s]);
+                    } else {
+                        // a short block: only its groups, 16 rows per copy,
+                        // so that no row outside the range leaves memory
+                        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(cnt) * 16 * PITCH);
+                        for (int64_t i = 0; i < cnt; ++i)
+                            tma_load_2d(dst + i * 16 * PITCH, &wmap16, ks * (PITCH / 2),
+                                        static_cast<int32_t>(erow0 + (g0 + i) * 16), &full[s]);
+                    }
                 }
                 __syncwarp();
             }
@@ -445,20 +455,25 @@ __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_const
 }
 
 template <int NT, bool DUMP>
-static int launch_gemv_mma_nt(const GemvPlan& plan, const CUtensorMap& wmap, const GemvArgs& a, cudaStream_t s) {
+static int launch_gemv_mma_nt(const GemvPlan& plan, const CUtensorMap& wmap, const CUtensorMap& wmap16, const GemvArgs& a,
+                              cudaStream_t s) {
     const void* kernel = reinterpret_cast<const void*>(moe_gemv_mma_kernel<NT, DUMP>);
     if (int st = set_smem_limit(kernel, static_cast<int>(plan.smem))) return st;
     const int threads = 32 * (plan.row_warps + 1);
     // one CTA per SM (or as many as fit); each takes an equal share of the work
     const dim3 grid(static_cast<unsigned>(sm_count() * resident_ctas(kernel, threads, plan.smem)));
     const dim3 block(threads);
-    moe_gemv_mma_kernel<NT, DUMP><<<grid, block, plan.smem, s>>>(wmap, a);
+    moe_gemv_mma_kernel<NT, DUMP><<<grid, block, plan.smem, s>>>(wmap, wmap16, a);
     return check_launch(DUMP ? "moe_gemv_mma_kernel<dump>" : "moe_gemv_mma_kernel", grid, block, plan.smem);
 }
 
-int launch_gemv_mma(const GemvPlan& plan, const CUtensorMap& wmap, const GemvArgs& a, bool dump, cudaStream_t s) {
-    if (plan.mma == 2) return dump ? launch_gemv_mma_nt<2, true>(plan, wmap, a, s) : launch_gemv_mma_nt<2, false>(plan, wmap, a, s);
-    return dump ? launch_gemv_mma_nt<1, true>(plan, wmap, a, s) : launch_gemv_mma_nt<1, false>(plan, wmap, a, s);
+int launch_gemv_mma(const GemvPlan& plan, const CUtensorMap& wmap, const CUtensorMap& wmap16, const GemvArgs& a,
+                    bool dump, cudaStream_t s) {
+    if (plan.mma == 2)
+        return dump ? launch_gemv_mma_nt<2, true>(plan, wmap, wmap16, a, s)
+                    : launch_gemv_mma_nt<2, false>(plan, wmap, wmap16, a, s);
+    return dump ? launch_gemv_mma_nt<1, true>(plan, wmap, wmap16, a, s)
+                : launch_gemv_mma_nt<1, false>(plan, wmap, wmap16, a, s);
 }
 
 }  // namespace ft

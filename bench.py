@@ -55,6 +55,10 @@ GEMM_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemm_tc.cu", "bit_qua
                 "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh")
 GEMM_CONSTANTS = ("bit_quantized_moe_quantize_gb300/csrc/ft_internal.h", "kGemm")
 NCU_TRAFFIC = {("moe_gemm_tc_kernel", "f14bdd613c5afc3d", "prefill:8191"): 666726144 + 340649472}
+# the same for the mma.sync GEMV kernel (profiles/moe_gemv_mma_decode.md)
+MMA_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemv_mma.cu", "bit_quantized_moe_quantize_gb300/csrc/gemv_rows.cuh",
+               "bit_quantized_moe_quantize_gb300/csrc/gemv_blocks.cuh", "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh")
+NCU_TRAFFIC_GEMV = {("moe_gemv_mma_kernel", "31efe919d87afb75", "mixtral_8x7b:32"): 264452864 + 4817408}
 
 
 def kernel_source_hash(files, constants=GEMM_CONSTANTS) -> str:
@@ -548,7 +552,12 @@ def ours(args):
                 "algorithmic": f"unique expert weights + {'fp16 x' if fused else 'Q8_1 act'} + fp32 out = "
                                f"{alg_bytes} B per launch",
                 "kernel_ms": mm_ms}
-    tr = NCU_TRAFFIC.get((kern, kernel_source_hash(GEMM_SOURCES), args.workload)) if path == "gemm" else None
+    if path == "gemm":
+        tr = NCU_TRAFFIC.get((kern, kernel_source_hash(GEMM_SOURCES), args.workload))
+    elif kern == "moe_gemv_mma_kernel":
+        tr = NCU_TRAFFIC_GEMV.get((kern, kernel_source_hash(MMA_SOURCES, None), args.workload))
+    else:
+        tr = None
     roof["traffic"] = tr
     if path == "gemv":
         # the same number of bytes streamed by a plain read kernel (L2 flushed

@@ -343,20 +343,31 @@ static bool gemm_shape_ok(const Shape& sh) {
 // pays off once experts see enough slots to fill a 128-column MMA tile.
 static bool gemm_type_ok(int wtype) { return wtype == FT_TYPE_Q4_0 || wtype == FT_TYPE_Q4_K; }
 
+// Routed slots per expert on average from which the tensor-core path is
+// chosen: 40 where the GEMV would run 16-slot mma.sync tiles (Q4_0 whose
+// activation tile fits; measured: those beat the GEMM up to 32 slots per
+// expert on the three workload shapes by 1.1-1.5x and lose from 48), else 16
+// (the dp4a tiles).
+static double gemm_min_mean(const Shape& sh, int setting) {
+    if (sh.wtype != FT_TYPE_Q4_0 || setting == FT_PATH_GEMV_DP4A) return 16.0;
+    const double m = sh.mean() > 16.0 ? sh.mean() : 16.0;
+    return plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols, m, sh.wtype, true).mma ? 40.0 : 16.0;
+}
+
 static int choose_path(const Shape& sh, int setting) {
     if (setting == FT_PATH_GEMV || setting == FT_PATH_GEMV_DP4A) return FT_PATH_GEMV;
     if (!gemm_type_ok(sh.wtype)) return setting == FT_PATH_GEMM ? FT_PATH_GEMM : FT_PATH_GEMV;
     if (setting == FT_PATH_GEMM) return FT_PATH_GEMM;
     if (!gemm_shape_ok(sh)) return FT_PATH_GEMV;
-    return sh.mean() >= 16.0 ? FT_PATH_GEMM : FT_PATH_GEMV;
+    return sh.mean() >= gemm_min_mean(sh, setting) ? FT_PATH_GEMM : FT_PATH_GEMV;
 }
 
 // Slots above which the GEMV path is never chosen by itself (the tensor-core
-// path takes over at 16 routed slots per expert on average).
+// path takes over at gemm_min_mean routed slots per expert on average).
 static int64_t gemv_max_slots(const Shape& sh) {
     const int setting = path_setting();
     if (setting == FT_PATH_GEMV || setting == FT_PATH_GEMV_DP4A || !gemm_shape_ok(sh) || sh.wtype != FT_TYPE_Q4_0) return sh.n_slots;
-    const int64_t lim = 16 * static_cast<int64_t>(sh.n_global);
+    const int64_t lim = static_cast<int64_t>(gemm_min_mean(sh, setting)) * sh.n_global;
     return sh.n_slots < lim ? sh.n_slots : lim;
 }
 

@@ -212,7 +212,9 @@ FT_API int ft_moe_route_offsets_noalloc(const int32_t* topk_ids, int64_t tokens,
 /*
  * ft_moe_q4_0_q8_1 - the routed expert matmul defined at the top of this file.
  * Routes internally (into the workspace), then runs the GEMV or the grouped
- * GEMM path (FT_PATH_AUTO decides on the host, without reading the device).
+ * GEMM path (FT_PATH_AUTO decides on the host, without reading the device:
+ * the GEMM from 40 routed slots per expert on average where the GEMV runs
+ * its 16-slot mma.sync tiles, else from 16).
  *
  *   weights   device, Q4_0 [n_experts][nrows][ncols/32]; 16-byte aligned
  *   act       device, Q8_1 [tokens][ncols/32] (from ft_quantize_q8_1); 16-byte aligned

@@ -61,6 +61,17 @@ MMA_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemv_mma.cu", "bit_qua
 NCU_TRAFFIC_GEMV = {("moe_gemv_mma_kernel", "31efe919d87afb75", "mixtral_8x7b:32"): 264452864 + 4817408}
 
 
+def mma_tiles(S, E, K) -> bool:
+    """The library's rule for the mma.sync GEMV tiles of a Q4_0 batch (rows of
+    whole 256-weight runs): more than 4 slots per expert on average, and the
+    staged activations of an 8-slot tile (352 B per block) plus a ring of two
+    16-row boxes within 227 KB of shared memory."""
+    nb = K // 32
+    head = 8 * 2 * 16 + 16
+    ring0 = (head + nb * 352 + 127) // 128 * 128
+    return S / E > 4.0 and ring0 + 2 * 144 * 16 <= 227 * 1024
+
+
 def kernel_source_hash(files, constants=GEMM_CONSTANTS) -> str:
     import hashlib
     h = hashlib.sha256()
@@ -541,10 +552,7 @@ def ours(args):
         # 256-weight runs (all types but Q6_K, Q2_K, Q3_K), else one block per lane
         rows_ok = K % 256 == 0 and wtype not in ("q6_k", "q2_k", "q3_k")
         kern = ("moe_gemv_rows_kernel<fused>" if fused else "moe_gemv_rows_kernel") if rows_ok else "moe_gemv_kernel"
-        # 8-slot Q4_0 tiles (more than 4 slots per expert on average) run on the
-        # mma.sync kernel when its fp16 activation tile and two boxes fit
-        if (rows_ok and not fused and wtype == "q4_0" and S / E > 4.0 and path_setting != "gemv_dp4a"
-                and nb * 576 + 2 * 144 * 32 <= 227 * 1024):
+        if rows_ok and not fused and wtype == "q4_0" and path_setting != "gemv_dp4a" and mma_tiles(S, E, K):
             kern = "moe_gemv_mma_kernel"
         achieved = alg_bytes / (mm_ms / 1000.0) / 1e9
         roof = {"kernel": kern, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -720,7 +728,8 @@ def ffn(args):
     else:
         l1_bytes = E * 2 * I * (H // 32) * 18 + T * (H // 32) * 36 + S * (I // 32) * 36
         achieved = l1_bytes / (st_ms["layer1_act_fused"] / 1000.0) / 1e9
-        roof = {"kernel": "moe_gemv_rows_kernel + act_mul_quantize_q8_1_kernel", "bound": "hbm",
+        gemv_k = "moe_gemv_mma_kernel" if H % 256 == 0 and mma_tiles(S, E, H) else "moe_gemv_rows_kernel"
+        roof = {"kernel": f"{gemv_k} + act_mul_quantize_q8_1_kernel", "bound": "hbm",
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
                 "algorithmic": f"all expert weights + act + act_mid = {l1_bytes} B per call",

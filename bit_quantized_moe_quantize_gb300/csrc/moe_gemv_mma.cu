@@ -66,10 +66,9 @@ namespace ft {
 
 // Shared memory: mbarriers full/empty [kMaxRowStages] | work range int64[2] |
 // qb [nb][NT][32 lanes] uint2 (codes + 128 at P_t: first / last 16) | xc
-// [nb][NT][4] float4 (the
-// accumulator's start for lane t: minus the offset sums of slots 2t, 2t+1,
-// twice, as the MMA's C quad) | xd [nb][NT][4] float2 (d_a of slots 2t, 2t+1)
-// | ring (128-byte aligned)
+// [nb][NT][4] float4 (the accumulator's start for lane t: minus the offset
+// sums of slots 2t, 2t+1, twice, as the MMA's C quad) | xd [nb][NT][4] float2
+// (d_a of slots 2t, 2t+1) | ring (128-byte aligned)
 __host__ __device__ inline size_t gemv_mma_qb_offset() { return 8 * 2 * kMaxRowStages + 16; }
 __host__ __device__ inline size_t gemv_mma_ring_offset(int nb, int nt) {
     return (gemv_mma_qb_offset() + static_cast<size_t>(nb) * nt * (256 + 64 + 32) + 127) / 128 * 128;

@@ -58,17 +58,19 @@ NCU_TRAFFIC = {("moe_gemm_tc_kernel", "205cc48df0b79f32", "prefill:8191"): 66658
 # the same for the mma.sync GEMV kernel (profiles/moe_gemv_mma_decode.md)
 MMA_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemv_mma.cu", "bit_quantized_moe_quantize_gb300/csrc/gemv_rows.cuh",
                "bit_quantized_moe_quantize_gb300/csrc/gemv_blocks.cuh", "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh")
-NCU_TRAFFIC_GEMV = {("moe_gemv_mma_kernel", "31efe919d87afb75", "mixtral_8x7b:32"): 264452864 + 4817408}
+NCU_TRAFFIC_GEMV = {("moe_gemv_mma_kernel", "31efe919d87afb75", "mixtral_8x7b:32", "q4_0"): 264452864 + 4817408}
 
 
-def mma_tiles(S, E, K) -> bool:
-    """The library's rule for the mma.sync GEMV tiles of a Q4_0 batch (rows of
-    whole 256-weight runs): more than 4 slots per expert on average, and the
-    staged activations of an 8-slot tile (352 B per block) plus a ring of two
-    16-row boxes within 227 KB of shared memory."""
+def mma_tiles(S, E, K, wtype="q4_0") -> bool:
+    """The library's rule for the mma.sync GEMV tiles of a Q4_0 or Q4_K batch
+    (rows of whole 256-weight runs): more than 4 slots per expert on average,
+    and the staged activations of an 8-slot tile (352 B per block, 384 for
+    Q4_K) plus a ring of two 16-row boxes within 227 KB of shared memory."""
+    if wtype not in ("q4_0", "q4_k"):
+        return False
     nb = K // 32
     head = 8 * 2 * 16 + 16
-    ring0 = (head + nb * 352 + 127) // 128 * 128
+    ring0 = (head + nb * (384 if wtype == "q4_k" else 352) + 127) // 128 * 128
     return S / E > 4.0 and ring0 + 2 * 144 * 16 <= 227 * 1024
 
 
@@ -347,10 +349,10 @@ def ours(args):
         from bit_quantized_moe_quantize_gb300 import synth
         x = synth.make_activations(replica_workload(wl, rank), S)
     rows = S if args.per_slot else T
-    # the tensor-core path takes Q4_0 and Q4_K weights (the same shape rule)
+    # the path the library takes for this shape and weight type
     path_setting = args.path
     ft.set_path(path_setting)
-    path = {1: "gemv", 2: "gemm"}[ft.selected_path(T, k, E, N, K)] if wtype in ("q4_0", "q4_k") else "gemv"
+    path = {1: "gemv", 2: "gemm"}[ft.selected_path(T, k, E, N, K, wtype)]
 
     dw = torch.from_numpy(w).to(dev)
     dx = torch.from_numpy(x).to(dev)
@@ -552,7 +554,7 @@ def ours(args):
         # 256-weight runs (all types but Q6_K, Q2_K, Q3_K), else one block per lane
         rows_ok = K % 256 == 0 and wtype not in ("q6_k", "q2_k", "q3_k")
         kern = ("moe_gemv_rows_kernel<fused>" if fused else "moe_gemv_rows_kernel") if rows_ok else "moe_gemv_kernel"
-        if rows_ok and not fused and wtype == "q4_0" and path_setting != "gemv_dp4a" and mma_tiles(S, E, K):
+        if rows_ok and not fused and path_setting != "gemv_dp4a" and mma_tiles(S, E, K, wtype):
             kern = "moe_gemv_mma_kernel"
         achieved = alg_bytes / (mm_ms / 1000.0) / 1e9
         roof = {"kernel": kern, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -563,7 +565,7 @@ def ours(args):
     if path == "gemm":
         tr = NCU_TRAFFIC.get((kern, kernel_source_hash(GEMM_SOURCES), args.workload))
     elif kern == "moe_gemv_mma_kernel":
-        tr = NCU_TRAFFIC_GEMV.get((kern, kernel_source_hash(MMA_SOURCES, None), args.workload))
+        tr = NCU_TRAFFIC_GEMV.get((kern, kernel_source_hash(MMA_SOURCES, None), args.workload, wtype))
     else:
         tr = None
     roof["traffic"] = tr

@@ -27,7 +27,7 @@ PATHS = {"auto": FT_PATH_AUTO, "gemv": FT_PATH_GEMV, "gemm": FT_PATH_GEMM, "gemv
 
 EXPORTS = ("ft_quantize_q8_1", "ft_moe_route_offsets", "ft_moe_q4_0_q8_1", "ft_moe_workspace_bytes",
            "ft_moe_reserve", "ft_moe_release", "ft_moe_read_device_error", "ft_moe_set_path",
-           "ft_moe_selected_path", "ft_moe_block_dots", "ft_last_error", "ft_abi_version", "ft_profile_enable",
+           "ft_moe_selected_path", "ft_moe_gguf_selected_path", "ft_moe_block_dots", "ft_last_error", "ft_abi_version", "ft_profile_enable",
            "ft_profile_read", "ft_moe_route_offsets_noalloc", "ft_moe_q4_0_q8_1_slots",
            "ft_moe_q4_0_q8_1_ep", "ft_act_mul_quantize_q8_1", "ft_moe_ffn_q4_0_q8_1", "ft_moe_gguf_q8_1",
            "ft_repack_q4_0_soa", "ft_debug_wait_timeout", "ft_moe_q4_0_q8_1_act", "ft_moe_ffn_reserve",
@@ -81,6 +81,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.ft_moe_read_device_error.argtypes = [vp, u32p]
         L.ft_moe_set_path.argtypes = [i32]
         L.ft_moe_selected_path.argtypes = [i64, i32, i32, i64, i64]
+        L.ft_moe_gguf_selected_path.argtypes = [i32, i64, i32, i32, i64, i64]
         L.ft_last_error.argtypes = []
         L.ft_last_error.restype = ctypes.c_char_p
         L.ft_abi_version.argtypes = []
@@ -420,8 +421,12 @@ def set_path(path) -> int:
     return prev
 
 
-def selected_path(tokens, top_k, n_experts, nrows, ncols) -> int:
-    return int(load().ft_moe_selected_path(tokens, top_k, n_experts, nrows, ncols))
+def selected_path(tokens, top_k, n_experts, nrows, ncols, wtype="q4_0") -> int:
+    """The path (FT_PATH_GEMV / FT_PATH_GEMM) the matmul would take for this shape
+    and weight type under the current setting, or -1."""
+    if wtype == "q4_0":
+        return int(load().ft_moe_selected_path(tokens, top_k, n_experts, nrows, ncols))
+    return int(load().ft_moe_gguf_selected_path(WEIGHT_TYPES[wtype][0], tokens, top_k, n_experts, nrows, ncols))
 
 
 def profile_enable(max_calls: int):

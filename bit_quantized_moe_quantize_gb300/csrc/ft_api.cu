@@ -344,12 +344,12 @@ static bool gemm_shape_ok(const Shape& sh) {
 static bool gemm_type_ok(int wtype) { return wtype == FT_TYPE_Q4_0 || wtype == FT_TYPE_Q4_K; }
 
 // Routed slots per expert on average from which the tensor-core path is
-// chosen: 40 where the GEMV would run 16-slot mma.sync tiles (Q4_0 whose
-// activation tile fits; measured: those beat the GEMM up to 32 slots per
-// expert on the three workload shapes by 1.1-1.5x and lose from 48), else 16
-// (the dp4a tiles).
+// chosen: 40 where the GEMV would run 16-slot mma.sync tiles (Q4_0 or Q4_K
+// whose activation tile fits; measured on Q4_0: those beat the GEMM up to 32
+// slots per expert on the three workload shapes by 1.1-1.5x and lose from
+// 48), else 16 (the dp4a tiles).
 static double gemm_min_mean(const Shape& sh, int setting) {
-    if (sh.wtype != FT_TYPE_Q4_0 || setting == FT_PATH_GEMV_DP4A) return 16.0;
+    if ((sh.wtype != FT_TYPE_Q4_0 && sh.wtype != FT_TYPE_Q4_K) || setting == FT_PATH_GEMV_DP4A) return 16.0;
     const double m = sh.mean() > 16.0 ? sh.mean() : 16.0;
     return plan_gemv(sh.n_slots, sh.n_experts, sh.nrows, sh.ncols, m, sh.wtype, true).mma ? 40.0 : 16.0;
 }
@@ -366,7 +366,8 @@ static int choose_path(const Shape& sh, int setting) {
 // path takes over at gemm_min_mean routed slots per expert on average).
 static int64_t gemv_max_slots(const Shape& sh) {
     const int setting = path_setting();
-    if (setting == FT_PATH_GEMV || setting == FT_PATH_GEMV_DP4A || !gemm_shape_ok(sh) || sh.wtype != FT_TYPE_Q4_0) return sh.n_slots;
+    if (setting == FT_PATH_GEMV || setting == FT_PATH_GEMV_DP4A || !gemm_shape_ok(sh) || !gemm_type_ok(sh.wtype))
+        return sh.n_slots;
     const int64_t lim = static_cast<int64_t>(gemm_min_mean(sh, setting)) * sh.n_global;
     return sh.n_slots < lim ? sh.n_slots : lim;
 }
@@ -909,11 +910,17 @@ int ft_moe_set_path(int32_t path) {
 }
 
 int ft_moe_selected_path(int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows, int64_t ncols) {
+    return ft_moe_gguf_selected_path(FT_TYPE_Q4_0, tokens, top_k, n_experts, nrows, ncols);
+}
+
+int ft_moe_gguf_selected_path(int32_t wtype, int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows,
+                              int64_t ncols) {
     Shape sh{};
     std::string keep = g_last_error;
     const int st = check_matmul_args(tokens, top_k, n_experts, nrows, ncols, &sh);
     g_last_error = keep;
-    if (st) return -1;
+    if (st || weight_block_bytes(wtype) == 0 || ncols % weight_block_values(wtype) != 0) return -1;
+    sh.wtype = wtype;
     return choose_path(sh, path_setting());
 }
 

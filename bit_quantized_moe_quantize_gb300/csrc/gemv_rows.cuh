@@ -556,12 +556,12 @@ static int launch_gemv_rows_type(const GemvPlan& plan, const CUtensorMap& wmap, 
 int launch_gemv_rows_gguf(int wtype, const GemvPlan& plan, const CUtensorMap& wmap, const GemvArgs& a,
                           cudaStream_t s);
 
-// Q4_0 tiles of nt groups of 8 slots on mma.sync (moe_gemv_mma.cu): shared
+// Q4_0 and Q4_K tiles of nt groups of 8 slots on mma.sync (moe_gemv_mma.cu): shared
 // memory of a CTA of row_warps warps of 16 rows with a ring of `stages` boxes,
 // and the launch (dump: block dots); wmap's box is 16 * row_warps rows high,
 // wmap16's 16 rows (for the short row blocks at the ends of a CTA's range).
-size_t gemv_mma_smem(int nb, int nt, int row_warps, int stages);
+size_t gemv_mma_smem(int nb, int nt, int row_warps, int stages, int wtype);
 int launch_gemv_mma(const GemvPlan& plan, const CUtensorMap& wmap, const CUtensorMap& wmap16, const GemvArgs& a,
-                    bool dump, cudaStream_t s);
+                    bool dump, int wtype, cudaStream_t s);
 
 }  // namespace ft

@@ -138,7 +138,7 @@ GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t nc
         p.rows_per_cta = (nrows + 32 * rw - 1) / (32 * rw);   // row blocks per slot tile
         p.min_tiles = min_tiles;
         p.row_tiles = 0;
-        if (mma && wtype == FT_TYPE_Q4_0 && mean > 4.0) {
+        if (mma && (wtype == FT_TYPE_Q4_0 || wtype == FT_TYPE_Q4_K) && mean > 4.0) {
             // tiles on mma.sync: 16 slots (two groups of 8) where their fp16
             // activation tile leaves room for a ring, else 8.  One CTA per SM
             // of RW warps of 16 rows (fewer when the batch has fewer row blocks
@@ -153,7 +153,7 @@ GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t nc
                     for (int mrw : kRowWarps) {
                         // fewer rows per block only where the row blocks would not cover the SMs
                         if (mrw > 1 && tiles * ((groups16 + mrw - 1) / mrw) < sms) continue;
-                        const size_t r0 = gemv_mma_smem(static_cast<int>(nb), nt, mrw, 0);
+                        const size_t r0 = gemv_mma_smem(static_cast<int>(nb), nt, mrw, 0, wtype);
                         const size_t stg = static_cast<size_t>(row_box_pitch(wtype)) * 16 * mrw;
                         int st = cap > r0 ? static_cast<int>((cap - r0) / stg) : 0;
                         st = st > kMaxRowStages ? kMaxRowStages : st;
@@ -169,7 +169,7 @@ GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t nc
                 p.row_warps = best_rw;
                 p.ksplit = 1;
                 p.stages = best_st;
-                p.smem = gemv_mma_smem(static_cast<int>(nb), nt, best_rw, best_st);
+                p.smem = gemv_mma_smem(static_cast<int>(nb), nt, best_rw, best_st, wtype);
                 p.min_tiles = tiles > 0 ? tiles : 1;
                 const int64_t ub2 = (n_slots + p.group - 1) / p.group + (n_experts < n_slots ? n_experts : n_slots);
                 p.grid_x = ub2 < n_slots ? ub2 : n_slots;
@@ -276,15 +276,15 @@ int launch_gemv(const GemvPlan& plan, const uint8_t* weights, const uint8_t* act
                                static_cast<uint64_t>(n_experts) * nrows, row_bytes, pitch / 2,
                                (plan.mma ? 16 : 32) * plan.row_warps, CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
             return st;
-        if (wtype != FT_TYPE_Q4_0) return launch_gemv_rows_gguf(wtype, plan, wmap, a, s);
         if (plan.mma) {
             CUtensorMap wmap16;
             if (int st = encode_2d(&wmap16, CU_TENSOR_MAP_DATA_TYPE_UINT16, weights, row_bytes / 2,
                                    static_cast<uint64_t>(n_experts) * nrows, row_bytes, pitch / 2, 16,
                                    CU_TENSOR_MAP_SWIZZLE_NONE, "weights"))
                 return st;
-            return launch_gemv_mma(plan, wmap, wmap16, a, dump, s);
+            return launch_gemv_mma(plan, wmap, wmap16, a, dump, wtype, s);
         }
+        if (wtype != FT_TYPE_Q4_0) return launch_gemv_rows_gguf(wtype, plan, wmap, a, s);
         switch (plan.group) {
             case 1: return dump ? launch_gemv_rows<FT_TYPE_Q4_0, 1, true>(plan, wmap, a, s) : launch_gemv_rows<FT_TYPE_Q4_0, 1, false>(plan, wmap, a, s);
             case 2: return dump ? launch_gemv_rows<FT_TYPE_Q4_0, 2, true>(plan, wmap, a, s) : launch_gemv_rows<FT_TYPE_Q4_0, 2, false>(plan, wmap, a, s);

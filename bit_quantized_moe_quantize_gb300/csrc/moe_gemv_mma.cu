@@ -58,6 +58,8 @@
 // mbarrier ring filled by one producer warp, which runs ahead of the staging.
 // Warp r owns rows 16 r .. 16 r + 15 of each box (one m16 tile), so a CTA
 // keeps up to 16 row warps busy on one staged activation tile.
+#include <type_traits>
+
 #include <cuda_fp16.h>
 
 #include "gemv_rows.cuh"
@@ -68,13 +70,15 @@ namespace ft {
 // qb [nb][NT][32 lanes] uint2 (codes + 128 at P_t: first / last 16) | xc
 // [nb][NT][4] float4 (the accumulator's start for lane t: minus the offset
 // sums of slots 2t, 2t+1, twice, as the MMA's C quad) | xd [nb][NT][4] float2
-// (d_a of slots 2t, 2t+1) | ring (128-byte aligned)
+// (d_a of slots 2t, 2t+1; Q4_K: float4, then d_a sum(q_a) of those slots) |
+// ring (128-byte aligned)
 __host__ __device__ inline size_t gemv_mma_qb_offset() { return 8 * 2 * kMaxRowStages + 16; }
-__host__ __device__ inline size_t gemv_mma_ring_offset(int nb, int nt) {
-    return (gemv_mma_qb_offset() + static_cast<size_t>(nb) * nt * (256 + 64 + 32) + 127) / 128 * 128;
+__host__ __device__ inline size_t gemv_mma_ring_offset(int nb, int nt, bool kq) {
+    return (gemv_mma_qb_offset() + static_cast<size_t>(nb) * nt * (256 + 64 + (kq ? 64 : 32)) + 127) / 128 * 128;
 }
-size_t gemv_mma_smem(int nb, int nt, int row_warps, int stages) {
-    return gemv_mma_ring_offset(nb, nt) + static_cast<size_t>(stages) * RowBox<FT_TYPE_Q4_0>::PITCH * 16 * row_warps;
+size_t gemv_mma_smem(int nb, int nt, int row_warps, int stages, int wtype) {
+    return gemv_mma_ring_offset(nb, nt, wtype == FT_TYPE_Q4_K) +
+           static_cast<size_t>(stages) * RowBox<FT_TYPE_Q4_0>::PITCH * 16 * row_warps;
 }
 
 // D = A B + C on m16n8k16, fp16 operands, fp32 accumulators (not volatile: a
@@ -133,9 +137,10 @@ __device__ __forceinline__ void codes_hi(uint32_t u, uint32_t& b0, uint32_t& b1)
 // Enter slot tile `tile` (compute warps, n_threads of them): stage its
 // activations as B fragments and offset sums, and return its slot count and
 // the slot ids of this thread's output columns (-1: none).
-template <int NT>
-__device__ __forceinline__ void mma_stage_tile(const GemvArgs& a, int64_t tile, uint2* qb, float4* xc, float2* xd,
+template <int NT, int WT, typename XD>
+__device__ __forceinline__ void mma_stage_tile(const GemvArgs& a, int64_t tile, uint2* qb, float4* xc, XD* xd,
                                                int32_t n_threads, int32_t& ng, int32_t (&sid)[NT][2]) {
+    constexpr bool KQ = WT == FT_TYPE_Q4_K;
     constexpr int G = 8 * NT;
     const int32_t nb = a.nb;
     const int32_t e = find_expert(a.tiles, a.n_experts, tile);
@@ -160,8 +165,13 @@ __device__ __forceinline__ void mma_stage_tile(const GemvArgs& a, int64_t tile, 
             const int64_t tok = __ldg(a.perm + p0 + n) / a.top_k;
             const uint8_t* blk = a.act + (tok * nb + b) * Q8_1_BYTES;
             d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(blk))));
-            wl = code_word(blk + 4, b, tq);
-            wh = code_word(blk + 20, b, tq);
+            if constexpr (KQ) {                              // P_t = 4t..4t+3 for every sub-block
+                wl = __ldg(reinterpret_cast<const uint32_t*>(blk + 4) + tq);
+                wh = __ldg(reinterpret_cast<const uint32_t*>(blk + 20) + tq);
+            } else {
+                wl = code_word(blk + 4, b, tq);
+                wh = code_word(blk + 20, b, tq);
+            }
         }
         qb[i] = make_uint2(wl ^ 0x80808080u, wh ^ 0x80808080u);
         int sl = __dp4a(static_cast<int>(wl), 0x01010101, 0), sh = __dp4a(static_cast<int>(wh), 0x01010101, 0);
@@ -171,10 +181,16 @@ __device__ __forceinline__ void mma_stage_tile(const GemvArgs& a, int64_t tile, 
         sh += __shfl_xor_sync(0xFFFFFFFFu, sh, 2);
         if (tq == 0) {
             float* c = reinterpret_cast<float*>(xc + static_cast<size_t>(bn) * 4 + (g >> 1));
-            const float c0 = -static_cast<float>(1032 * sl + 72 * sh);
+            // Q4_0: A = 1024 + q (first 16) and 1024 + 16 q with B / 16 (last 16),
+            // level 8; Q4_K (levels 0..15, sub-block j = b mod 8 = the low
+            // nibbles for even j, the high ones as 1024 + 16 q with B / 16 for odd)
+            const float c0 = KQ ? -static_cast<float>(((b & 1) ? 64 : 1024) * (sl + sh))
+                                : -static_cast<float>(1032 * sl + 72 * sh);
             c[g & 1] = c0;
             c[2 + (g & 1)] = c0;
-            reinterpret_cast<float*>(xd + static_cast<size_t>(bn) * 4 + (g >> 1))[g & 1] = d;
+            float* x = reinterpret_cast<float*>(xd + static_cast<size_t>(bn) * 4 + (g >> 1));
+            x[g & 1] = d;
+            if constexpr (KQ) x[2 + (g & 1)] = d * small_int_to_float(sl + sh);   // the offset term's d_a sum(q_a)
         }
     }
 }
@@ -271,11 +287,15 @@ __device__ void mma_work_range(const GemvArgs& a, int64_t n_u, int64_t* range) {
     }
 }
 
-template <int NT, bool DUMP>
+template <int NT, int WT, bool DUMP>
 __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const __grid_constant__ CUtensorMap wmap16,
                                                               const GemvArgs a) {
-    constexpr int PITCH = RowBox<FT_TYPE_Q4_0>::PITCH;   // 144: 8 blocks of 18 bytes
+    constexpr int PITCH = RowBox<FT_TYPE_Q4_0>::PITCH;   // 144: 8 Q4_0 blocks, or one Q4_K super-block
+    constexpr bool KQ = WT == FT_TYPE_Q4_K;
+    static_assert(WT == FT_TYPE_Q4_0 || KQ, "weight type of the mma.sync kernel");
+    static_assert(!DUMP || !KQ, "block dots are a Q4_0 diagnostic");
+    using XD = std::conditional_t<KQ, float4, float2>;
     const int32_t RW = a.row_warps;                       // warps of 16 rows
     const int32_t E = a.n_experts;
     const int32_t nb = a.nb;
@@ -289,8 +309,8 @@ __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_const
     int64_t* range = reinterpret_cast<int64_t*>(empty + kMaxRowStages);
     uint2* qb = reinterpret_cast<uint2*>(smem_mma + gemv_mma_qb_offset());          // [nb][NT][32]
     float4* xc = reinterpret_cast<float4*>(qb + static_cast<size_t>(nb) * NT * 32);  // [nb][NT][4]
-    float2* xd = reinterpret_cast<float2*>(xc + static_cast<size_t>(nb) * NT * 4);   // [nb][NT][4]
-    uint8_t* ring = smem_mma + gemv_mma_ring_offset(nb, NT);
+    XD* xd = reinterpret_cast<XD*>(xc + static_cast<size_t>(nb) * NT * 4);             // [nb][NT][4]
+    uint8_t* ring = smem_mma + gemv_mma_ring_offset(nb, NT, KQ);
     const uint32_t stage_bytes = static_cast<uint32_t>(PITCH * 16 * RW);
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
     if (threadIdx.x == 0) {
@@ -356,7 +376,7 @@ __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_const
         u += cnt;
         if (tile != cur) {
             if (cur >= 0) named_bar_sync(1, n_threads);  // every warp is done with the previous tile
-            mma_stage_tile<NT>(a, tile, qb, xc, xd, static_cast<int32_t>(n_threads), ng, sid);
+            mma_stage_tile<NT, WT>(a, tile, qb, xc, xd, static_cast<int32_t>(n_threads), ng, sid);
             named_bar_sync(1, n_threads);
             cur = tile;
         }
@@ -376,23 +396,65 @@ __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_const
             auto block = [&](auto J) {
                 constexpr int j = decltype(J)::value;
                 const int32_t b = ks * 8 + j;
-                const uint32_t wa = nibble_word<j>(ra, tq), wb = nibble_word<j>(rb8, tq);
-                const float dwa = __half2float(*reinterpret_cast<const __half*>(ra + 18 * j));
-                const float dwb = __half2float(*reinterpret_cast<const __half*>(rb8 + 18 * j));
-                const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-                const uint32_t alo[4] = {(wa & 0x000F000Fu) | 0x64006400u, (wb & 0x000F000Fu) | 0x64006400u,
-                                         (wa8 & 0x000F000Fu) | 0x64006400u, (wb8 & 0x000F000Fu) | 0x64006400u};
-                const uint32_t ahi[4] = {(wa & 0x00F000F0u) | 0x64006400u, (wb & 0x00F000F0u) | 0x64006400u,
-                                         (wa8 & 0x00F000F0u) | 0x64006400u, (wb8 & 0x00F000F0u) | 0x64006400u};
+                uint32_t alo[4], ahi[4];                    // A of weights 0..15 and 16..31
+                float dwa, dwb, mwa = 0.0f, mwb = 0.0f;
+                if constexpr (KQ) {
+                    // sub-block j: the low (even j) or high (odd j) nibbles of
+                    // qs[32 (j / 2) ..] (the super-block's bytes 16 + ..): weights
+                    // 4t..4t+3 and 16+4t.. of it in two aligned words per row
+                    constexpr int Q = 16 + 32 * (j >> 1);
+                    constexpr uint32_t MASK = (j & 1) ? 0x00F000F0u : 0x000F000Fu;
+                    const uint32_t wa0 = lds32(ra + Q + 4 * tq), wa1 = lds32(ra + Q + 16 + 4 * tq);
+                    const uint32_t wb0 = lds32(rb8 + Q + 4 * tq), wb1 = lds32(rb8 + Q + 16 + 4 * tq);
+                    alo[0] = (wa0 & MASK) | 0x64006400u;
+                    alo[1] = (wb0 & MASK) | 0x64006400u;
+                    alo[2] = ((wa0 >> 8) & MASK) | 0x64006400u;
+                    alo[3] = ((wb0 >> 8) & MASK) | 0x64006400u;
+                    ahi[0] = (wa1 & MASK) | 0x64006400u;
+                    ahi[1] = (wb1 & MASK) | 0x64006400u;
+                    ahi[2] = ((wa1 >> 8) & MASK) | 0x64006400u;
+                    ahi[3] = ((wb1 >> 8) & MASK) | 0x64006400u;
+                    // d sc_j and d_min m_j of each row, as the dp4a kernels form them
+                    const uint4 ha = *reinterpret_cast<const uint4*>(ra), hb = *reinterpret_cast<const uint4*>(rb8);
+                    const uint32_t sa[3] = {ha.y, ha.z, ha.w}, sb[3] = {hb.y, hb.z, hb.w};
+                    int sca, mna, scb, mnb;
+                    kquant_scale_min(sa, j, sca, mna);
+                    kquant_scale_min(sb, j, scb, mnb);
+                    dwa = __half2float(__ushort_as_half(static_cast<unsigned short>(ha.x & 0xFFFFu))) * static_cast<float>(sca);
+                    dwb = __half2float(__ushort_as_half(static_cast<unsigned short>(hb.x & 0xFFFFu))) * static_cast<float>(scb);
+                    mwa = __half2float(__ushort_as_half(static_cast<unsigned short>(ha.x >> 16))) * static_cast<float>(mna);
+                    mwb = __half2float(__ushort_as_half(static_cast<unsigned short>(hb.x >> 16))) * static_cast<float>(mnb);
+                } else {
+                    (void)mwa;
+                    (void)mwb;
+                    const uint32_t wa = nibble_word<j>(ra, tq), wb = nibble_word<j>(rb8, tq);
+                    dwa = __half2float(*reinterpret_cast<const __half*>(ra + 18 * j));
+                    dwb = __half2float(*reinterpret_cast<const __half*>(rb8 + 18 * j));
+                    const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+                    alo[0] = (wa & 0x000F000Fu) | 0x64006400u;
+                    alo[1] = (wb & 0x000F000Fu) | 0x64006400u;
+                    alo[2] = (wa8 & 0x000F000Fu) | 0x64006400u;
+                    alo[3] = (wb8 & 0x000F000Fu) | 0x64006400u;
+                    ahi[0] = (wa & 0x00F000F0u) | 0x64006400u;
+                    ahi[1] = (wb & 0x00F000F0u) | 0x64006400u;
+                    ahi[2] = (wa8 & 0x00F000F0u) | 0x64006400u;
+                    ahi[3] = (wb8 & 0x00F000F0u) | 0x64006400u;
+                }
 #pragma unroll
                 for (int nt = 0; nt < USE; ++nt) {
                     const size_t bn = static_cast<size_t>(b) * NT + nt;
                     const uint2 Q = qb[bn * 32 + lane];
                     const float4 C = xc[bn * 4 + tq];
-                    const float2 D = xd[bn * 4 + tq];
+                    const XD D = xd[bn * 4 + tq];
                     uint32_t bl0, bl1, bh0, bh1;
-                    codes_lo(Q.x, bl0, bl1);
-                    codes_hi(Q.y, bh0, bh1);
+                    if (!KQ || (j & 1) == 0) {
+                        if (KQ) codes_lo(Q.y, bh0, bh1);    // Q4_K, low nibbles: both halves as q
+                        else codes_hi(Q.y, bh0, bh1);      // Q4_0: the high nibbles' codes as q / 16
+                        codes_lo(Q.x, bl0, bl1);
+                    } else {                                // Q4_K, high nibbles: both halves as q / 16
+                        codes_hi(Q.x, bl0, bl1);
+                        codes_hi(Q.y, bh0, bh1);
+                    }
                     float d0[4], d1[4];
                     mma_16816(d0, alo, bl0, bl1, C.x, C.y, C.z, C.w);
                     mma_16816(d1, ahi, bh0, bh1, d0[0], d0[1], d0[2], d0[3]);
@@ -410,6 +472,12 @@ __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_const
                         acc[nt][1] = fmaf(d1[1], dwa * D.y, acc[nt][1]);
                         acc[nt][2] = fmaf(d1[2], dwb * D.x, acc[nt][2]);
                         acc[nt][3] = fmaf(d1[3], dwb * D.y, acc[nt][3]);
+                        if constexpr (KQ) {                 // minus d_min m_j d_a sum(q_a)
+                            acc[nt][0] = fmaf(-mwa, D.z, acc[nt][0]);
+                            acc[nt][1] = fmaf(-mwa, D.w, acc[nt][1]);
+                            acc[nt][2] = fmaf(-mwb, D.z, acc[nt][2]);
+                            acc[nt][3] = fmaf(-mwb, D.w, acc[nt][3]);
+                        }
                     }
                 }
             };
@@ -453,26 +521,31 @@ __global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_const
     }
 }
 
-template <int NT, bool DUMP>
+template <int NT, int WT, bool DUMP>
 static int launch_gemv_mma_nt(const GemvPlan& plan, const CUtensorMap& wmap, const CUtensorMap& wmap16, const GemvArgs& a,
                               cudaStream_t s) {
-    const void* kernel = reinterpret_cast<const void*>(moe_gemv_mma_kernel<NT, DUMP>);
+    const void* kernel = reinterpret_cast<const void*>(moe_gemv_mma_kernel<NT, WT, DUMP>);
     if (int st = set_smem_limit(kernel, static_cast<int>(plan.smem))) return st;
     const int threads = 32 * (plan.row_warps + 1);
     // one CTA per SM (or as many as fit); each takes an equal share of the work
     const dim3 grid(static_cast<unsigned>(sm_count() * resident_ctas(kernel, threads, plan.smem)));
     const dim3 block(threads);
-    moe_gemv_mma_kernel<NT, DUMP><<<grid, block, plan.smem, s>>>(wmap, wmap16, a);
+    moe_gemv_mma_kernel<NT, WT, DUMP><<<grid, block, plan.smem, s>>>(wmap, wmap16, a);
     return check_launch(DUMP ? "moe_gemv_mma_kernel<dump>" : "moe_gemv_mma_kernel", grid, block, plan.smem);
 }
 
 int launch_gemv_mma(const GemvPlan& plan, const CUtensorMap& wmap, const CUtensorMap& wmap16, const GemvArgs& a,
-                    bool dump, cudaStream_t s) {
+                    bool dump, int wtype, cudaStream_t s) {
+    if (wtype == FT_TYPE_Q4_K) {
+        if (dump) return fail(FT_ERR_ARG, "block dots are Q4_0 only");
+        return plan.mma == 2 ? launch_gemv_mma_nt<2, FT_TYPE_Q4_K, false>(plan, wmap, wmap16, a, s)
+                             : launch_gemv_mma_nt<1, FT_TYPE_Q4_K, false>(plan, wmap, wmap16, a, s);
+    }
     if (plan.mma == 2)
-        return dump ? launch_gemv_mma_nt<2, true>(plan, wmap, wmap16, a, s)
-                    : launch_gemv_mma_nt<2, false>(plan, wmap, wmap16, a, s);
-    return dump ? launch_gemv_mma_nt<1, true>(plan, wmap, wmap16, a, s)
-                : launch_gemv_mma_nt<1, false>(plan, wmap, wmap16, a, s);
+        return dump ? launch_gemv_mma_nt<2, FT_TYPE_Q4_0, true>(plan, wmap, wmap16, a, s)
+                    : launch_gemv_mma_nt<2, FT_TYPE_Q4_0, false>(plan, wmap, wmap16, a, s);
+    return dump ? launch_gemv_mma_nt<1, FT_TYPE_Q4_0, true>(plan, wmap, wmap16, a, s)
+                : launch_gemv_mma_nt<1, FT_TYPE_Q4_0, false>(plan, wmap, wmap16, a, s);
 }
 
 }  // namespace ft

@@ -509,6 +509,12 @@ FT_API int ft_moe_set_path(int32_t path);
 FT_API int ft_moe_selected_path(int64_t tokens, int32_t top_k, int32_t n_experts, int64_t nrows,
                          int64_t ncols);
 
+/* ft_moe_gguf_selected_path - the same for ft_moe_gguf_q8_1 with weights of
+ * FT_TYPE_* wtype (-1 also for an unknown type or ncols not a whole number
+ * of its blocks). */
+FT_API int ft_moe_gguf_selected_path(int32_t wtype, int64_t tokens, int32_t top_k, int32_t n_experts,
+                                     int64_t nrows, int64_t ncols);
+
 /*
  * ft_moe_block_dots - diagnostic: run the selected path in a mode that writes
  * every per-block integer dot instead of the scaled sum:

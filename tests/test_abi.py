@@ -113,7 +113,17 @@ def test_workspace_and_path_selection(lib):
         assert sel(1, 8, 128, 768, 2048) == 1            # decode: GEMV
         assert sel(8191, 8, 128, 1408, 2816) == 2        # prefill: tensor cores
         assert sel(8191, 8, 128, 1408, 2816 + 32) == 1   # ncols % 256 != 0: GEMV only
-        assert lib.ft_moe_set_path(2) == 0
+        # 32 routed slots per expert: the GEMV's 16-slot mma.sync tiles; 48: tensor cores
+        assert sel(512, 8, 128, 768, 2048) == 1 and sel(768, 8, 128, 768, 2048) == 2
+        gsel = lib.ft_moe_gguf_selected_path
+        assert gsel(12, 8191, 8, 128, 1408, 2816) == 2   # Q4_K: tensor cores
+        assert gsel(14, 8191, 8, 128, 1408, 2816) == 1   # Q6_K: GEMV only
+        assert gsel(12, 512, 8, 128, 768, 2048) == 1     # Q4_K, 32 slots per expert: mma.sync tiles
+        assert gsel(99, 1, 8, 128, 768, 2048) == -1      # unknown type
+        assert gsel(12, 1, 8, 128, 768, 2816 + 32) == -1  # not whole super-blocks
+        assert lib.ft_moe_set_path(3) == 0               # the GEMV path on the dp4a kernels, forced
+        assert sel(512, 8, 128, 768, 2048) == 1 and sel(8191, 8, 128, 1408, 2816) == 1
+        assert lib.ft_moe_set_path(2) == 3
         assert sel(1, 8, 128, 768, 2048) == 2
         assert lib.ft_moe_set_path(7) == -1
         assert sel(1, 8, 128, 768, 100) == -1

@@ -143,6 +143,56 @@ def test_q4_k_tensor_cores_full_size(ft, oracle):
     G.check_close(got[toks], ref, wn[ids[toks]], np.broadcast_to(xn[:, None, None], (16, k, N)), "q4_k gemm full size")
 
 
+# Q4_K decode tiles on mma.sync (more than 4 slots per expert on average):
+# (E, k, K, N, T, seed) and whether the dp4a row kernel leaves K unsplit there
+# (one super-block per row), so that the two agree bit for bit
+Q4K_MMA = [(8, 2, 256, 77, 20, 110, True), (6, 3, 256, 1000, 13, 111, True), (16, 4, 2048, 520, 30, 112, False),
+           (4, 4, 768, 300, 7, 113, False), (3, 2, 512, 1000, 11, 114, False)]
+
+
+@pytest.mark.parametrize("E,k,K,N,T,seed,same", Q4K_MMA)
+def test_q4_k_mma_tiles(ft, oracle, E, k, K, N, T, seed, same):
+    w, x, ids = _case("q4_k", E, k, K, N, T, seed)
+    ids = ids.copy()
+    ids[T // 2, 0] = E                                    # a bad id: zero row, flag
+    assert 4.0 < T * k / E <= 16.0
+    ft.read_device_error()
+    a, ref = _check(ft, oracle, "q4_k", w, x, ids, f"q4_k mma {E},{k},{K},{N},{T}")
+    assert not a[T // 2, 0].any()
+    assert ft.read_device_error() & ft.FT_DEVERR_BAD_EXPERT_ID
+    act = G.dev(oracle.quantize_q8_1(x))
+    prev = ft.set_path("gemv_dp4a")
+    try:
+        b = G.host(ft.moe_gguf_q8_1("q4_k", G.dev(w), act, G.dev(ids)))
+    finally:
+        ft.set_path(prev)
+    ft.read_device_error()
+    if same:
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_q4_k_mma_full_size(ft, oracle):
+    """The 8-expert top-2 layer (14336 x 4096) with Q4_K weights at 32 tokens:
+    the mma.sync tiles equal the dp4a row kernel bit for bit (K unsplit at this
+    size), and every output of two tokens matches the oracle."""
+    w, x, ids = _case("q4_k", 8, 2, 4096, 14336, 32, 115)
+    act = oracle.quantize_q8_1(x)
+    a = G.host(ft.moe_gguf_q8_1("q4_k", G.dev(w), G.dev(act), G.dev(ids)))
+    prev = ft.set_path("gemv_dp4a")
+    try:
+        b = G.host(ft.moe_gguf_q8_1("q4_k", G.dev(w), G.dev(act), G.dev(ids)))
+    finally:
+        ft.set_path(prev)
+    assert ft.read_device_error() == 0
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    toks = np.array([3, 29])
+    ref = oracle.moe_gguf("q4_k", w, act[toks], ids[toks])
+    E, N = 8, 14336
+    wn = np.linalg.norm(oracle.dequantize_gguf("q4_k", w.reshape(E * N, -1, 144)), axis=-1).reshape(E, N)
+    xn = G.act_norms(oracle, act[toks])
+    G.check_close(a[toks], ref, wn[ids[toks]], np.broadcast_to(xn[:, None, None], (2, 2, N)), "q4_k mma full size")
+
+
 def test_gguf_rejects_what_the_path_cannot_run(ft, oracle):
     import torch
     w, x, ids = _case("q8_0", 8, 2, 256, 128, 4, 97)

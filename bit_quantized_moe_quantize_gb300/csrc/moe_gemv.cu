@@ -139,16 +139,19 @@ GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t nc
         p.min_tiles = min_tiles;
         p.row_tiles = 0;
         if (mma && (wtype == FT_TYPE_Q4_0 || wtype == FT_TYPE_Q4_K) && mean > 4.0) {
-            // tiles on mma.sync: 16 slots (two groups of 8) where their fp16
+            // tiles on mma.sync: 16 slots (two groups of 8) where their staged
             // activation tile leaves room for a ring, else 8.  One CTA per SM
             // of RW warps of 16 rows (fewer when the batch has fewer row blocks
-            // than SMs), RW chosen for a ring of at least 3 boxes where one exists
+            // than SMs), RW chosen for a ring of at least 3 boxes where one
+            // exists; at most 15, so that with the producer each scheduler runs
+            // 4 warps and a thread may hold 128 registers (a 17th warp puts 5 on
+            // one scheduler and caps them at 96)
             const size_t cap = 227 * 1024;
             const int64_t groups16 = (nrows + 15) / 16;
             for (int nt = 2; nt >= 1; --nt) {
                 const int64_t tiles = (local + 8 * nt - 1) / (8 * nt);
                 int best_rw = 0, best_st = 0;
-                static const int kRowWarps[] = {16, 12, 8, 4, 2, 1};
+                static const int kRowWarps[] = {15, 12, 8, 4, 2, 1};
                 for (int need = 3; need >= 2 && best_rw == 0; --need)
                     for (int mrw : kRowWarps) {
                         // fewer rows per block only where the row blocks would not cover the SMs

@@ -40,7 +40,7 @@
 // to unsigned bytes), 8 bytes per lane, block and slot group (one
 // conflict-free 8-byte load), and turned into fp16 pairs with a byte permute
 // and one fp16 op per pair: half the shared memory of staged fp16 pairs,
-// which leaves room for 16 row warps and a 3-box ring.
+// which leaves room for 15 row warps and a 3-box ring.
 //
 // Work split.  The grid is one CTA per SM.  A work unit is (slot tile, group
 // of 16 rows), numbered tile-major; there are tiles x ceil(rows / 16) of them
@@ -57,7 +57,7 @@
 // of 256 weights (8 blocks, 144 bytes per row) x 16 RW rows through an
 // mbarrier ring filled by one producer warp, which runs ahead of the staging.
 // Warp r owns rows 16 r .. 16 r + 15 of each box (one m16 tile), so a CTA
-// keeps up to 16 row warps busy on one staged activation tile.
+// keeps up to 15 row warps busy on one staged activation tile.
 #include <type_traits>
 
 #include <cuda_fp16.h>
@@ -288,7 +288,7 @@ __device__ void mma_work_range(const GemvArgs& a, int64_t n_u, int64_t* range) {
 }
 
 template <int NT, int WT, bool DUMP>
-__global__ void __launch_bounds__(544, 1) moe_gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap,
+__global__ void __launch_bounds__(512, 1) moe_gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const __grid_constant__ CUtensorMap wmap16,
                                                               const GemvArgs a) {
     constexpr int PITCH = RowBox<FT_TYPE_Q4_0>::PITCH;   // 144: 8 Q4_0 blocks, or one Q4_K super-block

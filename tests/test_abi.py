@@ -240,3 +240,17 @@ def test_debug_wait_timeout_rejects_bad_limits_on_the_host(lib):
     for bad in (0, 999, 2_000_000_000):
         assert lib.ft_debug_wait_timeout(bad, vp(0)) == 1
     assert "limit_ns" in _err(lib)
+
+
+@pytest.mark.parametrize("value,code", [("gemv", 1), ("gemm", 2), ("gemv_dp4a", 3), ("auto", 0), ("bogus", 0)])
+def test_path_environment_variable(lib, value, code):
+    """FT_MOE_PATH sets the initial path setting (read once, at the first
+    use, in a fresh process): ft_moe_set_path returns it as the previous one."""
+    import subprocess
+    import sys
+    prog = ("import ctypes, sys; from bit_quantized_moe_quantize_gb300 import _lib; "
+            "L = _lib.load(); sys.stdout.write(str(L.ft_moe_set_path(0)))")
+    env = dict(os.environ, FT_MOE_PATH=value)
+    got = subprocess.run([sys.executable, "-c", prog], env=env, cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert got.returncode == 0, got.stderr
+    assert got.stdout.strip() == str(code)

@@ -62,16 +62,18 @@ NCU_TRAFFIC_GEMV = {("moe_gemv_mma_kernel", "9abf780d2a1c171b", "mixtral_8x7b:32
 
 
 def mma_tiles(S, E, K, wtype="q4_0") -> bool:
-    """The library's rule for the mma.sync GEMV tiles of a Q4_0 or Q4_K batch
-    (rows of whole 256-weight runs): more than 4 slots per expert on average,
-    and the staged activations of an 8-slot tile (352 B per block, 384 for
-    Q4_K) plus a ring of two 16-row boxes within 227 KB of shared memory."""
-    if wtype not in ("q4_0", "q4_k"):
+    """The library's rule for the mma.sync GEMV tiles of a Q4_0, Q4_1, Q8_0 or
+    Q4_K batch (rows of whole 256-weight runs): more than 4 slots per expert
+    on average, and the staged activations of an 8-slot tile (352 B per block,
+    384 for the types with an offset term) plus a ring of two 16-row boxes
+    within 227 KB of shared memory."""
+    pitch = {"q4_0": 144, "q4_k": 144, "q4_1": 176, "q8_0": 272}.get(wtype)
+    if pitch is None:
         return False
     nb = K // 32
     head = 8 * 2 * 16 + 16
-    ring0 = (head + nb * (384 if wtype == "q4_k" else 352) + 127) // 128 * 128
-    return S / E > 4.0 and ring0 + 2 * 144 * 16 <= 227 * 1024
+    ring0 = (head + nb * (384 if wtype in ("q4_k", "q4_1") else 352) + 127) // 128 * 128
+    return S / E > 4.0 and ring0 + 2 * pitch * 16 <= 227 * 1024
 
 
 def kernel_source_hash(files, constants=GEMM_CONSTANTS) -> str:

@@ -138,7 +138,8 @@ GemvPlan plan_gemv(int64_t n_slots, int32_t n_experts, int64_t nrows, int64_t nc
         p.rows_per_cta = (nrows + 32 * rw - 1) / (32 * rw);   // row blocks per slot tile
         p.min_tiles = min_tiles;
         p.row_tiles = 0;
-        if (mma && (wtype == FT_TYPE_Q4_0 || wtype == FT_TYPE_Q4_K) && mean > 4.0) {
+        if (mma && (wtype == FT_TYPE_Q4_0 || wtype == FT_TYPE_Q4_1 || wtype == FT_TYPE_Q8_0 || wtype == FT_TYPE_Q4_K) &&
+            mean > 4.0) {
             // tiles on mma.sync: 16 slots (two groups of 8) where their staged
             // activation tile leaves room for a ring, else 8.  One CTA per SM
             // of RW warps of 16 rows (fewer when the batch has fewer row blocks

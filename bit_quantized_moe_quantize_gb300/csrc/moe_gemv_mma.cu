@@ -73,12 +73,32 @@ namespace ft {
 // (d_a of slots 2t, 2t+1; Q4_K: float4, then d_a sum(q_a) of those slots) |
 // ring (128-byte aligned)
 __host__ __device__ inline size_t gemv_mma_qb_offset() { return 8 * 2 * kMaxRowStages + 16; }
-__host__ __device__ inline size_t gemv_mma_ring_offset(int nb, int nt, bool kq) {
-    return (gemv_mma_qb_offset() + static_cast<size_t>(nb) * nt * (256 + 64 + (kq ? 64 : 32)) + 127) / 128 * 128;
+__host__ __device__ inline size_t gemv_mma_ring_offset(int nb, int nt, bool offset) {
+    return (gemv_mma_qb_offset() + static_cast<size_t>(nb) * nt * (256 + 64 + (offset ? 64 : 32)) + 127) / 128 * 128;
 }
+
+// The weight types of this kernel: box row bytes and pitch of 256 weights
+// (RowBox), whether a block has an offset term (m, or minus d_min m_j) and
+// whether the nibble / code words of lane t are the block's bytes 4t..4t+3
+// for every block (Q4_1's and Q4_K's data start 4-byte aligned; Q4_0's and
+// Q8_0's every other block 2 bytes off a word).
+template <int WT>
+struct MmaType {
+    static constexpr int PITCH = RowBox<WT>::PITCH;
+    static constexpr int BYTES = RowBox<WT>::BYTES;
+    static constexpr bool KQ = WT == FT_TYPE_Q4_K;
+    static constexpr bool OFFSET = WT == FT_TYPE_Q4_K || WT == FT_TYPE_Q4_1;
+    static constexpr bool ALIGNED = WT == FT_TYPE_Q4_K || WT == FT_TYPE_Q4_1;
+    static_assert(WT == FT_TYPE_Q4_0 || WT == FT_TYPE_Q4_1 || WT == FT_TYPE_Q8_0 || KQ,
+                  "weight type of the mma.sync kernel");
+};
+
 size_t gemv_mma_smem(int nb, int nt, int row_warps, int stages, int wtype) {
-    return gemv_mma_ring_offset(nb, nt, wtype == FT_TYPE_Q4_K) +
-           static_cast<size_t>(stages) * RowBox<FT_TYPE_Q4_0>::PITCH * 16 * row_warps;
+    const bool offset = wtype == FT_TYPE_Q4_K || wtype == FT_TYPE_Q4_1;
+    const int pitch = wtype == FT_TYPE_Q4_1 ? MmaType<FT_TYPE_Q4_1>::PITCH
+                      : wtype == FT_TYPE_Q8_0 ? MmaType<FT_TYPE_Q8_0>::PITCH
+                                              : MmaType<FT_TYPE_Q4_0>::PITCH;
+    return gemv_mma_ring_offset(nb, nt, offset) + static_cast<size_t>(stages) * pitch * 16 * row_warps;
 }
 
 // D = A B + C on m16n8k16, fp16 operands, fp32 accumulators (not volatile: a
@@ -105,6 +125,29 @@ __device__ __forceinline__ uint32_t nibble_word(const uint8_t* row, uint32_t t) 
         const uint32_t y = lds32(row + 18 * J + (t ? 4 * t : 16));
         return __byte_perm(x, y, t ? 0x3210u : 0x5432u);
     }
+}
+
+// The word of bytes P_t of 16 bytes that start 2 bytes after `base` (the
+// first or second half of a Q8_0 block's codes; base 4-byte aligned when the
+// block index is even, 2 bytes off when odd): aligned load when ODD, two loads
+// and a byte permute (for t = 0) when not, as in nibble_word.
+template <bool ODD>
+__device__ __forceinline__ uint32_t word_at(const uint8_t* base, uint32_t t) {
+    if constexpr (ODD) {
+        return lds32(base + 2 + 4 * t);
+    } else {
+        const uint32_t x = lds32(base + 4 * t);
+        const uint32_t y = lds32(base + (t ? 4 * t : 16));
+        return __byte_perm(x, y, t ? 0x3210u : 0x5432u);
+    }
+}
+
+// Four int8 bytes of a word as fp16 pairs under the pattern of 1024: bytes 0, 2
+// and 1, 3 -> 1152 + q each (q + 128 is the byte's unsigned value)
+__device__ __forceinline__ void int8_to_a(uint32_t w, uint32_t& a02, uint32_t& a13) {
+    const uint32_t u = w ^ 0x80808080u;
+    a02 = __byte_perm(u, 0x64646464u, 0x4240u);
+    a13 = __byte_perm(u, 0x64646464u, 0x4341u);
 }
 
 // Activation codes of the staging item (slot, block b, lane t): the 4 bytes
@@ -140,7 +183,8 @@ __device__ __forceinline__ void codes_hi(uint32_t u, uint32_t& b0, uint32_t& b1)
 template <int NT, int WT, typename XD>
 __device__ __forceinline__ void mma_stage_tile(const GemvArgs& a, int64_t tile, uint2* qb, float4* xc, XD* xd,
                                                int32_t n_threads, int32_t& ng, int32_t (&sid)[NT][2]) {
-    constexpr bool KQ = WT == FT_TYPE_Q4_K;
+    using T = MmaType<WT>;
+    constexpr bool KQ = T::KQ;
     constexpr int G = 8 * NT;
     const int32_t nb = a.nb;
     const int32_t e = find_expert(a.tiles, a.n_experts, tile);
@@ -165,7 +209,7 @@ __device__ __forceinline__ void mma_stage_tile(const GemvArgs& a, int64_t tile, 
             const int64_t tok = __ldg(a.perm + p0 + n) / a.top_k;
             const uint8_t* blk = a.act + (tok * nb + b) * Q8_1_BYTES;
             d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(blk))));
-            if constexpr (KQ) {                              // P_t = 4t..4t+3 for every sub-block
+            if constexpr (T::ALIGNED) {                      // P_t = 4t..4t+3 for every block
                 wl = __ldg(reinterpret_cast<const uint32_t*>(blk + 4) + tq);
                 wh = __ldg(reinterpret_cast<const uint32_t*>(blk + 20) + tq);
             } else {
@@ -182,15 +226,18 @@ __device__ __forceinline__ void mma_stage_tile(const GemvArgs& a, int64_t tile, 
         if (tq == 0) {
             float* c = reinterpret_cast<float*>(xc + static_cast<size_t>(bn) * 4 + (g >> 1));
             // Q4_0: A = 1024 + q (first 16) and 1024 + 16 q with B / 16 (last 16),
-            // level 8; Q4_K (levels 0..15, sub-block j = b mod 8 = the low
-            // nibbles for even j, the high ones as 1024 + 16 q with B / 16 for odd)
-            const float c0 = KQ ? -static_cast<float>(((b & 1) ? 64 : 1024) * (sl + sh))
-                                : -static_cast<float>(1032 * sl + 72 * sh);
+            // level 8; Q4_1 the same with levels 0..15; Q4_K (levels 0..15,
+            // sub-block j = b mod 8 = the low nibbles for even j, the high ones
+            // as 1024 + 16 q with B / 16 for odd); Q8_0: A = 1152 + q
+            const float c0 = KQ                     ? -static_cast<float>(((b & 1) ? 64 : 1024) * (sl + sh))
+                             : WT == FT_TYPE_Q4_1 ? -static_cast<float>(1024 * sl + 64 * sh)
+                             : WT == FT_TYPE_Q8_0 ? -static_cast<float>(1152 * (sl + sh))
+                                                  : -static_cast<float>(1032 * sl + 72 * sh);
             c[g & 1] = c0;
             c[2 + (g & 1)] = c0;
             float* x = reinterpret_cast<float*>(xd + static_cast<size_t>(bn) * 4 + (g >> 1));
             x[g & 1] = d;
-            if constexpr (KQ) x[2 + (g & 1)] = d * small_int_to_float(sl + sh);   // the offset term's d_a sum(q_a)
+            if constexpr (T::OFFSET) x[2 + (g & 1)] = d * small_int_to_float(sl + sh);   // the offset term's d_a sum(q_a)
         }
     }
 }
@@ -291,11 +338,11 @@ template <int NT, int WT, bool DUMP>
 __global__ void __launch_bounds__(512, 1) moe_gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const __grid_constant__ CUtensorMap wmap16,
                                                               const GemvArgs a) {
-    constexpr int PITCH = RowBox<FT_TYPE_Q4_0>::PITCH;   // 144: 8 Q4_0 blocks, or one Q4_K super-block
-    constexpr bool KQ = WT == FT_TYPE_Q4_K;
-    static_assert(WT == FT_TYPE_Q4_0 || KQ, "weight type of the mma.sync kernel");
-    static_assert(!DUMP || !KQ, "block dots are a Q4_0 diagnostic");
-    using XD = std::conditional_t<KQ, float4, float2>;
+    using T = MmaType<WT>;
+    constexpr int PITCH = T::PITCH;                       // a box row: 8 blocks, or one Q4_K super-block
+    constexpr bool KQ = T::KQ;
+    static_assert(!DUMP || WT == FT_TYPE_Q4_0, "block dots are a Q4_0 diagnostic");
+    using XD = std::conditional_t<T::OFFSET, float4, float2>;
     const int32_t RW = a.row_warps;                       // warps of 16 rows
     const int32_t E = a.n_experts;
     const int32_t nb = a.nb;
@@ -310,7 +357,7 @@ __global__ void __launch_bounds__(512, 1) moe_gemv_mma_kernel(const __grid_const
     uint2* qb = reinterpret_cast<uint2*>(smem_mma + gemv_mma_qb_offset());          // [nb][NT][32]
     float4* xc = reinterpret_cast<float4*>(qb + static_cast<size_t>(nb) * NT * 32);  // [nb][NT][4]
     XD* xd = reinterpret_cast<XD*>(xc + static_cast<size_t>(nb) * NT * 4);             // [nb][NT][4]
-    uint8_t* ring = smem_mma + gemv_mma_ring_offset(nb, NT, KQ);
+    uint8_t* ring = smem_mma + gemv_mma_ring_offset(nb, NT, T::OFFSET);
     const uint32_t stage_bytes = static_cast<uint32_t>(PITCH * 16 * RW);
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
     if (threadIdx.x == 0) {
@@ -344,13 +391,13 @@ __global__ void __launch_bounds__(512, 1) moe_gemv_mma_kernel(const __grid_const
                     uint8_t* dst = ring + static_cast<size_t>(s) * stage_bytes;
                     if (cnt == RW) {
                         mbar_arrive_expect_tx(&full[s], stage_bytes);
-                        tma_load_2d(dst, &wmap, ks * (PITCH / 2), static_cast<int32_t>(erow0 + g0 * 16), &full[s]);
+                        tma_load_2d(dst, &wmap, ks * (T::BYTES / 2), static_cast<int32_t>(erow0 + g0 * 16), &full[s]);
                     } else {
                         // a short block: only its groups, 16 rows per copy,
                         // so that no row outside the range leaves memory
                         mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(cnt) * 16 * PITCH);
                         for (int64_t i = 0; i < cnt; ++i)
-                            tma_load_2d(dst + i * 16 * PITCH, &wmap16, ks * (PITCH / 2),
+                            tma_load_2d(dst + i * 16 * PITCH, &wmap16, ks * (T::BYTES / 2),
                                         static_cast<int32_t>(erow0 + (g0 + i) * 16), &full[s]);
                     }
                 }
@@ -424,6 +471,36 @@ __global__ void __launch_bounds__(512, 1) moe_gemv_mma_kernel(const __grid_const
                     dwb = __half2float(__ushort_as_half(static_cast<unsigned short>(hb.x & 0xFFFFu))) * static_cast<float>(scb);
                     mwa = __half2float(__ushort_as_half(static_cast<unsigned short>(ha.x >> 16))) * static_cast<float>(mna);
                     mwb = __half2float(__ushort_as_half(static_cast<unsigned short>(hb.x >> 16))) * static_cast<float>(mnb);
+                } else if constexpr (WT == FT_TYPE_Q4_1) {
+                    // d, m, then the 16 nibble bytes, 4-byte aligned in every block
+                    constexpr int O = 20 * j;
+                    const uint32_t wa = lds32(ra + O + 4 + 4 * tq), wb = lds32(rb8 + O + 4 + 4 * tq);
+                    dwa = __half2float(*reinterpret_cast<const __half*>(ra + O));
+                    dwb = __half2float(*reinterpret_cast<const __half*>(rb8 + O));
+                    mwa = __half2float(*reinterpret_cast<const __half*>(ra + O + 2));
+                    mwb = __half2float(*reinterpret_cast<const __half*>(rb8 + O + 2));
+                    const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+                    alo[0] = (wa & 0x000F000Fu) | 0x64006400u;
+                    alo[1] = (wb & 0x000F000Fu) | 0x64006400u;
+                    alo[2] = (wa8 & 0x000F000Fu) | 0x64006400u;
+                    alo[3] = (wb8 & 0x000F000Fu) | 0x64006400u;
+                    ahi[0] = (wa & 0x00F000F0u) | 0x64006400u;
+                    ahi[1] = (wb & 0x00F000F0u) | 0x64006400u;
+                    ahi[2] = (wa8 & 0x00F000F0u) | 0x64006400u;
+                    ahi[3] = (wb8 & 0x00F000F0u) | 0x64006400u;
+                } else if constexpr (WT == FT_TYPE_Q8_0) {
+                    // d, then 32 int8 levels: P_t of the first and of the last 16
+                    (void)mwa;
+                    (void)mwb;
+                    constexpr int O = 34 * j;
+                    const uint32_t w0a = word_at<(j & 1) != 0>(ra + O, tq), w1a = word_at<(j & 1) != 0>(ra + O + 16, tq);
+                    const uint32_t w0b = word_at<(j & 1) != 0>(rb8 + O, tq), w1b = word_at<(j & 1) != 0>(rb8 + O + 16, tq);
+                    dwa = __half2float(*reinterpret_cast<const __half*>(ra + O));
+                    dwb = __half2float(*reinterpret_cast<const __half*>(rb8 + O));
+                    int8_to_a(w0a, alo[0], alo[2]);
+                    int8_to_a(w0b, alo[1], alo[3]);
+                    int8_to_a(w1a, ahi[0], ahi[2]);
+                    int8_to_a(w1b, ahi[1], ahi[3]);
                 } else {
                     (void)mwa;
                     (void)mwb;
@@ -447,12 +524,14 @@ __global__ void __launch_bounds__(512, 1) moe_gemv_mma_kernel(const __grid_const
                     const float4 C = xc[bn * 4 + tq];
                     const XD D = xd[bn * 4 + tq];
                     uint32_t bl0, bl1, bh0, bh1;
-                    if (!KQ || (j & 1) == 0) {
-                        if (KQ) codes_lo(Q.y, bh0, bh1);    // Q4_K, low nibbles: both halves as q
-                        else codes_hi(Q.y, bh0, bh1);      // Q4_0: the high nibbles' codes as q / 16
-                        codes_lo(Q.x, bl0, bl1);
-                    } else {                                // Q4_K, high nibbles: both halves as q / 16
+                    if constexpr (WT == FT_TYPE_Q8_0 || (KQ && (j & 1) == 0)) {
+                        codes_lo(Q.x, bl0, bl1);            // both halves as q
+                        codes_lo(Q.y, bh0, bh1);
+                    } else if constexpr (KQ) {              // Q4_K, high nibbles: both halves as q / 16
                         codes_hi(Q.x, bl0, bl1);
+                        codes_hi(Q.y, bh0, bh1);
+                    } else {                                // Q4_0, Q4_1: the high nibbles' codes as q / 16
+                        codes_lo(Q.x, bl0, bl1);
                         codes_hi(Q.y, bh0, bh1);
                     }
                     float d0[4], d1[4];
@@ -472,11 +551,12 @@ __global__ void __launch_bounds__(512, 1) moe_gemv_mma_kernel(const __grid_const
                         acc[nt][1] = fmaf(d1[1], dwa * D.y, acc[nt][1]);
                         acc[nt][2] = fmaf(d1[2], dwb * D.x, acc[nt][2]);
                         acc[nt][3] = fmaf(d1[3], dwb * D.y, acc[nt][3]);
-                        if constexpr (KQ) {                 // minus d_min m_j d_a sum(q_a)
-                            acc[nt][0] = fmaf(-mwa, D.z, acc[nt][0]);
-                            acc[nt][1] = fmaf(-mwa, D.w, acc[nt][1]);
-                            acc[nt][2] = fmaf(-mwb, D.z, acc[nt][2]);
-                            acc[nt][3] = fmaf(-mwb, D.w, acc[nt][3]);
+                        if constexpr (T::OFFSET) {          // + m d_a sum(q_a); Q4_K: minus d_min m_j d_a sum(q_a)
+                            constexpr float SG = KQ ? -1.0f : 1.0f;
+                            acc[nt][0] = fmaf(SG * mwa, D.z, acc[nt][0]);
+                            acc[nt][1] = fmaf(SG * mwa, D.w, acc[nt][1]);
+                            acc[nt][2] = fmaf(SG * mwb, D.z, acc[nt][2]);
+                            acc[nt][3] = fmaf(SG * mwb, D.w, acc[nt][3]);
                         }
                     }
                 }
@@ -536,11 +616,16 @@ static int launch_gemv_mma_nt(const GemvPlan& plan, const CUtensorMap& wmap, con
 
 int launch_gemv_mma(const GemvPlan& plan, const CUtensorMap& wmap, const CUtensorMap& wmap16, const GemvArgs& a,
                     bool dump, int wtype, cudaStream_t s) {
-    if (wtype == FT_TYPE_Q4_K) {
-        if (dump) return fail(FT_ERR_ARG, "block dots are Q4_0 only");
+    if (wtype != FT_TYPE_Q4_0 && dump) return fail(FT_ERR_ARG, "block dots are Q4_0 only");
+    if (wtype == FT_TYPE_Q4_K)
         return plan.mma == 2 ? launch_gemv_mma_nt<2, FT_TYPE_Q4_K, false>(plan, wmap, wmap16, a, s)
                              : launch_gemv_mma_nt<1, FT_TYPE_Q4_K, false>(plan, wmap, wmap16, a, s);
-    }
+    if (wtype == FT_TYPE_Q4_1)
+        return plan.mma == 2 ? launch_gemv_mma_nt<2, FT_TYPE_Q4_1, false>(plan, wmap, wmap16, a, s)
+                             : launch_gemv_mma_nt<1, FT_TYPE_Q4_1, false>(plan, wmap, wmap16, a, s);
+    if (wtype == FT_TYPE_Q8_0)
+        return plan.mma == 2 ? launch_gemv_mma_nt<2, FT_TYPE_Q8_0, false>(plan, wmap, wmap16, a, s)
+                             : launch_gemv_mma_nt<1, FT_TYPE_Q8_0, false>(plan, wmap, wmap16, a, s);
     if (plan.mma == 2)
         return dump ? launch_gemv_mma_nt<2, FT_TYPE_Q4_0, true>(plan, wmap, wmap16, a, s)
                     : launch_gemv_mma_nt<2, FT_TYPE_Q4_0, false>(plan, wmap, wmap16, a, s);

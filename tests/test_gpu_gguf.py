@@ -171,6 +171,52 @@ def test_q4_k_mma_tiles(ft, oracle, E, k, K, N, T, seed, same):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
+@pytest.mark.parametrize("wtype", ["q4_1", "q8_0"])
+@pytest.mark.parametrize("E,k,K,N,T,seed,same", Q4K_MMA)
+def test_32_weight_types_mma_tiles(ft, oracle, wtype, E, k, K, N, T, seed, same):
+    """Q4_1 and Q8_0 on the mma.sync tiles: against the oracle, a bad id, and
+    bit for bit against the dp4a row kernel where it leaves K unsplit."""
+    w, x, ids = _case(wtype, E, k, K, N, T, seed)
+    ids = ids.copy()
+    ids[T // 2, 0] = -1
+    ft.read_device_error()
+    a, ref = _check(ft, oracle, wtype, w, x, ids, f"{wtype} mma {E},{k},{K},{N},{T}")
+    assert not a[T // 2, 0].any()
+    assert ft.read_device_error() & ft.FT_DEVERR_BAD_EXPERT_ID
+    act = G.dev(oracle.quantize_q8_1(x))
+    prev = ft.set_path("gemv_dp4a")
+    try:
+        b = G.host(ft.moe_gguf_q8_1(wtype, G.dev(w), act, G.dev(ids)))
+    finally:
+        ft.set_path(prev)
+    ft.read_device_error()
+    if same:
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("wtype", ["q4_1", "q8_0"])
+def test_32_weight_types_mma_full_size(ft, oracle, wtype):
+    """The 8-expert top-2 layer (14336 x 4096) at 32 tokens: the mma.sync tiles
+    equal the dp4a row kernel bit for bit, and two tokens match the oracle."""
+    w, x, ids = _case(wtype, 8, 2, 4096, 14336, 32, 116)
+    act = oracle.quantize_q8_1(x)
+    a = G.host(ft.moe_gguf_q8_1(wtype, G.dev(w), G.dev(act), G.dev(ids)))
+    prev = ft.set_path("gemv_dp4a")
+    try:
+        b = G.host(ft.moe_gguf_q8_1(wtype, G.dev(w), G.dev(act), G.dev(ids)))
+    finally:
+        ft.set_path(prev)
+    assert ft.read_device_error() == 0
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    toks = np.array([5, 30])
+    ref = oracle.moe_gguf(wtype, w, act[toks], ids[toks])
+    E, N = 8, 14336
+    bb = w.shape[-1]
+    wn = np.linalg.norm(oracle.dequantize_gguf(wtype, w.reshape(E * N, -1, bb)), axis=-1).reshape(E, N)
+    xn = G.act_norms(oracle, act[toks])
+    G.check_close(a[toks], ref, wn[ids[toks]], np.broadcast_to(xn[:, None, None], (2, 2, N)), f"{wtype} mma full size")
+
+
 def test_q4_k_mma_full_size(ft, oracle):
     """The 8-expert top-2 layer (14336 x 4096) with Q4_K weights at 32 tokens:
     the mma.sync tiles equal the dp4a row kernel bit for bit (K unsplit at this

@@ -58,7 +58,7 @@ NCU_TRAFFIC = {("moe_gemm_tc_kernel", "205cc48df0b79f32", "prefill:8191"): 66658
 # the same for the mma.sync GEMV kernel (profiles/moe_gemv_mma_decode.md)
 MMA_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemv_mma.cu", "bit_quantized_moe_quantize_gb300/csrc/gemv_rows.cuh",
                "bit_quantized_moe_quantize_gb300/csrc/gemv_blocks.cuh", "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh")
-NCU_TRAFFIC_GEMV = {("moe_gemv_mma_kernel", "9abf780d2a1c171b", "mixtral_8x7b:32", "q4_0"): 264468224 + 4952832}
+NCU_TRAFFIC_GEMV = {("moe_gemv_mma_kernel", "87fb6d28d029d2e4", "mixtral_8x7b:32", "q4_0"): 264453120 + 4717568}
 
 
 def mma_tiles(S, E, K, wtype="q4_0") -> bool:

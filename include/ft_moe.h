@@ -318,10 +318,12 @@ FT_API int ft_moe_q4_0_q8_1_ep(const void* weights_local, const void* act, const
  *   ft_moe_q4_0_q8_1.
  * Q4_0 and Q4_K take either path by the rule of ft_moe_q4_0_q8_1 (Q4_K on the
  * tensor cores: one 144-byte super-block per row and stage, its sub-block
- * scales and mins applied in the drain; on the GEMV path with more than 4
- * slots per expert, the mma.sync tiles, with those scales and mins applied per
- * sub-block after its two MMAs); the other types always take the GEMV path,
- * and ft_moe_set_path(FT_PATH_GEMM) makes them fail with FT_ERR_ARG.
+ * scales and mins applied in the drain); the other types always take the
+ * GEMV path, and ft_moe_set_path(FT_PATH_GEMM) makes them fail with
+ * FT_ERR_ARG.  On the GEMV path, batches with more than 4 slots per expert of
+ * Q4_0, Q4_1, Q8_0 and Q4_K run tiles of 8 or 16 slots on mma.sync (exact
+ * integer block dots; each block's or sub-block's scale and offset applied
+ * after its two MMAs, as the dp4a kernels do).
  * ft_moe_gguf_selected_path tells which path a shape takes.
  * Errors as for ft_moe_q4_0_q8_1, plus FT_ERR_ARG for an unknown wtype.
  */

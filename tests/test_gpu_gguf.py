@@ -7,7 +7,9 @@ Against the oracle's matmul of the same type within the matmul tolerance
 (max |err| <= 1e-3 ||w_row|| ||x||, relative L2 <= 1e-4, ||w_row|| of the
 dequantized weight row); Q4_0 through the same entry point bit for bit equal
 to ft_moe_q4_0_q8_1; bad ids; rows not 16-byte aligned; a full-size decode
-step of the 8-expert 14336 x 4096 layer; the shapes the path rejects."""
+step of the 8-expert 14336 x 4096 layer; Q4_K on the tensor cores; the
+mma.sync decode tiles of Q4_1, Q8_0 and Q4_K, bit for bit against the dp4a
+row kernel where it leaves K unsplit; the shapes the path rejects."""
 
 import numpy as np
 import pytest

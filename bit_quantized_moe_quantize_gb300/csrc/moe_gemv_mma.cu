@@ -1,7 +1,11 @@
 // GEMV tiles of 8 or 16 slots of the routed Q4_0 x Q8_1 expert matmul
-// (moe_vec_q4_0_q8_1 on FreeToken PR #185, "Problem" and "Notes") on the
-// warp-level tensor-core instruction mma.sync.m16n8k16 (fp16 operands, fp32
-// accumulation), for decode batches with more than 4 slots per expert.
+// (moe_vec_q4_0_q8_1 on FreeToken PR #185, "Problem" and "Notes"), and of its
+// Q4_1, Q8_0 and Q4_K forms (the per-type launchers of moe_vec.cuh there), on
+// the warp-level tensor-core instruction mma.sync.m16n8k16 (fp16 operands,
+// fp32 accumulation), for decode batches with more than 4 slots per expert.
+// The notes below describe Q4_0; the other types differ only in how a lane's
+// weight words are found and widened, in the accumulator's start and in the
+// offset term after the dot (at the weight-type branches below).
 //
 // Why: with 8 slots per tile the row-per-lane kernel (gemv_rows.cuh) spends
 // 8 dp4a, three shared loads and two float ops per weight block and slot, and
@@ -48,13 +52,13 @@
 // range, cut by weight: a unit whose tile uses its second slot group counts
 // 3, any other 2 (about their costs), so the SMs finish together whatever
 // the routing; where the tiles are few, each tile gets its share of the CTAs
-// so that no CTA stages two tiles.  The CTA walks its range in row blocks of RW groups
-// (one TMA box high), cut short at the end of a tile and of the range (the
+// so that no CTA stages two tiles.  The CTA walks its range in row blocks of
+// RW groups (one TMA box high), cut short at the end of a tile and of the range (the
 // warps without a group there skip that block), and restages the activations
 // only where the range enters a new tile (units handed out one by one from a
 // global counter balance as well but restage at nearly every block, which
 // measured slower).  Weights stream as in the row-per-lane kernel: TMA boxes
-// of 256 weights (8 blocks, 144 bytes per row) x 16 RW rows through an
+// of 256 weights (8 blocks; 144 bytes per row for Q4_0) x 16 RW rows through an
 // mbarrier ring filled by one producer warp, which runs ahead of the staging.
 // Warp r owns rows 16 r .. 16 r + 15 of each box (one m16 tile), so a CTA
 // keeps up to 15 row warps busy on one staged activation tile.
@@ -70,8 +74,8 @@ namespace ft {
 // qb [nb][NT][32 lanes] uint2 (codes + 128 at P_t: first / last 16) | xc
 // [nb][NT][4] float4 (the accumulator's start for lane t: minus the offset
 // sums of slots 2t, 2t+1, twice, as the MMA's C quad) | xd [nb][NT][4] float2
-// (d_a of slots 2t, 2t+1; Q4_K: float4, then d_a sum(q_a) of those slots) |
-// ring (128-byte aligned)
+// (d_a of slots 2t, 2t+1; for the types with an offset term float4, then d_a
+// sum(q_a) of those slots) | ring (128-byte aligned)
 __host__ __device__ inline size_t gemv_mma_qb_offset() { return 8 * 2 * kMaxRowStages + 16; }
 __host__ __device__ inline size_t gemv_mma_ring_offset(int nb, int nt, bool offset) {
     return (gemv_mma_qb_offset() + static_cast<size_t>(nb) * nt * (256 + 64 + (offset ? 64 : 32)) + 127) / 128 * 128;

@@ -54,11 +54,11 @@ PAGES_T4_TOKENS_PER_S = {("prefill", 8191): 8191 / 0.7058, ("prefill", 4096): 40
 GEMM_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemm_tc.cu", "bit_quantized_moe_quantize_gb300/csrc/gemm_common.cuh",
                 "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh")
 GEMM_CONSTANTS = ("bit_quantized_moe_quantize_gb300/csrc/ft_internal.h", "kGemm")
-NCU_TRAFFIC = {("moe_gemm_tc_kernel", "205cc48df0b79f32", "prefill:8191"): 666582016 + 340652544}
+NCU_TRAFFIC = {("moe_gemm_tc_kernel", "6a535597f4d7cafa", "prefill:8191"): 666582016 + 340652544}
 # the same for the mma.sync GEMV kernel (profiles/moe_gemv_mma_decode.md)
 MMA_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemv_mma.cu", "bit_quantized_moe_quantize_gb300/csrc/gemv_rows.cuh",
                "bit_quantized_moe_quantize_gb300/csrc/gemv_blocks.cuh", "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh")
-NCU_TRAFFIC_GEMV = {("moe_gemv_mma_kernel", "87fb6d28d029d2e4", "mixtral_8x7b:32", "q4_0"): 264453120 + 4717568}
+NCU_TRAFFIC_GEMV = {("moe_gemv_mma_kernel", "84c18d9629a18982", "mixtral_8x7b:32", "q4_0"): 264453120 + 4717568}
 
 
 def mma_tiles(S, E, K, wtype="q4_0") -> bool:
@@ -77,12 +77,18 @@ def mma_tiles(S, E, K, wtype="q4_0") -> bool:
 
 
 def kernel_source_hash(files, constants=GEMM_CONSTANTS) -> str:
+    """Hash of the code of a kernel's source files (comments and blank space
+    left out, so that a comment edit keeps a capture valid) and, optionally,
+    of the lines of a header that hold its constants."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, f), "rb") as fh:
+        with open(os.path.join(ROOT, f)) as fh:
+            code = re.sub(r"/\*.*?\*/", " ", fh.read(), flags=re.S)
+            code = re.sub(r"//[^\n]*", " ", code)
             h.update(os.path.basename(f).encode())
-            h.update(fh.read())
+            h.update(" ".join(code.split()).encode())
     if constants:
         path, key = constants
         with open(os.path.join(ROOT, path)) as fh:

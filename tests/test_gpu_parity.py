@@ -277,6 +277,50 @@ def test_gemv_mma_tiles(path, oracle, E, k, K, N, T, seed, same):
         G.check_close(a, b, wn, xn, f"mma vs dp4a {E},{k},{K},{N},{T}")
 
 
+@pytest.mark.parametrize("wtype", ["q4_0", "q4_k"])
+def test_gemv_mma_one_slot_group_long_rows(path, oracle, wtype):
+    """Rows of 14336 weights (the Mixtral-shaped second layer, 4096 rows): the
+    staged 16-slot activation tile does not fit, so the tiles hold one group
+    of 8 slots (experts with more get a second tile) and 56 boxes per row;
+    sampled outputs of every slot against the oracle, a bad id."""
+    from bit_quantized_moe_quantize_gb300 import synth
+    E, k, K, N, T = 8, 2, 14336, 4096, 30
+    wl = synth.custom_workload(E, k, K, N, 120)
+    w = synth.make_weights(wl) if wtype == "q4_0" else synth.make_weights_gguf(wl, wtype)
+    x, ids = synth.make_activations(wl, T), synth.make_topk_ids(wl, T).copy()
+    ids[7, 1] = -1
+    act = oracle.quantize_q8_1(x)
+    path.set_path("auto")
+    path.read_device_error()
+    if wtype == "q4_0":
+        got = G.host(path.moe_q4_0_q8_1(G.dev(w), G.dev(act), G.dev(ids)))
+    else:
+        got = G.host(path.moe_gguf_q8_1(wtype, G.dev(w), G.dev(act), G.dev(ids)))
+    assert path.read_device_error() & path.FT_DEVERR_BAD_EXPERT_ID
+    assert not got[7, 1].any()
+    S = T * k
+    rng = np.random.default_rng(121)
+    slots = np.repeat(np.arange(S), 40)
+    rows = rng.integers(0, N, slots.size)
+    keep = ids.reshape(-1)[slots] >= 0
+    slots, rows = slots[keep], rows[keep]
+    flat = ids.reshape(-1)
+    if wtype == "q4_0":
+        ref = oracle.moe_sample(w, act, ids, slots, rows)
+        wn = G.row_norms_w(oracle, w, flat[slots], rows)
+    else:
+        toks = np.unique(slots // k)[:3]
+        sel = np.isin(slots // k, toks)
+        slots, rows = slots[sel], rows[sel]
+        full = oracle.moe_gguf(wtype, w, act[toks], ids[toks]).reshape(len(toks) * k, N)
+        pos = {t: i for i, t in enumerate(toks)}
+        ref = full[[pos[s // k] * k + s % k for s in slots], rows]
+        deq = oracle.dequantize_gguf(wtype, w[flat[slots], rows])
+        wn = np.linalg.norm(deq, axis=-1)
+    xn = G.act_norms(oracle, act)[slots // k]
+    G.check_close(got.reshape(S, N)[slots, rows], ref, wn, xn, f"{wtype} long rows")
+
+
 @pytest.mark.parametrize("T", [24, 32])
 def test_gemv_mma_full_size_matches_dp4a(path, oracle, T):
     """The Mixtral-shaped layer at 6 and 8 slots per expert: the mma.sync tiles

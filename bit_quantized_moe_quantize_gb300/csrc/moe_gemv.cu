@@ -1,31 +1,34 @@
 // GEMV path of the routed Q4_0 x Q8_1 expert matmul (moe_vec_q4_0_q8_1 on
-// FreeToken PR #185), for batches with few slots per expert (decode).  Two
-// kernels share the launch geometry below: moe_gemv_rows_kernel (one weight
-// row per lane, gemv_rows.cuh; rows a whole number of 256-weight runs) and
-// moe_gemv_kernel (one block per lane, gemv_blocks.cuh; any row length).
+// FreeToken PR #185) and of its other GGUF weight types, for batches with few
+// slots per expert (decode): the plan (plan_gemv) and the launch
+// (launch_gemv) of three kernels:
+//  - moe_gemv_mma_kernel (moe_gemv_mma.cu): Q4_0, Q4_1, Q8_0, Q4_K rows of
+//    whole 256-weight runs with more than 4 slots per expert on average;
+//    tiles of 8 or 16 slots on mma.sync, one CTA per SM over a weighted
+//    split of (tile, 16-row group) units;
+//  - moe_gemv_rows_kernel (gemv_rows.cuh): one weight row per lane, rows of
+//    whole 256-weight runs of the types with 16-byte box rows, tiles of 1, 2,
+//    4 or 8 slots;
+//  - moe_gemv_kernel (gemv_blocks.cuh): one 32-weight block per lane, any row
+//    length and every type.
 //
-// Launch geometry.  grid.x enumerates slot tiles: each is up to G slots of
-// one expert taken from the router's permutation, so grid.x is bounded by
-// ceil(S / G) + min(E, S) and can reach 2^31 - 1 (FreeToken PR #185, "Fix":
-// the flat (token, top-k) index belongs on grid.x, never on grid.z).  The
-// tile -> expert map is a binary search over the router's tile prefix, i.e.
-// searchsorted(right=True) (nvfp4-megamoe-kernel CURRENT_BUG.md, Bug 2), so
-// empty experts own no tile.  grid.y splits the expert's rows into contiguous
-// ranges, sized from the SM count so that all CTAs stream at once (<= 65535).
-// Extra CTAs of the upper bound exit.
+// Launch geometry of the last two.  grid.x enumerates slot tiles: each is up
+// to G slots of one expert taken from the router's permutation, so grid.x is
+// bounded by ceil(S / G) + min(E, S) and can reach 2^31 - 1 (FreeToken PR
+// #185, "Fix": the flat (token, top-k) index belongs on grid.x, never on
+// grid.z).  The tile -> expert map is a binary search over the router's tile
+// prefix, i.e. searchsorted(right=True) (nvfp4-megamoe-kernel CURRENT_BUG.md,
+// Bug 2), so empty experts own no tile.  grid.y splits the expert's rows into
+// contiguous ranges, sized from the SM count so that all CTAs stream at once
+// (<= 65535).  Extra CTAs of the upper bound exit.
 //
-// Per CTA: the G activation rows are staged once in shared memory as 16-byte
-// aligned int8 blocks plus fp32 scales and exact block sums; the row range's
-// Q4_0 bytes (contiguous, because an expert's rows are) stream through a ring
-// of up to four mbarrier-tracked bulk copies (cp.async.bulk) of ~40 KB, so
-// several copies are in flight while the previous stage is computed.  Each
-// weight block is read once from shared memory and dotted with all G slots,
-// so weight bytes leave HBM once per (expert, slot group).
-//
-// Arithmetic: per block, sum_i q_w[i] * q_a[i] with dp4a on the raw nibbles,
-// then minus 8 * sum_i q_a[i] (exact integer), so the block dot is bit-exact;
-// it is scaled by d_w * d_a in fp32 and summed over the lane's blocks, then
-// across lanes with shuffles.
+// Every kernel stages a tile's activation rows once per CTA and streams the
+// tile's expert rows (contiguous, because an expert's rows are) through an
+// mbarrier-tracked ring of TMA boxes or bulk copies, so each weight block is
+// read once from shared memory for all the tile's slots and weight bytes
+// leave HBM once per (expert, slot group).  Every block dot is the exact
+// integer sum_i q_w[i] q_a[i] (minus level0 sum_i q_a[i]), scaled by d_w d_a
+// in fp32 (plus the type's offset term).
 #include <mutex>
 
 #include <cuda_fp16.h>

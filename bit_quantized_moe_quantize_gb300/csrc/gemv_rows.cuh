@@ -2,8 +2,11 @@
 // and the other per-type launchers of moe_vec.cuh on FreeToken PR #185,
 // "Problem" and "Notes"), templated on the weight type, for rows that are a
 // whole number of 256-weight runs (ncols % 256 == 0).  moe_gemv.cu
-// instantiates it for Q4_0 (with the block-dot dump), moe_gemv_gguf.cu for
-// Q4_1, Q5_0, Q5_1, Q8_0, Q4_K and Q5_K.
+// instantiates it for Q4_0 (with the block-dot dump), moe_decode.cu its
+// one-launch decode form, moe_gemv_rows_gguf.cu the Q4_1, Q5_0, Q5_1, Q8_0,
+// Q4_K and Q5_K forms.  (Tiles with more than 4 slots per expert of Q4_0,
+// Q4_1, Q8_0 and Q4_K run on moe_gemv_mma.cu instead, unless the dp4a
+// kernels are forced.)
 //
 // grid.x: slot tiles (G slots of one expert); grid.y: blocks of 32 RW weight
 // rows of that expert (looping past 65535).  Lane l of a compute warp owns one

@@ -54,7 +54,7 @@ PAGES_T4_TOKENS_PER_S = {("prefill", 8191): 8191 / 0.7058, ("prefill", 4096): 40
 GEMM_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemm_tc.cu", "bit_quantized_moe_quantize_gb300/csrc/gemm_common.cuh",
                 "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh")
 GEMM_CONSTANTS = ("bit_quantized_moe_quantize_gb300/csrc/ft_internal.h", "kGemm")
-NCU_TRAFFIC = {("moe_gemm_tc_kernel", "6a535597f4d7cafa", "prefill:8191"): 666582016 + 340652544}
+NCU_TRAFFIC = {("moe_gemm_tc_kernel", "9356abed6442eb8b", "prefill:8191"): 667560704 + 341054720}
 # the same for the mma.sync GEMV kernel (profiles/moe_gemv_mma_decode.md)
 MMA_SOURCES = ("bit_quantized_moe_quantize_gb300/csrc/moe_gemv_mma.cu", "bit_quantized_moe_quantize_gb300/csrc/gemv_rows.cuh",
                "bit_quantized_moe_quantize_gb300/csrc/gemv_blocks.cuh", "bit_quantized_moe_quantize_gb300/csrc/ft_common.cuh")

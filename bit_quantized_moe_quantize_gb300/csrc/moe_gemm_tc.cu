@@ -797,42 +797,42 @@ __global__ void __launch_bounds__(FUSE ? Gemm<BN>::THREADS_FUSED : Gemm<BN>::THR
 }
 
 // --------------------------------------------------------------- gather
-// One warp per router position p: slot s = perm[p] of token t = s / k.  The
-// warp walks the token's Q8_1 row as consecutive 4-byte words (coalesced):
-// word 9b of the row is block b's (d, s) pair, words 9b+1 .. 9b+8 its 32 int8
-// values, which become 4 fp16 each (exact integers) at xh[p][32b + 4(w-1)].
-// Positions past the routed slots (bad ids, and the padding up to a multiple
-// of 128 rows) are written as zeros.
+// One warp per router position p: slot s = perm[p] of token t = s / k.  Four
+// lanes per Q8_1 block, eight blocks per step: lane 4i + q of block b loads
+// the block's code words 1 + 2q and 2 + 2q (the warp reads 8 whole blocks,
+// 288 contiguous bytes) and stores their 8 codes as fp16 (exact integers) in
+// one 16-byte store at xh[p][32b + 8q] (the warp writes 512 contiguous
+// bytes); lane q = 0 also copies the block's fp16 d to da[p][b].  Positions
+// past the routed slots (bad ids, and the padding up to a multiple of 128
+// rows) are written as zeros.
 __global__ void __launch_bounds__(256)
     gather_act_kernel(const uint8_t* __restrict__ act, const int32_t* __restrict__ perm,
                       const int32_t* __restrict__ offsets, int32_t n_experts, int32_t top_k, int32_t nb,
-                      int64_t n_rows, uint2* __restrict__ xh, uint16_t* __restrict__ da) {
+                      int64_t n_rows, uint4* __restrict__ xh, uint16_t* __restrict__ da) {
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int64_t n_valid = offsets[n_experts];
-    const uint32_t lane = lane_id();
-    const int32_t words = nb * (Q8_1_BYTES / 4);
+    const uint32_t lane = lane_id(), q = lane & 3u;
+    const int32_t b0 = static_cast<int32_t>(lane >> 2);
     for (int64_t p = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); p < n_rows;
          p += warps) {
-        uint2* xrow = xh + p * nb * 8;      // 8 x 8 bytes per block
+        uint4* xrow = xh + p * nb * 4;      // 4 x 16 bytes per block
         uint16_t* drow = da + p * nb;
         if (p < n_valid) {
             const int64_t t = perm[p] / top_k;
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(act + t * nb * Q8_1_BYTES);
-#pragma unroll 4
-            for (int32_t j = lane; j < words; j += 32) {
-                const uint32_t v = __ldg(src + j);
-                const int32_t b = j / 9, r = j - 9 * b;
-                if (r == 0) {
-                    drow[b] = static_cast<uint16_t>(v & 0xFFFFu);
-                } else {
-                    uint32_t lo, hi;
-                    i8x4_to_h2(v, lo, hi);
-                    xrow[b * 8 + (r - 1)] = make_uint2(lo, hi);
-                }
+            const uint8_t* src = act + t * nb * Q8_1_BYTES;
+#pragma unroll 2
+            for (int32_t b = b0; b < nb; b += 8) {
+                const uint32_t* w = reinterpret_cast<const uint32_t*>(src + static_cast<int64_t>(b) * Q8_1_BYTES);
+                const uint32_t v0 = __ldg(w + 1 + 2 * q), v1 = __ldg(w + 2 + 2 * q);
+                uint4 o;
+                i8x4_to_h2(v0, o.x, o.y);
+                i8x4_to_h2(v1, o.z, o.w);
+                xrow[b * 4 + q] = o;
+                if (q == 0) drow[b] = static_cast<uint16_t>(__ldg(w) & 0xFFFFu);
             }
         } else {
-            for (int32_t j = lane; j < nb * 8; j += 32) xrow[j] = make_uint2(0, 0);
-            for (int32_t b = lane; b < nb; b += 32) drow[b] = 0;
+            for (int32_t j = static_cast<int32_t>(lane); j < nb * 4; j += 32) xrow[j] = make_uint4(0, 0, 0, 0);
+            for (int32_t b = static_cast<int32_t>(lane); b < nb; b += 32) drow[b] = 0;
         }
     }
 }
@@ -919,7 +919,7 @@ int launch_gather(const uint8_t* act, const int32_t* perm, const int32_t* offset
         return check_launch("gather_act_sums_kernel", grid, dim3(256), 0);
     }
     gather_act_kernel<<<grid, 256, 0, s>>>(act, perm, offsets, n_experts, top_k, static_cast<int32_t>(nb), rows,
-                                           reinterpret_cast<uint2*>(xh), da);
+                                           reinterpret_cast<uint4*>(xh), da);
     return check_launch("gather_act_kernel", grid, dim3(256), 0);
 }
 
